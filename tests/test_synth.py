@@ -1,0 +1,62 @@
+"""The seeded input generator: determinism, slicing, and the workload
+distributions (CPU)."""
+import math
+
+import numpy as np
+import torch
+
+from moe_expert_nvfp4_gb300 import synth
+
+
+def test_hash_is_deterministic_and_keyed():
+    k1 = synth.stream_key(0, 1, 2)
+    k2 = synth.stream_key(0, 1, 3)
+    a = synth.bits32(k1, 0, 1000)
+    assert torch.equal(a, synth.bits32(k1, 0, 1000))
+    assert not torch.equal(a, synth.bits32(k2, 0, 1000))
+    assert int(a.min()) >= 0 and int(a.max()) < 2 ** 32
+
+
+def test_hash_matches_pure_python_reference():
+    key = synth.stream_key(7, 3)
+    w = synth.bits32(key, 10, 5).tolist()
+    ref = [synth._py_lowbias32(synth._py_lowbias32((i + key[0]) & 0xFFFFFFFF) ^ key[1])
+           for i in range(10, 15)]
+    assert w == ref
+
+
+def test_row_slices_regenerate_exactly():
+    c, s = synth.nvfp4_weight(3, 96, 256, 5)
+    c2, s2 = synth.nvfp4_weight(3, 96, 256, 5, row_lo=40, row_hi=71)
+    assert torch.equal(c[40:71], c2) and torch.equal(s[40:71], s2)
+
+
+def test_activation_prefix_property():
+    a = synth.activations_bf16(1, 8, 64)
+    b = synth.activations_bf16(1, 3, 64)
+    assert torch.equal(a[:3], b)
+
+
+def test_code_and_scale_distributions():
+    c, s = synth.nvfp4_weight(11, 512, 2048)
+    nib = torch.cat([c & 15, c >> 4]).flatten().bincount(minlength=16).double()
+    assert float((nib / nib.sum() - 1 / 16).abs().max()) < 0.003
+    assert int(s.min()) >= 0x18 and int(s.max()) <= 0x48
+    vals = s.view(torch.float8_e4m3fn).double()
+    lg = torch.log2(vals)
+    assert abs(float(lg.mean()) - (-1.0)) < 0.02           # log-uniform on [-4, 2]
+    assert abs(float(lg.var()) - 3.0) < 0.05                 # var of U(-4,2) is 3
+    assert float(vals.min()) == 0.0625 and float(vals.max()) == 4.0
+
+
+def test_normal_moments():
+    z = synth.activations_bf16(2, 256, 1024).double()
+    assert abs(float(z.mean())) < 0.01 and abs(float(z.var()) - 1.0) < 0.01
+    g = synth.router_logits(2, 64, 256)
+    assert g.dtype == torch.float32 and abs(float(g.double().var()) - 1.0) < 0.03
+
+
+def test_expert_host_matches_stack():
+    st = synth.expert_stack(4, 0, [3, 9], 64, 32)
+    h = synth.expert_host(4, 0, 9, 64, 32)
+    assert np.array_equal(st[0][1].numpy(), h[0]) and np.array_equal(st[3][1].numpy(), h[4])
