@@ -1,0 +1,164 @@
+/*
+ * nvfp4moe.h -- C ABI of the GB300 (sm_103a) NVFP4 decode library.
+ *
+ * The library computes the decode-time "skinny" matmuls of 4-bit NVFP4
+ * models: 1..32 rows of BF16 activations times a large NVFP4 weight matrix
+ * (W4A16), as a dense projection / head (with an optional fused argmax) and as
+ * a top-k routed mixture-of-experts layer with an always-on shared expert.
+ *
+ * Sources.  "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", section "Making
+ * decode faster": paragraph "Skinny matrix multiplies" (decode matmuls are
+ * four to sixteen rows of 16-bit activations times a large weight matrix,
+ * 4-bit weights with 16-bit activations; split-K), paragraph "One environment
+ * variable" (the fused MoE finalize: weighted top-k combine), paragraph
+ * "FR-Spec, and a silent bug" (a 4-bit head).  The pages name NVFP4 without
+ * defining it; the layout below is this library's specification of it.
+ *
+ * NVFP4 layout (plain row-major, no repacking):
+ *   codes  uint8 [N, K/2]   E2M1 codes, byte j of a row holds k = 2j in bits
+ *                           3..0 and k = 2j+1 in bits 7..4;
+ *   scales uint8 [N, K/16]  FP8 E4M3 ("fn") scale of the block k / 16;
+ *   global float32 (device) per-tensor scale;
+ *   W[n][k] = e2m1(code) * e4m3(scale) * global.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise.  The caller
+ *     owns every buffer; the library never allocates, frees or synchronises
+ *     in a compute call.  Calls are asynchronous on `stream` and may be
+ *     captured in a CUDA graph.
+ *   - Activations are BF16 (uint16 bit patterns of bfloat16), row-major with
+ *     a leading dimension in elements.  Pointers and leading dimensions must
+ *     give 16-byte aligned rows; weight pointers must be 16-byte aligned.
+ *   - K must be a multiple of 256 (one 256-wide stage of the weight stream);
+ *     1 <= M, T <= 32.
+ *   - Return value: NVFP4_OK or a negative status.  On a negative status
+ *     nothing was launched and nvfp4_last_error() describes why.  No C++
+ *     exception crosses this boundary.
+ *   - Workspace: a device buffer of at least the queried size, zero-filled
+ *     once before its first use (nvfp4_workspace_init).  Kernels leave their
+ *     counters at zero again.  One workspace must not be used by two calls
+ *     that may run concurrently.
+ *   - Problems found on the device (an expert id outside [0, E), a pipeline
+ *     wait that gave up) never trap: they set bits in the workspace's status
+ *     word, read by nvfp4_read_device_status().
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (same type); NULL is the legacy default stream. */
+typedef struct CUstream_st* nvfp4_stream_t;
+
+enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID = -1,   /* null pointer, bad count, k > E ... */
+  NVFP4_ERR_ALIGN = -2,     /* pointer / leading dimension not 16-byte aligned */
+  NVFP4_ERR_SHAPE = -3,     /* K % 256 != 0, M or T outside [1, 32], E too large */
+  NVFP4_ERR_ARCH = -4,      /* current device is not compute capability 10.3 */
+  NVFP4_ERR_CUDA = -5,      /* a CUDA runtime / launch error */
+  NVFP4_ERR_WORKSPACE = -6  /* workspace missing or smaller than required */
+};
+
+/* call flags */
+#define NVFP4_FLAG_RMS_INPUT 1u /* scale each input row by 1/sqrt(mean(x^2)+1e-6) */
+#define NVFP4_FLAG_NO_PDL 2u    /* launch without programmatic dependent launch */
+
+/* device status bits */
+#define NVFP4_STATUS_BAD_EXPERT_ID 1u /* an id outside [0, E): its slot was skipped */
+#define NVFP4_STATUS_WAIT_TIMEOUT 2u  /* a pipeline wait gave up; outputs invalid */
+
+typedef struct nvfp4_weight {
+  const uint8_t* codes;       /* [n, k/2] */
+  const uint8_t* scales;      /* [n, k/16] */
+  const float* global_scale;  /* 1 float */
+  int32_t n, k;
+} nvfp4_weight;
+
+/* E experts stacked: gu_codes [E, 2I, H/2], gu_scales [E, 2I, H/16],
+ * dn_codes [E, H, I/2], dn_scales [E, H, I/16], gu_global / dn_global [E].
+ * Rows [0, I) of each gate_up matrix are the gate, rows [I, 2I) the up
+ * projection.  A single (shared) expert is a stack with E = 1. */
+typedef struct nvfp4_expert_stack {
+  const uint8_t* gu_codes;
+  const uint8_t* gu_scales;
+  const uint8_t* dn_codes;
+  const uint8_t* dn_scales;
+  const float* gu_global;
+  const float* dn_global;
+  int32_t num_experts, hidden, inter;
+} nvfp4_expert_stack;
+
+/* NVFP4_OK if `device` is compute capability 10.3 (GB300), else
+ * NVFP4_ERR_ARCH (or NVFP4_ERR_CUDA if the device cannot be queried). */
+int nvfp4_device_check(int device);
+
+/* Zero-fill a workspace (asynchronous, on `stream`). */
+int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream);
+
+/* ---- dense skinny GEMM --------------------------------------------------
+ * C[m][n] = bf16( sum_k A'[m][k] * W[n][k] ),  m < M, n < W->n,
+ * accumulated in FP32 after each activation row is brought to FP16 exactly
+ * by a power-of-two scale; A' = A, or with NVFP4_FLAG_RMS_INPUT
+ * A'[m] = A[m] / sqrt(mean_k A[m][k]^2 + 1e-6) (FP32).
+ *   A [M, lda] bf16, lda >= K;  C [M, ldc] bf16, ldc >= N.
+ *   argmax_out: NULL, or int32 [M]: index of the first maximum of each row of
+ *   the BF16 output C (ties to the lowest index).
+ * Split-K partial sums are reduced in a fixed order: results are
+ * deterministic. */
+size_t nvfp4_gemm_skinny_workspace(int M, int N, int K);
+int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
+                      void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
+                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ---- top-k softmax routing ----------------------------------------------
+ * logits float32 [T, E] (row-major).  For each row the k experts with the
+ * largest logits, compared as float32, ties to the lower index, listed in
+ * that order -> topk_ids int32 [T, k].  topk_w float32 [T, k]: softmax
+ * probabilities, renormalised over the chosen k when `renormalize` != 0.
+ * Limits: 1 <= k <= E <= 512, k <= 32, T >= 1 (any T: rows are independent). */
+int topk_softmax_route(const float* logits, int T, int E, int k, int renormalize,
+                       int32_t* topk_ids, float* topk_w, nvfp4_stream_t stream);
+
+/* ---- MoE decode layer ----------------------------------------------------
+ * out[t] = bf16( sum_j w[t][j] * E_{ids[t][j]}(x'[t]) + E_shared(x'[t]) ),
+ * E(x) = W_down (silu(W_gate x) * (W_up x)), silu(z) = z / (1 + exp(-z)).
+ * Only the experts some token routes to are read.  x' as A' above.
+ *   x [T, ldx] bf16 (ldx >= H);  topk_ids int32 [T, k];  topk_w float32 [T, k];
+ *   experts: the routed stack; shared: NULL or a stack with E = 1 and the
+ *   same H and I;  out [T, ldo] bf16.
+ * Intermediates (gate/up sums, silu(g)*u, per-expert down outputs and the
+ * combine) are FP32; the per-slot outputs are summed in slot order, the
+ * shared expert last: deterministic.  Ids outside [0, E) are skipped and set
+ * NVFP4_STATUS_BAD_EXPERT_ID.  Limits: T <= 32, k <= 16, E <= 512,
+ * H % 256 == 0, I % 256 == 0. */
+size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* experts);
+int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
+                     const float* topk_w, int k, const nvfp4_expert_stack* experts,
+                     const nvfp4_expert_stack* shared, void* out, int64_t ldo,
+                     uint32_t flags, void* workspace, size_t workspace_bytes,
+                     nvfp4_stream_t stream);
+
+/* ---- diagnostics ---------------------------------------------------------
+ * Copy the workspace's status word to *flags and clear it.  Synchronises
+ * `stream`: for tests, not for the decode loop. */
+int nvfp4_read_device_status(void* workspace, uint32_t* flags, nvfp4_stream_t stream);
+
+/* Text describing the launches of this thread's last successful call
+ * (kernel, grid, work items, split): tests assert the intended path ran.
+ * Writes at most n bytes including the terminating NUL; returns the length. */
+int nvfp4_last_dispatch(char* buf, size_t n);
+
+/* Message for this thread's last failed call ("" if none). */
+const char* nvfp4_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

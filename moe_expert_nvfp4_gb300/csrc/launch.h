@@ -1,0 +1,83 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Shared-memory carve-up of the streaming kernels (byte offsets from a
+// 1024-byte aligned base).  x staging comes last and is sized per launch.
+constexpr int kSmemRing = 0;
+constexpr int kSmemBars = kSmemRing + 8 * 9216;        // kStages * kStageBytes
+constexpr int kSmemMisc = kSmemBars + 2 * 8 * 8;       // full + empty mbarriers
+constexpr int kSmemEp = kSmemMisc + 512;               // sig[32], rms[32], flags
+constexpr int kSmemSched = kSmemEp + 32 * 64 * 4;      // epilogue tile [32][64] f32
+constexpr int kSchedInts(int E, int P, int T) { return 4 * (E + 2) + P + (P + T) + 4; }
+constexpr int kSmemAlignPad = 1024;
+
+struct DenseArgs {
+  const __nv_bfloat16* A;
+  int64_t lda;
+  __nv_bfloat16* C;
+  int64_t ldc;
+  int32_t* argmax_out;     // nullable
+  const float* gscale;
+  int M, N, K;
+  int n_tiles, splits, nkb; // nkb = K / 256
+  int items;               // n_tiles * splits
+  int xrow_bytes;          // staged row stride (bytes)
+  int x_offset;            // smem offset of the x staging area
+  int rms;                 // NVFP4_FLAG_RMS_INPUT
+  uint32_t* status;
+  uint32_t* tile_cnt;      // [n_tiles]
+  uint32_t* argmax_cnt;    // [1]
+  float* partials;         // [splits][n_tiles][M][64]
+  int2* am_part;           // [M][n_tiles] (float bits of value, index)
+};
+
+struct MoeArgs {
+  const __nv_bfloat16* x;
+  int64_t ldx;
+  const int32_t* ids;
+  const float* w;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  const float* gu_global;  // [E]
+  const float* dn_global;  // [E]
+  const float* sh_gu_global;
+  const float* sh_dn_global;
+  int T, k, E, H, I;
+  int has_shared;
+  int rms;
+  int xrow_bytes;
+  int x_offset;
+  int sched_offset;
+  uint32_t* status;
+  uint32_t* tile_cnt;      // [H / 64]
+  float* h;                // [T*k + T][I]
+  float* y;                // [T*k + T][H]
+};
+
+struct RouteArgs {
+  const float* logits;
+  int T, E, k, renorm;
+  int32_t* ids;
+  float* w;
+};
+
+// maps: codes / scales of the weight (dense), or routed gate_up, routed down,
+// shared gate_up, shared down (MoE).
+cudaError_t launch_dense(const CUtensorMap* maps, const DenseArgs& a, int grid, size_t smem,
+                         cudaStream_t s, bool pdl);
+cudaError_t launch_moe_gate_up(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
+                               cudaStream_t s, bool pdl);
+cudaError_t launch_moe_down(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
+                            cudaStream_t s, bool pdl);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
+
+}  // namespace nvfp4

@@ -1,0 +1,424 @@
+// Top-k routed NVFP4 MoE decode layer with an always-on shared expert.
+//
+//   gate_up kernel: for every active expert e and every 32-wide block j of
+//     the intermediate dimension, one work item streams gate rows
+//     [32j, 32j+32) and up rows [I+32j, I+32j+32) over the full hidden K,
+//     against the FP16-staged activations of the tokens routed to e, and
+//     writes h = silu(gate) * up (FP32) for each (token, slot) pair.
+//   down kernel: for every active expert and 64-row tile of the down matrix,
+//     one item computes the expert's down output for its pairs (FP32); the
+//     last item to finish a tile column (atomic counter) combines
+//     out[t] = sum_j w[t][j] * y[pair(t, j)] + y[shared pair(t)] in slot
+//     order and writes BF16.
+//   Both kernels rebuild the same schedule from the ids in every CTA: expert
+//   histogram, exclusive offsets, the ascending list of active experts (the
+//   shared expert is id E, last), and for every flat slot t*k+j its pair
+//   index = offset[id] + number of earlier slots with the same id.  Only
+//   active experts' weights are streamed.
+//
+// Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
+// faster" / "One environment variable" (the fused MoE finalize: weighted
+// combine of the top-k expert outputs) and "What didn't work" (the shared
+// expert kept as its own always-on expert).
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "stream.cuh"
+
+namespace nvfp4 {
+
+__device__ __forceinline__ uint8_t* align1024m(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+struct Sched {
+  int* cnt;        // [E+1]
+  int* off;        // [E+2]
+  int* active;     // [E+1]
+  int* run;        // [E+1]
+  int* flat_pair;  // [P]
+  int* pair_tok;   // [P+T]
+  int* n_active;   // [1]
+};
+
+__device__ __forceinline__ Sched sched_layout(uint8_t* base, int E, int P) {
+  int* p = reinterpret_cast<int*>(base);
+  Sched s;
+  s.cnt = p;
+  s.off = s.cnt + (E + 1);
+  s.active = s.off + (E + 2);
+  s.run = s.active + (E + 1);
+  s.flat_pair = s.run + (E + 1);
+  s.pair_tok = s.flat_pair + P;
+  s.n_active = s.pair_tok + P + 32;
+  return s;
+}
+
+// All threads of the CTA.  Deterministic: the result does not depend on
+// the order of the shared-memory atomics.
+__device__ void build_schedule(const int32_t* ids, int T, int k, int E, int has_shared,
+                               const Sched& s, uint32_t* status) {
+  const int P = T * k;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i <= E; i += nthr) {
+    s.cnt[i] = 0;
+    s.run[i] = 0;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int p = tid; p < P; p += nthr) {
+    const int id = ids[p];
+    if (id >= 0 && id < E)
+      atomicAdd(&s.cnt[id], 1);
+    else
+      bad = true;
+  }
+  if (bad && blockIdx.x == 0) atomicOr(status, kStatusBadId);
+  if (tid == 0) s.cnt[E] = has_shared ? T : 0;
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0, acarry = 0;
+    for (int base = 0; base <= E; base += 32) {
+      const int i = base + lane;
+      const int c = (i <= E) ? s.cnt[i] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (i <= E) s.off[i] = carry + incl - c;
+      const unsigned bal = __ballot_sync(0xffffffffu, c > 0);
+      if (c > 0) s.active[acarry + __popc(bal & ((1u << lane) - 1u))] = i;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+      acarry += __popc(bal);
+    }
+    if (lane == 0) {
+      s.off[E + 1] = carry;
+      *s.n_active = acarry;
+    }
+    __syncwarp();
+    for (int base = 0; base < P; base += 32) {
+      const int p = base + lane;
+      const int id = (p < P) ? ids[p] : -1;
+      const bool valid = (p < P) && id >= 0 && id < E;
+      const unsigned grp = __match_any_sync(0xffffffffu, valid ? id : -1 - lane);
+      if (valid) {
+        const int pr = s.off[id] + s.run[id] + __popc(grp & ((1u << lane) - 1u));
+        s.flat_pair[p] = pr;
+        s.pair_tok[pr] = p / k;
+      } else if (p < P) {
+        s.flat_pair[p] = -1;
+      }
+      __syncwarp();
+      if (valid && lane == 31 - __clz(grp)) s.run[id] += __popc(grp);
+      __syncwarp();
+    }
+    if (has_shared)
+      for (int t = lane; t < T; t += 32) s.pair_tok[s.off[E] + t] = t;
+  }
+  __syncthreads();
+}
+
+struct MoeSmem {
+  Ring ring;
+  int* sig;
+  float* rms;
+  volatile int* abort_flag;
+  volatile int* bcast;
+  float* ep;
+  uint8_t* xs;
+  Sched sched;
+};
+
+__device__ __forceinline__ MoeSmem moe_smem(uint8_t* smem_raw, const MoeArgs& a) {
+  uint8_t* smem = align1024m(smem_raw);
+  MoeSmem m;
+  m.ring = Ring{smem + kSmemRing, reinterpret_cast<uint64_t*>(smem + kSmemBars),
+                reinterpret_cast<uint64_t*>(smem + kSmemBars) + kStages};
+  m.sig = reinterpret_cast<int*>(smem + kSmemMisc);
+  m.rms = reinterpret_cast<float*>(smem + kSmemMisc + 128);
+  m.abort_flag = reinterpret_cast<int*>(smem + kSmemMisc + 256);
+  m.bcast = reinterpret_cast<int*>(smem + kSmemMisc + 260);
+  m.ep = reinterpret_cast<float*>(smem + kSmemEp);
+  m.xs = smem + a.x_offset;
+  m.sched = sched_layout(smem + a.sched_offset, a.E, a.T * a.k);
+  return m;
+}
+
+// ---------------------------------------------------------------- gate_up
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gate_up_kernel(const __grid_constant__ CUtensorMap gu_codes,
+                       const __grid_constant__ CUtensorMap gu_scales,
+                       const __grid_constant__ CUtensorMap sh_codes,
+                       const __grid_constant__ CUtensorMap sh_scales, const MoeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const MoeSmem S = moe_smem(smem_raw, a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ring_init(S.ring);
+    *S.abort_flag = 0;
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, S.sched, a.status);
+
+  const int G = gridDim.x;
+  const int per_e = a.I / 32;
+  const int items = *S.sched.n_active * per_e;
+  const int nkb = a.H / kStageK;
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      Pipe p;
+      long issued = 0;
+      for (int it = blockIdx.x; it < items; it += G) {
+        const int e = S.sched.active[it / per_e];
+        const int jb = it % per_e;
+        const bool sh = (e == a.E);
+        const CUtensorMap* mc = sh ? &sh_codes : &gu_codes;
+        const CUtensorMap* ms = sh ? &sh_scales : &gu_scales;
+        const int base = sh ? 0 : e * 2 * a.I;
+        const int row0 = base + jb * 32, row1 = base + a.I + jb * 32;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!produce_stage(S.ring, p, mc, ms, row0, row1, kb, pol, a.status, S.abort_flag))
+            goto drained;
+          ++issued;
+        }
+      }
+    drained:
+      producer_drain(S.ring, p, issued, a.status);
+    }
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  Pipe p;
+  int staged_e = -1;
+  for (int it = blockIdx.x; it < items; it += G) {
+    const int e = S.sched.active[it / per_e];
+    const int jb = it % per_e;
+    const int cnt = S.sched.cnt[e];
+    const int off = S.sched.off[e];
+    const int ntiles = (cnt + 7) >> 3;
+    if (e != staged_e) {
+      const __nv_bfloat16* X = a.x;
+      const int64_t ldx = a.ldx;
+      const int* ptok = S.sched.pair_tok + off;
+      stage_rows<__nv_bfloat16>([&](int q) { return X + ptok[q] * ldx; }, cnt, ntiles * 8, 0,
+                                a.H, a.H, S.xs, a.xrow_bytes, S.sig, a.rms ? S.rms : nullptr,
+                                warp, lane);
+      staged_e = e;
+      consumer_sync();
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!*S.abort_flag) wait_or_abort(&S.ring.full[p.stage], p.phase, a.status, S.abort_flag);
+      consume_stage(S.ring.codes(p.stage), S.ring.scales(p.stage), S.xs, a.xrow_bytes,
+                    kb * kStageK, warp, lane, ntiles, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ring.empty[p.stage]);
+      p.advance();
+    }
+    const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+    int R0, R1, c0;
+    acc_coords(warp, lane, R0, R1, c0);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      if (nt < ntiles) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int q = nt * 8 + c0 + (q4 & 1);
+          const int R = (q4 < 2) ? R0 : R1;
+          if (q < cnt) {
+            float v = scale_pow2(acc[nt][q4], -S.sig[q]) * g;
+            if (a.rms) v *= S.rms[q];
+            S.ep[q * 64 + R] = v;
+          }
+        }
+      }
+    }
+    consumer_sync();
+    // tile rows [0, 32) are gate j = 32jb + r, rows [32, 64) the matching up
+    for (int i = tid; i < cnt * 32; i += kConsumerThreads) {
+      const int q = i >> 5, r = i & 31;
+      const float gt = S.ep[q * 64 + r];
+      const float up = S.ep[q * 64 + 32 + r];
+      const float hv = gt / (1.0f + expf(-gt)) * up;
+      a.h[static_cast<size_t>(off + q) * a.I + jb * 32 + r] = hv;
+    }
+    consumer_sync();
+  }
+}
+
+// ---------------------------------------------------------------- down + combine
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_down_kernel(const __grid_constant__ CUtensorMap dn_codes,
+                    const __grid_constant__ CUtensorMap dn_scales,
+                    const __grid_constant__ CUtensorMap sh_codes,
+                    const __grid_constant__ CUtensorMap sh_scales, const MoeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const MoeSmem S = moe_smem(smem_raw, a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    ring_init(S.ring);
+    *S.abort_flag = 0;
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, S.sched, a.status);
+
+  const int G = gridDim.x;
+  const int per_e = a.H / kTileRows;
+  const int n_active = *S.sched.n_active;
+  const int items = n_active * per_e;
+  const int nkb = a.I / kStageK;
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      Pipe p;
+      long issued = 0;
+      for (int it = blockIdx.x; it < items; it += G) {
+        const int e = S.sched.active[it / per_e];
+        const int nt = it % per_e;
+        const bool sh = (e == a.E);
+        const CUtensorMap* mc = sh ? &sh_codes : &dn_codes;
+        const CUtensorMap* ms = sh ? &sh_scales : &dn_scales;
+        const int row0 = (sh ? 0 : e * a.H) + nt * kTileRows;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!produce_stage(S.ring, p, mc, ms, row0, row0 + kBoxRows, kb, pol, a.status,
+                             S.abort_flag))
+            goto drained;
+          ++issued;
+        }
+      }
+    drained:
+      producer_drain(S.ring, p, issued, a.status);
+    }
+    return;
+  }
+
+  const int tid = threadIdx.x;
+  if (items == 0 && blockIdx.x == 0) {
+    // nothing routed and no shared expert: the layer output is zero
+    for (int i = tid; i < a.T * a.H; i += kConsumerThreads)
+      a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
+  }
+  Pipe p;
+  int staged_e = -1;
+  for (int it = blockIdx.x; it < items; it += G) {
+    const int e = S.sched.active[it / per_e];
+    const int nt = it % per_e;
+    const int cnt = S.sched.cnt[e];
+    const int off = S.sched.off[e];
+    const int ntiles = (cnt + 7) >> 3;
+    if (e != staged_e) {
+      const float* Hs = a.h;
+      const int I = a.I;
+      stage_rows<float>([&](int q) { return Hs + static_cast<size_t>(off + q) * I; }, cnt,
+                        ntiles * 8, 0, a.I, a.I, S.xs, a.xrow_bytes, S.sig, nullptr, warp, lane);
+      staged_e = e;
+      consumer_sync();
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!*S.abort_flag) wait_or_abort(&S.ring.full[p.stage], p.phase, a.status, S.abort_flag);
+      consume_stage(S.ring.codes(p.stage), S.ring.scales(p.stage), S.xs, a.xrow_bytes,
+                    kb * kStageK, warp, lane, ntiles, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.ring.empty[p.stage]);
+      p.advance();
+    }
+    const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+    int R0, R1, c0;
+    acc_coords(warp, lane, R0, R1, c0);
+#pragma unroll
+    for (int t4 = 0; t4 < 4; ++t4) {
+      if (t4 < ntiles) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int q = t4 * 8 + c0 + (q4 & 1);
+          const int R = (q4 < 2) ? R0 : R1;
+          if (q < cnt) S.ep[q * 64 + R] = scale_pow2(acc[t4][q4], -S.sig[q]) * g;
+        }
+      }
+    }
+    consumer_sync();
+    for (int i = tid; i < cnt * 64; i += kConsumerThreads) {
+      const int q = i >> 6, r = i & 63;
+      a.y[static_cast<size_t>(off + q) * a.H + nt * kTileRows + r] = S.ep[i];
+    }
+    __threadfence();
+    consumer_sync();
+    if (tid == 0) {
+      const uint32_t prev = atomicAdd(&a.tile_cnt[nt], 1u);
+      *S.bcast = (prev == static_cast<uint32_t>(n_active - 1)) ? 1 : 0;
+    }
+    consumer_sync();
+    if (*S.bcast) {
+      __threadfence();
+      const int* fp = S.sched.flat_pair;
+      const int sh_off = S.sched.off[a.E];
+      for (int i = tid; i < a.T * 64; i += kConsumerThreads) {
+        const int t = i >> 6, r = i & 63;
+        const int n = nt * kTileRows + r;
+        float s = 0.0f;
+        for (int j = 0; j < a.k; ++j) {
+          const int pr = fp[t * a.k + j];
+          if (pr >= 0) s = fmaf(a.w[t * a.k + j], __ldcg(a.y + static_cast<size_t>(pr) * a.H + n), s);
+        }
+        if (a.has_shared) s += __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+        a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
+      }
+      if (tid == 0) a.tile_cnt[nt] = 0u;
+    }
+    consumer_sync();
+  }
+}
+
+template <typename K>
+static cudaError_t launch4(K kernel, const CUtensorMap* maps, const MoeArgs& a, int grid,
+                           size_t smem, cudaStream_t s, bool pdl, bool& attr_set) {
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], a);
+}
+
+cudaError_t launch_moe_gate_up(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
+                               cudaStream_t s, bool pdl) {
+  static bool attr_set = false;
+  return launch4(moe_gate_up_kernel, maps, a, grid, smem, s, pdl, attr_set);
+}
+
+cudaError_t launch_moe_down(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
+                            cudaStream_t s, bool pdl) {
+  static bool attr_set = false;
+  return launch4(moe_down_kernel, maps, a, grid, smem, s, pdl, attr_set);
+}
+
+}  // namespace nvfp4

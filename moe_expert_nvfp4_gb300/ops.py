@@ -1,0 +1,253 @@
+"""Python binding of libnvfp4moe.so: torch tensors in, pointers and sizes out.
+
+Argument marshalling only -- every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+or the device is not a GB300 (compute capability 10.3) the calls raise.
+Names follow the C ABI in include/nvfp4moe.h.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnvfp4moe.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "nvfp4moe.h")
+
+NVFP4_OK = 0
+ERRORS = {-1: "invalid argument", -2: "misaligned", -3: "unsupported shape",
+          -4: "wrong architecture", -5: "CUDA error", -6: "workspace too small"}
+FLAG_RMS_INPUT = 1
+FLAG_NO_PDL = 2
+STATUS_BAD_EXPERT_ID = 1
+STATUS_WAIT_TIMEOUT = 2
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("global_scale", ctypes.c_void_p), ("n", ctypes.c_int32), ("k", ctypes.c_int32)]
+
+
+class _Stack(ctypes.Structure):
+    _fields_ = [("gu_codes", ctypes.c_void_p), ("gu_scales", ctypes.c_void_p),
+                ("dn_codes", ctypes.c_void_p), ("dn_scales", ctypes.c_void_p),
+                ("gu_global", ctypes.c_void_p), ("dn_global", ctypes.c_void_p),
+                ("num_experts", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("inter", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def declared_functions() -> list[str]:
+    """Function names declared in the public header."""
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|size_t|const char\*)\s+(\w+)\(", txt, re.M)))
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with moe_expert_nvfp4_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint32
+    L.nvfp4_device_check.argtypes = [i32]
+    L.nvfp4_workspace_init.argtypes = [vp, sz, vp]
+    L.nvfp4_gemm_skinny_workspace.argtypes = [i32, i32, i32]
+    L.nvfp4_gemm_skinny_workspace.restype = sz
+    L.nvfp4_gemm_skinny.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, i64, vp, u32, vp, sz, vp]
+    L.topk_softmax_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
+    L.moe_nvfp4_decode_workspace.argtypes = [i32, i32, ctypes.POINTER(_Stack)]
+    L.moe_nvfp4_decode_workspace.restype = sz
+    L.moe_nvfp4_decode.argtypes = [vp, i64, i32, vp, vp, i32, ctypes.POINTER(_Stack),
+                                   ctypes.POINTER(_Stack), vp, i64, u32, vp, sz, vp]
+    L.nvfp4_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+    L.nvfp4_last_dispatch.argtypes = [ctypes.c_char_p, sz]
+    L.nvfp4_last_error.restype = ctypes.c_char_p
+    for name in declared_functions():
+        getattr(L, name)  # every declared symbol must resolve
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load().nvfp4_last_error().decode()
+
+
+def last_dispatch() -> str:
+    buf = ctypes.create_string_buffer(512)
+    load().nvfp4_last_dispatch(buf, 512)
+    return buf.value.decode()
+
+
+def _check(rc: int, what: str):
+    if rc != NVFP4_OK:
+        raise RuntimeError(f"{what} failed ({rc}: {ERRORS.get(rc, '?')}): {last_error()}")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------ weights
+
+@dataclass
+class NVFP4Weight:
+    """An NVFP4 matrix [n, k] on the device: codes uint8 [n, k/2], scales
+    uint8 [n, k/16] (E4M3 bytes), global_scale float32 [1]."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    global_scale: torch.Tensor
+
+    @property
+    def n(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.codes.shape[1] * 2
+
+    def c(self) -> _Weight:
+        return _Weight(self.codes.data_ptr(), self.scales.data_ptr(), self.global_scale.data_ptr(),
+                       self.n, self.k)
+
+
+@dataclass
+class ExpertStack:
+    """E experts stacked: gu_codes [E, 2I, H/2], gu_scales [E, 2I, H/16],
+    dn_codes [E, H, I/2], dn_scales [E, H, I/16], gu_global / dn_global
+    float32 [E].  Gate rows are [0, I) of each gate_up matrix."""
+    gu_codes: torch.Tensor
+    gu_scales: torch.Tensor
+    dn_codes: torch.Tensor
+    dn_scales: torch.Tensor
+    gu_global: torch.Tensor
+    dn_global: torch.Tensor
+
+    @property
+    def num_experts(self) -> int:
+        return self.gu_codes.shape[0]
+
+    @property
+    def hidden(self) -> int:
+        return self.gu_codes.shape[2] * 2
+
+    @property
+    def inter(self) -> int:
+        return self.gu_codes.shape[1] // 2
+
+    def c(self) -> _Stack:
+        return _Stack(self.gu_codes.data_ptr(), self.gu_scales.data_ptr(), self.dn_codes.data_ptr(),
+                      self.dn_scales.data_ptr(), self.gu_global.data_ptr(), self.dn_global.data_ptr(),
+                      self.num_experts, self.hidden, self.inter)
+
+
+# ------------------------------------------------------------------ workspaces
+
+class Workspace:
+    """A zero-initialised device buffer reused across calls (one stream)."""
+
+    def __init__(self, nbytes: int, device=None):
+        self.buf = torch.zeros(max(int(nbytes), 256), dtype=torch.uint8,
+                               device=device or torch.device("cuda"))
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, stream=None) -> int:
+        """Read and clear the device status bits (synchronises)."""
+        v = ctypes.c_uint32(0)
+        _check(load().nvfp4_read_device_status(self.ptr(), ctypes.byref(v), _stream(stream)),
+               "nvfp4_read_device_status")
+        return v.value
+
+
+def gemm_workspace_bytes(m: int, n: int, k: int) -> int:
+    return int(load().nvfp4_gemm_skinny_workspace(m, n, k))
+
+
+def moe_workspace_bytes(t: int, k: int, experts: ExpertStack) -> int:
+    st = experts.c()
+    return int(load().moe_nvfp4_decode_workspace(t, k, ctypes.byref(st)))
+
+
+def device_check(device: int = 0) -> int:
+    return int(load().nvfp4_device_check(device))
+
+
+# ------------------------------------------------------------------ calls
+
+def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
+         argmax: bool = False, rms_input: bool = False, workspace: Optional[Workspace] = None,
+         pdl: bool = True, stream=None):
+    """C = A W^T for BF16 A [M, >=K] (row stride a.stride(0)).  Returns C
+    (BF16 [M, N]) and, with argmax=True, also int32 [M] row argmaxes."""
+    L = load()
+    m = a.shape[0]
+    if out is None:
+        out = torch.empty(m, w.n, dtype=torch.bfloat16, device=a.device)
+    ids = torch.empty(m, dtype=torch.int32, device=a.device) if argmax else None
+    if workspace is None:
+        workspace = Workspace(gemm_workspace_bytes(m, w.n, w.k), a.device)
+    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+    wc = w.c()
+    _check(L.nvfp4_gemm_skinny(a.data_ptr(), a.stride(0), m, ctypes.byref(wc), out.data_ptr(),
+                               out.stride(0), _ptr(ids), flags, workspace.ptr(), workspace.nbytes,
+                               _stream(stream)), "nvfp4_gemm_skinny")
+    return (out, ids) if argmax else out
+
+
+def route(logits: torch.Tensor, k: int, renormalize: bool = True,
+          ids: Optional[torch.Tensor] = None, weights: Optional[torch.Tensor] = None, stream=None):
+    """Top-k softmax routing of float32 logits [T, E] -> (ids int32 [T, k],
+    weights float32 [T, k])."""
+    L = load()
+    t, e = logits.shape
+    assert logits.is_contiguous() and logits.dtype == torch.float32
+    if ids is None:
+        ids = torch.empty(t, k, dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty(t, k, dtype=torch.float32, device=logits.device)
+    _check(L.topk_softmax_route(logits.data_ptr(), t, e, k, 1 if renormalize else 0,
+                                ids.data_ptr(), weights.data_ptr(), _stream(stream)),
+           "topk_softmax_route")
+    return ids, weights
+
+
+def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
+        shared: Optional[ExpertStack] = None, out: Optional[torch.Tensor] = None,
+        rms_input: bool = False, workspace: Optional[Workspace] = None, pdl: bool = True,
+        stream=None) -> torch.Tensor:
+    """MoE decode layer: BF16 x [T, >=H] -> BF16 out [T, H]."""
+    L = load()
+    t, k = ids.shape
+    assert ids.is_contiguous() and weights.is_contiguous()
+    if out is None:
+        out = torch.empty(t, experts.hidden, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = Workspace(moe_workspace_bytes(t, k, experts), x.device)
+    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+    ec = experts.c()
+    sc = shared.c() if shared is not None else None
+    _check(L.moe_nvfp4_decode(x.data_ptr(), x.stride(0), t, ids.data_ptr(), weights.data_ptr(), k,
+                              ctypes.byref(ec), ctypes.byref(sc) if sc is not None else None,
+                              out.data_ptr(), out.stride(0), flags, workspace.ptr(),
+                              workspace.nbytes, _stream(stream)), "moe_nvfp4_decode")
+    return out

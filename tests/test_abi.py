@@ -1,0 +1,87 @@
+"""The C-ABI library without a GPU: it loads, exports every function the
+public header declares, and its host-side validation returns the documented
+status codes before touching a device."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from moe_expert_nvfp4_gb300 import build as B
+from moe_expert_nvfp4_gb300 import ops
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return ops.load()
+
+
+def test_header_declares_the_boundary():
+    names = ops.declared_functions()
+    for n in ["nvfp4_gemm_skinny", "moe_nvfp4_decode", "topk_softmax_route",
+              "nvfp4_gemm_skinny_workspace", "moe_nvfp4_decode_workspace", "nvfp4_device_check",
+              "nvfp4_workspace_init", "nvfp4_read_device_status", "nvfp4_last_dispatch",
+              "nvfp4_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ops.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in ops.declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def _w(codes=1 << 20, scales=1 << 20, g=1 << 20, n=64, k=2048):
+    return ops._Weight(codes, scales, g, n, k)
+
+
+def _gemm(lib, a=1 << 20, lda=2048, m=4, w=None, c=1 << 20, ldc=64, ws=1 << 20, wsb=1 << 30):
+    w = w or _w()
+    return lib.nvfp4_gemm_skinny(a, lda, m, ctypes.byref(w), c, ldc, None, 0, ws, wsb, None)
+
+
+def test_gemm_validation_codes(lib):
+    assert _gemm(lib, a=0) == -1
+    assert _gemm(lib, m=0) == -3
+    assert _gemm(lib, m=33) == -3
+    assert _gemm(lib, w=_w(k=2000)) == -3           # K not a multiple of 256
+    assert _gemm(lib, w=_w(codes=(1 << 20) + 8)) == -2  # misaligned weight
+    assert _gemm(lib, a=(1 << 20) + 2) == -2           # misaligned A
+    assert _gemm(lib, lda=2052) == -2                  # row stride not 16-byte multiple
+    assert _gemm(lib, lda=1024) == -1                  # lda < K
+    assert _gemm(lib, w=_w(g=0)) == -1
+    assert "16-byte" in ops.last_error() or "NULL" in ops.last_error()
+
+
+def test_route_validation_codes(lib):
+    p = 1 << 20
+    assert lib.topk_softmax_route(0, 4, 256, 8, 1, p, p, None) == -1
+    assert lib.topk_softmax_route(p, 4, 8, 9, 1, p, p, None) == -1   # k > E
+    assert lib.topk_softmax_route(p, 4, 1024, 8, 1, p, p, None) == -3
+    assert lib.topk_softmax_route(p, 0, 256, 8, 1, p, p, None) == -1
+
+
+def _stack(e=256, h=2048, i=512, base=1 << 20):
+    return ops._Stack(base, base, base, base, base, base, e, h, i)
+
+
+def test_moe_validation_codes(lib):
+    p = 1 << 20
+    st = _stack()
+
+    def call(x=p, ldx=2048, t=4, k=8, ex=st, sh=None, out=p):
+        return lib.moe_nvfp4_decode(x, ldx, t, p, p, k, ctypes.byref(ex),
+                                    ctypes.byref(sh) if sh is not None else None, out, 2048, 0,
+                                    p, 1 << 30, None)
+
+    assert call(x=0) == -1
+    assert call(t=33) == -3
+    assert call(k=17) == -3
+    assert call(ex=_stack(h=2000)) == -3
+    assert call(ex=_stack(base=p + 4)) == -2
+    assert call(sh=_stack(e=2)) == -1
+    assert call(x=p + 2) == -2
