@@ -1,0 +1,415 @@
+#!/usr/bin/env python3
+"""Benchmark: the stacked NVFP4 decode step on GB300.
+
+One step = one pass of the whole hot path over one batch of T tokens:
+routing for 40 layers, then per layer the QKV (2048 -> 5120) and O
+(4096 -> 2048) projections and the 256+1-expert MoE layer (hidden 2048,
+intermediate 512, top-8), then the 151,936-row 4-bit head with argmax;
+about 18.8 GB of NVFP4 weights resident in HBM.  The metric is the
+algorithmic weight bytes one step must read (every projection, every
+distinct routed expert plus the shared expert of each layer, and the head)
+divided by the step time, in GB/s; the step's microseconds are reported too.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T]
+  python bench.py --impl reference ...   # the float64 CPU oracle, same metric
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun): the
+path has no exchange step, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 skinny-GEMM/MoE decode µs and HBM GB/s (frac of GB300 peak), M=1–32"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--tokens", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def workload_name(t):
+    return (f"stacked decode step, T={t} tokens: 40 x (QKV NVFP4 2048->5120, O NVFP4 "
+            f"4096->2048, MoE 256 routed + 1 shared experts, hidden 2048, inter 512, top-8) "
+            f"+ NVFP4 head 151936x2048 + argmax")
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(n):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n and world > 1:
+        raise SystemExit(f"--gpus {n} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.samples = []
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch recorded from an ncu capture, valid only while
+    the kernel sources are unchanged (same hash)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from moe_expert_nvfp4_gb300 import build as B
+    ent = d.get(kernel_key)
+    if not ent or ent.get("source_hash") != B.source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def timed_replays(graph, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps  # ms per replay
+
+
+class OracleSample:
+    """The float64 oracle on layer 0 of the step, one op at a time: routing,
+    the QKV projection, the O projection, then each expert the layer routes
+    to (shared expert first).  Each ``step()`` runs the next op in that
+    cycle and returns (weight bytes it read, seconds).  Host copies of the
+    weights are made once, outside the timed calls."""
+
+    def __init__(self, tokens, x_host, logits_host, layer=0):
+        import oracle as O
+        from moe_expert_nvfp4_gb300 import synth
+        from moe_expert_nvfp4_gb300.decode_step import ROLE_O, ROLE_QKV, nvfp4_bytes
+        H, I, E, k, qo, oi, seed = 2048, 512, 256, 8, 5120, 4096, 6
+        self.O = O
+        qkv = synth.nvfp4_weight(seed, qo, H, ROLE_QKV, layer)
+        o = synth.nvfp4_weight(seed, H, oi, ROLE_O, layer)
+        self.qkv = (qkv[0].numpy(), qkv[1].numpy(), synth.GLOBAL_SCALE)
+        self.o = (o[0].numpy(), o[1].numpy(), synth.GLOBAL_SCALE)
+        self.lg = logits_host[layer * tokens:(layer + 1) * tokens].numpy()
+        self.ids, self.w = O.topk_softmax_route(self.lg, k)
+        routed = sorted(set(self.ids.flatten().tolist()))
+        self.experts = {e: synth.expert_host(seed, layer, e, H, I) for e in [E] + routed}
+        self.x = x_host.double().numpy()
+        self.k, self.E = k, E
+        per_expert = nvfp4_bytes(2 * I, H) + nvfp4_bytes(H, I)
+        self.ops = ([("route", 0), ("qkv", nvfp4_bytes(qo, H)), ("o", nvfp4_bytes(H, oi))]
+                    + [(e, per_expert) for e in [E] + routed])
+        self.i = 0
+
+    def step(self):
+        O = self.O
+        name, nbytes = self.ops[self.i % len(self.ops)]
+        self.i += 1
+        t0 = time.perf_counter()
+        if name == "route":
+            O.topk_softmax_route(self.lg, self.k)
+        elif name == "qkv":
+            O.gemm_bf16(O.rms_scale(self.x), *self.qkv)
+        elif name == "o":
+            O.gemm_bf16(O.rms_scale(self.x[:, :2048].repeat(2, axis=1)), *self.o)
+        else:
+            rows = np.arange(self.x.shape[0]) if name == self.E else np.nonzero(
+                (self.ids == name).any(axis=1))[0]
+            O.expert_ffn64(O.rms_scale(self.x[rows]), self.experts[name])
+        return nbytes, time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads") for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    import torch
+    from moe_expert_nvfp4_gb300 import synth
+    t = args.tokens
+    x = synth.activations_bf16(6, t, 2048, 31)
+    lg = torch.cat([synth.router_logits(6, t, 256, 32, l) for l in range(1)])
+    sampler = OracleSample(t, x, lg)
+    for _ in range(args.warmup):
+        sampler.step()
+    sampler.i = 0
+    tot_b, tot_s = 0, 0.0
+    for _ in range(args.steps):
+        b, dt = sampler.step()
+        tot_b += b
+        tot_s += dt
+    value = tot_b / tot_s / 1e9
+    cores = blas_threads()
+    sample = (f"layer 0 of the T={t} step, one oracle op per timed step, cycling through "
+              f"routing, QKV, O and each routed expert ({len(sampler.ops)} ops)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_name(t), "tokens": t},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from moe_expert_nvfp4_gb300 import build as B
+    from moe_expert_nvfp4_gb300 import ops
+    from moe_expert_nvfp4_gb300.decode_step import DecodeStep
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    B.build()
+    ops.load()
+    if ops.device_check(local) != 0:
+        raise SystemExit(ops.last_error())
+    stream = torch.cuda.current_stream()
+    model = DecodeStep(seed=6)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def one_config(t, steps, warmup, sample_clocks):
+        b = model.buffers(t)
+        x, lg = model.inputs(t)
+        b["x"].copy_(x)
+        b["logits"].copy_(lg)
+        g = model.capture(b)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        clk = ClockSampler(local) if sample_clocks else None
+        if clk:
+            clk.start()
+            time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        ms = timed_replays(g, steps, stream)
+        torch.cuda.synchronize()
+        barrier()
+        clocks = clk.stop() if clk else None
+        if dist is not None:
+            tt = torch.tensor([ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            ms = float(tt.item())
+        nbytes = model.step_bytes(b["ids"], t)
+        status = b["ws"].status()
+        if status:
+            raise SystemExit(f"device status {status} after the timed steps")
+        am = b["argmax"].cpu()
+        if ms <= 0 or nbytes <= 0 or int(am.min()) < 0 or int(am.max()) >= model.s.vocab:
+            raise SystemExit("benchmark produced an empty or invalid result")
+        return b, g, x, lg, ms, nbytes, clocks
+
+    t = args.tokens
+    b, g, x, lg, ms, nbytes, clocks = one_config(t, args.steps, args.warmup, True)
+    n_launch = 1 + 4 * model.s.layers + 1
+    value = nbytes * world / (ms * 1e-3) / 1e9
+
+    # ---- end to end: pinned host inputs in, argmax ids out, every step
+    xh = x.pin_memory()
+    lgh = lg.pin_memory()
+    outh = torch.empty(t, dtype=torch.int32).pin_memory()
+    e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        b["x"].copy_(xh, non_blocking=True)
+        b["logits"].copy_(lgh, non_blocking=True)
+        g.replay()
+        outh.copy_(b["argmax"], non_blocking=True)
+        stream.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        b["x"].copy_(xh, non_blocking=True)
+        b["logits"].copy_(lgh, non_blocking=True)
+        g.replay()
+        outh.copy_(b["argmax"], non_blocking=True)
+        stream.synchronize()
+    e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
+    barrier()
+    e2e = {"value": nbytes * world / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": xh.numel() * xh.element_size() + lgh.numel() * lgh.element_size(),
+           "d2h_bytes_per_step": outh.numel() * outh.element_size(), "ms_per_step": e_ms,
+           "steps": e_steps}
+
+    # ---- the dominant op: the MoE layer call (gate_up + down kernels), 40 layers
+    s = model.s
+    moe_g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(moe_g):
+        for l in range(s.layers):
+            ops.moe(b["o"][0], b["ids"][l * t:(l + 1) * t], b["w"][l * t:(l + 1) * t],
+                    model.experts[l], model.shared[l], out=b["y"][0], rms_input=True,
+                    workspace=b["ws"])
+    for _ in range(3):
+        moe_g.replay()
+    torch.cuda.synchronize()
+    moe_ms = timed_replays(moe_g, max(5, min(args.steps, 100)), stream)
+    per_expert = 3 * 2048 * 512 * 9 // 16  # gate_up + down bytes of one expert
+    ids_l = b["ids"].view(s.layers, -1).cpu()
+    moe_bytes = sum((torch.unique(ids_l[l]).numel() + 1) * per_expert for l in range(s.layers))
+    peak, peak_kind = measured_peak()
+    achieved = moe_bytes / (moe_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(f"moe_layer_T{t}"),
+                "kernel": "moe_nvfp4_decode (moe_gate_up_kernel + moe_down_kernel), per call",
+                "bytes_per_launch": moe_bytes / s.layers, "us_per_launch": moe_ms * 1e3 / s.layers,
+                "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+
+    # ---- other token counts of the same step (context)
+    sweep = {}
+    if not args.no_sweep:
+        del moe_g
+        for tt in (1, 8, 32):
+            if tt == t:
+                sweep[str(tt)] = {"us_per_step": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                  "weight_bytes": nbytes}
+                continue
+            _, g2, _, _, ms2, nb2, _ = one_config(tt, max(5, min(args.steps, 100)), 3, False)
+            sweep[str(tt)] = {"us_per_step": ms2 * 1e3, "gbs": nb2 / (ms2 * 1e-3) / 1e9,
+                              "weight_bytes": nb2}
+            del g2
+
+    # ---- CPU baseline: the oracle on one layer of the same step
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        sampler = OracleSample(t, x, lg)
+        tot_b, tot_s = 0, 0.0
+        while tot_s < 10.0 or sampler.i < len(sampler.ops):
+            nb, dt = sampler.step()
+            tot_b += nb
+            tot_s += dt
+        cpu = {"value": tot_b / tot_s / 1e9, "unit": UNIT, "cores": blas_threads(),
+               "kind": "oracle",
+               "sample": f"oracle float64 ops of layer 0 at T={t} (routing, QKV, O and the "
+                         f"{len(sampler.ops) - 3} experts it reads), {sampler.i} ops, "
+                         f"{tot_s:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp16 mma (exact NVFP4 and BF16 operands), fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": workload_name(t), "tokens": t, "weight_bytes_per_step": nbytes,
+                       "frac_of_8tbs": value / world / 8000.0,
+                       "l2": "inputs larger than L2 (each step streams the weights once)",
+                       "parallelism": f"{world} independent replica(s)"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": n_launch * args.steps, "clocks": clocks, "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

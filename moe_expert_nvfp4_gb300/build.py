@@ -37,6 +37,19 @@ def _deps() -> list[str]:
     return out
 
 
+def source_hash() -> str:
+    """sha256 over the kernel sources and the public header (identifies the
+    kernel version a profile was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(ROOT, "include", "nvfp4moe.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True

@@ -1,0 +1,154 @@
+"""Stacked decode step: the full decode-time weight stream of a 4-bit MoE model.
+
+L layers, each: RMS glue -> QKV projection (hidden -> qkv_out) -> RMS glue on
+the first o_in columns -> O projection (o_in -> hidden) -> RMS glue ->
+top-k routed MoE layer with a shared expert; then RMS glue -> 4-bit head ->
+argmax.  Router logits are inputs (one [T, E] block per layer), so routing
+for all layers runs first, in one launch.  Every step is a library call
+(route, gemm, moe); the RMS glue is fused into the consuming call
+(NVFP4_FLAG_RMS_INPUT).  The whole step is captured as one CUDA graph; with
+programmatic dependent launch each kernel starts streaming its weights
+while its predecessor finishes.
+
+The glue is this library's stand-in for the model's normalisation layers
+(the pages give none): without it 40 random layers leave the BF16 range.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import ops, synth
+
+ROLE_QKV = 21
+ROLE_O = 22
+ROLE_HEAD = 23
+
+
+def nvfp4_bytes(n: int, k: int) -> int:
+    """Bytes one read of an NVFP4 [n, k] matrix moves (codes + block scales)."""
+    return n * k // 2 + n * k // 16
+
+
+@dataclass
+class StepShape:
+    layers: int = 40
+    num_experts: int = 256
+    hidden: int = 2048
+    inter: int = 512
+    top_k: int = 8
+    qkv_out: int = 5120
+    o_in: int = 4096
+    vocab: int = 151936
+
+
+class DecodeStep:
+    """Weights of the stacked model on the device, generated from ``seed``."""
+
+    def __init__(self, seed: int = 6, shape: StepShape = StepShape(), device: str = "cuda"):
+        self.seed, self.s, self.device = seed, shape, device
+        s = shape
+        g1 = torch.full((1,), synth.GLOBAL_SCALE, dtype=torch.float32, device=device)
+        gE = torch.full((s.num_experts,), synth.GLOBAL_SCALE, dtype=torch.float32, device=device)
+        self.qkv, self.o, self.experts, self.shared = [], [], [], []
+        for l in range(s.layers):
+            c, sc = synth.nvfp4_weight(seed, s.qkv_out, s.hidden, ROLE_QKV, l, device=device)
+            self.qkv.append(ops.NVFP4Weight(c, sc, g1))
+            c, sc = synth.nvfp4_weight(seed, s.hidden, s.o_in, ROLE_O, l, device=device)
+            self.o.append(ops.NVFP4Weight(c, sc, g1))
+            gc, gs, dc, ds = synth.expert_stack(seed, l, range(s.num_experts), s.hidden, s.inter,
+                                                device)
+            self.experts.append(ops.ExpertStack(gc, gs, dc, ds, gE, gE))
+            gc, gs, dc, ds = synth.expert_stack(seed, l, [s.num_experts], s.hidden, s.inter,
+                                                device)
+            self.shared.append(ops.ExpertStack(gc, gs, dc, ds, g1, g1))
+        c, sc = synth.nvfp4_weight(seed, s.vocab, s.hidden, ROLE_HEAD, device=device)
+        self.head = ops.NVFP4Weight(c, sc, g1)
+
+    # ------------------------------------------------------------ inputs
+    def inputs(self, tokens: int, seed: Optional[int] = None):
+        """Host inputs of one step: activations BF16 [T, hidden] and router
+        logits float32 [layers * T, E] (layer-major)."""
+        seed = self.seed if seed is None else seed
+        s = self.s
+        x = synth.activations_bf16(seed, tokens, s.hidden, 31)
+        lg = torch.cat([synth.router_logits(seed, tokens, s.num_experts, 32, l)
+                        for l in range(s.layers)])
+        return x, lg
+
+    # ------------------------------------------------------------ buffers
+    def buffers(self, tokens: int, keep: bool = False) -> dict:
+        s, d, T = self.s, self.device, tokens
+        ws = max(ops.gemm_workspace_bytes(T, s.qkv_out, s.hidden),
+                 ops.gemm_workspace_bytes(T, s.hidden, s.o_in),
+                 ops.gemm_workspace_bytes(T, s.vocab, s.hidden),
+                 ops.moe_workspace_bytes(T, s.top_k, self.experts[0]))
+        n_act = s.layers if keep else 1
+        b = {
+            "T": T,
+            "x": torch.zeros(T, s.hidden, dtype=torch.bfloat16, device=d),
+            "logits": torch.zeros(s.layers * T, s.num_experts, dtype=torch.float32, device=d),
+            "ids": torch.zeros(s.layers * T, s.top_k, dtype=torch.int32, device=d),
+            "w": torch.zeros(s.layers * T, s.top_k, dtype=torch.float32, device=d),
+            "q": [torch.zeros(T, s.qkv_out, dtype=torch.bfloat16, device=d) for _ in range(n_act)],
+            "o": [torch.zeros(T, s.hidden, dtype=torch.bfloat16, device=d) for _ in range(n_act)],
+            "y": [torch.zeros(T, s.hidden, dtype=torch.bfloat16, device=d)
+                  for _ in range(s.layers if keep else 2)],
+            "head": torch.zeros(T, s.vocab, dtype=torch.bfloat16, device=d),
+            "argmax": torch.zeros(T, dtype=torch.int32, device=d),
+            "ws": ops.Workspace(ws, d),
+            "keep": keep,
+        }
+        return b
+
+    # ------------------------------------------------------------ the step
+    def run(self, b: dict, pdl: bool = True) -> int:
+        """Launch one step on the current stream; returns the number of
+        kernel launches it made."""
+        s, T, ws = self.s, b["T"], b["ws"]
+        launches = 0
+        ops.route(b["logits"], s.top_k, True, b["ids"], b["w"])
+        launches += 1
+        x = b["x"]
+        for l in range(s.layers):
+            i = l if b["keep"] else 0
+            q, o = b["q"][i], b["o"][i]
+            y = b["y"][l if b["keep"] else l % 2]
+            ops.gemm(x, self.qkv[l], out=q, rms_input=True, workspace=ws, pdl=pdl)
+            ops.gemm(q[:, :s.o_in], self.o[l], out=o, rms_input=True, workspace=ws, pdl=pdl)
+            ops.moe(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T], self.experts[l],
+                    self.shared[l], out=y, rms_input=True, workspace=ws, pdl=pdl)
+            launches += 4
+            x = y
+        ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,
+                 pdl=pdl)
+        launches += 1
+        return launches
+
+    def capture(self, b: dict, pdl: bool = True) -> torch.cuda.CUDAGraph:
+        """Warm up, then capture one step as a CUDA graph."""
+        self.run(b, pdl)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(b, pdl)
+        torch.cuda.synchronize()
+        return g
+
+    # ------------------------------------------------------------ accounting
+    def step_bytes(self, ids: torch.Tensor, tokens: int) -> int:
+        """Algorithmic weight bytes of one step for the given routing: every
+        projection once, every distinct routed expert of each layer plus its
+        shared expert once, and the head."""
+        s = self.s
+        per_expert = nvfp4_bytes(2 * s.inter, s.hidden) + nvfp4_bytes(s.hidden, s.inter)
+        ids = ids.view(s.layers, tokens * s.top_k).cpu()
+        total = 0
+        for l in range(s.layers):
+            valid = ids[l][(ids[l] >= 0) & (ids[l] < s.num_experts)]
+            total += (torch.unique(valid).numel() + 1) * per_expert
+        total += s.layers * (nvfp4_bytes(s.qkv_out, s.hidden) + nvfp4_bytes(s.hidden, s.o_in))
+        total += nvfp4_bytes(s.vocab, s.hidden)
+        return total

@@ -196,14 +196,18 @@ def device_check(device: int = 0) -> int:
 
 def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
          argmax: bool = False, rms_input: bool = False, workspace: Optional[Workspace] = None,
-         pdl: bool = True, stream=None):
+         pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None):
     """C = A W^T for BF16 A [M, >=K] (row stride a.stride(0)).  Returns C
-    (BF16 [M, N]) and, with argmax=True, also int32 [M] row argmaxes."""
+    (BF16 [M, N]) and, with argmax=True (or an int32 [M] ``argmax_out``),
+    also the row argmaxes."""
     L = load()
     m = a.shape[0]
     if out is None:
         out = torch.empty(m, w.n, dtype=torch.bfloat16, device=a.device)
-    ids = torch.empty(m, dtype=torch.int32, device=a.device) if argmax else None
+    argmax = argmax or argmax_out is not None
+    ids = argmax_out
+    if argmax and ids is None:
+        ids = torch.empty(m, dtype=torch.int32, device=a.device)
     if workspace is None:
         workspace = Workspace(gemm_workspace_bytes(m, w.n, w.k), a.device)
     flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)

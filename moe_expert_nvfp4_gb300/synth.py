@@ -177,23 +177,49 @@ def expert_weight(seed: int, layer: int, e: int, hidden: int, inter: int, device
     return gc, gs, dc, ds
 
 
+def _keyed_bits(k0: torch.Tensor, k1: torch.Tensor, count: int, device) -> torch.Tensor:
+    """Words 0..count-1 of several streams at once: k0, k1 int64 [S, 1]."""
+    i = torch.arange(count, dtype=torch.int64, device=device).view(1, -1)
+    return _lowbias32(_lowbias32((i + k0) & _M32) ^ k1)
+
+
+def _stack_matrices(seed: int, role: int, layer: int, experts: list, n: int, k: int,
+                    codes_out: torch.Tensor, scales_out: torch.Tensor, group: int = 16):
+    """Fill codes_out [E, n, k/2] and scales_out [E, n, k/16] with the
+    matrices (seed, n, k, role, layer, e) for e in ``experts``; identical to
+    drawing each with nvfp4_weight, but generated ``group`` experts at once."""
+    dev = codes_out.device
+    for g0 in range(0, len(experts), group):
+        ids = experts[g0:g0 + group]
+        ck = [weight_keys(seed, n, k, role, layer, e) for e in ids]
+        c0 = torch.tensor([c[0][0] for c in ck], dtype=torch.int64, device=dev).view(-1, 1)
+        c1 = torch.tensor([c[0][1] for c in ck], dtype=torch.int64, device=dev).view(-1, 1)
+        s0 = torch.tensor([c[1][0] for c in ck], dtype=torch.int64, device=dev).view(-1, 1)
+        s1 = torch.tensor([c[1][1] for c in ck], dtype=torch.int64, device=dev).view(-1, 1)
+        w = _keyed_bits(c0, c1, n * k // 8, dev)
+        w = torch.where(w >= 2 ** 31, w - 2 ** 32, w)
+        codes_out[g0:g0 + len(ids)].copy_(
+            w.to(torch.int32).view(torch.uint8).view(len(ids), n, k // 2))
+        r = _keyed_bits(s0, s1, n * k // 16, dev) >> 8
+        idx = torch.searchsorted(_THRESH.to(dev), r.contiguous(), right=True)
+        scales_out[g0:g0 + len(ids)].copy_((idx + _SCALE_BASE).to(torch.uint8)
+                                           .view(len(ids), n, k // 16))
+        del w, r, idx
+
+
 def expert_stack(seed: int, layer: int, experts: Iterable[int], hidden: int, inter: int,
                  device="cpu"):
     """Stacked weights of the listed experts: gu_codes [E, 2I, H/2],
     gu_scales [E, 2I, H/16], dn_codes [E, H, I/2], dn_scales [E, H, I/16],
-    each expert generated on ``device`` directly into its slot."""
+    generated on ``device``; expert e's slices equal expert_weight(..., e)."""
     experts = list(experts)
     ne = len(experts)
     gu_c = torch.empty(ne, 2 * inter, hidden // 2, dtype=torch.uint8, device=device)
     gu_s = torch.empty(ne, 2 * inter, hidden // 16, dtype=torch.uint8, device=device)
     dn_c = torch.empty(ne, hidden, inter // 2, dtype=torch.uint8, device=device)
     dn_s = torch.empty(ne, hidden, inter // 16, dtype=torch.uint8, device=device)
-    for slot, e in enumerate(experts):
-        gc, gs, dc, ds = expert_weight(seed, layer, e, hidden, inter, device)
-        gu_c[slot].copy_(gc)
-        gu_s[slot].copy_(gs)
-        dn_c[slot].copy_(dc)
-        dn_s[slot].copy_(ds)
+    _stack_matrices(seed, ROLE_GATE_UP, layer, experts, 2 * inter, hidden, gu_c, gu_s)
+    _stack_matrices(seed, ROLE_DOWN, layer, experts, hidden, inter, dn_c, dn_s)
     return gu_c, gu_s, dn_c, dn_s
 
 

@@ -1,0 +1,204 @@
+"""GPU parity of top-k routing and the NVFP4 MoE decode layer (35B-A3B shape:
+hidden 2048, 256 experts of intermediate 512, top-8, one shared expert)
+against the float64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import (assert_close, device_experts, device_shared, device_weight, f64,
+                     host_expert_fn, host_weight)
+from moe_expert_nvfp4_gb300 import ops, synth
+
+pytestmark = pytest.mark.gpu
+E, H, I, K = 256, 2048, 512, 8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_nvfp4_gb300 import build
+    build.build()
+    ops.load()
+    assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
+
+
+@pytest.fixture(scope="module")
+def layer4():
+    """The seed-4 expert layer on the device, and its host accessor."""
+    ex = device_experts(4, 0, E, H, I)
+    sh = device_shared(4, 0, E, H, I)
+    get = host_expert_fn(4, 0, H, I)
+    return ex, sh, get
+
+
+# ------------------------------------------------------------------ routing
+
+def _check_route(logits, k, renorm=True):
+    ids, w = ops.route(logits.cuda(), k, renorm)
+    rid, rw = O.topk_softmax_route(logits.numpy(), k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().double().numpy(), rw, rtol=2e-6, atol=1e-12)
+    return ids, w
+
+
+@pytest.mark.parametrize("t", [1, 4, 8, 16, 32, 1280])
+def test_route_top8_of_256(t):
+    _check_route(synth.router_logits(4, t, E), K)
+
+
+def test_route_without_renormalisation_and_wide_shapes():
+    _check_route(synth.router_logits(5, 64, 256), 8, renorm=False)
+    _check_route(synth.router_logits(5, 40, 512), 32)
+    _check_route(synth.router_logits(5, 9, 37), 37)
+    _check_route(synth.router_logits(5, 3, 1), 1)
+
+
+def test_route_ties_lowest_index_first():
+    l = torch.zeros(3, 256, dtype=torch.float32)
+    l[0, [200, 5, 77]] = 1.0
+    l[1, :] = 0.5
+    l[2, 255] = 3.0
+    l[2, 0] = 3.0
+    ids, _ = _check_route(l, 8)
+    assert ids[0, :3].tolist() == [5, 77, 200]
+    assert ids[1].tolist() == list(range(8))
+    assert ids[2, :2].tolist() == [0, 255]
+
+
+# ------------------------------------------------------------------ MoE
+
+def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
+    ex, sh, get = layer4
+    x = synth.activations_bf16(seed, 32, H, 1)[:t]
+    if ids is None:
+        ids, w = ops.route(synth.router_logits(seed, 32, E, 1)[:t].cuda(), K)
+    ws = ops.Workspace(ops.moe_workspace_bytes(t, ids.shape[1], ex))
+    out = ops.moe(x.cuda(), ids, w, ex, sh if shared else None, rms_input=rms, workspace=ws)
+    disp = ops.last_dispatch()
+    status = ws.status()
+    x64 = f64(x)
+    ref64 = O.moe_decode64(O.rms_scale(x64) if rms else x64, ids.cpu().numpy(),
+                           w.cpu().double().numpy(), get, E, get(E) if shared else None)
+    return out, ref64, disp, status, (x, ids, w, ws)
+
+
+@pytest.mark.parametrize("t", [1, 4, 8, 16, 32])
+def test_moe_layer_35b_shape(layer4, t):
+    out, ref, disp, status, _ = _moe_case(layer4, t)
+    assert status == 0
+    assert "shared=1" in disp
+    assert_close(f64(out), O.bf16_round(ref), f"MoE T={t}")
+
+
+def test_moe_without_shared_expert(layer4):
+    out, ref, _, status, _ = _moe_case(layer4, 8, shared=False)
+    assert status == 0
+    assert_close(f64(out), O.bf16_round(ref), "MoE no shared")
+
+
+def test_moe_rms_input(layer4):
+    out, ref, disp, _, _ = _moe_case(layer4, 4, rms=True)
+    assert "rms=1" in disp
+    assert_close(f64(out), O.bf16_round(ref), "MoE rms")
+
+
+def test_moe_shared_expert_is_additive(layer4):
+    """The fused layer equals routed-only plus the shared expert on its own
+    (the failure mode of fusing the shared expert into the main MoE)."""
+    ex, sh, get = layer4
+    t = 6
+    x = synth.activations_bf16(4, t, H, 7).cuda()
+    ids, w = ops.route(synth.router_logits(4, t, E, 7).cuda(), K)
+    both = f64(ops.moe(x, ids, w, ex, sh))
+    routed = f64(ops.moe(x, ids, w, ex, None))
+    ref_sh = O.expert_ffn64(f64(x), get(E))
+    ref_both = O.moe_decode64(f64(x), ids.cpu().numpy(), w.cpu().double().numpy(), get, E, get(E))
+    assert_close(both, O.bf16_round(ref_both), "both")
+    # |both - routed - shared| within the sum of the two outputs' tolerances
+    rms = np.sqrt(np.mean(ref_both ** 2))
+    assert np.all(np.abs(both - routed - ref_sh) <= 1.6e-2 * np.abs(ref_both) + 6e-3 * rms)
+
+
+def test_moe_bad_ids_are_skipped_and_flagged(layer4):
+    ex, sh, get = layer4
+    t = 4
+    ids, w = ops.route(synth.router_logits(4, t, E, 9).cuda(), K)
+    ids[1, 3] = 300
+    ids[2, 0] = -5
+    out, ref, _, status, _ = _moe_case(layer4, t, ids=ids, w=w)
+    assert status & ops.STATUS_BAD_EXPERT_ID
+    assert_close(f64(out), O.bf16_round(ref), "bad ids")
+
+
+def test_moe_duplicate_ids_are_summed(layer4):
+    ids = torch.tensor([[3, 3, 9, 9, 9, 1, 2, 200]], dtype=torch.int32, device="cuda")
+    w = torch.full((1, 8), 0.125, dtype=torch.float32, device="cuda")
+    out, ref, _, status, _ = _moe_case(layer4, 1, ids=ids, w=w)
+    assert status == 0
+    assert_close(f64(out), O.bf16_round(ref), "duplicates")
+
+
+def test_moe_all_tokens_one_expert(layer4):
+    t = 32
+    ids = torch.arange(K, dtype=torch.int32, device="cuda").repeat(t, 1)
+    w = torch.full((t, K), 1.0 / K, dtype=torch.float32, device="cuda")
+    out, ref, _, status, _ = _moe_case(layer4, t, ids=ids, w=w)
+    assert status == 0
+    assert_close(f64(out), O.bf16_round(ref), "all tokens on experts 0..7")
+
+
+def test_moe_deterministic(layer4):
+    out, _, _, _, (x, ids, w, ws) = _moe_case(layer4, 16)
+    ex, sh, _ = layer4
+    again = [ops.moe(x.cuda(), ids, w, ex, sh, workspace=ws) for _ in range(3)]
+    torch.cuda.synchronize()
+    for a in again:
+        assert torch.equal(a, out)
+
+
+def test_moe_reads_only_routed_experts(layer4):
+    """Poison every expert that no token routes to: the output must not change."""
+    ex, sh, get = layer4
+    t = 2
+    x = synth.activations_bf16(4, t, H, 3).cuda()
+    ids, w = ops.route(synth.router_logits(4, t, E, 3).cuda(), K)
+    ref = ops.moe(x, ids, w, ex, sh)
+    used = set(ids.flatten().tolist())
+    unused = torch.tensor([e for e in range(E) if e not in used], device="cuda")
+    poisoned = ops.ExpertStack(ex.gu_codes.clone(), ex.gu_scales.clone(), ex.dn_codes.clone(),
+                               ex.dn_scales.clone(), ex.gu_global, ex.dn_global)
+    poisoned.gu_scales[unused] = 0x7F   # E4M3 NaN
+    poisoned.dn_scales[unused] = 0x7F
+    out = ops.moe(x, ids, w, poisoned, sh)
+    assert torch.equal(out, ref)
+
+
+# ------------------------------------------------------------------ MTP-verify batch
+
+def test_mtp_verify_batch_moe_then_lm_head_argmax():
+    """32 rows (8 requests x 4 draft tokens) through a seed-5 MoE layer, then
+    the 151,936-row 4-bit head with argmax; the head is checked from the
+    GPU's own BF16 MoE output (teacher forcing)."""
+    ex = device_experts(5, 0, E, H, I)
+    sh = device_shared(5, 0, E, H, I)
+    get = host_expert_fn(5, 0, H, I)
+    t = 32
+    x = synth.activations_bf16(5, t, H, 1)
+    logits = synth.router_logits(5, t, E, 1)
+    ids, w = _check_route(logits, K)
+    y = ops.moe(x.cuda(), ids, w, ex, sh)
+    ref = O.moe_decode64(f64(x), ids.cpu().numpy(), w.cpu().double().numpy(), get, E, get(E))
+    assert_close(f64(y), O.bf16_round(ref), "MTP MoE")
+    del ex, sh
+    lm = device_weight(5, 151936, H, 2)
+    logits_out, am = ops.gemm(y, lm, argmax=True)
+    ref_logits = O.gemm64(f64(y), *host_weight(5, 151936, H, 2))
+    assert_close(f64(logits_out), O.bf16_round(ref_logits), "MTP head")
+    gl = f64(logits_out)
+    assert np.array_equal(am.cpu().numpy(), O.argmax_first(gl, axis=1))
+    ref_ids = O.argmax_first(O.bf16_round(ref_logits), axis=1)
+    for r in np.nonzero(am.cpu().numpy() != ref_ids)[0]:
+        a, b = ref_logits[r, am[r].item()], ref_logits[r, ref_ids[r]]
+        assert abs(a - b) <= 2.0 ** (np.floor(np.log2(abs(b))) - 7), r

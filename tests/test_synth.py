@@ -60,3 +60,11 @@ def test_expert_host_matches_stack():
     st = synth.expert_stack(4, 0, [3, 9], 64, 32)
     h = synth.expert_host(4, 0, 9, 64, 32)
     assert np.array_equal(st[0][1].numpy(), h[0]) and np.array_equal(st[3][1].numpy(), h[4])
+
+
+def test_batched_expert_stack_equals_per_expert_draws():
+    st = synth.expert_stack(5, 2, [0, 7, 3, 256], 256, 256)
+    for slot, e in enumerate([0, 7, 3, 256]):
+        gc, gs, dc, ds = synth.expert_weight(5, 2, e, 256, 256)
+        assert torch.equal(st[0][slot], gc) and torch.equal(st[1][slot], gs)
+        assert torch.equal(st[2][slot], dc) and torch.equal(st[3][slot], ds)
