@@ -35,9 +35,11 @@
  *     nothing was launched and nvfp4_last_error() describes why.  No C++
  *     exception crosses this boundary.
  *   - Workspace: a device buffer of at least the queried size, zero-filled
- *     once before its first use (nvfp4_workspace_init).  Kernels leave their
- *     counters at zero again.  One workspace must not be used by two calls
- *     that may run concurrently.
+ *     once before its first use (nvfp4_workspace_init).  Every call keeps
+ *     the same header (status word, then tile counters that kernels leave at
+ *     zero again) and puts its scratch after it, so one workspace of the
+ *     largest queried size may serve any sequence of calls on one stream.
+ *     It must not be used by two calls that may run concurrently.
  *   - Problems found on the device (an expert id outside [0, E), a pipeline
  *     wait that gave up) never trap: they set bits in the workspace's status
  *     word, read by nvfp4_read_device_status().

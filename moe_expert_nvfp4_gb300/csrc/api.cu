@@ -127,6 +127,7 @@ bool plan_dense(int M, int N, int K, int sms, DensePlan* p) {
   int best_s = -1;
   double best_cost = 1e30;
   for (int s = 1; s <= p->nkb && s <= 64; ++s) {
+    if (s > 1 && p->n_tiles > kWsMaxCounters) break;  // split-K needs one counter per tile
     const int kmax = (p->nkb + s - 1) / s * kStageK;
     if (static_cast<size_t>(p->mpad) * (2 * kmax + kXPad) > x_avail) continue;
     const int per = sms / s * s;
@@ -148,8 +149,8 @@ bool plan_dense(int M, int N, int K, int sms, DensePlan* p) {
   const int kmax = (p->nkb + best_s - 1) / best_s * kStageK;
   p->xrow_bytes = 2 * kmax + kXPad;
   p->smem = kSmemAlignPad + kSmemSched + static_cast<size_t>(p->mpad) * p->xrow_bytes;
-  p->off_tile_cnt = 256;
-  p->off_partials = round_up(p->off_tile_cnt + 4ull * p->n_tiles, 256);
+  p->off_tile_cnt = kWsCounters;
+  p->off_partials = kWsScratch;
   const size_t part = p->splits > 1 ? 4ull * p->splits * p->n_tiles * M * 64 : 0;
   p->off_am = round_up(p->off_partials + part, 256);
   p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
@@ -179,8 +180,9 @@ bool plan_moe(int T, int k, int E, int H, int I, int sms, MoePlan* p) {
   p->grid_gu = static_cast<int>(gu_items < sms ? gu_items : sms);
   p->grid_dn = static_cast<int>(dn_items < sms ? dn_items : sms);
   const size_t pairs = static_cast<size_t>(p->P + T);
-  p->off_tile_cnt = 256;
-  p->off_h = round_up(p->off_tile_cnt + 4ull * (H / kTileRows), 256);
+  if (H / kTileRows > kWsMaxCounters) return false;
+  p->off_tile_cnt = kWsCounters;
+  p->off_h = kWsScratch;
   p->off_y = round_up(p->off_h + 4ull * pairs * I, 256);
   p->ws_bytes = round_up(p->off_y + 4ull * pairs * H, 256);
   return true;
@@ -275,8 +277,8 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   a.xrow_bytes = p.xrow_bytes;
   a.x_offset = kSmemSched;
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
-  a.status = reinterpret_cast<uint32_t*>(ws);
-  a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + 4);
+  a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
+  a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
   a.tile_cnt = reinterpret_cast<uint32_t*>(ws + p.off_tile_cnt);
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
@@ -380,7 +382,7 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.x_offset = kSmemSched + p.sched_bytes;
   a.sched_offset = kSmemSched;
-  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
   a.tile_cnt = reinterpret_cast<uint32_t*>(ws + p.off_tile_cnt);
   a.h = reinterpret_cast<float*>(ws + p.off_h);
   a.y = reinterpret_cast<float*>(ws + p.off_y);

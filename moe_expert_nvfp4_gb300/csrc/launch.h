@@ -17,8 +17,17 @@ constexpr int kSmemBars = kSmemRing + 8 * 9216;        // kStages * kStageBytes
 constexpr int kSmemMisc = kSmemBars + 2 * 8 * 8;       // full + empty mbarriers
 constexpr int kSmemEp = kSmemMisc + 512;               // sig[32], rms[32], flags
 constexpr int kSmemSched = kSmemEp + 32 * 64 * 4;      // epilogue tile [32][64] f32
-constexpr int kSchedInts(int E, int P, int T) { return 4 * (E + 2) + P + (P + T) + 4; }
 constexpr int kSmemAlignPad = 1024;
+
+// Workspace layout shared by every call, so that one workspace can serve a
+// sequence of different calls: [0, 256) status word and the argmax counter;
+// [256, kWsScratch) the tile counters (kept at zero between calls); call
+// scratch (partials, h, per-pair outputs) from kWsScratch on.
+constexpr size_t kWsStatus = 0;
+constexpr size_t kWsArgmaxCnt = 4;
+constexpr size_t kWsCounters = 256;
+constexpr int kWsMaxCounters = 16384;
+constexpr size_t kWsScratch = kWsCounters + 4 * kWsMaxCounters;
 
 struct DenseArgs {
   const __nv_bfloat16* A;

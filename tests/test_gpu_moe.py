@@ -202,3 +202,22 @@ def test_mtp_verify_batch_moe_then_lm_head_argmax():
     for r in np.nonzero(am.cpu().numpy() != ref_ids)[0]:
         a, b = ref_logits[r, am[r].item()], ref_logits[r, ref_ids[r]]
         assert abs(a - b) <= 2.0 ** (np.floor(np.log2(abs(b))) - 7), r
+
+
+def test_one_workspace_serves_moe_then_split_k_gemm(layer4):
+    """A dense split-K GEMM after an MoE call on the same workspace: the MoE
+    scratch must not disturb the GEMM's tile counters."""
+    ex, sh, _ = layer4
+    t = 4
+    W = device_weight(21, 5120, H)
+    ws = ops.Workspace(max(ops.gemm_workspace_bytes(t, 5120, H), ops.moe_workspace_bytes(t, K, ex)))
+    x = synth.activations_bf16(21, t, H).cuda()
+    ids, w = ops.route(synth.router_logits(21, t, E).cuda(), K)
+    for _ in range(2):
+        ops.moe(x, ids, w, ex, sh, workspace=ws)
+        c = ops.gemm(x, W, workspace=ws)
+        assert "splits=1" not in ops.last_dispatch()
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    ref = O.gemm_bf16(f64(x), *host_weight(21, 5120, H))
+    assert_close(f64(c), ref, "gemm after moe")
