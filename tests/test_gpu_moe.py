@@ -51,8 +51,10 @@ def test_route_top8_of_256(t):
 def test_route_without_renormalisation_and_wide_shapes():
     _check_route(synth.router_logits(5, 64, 256), 8, renorm=False)
     _check_route(synth.router_logits(5, 40, 512), 32)
-    _check_route(synth.router_logits(5, 9, 37), 37)
+    _check_route(synth.router_logits(5, 9, 37), 32)
     _check_route(synth.router_logits(5, 3, 1), 1)
+    with pytest.raises(RuntimeError, match="unsupported shape"):
+        ops.route(synth.router_logits(5, 2, 40).cuda(), 33)
 
 
 def test_route_ties_lowest_index_first():
