@@ -41,14 +41,16 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--tokens", type=int, default=8)
+    p.add_argument("--layers", type=int, default=40,
+                   help="layers of the stacked step (fewer only for small profiling runs)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args()
 
 
-def workload_name(t):
-    return (f"stacked decode step, T={t} tokens: 40 x (QKV NVFP4 2048->5120, O NVFP4 "
+def workload_name(t, layers=40):
+    return (f"stacked decode step, T={t} tokens: {layers} x (QKV NVFP4 2048->5120, O NVFP4 "
             f"4096->2048, MoE 256 routed + 1 shared experts, hidden 2048, inter 512, top-8) "
             f"+ NVFP4 head 151936x2048 + argmax")
 
@@ -248,7 +250,7 @@ def run_ours(args, rank, world, local):
 
     from moe_expert_nvfp4_gb300 import build as B
     from moe_expert_nvfp4_gb300 import ops
-    from moe_expert_nvfp4_gb300.decode_step import DecodeStep
+    from moe_expert_nvfp4_gb300.decode_step import DecodeStep, StepShape
 
     torch.cuda.set_device(local)
     dist = None
@@ -260,7 +262,7 @@ def run_ours(args, rank, world, local):
     if ops.device_check(local) != 0:
         raise SystemExit(ops.last_error())
     stream = torch.cuda.current_stream()
-    model = DecodeStep(seed=6)
+    model = DecodeStep(seed=6, shape=StepShape(layers=args.layers))
     torch.cuda.synchronize()
 
     def barrier():
@@ -390,7 +392,7 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 mma (exact NVFP4 and BF16 operands), fp32 accumulate",
             "data": "synthetic",
-            "config": {"workload": workload_name(t), "tokens": t, "weight_bytes_per_step": nbytes,
+            "config": {"workload": workload_name(t, args.layers), "tokens": t, "weight_bytes_per_step": nbytes,
                        "frac_of_8tbs": value / world / 8000.0,
                        "l2": "inputs larger than L2 (each step streams the weights once)",
                        "parallelism": f"{world} independent replica(s)"},
