@@ -70,6 +70,11 @@ enum {
 /* call flags */
 #define NVFP4_FLAG_RMS_INPUT 1u /* scale each input row by 1/sqrt(mean(x^2)+1e-6) */
 #define NVFP4_FLAG_NO_PDL 2u    /* launch without programmatic dependent launch */
+/* moe_nvfp4_decode: the ids and weights were complete before the previous
+ * kernel on the stream started (e.g. routing done earlier in the step), so
+ * the kernels may read them, and start streaming the routed experts'
+ * weights, before waiting for that kernel to finish. */
+#define NVFP4_FLAG_IDS_READY 4u
 
 /* device status bits */
 #define NVFP4_STATUS_BAD_EXPERT_ID 1u /* an id outside [0, E): its slot was skipped */

@@ -14,6 +14,7 @@
 #include "../../include/nvfp4moe.h"
 #include "common.cuh"
 #include "launch.h"
+#include "stream.cuh"
 
 namespace {
 
@@ -114,45 +115,31 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------- dense plan
 struct DensePlan {
-  int n_tiles, nkb, splits, grid, items, mpad, xrow_bytes;
+  int n_tiles, nkb, grid, mpad, win_stages, xrow_bytes;
+  long units;
   size_t smem;
-  size_t off_tile_cnt, off_partials, off_am, ws_bytes;
+  size_t off_partials, off_am, ws_bytes;
 };
 
+// Stream-K: one CTA per SM (or per unit when there are fewer units), each
+// with an equal contiguous range of (tile, k-stage) units; activations are
+// staged in windows of at most win_stages stages.
 bool plan_dense(int M, int N, int K, int sms, DensePlan* p) {
   p->n_tiles = (N + kTileRows - 1) / kTileRows;
+  if (p->n_tiles > kWsMaxCounters) return false;
   p->nkb = K / kStageK;
+  p->units = static_cast<long>(p->n_tiles) * p->nkb;
+  p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   p->mpad = (M + 7) / 8 * 8;
   const size_t x_avail = kSmemLimit - kSmemAlignPad - kSmemSched;
-  int best_s = -1;
-  double best_cost = 1e30;
-  for (int s = 1; s <= p->nkb && s <= 64; ++s) {
-    if (s > 1 && p->n_tiles > kWsMaxCounters) break;  // split-K needs one counter per tile
-    const int kmax = (p->nkb + s - 1) / s * kStageK;
-    if (static_cast<size_t>(p->mpad) * (2 * kmax + kXPad) > x_avail) continue;
-    const int per = sms / s * s;
-    if (per == 0) break;
-    const long items = static_cast<long>(p->n_tiles) * s;
-    const long grid = items < per ? items : per;
-    const long waves = (items + grid - 1) / grid;
-    const double cost = waves * ((p->nkb + s - 1) / s + (s > 1 ? 0.5 : 0.0));
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best_s = s;
-    }
-  }
-  if (best_s < 0) return false;
-  p->splits = best_s;
-  p->items = p->n_tiles * best_s;
-  const int per = sms / best_s * best_s;
-  p->grid = p->items < per ? p->items : per;
-  const int kmax = (p->nkb + best_s - 1) / best_s * kStageK;
-  p->xrow_bytes = 2 * kmax + kXPad;
+  int w = p->nkb;
+  while (w > 1 && static_cast<size_t>(p->mpad) * xrow_stride(w * kStageK) > x_avail) --w;
+  if (static_cast<size_t>(p->mpad) * xrow_stride(w * kStageK) > x_avail) return false;
+  p->win_stages = w;
+  p->xrow_bytes = xrow_stride(w * kStageK);
   p->smem = kSmemAlignPad + kSmemSched + static_cast<size_t>(p->mpad) * p->xrow_bytes;
-  p->off_tile_cnt = kWsCounters;
   p->off_partials = kWsScratch;
-  const size_t part = p->splits > 1 ? 4ull * p->splits * p->n_tiles * M * 64 : 0;
-  p->off_am = round_up(p->off_partials + part, 256);
+  p->off_am = round_up(p->off_partials + 4ull * p->grid * 2 * M * 64, 256);
   p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
   return true;
 }
@@ -169,10 +156,10 @@ bool plan_moe(int T, int k, int E, int H, int I, int sms, MoePlan* p) {
   p->P = T * k;
   p->tpad = (T + 7) / 8 * 8;
   p->sched_bytes = static_cast<int>(round_up(4ull * (4 * E + 5 + 2 * p->P + 33), 16));
-  p->xrow_gu = 2 * H + kXPad;
-  p->xrow_dn = 2 * I + kXPad;
+  p->xrow_gu = xrow_stride(H);
+  p->xrow_dn = xrow_stride(I);
   const size_t base = kSmemAlignPad + kSmemSched + p->sched_bytes;
-  p->smem_gu = base + static_cast<size_t>(p->tpad) * p->xrow_gu;
+  p->smem_gu = base + static_cast<size_t>(p->tpad + 1) * p->xrow_gu;  // + an all-zero row
   p->smem_dn = base + static_cast<size_t>(p->tpad) * p->xrow_dn;
   if (p->smem_gu > kSmemLimit || p->smem_dn > kSmemLimit) return false;
   const long max_active = (p->P < E ? p->P : E) + 1;
@@ -252,7 +239,7 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   int rc = current_device(&sms);
   if (rc) return rc;
   DensePlan p;
-  if (!plan_dense(M, N, K, sms, &p)) return fail(NVFP4_ERR_SHAPE, "no feasible split plan");
+  if (!plan_dense(M, N, K, sms, &p)) return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
   if (!workspace || workspace_bytes < p.ws_bytes)
     return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
   if ((rc = get_encoder())) return rc;
@@ -271,15 +258,14 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   a.N = N;
   a.K = K;
   a.n_tiles = p.n_tiles;
-  a.splits = p.splits;
   a.nkb = p.nkb;
-  a.items = p.items;
+  a.win_stages = p.win_stages;
   a.xrow_bytes = p.xrow_bytes;
   a.x_offset = kSmemSched;
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
   a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
-  a.tile_cnt = reinterpret_cast<uint32_t*>(ws + p.off_tile_cnt);
+  a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
   cudaError_t e = launch_dense(maps, a, p.grid, p.smem, reinterpret_cast<cudaStream_t>(stream),
@@ -287,10 +273,10 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   if (e != cudaSuccess) return cuda_fail(e, "dense_gemm_kernel launch");
   char buf[256];
   snprintf(buf, sizeof(buf),
-           "dense_gemm_kernel grid=%d splits=%d tiles=%d items=%d stages_per_item=%d smem=%zu "
+           "dense_gemm_kernel grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d smem=%zu "
            "argmax=%d rms=%d",
-           p.grid, p.splits, p.n_tiles, p.items, (p.nkb + p.splits - 1) / p.splits, p.smem,
-           argmax_out ? 1 : 0, a.rms);
+           p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_stages,
+           p.smem, argmax_out ? 1 : 0, a.rms);
   g_dispatch = buf;
   return NVFP4_OK;
 }
@@ -380,6 +366,7 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   a.I = I;
   a.has_shared = shared ? 1 : 0;
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
   a.x_offset = kSmemSched + p.sched_bytes;
   a.sched_offset = kSmemSched;
   a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
@@ -397,8 +384,8 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   char buf[256];
   snprintf(buf, sizeof(buf),
            "moe_gate_up_kernel grid=%d smem=%zu; moe_down_kernel grid=%d smem=%zu; T=%d k=%d "
-           "E=%d shared=%d rms=%d",
-           p.grid_gu, p.smem_gu, p.grid_dn, p.smem_dn, T, k, E, a.has_shared, a.rms);
+           "E=%d shared=%d rms=%d ids_ready=%d",
+           p.grid_gu, p.smem_gu, p.grid_dn, p.smem_dn, T, k, E, a.has_shared, a.rms, a.ids_ready);
   g_dispatch = buf;
   return NVFP4_OK;
 }

@@ -21,7 +21,7 @@ constexpr int kStageCodeBytes = kTileRows * kStageK / 2;   // 8192, 128B-swizzle
 constexpr int kStageScaleBytes = kTileRows * kStageK / 16; // 1024
 constexpr int kStageBytes = kStageCodeBytes + kStageScaleBytes;
 constexpr int kStages = 8;
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;            // + one producer warp
 constexpr int kMaxM = 32;

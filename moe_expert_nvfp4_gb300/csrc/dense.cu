@@ -1,16 +1,21 @@
 // Dense NVFP4 skinny GEMM: C[M, N] = A[M, K] * W[N, K]^T, M <= 32.
 //
-// Work item = (64-row tile of W, K split).  A persistent grid of at most one
-// CTA per SM walks items with stride gridDim.x; gridDim.x is a multiple of
-// the split count, so each CTA keeps one K slice and stages its slice of A
-// once.  Split partial sums go to the workspace; the last CTA to finish a
-// tile (atomic counter) adds them in split order, so results do not depend
-// on timing.  An optional argmax is fused the same way: per-tile (value,
-// index) partials, reduced by the last tile to finish.
+// Stream-K work split: the (64-row tile, 256-K stage) units of the whole
+// GEMM are cut into gridDim.x equal contiguous ranges, one per CTA, so every
+// SM streams the same number of weight bytes whatever the shape.  A CTA's
+// range covers the tail of one tile, whole tiles, and the head of another;
+// whole tiles are stored directly, partial ones go to a per-CTA workspace
+// slot and the last CTA to finish a tile (atomic counter) adds the slots in
+// CTA order, so results do not depend on timing.  Activations are staged
+// once per CTA when K fits in shared memory, else per window of stages,
+// each window folded into the FP32 total with its own power-of-two shift.
+// An optional argmax is fused the same way: per-tile (value, index)
+// partials, reduced by the last tile to finish.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
 // faster" / "Skinny matrix multiplies" (split-K for 4..16-row decode
-// matmuls; 4-bit weights with 16-bit activations).
+// matmuls that otherwise leave most SMs idle; 4-bit weights with 16-bit
+// activations).
 #include <cuda_bf16.h>
 #include <float.h>
 
@@ -23,8 +28,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// (value, index) pair order for argmax: larger value wins, equal values go
-// to the lower index; an empty slot has index INT_MAX.
+// (value, index) order for argmax: larger value wins, equal values go to the
+// lower index; an empty slot has index INT_MAX.
 __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
   return bi == 0x7fffffff || v > bv || (v == bv && i < bi);
 }
@@ -40,6 +45,15 @@ __device__ __forceinline__ void am_warp_reduce(float& bv, int& bi) {
     }
   }
 }
+
+struct StreamK {
+  long U;  // total units
+  int G;
+  __device__ __forceinline__ long begin(int b) const { return static_cast<long>(b) * U / G; }
+  __device__ __forceinline__ int cta_of(long u) const {
+    return static_cast<int>(((u + 1) * G - 1) / U);
+  }
+};
 
 __global__ void __launch_bounds__(kThreads, 1)
     dense_gemm_kernel(const __grid_constant__ CUtensorMap map_codes,
@@ -62,10 +76,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
-  const int G = gridDim.x;
-  const int split = blockIdx.x % a.splits;
-  const int kb0 = split * a.nkb / a.splits;
-  const int kb1 = (split + 1) * a.nkb / a.splits;
+  const StreamK sk{static_cast<long>(a.n_tiles) * a.nkb, static_cast<int>(gridDim.x)};
+  const int b = blockIdx.x;
+  const long u0 = sk.begin(b), u1 = sk.begin(b + 1);
 
   if (warp == kConsumerWarps) {
     // ---------------- producer: weights never depend on the previous grid,
@@ -76,16 +89,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = l2_policy_evict_first();
       Pipe p;
       long issued = 0;
-      for (int it = blockIdx.x; it < a.items; it += G) {
-        const int row0 = (it / a.splits) * kTileRows;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!produce_stage(ring, p, &map_codes, &map_scales, row0, row0 + kBoxRows, kb, pol,
-                             a.status, abort_flag))
-            goto drained;
-          ++issued;
-        }
+      for (long u = u0; u < u1; ++u) {
+        const int row0 = static_cast<int>(u / a.nkb) * kTileRows;
+        if (!produce_stage(ring, p, &map_codes, &map_scales, row0, row0 + kBoxRows,
+                           static_cast<int>(u % a.nkb), pol, a.status, abort_flag))
+          break;
+        ++issued;
       }
-    drained:
       producer_drain(ring, p, issued, a.status);
     }
     return;
@@ -94,66 +104,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- consumers
   pdl_wait();
   pdl_launch_dependents();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, cw = warp, h = cw >> 2, wg = cw & 3;
   const int ntiles = (a.M + 7) >> 3;
-  const int klen = (kb1 - kb0) * kStageK;
+  const int mpad = ntiles * 8;
   const __nv_bfloat16* A = a.A;
   const int64_t lda = a.lda;
-  stage_rows<__nv_bfloat16>([&](int q) { return A + q * lda; }, a.M, ntiles * 8, kb0 * kStageK,
-                            klen, a.K, xs, a.xrow_bytes, sig, a.rms ? rms : nullptr, warp, lane);
+  auto rowp = [&](int q) { return A + q * lda; };
+  const uint8_t* xr[4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) xr[nt] = xs + (nt * 8 + (lane >> 2)) * a.xrow_bytes;
+
+  const bool full_k = a.win_stages >= a.nkb;
+  int st0 = 0, st1 = 0;  // staged stage range [st0, st1)
+  if (full_k) {
+    stage_rows<__nv_bfloat16>(rowp, a.M, mpad, 0, a.K, a.K, xs, a.xrow_bytes, sig,
+                              a.rms ? rms : nullptr, cw, lane);
+    st1 = a.nkb;
+  } else if (a.rms) {
+    for (int q = cw; q < a.M; q += kConsumerWarps) {
+      float ss = 0.0f;
+      for (int v = lane; v < a.K / 8; v += 32) {
+        const uint4 u = *reinterpret_cast<const uint4*>(rowp(q) + v * 8);
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(static_cast<float>(e[i]), static_cast<float>(e[i]), ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) rms[q] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+    }
+  }
   consumer_sync();
   const float gs = *a.gscale;
+  const int first_tile = static_cast<int>(u0 / a.nkb);
 
   Pipe p;
-  for (int it = blockIdx.x; it < a.items; it += G) {
-    const int tile = it / a.splits;
-    float acc[4][4];
+  for (long u = u0; u < u1;) {
+    const int tile = static_cast<int>(u / a.nkb);
+    const int kbs = static_cast<int>(u % a.nkb);
+    const int kbe = static_cast<int>(min(static_cast<long>(a.nkb), kbs + (u1 - u)));
+    float tot[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-    for (int kb = kb0; kb < kb1; ++kb) {
-      if (!*abort_flag) wait_or_abort(&ring.full[p.stage], p.phase, a.status, abort_flag);
-      consume_stage(ring.codes(p.stage), ring.scales(p.stage), xs, a.xrow_bytes,
-                    (kb - kb0) * kStageK, warp, lane, ntiles, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring.empty[p.stage]);
-      p.advance();
-    }
-
-    // accumulators -> ep[m][row], undoing the FP16 staging shift
-    int R0, R1, c0;
-    acc_coords(warp, lane, R0, R1, c0);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      if (nt < ntiles) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = nt * 8 + c0 + (e & 1);
-          const int R = (e < 2) ? R0 : R1;
-          if (m < a.M) ep[m * 64 + R] = scale_pow2(acc[nt][e], -sig[m]);
-        }
+      for (int j = 0; j < 4; ++j) tot[i][j] = 0.0f;
+    for (int w0 = kbs; w0 < kbe; w0 += a.win_stages) {
+      const int w1 = min(kbe, w0 + a.win_stages);
+      if (w0 < st0 || w1 > st1) {
+        consumer_sync();
+        const int n1 = min(a.nkb, w0 + a.win_stages);
+        stage_rows<__nv_bfloat16>(rowp, a.M, mpad, w0 * kStageK, (n1 - w0) * kStageK, a.K, xs,
+                                  a.xrow_bytes, sig, nullptr, cw, lane);
+        st0 = w0;
+        st1 = n1;
+        consumer_sync();
       }
+      Acc acc;
+      acc.zero();
+      for (int kb = w0; kb < w1; ++kb) {
+        if (!*abort_flag) wait_or_abort(&ring.full[p.stage], p.phase, a.status, abort_flag);
+        consume_half(ring.codes(p.stage), ring.scales(p.stage), h, wg, lane, xr,
+                     (kb - st0) * kStageK, ntiles, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[p.stage]);
+        p.advance();
+      }
+      fold_window(acc, tot, ntiles, lane, [&](int q) { return sig[q]; });
     }
-    consumer_sync();
+    groups_to_ep(tot, ep, ntiles, a.M, cw, lane);
+    u += kbe - kbs;
 
     const int nval = a.M * 64;
-    if (a.splits > 1) {
-      float* part = a.partials + (static_cast<size_t>(split) * a.n_tiles + tile) * nval;
+    if (!(kbs == 0 && kbe == a.nkb)) {
+      // partial tile: publish this CTA's slot; the last contributor reduces
+      const int slot = (tile == first_tile) ? 0 : 1;
+      float* part = a.partials + static_cast<size_t>(b * 2 + slot) * nval;
       for (int i = tid; i < nval; i += kConsumerThreads) part[i] = ep[i];
       __threadfence();
       consumer_sync();
+      const int blo = sk.cta_of(static_cast<long>(tile) * a.nkb);
+      const int bhi = sk.cta_of(static_cast<long>(tile + 1) * a.nkb - 1);
       if (tid == 0) {
         const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
-        *bcast = (prev == static_cast<uint32_t>(a.splits - 1)) ? 1 : 0;
+        *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
       }
       consumer_sync();
       if (!*bcast) continue;  // uniform across the consumer warps
       __threadfence();
       for (int i = tid; i < nval; i += kConsumerThreads) {
         float s = 0.0f;
-        for (int sp = 0; sp < a.splits; ++sp)
-          s += __ldcg(a.partials + (static_cast<size_t>(sp) * a.n_tiles + tile) * nval + i);
+        for (int bb = blo; bb <= bhi; ++bb) {
+          const int sl = (sk.begin(bb) / a.nkb == tile) ? 0 : 1;
+          s += __ldcg(a.partials + static_cast<size_t>(bb * 2 + sl) * nval + i);
+        }
         ep[i] = s;
       }
       if (tid == 0) a.tile_cnt[tile] = 0u;
@@ -167,16 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n < a.N) {
         float v = ep[i] * gs;
         if (a.rms) v *= rms[m];
-        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        a.C[m * a.ldc + n] = b;
-        ep[i] = __bfloat162float(b);
+        const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+        a.C[m * a.ldc + n] = bv;
+        ep[i] = __bfloat162float(bv);
       } else {
         ep[i] = -FLT_MAX;
       }
     }
     if (a.argmax_out) {
       consumer_sync();
-      for (int m = warp; m < a.M; m += kConsumerWarps) {
+      for (int m = cw; m < a.M; m += kConsumerWarps) {
         float bv = -FLT_MAX;
         int bi = 0x7fffffff;
         const int n0 = tile * kTileRows;
@@ -200,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       consumer_sync();
       if (*bcast) {
         __threadfence();
-        for (int m = warp; m < a.M; m += kConsumerWarps) {
+        for (int m = cw; m < a.M; m += kConsumerWarps) {
           float bv = -FLT_MAX;
           int bi = 0x7fffffff;
           for (int j = lane; j < a.n_tiles; j += 32) {

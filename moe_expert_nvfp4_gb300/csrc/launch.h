@@ -37,15 +37,15 @@ struct DenseArgs {
   int32_t* argmax_out;     // nullable
   const float* gscale;
   int M, N, K;
-  int n_tiles, splits, nkb; // nkb = K / 256
-  int items;               // n_tiles * splits
+  int n_tiles, nkb;        // 64-row tiles; K / 256 stages per tile
+  int win_stages;          // stages of activations staged at once
   int xrow_bytes;          // staged row stride (bytes)
   int x_offset;            // smem offset of the x staging area
   int rms;                 // NVFP4_FLAG_RMS_INPUT
   uint32_t* status;
   uint32_t* tile_cnt;      // [n_tiles]
   uint32_t* argmax_cnt;    // [1]
-  float* partials;         // [splits][n_tiles][M][64]
+  float* partials;         // [gridDim.x][2][M][64]
   int2* am_part;           // [M][n_tiles] (float bits of value, index)
 };
 
@@ -63,6 +63,7 @@ struct MoeArgs {
   int T, k, E, H, I;
   int has_shared;
   int rms;
+  int ids_ready;           // ids/weights complete before the previous kernel started
   int xrow_bytes;
   int x_offset;
   int sched_offset;

@@ -148,6 +148,9 @@ __device__ __forceinline__ MoeSmem moe_smem(uint8_t* smem_raw, const MoeArgs& a)
 }
 
 // ---------------------------------------------------------------- gate_up
+// Items: (active expert a, 32-wide block jb of the intermediate dimension).
+// All T tokens are staged once per CTA; an item's MMA columns gather the
+// staged rows of the tokens routed to its expert.
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gate_up_kernel(const __grid_constant__ CUtensorMap gu_codes,
                        const __grid_constant__ CUtensorMap gu_scales,
@@ -160,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ring_init(S.ring);
     *S.abort_flag = 0;
   }
-  pdl_wait();
-  pdl_launch_dependents();
+  // ids written before the previous kernel started may be read before the
+  // dependency wait, so the weight stream can start during its tail
+  if (!a.ids_ready) pdl_wait();
   build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, S.sched, a.status);
 
   const int G = gridDim.x;
@@ -194,70 +198,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  const int tid = threadIdx.x;
+  // ---------------- consumers
+  if (a.ids_ready) pdl_wait();
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, cw = warp, h = cw >> 2, wg = cw & 3;
+  const int tpad = (a.T + 7) & ~7;
+  const __nv_bfloat16* X = a.x;
+  const int64_t ldx = a.ldx;
+  // rows [0, tpad) hold the tokens (zeros past T); row tpad is all zeros
+  stage_rows<__nv_bfloat16>([&](int q) { return X + q * ldx; }, a.T, tpad + 1, 0, a.H, a.H,
+                            S.xs, a.xrow_bytes, S.sig, a.rms ? S.rms : nullptr, cw, lane);
+  consumer_sync();
+  const uint8_t* zero_row = S.xs + tpad * a.xrow_bytes;
+
   Pipe p;
-  int staged_e = -1;
   for (int it = blockIdx.x; it < items; it += G) {
     const int e = S.sched.active[it / per_e];
     const int jb = it % per_e;
     const int cnt = S.sched.cnt[e];
-    const int off = S.sched.off[e];
+    const int* tok = S.sched.pair_tok + S.sched.off[e];
     const int ntiles = (cnt + 7) >> 3;
-    if (e != staged_e) {
-      const __nv_bfloat16* X = a.x;
-      const int64_t ldx = a.ldx;
-      const int* ptok = S.sched.pair_tok + off;
-      stage_rows<__nv_bfloat16>([&](int q) { return X + ptok[q] * ldx; }, cnt, ntiles * 8, 0,
-                                a.H, a.H, S.xs, a.xrow_bytes, S.sig, a.rms ? S.rms : nullptr,
-                                warp, lane);
-      staged_e = e;
-      consumer_sync();
+    const uint8_t* xr[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int q = nt * 8 + (lane >> 2);
+      xr[nt] = (q < cnt) ? S.xs + tok[q] * a.xrow_bytes : zero_row;
     }
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    Acc acc;
+    acc.zero();
     for (int kb = 0; kb < nkb; ++kb) {
       if (!*S.abort_flag) wait_or_abort(&S.ring.full[p.stage], p.phase, a.status, S.abort_flag);
-      consume_stage(S.ring.codes(p.stage), S.ring.scales(p.stage), S.xs, a.xrow_bytes,
-                    kb * kStageK, warp, lane, ntiles, acc);
+      consume_half(S.ring.codes(p.stage), S.ring.scales(p.stage), h, wg, lane, xr, kb * kStageK,
+                   ntiles, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.ring.empty[p.stage]);
       p.advance();
     }
-    const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
-    int R0, R1, c0;
-    acc_coords(warp, lane, R0, R1, c0);
+    float tot[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      if (nt < ntiles) {
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int q = nt * 8 + c0 + (q4 & 1);
-          const int R = (q4 < 2) ? R0 : R1;
-          if (q < cnt) {
-            float v = scale_pow2(acc[nt][q4], -S.sig[q]) * g;
-            if (a.rms) v *= S.rms[q];
-            S.ep[q * 64 + R] = v;
-          }
-        }
-      }
-    }
-    consumer_sync();
+      for (int j = 0; j < 4; ++j) tot[i][j] = 0.0f;
+    fold_window(acc, tot, ntiles, lane, [&](int q) { return q < cnt ? S.sig[tok[q]] : 0; });
+    groups_to_ep(tot, S.ep, ntiles, cnt, cw, lane);
     // tile rows [0, 32) are gate j = 32jb + r, rows [32, 64) the matching up
+    const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+    const int off = S.sched.off[e];
     for (int i = tid; i < cnt * 32; i += kConsumerThreads) {
       const int q = i >> 5, r = i & 31;
-      const float gt = S.ep[q * 64 + r];
-      const float up = S.ep[q * 64 + 32 + r];
-      const float hv = gt / (1.0f + expf(-gt)) * up;
-      a.h[static_cast<size_t>(off + q) * a.I + jb * 32 + r] = hv;
+      const float f = a.rms ? g * S.rms[tok[q]] : g;
+      const float gt = S.ep[q * 64 + r] * f;
+      const float up = S.ep[q * 64 + 32 + r] * f;
+      a.h[static_cast<size_t>(off + q) * a.I + jb * 32 + r] = gt / (1.0f + expf(-gt)) * up;
     }
     consumer_sync();
   }
 }
 
 // ---------------------------------------------------------------- down + combine
+// Items: (active expert a, group of m consecutive 64-row tiles), m chosen
+// from the number of active experts so that there are about two items per
+// CTA.  The expert's h rows are staged once per item.
+__device__ __forceinline__ int down_group(int n_active, int tiles_per_e, int grid) {
+  int m = 8;
+  while (m > 1 && (tiles_per_e % m != 0 || n_active * (tiles_per_e / m) < 2 * grid)) m >>= 1;
+  return m;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     moe_down_kernel(const __grid_constant__ CUtensorMap dn_codes,
                     const __grid_constant__ CUtensorMap dn_scales,
@@ -270,13 +277,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     ring_init(S.ring);
     *S.abort_flag = 0;
   }
-  pdl_wait();
-  pdl_launch_dependents();
+  // The ids are complete here: the gate_up grid before this one read them
+  // after its own dependency wait and only then allowed this grid to start.
   build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, S.sched, a.status);
 
   const int G = gridDim.x;
-  const int per_e = a.H / kTileRows;
+  const int tiles_per_e = a.H / kTileRows;
   const int n_active = *S.sched.n_active;
+  const int m = down_group(n_active, tiles_per_e, G);
+  const int per_e = tiles_per_e / m;
   const int items = n_active * per_e;
   const int nkb = a.I / kStageK;
 
@@ -287,17 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       long issued = 0;
       for (int it = blockIdx.x; it < items; it += G) {
         const int e = S.sched.active[it / per_e];
-        const int nt = it % per_e;
         const bool sh = (e == a.E);
         const CUtensorMap* mc = sh ? &sh_codes : &dn_codes;
         const CUtensorMap* ms = sh ? &sh_scales : &dn_scales;
-        const int row0 = (sh ? 0 : e * a.H) + nt * kTileRows;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!produce_stage(S.ring, p, mc, ms, row0, row0 + kBoxRows, kb, pol, a.status,
-                             S.abort_flag))
-            goto drained;
-          ++issued;
-        }
+        const int row_base = (sh ? 0 : e * a.H) + (it % per_e) * m * kTileRows;
+        for (int ti = 0; ti < m; ++ti)
+          for (int kb = 0; kb < nkb; ++kb) {
+            const int row0 = row_base + ti * kTileRows;
+            if (!produce_stage(S.ring, p, mc, ms, row0, row0 + kBoxRows, kb, pol, a.status,
+                               S.abort_flag))
+              goto drained;
+            ++issued;
+          }
       }
     drained:
       producer_drain(S.ring, p, issued, a.status);
@@ -305,85 +315,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  const int tid = threadIdx.x;
+  pdl_wait();  // h comes from the gate_up grid
+  pdl_launch_dependents();
+  const int tid = threadIdx.x, cw = warp, h = cw >> 2, wg = cw & 3;
   if (items == 0 && blockIdx.x == 0) {
     // nothing routed and no shared expert: the layer output is zero
     for (int i = tid; i < a.T * a.H; i += kConsumerThreads)
       a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
   }
   Pipe p;
-  int staged_e = -1;
   for (int it = blockIdx.x; it < items; it += G) {
     const int e = S.sched.active[it / per_e];
-    const int nt = it % per_e;
     const int cnt = S.sched.cnt[e];
     const int off = S.sched.off[e];
     const int ntiles = (cnt + 7) >> 3;
-    if (e != staged_e) {
-      const float* Hs = a.h;
-      const int I = a.I;
-      stage_rows<float>([&](int q) { return Hs + static_cast<size_t>(off + q) * I; }, cnt,
-                        ntiles * 8, 0, a.I, a.I, S.xs, a.xrow_bytes, S.sig, nullptr, warp, lane);
-      staged_e = e;
+    const float* Hs = a.h;
+    const int I = a.I;
+    consumer_sync();  // the previous item is done with the staged rows
+    stage_rows<float>([&](int q) { return Hs + static_cast<size_t>(off + q) * I; }, cnt,
+                      ntiles * 8, 0, a.I, a.I, S.xs, a.xrow_bytes, S.sig, nullptr, cw, lane);
+    consumer_sync();
+    const uint8_t* xr[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) xr[nt] = S.xs + (nt * 8 + (lane >> 2)) * a.xrow_bytes;
+    const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+    for (int ti = 0; ti < m; ++ti) {
+      const int nt_tile = (it % per_e) * m + ti;
+      Acc acc;
+      acc.zero();
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!*S.abort_flag) wait_or_abort(&S.ring.full[p.stage], p.phase, a.status, S.abort_flag);
+        consume_half(S.ring.codes(p.stage), S.ring.scales(p.stage), h, wg, lane, xr,
+                     kb * kStageK, ntiles, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ring.empty[p.stage]);
+        p.advance();
+      }
+      float tot[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tot[i][j] = 0.0f;
+      fold_window(acc, tot, ntiles, lane, [&](int q) { return S.sig[q]; });
+      groups_to_ep(tot, S.ep, ntiles, cnt, cw, lane);
+      for (int i = tid; i < cnt * 64; i += kConsumerThreads) {
+        const int q = i >> 6, r = i & 63;
+        a.y[static_cast<size_t>(off + q) * a.H + nt_tile * kTileRows + r] = S.ep[i] * g;
+      }
+      __threadfence();
+      consumer_sync();
+      if (tid == 0) {
+        const uint32_t prev = atomicAdd(&a.tile_cnt[nt_tile], 1u);
+        *S.bcast = (prev == static_cast<uint32_t>(n_active - 1)) ? 1 : 0;
+      }
+      consumer_sync();
+      if (*S.bcast) {
+        // last expert to finish this tile column: weighted combine in slot order
+        __threadfence();
+        const int* fp = S.sched.flat_pair;
+        const int sh_off = S.sched.off[a.E];
+        for (int i = tid; i < a.T * 64; i += kConsumerThreads) {
+          const int t = i >> 6, r = i & 63;
+          const int n = nt_tile * kTileRows + r;
+          float s = 0.0f;
+          for (int j = 0; j < a.k; ++j) {
+            const int pr = fp[t * a.k + j];
+            if (pr >= 0)
+              s = fmaf(a.w[t * a.k + j], __ldcg(a.y + static_cast<size_t>(pr) * a.H + n), s);
+          }
+          if (a.has_shared) s += __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+          a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
+        }
+        if (tid == 0) a.tile_cnt[nt_tile] = 0u;
+      }
       consumer_sync();
     }
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (!*S.abort_flag) wait_or_abort(&S.ring.full[p.stage], p.phase, a.status, S.abort_flag);
-      consume_stage(S.ring.codes(p.stage), S.ring.scales(p.stage), S.xs, a.xrow_bytes,
-                    kb * kStageK, warp, lane, ntiles, acc);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.ring.empty[p.stage]);
-      p.advance();
-    }
-    const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
-    int R0, R1, c0;
-    acc_coords(warp, lane, R0, R1, c0);
-#pragma unroll
-    for (int t4 = 0; t4 < 4; ++t4) {
-      if (t4 < ntiles) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int q = t4 * 8 + c0 + (q4 & 1);
-          const int R = (q4 < 2) ? R0 : R1;
-          if (q < cnt) S.ep[q * 64 + R] = scale_pow2(acc[t4][q4], -S.sig[q]) * g;
-        }
-      }
-    }
-    consumer_sync();
-    for (int i = tid; i < cnt * 64; i += kConsumerThreads) {
-      const int q = i >> 6, r = i & 63;
-      a.y[static_cast<size_t>(off + q) * a.H + nt * kTileRows + r] = S.ep[i];
-    }
-    __threadfence();
-    consumer_sync();
-    if (tid == 0) {
-      const uint32_t prev = atomicAdd(&a.tile_cnt[nt], 1u);
-      *S.bcast = (prev == static_cast<uint32_t>(n_active - 1)) ? 1 : 0;
-    }
-    consumer_sync();
-    if (*S.bcast) {
-      __threadfence();
-      const int* fp = S.sched.flat_pair;
-      const int sh_off = S.sched.off[a.E];
-      for (int i = tid; i < a.T * 64; i += kConsumerThreads) {
-        const int t = i >> 6, r = i & 63;
-        const int n = nt * kTileRows + r;
-        float s = 0.0f;
-        for (int j = 0; j < a.k; ++j) {
-          const int pr = fp[t * a.k + j];
-          if (pr >= 0) s = fmaf(a.w[t * a.k + j], __ldcg(a.y + static_cast<size_t>(pr) * a.H + n), s);
-        }
-        if (a.has_shared) s += __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
-        a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
-      }
-      if (tid == 0) a.tile_cnt[nt] = 0u;
-    }
-    consumer_sync();
   }
 }
 

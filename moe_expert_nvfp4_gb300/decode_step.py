@@ -119,7 +119,8 @@ class DecodeStep:
             ops.gemm(x, self.qkv[l], out=q, rms_input=True, workspace=ws, pdl=pdl)
             ops.gemm(q[:, :s.o_in], self.o[l], out=o, rms_input=True, workspace=ws, pdl=pdl)
             ops.moe(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T], self.experts[l],
-                    self.shared[l], out=y, rms_input=True, workspace=ws, pdl=pdl)
+                    self.shared[l], out=y, rms_input=True, workspace=ws, pdl=pdl,
+                    ids_ready=True)
             launches += 4
             x = y
         ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,

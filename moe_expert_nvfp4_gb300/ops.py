@@ -24,6 +24,7 @@ ERRORS = {-1: "invalid argument", -2: "misaligned", -3: "unsupported shape",
           -4: "wrong architecture", -5: "CUDA error", -6: "workspace too small"}
 FLAG_RMS_INPUT = 1
 FLAG_NO_PDL = 2
+FLAG_IDS_READY = 4
 STATUS_BAD_EXPERT_ID = 1
 STATUS_WAIT_TIMEOUT = 2
 
@@ -238,8 +239,9 @@ def route(logits: torch.Tensor, k: int, renormalize: bool = True,
 def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
         shared: Optional[ExpertStack] = None, out: Optional[torch.Tensor] = None,
         rms_input: bool = False, workspace: Optional[Workspace] = None, pdl: bool = True,
-        stream=None) -> torch.Tensor:
-    """MoE decode layer: BF16 x [T, >=H] -> BF16 out [T, H]."""
+        stream=None, ids_ready: bool = False) -> torch.Tensor:
+    """MoE decode layer: BF16 x [T, >=H] -> BF16 out [T, H].  ids_ready: the
+    ids/weights were complete before the previous kernel started."""
     L = load()
     t, k = ids.shape
     assert ids.is_contiguous() and weights.is_contiguous()
@@ -247,7 +249,8 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
         out = torch.empty(t, experts.hidden, dtype=torch.bfloat16, device=x.device)
     if workspace is None:
         workspace = Workspace(moe_workspace_bytes(t, k, experts), x.device)
-    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+    flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+             | (FLAG_IDS_READY if ids_ready else 0))
     ec = experts.c()
     sc = shared.c() if shared is not None else None
     _check(L.moe_nvfp4_decode(x.data_ptr(), x.stride(0), t, ids.data_ptr(), weights.data_ptr(), k,
