@@ -236,7 +236,8 @@ __device__ __forceinline__ int xstage_off(int kk) {
 __host__ __device__ constexpr int xrow_stride(int klen) { return 2 * klen + 64; }
 
 // Stage activation rows into shared memory as FP16.
-//   rows real rows; pad_rows >= rows rows are written (zeros past rows);
+//   rows <= kMaxM real rows; pad_rows >= rows rows are written (zeros past
+//   rows; only rows below kMaxM get sig / rms entries);
 //   src(q) = pointer to row q; elements [k0, k0+klen) are staged into
 //   xs + q * xrow_bytes in fragment order (xstage_off); row q gets its own
 //   power-of-two shift sig[q] (see f16_row_shift).  When rms != nullptr,
@@ -252,7 +253,7 @@ __device__ __forceinline__ void stage_rows(RowPtr src, int rows, int pad_rows, i
     if (q >= rows) {
       for (int v = lane; v < klen / 8; v += 32)
         *reinterpret_cast<uint4*>(dst + 16 * v) = make_uint4(0u, 0u, 0u, 0u);
-      if (lane == 0) {
+      if (lane == 0 && q < kMaxM) {  // sig and rms hold kMaxM entries
         sig[q] = 0;
         if (rms) rms[q] = 0.0f;
       }
