@@ -75,6 +75,9 @@ enum {
  * the kernels may read them, and start streaming the routed experts'
  * weights, before waiting for that kernel to finish. */
 #define NVFP4_FLAG_IDS_READY 4u
+/* Use the warp-level MMA kernels (mma.sync) instead of the default tcgen05
+ * kernels; kept for comparison, with the same results. */
+#define NVFP4_FLAG_WARP_MMA 8u
 
 /* device status bits */
 #define NVFP4_STATUS_BAD_EXPERT_ID 1u /* an id outside [0, E): its slot was skipped */

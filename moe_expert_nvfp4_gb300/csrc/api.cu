@@ -175,6 +175,57 @@ bool plan_moe(int T, int k, int E, int H, int I, int sms, MoePlan* p) {
   return true;
 }
 
+// ------------------------------------------------------------- tcgen05 plans
+constexpr size_t kTcXBudget = kSmemLimit - kSmemAlignPad - kTcOffSched;
+
+struct TcDensePlan {
+  int n_tiles, nkb, grid, npad, win_k;
+  long units;
+  size_t smem, off_partials, off_am, ws_bytes;
+};
+
+bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
+  p->n_tiles = (N + 127) / 128;
+  if (p->n_tiles > kTcColCntBase) return false;
+  p->nkb = K / kStageK;
+  p->units = static_cast<long>(p->n_tiles) * p->nkb;
+  p->grid = static_cast<int>(p->units < sms ? p->units : sms);
+  p->npad = M <= 16 ? 16 : 32;
+  int w = K;
+  while (w > kStageK && static_cast<size_t>(p->npad) * w * 2 > kTcXBudget) w -= kStageK;
+  if (static_cast<size_t>(p->npad) * w * 2 > kTcXBudget) return false;
+  p->win_k = w;
+  p->smem = kSmemAlignPad + kTcOffSched + static_cast<size_t>(p->npad) * w * 2;
+  p->off_partials = kWsScratch;
+  p->off_am = round_up(p->off_partials + 4ull * p->grid * 2 * 32 * 128, 256);
+  p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
+  return true;
+}
+
+struct TcMoePlan {
+  int P, npad, sched_bytes, grid;
+  size_t smem_gu, smem_dn, off_partials, off_h, off_y, ws_bytes;
+};
+
+bool plan_tc_moe(int T, int k, int E, int H, int I, int sms, TcMoePlan* p) {
+  p->P = T * k;
+  p->npad = T <= 16 ? 16 : 32;
+  p->sched_bytes = static_cast<int>(round_up(4ull * (4 * E + 5 + 2 * p->P + 33), 128));
+  const size_t base = kSmemAlignPad + kTcOffSched + p->sched_bytes;
+  p->smem_gu = base + static_cast<size_t>(p->npad) * H * 2;
+  p->smem_dn = base + static_cast<size_t>(p->npad) * I * 2;
+  if (p->smem_gu > kSmemLimit || p->smem_dn > kSmemLimit) return false;
+  const long max_active = (p->P < E ? p->P : E) + 1;
+  if (max_active * (H / 128) > kTcColCntBase || H / 128 > kWsMaxCounters - kTcColCntBase) return false;
+  p->grid = sms;
+  const size_t pairs = static_cast<size_t>(p->P + T);
+  p->off_partials = kWsScratch;
+  p->off_h = round_up(p->off_partials + 4ull * p->grid * 2 * 32 * 128, 256);
+  p->off_y = round_up(p->off_h + 4ull * pairs * I, 256);
+  p->ws_bytes = round_up(p->off_y + 4ull * pairs * H, 256);
+  return true;
+}
+
 int check_stack(const nvfp4_expert_stack* s, const char* name) {
   if (!s) return fail(NVFP4_ERR_INVALID, "%s is NULL", name);
   if (!s->gu_codes || !s->gu_scales || !s->dn_codes || !s->dn_scales || !s->gu_global ||
@@ -218,7 +269,10 @@ size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
   if (M < 1 || M > kMaxM || N < 1 || K < kStageK || K % kStageK) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
   DensePlan p;
-  return plan_dense(M, N, K, sms, &p) ? p.ws_bytes : 0;
+  TcDensePlan t;
+  const size_t a = plan_dense(M, N, K, sms, &p) ? p.ws_bytes : 0;
+  const size_t b = plan_tc_dense(M, N, K, sms, &t) ? t.ws_bytes : 0;
+  return a > b ? a : b;
 }
 
 int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
@@ -238,6 +292,49 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   int sms = 0;
   int rc = current_device(&sms);
   if (rc) return rc;
+  if (!(flags & NVFP4_FLAG_WARP_MMA)) {
+    TcDensePlan p;
+    if (!plan_tc_dense(M, N, K, sms, &p))
+      return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
+    if (!workspace || workspace_bytes < p.ws_bytes)
+      return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
+    if ((rc = get_encoder())) return rc;
+    CUtensorMap maps[4];
+    if ((rc = weight_maps(&maps[0], &maps[1], W->codes, W->scales, static_cast<uint64_t>(N), K)))
+      return rc;
+    maps[2] = maps[0];
+    maps[3] = maps[1];
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    TcArgs a = {};
+    a.A = static_cast<const __nv_bfloat16*>(A);
+    a.lda = lda;
+    a.C = static_cast<__nv_bfloat16*>(C);
+    a.ldc = ldc;
+    a.argmax_out = argmax_out;
+    a.gscale = W->global_scale;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+    a.win_k = p.win_k;
+    a.x_offset = kTcOffSched;
+    a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
+    a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
+    a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
+    a.partials = reinterpret_cast<float*>(ws + p.off_partials);
+    a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
+    cudaError_t e = launch_tc(kTcDense, maps, a, p.grid, p.smem,
+                              reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL));
+    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<dense> launch");
+    char buf[256];
+    snprintf(buf, sizeof(buf),
+             "stream_tc_kernel<dense> grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d "
+             "n=%d smem=%zu argmax=%d rms=%d",
+             p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_k, p.npad,
+             p.smem, argmax_out ? 1 : 0, a.rms);
+    g_dispatch = buf;
+    return NVFP4_OK;
+  }
   DensePlan p;
   if (!plan_dense(M, N, K, sms, &p)) return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
   if (!workspace || workspace_bytes < p.ws_bytes)
@@ -304,8 +401,12 @@ size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* expert
   if (!experts || T < 1 || T > kMaxM || k < 1 || k > 16) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
   MoePlan p;
-  if (!plan_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &p)) return 0;
-  return p.ws_bytes;
+  TcMoePlan t;
+  const size_t a = plan_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &p)
+                       ? p.ws_bytes : 0;
+  const size_t b = plan_tc_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &t)
+                       ? t.ws_bytes : 0;
+  return a > b ? a : b;
 }
 
 int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
@@ -330,6 +431,69 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   if (reinterpret_cast<uintptr_t>(out) & 1u) return fail(NVFP4_ERR_ALIGN, "out must be 2-byte aligned");
   int sms = 0;
   if ((rc = current_device(&sms))) return rc;
+  if (!(flags & NVFP4_FLAG_WARP_MMA)) {
+    TcMoePlan p;
+    if (!plan_tc_moe(T, k, E, H, I, sms, &p))
+      return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d, E=%d: staged activations exceed shared memory",
+                  T, H, E);
+    if (!workspace || workspace_bytes < p.ws_bytes)
+      return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
+    if ((rc = get_encoder())) return rc;
+    const nvfp4_expert_stack* sh = shared ? shared : experts;
+    CUtensorMap gu[4], dn[4];
+    if ((rc = weight_maps(&gu[0], &gu[1], experts->gu_codes, experts->gu_scales,
+                          2ull * I * E, H)) ||
+        (rc = weight_maps(&gu[2], &gu[3], sh->gu_codes, sh->gu_scales,
+                          2ull * I * sh->num_experts, H)) ||
+        (rc = weight_maps(&dn[0], &dn[1], experts->dn_codes, experts->dn_scales,
+                          static_cast<uint64_t>(H) * E, I)) ||
+        (rc = weight_maps(&dn[2], &dn[3], sh->dn_codes, sh->dn_scales,
+                          static_cast<uint64_t>(H) * sh->num_experts, I)))
+      return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    TcArgs a = {};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.ldx = ldx;
+    a.ids = topk_ids;
+    a.w = topk_w;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.ldo = ldo;
+    a.gu_global = experts->gu_global;
+    a.dn_global = experts->dn_global;
+    a.sh_gu_global = sh->gu_global;
+    a.sh_dn_global = sh->dn_global;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.has_shared = shared ? 1 : 0;
+    a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
+    a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+    a.sched_offset = kTcOffSched;
+    a.x_offset = kTcOffSched + p.sched_bytes;
+    a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
+    a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
+    a.partials = reinterpret_cast<float*>(ws + p.off_partials);
+    a.h = reinterpret_cast<float*>(ws + p.off_h);
+    a.y = reinterpret_cast<float*>(ws + p.off_y);
+    const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    a.win_k = H;
+    cudaError_t e = launch_tc(kTcGateUp, gu, a, p.grid, p.smem_gu, s, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<gate_up> launch");
+    a.win_k = I;
+    e = launch_tc(kTcDown, dn, a, p.grid, p.smem_dn, s, pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<down> launch");
+    char buf[256];
+    snprintf(buf, sizeof(buf),
+             "stream_tc_kernel<gate_up> grid=%d smem=%zu; stream_tc_kernel<down> grid=%d smem=%zu; "
+             "T=%d k=%d E=%d n=%d shared=%d rms=%d ids_ready=%d",
+             p.grid, p.smem_gu, p.grid, p.smem_dn, T, k, E, p.npad, a.has_shared, a.rms,
+             a.ids_ready);
+    g_dispatch = buf;
+    return NVFP4_OK;
+  }
   MoePlan p;
   if (!plan_moe(T, k, E, H, I, sms, &p))
     return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d: staged activations exceed shared memory", T, H);

@@ -73,6 +73,56 @@ struct MoeArgs {
   float* y;                // [T*k + T][H]
 };
 
+// ---- tcgen05 streaming kernel (stream_tc.cu) ------------------------------
+constexpr int kTcStages = 4;                              // 18 KB stages
+constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;
+constexpr int kTcOffBars = kTcStages * kTcStageBytes;     // 73728
+constexpr int kTcOffMisc = kTcOffBars + 256;
+constexpr int kTcOffEp = kTcOffMisc + 512;
+constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;      // after the [32][128] f32 tile
+constexpr int kTcThreads = 320;                           // producer, MMA, 8 decode warps
+constexpr int kTcColCntBase = 8192;                       // down combine counters
+
+enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2 };
+
+struct TcArgs {
+  // dense
+  const __nv_bfloat16* A;
+  int64_t lda;
+  __nv_bfloat16* C;
+  int64_t ldc;
+  int32_t* argmax_out;
+  const float* gscale;
+  int M, N, K;
+  // MoE
+  const __nv_bfloat16* x;
+  int64_t ldx;
+  const int32_t* ids;
+  const float* w;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  const float* gu_global;
+  const float* dn_global;
+  const float* sh_gu_global;
+  const float* sh_dn_global;
+  int T, k, E, H, I, has_shared, ids_ready;
+  float* h;
+  float* y;
+  // common
+  int rms;
+  int win_k;        // staged activation window capacity (elements, multiple of 256)
+  int x_offset;     // smem offset of the staged activations
+  int sched_offset; // smem offset of the expert schedule (MoE)
+  uint32_t* status;
+  uint32_t* tile_cnt;   // counters region
+  uint32_t* argmax_cnt;
+  float* partials;      // [grid][2][32][128]
+  int2* am_part;        // [M][n_tiles]
+};
+
+cudaError_t launch_tc(int mode, const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
+                      cudaStream_t s, bool pdl);
+
 struct RouteArgs {
   const float* logits;
   int T, E, k, renorm;

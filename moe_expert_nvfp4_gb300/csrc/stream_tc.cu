@@ -1,0 +1,757 @@
+// NVFP4 weight streaming on the 5th-generation tensor cores (tcgen05).
+//
+// One kernel, three epilogues: the dense skinny GEMM (C = A W^T, optional
+// argmax), the MoE gate_up projection (h = silu(gate) * up per routed pair)
+// and the MoE down projection with the weighted top-k combine.
+//
+// Tile = 128 weight rows = the 128 lanes of tensor memory, built from four
+// independent 32-row TMA boxes (for gate_up: the gate and up boxes of two
+// 32-wide intermediate blocks, possibly of different experts).  Stage = one
+// tile x 256 K: 16 KB of 128B-swizzled E2M1 codes + 2 KB of E4M3 scales.
+// Work split: the (tile, stage) units of the launch are cut into gridDim.x
+// equal contiguous ranges, one per CTA ("stream-K"); a tile split between
+// CTAs is reduced by the last CTA to finish it (atomic counter), adding the
+// per-CTA partials in CTA order, so results do not depend on timing.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer: streams stages into a 4-deep ring (full/empty
+//               mbarriers);
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma:
+//               D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
+//               memory), 16 MMAs per stage, N = tokens rounded up to 16;
+//   warps 2-9   decode: lane l of a warp in lane quarter q owns tile row
+//               32q + l; warps 2-5 decode the first 128 K of each stage,
+//               6-9 the second.  E2M1 -> FP16 by the hardware convert, times
+//               the E4M3 block scale (exact in FP16), written to a tensor-
+//               memory A buffer with tcgen05.st (two A buffers).  The same
+//               warps stage the activations (B) into shared memory as FP16
+//               with a power-of-two shift per row and window, read the FP32
+//               accumulator back with tcgen05.ld, undo the shift, and run the
+//               epilogue.
+//
+// Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
+// faster": "Skinny matrix multiplies" (split-K decode matmuls, 4-bit weights
+// with 16-bit activations), "One environment variable" (fused MoE finalize),
+// "What didn't work" (the shared expert kept separate, always on).
+#include <cuda_bf16.h>
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "sched.cuh"
+#include "tc.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kBox = 32;
+constexpr int kSK = 256;                       // K per stage
+constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
+constexpr int kStages = kTcStages;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
+constexpr int kDCol = 2 * kACols;              // D buffers at columns 256 and 288
+constexpr uint32_t kTmemCols = 512;
+
+static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
+static_assert(kTcThreads == (2 + kDecWarps) * 32, "thread count");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void dsync() {  // the eight decode warps
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory");
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                              volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (*abort_flag) return false;
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                         volatile int* abort_flag) {
+  if (!*abort_flag) wait_or_abort(bar, parity, status, abort_flag);
+}
+
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+  return bi == 0x7fffffff || v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void am_warp_reduce(float& bv, int& bi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi != 0x7fffffff && am_better(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+}
+
+// One 32-row box of a tile: tensor maps and first row.
+struct Box {
+  const CUtensorMap* mc;
+  const CUtensorMap* ms;
+  int row;
+};
+
+// Per-launch work description shared by all roles (all fields derived
+// deterministically from the arguments and the schedule).
+struct Work {
+  int n_tiles, nkb, per_e, pb_count;
+  long U;
+  int G;
+  __device__ __forceinline__ long begin(int b) const { return static_cast<long>(b) * U / G; }
+  __device__ __forceinline__ int cta_of(long u) const {
+    return static_cast<int>(((u + 1) * G - 1) / U);
+  }
+};
+
+template <int MODE>
+struct Kernel {
+  const TcArgs& a;
+  const Sched& sc;
+  const Work& wk;
+  const CUtensorMap *m0, *m1, *m2, *m3;
+
+  // expert of a gate_up pair-box / down tile
+  __device__ __forceinline__ int pb_expert(int pb) const { return sc.active[pb / wk.per_e]; }
+
+  __device__ __forceinline__ void tile_boxes(int tile, Box (&bx)[4]) const {
+    if (MODE == kTcDense) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bx[b] = Box{m0, m1, tile * kRows + b * kBox};
+    } else if (MODE == kTcGateUp) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        int pb = 2 * tile + h;
+        if (pb >= wk.pb_count) pb = 2 * tile;  // odd count: repeat the first pair-box
+        const int e = pb_expert(pb), jb = pb % wk.per_e;
+        const bool sh = (e == a.E);
+        const int base = sh ? 0 : e * 2 * a.I;
+        bx[2 * h] = Box{sh ? m2 : m0, sh ? m3 : m1, base + jb * kBox};
+        bx[2 * h + 1] = Box{sh ? m2 : m0, sh ? m3 : m1, base + a.I + jb * kBox};
+      }
+    } else {
+      const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
+      const bool sh = (e == a.E);
+      const int base = (sh ? 0 : e * a.H) + nt * kRows;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bx[b] = Box{sh ? m2 : m0, sh ? m3 : m1, base + b * kBox};
+    }
+  }
+
+  // B operand source of a tile: key identifies the staged rows (restage when
+  // it changes), n_rows the number of real rows.
+  __device__ __forceinline__ int b_key(int tile) const {
+    return MODE == kTcDown ? sc.active[tile / wk.per_e] : 0;
+  }
+  __device__ __forceinline__ int b_rows(int tile) const {
+    if (MODE == kTcDense) return a.M;
+    if (MODE == kTcGateUp) return a.T;
+    return sc.cnt[sc.active[tile / wk.per_e]];
+  }
+  __device__ __forceinline__ int win_stages() const { return a.win_k / kSK; }
+};
+
+// Staged-row bookkeeping shared (identically) by the MMA thread and the
+// decode warps: which rows and which stage range the shared-memory B
+// operand holds.
+struct XState {
+  int key = -1, k0 = 0, k1 = 0;
+  __device__ __forceinline__ bool covers(int key_, int w0, int w1) const {
+    return key == key_ && w0 >= k0 && w1 <= k1;
+  }
+};
+
+// Window [w0, w1) of a segment starting at stage w0 (MoE: the whole
+// segment; dense: at most win_stages stages).
+template <int MODE>
+__device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kbe) {
+  if (MODE != kTcDense) return kbe;
+  return min(kbe, w0 + kk.win_stages());
+}
+
+// Restaged range when a window is not covered: as many stages from w0 as
+// fit (dense) / the whole K (MoE).
+template <int MODE>
+__device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int& k0, int& k1) {
+  if (MODE == kTcDense && kk.win_stages() < kk.wk.nkb) {
+    k0 = w0;
+    k1 = min(kk.wk.nkb, w0 + kk.win_stages());
+  } else {
+    k0 = 0;
+    k1 = kk.wk.nkb;
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    stream_tc_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+                     const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
+                     const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcOffBars);
+  uint64_t* ring_full = bars;
+  uint64_t* ring_empty = bars + 4;
+  uint64_t* a_full = bars + 8;
+  uint64_t* a_empty = bars + 10;
+  uint64_t* d_full = bars + 12;
+  uint64_t* d_empty = bars + 14;
+  uint64_t* x_full = bars + 16;
+  uint64_t* mma_done = bars + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTcOffMisc);
+  volatile int* abort_flag = reinterpret_cast<int*>(smem + kTcOffMisc + 4);
+  volatile int* bcast = reinterpret_cast<int*>(smem + kTcOffMisc + 8);
+  int* sig = reinterpret_cast<int*>(smem + kTcOffMisc + 64);
+  float* rms = reinterpret_cast<float*>(smem + kTcOffMisc + 192);
+  float* ep = reinterpret_cast<float*>(smem + kTcOffEp);
+  uint8_t* xs = smem + a.x_offset;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], kDecWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&a_full[b], kDecWarps);
+      mbar_init(&a_empty[b], 1);
+      mbar_init(&d_full[b], 1);
+      mbar_init(&d_empty[b], kDecWarps);
+    }
+    mbar_init(x_full, kDecWarps);
+    mbar_init(mma_done, 1);
+    fence_mbarrier_init();
+    *abort_flag = 0;
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+
+  Sched sc{};
+  if (MODE != kTcDense) {
+    // gate_up may read ids written before the previous kernel started
+    // (NVFP4_FLAG_IDS_READY) before its dependency wait; down always can:
+    // the gate_up grid before it read them after its own wait.
+    if (MODE == kTcGateUp && !a.ids_ready) pdl_wait();
+    sc = sched_layout(smem + a.sched_offset, a.E, a.T * a.k);
+    build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, sc, a.status);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  Work wk{};
+  if (MODE == kTcDense) {
+    wk.n_tiles = (a.N + kRows - 1) / kRows;
+    wk.nkb = a.K / kSK;
+  } else if (MODE == kTcGateUp) {
+    wk.per_e = a.I / kBox;
+    wk.pb_count = *sc.n_active * wk.per_e;
+    wk.n_tiles = (wk.pb_count + 1) / 2;
+    wk.nkb = a.H / kSK;
+  } else {
+    wk.per_e = a.H / kRows;
+    wk.n_tiles = *sc.n_active * wk.per_e;
+    wk.nkb = a.I / kSK;
+  }
+  wk.U = static_cast<long>(wk.n_tiles) * wk.nkb;
+  wk.G = static_cast<int>(min(static_cast<long>(gridDim.x), wk.U));
+  const int b = blockIdx.x;
+  const bool active_cta = b < wk.G;
+  const long u0 = active_cta ? wk.begin(b) : 0, u1 = active_cta ? wk.begin(b + 1) : 0;
+  const Kernel<MODE> kk{a, sc, wk, &m0, &m1, &m2, &m3};
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0 && u0 < u1) {
+      prefetch_tensormap(&m0);
+      prefetch_tensormap(&m1);
+      const uint64_t pol = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      for (long u = u0; u < u1; ++u) {
+        Box bx[4];
+        kk.tile_boxes(static_cast<int>(u / wk.nkb), bx);
+        const int kb = static_cast<int>(u % wk.nkb);
+        if (*abort_flag || !wait_or_abort(&ring_empty[stage], phase ^ 1u, a.status, abort_flag))
+          break;
+        mbar_arrive_expect_tx(&ring_full[stage], kTcStageBytes);
+        uint8_t* st = smem + stage * kTcStageBytes;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          tma_load_2d(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row,
+                      &ring_full[stage], pol);
+          tma_load_2d(st + kCodeBytes + bb * (kRows * kSK / 16 / 4), bx[bb].ms, kb * (kSK / 16),
+                      bx[bb].row, &ring_full[stage], pol);
+        }
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // wait for the TMA writes still in flight (bounded, ignores aborts)
+      const int n = issued < kStages ? static_cast<int>(issued) : kStages;
+      for (int i = 0; i < n; ++i) {
+        if (stage == 0) {
+          stage = kStages - 1;
+          phase ^= 1u;
+        } else {
+          --stage;
+        }
+        mbar_wait(&ring_full[stage], phase, a.status);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0 && u0 < u1) {
+      XState xst;
+      uint32_t acount = 0, dcount = 0, xcount = 0;
+      const uint32_t xs_addr = smem_u32(xs);
+      const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
+      for (long u = u0; u < u1;) {
+        const int tile = static_cast<int>(u / wk.nkb);
+        const int kbs = static_cast<int>(u % wk.nkb);
+        const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+        const int key = kk.b_key(tile);
+        const int nr = kk.b_rows(tile);
+        const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32);
+        for (int w0 = kbs; w0 < kbe;) {
+          const int w1 = window_end(kk, w0, kbe);
+          if (!xst.covers(key, w0, w1)) {
+            restage_range(kk, w0, xst.k0, xst.k1);
+            xst.key = key;
+            wait_bar(x_full, xcount & 1u, a.status, abort_flag);
+            ++xcount;
+          }
+          const uint32_t db = dcount & 1u;
+          wait_bar(&d_empty[db], ((dcount >> 1) & 1u) ^ 1u, a.status, abort_flag);
+          const uint32_t d_t = tmem + kDCol + 32u * db;
+          for (int kb = w0; kb < w1; ++kb) {
+            const uint32_t ab = acount & 1u;
+            wait_bar(&a_full[ab], (acount >> 1) & 1u, a.status, abort_flag);
+            tc::fence_after_sync();
+            if (!*abort_flag) {
+              const uint32_t a_t = tmem + kACols * ab;
+              const uint32_t bbase = xs_addr + static_cast<uint32_t>(kb - xst.k0) * 4096u;
+#pragma unroll
+              for (int j = 0; j < kSK / 16; ++j)
+                tc::mma_f16_ts(d_t, a_t + 8 * j, tc::smem_desc(bbase + 256u * j, sbo), idesc,
+                               (kb > w0 || j > 0) ? 1u : 0u);
+            }
+            tc::commit(&a_empty[ab]);
+            ++acount;
+          }
+          tc::commit(&d_full[db]);
+          ++dcount;
+          w0 = w1;
+        }
+        u += kbe - kbs;
+      }
+      // every MMA has completed before tensor memory is released
+      tc::commit(mma_done);
+      mbar_wait(mma_done, 0, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ decode + epilogue warps
+    const int dw = warp - 2, q = warp & 3, half = dw >> 2;
+    const int dtid = threadIdx.x - 64;
+    const int r = 32 * q + lane;  // tile row = tensor-memory lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    if (MODE == kTcDense || MODE == kTcDown || a.ids_ready) pdl_wait();
+    pdl_launch_dependents();
+
+    if (MODE == kTcDown && wk.n_tiles == 0 && b == 0) {
+      // nothing routed and no shared expert: the layer output is zero
+      for (int i = dtid; i < a.T * a.H; i += kDecThreads)
+        a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
+    }
+    // dense with windows: the RMS factor needs whole rows (one pass)
+    if (MODE == kTcDense && a.rms && a.win_k < a.K) {
+      for (int m = dw; m < a.M; m += kDecWarps) {
+        float ss = 0.0f;
+        const __nv_bfloat16* row = a.A + m * a.lda;
+        for (int v = lane; v < a.K / 8; v += 32) {
+          const uint4 uu = *reinterpret_cast<const uint4*>(row + v * 8);
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss = fmaf(static_cast<float>(e[i]), static_cast<float>(e[i]), ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+      }
+    }
+    const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
+    XState xst;
+    uint32_t acount = 0, dcount = 0;
+    int rstage = 0;
+    uint32_t rphase = 0;
+    const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
+    const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
+
+    for (long u = u0; u < u1;) {
+      const int tile = static_cast<int>(u / wk.nkb);
+      const int kbs = static_cast<int>(u % wk.nkb);
+      const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+      const int key = kk.b_key(tile);
+      const int nr = kk.b_rows(tile);
+      const int npad = nr <= 16 ? 16 : 32;
+      float tot[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tot[j] = 0.0f;
+
+      for (int w0 = kbs; w0 < kbe;) {
+        const int w1 = window_end(kk, w0, kbe);
+        if (!xst.covers(key, w0, w1)) {
+          restage_range(kk, w0, xst.k0, xst.k1);
+          xst.key = key;
+          // stage B rows [0, npad) of K range [k0, k1) in core-matrix order;
+          // the previous window's MMAs are complete (its D was read)
+          const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
+          const bool full_rms = a.rms && (MODE != kTcDown) && klen == ((MODE == kTcDense) ? a.K : a.H);
+          for (int n = dw; n < npad; n += kDecWarps) {
+            uint8_t* rowbase = xs + (n >> 3) * sbo + (n & 7) * 16;
+            if (n >= nr) {
+              for (int v = lane; v < klen / 4; v += 32) {
+                const int kq = v * 4;
+                *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) =
+                    make_uint2(0u, 0u);
+              }
+              if (lane == 0) sig[n] = 0;
+              continue;
+            }
+            float amax = 0.0f, ss = 0.0f;
+            if (MODE == kTcDown) {
+              const float* src = a.h + static_cast<size_t>(sc.off[key] + n) * a.I;
+              for (int v = lane; v < klen / 4; v += 32) {
+                const float4 f = *reinterpret_cast<const float4*>(src + kbeg + v * 4);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+              }
+              amax = warp_max(amax);
+              const int s = f16_row_shift(amax);
+              if (lane == 0) sig[n] = s;
+              for (int v = lane; v < klen / 4; v += 32) {
+                const float4 f = *reinterpret_cast<const float4*>(src + kbeg + v * 4);
+                const int kq = v * 4;
+                *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) =
+                    make_uint2(pack_f16x2(scale_pow2(f.x, s), scale_pow2(f.y, s)),
+                               pack_f16x2(scale_pow2(f.z, s), scale_pow2(f.w, s)));
+              }
+            } else {
+              const __nv_bfloat16* src = (MODE == kTcDense) ? a.A + n * a.lda : a.x + n * a.ldx;
+              for (int v = lane; v < klen / 8; v += 32) {
+                const uint4 uu = *reinterpret_cast<const uint4*>(src + kbeg + v * 8);
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float f = static_cast<float>(e[i]);
+                  amax = fmaxf(amax, fabsf(f));
+                  ss = fmaf(f, f, ss);
+                }
+              }
+              amax = warp_max(amax);
+              const int s = f16_row_shift(amax);
+              if (lane == 0) sig[n] = s;
+              if (full_rms) {
+                ss = warp_sum(ss);
+                if (lane == 0) rms[n] = rsqrtf(ss / static_cast<float>(klen) + 1e-6f);
+              }
+              for (int v = lane; v < klen / 8; v += 32) {
+                const uint4 uu = *reinterpret_cast<const uint4*>(src + kbeg + v * 8);
+                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+                uint32_t p[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  p[i] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * i]), s),
+                                    scale_pow2(static_cast<float>(e[2 * i + 1]), s));
+                const int kq = v * 8;  // a whole 8-element core-matrix row
+                *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(p[0], p[1], p[2], p[3]);
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          dsync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(x_full);
+        }
+
+        // ---- decode the window's stages into tensor memory
+        for (int kb = w0; kb < w1; ++kb) {
+          wait_bar(&ring_full[rstage], rphase, a.status, abort_flag);
+          const uint32_t ab = acount & 1u;
+          wait_bar(&a_empty[ab], ((acount >> 1) & 1u) ^ 1u, a.status, abort_flag);
+          tc::fence_after_sync();
+          const uint8_t* st = smem + rstage * kTcStageBytes;
+          const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
+          const uint2 sb =
+              *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
+          const uint32_t sbw[2] = {sb.x, sb.y};
+#pragma unroll
+          for (int ci = 0; ci < 4; ++ci) {
+            const int c = 4 * half + ci;
+            const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((c ^ (lane & 7)) << 4));
+            const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
+            const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
+            const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
+            const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
+            uint32_t v[16];
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+              const uint32_t s = wi < 2 ? s_lo : s_hi;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], s);
+            }
+            tc::st_x16(lane_addr + kACols * ab + 16 * c, v);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ring_empty[rstage]);
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[ab]);
+          ++acount;
+          if (++rstage == kStages) {
+            rstage = 0;
+            rphase ^= 1u;
+          }
+        }
+
+        // ---- fold the window's accumulator into the segment total
+        const uint32_t db = dcount & 1u;
+        wait_bar(&d_full[db], (dcount >> 1) & 1u, a.status, abort_flag);
+        tc::fence_after_sync();
+        uint32_t dv[16];
+        tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * half, dv);
+        tc::wait_ld();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&d_empty[db]);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (16 * half + j < nr) tot[j] += scale_pow2(__uint_as_float(dv[j]), -sig[16 * half + j]);
+        ++dcount;
+        w0 = w1;
+      }
+      u += kbe - kbs;
+
+      // ---- stream-K: a tile split between CTAs is reduced by its last CTA
+      if (!(kbs == 0 && kbe == wk.nkb)) {
+        const int slot = (tile == first_tile) ? 0 : 1;
+        float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(16 * half + j) * kRows + r] = tot[j];
+        __threadfence();
+        dsync();
+        const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
+        const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
+        if (dtid == 0) {
+          const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
+          *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
+        }
+        dsync();
+        if (!*bcast) continue;  // uniform across the decode warps
+        __threadfence();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tot[j] = 0.0f;
+        for (int bb = blo; bb <= bhi; ++bb) {
+          const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
+          const float* pp = a.partials + static_cast<size_t>(bb * 2 + sl) * (32 * kRows);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) tot[j] += __ldcg(pp + (16 * half + j) * kRows + r);
+        }
+        if (dtid == 0) a.tile_cnt[tile] = 0u;
+      }
+
+      // ---- epilogues
+      if (MODE == kTcDense) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = 16 * half + j;
+          if (m < a.M) ep[m * kRows + r] = tot[j] * gs * (a.rms ? rms[m] : 1.0f);
+        }
+        dsync();
+        const int n0 = tile * kRows;
+        for (int m = dw; m < a.M; m += kDecWarps) {
+          float bv = -FLT_MAX;
+          int bi = 0x7fffffff;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int rr = 4 * lane + i, n = n0 + rr;
+            if (n < a.N) {
+              const __nv_bfloat16 o = __float2bfloat16_rn(ep[m * kRows + rr]);
+              a.C[m * a.ldc + n] = o;
+              const float ov = __bfloat162float(o);
+              if (am_better(ov, n, bv, bi)) {
+                bv = ov;
+                bi = n;
+              }
+            }
+          }
+          if (a.argmax_out) {
+            am_warp_reduce(bv, bi);
+            if (lane == 0) a.am_part[m * wk.n_tiles + tile] = make_int2(__float_as_int(bv), bi);
+          }
+        }
+        if (a.argmax_out) {
+          __threadfence();
+          dsync();
+          if (dtid == 0) {
+            const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
+            *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
+          }
+          dsync();
+          if (*bcast) {
+            __threadfence();
+            for (int m = dw; m < a.M; m += kDecWarps) {
+              float bv = -FLT_MAX;
+              int bi = 0x7fffffff;
+              for (int j = lane; j < wk.n_tiles; j += 32) {
+                const int2 pr = __ldcg(a.am_part + m * wk.n_tiles + j);
+                const float v = __int_as_float(pr.x);
+                if (pr.y != 0x7fffffff && am_better(v, pr.y, bv, bi)) {
+                  bv = v;
+                  bi = pr.y;
+                }
+              }
+              am_warp_reduce(bv, bi);
+              if (lane == 0) a.argmax_out[m] = bi;
+            }
+            if (dtid == 0) *a.argmax_cnt = 0u;
+          }
+        }
+      } else if (MODE == kTcGateUp) {
+        // rows 0-31 gate and 32-63 up of pair-box 2*tile; 64-127 likewise
+        // for pair-box 2*tile+1 (absent when the count is odd)
+        if (q & 1) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ep[(16 * half + j) * kRows + r] = tot[j];
+        }
+        dsync();
+        const int pb = 2 * tile + (q >> 1);
+        if (!(q & 1) && pb < wk.pb_count) {
+          const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
+          const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+          const int cnt = sc.cnt[e], off = sc.off[e];
+          for (int qq = 0; qq < cnt; ++qq) {
+            const int p = off + qq;
+            const int t = sc.pair_tok[p];
+            if ((t >> 4) != half) continue;
+            const float f = a.rms ? g * rms[t] : g;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (j == (t & 15)) {
+                const float gt = tot[j] * f;
+                const float up = ep[t * kRows + r + 32] * f;
+                a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
+              }
+            }
+          }
+        }
+      } else {
+        const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
+        const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+        const int cnt = sc.cnt[e], off = sc.off[e];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int qq = 16 * half + j;
+          if (qq < cnt) a.y[static_cast<size_t>(off + qq) * a.H + nt * kRows + r] = tot[j] * g;
+        }
+        __threadfence();
+        dsync();
+        uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
+        if (dtid == 0) {
+          const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
+          *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
+        }
+        dsync();
+        if (*bcast) {
+          // the last expert to finish this column: weighted combine in slot order
+          __threadfence();
+          const int sh_off = sc.off[a.E];
+          for (int i = dtid; i < a.T * kRows; i += kDecThreads) {
+            const int t = i >> 7, c = i & 127;
+            const int n = nt * kRows + c;
+            float s = 0.0f;
+            for (int j = 0; j < a.k; ++j) {
+              const int pr = sc.flat_pair[t * a.k + j];
+              if (pr >= 0)
+                s = fmaf(a.w[t * a.k + j], __ldcg(a.y + static_cast<size_t>(pr) * a.H + n), s);
+            }
+            if (a.has_shared) s += __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+            a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
+          }
+          if (dtid == 0) col_cnt[nt] = 0u;
+        }
+      }
+      dsync();
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
+                        cudaStream_t s, bool pdl) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(stream_tc_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // One CTA per SM: each CTA allocates all 512 tensor-memory columns, so a
+  // second resident CTA would only queue on the allocation.
+  const size_t kOnePerSm = 120 * 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem < kOnePerSm ? kOnePerSm : smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, stream_tc_kernel<MODE>, maps[0], maps[1], maps[2], maps[3], a);
+}
+
+}  // namespace
+
+cudaError_t launch_tc(int mode, const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
+                      cudaStream_t s, bool pdl) {
+  switch (mode) {
+    case kTcDense:
+      return launch_mode<kTcDense>(maps, a, grid, smem, s, pdl);
+    case kTcGateUp:
+      return launch_mode<kTcGateUp>(maps, a, grid, smem, s, pdl);
+    default:
+      return launch_mode<kTcDown>(maps, a, grid, smem, s, pdl);
+  }
+}
+
+}  // namespace nvfp4

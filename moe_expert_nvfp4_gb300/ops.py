@@ -25,6 +25,7 @@ ERRORS = {-1: "invalid argument", -2: "misaligned", -3: "unsupported shape",
 FLAG_RMS_INPUT = 1
 FLAG_NO_PDL = 2
 FLAG_IDS_READY = 4
+FLAG_WARP_MMA = 8
 STATUS_BAD_EXPERT_ID = 1
 STATUS_WAIT_TIMEOUT = 2
 
@@ -197,10 +198,12 @@ def device_check(device: int = 0) -> int:
 
 def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
          argmax: bool = False, rms_input: bool = False, workspace: Optional[Workspace] = None,
-         pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None):
+         pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None,
+         warp_mma: bool = False):
     """C = A W^T for BF16 A [M, >=K] (row stride a.stride(0)).  Returns C
     (BF16 [M, N]) and, with argmax=True (or an int32 [M] ``argmax_out``),
-    also the row argmaxes."""
+    also the row argmaxes.  warp_mma: use the warp-level MMA kernel instead
+    of the tcgen05 one."""
     L = load()
     m = a.shape[0]
     if out is None:
@@ -211,7 +214,8 @@ def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
         ids = torch.empty(m, dtype=torch.int32, device=a.device)
     if workspace is None:
         workspace = Workspace(gemm_workspace_bytes(m, w.n, w.k), a.device)
-    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+    flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+             | (FLAG_WARP_MMA if warp_mma else 0))
     wc = w.c()
     _check(L.nvfp4_gemm_skinny(a.data_ptr(), a.stride(0), m, ctypes.byref(wc), out.data_ptr(),
                                out.stride(0), _ptr(ids), flags, workspace.ptr(), workspace.nbytes,
@@ -239,9 +243,10 @@ def route(logits: torch.Tensor, k: int, renormalize: bool = True,
 def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
         shared: Optional[ExpertStack] = None, out: Optional[torch.Tensor] = None,
         rms_input: bool = False, workspace: Optional[Workspace] = None, pdl: bool = True,
-        stream=None, ids_ready: bool = False) -> torch.Tensor:
+        stream=None, ids_ready: bool = False, warp_mma: bool = False) -> torch.Tensor:
     """MoE decode layer: BF16 x [T, >=H] -> BF16 out [T, H].  ids_ready: the
-    ids/weights were complete before the previous kernel started."""
+    ids/weights were complete before the previous kernel started.  warp_mma:
+    use the warp-level MMA kernels instead of the tcgen05 ones."""
     L = load()
     t, k = ids.shape
     assert ids.is_contiguous() and weights.is_contiguous()
@@ -250,7 +255,7 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
     if workspace is None:
         workspace = Workspace(moe_workspace_bytes(t, k, experts), x.device)
     flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
-             | (FLAG_IDS_READY if ids_ready else 0))
+             | (FLAG_IDS_READY if ids_ready else 0) | (FLAG_WARP_MMA if warp_mma else 0))
     ec = experts.c()
     sc = shared.c() if shared is not None else None
     _check(L.moe_nvfp4_decode(x.data_ptr(), x.stride(0), t, ids.data_ptr(), weights.data_ptr(), k,

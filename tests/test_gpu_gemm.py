@@ -20,12 +20,12 @@ def _lib():
     assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
 
 
-def _case(seed, m, n, k, *ids, rms=False, argmax=False, lda=None):
+def _case(seed, m, n, k, *ids, rms=False, argmax=False, lda=None, warp_mma=False):
     W = device_weight(seed, n, k, *ids)
     a_full = synth.activations_bf16(seed, m, lda or k, 900, *ids)
     a = a_full.cuda()[:, :k] if lda else a_full.cuda()
     ws = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
-    res = ops.gemm(a, W, argmax=argmax, rms_input=rms, workspace=ws)
+    res = ops.gemm(a, W, argmax=argmax, rms_input=rms, workspace=ws, warp_mma=warp_mma)
     disp = ops.last_dispatch()
     torch.cuda.synchronize()
     assert ws.status() == 0
@@ -44,6 +44,7 @@ def test_projection_2048_to_64_m4():
     c, ref, disp, _ = _case(0, 4, 64, 2048)
     assert_close(f64(c), O.bf16_round(ref), "2048->64")
     assert "grid=8 " in disp and "units_per_cta=1.00" in disp   # split-K over 8 CTAs
+    assert disp.startswith("stream_tc_kernel<dense>")
 
 
 @pytest.mark.parametrize("m", [1, 4, 8, 16, 32])
@@ -51,6 +52,13 @@ def test_projection_2048_to_64_m4():
 def test_dense_sweep(seed, n, k, m):
     c, ref, disp, _ = _case(seed, m, n, k)
     assert_close(f64(c), O.bf16_round(ref), f"M={m} N={n} K={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(4, 64, 2048), (8, 4096, 2048), (32, 2048, 4096), (13, 200, 768)])
+def test_warp_mma_path(m, n, k):
+    c, ref, disp, _ = _case(1, m, n, k, warp_mma=True)
+    assert disp.startswith("dense_gemm_kernel")
+    assert_close(f64(c), O.bf16_round(ref), f"warp mma M={m} N={n} K={k}")
 
 
 @pytest.mark.parametrize("m,n,k", [(3, 200, 768), (13, 200, 768), (27, 1000, 256), (1, 64, 256),

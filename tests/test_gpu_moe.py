@@ -71,13 +71,14 @@ def test_route_ties_lowest_index_first():
 
 # ------------------------------------------------------------------ MoE
 
-def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
+def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4, warp_mma=False):
     ex, sh, get = layer4
     x = synth.activations_bf16(seed, 32, H, 1)[:t]
     if ids is None:
         ids, w = ops.route(synth.router_logits(seed, 32, E, 1)[:t].cuda(), K)
     ws = ops.Workspace(ops.moe_workspace_bytes(t, ids.shape[1], ex))
-    out = ops.moe(x.cuda(), ids, w, ex, sh if shared else None, rms_input=rms, workspace=ws)
+    out = ops.moe(x.cuda(), ids, w, ex, sh if shared else None, rms_input=rms, workspace=ws,
+                  warp_mma=warp_mma)
     disp = ops.last_dispatch()
     status = ws.status()
     x64 = f64(x)
@@ -90,8 +91,15 @@ def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
 def test_moe_layer_35b_shape(layer4, t):
     out, ref, disp, status, _ = _moe_case(layer4, t)
     assert status == 0
-    assert "shared=1" in disp
+    assert "shared=1" in disp and disp.startswith("stream_tc_kernel<gate_up>")
     assert_close(f64(out), O.bf16_round(ref), f"MoE T={t}")
+
+
+@pytest.mark.parametrize("t", [1, 8, 32])
+def test_moe_warp_mma_path(layer4, t):
+    out, ref, disp, status, _ = _moe_case(layer4, t, warp_mma=True)
+    assert status == 0 and disp.startswith("moe_gate_up_kernel")
+    assert_close(f64(out), O.bf16_round(ref), f"warp mma MoE T={t}")
 
 
 def test_moe_without_shared_expert(layer4):
