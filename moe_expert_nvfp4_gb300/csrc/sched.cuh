@@ -38,7 +38,7 @@ __device__ __forceinline__ Sched sched_layout(uint8_t* base, int E, int P) {
 
 // All threads of the CTA.  Deterministic: the result does not depend on
 // the order of the shared-memory atomics.
-__device__ void build_schedule(const int32_t* ids, int T, int k, int E, int has_shared,
+static __device__ void build_schedule(const int32_t* ids, int T, int k, int E, int has_shared,
                                const Sched& s, uint32_t* status) {
   const int P = T * k;
   const int tid = threadIdx.x, nthr = blockDim.x;
