@@ -11,7 +11,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/nvfp4moe.h"
+#include "nvfp4moe.h"
 #include "common.cuh"
 #include "launch.h"
 #include "stream.cuh"
