@@ -176,12 +176,30 @@ bool plan_moe(int T, int k, int E, int H, int I, int sms, MoePlan* p) {
 }
 
 // ------------------------------------------------------------- tcgen05 plans
-constexpr size_t kTcXBudget = kSmemLimit - kSmemAlignPad - kTcOffSched;
+// Shared memory: fixed header (barriers, misc, epilogue tile), the expert
+// schedule, the staged activations [npad][win_k] f16, then as many 18 KB
+// weight stages as fit (3..8).
+struct TcLayout {
+  int x_offset, ring_offset, n_stages;
+  size_t smem;
+};
+
+bool tc_layout(int sched_bytes, size_t x_bytes, TcLayout* L) {
+  L->x_offset = static_cast<int>(round_up(kTcOffSched + sched_bytes, 128));
+  L->ring_offset = static_cast<int>(round_up(L->x_offset + x_bytes, 1024));
+  const long room = static_cast<long>(kSmemLimit) - kSmemAlignPad - L->ring_offset;
+  L->n_stages = static_cast<int>(room / kTcStageBytes);
+  if (L->n_stages > kTcMaxStages) L->n_stages = kTcMaxStages;
+  if (L->n_stages < 3) return false;
+  L->smem = kSmemAlignPad + L->ring_offset + static_cast<size_t>(L->n_stages) * kTcStageBytes;
+  return true;
+}
 
 struct TcDensePlan {
   int n_tiles, nkb, grid, npad, win_k;
   long units;
-  size_t smem, off_partials, off_am, ws_bytes;
+  TcLayout L;
+  size_t off_partials, off_am, ws_bytes;
 };
 
 bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
@@ -191,11 +209,8 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
   p->units = static_cast<long>(p->n_tiles) * p->nkb;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   p->npad = M <= 16 ? 16 : 32;
-  int w = K;
-  while (w > kStageK && static_cast<size_t>(p->npad) * w * 2 > kTcXBudget) w -= kStageK;
-  if (static_cast<size_t>(p->npad) * w * 2 > kTcXBudget) return false;
-  p->win_k = w;
-  p->smem = kSmemAlignPad + kTcOffSched + static_cast<size_t>(p->npad) * w * 2;
+  p->win_k = K < kTcMaxWinK ? K : kTcMaxWinK;
+  if (!tc_layout(0, static_cast<size_t>(p->npad) * p->win_k * 2, &p->L)) return false;
   p->off_partials = kWsScratch;
   p->off_am = round_up(p->off_partials + 4ull * p->grid * 2 * 32 * 128, 256);
   p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
@@ -204,17 +219,18 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
 
 struct TcMoePlan {
   int P, npad, sched_bytes, grid;
-  size_t smem_gu, smem_dn, off_partials, off_h, off_y, ws_bytes;
+  TcLayout gu, dn;
+  size_t off_partials, off_h, off_y, ws_bytes;
 };
 
 bool plan_tc_moe(int T, int k, int E, int H, int I, int sms, TcMoePlan* p) {
   p->P = T * k;
   p->npad = T <= 16 ? 16 : 32;
+  if (H > 4096 || I > 2048) return false;  // staged rows are read once into registers
   p->sched_bytes = static_cast<int>(round_up(4ull * (4 * E + 5 + 2 * p->P + 33), 128));
-  const size_t base = kSmemAlignPad + kTcOffSched + p->sched_bytes;
-  p->smem_gu = base + static_cast<size_t>(p->npad) * H * 2;
-  p->smem_dn = base + static_cast<size_t>(p->npad) * I * 2;
-  if (p->smem_gu > kSmemLimit || p->smem_dn > kSmemLimit) return false;
+  if (!tc_layout(p->sched_bytes, static_cast<size_t>(p->npad) * H * 2, &p->gu) ||
+      !tc_layout(p->sched_bytes, static_cast<size_t>(p->npad) * I * 2, &p->dn))
+    return false;
   const long max_active = (p->P < E ? p->P : E) + 1;
   if (max_active * (H / 128) > kTcColCntBase || H / 128 > kWsMaxCounters - kTcColCntBase) return false;
   p->grid = sms;
@@ -317,21 +333,23 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
     a.K = K;
     a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
     a.win_k = p.win_k;
-    a.x_offset = kTcOffSched;
+    a.x_offset = p.L.x_offset;
+    a.ring_offset = p.L.ring_offset;
+    a.n_stages = p.L.n_stages;
     a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
     a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
     a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
     a.partials = reinterpret_cast<float*>(ws + p.off_partials);
     a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
-    cudaError_t e = launch_tc(kTcDense, maps, a, p.grid, p.smem,
+    cudaError_t e = launch_tc(kTcDense, maps, a, p.grid, p.L.smem,
                               reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL));
     if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<dense> launch");
     char buf[256];
     snprintf(buf, sizeof(buf),
              "stream_tc_kernel<dense> grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d "
-             "n=%d smem=%zu argmax=%d rms=%d",
+             "n=%d stages=%d smem=%zu argmax=%d rms=%d",
              p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_k, p.npad,
-             p.smem, argmax_out ? 1 : 0, a.rms);
+             p.L.n_stages, p.L.smem, argmax_out ? 1 : 0, a.rms);
     g_dispatch = buf;
     return NVFP4_OK;
   }
@@ -471,7 +489,6 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
     a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
     a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
     a.sched_offset = kTcOffSched;
-    a.x_offset = kTcOffSched + p.sched_bytes;
     a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
     a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
     a.partials = reinterpret_cast<float*>(ws + p.off_partials);
@@ -480,17 +497,23 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
     const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     a.win_k = H;
-    cudaError_t e = launch_tc(kTcGateUp, gu, a, p.grid, p.smem_gu, s, pdl);
+    a.x_offset = p.gu.x_offset;
+    a.ring_offset = p.gu.ring_offset;
+    a.n_stages = p.gu.n_stages;
+    cudaError_t e = launch_tc(kTcGateUp, gu, a, p.grid, p.gu.smem, s, pdl);
     if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<gate_up> launch");
     a.win_k = I;
-    e = launch_tc(kTcDown, dn, a, p.grid, p.smem_dn, s, pdl);
+    a.x_offset = p.dn.x_offset;
+    a.ring_offset = p.dn.ring_offset;
+    a.n_stages = p.dn.n_stages;
+    e = launch_tc(kTcDown, dn, a, p.grid, p.dn.smem, s, pdl);
     if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<down> launch");
     char buf[256];
     snprintf(buf, sizeof(buf),
-             "stream_tc_kernel<gate_up> grid=%d smem=%zu; stream_tc_kernel<down> grid=%d smem=%zu; "
-             "T=%d k=%d E=%d n=%d shared=%d rms=%d ids_ready=%d",
-             p.grid, p.smem_gu, p.grid, p.smem_dn, T, k, E, p.npad, a.has_shared, a.rms,
-             a.ids_ready);
+             "stream_tc_kernel<gate_up> grid=%d stages=%d smem=%zu; stream_tc_kernel<down> grid=%d "
+             "stages=%d smem=%zu; T=%d k=%d E=%d n=%d shared=%d rms=%d ids_ready=%d",
+             p.grid, p.gu.n_stages, p.gu.smem, p.grid, p.dn.n_stages, p.dn.smem, T, k, E, p.npad,
+             a.has_shared, a.rms, a.ids_ready);
     g_dispatch = buf;
     return NVFP4_OK;
   }

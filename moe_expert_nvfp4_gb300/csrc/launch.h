@@ -74,14 +74,18 @@ struct MoeArgs {
 };
 
 // ---- tcgen05 streaming kernel (stream_tc.cu) ------------------------------
-constexpr int kTcStages = 4;                              // 18 KB stages
-constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;
-constexpr int kTcOffBars = kTcStages * kTcStageBytes;     // 73728
-constexpr int kTcOffMisc = kTcOffBars + 256;
-constexpr int kTcOffEp = kTcOffMisc + 512;
-constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;      // after the [32][128] f32 tile
-constexpr int kTcThreads = 320;                           // producer, MMA, 8 decode warps
-constexpr int kTcColCntBase = 8192;                       // down combine counters
+// Shared memory (from a 1024-byte aligned base): barriers, misc, the
+// [32][128] f32 epilogue tile, the expert schedule, the staged activations,
+// then the weight ring (1024-aligned, n_stages x 18 KB).
+constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;  // 18432
+constexpr int kTcMaxStages = 8;
+constexpr int kTcOffBars = 0;
+constexpr int kTcOffMisc = 256;
+constexpr int kTcOffEp = 768;
+constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17152
+constexpr int kTcThreads = 320;                          // producer, MMA, 8 decode warps
+constexpr int kTcColCntBase = 8192;                      // down combine counters
+constexpr int kTcMaxWinK = 2048;                         // activations staged per window
 
 enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2 };
 
@@ -112,6 +116,8 @@ struct TcArgs {
   int rms;
   int win_k;        // staged activation window capacity (elements, multiple of 256)
   int x_offset;     // smem offset of the staged activations
+  int ring_offset;  // smem offset of the weight ring (1024-aligned)
+  int n_stages;     // ring depth (3..kTcMaxStages)
   int sched_offset; // smem offset of the expert schedule (MoE)
   uint32_t* status;
   uint32_t* tile_cnt;   // counters region

@@ -48,11 +48,11 @@ constexpr int kRows = 128;
 constexpr int kBox = 32;
 constexpr int kSK = 256;                       // K per stage
 constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
-constexpr int kStages = kTcStages;
 constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kABufs = 3;                      // A operand buffers in tensor memory
 constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
-constexpr int kDCol = 2 * kACols;              // D buffers at columns 256 and 288
+constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384 and 416
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
@@ -180,24 +180,91 @@ struct XState {
   }
 };
 
-// Window [w0, w1) of a segment starting at stage w0 (MoE: the whole
-// segment; dense: at most win_stages stages).
+// Window [w0, w1) of a segment starting at stage w0: MoE, the whole segment
+// (its K is staged once); dense, at most win_stages stages, staged exactly.
 template <int MODE>
 __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kbe) {
   if (MODE != kTcDense) return kbe;
   return min(kbe, w0 + kk.win_stages());
 }
 
-// Restaged range when a window is not covered: as many stages from w0 as
-// fit (dense) / the whole K (MoE).
+// Stage range restaged when a window is not covered: dense, the window;
+// MoE, the whole K.
 template <int MODE>
-__device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int& k0, int& k1) {
-  if (MODE == kTcDense && kk.win_stages() < kk.wk.nkb) {
+__device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1, int& k0,
+                                              int& k1) {
+  if (MODE == kTcDense) {
     k0 = w0;
-    k1 = min(kk.wk.nkb, w0 + kk.win_stages());
+    k1 = w1;
   } else {
     k0 = 0;
     k1 = kk.wk.nkb;
+  }
+}
+
+// Stage B rows [0, npad) of K range [kbeg, kbeg + klen) into shared memory as
+// FP16 core matrices (see tc::smem_desc), one power-of-two shift per row
+// (sig), and optionally rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged
+// range.  Each warp takes rows dw, dw + 8, ...; a row is read once into
+// registers (klen <= kTcMaxWinK: at most 8 x 16 bytes per lane).
+template <typename T, typename RowFn>
+__device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, int klen,
+                                        uint8_t* xs, uint32_t sbo, int* sig, float* rms, int dw,
+                                        int lane) {
+  constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
+  const int nv = klen / (32 * kVec);    // loads per lane (<= 8 for bf16, <= 16 for f32)
+  for (int n = dw; n < npad; n += kDecWarps) {
+    uint8_t* rowbase = xs + (n >> 3) * sbo + (n & 7) * 16;
+    if (n >= nr) {
+      for (int v = lane; v < klen / 8; v += 32)
+        *reinterpret_cast<uint4*>(rowbase + v * 128) = make_uint4(0u, 0u, 0u, 0u);
+      if (lane == 0) sig[n] = 0;
+      continue;
+    }
+    const T* src = rowp(n) + kbeg;
+    uint4 buf[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + (i * 32 + lane) * kVec);
+    float amax = 0.0f, ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < nv) {
+        const T* e = reinterpret_cast<const T*>(&buf[i]);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+          const float f = static_cast<float>(e[j]);
+          amax = fmaxf(amax, fabsf(f));
+          ss = fmaf(f, f, ss);
+        }
+      }
+    amax = warp_max(amax);
+    const int sh = f16_row_shift(amax);
+    if (lane == 0) sig[n] = sh;
+    if (rms) {
+      ss = warp_sum(ss);
+      if (lane == 0) rms[n] = rsqrtf(ss / static_cast<float>(klen) + 1e-6f);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (i < nv) {
+        const T* e = reinterpret_cast<const T*>(&buf[i]);
+        const int kq = (i * 32 + lane) * kVec;  // element offset of this load
+        if constexpr (sizeof(T) == 2) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pk[j] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * j]), sh),
+                               scale_pow2(static_cast<float>(e[2 * j + 1]), sh));
+          *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        } else {
+          const uint32_t p0 = pack_f16x2(scale_pow2(static_cast<float>(e[0]), sh),
+                                         scale_pow2(static_cast<float>(e[1]), sh));
+          const uint32_t p1 = pack_f16x2(scale_pow2(static_cast<float>(e[2]), sh),
+                                         scale_pow2(static_cast<float>(e[3]), sh));
+          *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) = make_uint2(p0, p1);
+        }
+      }
   }
 }
 
@@ -209,14 +276,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcOffBars);
-  uint64_t* ring_full = bars;
-  uint64_t* ring_empty = bars + 4;
-  uint64_t* a_full = bars + 8;
-  uint64_t* a_empty = bars + 10;
-  uint64_t* d_full = bars + 12;
-  uint64_t* d_empty = bars + 14;
-  uint64_t* x_full = bars + 16;
-  uint64_t* mma_done = bars + 17;
+  uint64_t* ring_full = bars;                   // [kTcMaxStages]
+  uint64_t* ring_empty = bars + kTcMaxStages;   // [kTcMaxStages]
+  uint64_t* a_full = bars + 2 * kTcMaxStages;   // [kABufs]
+  uint64_t* a_empty = a_full + kABufs;          // [kABufs]
+  uint64_t* d_full = a_empty + kABufs;          // [2]
+  uint64_t* d_empty = d_full + 2;               // [2]
+  uint64_t* x_full = d_empty + 2;
+  uint64_t* mma_done = x_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTcOffMisc);
   volatile int* abort_flag = reinterpret_cast<int*>(smem + kTcOffMisc + 4);
   volatile int* bcast = reinterpret_cast<int*>(smem + kTcOffMisc + 8);
@@ -224,16 +291,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* rms = reinterpret_cast<float*>(smem + kTcOffMisc + 192);
   float* ep = reinterpret_cast<float*>(smem + kTcOffEp);
   uint8_t* xs = smem + a.x_offset;
+  uint8_t* ring = smem + a.ring_offset;
+  const int n_stages = a.n_stages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < n_stages; ++s) {
       mbar_init(&ring_full[s], 1);
       mbar_init(&ring_empty[s], kDecWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kABufs; ++b) {
       mbar_init(&a_full[b], kDecWarps);
       mbar_init(&a_empty[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], kDecWarps);
     }
@@ -294,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (*abort_flag || !wait_or_abort(&ring_empty[stage], phase ^ 1u, a.status, abort_flag))
           break;
         mbar_arrive_expect_tx(&ring_full[stage], kTcStageBytes);
-        uint8_t* st = smem + stage * kTcStageBytes;
+        uint8_t* st = ring + stage * kTcStageBytes;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
           tma_load_2d(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row,
@@ -303,16 +374,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       bx[bb].row, &ring_full[stage], pol);
         }
         ++issued;
-        if (++stage == kStages) {
+        if (++stage == n_stages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       // wait for the TMA writes still in flight (bounded, ignores aborts)
-      const int n = issued < kStages ? static_cast<int>(issued) : kStages;
+      const int n = issued < n_stages ? static_cast<int>(issued) : n_stages;
       for (int i = 0; i < n; ++i) {
         if (stage == 0) {
-          stage = kStages - 1;
+          stage = n_stages - 1;
           phase ^= 1u;
         } else {
           --stage;
@@ -337,7 +408,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int w0 = kbs; w0 < kbe;) {
           const int w1 = window_end(kk, w0, kbe);
           if (!xst.covers(key, w0, w1)) {
-            restage_range(kk, w0, xst.k0, xst.k1);
+            restage_range(kk, w0, w1, xst.k0, xst.k1);
             xst.key = key;
             wait_bar(x_full, xcount & 1u, a.status, abort_flag);
             ++xcount;
@@ -346,8 +417,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wait_bar(&d_empty[db], ((dcount >> 1) & 1u) ^ 1u, a.status, abort_flag);
           const uint32_t d_t = tmem + kDCol + 32u * db;
           for (int kb = w0; kb < w1; ++kb) {
-            const uint32_t ab = acount & 1u;
-            wait_bar(&a_full[ab], (acount >> 1) & 1u, a.status, abort_flag);
+            const uint32_t ab = acount % kABufs;
+            wait_bar(&a_full[ab], (acount / kABufs) & 1u, a.status, abort_flag);
             tc::fence_after_sync();
             if (!*abort_flag) {
               const uint32_t a_t = tmem + kACols * ab;
@@ -385,8 +456,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int i = dtid; i < a.T * a.H; i += kDecThreads)
         a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
     }
-    // dense with windows: the RMS factor needs whole rows (one pass)
-    if (MODE == kTcDense && a.rms && a.win_k < a.K) {
+    // dense: the RMS factor needs whole rows when windows are partial
+    if (MODE == kTcDense && a.rms) {
       for (int m = dw; m < a.M; m += kDecWarps) {
         float ss = 0.0f;
         const __nv_bfloat16* row = a.A + m * a.lda;
@@ -422,71 +493,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int w0 = kbs; w0 < kbe;) {
         const int w1 = window_end(kk, w0, kbe);
         if (!xst.covers(key, w0, w1)) {
-          restage_range(kk, w0, xst.k0, xst.k1);
+          restage_range(kk, w0, w1, xst.k0, xst.k1);
           xst.key = key;
-          // stage B rows [0, npad) of K range [k0, k1) in core-matrix order;
-          // the previous window's MMAs are complete (its D was read)
+          // the previous window's MMAs are complete (its accumulator was read)
           const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
-          const bool full_rms = a.rms && (MODE != kTcDown) && klen == ((MODE == kTcDense) ? a.K : a.H);
-          for (int n = dw; n < npad; n += kDecWarps) {
-            uint8_t* rowbase = xs + (n >> 3) * sbo + (n & 7) * 16;
-            if (n >= nr) {
-              for (int v = lane; v < klen / 4; v += 32) {
-                const int kq = v * 4;
-                *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) =
-                    make_uint2(0u, 0u);
-              }
-              if (lane == 0) sig[n] = 0;
-              continue;
-            }
-            float amax = 0.0f, ss = 0.0f;
-            if (MODE == kTcDown) {
-              const float* src = a.h + static_cast<size_t>(sc.off[key] + n) * a.I;
-              for (int v = lane; v < klen / 4; v += 32) {
-                const float4 f = *reinterpret_cast<const float4*>(src + kbeg + v * 4);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-              }
-              amax = warp_max(amax);
-              const int s = f16_row_shift(amax);
-              if (lane == 0) sig[n] = s;
-              for (int v = lane; v < klen / 4; v += 32) {
-                const float4 f = *reinterpret_cast<const float4*>(src + kbeg + v * 4);
-                const int kq = v * 4;
-                *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) =
-                    make_uint2(pack_f16x2(scale_pow2(f.x, s), scale_pow2(f.y, s)),
-                               pack_f16x2(scale_pow2(f.z, s), scale_pow2(f.w, s)));
-              }
-            } else {
-              const __nv_bfloat16* src = (MODE == kTcDense) ? a.A + n * a.lda : a.x + n * a.ldx;
-              for (int v = lane; v < klen / 8; v += 32) {
-                const uint4 uu = *reinterpret_cast<const uint4*>(src + kbeg + v * 8);
-                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float f = static_cast<float>(e[i]);
-                  amax = fmaxf(amax, fabsf(f));
-                  ss = fmaf(f, f, ss);
-                }
-              }
-              amax = warp_max(amax);
-              const int s = f16_row_shift(amax);
-              if (lane == 0) sig[n] = s;
-              if (full_rms) {
-                ss = warp_sum(ss);
-                if (lane == 0) rms[n] = rsqrtf(ss / static_cast<float>(klen) + 1e-6f);
-              }
-              for (int v = lane; v < klen / 8; v += 32) {
-                const uint4 uu = *reinterpret_cast<const uint4*>(src + kbeg + v * 8);
-                const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
-                uint32_t p[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  p[i] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * i]), s),
-                                    scale_pow2(static_cast<float>(e[2 * i + 1]), s));
-                const int kq = v * 8;  // a whole 8-element core-matrix row
-                *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(p[0], p[1], p[2], p[3]);
-              }
-            }
+          if (MODE == kTcDown) {
+            const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
+            const int I = a.I;
+            stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, npad,
+                           kbeg, klen, xs, sbo, sig, nullptr, dw, lane);
+          } else {
+            const __nv_bfloat16* base = (MODE == kTcDense) ? a.A : a.x;
+            const int64_t ld = (MODE == kTcDense) ? a.lda : a.ldx;
+            stage_b<__nv_bfloat16>([&](int n) { return base + n * ld; }, nr, npad, kbeg, klen, xs,
+                                   sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr, dw,
+                                   lane);
           }
           fence_proxy_async_smem();
           dsync();
@@ -497,40 +518,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- decode the window's stages into tensor memory
         for (int kb = w0; kb < w1; ++kb) {
           wait_bar(&ring_full[rstage], rphase, a.status, abort_flag);
-          const uint32_t ab = acount & 1u;
-          wait_bar(&a_empty[ab], ((acount >> 1) & 1u) ^ 1u, a.status, abort_flag);
-          tc::fence_after_sync();
-          const uint8_t* st = smem + rstage * kTcStageBytes;
+          const uint8_t* st = ring + rstage * kTcStageBytes;
           const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
+          // all shared-memory reads of this stage first (their latency overlaps)
           const uint2 sb =
               *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
+          uint4 cw[4];
+#pragma unroll
+          for (int ci = 0; ci < 4; ++ci)
+            cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ring_empty[rstage]);
+          const uint32_t ab = acount % kABufs;
+          wait_bar(&a_empty[ab], ((acount / kABufs) & 1u) ^ 1u, a.status, abort_flag);
+          tc::fence_after_sync();
           const uint32_t sbw[2] = {sb.x, sb.y};
 #pragma unroll
           for (int ci = 0; ci < 4; ++ci) {
-            const int c = 4 * half + ci;
-            const uint4 cw = *reinterpret_cast<const uint4*>(crow + ((c ^ (lane & 7)) << 4));
             const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
             const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
             const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
-            const uint32_t wds[4] = {cw.x, cw.y, cw.z, cw.w};
+            const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
             uint32_t v[16];
 #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
               e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-              const uint32_t s = wi < 2 ? s_lo : s_hi;
+              const uint32_t sv = wi < 2 ? s_lo : s_hi;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], s);
+              for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
             }
-            tc::st_x16(lane_addr + kACols * ab + 16 * c, v);
+            tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ring_empty[rstage]);
           tc::wait_st();
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&a_full[ab]);
           ++acount;
-          if (++rstage == kStages) {
+          if (++rstage == n_stages) {
             rstage = 0;
             rphase ^= 1u;
           }
@@ -560,17 +584,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
 #pragma unroll
         for (int j = 0; j < 16; ++j) part[(16 * half + j) * kRows + r] = tot[j];
-        __threadfence();
         dsync();
         const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
         const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
         if (dtid == 0) {
+          __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
           const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
           *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
+          if (*bcast) __threadfence();
         }
         dsync();
         if (!*bcast) continue;  // uniform across the decode warps
-        __threadfence();
 #pragma unroll
         for (int j = 0; j < 16; ++j) tot[j] = 0.0f;
         for (int bb = blo; bb <= bhi; ++bb) {
@@ -613,15 +637,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (a.argmax_out) {
-          __threadfence();
           dsync();
           if (dtid == 0) {
+            __threadfence();
             const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
             *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
+            if (*bcast) __threadfence();
           }
           dsync();
           if (*bcast) {
-            __threadfence();
             for (int m = dw; m < a.M; m += kDecWarps) {
               float bv = -FLT_MAX;
               int bi = 0x7fffffff;
@@ -676,28 +700,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int qq = 16 * half + j;
           if (qq < cnt) a.y[static_cast<size_t>(off + qq) * a.H + nt * kRows + r] = tot[j] * g;
         }
-        __threadfence();
         dsync();
         uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
         if (dtid == 0) {
+          __threadfence();
           const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
           *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
+          if (*bcast) __threadfence();
         }
         dsync();
         if (*bcast) {
           // the last expert to finish this column: weighted combine in slot order
-          __threadfence();
           const int sh_off = sc.off[a.E];
           for (int i = dtid; i < a.T * kRows; i += kDecThreads) {
             const int t = i >> 7, c = i & 127;
             const int n = nt * kRows + c;
-            float s = 0.0f;
-            for (int j = 0; j < a.k; ++j) {
-              const int pr = sc.flat_pair[t * a.k + j];
-              if (pr >= 0)
-                s = fmaf(a.w[t * a.k + j], __ldcg(a.y + static_cast<size_t>(pr) * a.H + n), s);
+            float vals[17];
+#pragma unroll
+            for (int j = 0; j < 17; ++j) {
+              vals[j] = 0.0f;
+              if (j < a.k) {
+                const int pr = sc.flat_pair[t * a.k + j];
+                if (pr >= 0) vals[j] = a.w[t * a.k + j] * __ldcg(a.y + static_cast<size_t>(pr) * a.H + n);
+              } else if (j == a.k && a.has_shared) {
+                vals[j] = __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+              }
             }
-            if (a.has_shared) s += __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 17; ++j) s += vals[j];
             a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
           }
           if (dtid == 0) col_cnt[nt] = 0u;
