@@ -126,6 +126,23 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                       void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
                       void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
+/* ---- dense skinny GEMM without a workspace -------------------------------
+ * (This library's own addition; the pages have no counterpart.)  Same
+ * arguments and results as nvfp4_gemm_skinny minus the workspace, for
+ * callers that cannot allocate device memory (a plugin whose host runtime
+ * owns every allocation, a real-time loop that may not call cudaMalloc, a
+ * process with a fixed memory budget).  Scratch comes from an 8 MiB array
+ * built into the library, held on every GPU that loads it until exit; a
+ * shape that needs more is rejected with NVFP4_ERR_WORKSPACE.  The first call
+ * on a device (with that device current) looks the array's address up; make
+ * it before any stream capture.  Each call clears the array's status word
+ * and counters on `stream` first.  All calls share the one array: calls that
+ * may overlap on the GPU (other streams, concurrent graphs) race and must not
+ * be issued. */
+int nvfp4_gemm_skinny_noalloc(const void* A, int64_t lda, int M, const nvfp4_weight* W,
+                              void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
+                              nvfp4_stream_t stream);
+
 /* ---- top-k softmax routing ----------------------------------------------
  * logits float32 [T, E] (row-major).  For each row the k experts with the
  * largest logits, compared as float32, ties to the lower index, listed in

@@ -259,6 +259,10 @@ int check_stack(const nvfp4_expert_stack* s, const char* name) {
 
 }  // namespace
 
+namespace nvfp4 {
+void set_last_error(const char* msg) { g_error = msg; }
+}  // namespace nvfp4
+
 // =================================================================== C ABI
 extern "C" {
 

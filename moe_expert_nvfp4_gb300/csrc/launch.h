@@ -146,4 +146,7 @@ cudaError_t launch_moe_down(const CUtensorMap* maps, const MoeArgs& a, int grid,
                             cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
 
+// Record the message returned by nvfp4_last_error() for this thread.
+void set_last_error(const char* msg);
+
 }  // namespace nvfp4
