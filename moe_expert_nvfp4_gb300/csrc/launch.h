@@ -83,7 +83,7 @@ constexpr int kTcOffBars = 0;
 constexpr int kTcOffMisc = 256;
 constexpr int kTcOffEp = 768;
 constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17152
-constexpr int kTcThreads = 320;                          // producer, MMA, 8 decode warps
+constexpr int kTcThreads = 448;                          // producer, MMA, 8 decode, 4 epilogue warps
 constexpr int kTcColCntBase = 8192;                      // down combine counters
 constexpr int kTcMaxWinK = 2048;                         // activations staged per window
 

@@ -13,21 +13,22 @@
 // CTAs is reduced by the last CTA to finish it (atomic counter), adding the
 // per-CTA partials in CTA order, so results do not depend on timing.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: streams stages into a 4-deep ring (full/empty
-//               mbarriers);
-//   warp 1      allocates tensor memory; one thread issues tcgen05.mma:
-//               D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
-//               memory), 16 MMAs per stage, N = tokens rounded up to 16;
-//   warps 2-9   decode: lane l of a warp in lane quarter q owns tile row
-//               32q + l; warps 2-5 decode the first 128 K of each stage,
-//               6-9 the second.  E2M1 -> FP16 by the hardware convert, times
-//               the E4M3 block scale (exact in FP16), written to a tensor-
-//               memory A buffer with tcgen05.st (two A buffers).  The same
-//               warps stage the activations (B) into shared memory as FP16
-//               with a power-of-two shift per row and window, read the FP32
-//               accumulator back with tcgen05.ld, undo the shift, and run the
-//               epilogue.
+// Warp roles (448 threads):
+//   warp 0       TMA producer: streams stages into a shared-memory ring of
+//                3..8 stages (full/empty mbarriers);
+//   warp 1       allocates tensor memory; one thread issues tcgen05.mma:
+//                D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
+//                memory), 16 MMAs per stage, N = tokens rounded up to 16;
+//   warps 2-9    decode: lane l of a warp in lane quarter q owns tile row
+//                32q + l; warps 2-5 decode the first 128 K of each stage,
+//                6-9 the second.  E2M1 -> FP16 by the hardware convert, times
+//                the E4M3 block scale (exact in FP16), written to one of three
+//                tensor-memory A buffers with tcgen05.st.  They only stream.
+//   warps 10-13  epilogue: stage the activations (B) into shared memory as
+//                FP16 with a power-of-two shift per row and window, read the
+//                FP32 accumulator (two buffers) with tcgen05.ld, undo the
+//                shift, and run the stream-K reduction and the epilogue while
+//                the decode warps go on with the next tile.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
 // faster": "Skinny matrix multiplies" (split-K decode matmuls, 4-bit weights
@@ -49,21 +50,23 @@ constexpr int kBox = 32;
 constexpr int kSK = 256;                       // K per stage
 constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
 constexpr int kDecWarps = 8;
-constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kEpiWarps = 4;                   // one per tensor-memory lane quarter
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiWarp0 = 2 + kDecWarps;       // warps 10..13
 constexpr int kABufs = 3;                      // A operand buffers in tensor memory
 constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
 constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384 and 416
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
-static_assert(kTcThreads == (2 + kDecWarps) * 32, "thread count");
+static_assert(kTcThreads == (2 + kDecWarps + kEpiWarps) * 32, "thread count");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-__device__ __forceinline__ void dsync() {  // the eight decode warps
-  asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory");
+__device__ __forceinline__ void esync() {  // the four epilogue warps
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
@@ -205,15 +208,15 @@ __device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, in
 // Stage B rows [0, npad) of K range [kbeg, kbeg + klen) into shared memory as
 // FP16 core matrices (see tc::smem_desc), one power-of-two shift per row
 // (sig), and optionally rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged
-// range.  Each warp takes rows dw, dw + 8, ...; a row is read once into
-// registers (klen <= kTcMaxWinK: at most 8 x 16 bytes per lane).
+// range.  Warp dw of nwarps takes rows dw, dw + nwarps, ...; a row is read
+// once into registers (at most 16 x 16 bytes per lane).
 template <typename T, typename RowFn>
 __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, int klen,
                                         uint8_t* xs, uint32_t sbo, int* sig, float* rms, int dw,
-                                        int lane) {
+                                        int lane, int nwarps) {
   constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
-  const int nv = klen / (32 * kVec);    // loads per lane (<= 8 for bf16, <= 16 for f32)
-  for (int n = dw; n < npad; n += kDecWarps) {
+  const int nv = klen / (32 * kVec);    // loads per lane
+  for (int n = dw; n < npad; n += nwarps) {
     uint8_t* rowbase = xs + (n >> 3) * sbo + (n & 7) * 16;
     if (n >= nr) {
       for (int v = lane; v < klen / 8; v += 32)
@@ -222,22 +225,26 @@ __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, 
       continue;
     }
     const T* src = rowp(n) + kbeg;
-    uint4 buf[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + (i * 32 + lane) * kVec);
+    // pass 1: max |x| (and sum of squares); rows of up to 8 loads per lane
+    // stay in registers for pass 2, longer rows are read again
+    uint4 buf[8];
     float amax = 0.0f, ss = 0.0f;
+    for (int i0 = 0; i0 < nv; i0 += 8) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < nv) {
-        const T* e = reinterpret_cast<const T*>(&buf[i]);
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + ((i0 + i) * 32 + lane) * kVec);
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-          const float f = static_cast<float>(e[j]);
-          amax = fmaxf(amax, fabsf(f));
-          ss = fmaf(f, f, ss);
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < nv) {
+          const T* e = reinterpret_cast<const T*>(&buf[i]);
+#pragma unroll
+          for (int j = 0; j < kVec; ++j) {
+            const float f = static_cast<float>(e[j]);
+            amax = fmaxf(amax, fabsf(f));
+            ss = fmaf(f, f, ss);
+          }
         }
-      }
+    }
     amax = warp_max(amax);
     const int sh = f16_row_shift(amax);
     if (lane == 0) sig[n] = sh;
@@ -245,26 +252,34 @@ __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, 
       ss = warp_sum(ss);
       if (lane == 0) rms[n] = rsqrtf(ss / static_cast<float>(klen) + 1e-6f);
     }
+    // pass 2: convert and store
+    for (int i0 = 0; i0 < nv; i0 += 8) {
+      if (nv > 8) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (i < nv) {
-        const T* e = reinterpret_cast<const T*>(&buf[i]);
-        const int kq = (i * 32 + lane) * kVec;  // element offset of this load
-        if constexpr (sizeof(T) == 2) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            pk[j] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * j]), sh),
-                               scale_pow2(static_cast<float>(e[2 * j + 1]), sh));
-          *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        } else {
-          const uint32_t p0 = pack_f16x2(scale_pow2(static_cast<float>(e[0]), sh),
-                                         scale_pow2(static_cast<float>(e[1]), sh));
-          const uint32_t p1 = pack_f16x2(scale_pow2(static_cast<float>(e[2]), sh),
-                                         scale_pow2(static_cast<float>(e[3]), sh));
-          *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) = make_uint2(p0, p1);
-        }
+        for (int i = 0; i < 8; ++i)
+          if (i0 + i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + ((i0 + i) * 32 + lane) * kVec);
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i0 + i < nv) {
+          const T* e = reinterpret_cast<const T*>(&buf[i]);
+          const int kq = ((i0 + i) * 32 + lane) * kVec;  // element offset of this load
+          if constexpr (sizeof(T) == 2) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              pk[j] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * j]), sh),
+                                 scale_pow2(static_cast<float>(e[2 * j + 1]), sh));
+            *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          } else {
+            const uint32_t p0 = pack_f16x2(scale_pow2(static_cast<float>(e[0]), sh),
+                                           scale_pow2(static_cast<float>(e[1]), sh));
+            const uint32_t p1 = pack_f16x2(scale_pow2(static_cast<float>(e[2]), sh),
+                                           scale_pow2(static_cast<float>(e[3]), sh));
+            *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) = make_uint2(p0, p1);
+          }
+        }
+    }
   }
 }
 
@@ -306,9 +321,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&d_full[b], 1);
-      mbar_init(&d_empty[b], kDecWarps);
+      mbar_init(&d_empty[b], kEpiWarps);
     }
-    mbar_init(x_full, kDecWarps);
+    mbar_init(x_full, kEpiWarps);
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
     *abort_flag = 0;
@@ -442,10 +457,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_wait(mma_done, 0, a.status);
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------ decode + epilogue warps
+  } else if (warp < kEpiWarp0) {
+    // ------------------------------------------------ decode warps
     const int dw = warp - 2, q = warp & 3, half = dw >> 2;
-    const int dtid = threadIdx.x - 64;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    uint32_t acount = 0;
+    int rstage = 0;
+    uint32_t rphase = 0;
+    for (long u = u0; u < u1; ++u) {
+      wait_bar(&ring_full[rstage], rphase, a.status, abort_flag);
+      const uint8_t* st = ring + rstage * kTcStageBytes;
+      const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
+      // all shared-memory reads of this stage first (their latency overlaps)
+      const uint2 sb =
+          *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
+      uint4 cw[4];
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci)
+        cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring_empty[rstage]);
+      const uint32_t ab = acount % kABufs;
+      wait_bar(&a_empty[ab], ((acount / kABufs) & 1u) ^ 1u, a.status, abort_flag);
+      tc::fence_after_sync();
+      const uint32_t sbw[2] = {sb.x, sb.y};
+#pragma unroll
+      for (int ci = 0; ci < 4; ++ci) {
+        const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
+        const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
+        const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
+        const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
+        uint32_t v[16];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+          const uint32_t sv = wi < 2 ? s_lo : s_hi;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
+        }
+        tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[ab]);
+      ++acount;
+      if (++rstage == n_stages) {
+        rstage = 0;
+        rphase ^= 1u;
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int ew = warp - kEpiWarp0, q = warp & 3;
+    const int etid = threadIdx.x - kEpiWarp0 * 32;
     const int r = 32 * q + lane;  // tile row = tensor-memory lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
     if (MODE == kTcDense || MODE == kTcDown || a.ids_ready) pdl_wait();
@@ -453,12 +518,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (MODE == kTcDown && wk.n_tiles == 0 && b == 0) {
       // nothing routed and no shared expert: the layer output is zero
-      for (int i = dtid; i < a.T * a.H; i += kDecThreads)
+      for (int i = etid; i < a.T * a.H; i += kEpiThreads)
         a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
     }
-    // dense: the RMS factor needs whole rows when windows are partial
+    // dense: the RMS factor of each row over the whole K
     if (MODE == kTcDense && a.rms) {
-      for (int m = dw; m < a.M; m += kDecWarps) {
+      for (int m = ew; m < a.M; m += kEpiWarps) {
         float ss = 0.0f;
         const __nv_bfloat16* row = a.A + m * a.lda;
         for (int v = lane; v < a.K / 8; v += 32) {
@@ -473,9 +538,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
     XState xst;
-    uint32_t acount = 0, dcount = 0;
-    int rstage = 0;
-    uint32_t rphase = 0;
+    uint32_t dcount = 0;
     const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
     const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
 
@@ -486,9 +549,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int key = kk.b_key(tile);
       const int nr = kk.b_rows(tile);
       const int npad = nr <= 16 ? 16 : 32;
-      float tot[16];
+      float tot[32];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) tot[j] = 0.0f;
+      for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
 
       for (int w0 = kbs; w0 < kbe;) {
         const int w1 = window_end(kk, w0, kbe);
@@ -501,78 +564,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
             const int I = a.I;
             stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, npad,
-                           kbeg, klen, xs, sbo, sig, nullptr, dw, lane);
+                           kbeg, klen, xs, sbo, sig, nullptr, ew, lane, kEpiWarps);
           } else {
             const __nv_bfloat16* base = (MODE == kTcDense) ? a.A : a.x;
             const int64_t ld = (MODE == kTcDense) ? a.lda : a.ldx;
             stage_b<__nv_bfloat16>([&](int n) { return base + n * ld; }, nr, npad, kbeg, klen, xs,
-                                   sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr, dw,
-                                   lane);
+                                   sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr, ew,
+                                   lane, kEpiWarps);
           }
           fence_proxy_async_smem();
-          dsync();
+          esync();
           __syncwarp();
           if (lane == 0) mbar_arrive(x_full);
         }
-
-        // ---- decode the window's stages into tensor memory
-        for (int kb = w0; kb < w1; ++kb) {
-          wait_bar(&ring_full[rstage], rphase, a.status, abort_flag);
-          const uint8_t* st = ring + rstage * kTcStageBytes;
-          const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
-          // all shared-memory reads of this stage first (their latency overlaps)
-          const uint2 sb =
-              *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
-          uint4 cw[4];
-#pragma unroll
-          for (int ci = 0; ci < 4; ++ci)
-            cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ring_empty[rstage]);
-          const uint32_t ab = acount % kABufs;
-          wait_bar(&a_empty[ab], ((acount / kABufs) & 1u) ^ 1u, a.status, abort_flag);
-          tc::fence_after_sync();
-          const uint32_t sbw[2] = {sb.x, sb.y};
-#pragma unroll
-          for (int ci = 0; ci < 4; ++ci) {
-            const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
-            const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
-            const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
-            const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
-            uint32_t v[16];
-#pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-              e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-              const uint32_t sv = wi < 2 ? s_lo : s_hi;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
-            }
-            tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
-          }
-          tc::wait_st();
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[ab]);
-          ++acount;
-          if (++rstage == n_stages) {
-            rstage = 0;
-            rphase ^= 1u;
-          }
-        }
-
         // ---- fold the window's accumulator into the segment total
         const uint32_t db = dcount & 1u;
         wait_bar(&d_full[db], (dcount >> 1) & 1u, a.status, abort_flag);
         tc::fence_after_sync();
-        uint32_t dv[16];
-        tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * half, dv);
-        tc::wait_ld();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t dv[16];
+          tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * h, dv);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (16 * h + j < nr) tot[16 * h + j] += scale_pow2(__uint_as_float(dv[j]), -sig[16 * h + j]);
+        }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&d_empty[db]);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (16 * half + j < nr) tot[j] += scale_pow2(__uint_as_float(dv[j]), -sig[16 * half + j]);
         ++dcount;
         w0 = w1;
       }
@@ -583,39 +603,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int slot = (tile == first_tile) ? 0 : 1;
         float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) part[(16 * half + j) * kRows + r] = tot[j];
-        dsync();
+        for (int j = 0; j < 32; ++j)
+          if (j < nr) part[j * kRows + r] = tot[j];
+        esync();
         const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
         const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
-        if (dtid == 0) {
+        if (etid == 0) {
           __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
           const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
           *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
           if (*bcast) __threadfence();
         }
-        dsync();
-        if (!*bcast) continue;  // uniform across the decode warps
+        esync();
+        if (!*bcast) continue;  // uniform across the epilogue warps
 #pragma unroll
-        for (int j = 0; j < 16; ++j) tot[j] = 0.0f;
+        for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
         for (int bb = blo; bb <= bhi; ++bb) {
           const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
           const float* pp = a.partials + static_cast<size_t>(bb * 2 + sl) * (32 * kRows);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) tot[j] += __ldcg(pp + (16 * half + j) * kRows + r);
+          for (int j = 0; j < 32; ++j)
+            if (j < nr) tot[j] += __ldcg(pp + j * kRows + r);
         }
-        if (dtid == 0) a.tile_cnt[tile] = 0u;
+        if (etid == 0) a.tile_cnt[tile] = 0u;
       }
 
       // ---- epilogues
       if (MODE == kTcDense) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int m = 16 * half + j;
-          if (m < a.M) ep[m * kRows + r] = tot[j] * gs * (a.rms ? rms[m] : 1.0f);
-        }
-        dsync();
+        for (int j = 0; j < 32; ++j)
+          if (j < a.M) ep[j * kRows + r] = tot[j] * gs * (a.rms ? rms[j] : 1.0f);
+        esync();
         const int n0 = tile * kRows;
-        for (int m = dw; m < a.M; m += kDecWarps) {
+        for (int m = ew; m < a.M; m += kEpiWarps) {
           float bv = -FLT_MAX;
           int bi = 0x7fffffff;
 #pragma unroll
@@ -637,16 +657,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (a.argmax_out) {
-          dsync();
-          if (dtid == 0) {
+          esync();
+          if (etid == 0) {
             __threadfence();
             const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
             *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
             if (*bcast) __threadfence();
           }
-          dsync();
+          esync();
           if (*bcast) {
-            for (int m = dw; m < a.M; m += kDecWarps) {
+            for (int m = ew; m < a.M; m += kEpiWarps) {
               float bv = -FLT_MAX;
               int bi = 0x7fffffff;
               for (int j = lane; j < wk.n_tiles; j += 32) {
@@ -660,7 +680,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               am_warp_reduce(bv, bi);
               if (lane == 0) a.argmax_out[m] = bi;
             }
-            if (dtid == 0) *a.argmax_cnt = 0u;
+            if (etid == 0) *a.argmax_cnt = 0u;
           }
         }
       } else if (MODE == kTcGateUp) {
@@ -668,9 +688,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // for pair-box 2*tile+1 (absent when the count is odd)
         if (q & 1) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ep[(16 * half + j) * kRows + r] = tot[j];
+          for (int j = 0; j < 32; ++j) ep[j * kRows + r] = tot[j];
         }
-        dsync();
+        esync();
         const int pb = 2 * tile + (q >> 1);
         if (!(q & 1) && pb < wk.pb_count) {
           const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
@@ -679,16 +699,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int qq = 0; qq < cnt; ++qq) {
             const int p = off + qq;
             const int t = sc.pair_tok[p];
-            if ((t >> 4) != half) continue;
             const float f = a.rms ? g * rms[t] : g;
+            float gt = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (j == (t & 15)) {
-                const float gt = tot[j] * f;
-                const float up = ep[t * kRows + r + 32] * f;
-                a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
-              }
-            }
+            for (int j = 0; j < 32; ++j)
+              if (j == t) gt = tot[j];
+            gt *= f;
+            const float up = ep[t * kRows + r + 32] * f;
+            a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
           }
         }
       } else {
@@ -696,45 +714,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
         const int cnt = sc.cnt[e], off = sc.off[e];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int qq = 16 * half + j;
-          if (qq < cnt) a.y[static_cast<size_t>(off + qq) * a.H + nt * kRows + r] = tot[j] * g;
-        }
-        dsync();
+        for (int j = 0; j < 32; ++j)
+          if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
+        esync();
         uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
-        if (dtid == 0) {
+        if (etid == 0) {
           __threadfence();
           const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
           *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
           if (*bcast) __threadfence();
         }
-        dsync();
+        esync();
         if (*bcast) {
-          // the last expert to finish this column: weighted combine in slot order
+          // the last expert to finish this 128-column slice: weighted combine
+          // in slot order, shared expert last; warp per token, 4 columns a lane
           const int sh_off = sc.off[a.E];
-          for (int i = dtid; i < a.T * kRows; i += kDecThreads) {
-            const int t = i >> 7, c = i & 127;
-            const int n = nt * kRows + c;
-            float vals[17];
+          const int n = nt * kRows + 4 * lane;
+          for (int t = ew; t < a.T; t += kEpiWarps) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j0 = 0; j0 <= a.k; j0 += 8) {
+              float4 yv[8];
+              float wv[8];
 #pragma unroll
-            for (int j = 0; j < 17; ++j) {
-              vals[j] = 0.0f;
-              if (j < a.k) {
-                const int pr = sc.flat_pair[t * a.k + j];
-                if (pr >= 0) vals[j] = a.w[t * a.k + j] * __ldcg(a.y + static_cast<size_t>(pr) * a.H + n);
-              } else if (j == a.k && a.has_shared) {
-                vals[j] = __ldcg(a.y + static_cast<size_t>(sh_off + t) * a.H + n);
+              for (int jj = 0; jj < 8; ++jj) {
+                const int j = j0 + jj;
+                yv[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+                wv[jj] = 0.0f;
+                int pr = -1;
+                if (j < a.k) {
+                  pr = sc.flat_pair[t * a.k + j];
+                  if (pr >= 0) wv[jj] = a.w[t * a.k + j];
+                } else if (j == a.k && a.has_shared) {
+                  pr = sh_off + t;
+                  wv[jj] = 1.0f;
+                }
+                if (pr >= 0)
+                  yv[jj] = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pr) * a.H + n));
+              }
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                acc.x = fmaf(wv[jj], yv[jj].x, acc.x);
+                acc.y = fmaf(wv[jj], yv[jj].y, acc.y);
+                acc.z = fmaf(wv[jj], yv[jj].z, acc.z);
+                acc.w = fmaf(wv[jj], yv[jj].w, acc.w);
               }
             }
-            float s = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 17; ++j) s += vals[j];
-            a.out[t * a.ldo + n] = __float2bfloat16_rn(s);
+            __nv_bfloat16* o = a.out + t * a.ldo + n;
+            o[0] = __float2bfloat16_rn(acc.x);
+            o[1] = __float2bfloat16_rn(acc.y);
+            o[2] = __float2bfloat16_rn(acc.z);
+            o[3] = __float2bfloat16_rn(acc.w);
           }
-          if (dtid == 0) col_cnt[nt] = 0u;
+          if (etid == 0) col_cnt[nt] = 0u;
         }
       }
-      dsync();
+      esync();
     }
   }
 
