@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--path", default="program", choices=["program", "calls"],
+                   help="program: the step as one persistent launch after routing; calls: one "
+                        "kernel launch per call")
     return p.parse_args()
 
 
@@ -269,12 +272,15 @@ def run_ours(args, rank, world, local):
         if dist is not None:
             dist.barrier()
 
-    def one_config(t, steps, warmup, sample_clocks):
+    def one_config(t, steps, warmup, sample_clocks, path=None):
+        path = path or args.path
         b = model.buffers(t)
         x, lg = model.inputs(t)
         b["x"].copy_(x)
         b["logits"].copy_(lg)
-        g = model.capture(b)
+        prog = model.program(b) if path == "program" else None
+        g = model.capture(b, prog=prog)
+        b["prog"] = prog
         for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
@@ -303,7 +309,7 @@ def run_ours(args, rank, world, local):
 
     t = args.tokens
     b, g, x, lg, ms, nbytes, clocks = one_config(t, args.steps, args.warmup, True)
-    n_launch = 1 + 4 * model.s.layers + 1
+    n_launch = 2 if args.path == "program" else 1 + 4 * model.s.layers + 1
     value = nbytes * world / (ms * 1e-3) / 1e9
 
     # ---- end to end: pinned host inputs in, argmax ids out, every step
@@ -332,34 +338,51 @@ def run_ours(args, rank, world, local):
            "d2h_bytes_per_step": outh.numel() * outh.element_size(), "ms_per_step": e_ms,
            "steps": e_steps}
 
-    # ---- the dominant op: the MoE layer call (gate_up + down kernels), 40 layers
+    # ---- the dominant kernel, timed alone with CUDA events on its stream
     s = model.s
-    moe_g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(moe_g):
-        for l in range(s.layers):
-            ops.moe(b["o"][0], b["ids"][l * t:(l + 1) * t], b["w"][l * t:(l + 1) * t],
-                    model.experts[l], model.shared[l], out=b["y"][0], rms_input=True,
-                    workspace=b["ws"])
-    for _ in range(3):
-        moe_g.replay()
-    torch.cuda.synchronize()
-    moe_ms = timed_replays(moe_g, max(5, min(args.steps, 100)), stream)
-    per_expert = 3 * 2048 * 512 * 9 // 16  # gate_up + down bytes of one expert
-    ids_l = b["ids"].view(s.layers, -1).cpu()
-    moe_bytes = sum((torch.unique(ids_l[l]).numel() + 1) * per_expert for l in range(s.layers))
     peak, peak_kind = measured_peak()
-    achieved = moe_bytes / (moe_ms * 1e-3) / 1e9
+    peak_src = (f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s")
+    if args.path == "program":
+        # the program kernel: every projection, MoE layer and the head of the step
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg):
+            b["prog"].launch()
+        for _ in range(3):
+            kg.replay()
+        torch.cuda.synchronize()
+        k_ms = timed_replays(kg, max(5, min(args.steps, 100)), stream)
+        k_bytes, k_launches = nbytes, 1
+        k_name = f"stream_tc_kernel, program of the step ({3 * s.layers + 1} calls), per launch"
+        k_key = f"program_T{t}_L{s.layers}"
+    else:
+        # the MoE layer call (gate_up + down launches), 40 layers
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg):
+            for l in range(s.layers):
+                ops.moe(b["o"][0], b["ids"][l * t:(l + 1) * t], b["w"][l * t:(l + 1) * t],
+                        model.experts[l], model.shared[l], out=b["y"][0], rms_input=True,
+                        workspace=b["ws"])
+        for _ in range(3):
+            kg.replay()
+        torch.cuda.synchronize()
+        k_ms = timed_replays(kg, max(5, min(args.steps, 100)), stream)
+        per_expert = 3 * 2048 * 512 * 9 // 16  # gate_up + down bytes of one expert
+        ids_l = b["ids"].view(s.layers, -1).cpu()
+        k_bytes = sum((torch.unique(ids_l[l]).numel() + 1) * per_expert for l in range(s.layers))
+        k_launches = s.layers
+        k_name = "moe_nvfp4_decode (stream_tc_kernel gate_up + down), per call"
+        k_key = f"moe_layer_T{t}"
+    achieved = k_bytes / (k_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(f"moe_layer_T{t}"),
-                "kernel": "moe_nvfp4_decode (moe_gate_up_kernel + moe_down_kernel), per call",
-                "bytes_per_launch": moe_bytes / s.layers, "us_per_launch": moe_ms * 1e3 / s.layers,
-                "peak_source": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_kind == "measured" else "fallback 6.8 TB/s"}
+                "frac": achieved / peak, "traffic": profiled_traffic(k_key),
+                "kernel": k_name, "bytes_per_launch": k_bytes / k_launches,
+                "us_per_launch": k_ms * 1e3 / k_launches, "peak_source": peak_src}
+    del kg
 
     # ---- other token counts of the same step (context)
     sweep = {}
     if not args.no_sweep:
-        del moe_g
         for tt in (1, 8, 32):
             if tt == t:
                 sweep[str(tt)] = {"us_per_step": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
@@ -369,6 +392,14 @@ def run_ours(args, rank, world, local):
             sweep[str(tt)] = {"us_per_step": ms2 * 1e3, "gbs": nb2 / (ms2 * 1e-3) / 1e9,
                               "weight_bytes": nb2}
             del g2
+
+    # ---- the same step issued call by call (one kernel per call), for context
+    calls = None
+    if args.path == "program" and not args.no_sweep:
+        _, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, "calls")
+        calls = {"us_per_step": ms3 * 1e3, "gbs": nb3 / (ms3 * 1e-3) / 1e9,
+                 "launches_per_step": 1 + 4 * model.s.layers + 1}
+        del g3
 
     # ---- CPU baseline: the oracle on one layer of the same step
     cpu = None
@@ -398,6 +429,7 @@ def run_ours(args, rank, world, local):
                        "parallelism": f"{world} independent replica(s)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": n_launch * args.steps, "clocks": clocks, "sweep": sweep,
+            "path": args.path, "call_by_call": calls,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

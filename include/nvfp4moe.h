@@ -171,6 +171,67 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
                      uint32_t flags, void* workspace, size_t workspace_bytes,
                      nvfp4_stream_t stream);
 
+/* ---- programs: a chain of calls in one launch -----------------------------
+ * (This library's own runtime; the pages run each matmul as its own kernel
+ * replayed from a CUDA graph.)  A program is a fixed sequence of GEMM and MoE
+ * calls in which each call may read what the calls before it wrote, e.g. the
+ * projections and MoE layers of a whole decode step.  nvfp4_program_launch
+ * runs the sequence in one cooperative launch with one CTA per SM: each SM
+ * keeps streaming the weights of the calls ahead while the current call's
+ * split-K reductions finish, and a call reads its activations only once every
+ * CTA has finished the call before it (completion counters in the workspace).
+ * Results are bit-identical to issuing the same calls one by one.
+ *
+ * nvfp4_op: kind NVFP4_OP_GEMM takes the arguments of nvfp4_gemm_skinny (A,
+ * lda, M, W, C, ldc, argmax_out), kind NVFP4_OP_MOE those of moe_nvfp4_decode
+ * (x ... ldo; shared.num_experts == 0 means no shared expert).  flags:
+ * NVFP4_FLAG_RMS_INPUT per op (NVFP4_FLAG_NO_PDL and NVFP4_FLAG_IDS_READY are
+ * accepted and ignored).  Every MoE op's topk_ids / topk_w must be complete
+ * before the launch (e.g. routed earlier on the stream).  Limits as for the
+ * single calls; at most 4,095 kernel ops (a MoE op counts two).
+ *
+ * nvfp4_program_create validates every op, encodes its tensor maps, and
+ * copies the op table to device memory: the one call of this library that
+ * allocates (cudaMalloc) and synchronises; do it once, before any capture.
+ * The program binds every pointer given, including the workspace (at least
+ * nvfp4_program_workspace() bytes, zero-filled once); nvfp4_program_launch is
+ * asynchronous and graph-capturable.  The workspace must not be used by
+ * another call while a launch may be running.  nvfp4_program_destroy frees
+ * the table (after the last launch has finished). */
+enum { NVFP4_OP_GEMM = 1, NVFP4_OP_MOE = 2 };
+
+typedef struct nvfp4_op {
+  int32_t kind;
+  uint32_t flags;
+  /* NVFP4_OP_GEMM */
+  const void* A;
+  int64_t lda;
+  int32_t M;
+  nvfp4_weight W;
+  void* C;
+  int64_t ldc;
+  int32_t* argmax_out;
+  /* NVFP4_OP_MOE */
+  const void* x;
+  int64_t ldx;
+  int32_t T;
+  const int32_t* topk_ids;
+  const float* topk_w;
+  int32_t k;
+  nvfp4_expert_stack experts;
+  nvfp4_expert_stack shared;
+  void* out;
+  int64_t ldo;
+} nvfp4_op;
+
+typedef struct nvfp4_program nvfp4_program;
+
+size_t nvfp4_program_workspace(const nvfp4_op* ops, int n_ops);
+int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace,
+                         size_t workspace_bytes, nvfp4_program** program);
+int nvfp4_program_launch(const nvfp4_program* program, nvfp4_stream_t stream);
+int nvfp4_program_destroy(nvfp4_program* program);
+
 /* ---- diagnostics ---------------------------------------------------------
  * Copy the workspace's status word to *flags and clear it.  Synchronises
  * `stream`: for tests, not for the decode loop. */

@@ -8,8 +8,11 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
+#include <new>
 #include <string>
+#include <vector>
 
 #include "nvfp4moe.h"
 #include "common.cuh"
@@ -91,10 +94,10 @@ int get_encoder() {
 // uint8 matrix [rows, cols] (row stride = cols bytes) read in boxes of
 // box_cols x 32 rows; codes use the 128-byte swizzle.
 int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-             bool swizzle) {
+             bool swizzle, uint32_t box_rows) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {box_cols, static_cast<cuuint32_t>(kBoxRows)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -104,11 +107,14 @@ int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
   return NVFP4_OK;
 }
 
+// Codes and scales of a weight, one 256-K stage wide; boxes of box_rows rows
+// (32 for the warp-MMA kernels and the gate_up tiles, 128 for whole
+// 128-row tiles).
 int weight_maps(CUtensorMap* mc, CUtensorMap* ms, const uint8_t* codes, const uint8_t* scales,
-                uint64_t rows, int k) {
-  int rc = make_map(mc, codes, static_cast<uint64_t>(k) / 2, rows, kStageK / 2, true);
+                uint64_t rows, int k, uint32_t box_rows = kBoxRows) {
+  int rc = make_map(mc, codes, static_cast<uint64_t>(k) / 2, rows, kStageK / 2, true, box_rows);
   if (rc) return rc;
-  return make_map(ms, scales, static_cast<uint64_t>(k) / 16, rows, kStageK / 16, false);
+  return make_map(ms, scales, static_cast<uint64_t>(k) / 16, rows, kStageK / 16, false, box_rows);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -126,7 +132,7 @@ struct DensePlan {
 // staged in windows of at most win_stages stages.
 bool plan_dense(int M, int N, int K, int sms, DensePlan* p) {
   p->n_tiles = (N + kTileRows - 1) / kTileRows;
-  if (p->n_tiles > kWsMaxCounters) return false;
+  if (p->n_tiles > kTcColCntBase) return false;
   p->nkb = K / kStageK;
   p->units = static_cast<long>(p->n_tiles) * p->nkb;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
@@ -257,11 +263,188 @@ int check_stack(const nvfp4_expert_stack* s, const char* name) {
   return NVFP4_OK;
 }
 
+
+// ------------------------------------------------------------- validation
+int check_gemm(const void* A, int64_t lda, int M, const nvfp4_weight* W, const void* C,
+               int64_t ldc) {
+  if (!A || !W || !C) return fail(NVFP4_ERR_INVALID, "A, W and C must be non-NULL");
+  if (!W->codes || !W->scales || !W->global_scale)
+    return fail(NVFP4_ERR_INVALID, "weight has a NULL pointer");
+  const int N = W->n, K = W->k;
+  if (M < 1 || M > kMaxM) return fail(NVFP4_ERR_SHAPE, "M=%d outside [1, 32]", M);
+  if (N < 1 || K < 1) return fail(NVFP4_ERR_INVALID, "N=%d K=%d must be positive", N, K);
+  if (K % kStageK) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 256", K);
+  if (lda < K || ldc < N) return fail(NVFP4_ERR_INVALID, "lda < K or ldc < N");
+  if (!aligned16(A) || (lda * 2) % 16 || !aligned16(W->codes) || !aligned16(W->scales))
+    return fail(NVFP4_ERR_ALIGN, "A rows and weight arrays must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(C) & 1u) return fail(NVFP4_ERR_ALIGN, "C must be 2-byte aligned");
+  return NVFP4_OK;
+}
+
+int check_moe(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const float* topk_w,
+              int k, const nvfp4_expert_stack* experts, const nvfp4_expert_stack* shared,
+              const void* out, int64_t ldo) {
+  if (!x || !topk_ids || !topk_w || !out) return fail(NVFP4_ERR_INVALID, "NULL pointer");
+  int rc = check_stack(experts, "experts");
+  if (rc) return rc;
+  if (shared) {
+    if ((rc = check_stack(shared, "shared"))) return rc;
+    if (shared->num_experts != 1 || shared->hidden != experts->hidden ||
+        shared->inter != experts->inter)
+      return fail(NVFP4_ERR_INVALID, "shared must be one expert of the same shape");
+  }
+  const int E = experts->num_experts, H = experts->hidden;
+  if (T < 1 || T > kMaxM) return fail(NVFP4_ERR_SHAPE, "T=%d outside [1, 32]", T);
+  if (k < 1 || k > 16 || k > E) return fail(NVFP4_ERR_SHAPE, "need 1 <= k <= min(16, E)");
+  if (E > 512) return fail(NVFP4_ERR_SHAPE, "E=%d > 512", E);
+  if (ldx < H || ldo < H) return fail(NVFP4_ERR_INVALID, "ldx and ldo must be >= hidden");
+  if (!aligned16(x) || (ldx * 2) % 16) return fail(NVFP4_ERR_ALIGN, "x rows must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(out) & 1u) return fail(NVFP4_ERR_ALIGN, "out must be 2-byte aligned");
+  return NVFP4_OK;
+}
+
+// ------------------------------------------------------------- tcgen05 ops
+void ws_header(TcArgs& a, uint8_t* ws) {
+  a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
+  a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
+}
+
+// Dense op of a planned GEMM (arguments already checked).
+int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C, int64_t ldc,
+                int32_t* argmax_out, uint32_t flags, uint8_t* ws, const TcDensePlan& p, TcOp* op) {
+  memset(op, 0, sizeof(*op));
+  int rc = weight_maps(&op->maps[0], &op->maps[1], W->codes, W->scales,
+                       static_cast<uint64_t>(W->n), W->k, kTcTileRows);
+  if (rc) return rc;
+  op->maps[2] = op->maps[0];
+  op->maps[3] = op->maps[1];
+  TcArgs& a = op->a;
+  a.A = static_cast<const __nv_bfloat16*>(A);
+  a.lda = lda;
+  a.C = static_cast<__nv_bfloat16*>(C);
+  a.ldc = ldc;
+  a.argmax_out = argmax_out;
+  a.gscale = W->global_scale;
+  a.M = M;
+  a.N = W->n;
+  a.K = W->k;
+  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  a.win_k = p.win_k;
+  ws_header(a, ws);
+  a.partials = reinterpret_cast<float*>(ws + p.off_partials);
+  a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
+  op->mode = kTcDense;
+  op->wait_prev = 1;
+  return NVFP4_OK;
+}
+
+// gate_up and down ops of a planned MoE layer (arguments already checked).
+int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const float* topk_w,
+               int k, const nvfp4_expert_stack* experts, const nvfp4_expert_stack* shared,
+               void* out, int64_t ldo, uint32_t flags, uint8_t* ws, const TcMoePlan& p,
+               TcOp* gu, TcOp* dn) {
+  const int E = experts->num_experts, H = experts->hidden, I = experts->inter;
+  const nvfp4_expert_stack* sh = shared ? shared : experts;
+  memset(gu, 0, sizeof(*gu));
+  int rc;
+  if ((rc = weight_maps(&gu->maps[0], &gu->maps[1], experts->gu_codes, experts->gu_scales,
+                        2ull * I * E, H)) ||
+      (rc = weight_maps(&gu->maps[2], &gu->maps[3], sh->gu_codes, sh->gu_scales,
+                        2ull * I * sh->num_experts, H)))
+    return rc;
+  TcArgs& a = gu->a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ldx = ldx;
+  a.ids = topk_ids;
+  a.w = topk_w;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = ldo;
+  a.gu_global = experts->gu_global;
+  a.dn_global = experts->dn_global;
+  a.sh_gu_global = sh->gu_global;
+  a.sh_dn_global = sh->dn_global;
+  a.T = T;
+  a.k = k;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.has_shared = shared ? 1 : 0;
+  a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
+  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  ws_header(a, ws);
+  a.partials = reinterpret_cast<float*>(ws + p.off_partials);
+  a.h = reinterpret_cast<float*>(ws + p.off_h);
+  a.y = reinterpret_cast<float*>(ws + p.off_y);
+  a.win_k = H;
+  gu->mode = kTcGateUp;
+  gu->new_sched = 1;
+  gu->wait_prev = 1;
+  *dn = *gu;
+  if ((rc = weight_maps(&dn->maps[0], &dn->maps[1], experts->dn_codes, experts->dn_scales,
+                        static_cast<uint64_t>(H) * E, I, kTcTileRows)) ||
+      (rc = weight_maps(&dn->maps[2], &dn->maps[3], sh->dn_codes, sh->dn_scales,
+                        static_cast<uint64_t>(H) * sh->num_experts, I, kTcTileRows)))
+    return rc;
+  dn->a.win_k = I;
+  dn->mode = kTcDown;
+  dn->new_sched = 0;
+  dn->last_sched_use = 1;
+  return NVFP4_OK;
+}
+
+// Shared-memory layout of a program whose largest op stages x_bytes of
+// activations and whose MoE schedules take sched_bytes (slots of them).
+bool tc_program_layout(size_t x_bytes, int sched_bytes, int slots, TcProgram* pr, size_t* smem) {
+  TcLayout L;
+  if (!tc_layout(sched_bytes * slots, x_bytes, &L)) return false;
+  pr->x_offset = L.x_offset;
+  pr->ring_offset = L.ring_offset;
+  pr->n_stages = L.n_stages;
+  pr->sched_offset = kTcOffSched;
+  pr->sched_bytes = sched_bytes;
+  pr->sched_slots = slots;
+  *smem = L.smem;
+  return true;
+}
+
+void tc_program_header(TcProgram* pr, uint8_t* ws) {
+  pr->status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
+  pr->done = reinterpret_cast<uint32_t*>(ws + kWsCounters) + kTcDoneBase;
+}
+
+// A one-op program passed by value.
+int tc_launch_one(const TcOp& op, size_t x_bytes, int sched_bytes, int grid, uint8_t* ws,
+                  cudaStream_t s, bool pdl, int* n_stages, size_t* smem, const char* what) {
+  TcProgram pr;
+  memset(&pr, 0, sizeof(pr));
+  if (!tc_program_layout(x_bytes, sched_bytes, 1, &pr, smem))
+    return fail(NVFP4_ERR_SHAPE, "%s: staged activations exceed shared memory", what);
+  tc_program_header(&pr, ws);
+  pr.ops = nullptr;
+  pr.n_ops = 1;
+  pr.inline_ops[0] = op;
+  pr.inline_ops[0].new_sched = op.mode == kTcDense ? 0 : 1;
+  pr.inline_ops[0].last_sched_use = op.mode == kTcDense ? 0 : 1;
+  *n_stages = pr.n_stages;
+  cudaError_t e = launch_tc(pr, grid, *smem, s, pdl, false);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return NVFP4_OK;
+}
 }  // namespace
 
 namespace nvfp4 {
 void set_last_error(const char* msg) { g_error = msg; }
 }  // namespace nvfp4
+
+// A program: its op table on the device and the launch that runs it.
+struct nvfp4_program {
+  nvfp4::TcOp* d_ops = nullptr;
+  nvfp4::TcProgram params;
+  int grid = 0;
+  int device = -1;
+  size_t smem = 0;
+  std::string desc;
+};
 
 // =================================================================== C ABI
 extern "C" {
@@ -298,20 +481,11 @@ size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
 int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
                       int64_t ldc, int32_t* argmax_out, uint32_t flags, void* workspace,
                       size_t workspace_bytes, nvfp4_stream_t stream) {
-  if (!A || !W || !C) return fail(NVFP4_ERR_INVALID, "A, W and C must be non-NULL");
-  if (!W->codes || !W->scales || !W->global_scale)
-    return fail(NVFP4_ERR_INVALID, "weight has a NULL pointer");
-  const int N = W->n, K = W->k;
-  if (M < 1 || M > kMaxM) return fail(NVFP4_ERR_SHAPE, "M=%d outside [1, 32]", M);
-  if (N < 1 || K < 1) return fail(NVFP4_ERR_INVALID, "N=%d K=%d must be positive", N, K);
-  if (K % kStageK) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 256", K);
-  if (lda < K || ldc < N) return fail(NVFP4_ERR_INVALID, "lda < K or ldc < N");
-  if (!aligned16(A) || (lda * 2) % 16 || !aligned16(W->codes) || !aligned16(W->scales))
-    return fail(NVFP4_ERR_ALIGN, "A rows and weight arrays must be 16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(C) & 1u) return fail(NVFP4_ERR_ALIGN, "C must be 2-byte aligned");
-  int sms = 0;
-  int rc = current_device(&sms);
+  int rc = check_gemm(A, lda, M, W, C, ldc);
   if (rc) return rc;
+  const int N = W->n, K = W->k;
+  int sms = 0;
+  if ((rc = current_device(&sms))) return rc;
   if (!(flags & NVFP4_FLAG_WARP_MMA)) {
     TcDensePlan p;
     if (!plan_tc_dense(M, N, K, sms, &p))
@@ -319,41 +493,21 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
     if (!workspace || workspace_bytes < p.ws_bytes)
       return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
     if ((rc = get_encoder())) return rc;
-    CUtensorMap maps[4];
-    if ((rc = weight_maps(&maps[0], &maps[1], W->codes, W->scales, static_cast<uint64_t>(N), K)))
-      return rc;
-    maps[2] = maps[0];
-    maps[3] = maps[1];
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    TcArgs a = {};
-    a.A = static_cast<const __nv_bfloat16*>(A);
-    a.lda = lda;
-    a.C = static_cast<__nv_bfloat16*>(C);
-    a.ldc = ldc;
-    a.argmax_out = argmax_out;
-    a.gscale = W->global_scale;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
-    a.win_k = p.win_k;
-    a.x_offset = p.L.x_offset;
-    a.ring_offset = p.L.ring_offset;
-    a.n_stages = p.L.n_stages;
-    a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
-    a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
-    a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
-    a.partials = reinterpret_cast<float*>(ws + p.off_partials);
-    a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
-    cudaError_t e = launch_tc(kTcDense, maps, a, p.grid, p.L.smem,
-                              reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL));
-    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<dense> launch");
+    TcOp op;
+    if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, flags, ws, p, &op))) return rc;
+    int n_stages = 0;
+    size_t smem = 0;
+    rc = tc_launch_one(op, static_cast<size_t>(p.npad) * p.win_k * 2, 0, p.grid, ws,
+                       reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL),
+                       &n_stages, &smem, "stream_tc_kernel<dense> launch");
+    if (rc) return rc;
     char buf[256];
     snprintf(buf, sizeof(buf),
              "stream_tc_kernel<dense> grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d "
              "n=%d stages=%d smem=%zu argmax=%d rms=%d",
              p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_k, p.npad,
-             p.L.n_stages, p.L.smem, argmax_out ? 1 : 0, a.rms);
+             n_stages, smem, argmax_out ? 1 : 0, op.a.rms);
     g_dispatch = buf;
     return NVFP4_OK;
   }
@@ -435,22 +589,9 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
                      const float* topk_w, int k, const nvfp4_expert_stack* experts,
                      const nvfp4_expert_stack* shared, void* out, int64_t ldo, uint32_t flags,
                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
-  if (!x || !topk_ids || !topk_w || !out) return fail(NVFP4_ERR_INVALID, "NULL pointer");
-  int rc = check_stack(experts, "experts");
+  int rc = check_moe(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo);
   if (rc) return rc;
-  if (shared) {
-    if ((rc = check_stack(shared, "shared"))) return rc;
-    if (shared->num_experts != 1 || shared->hidden != experts->hidden ||
-        shared->inter != experts->inter)
-      return fail(NVFP4_ERR_INVALID, "shared must be one expert of the same shape");
-  }
   const int E = experts->num_experts, H = experts->hidden, I = experts->inter;
-  if (T < 1 || T > kMaxM) return fail(NVFP4_ERR_SHAPE, "T=%d outside [1, 32]", T);
-  if (k < 1 || k > 16 || k > E) return fail(NVFP4_ERR_SHAPE, "need 1 <= k <= min(16, E)");
-  if (E > 512) return fail(NVFP4_ERR_SHAPE, "E=%d > 512", E);
-  if (ldx < H || ldo < H) return fail(NVFP4_ERR_INVALID, "ldx and ldo must be >= hidden");
-  if (!aligned16(x) || (ldx * 2) % 16) return fail(NVFP4_ERR_ALIGN, "x rows must be 16-byte aligned");
-  if (reinterpret_cast<uintptr_t>(out) & 1u) return fail(NVFP4_ERR_ALIGN, "out must be 2-byte aligned");
   int sms = 0;
   if ((rc = current_device(&sms))) return rc;
   if (!(flags & NVFP4_FLAG_WARP_MMA)) {
@@ -461,63 +602,26 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
     if (!workspace || workspace_bytes < p.ws_bytes)
       return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
     if ((rc = get_encoder())) return rc;
-    const nvfp4_expert_stack* sh = shared ? shared : experts;
-    CUtensorMap gu[4], dn[4];
-    if ((rc = weight_maps(&gu[0], &gu[1], experts->gu_codes, experts->gu_scales,
-                          2ull * I * E, H)) ||
-        (rc = weight_maps(&gu[2], &gu[3], sh->gu_codes, sh->gu_scales,
-                          2ull * I * sh->num_experts, H)) ||
-        (rc = weight_maps(&dn[0], &dn[1], experts->dn_codes, experts->dn_scales,
-                          static_cast<uint64_t>(H) * E, I)) ||
-        (rc = weight_maps(&dn[2], &dn[3], sh->dn_codes, sh->dn_scales,
-                          static_cast<uint64_t>(H) * sh->num_experts, I)))
-      return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    TcArgs a = {};
-    a.x = static_cast<const __nv_bfloat16*>(x);
-    a.ldx = ldx;
-    a.ids = topk_ids;
-    a.w = topk_w;
-    a.out = static_cast<__nv_bfloat16*>(out);
-    a.ldo = ldo;
-    a.gu_global = experts->gu_global;
-    a.dn_global = experts->dn_global;
-    a.sh_gu_global = sh->gu_global;
-    a.sh_dn_global = sh->dn_global;
-    a.T = T;
-    a.k = k;
-    a.E = E;
-    a.H = H;
-    a.I = I;
-    a.has_shared = shared ? 1 : 0;
-    a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
-    a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
-    a.sched_offset = kTcOffSched;
-    a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
-    a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
-    a.partials = reinterpret_cast<float*>(ws + p.off_partials);
-    a.h = reinterpret_cast<float*>(ws + p.off_h);
-    a.y = reinterpret_cast<float*>(ws + p.off_y);
+    TcOp gu, dn;
+    if ((rc = tc_moe_ops(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo, flags, ws, p,
+                         &gu, &dn)))
+      return rc;
     const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    a.win_k = H;
-    a.x_offset = p.gu.x_offset;
-    a.ring_offset = p.gu.ring_offset;
-    a.n_stages = p.gu.n_stages;
-    cudaError_t e = launch_tc(kTcGateUp, gu, a, p.grid, p.gu.smem, s, pdl);
-    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<gate_up> launch");
-    a.win_k = I;
-    a.x_offset = p.dn.x_offset;
-    a.ring_offset = p.dn.ring_offset;
-    a.n_stages = p.dn.n_stages;
-    e = launch_tc(kTcDown, dn, a, p.grid, p.dn.smem, s, pdl);
-    if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel<down> launch");
+    int st_gu = 0, st_dn = 0;
+    size_t sm_gu = 0, sm_dn = 0;
+    if ((rc = tc_launch_one(gu, static_cast<size_t>(p.npad) * H * 2, p.sched_bytes, p.grid, ws, s,
+                            pdl, &st_gu, &sm_gu, "stream_tc_kernel<gate_up> launch")) ||
+        (rc = tc_launch_one(dn, static_cast<size_t>(p.npad) * I * 2, p.sched_bytes, p.grid, ws, s,
+                            pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
+      return rc;
     char buf[256];
     snprintf(buf, sizeof(buf),
              "stream_tc_kernel<gate_up> grid=%d stages=%d smem=%zu; stream_tc_kernel<down> grid=%d "
              "stages=%d smem=%zu; T=%d k=%d E=%d n=%d shared=%d rms=%d ids_ready=%d",
-             p.grid, p.gu.n_stages, p.gu.smem, p.grid, p.dn.n_stages, p.dn.smem, T, k, E, p.npad,
-             a.has_shared, a.rms, a.ids_ready);
+             p.grid, st_gu, sm_gu, p.grid, st_dn, sm_dn, T, k, E, p.npad, gu.a.has_shared,
+             gu.a.rms, gu.a.ids_ready);
     g_dispatch = buf;
     return NVFP4_OK;
   }
@@ -579,6 +683,155 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
            p.grid_gu, p.smem_gu, p.grid_dn, p.smem_dn, T, k, E, a.has_shared, a.rms, a.ids_ready);
   g_dispatch = buf;
   return NVFP4_OK;
+}
+
+size_t nvfp4_program_workspace(const nvfp4_op* ops, int n_ops) {
+  int sms = 0;
+  if (!ops || n_ops < 1 || n_ops > kTcMaxOps) return 0;
+  if (current_device(&sms) != NVFP4_OK) return 0;
+  size_t need = kWsScratch;
+  for (int i = 0; i < n_ops; ++i) {
+    const nvfp4_op& o = ops[i];
+    size_t b = 0;
+    if (o.kind == NVFP4_OP_GEMM) {
+      TcDensePlan t;
+      if (o.M < 1 || o.M > kMaxM || o.W.k < kStageK || o.W.k % kStageK ||
+          !plan_tc_dense(o.M, o.W.n, o.W.k, sms, &t))
+        return 0;
+      b = t.ws_bytes;
+    } else if (o.kind == NVFP4_OP_MOE) {
+      TcMoePlan t;
+      if (o.T < 1 || o.T > kMaxM || o.k < 1 || o.k > 16 ||
+          !plan_tc_moe(o.T, o.k, o.experts.num_experts, o.experts.hidden, o.experts.inter, sms, &t))
+        return 0;
+      b = t.ws_bytes;
+    } else {
+      return 0;
+    }
+    if (b > need) need = b;
+  }
+  return need;
+}
+
+int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t workspace_bytes,
+                         nvfp4_program** program) {
+  if (!program) return fail(NVFP4_ERR_INVALID, "program is NULL");
+  *program = nullptr;
+  if (!ops || n_ops < 1) return fail(NVFP4_ERR_INVALID, "no ops");
+  int rc;
+  // host-side checks of every op first, then the device
+  for (int i = 0; i < n_ops; ++i) {
+    const nvfp4_op& o = ops[i];
+    if (o.kind == NVFP4_OP_GEMM)
+      rc = check_gemm(o.A, o.lda, o.M, &o.W, o.C, o.ldc);
+    else if (o.kind == NVFP4_OP_MOE)
+      rc = check_moe(o.x, o.ldx, o.T, o.topk_ids, o.topk_w, o.k, &o.experts,
+                     o.shared.num_experts ? &o.shared : nullptr, o.out, o.ldo);
+    else
+      rc = fail(NVFP4_ERR_INVALID, "op %d: unknown kind %d", i, o.kind);
+    if (rc) return rc;
+  }
+  int sms = 0;
+  if ((rc = current_device(&sms))) return rc;
+  if ((rc = get_encoder())) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  std::vector<TcOp> table;
+  size_t x_bytes = 0, need = kWsScratch;
+  int sched_bytes = 0, n_gemm = 0, n_moe = 0;
+  for (int i = 0; i < n_ops; ++i) {
+    const nvfp4_op& o = ops[i];
+    if (o.flags & ~static_cast<uint32_t>(NVFP4_FLAG_RMS_INPUT | NVFP4_FLAG_NO_PDL |
+                                         NVFP4_FLAG_IDS_READY))
+      return fail(NVFP4_ERR_INVALID, "op %d: unsupported flags 0x%x", i, o.flags);
+    if (o.kind == NVFP4_OP_GEMM) {
+      if ((rc = check_gemm(o.A, o.lda, o.M, &o.W, o.C, o.ldc))) return rc;
+      TcDensePlan p;
+      if (!plan_tc_dense(o.M, o.W.n, o.W.k, sms, &p))
+        return fail(NVFP4_ERR_SHAPE, "op %d: N=%d, K=%d: no feasible plan", i, o.W.n, o.W.k);
+      TcOp op;
+      if ((rc = tc_dense_op(o.A, o.lda, o.M, &o.W, o.C, o.ldc, o.argmax_out, o.flags, ws, p, &op)))
+        return rc;
+      table.push_back(op);
+      x_bytes = std::max(x_bytes, static_cast<size_t>(p.npad) * p.win_k * 2);
+      need = std::max(need, p.ws_bytes);
+      ++n_gemm;
+    } else if (o.kind == NVFP4_OP_MOE) {
+      const nvfp4_expert_stack* sh = o.shared.num_experts ? &o.shared : nullptr;
+      if ((rc = check_moe(o.x, o.ldx, o.T, o.topk_ids, o.topk_w, o.k, &o.experts, sh, o.out,
+                          o.ldo)))
+        return rc;
+      const int E = o.experts.num_experts, H = o.experts.hidden, I = o.experts.inter;
+      TcMoePlan p;
+      if (!plan_tc_moe(o.T, o.k, E, H, I, sms, &p))
+        return fail(NVFP4_ERR_SHAPE, "op %d: T=%d, H=%d, E=%d: no feasible plan", i, o.T, H, E);
+      TcOp gu, dn;
+      if ((rc = tc_moe_ops(o.x, o.ldx, o.T, o.topk_ids, o.topk_w, o.k, &o.experts, sh, o.out,
+                           o.ldo, o.flags | NVFP4_FLAG_IDS_READY, ws, p, &gu, &dn)))
+        return rc;
+      table.push_back(gu);
+      table.push_back(dn);
+      x_bytes = std::max(x_bytes, static_cast<size_t>(p.npad) * std::max(H, I) * 2);
+      sched_bytes = std::max(sched_bytes, p.sched_bytes);
+      need = std::max(need, p.ws_bytes);
+      ++n_moe;
+    } else {
+      return fail(NVFP4_ERR_INVALID, "op %d: unknown kind %d", i, o.kind);
+    }
+  }
+  const int n = static_cast<int>(table.size());
+  if (n > kTcMaxOps) return fail(NVFP4_ERR_SHAPE, "program of %d kernel ops > %d", n, kTcMaxOps);
+  if (!workspace || workspace_bytes < need)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+  table[0].wait_prev = 0;
+  auto* pg = new (std::nothrow) nvfp4_program();
+  if (!pg) return fail(NVFP4_ERR_INVALID, "out of host memory");
+  memset(&pg->params, 0, sizeof(pg->params));
+  if (!tc_program_layout(x_bytes, sched_bytes, sched_bytes ? 2 : 1, &pg->params, &pg->smem)) {
+    delete pg;
+    return fail(NVFP4_ERR_SHAPE, "staged activations exceed shared memory");
+  }
+  tc_program_header(&pg->params, ws);
+  cudaError_t e = cudaMalloc(&pg->d_ops, sizeof(TcOp) * n);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(pg->d_ops, table.data(), sizeof(TcOp) * n, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    if (pg->d_ops) cudaFree(pg->d_ops);
+    delete pg;
+    return cuda_fail(e, "program table");
+  }
+  cudaGetDevice(&pg->device);
+  pg->params.ops = pg->d_ops;
+  pg->params.n_ops = n;
+  pg->grid = sms;
+  char buf[256];
+  snprintf(buf, sizeof(buf),
+           "stream_tc_kernel program ops=%d (gemm=%d moe=%d) grid=%d stages=%d smem=%zu "
+           "sched_slots=%d cooperative=1",
+           n, n_gemm, n_moe, pg->grid, pg->params.n_stages, pg->smem, pg->params.sched_slots);
+  pg->desc = buf;
+  *program = pg;
+  return NVFP4_OK;
+}
+
+int nvfp4_program_launch(const nvfp4_program* program, nvfp4_stream_t stream) {
+  if (!program) return fail(NVFP4_ERR_INVALID, "program is NULL");
+  int dev = -1;
+  cudaGetDevice(&dev);
+  if (dev != program->device)
+    return fail(NVFP4_ERR_INVALID, "program was created on device %d, current is %d",
+                program->device, dev);
+  cudaError_t e = launch_tc(program->params, program->grid, program->smem,
+                            reinterpret_cast<cudaStream_t>(stream), false, true);
+  if (e != cudaSuccess) return cuda_fail(e, "stream_tc_kernel program launch");
+  g_dispatch = program->desc;
+  return NVFP4_OK;
+}
+
+int nvfp4_program_destroy(nvfp4_program* program) {
+  if (!program) return NVFP4_OK;
+  cudaError_t e = cudaFree(program->d_ops);
+  delete program;
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "cudaFree");
 }
 
 int nvfp4_read_device_status(void* workspace, uint32_t* flags, nvfp4_stream_t stream) {

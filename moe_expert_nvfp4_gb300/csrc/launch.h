@@ -74,18 +74,24 @@ struct MoeArgs {
 };
 
 // ---- tcgen05 streaming kernel (stream_tc.cu) ------------------------------
-// Shared memory (from a 1024-byte aligned base): barriers, misc, the
-// [32][128] f32 epilogue tile, the expert schedule, the staged activations,
-// then the weight ring (1024-aligned, n_stages x 18 KB).
+// One launch runs a program: a sequence of ops (dense GEMM, MoE gate_up, MoE
+// down), each reading what earlier ops wrote.  Shared memory (from a
+// 1024-byte aligned base): barriers, misc, the [32][128] f32 epilogue tile,
+// the expert-schedule slots, the staged activations, then the weight ring
+// (1024-aligned, n_stages x 18 KB); one layout for the whole program.
+constexpr int kTcTileRows = 128;                                // weight rows per tile
 constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;  // 18432
 constexpr int kTcMaxStages = 8;
 constexpr int kTcOffBars = 0;
 constexpr int kTcOffMisc = 256;
 constexpr int kTcOffEp = 768;
 constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17152
-constexpr int kTcThreads = 448;                          // producer, MMA, 8 decode, 4 epilogue warps
+constexpr int kTcThreads = 480;   // producer, MMA, 8 decode, 4 epilogue warps, scheduler warp
 constexpr int kTcColCntBase = 8192;                      // down combine counters
+constexpr int kTcDoneBase = 12288;                       // per-op completion counters
+constexpr int kTcMaxOps = kWsMaxCounters - kTcDoneBase - 1;
 constexpr int kTcMaxWinK = 2048;                         // activations staged per window
+constexpr int kTcInlineOps = 1;                          // ops passed by value in the launch
 
 enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2 };
 
@@ -114,20 +120,39 @@ struct TcArgs {
   float* y;
   // common
   int rms;
-  int win_k;        // staged activation window capacity (elements, multiple of 256)
-  int x_offset;     // smem offset of the staged activations
-  int ring_offset;  // smem offset of the weight ring (1024-aligned)
-  int n_stages;     // ring depth (3..kTcMaxStages)
-  int sched_offset; // smem offset of the expert schedule (MoE)
-  uint32_t* status;
+  int win_k;            // staged activation window capacity (elements, multiple of 256)
   uint32_t* tile_cnt;   // counters region
   uint32_t* argmax_cnt;
   float* partials;      // [grid][2][32][128]
   int2* am_part;        // [M][n_tiles]
 };
 
-cudaError_t launch_tc(int mode, const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
-                      cudaStream_t s, bool pdl);
+// One op of a program: its four tensor maps (dense: codes, scales of W, twice;
+// MoE: routed codes, routed scales, shared codes, shared scales) and its
+// arguments.
+struct TcOp {
+  CUtensorMap maps[4];
+  TcArgs a;
+  int mode;            // TcMode
+  int new_sched;       // MoE: build a new expert schedule from this op's ids
+  int last_sched_use;  // MoE: no later op uses the current schedule
+  int wait_prev;       // read inputs only after every CTA finished the previous op
+};
+
+struct TcProgram {
+  const TcOp* ops;     // device table of n_ops ops, or nullptr: inline_ops
+  int n_ops;
+  int x_offset, ring_offset, n_stages;
+  int sched_offset, sched_bytes, sched_slots;
+  uint32_t* status;
+  uint32_t* done;      // [n_ops + 1] completion counters (zero between launches)
+  TcOp inline_ops[kTcInlineOps];
+};
+
+// cooperative: the program's ops wait on each other across CTAs, so all CTAs
+// must be resident at once.
+cudaError_t launch_tc(const TcProgram& p, int grid, size_t smem, cudaStream_t s, bool pdl,
+                      bool cooperative);
 
 struct RouteArgs {
   const float* logits;

@@ -1,21 +1,24 @@
 // NVFP4 weight streaming on the 5th-generation tensor cores (tcgen05).
 //
-// One kernel, three epilogues: the dense skinny GEMM (C = A W^T, optional
-// argmax), the MoE gate_up projection (h = silu(gate) * up per routed pair)
-// and the MoE down projection with the weighted top-k combine.
+// One persistent kernel runs a program: a sequence of ops, each one of three
+// kinds -- the dense skinny GEMM (C = A W^T, optional argmax), the MoE
+// gate_up projection (h = silu(gate) * up per routed pair) and the MoE down
+// projection with the weighted top-k combine.  A single call of the C ABI is
+// a one-op program; a decode step is a program of a few hundred ops.
 //
 // Tile = 128 weight rows = the 128 lanes of tensor memory, built from four
 // independent 32-row TMA boxes (for gate_up: the gate and up boxes of two
 // 32-wide intermediate blocks, possibly of different experts).  Stage = one
 // tile x 256 K: 16 KB of 128B-swizzled E2M1 codes + 2 KB of E4M3 scales.
-// Work split: the (tile, stage) units of the launch are cut into gridDim.x
+// Work split: the (tile, stage) units of each op are cut into gridDim.x
 // equal contiguous ranges, one per CTA ("stream-K"); a tile split between
 // CTAs is reduced by the last CTA to finish it (atomic counter), adding the
 // per-CTA partials in CTA order, so results do not depend on timing.
 //
-// Warp roles (448 threads):
+// Warp roles (480 threads), each walking the whole program:
 //   warp 0       TMA producer: streams stages into a shared-memory ring of
-//                3..8 stages (full/empty mbarriers);
+//                3..8 stages (full/empty mbarriers), running ahead into the
+//                next ops' weights while the current op finishes;
 //   warp 1       allocates tensor memory; one thread issues tcgen05.mma:
 //                D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
 //                memory), 16 MMAs per stage, N = tokens rounded up to 16;
@@ -24,11 +27,15 @@
 //                6-9 the second.  E2M1 -> FP16 by the hardware convert, times
 //                the E4M3 block scale (exact in FP16), written to one of three
 //                tensor-memory A buffers with tcgen05.st.  They only stream.
-//   warps 10-13  epilogue: stage the activations (B) into shared memory as
-//                FP16 with a power-of-two shift per row and window, read the
-//                FP32 accumulator (two buffers) with tcgen05.ld, undo the
-//                shift, and run the stream-K reduction and the epilogue while
-//                the decode warps go on with the next tile.
+//   warps 10-13  epilogue: wait until every CTA finished the previous op
+//                (a completion counter per op), stage the activations (B)
+//                into shared memory as FP16 with a power-of-two shift per row
+//                and window, read the FP32 accumulator (two buffers) with
+//                tcgen05.ld, undo the shift, and run the stream-K reduction
+//                and the op's epilogue while the other roles go on with the
+//                next op;
+//   warp 14      builds the expert schedule of each MoE layer into one of
+//                two shared-memory slots.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
 // faster": "Skinny matrix multiplies" (split-K decode matmuls, 4-bit weights
@@ -53,13 +60,17 @@ constexpr int kDecWarps = 8;
 constexpr int kEpiWarps = 4;                   // one per tensor-memory lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiWarp0 = 2 + kDecWarps;       // warps 10..13
+constexpr int kSchedWarp = kEpiWarp0 + kEpiWarps;  // warp 14
+// arrivals that release a schedule slot: producer, MMA thread, 8 decode
+// warps, 4 epilogue warps
+constexpr int kSchedUsers = 2 + kDecWarps + kEpiWarps;
 constexpr int kABufs = 3;                      // A operand buffers in tensor memory
 constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
 constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384 and 416
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
-static_assert(kTcThreads == (2 + kDecWarps + kEpiWarps) * 32, "thread count");
+static_assert(kTcThreads == (3 + kDecWarps + kEpiWarps) * 32, "thread count");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -138,8 +149,7 @@ struct Kernel {
 
   __device__ __forceinline__ void tile_boxes(int tile, Box (&bx)[4]) const {
     if (MODE == kTcDense) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) bx[b] = Box{m0, m1, tile * kRows + b * kBox};
+      bx[0] = Box{m0, m1, tile * kRows};  // one 128-row box
     } else if (MODE == kTcGateUp) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -154,9 +164,7 @@ struct Kernel {
     } else {
       const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
       const bool sh = (e == a.E);
-      const int base = (sh ? 0 : e * a.H) + nt * kRows;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) bx[b] = Box{sh ? m2 : m0, sh ? m3 : m1, base + b * kBox};
+      bx[0] = Box{sh ? m2 : m0, sh ? m3 : m1, (sh ? 0 : e * a.H) + nt * kRows};  // one 128-row box
     }
   }
 
@@ -283,508 +291,785 @@ __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, 
   }
 }
 
+// ------------------------------------------------------------ CTA context
+
+// Shared-memory objects and program-wide constants of one CTA, derived on
+// use from the aligned shared-memory base and the launch parameters (nothing
+// to keep in registers).
+struct Cta {
+  uint8_t* base;
+  const TcProgram& prog;
+  uint32_t tmem;
+  __device__ __forceinline__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(base + kTcOffBars); }
+  __device__ __forceinline__ uint64_t* ring_full_at(int s) const { return bars() + s; }
+  __device__ __forceinline__ uint64_t* ring_empty_at(int s) const { return bars() + kTcMaxStages + s; }
+  __device__ __forceinline__ uint64_t* a_full_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + b; }
+  __device__ __forceinline__ uint64_t* a_empty_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + kABufs + b; }
+  __device__ __forceinline__ uint64_t* d_full_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + b; }
+  __device__ __forceinline__ uint64_t* d_empty_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 2 + b; }
+  __device__ __forceinline__ uint64_t* x_full() const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 4; }
+  __device__ __forceinline__ uint64_t* mma_done() const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 5; }
+  __device__ __forceinline__ uint64_t* sched_full_at(int b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 6 + b; }
+  __device__ __forceinline__ uint64_t* sched_empty_at(int b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 8 + b; }
+  __device__ __forceinline__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + kTcOffMisc); }
+  __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 4); }
+  __device__ __forceinline__ volatile int* bcast() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 8); }
+  __device__ __forceinline__ int* sig() const { return reinterpret_cast<int*>(base + kTcOffMisc + 64); }
+  __device__ __forceinline__ float* rms() const { return reinterpret_cast<float*>(base + kTcOffMisc + 192); }
+  __device__ __forceinline__ float* ep() const { return reinterpret_cast<float*>(base + kTcOffEp); }
+  __device__ __forceinline__ uint8_t* xs() const { return base + prog.x_offset; }
+  __device__ __forceinline__ uint8_t* ring() const { return base + prog.ring_offset; }
+  __device__ __forceinline__ uint8_t* sched() const { return base + prog.sched_offset; }
+  __device__ __forceinline__ int n_stages() const { return prog.n_stages; }
+  __device__ __forceinline__ int sched_bytes() const { return prog.sched_bytes; }
+  __device__ __forceinline__ int sched_slots() const { return prog.sched_slots; }
+  __device__ __forceinline__ uint32_t* status() const { return prog.status; }
+  __device__ __forceinline__ bool aborted() const { return *abort_flag() != 0; }
+};
+static_assert(2 * kTcMaxStages + 2 * kABufs + 10 <= kTcOffMisc / 8, "barrier area");
+
+__device__ __forceinline__ const TcOp& op_at(const TcProgram& p, int i) {
+  return p.ops ? p.ops[i] : p.inline_ops[i];
+}
+
+// The expert schedule an MoE op uses: every role keeps the same count of
+// schedules started, so all of them agree on the slot.  A slot is rebuilt
+// only after all kSchedUsers arrivals released its previous schedule.
+struct SchedCursor {
+  int idx = -1;
+  __device__ __forceinline__ Sched acquire(const Cta& c, const TcOp& op) {
+    if (op.new_sched) {
+      ++idx;
+      wait_bar(c.sched_full_at(idx % c.sched_slots()), (idx / c.sched_slots()) & 1, c.status(),
+               c.abort_flag());
+    }
+    const int slot = idx < 0 ? 0 : idx % c.sched_slots();
+    return sched_layout(c.sched() + slot * c.sched_bytes(), op.a.E, op.a.T * op.a.k);
+  }
+  // arrive: this thread speaks for its warp (or is the role's only thread)
+  __device__ __forceinline__ void release(const Cta& c, const TcOp& op, bool arrive) {
+    if (op.last_sched_use && arrive && idx >= 0) mbar_arrive(c.sched_empty_at(idx % c.sched_slots()));
+  }
+};
+
+// Units of an op and the contiguous range [u0, u1) of this CTA.  After an
+// abort the schedule may be incomplete: no units then.
 template <int MODE>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    stream_tc_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
-                     const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
-                     const TcArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcOffBars);
-  uint64_t* ring_full = bars;                   // [kTcMaxStages]
-  uint64_t* ring_empty = bars + kTcMaxStages;   // [kTcMaxStages]
-  uint64_t* a_full = bars + 2 * kTcMaxStages;   // [kABufs]
-  uint64_t* a_empty = a_full + kABufs;          // [kABufs]
-  uint64_t* d_full = a_empty + kABufs;          // [2]
-  uint64_t* d_empty = d_full + 2;               // [2]
-  uint64_t* x_full = d_empty + 2;
-  uint64_t* mma_done = x_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kTcOffMisc);
-  volatile int* abort_flag = reinterpret_cast<int*>(smem + kTcOffMisc + 4);
-  volatile int* bcast = reinterpret_cast<int*>(smem + kTcOffMisc + 8);
-  int* sig = reinterpret_cast<int*>(smem + kTcOffMisc + 64);
-  float* rms = reinterpret_cast<float*>(smem + kTcOffMisc + 192);
-  float* ep = reinterpret_cast<float*>(smem + kTcOffEp);
-  uint8_t* xs = smem + a.x_offset;
-  uint8_t* ring = smem + a.ring_offset;
-  const int n_stages = a.n_stages;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < n_stages; ++s) {
-      mbar_init(&ring_full[s], 1);
-      mbar_init(&ring_empty[s], kDecWarps);
-    }
-    for (int b = 0; b < kABufs; ++b) {
-      mbar_init(&a_full[b], kDecWarps);
-      mbar_init(&a_empty[b], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&d_full[b], 1);
-      mbar_init(&d_empty[b], kEpiWarps);
-    }
-    mbar_init(x_full, kEpiWarps);
-    mbar_init(mma_done, 1);
-    fence_mbarrier_init();
-    *abort_flag = 0;
-  }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
-
-  Sched sc{};
-  if (MODE != kTcDense) {
-    // gate_up may read ids written before the previous kernel started
-    // (NVFP4_FLAG_IDS_READY) before its dependency wait; down always can:
-    // the gate_up grid before it read them after its own wait.
-    if (MODE == kTcGateUp && !a.ids_ready) pdl_wait();
-    sc = sched_layout(smem + a.sched_offset, a.E, a.T * a.k);
-    build_schedule(a.ids, a.T, a.k, a.E, a.has_shared, sc, a.status);
-  }
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-
+__device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, const Cta& c,
+                                          long& u0, long& u1) {
   Work wk{};
   if (MODE == kTcDense) {
     wk.n_tiles = (a.N + kRows - 1) / kRows;
     wk.nkb = a.K / kSK;
-  } else if (MODE == kTcGateUp) {
-    wk.per_e = a.I / kBox;
-    wk.pb_count = *sc.n_active * wk.per_e;
-    wk.n_tiles = (wk.pb_count + 1) / 2;
-    wk.nkb = a.H / kSK;
   } else {
-    wk.per_e = a.H / kRows;
-    wk.n_tiles = *sc.n_active * wk.per_e;
-    wk.nkb = a.I / kSK;
+    const int na = c.aborted() ? 0 : min(max(*sc.n_active, 0), a.E + 1);
+    if (MODE == kTcGateUp) {
+      wk.per_e = a.I / kBox;
+      wk.pb_count = na * wk.per_e;
+      wk.n_tiles = (wk.pb_count + 1) / 2;
+      wk.nkb = a.H / kSK;
+    } else {
+      wk.per_e = a.H / kRows;
+      wk.n_tiles = na * wk.per_e;
+      wk.nkb = a.I / kSK;
+    }
   }
   wk.U = static_cast<long>(wk.n_tiles) * wk.nkb;
   wk.G = static_cast<int>(min(static_cast<long>(gridDim.x), wk.U));
   const int b = blockIdx.x;
-  const bool active_cta = b < wk.G;
-  const long u0 = active_cta ? wk.begin(b) : 0, u1 = active_cta ? wk.begin(b + 1) : 0;
-  const Kernel<MODE> kk{a, sc, wk, &m0, &m1, &m2, &m3};
+  const bool active = b < wk.G && !c.aborted();
+  u0 = active ? wk.begin(b) : 0;
+  u1 = active ? wk.begin(b + 1) : 0;
+  return wk;
+}
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer
-    if (lane == 0 && u0 < u1) {
-      prefetch_tensormap(&m0);
-      prefetch_tensormap(&m1);
-      const uint64_t pol = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      long issued = 0;
-      for (long u = u0; u < u1; ++u) {
-        Box bx[4];
-        kk.tile_boxes(static_cast<int>(u / wk.nkb), bx);
-        const int kb = static_cast<int>(u % wk.nkb);
-        if (*abort_flag || !wait_or_abort(&ring_empty[stage], phase ^ 1u, a.status, abort_flag))
-          break;
-        mbar_arrive_expect_tx(&ring_full[stage], kTcStageBytes);
-        uint8_t* st = ring + stage * kTcStageBytes;
+// Wait until *ctr reaches target (every CTA finished an op), bounded; gives
+// up at once if another CTA already timed out.
+__device__ __forceinline__ void grid_wait(const uint32_t* ctr, uint32_t target, uint32_t* status,
+                                          volatile int* abort_flag) {
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) break;
+    if (*abort_flag) return;
+    if (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) {
+      *abort_flag = 1;
+      return;
+    }
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      *abort_flag = 1;
+      return;
+    }
+    __nanosleep(64);
+  }
+  __threadfence();
+}
+
+// Tensor maps of the device op table were written by the host before the
+// launch; order them for the tensor-map proxy before the first copy.
+__device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
+}
+
+// ------------------------------------------------------------ roles, per op
+
+// The producer warp, one op.  Converged like the MMA warp: lane 0 waits for
+// a free ring stage, one elected lane issues the copies.  Dense and down
+// tiles are 128 consecutive weight rows: one box of codes and one of scales
+// per stage; a gate_up tile is four 32-row boxes.
+template <int MODE>
+__device__ __forceinline__ void produce_op(const Cta& c, const TcOp& op, bool table, int lane,
+                                           SchedCursor& cur, int& stage, uint32_t& phase,
+                                           long& issued, uint64_t pol) {
+  const TcArgs& a = op.a;
+  Sched sc{};
+  if (MODE != kTcDense) sc = cur.acquire(c, op);
+  long u0, u1;
+  const Work wk = make_work<MODE>(a, sc, c, u0, u1);
+  const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
+  if (u0 < u1 && tc::elect_one()) {
+    const int nm = MODE == kTcDense ? 2 : 4;
+    for (int m = 0; m < nm; ++m) {
+      if (table) acquire_tensormap(&op.maps[m]);
+      prefetch_tensormap(&op.maps[m]);
+    }
+  }
+  __syncwarp();
+  uint8_t* const ring = c.ring();
+  const int n_stages = c.n_stages();
+  int cur_tile = -1;
+  Box bx[4];
+  for (long u = u0; u < u1; ++u) {
+    const int tile = static_cast<int>(u / wk.nkb);
+    const int kb = static_cast<int>(u - static_cast<long>(tile) * wk.nkb);
+    if (tile != cur_tile) {
+      kk.tile_boxes(tile, bx);
+      cur_tile = tile;
+    }
+    bool ok = true;
+    if (lane == 0)
+      ok = !c.aborted() && wait_or_abort(c.ring_empty_at(stage), phase ^ 1u, c.status(), c.abort_flag());
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    if (tc::elect_one()) {
+      uint64_t* full = c.ring_full_at(stage);
+      mbar_arrive_expect_tx(full, kTcStageBytes);
+      uint8_t* st = ring + stage * kTcStageBytes;
+      if (MODE == kTcGateUp) {
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
-          tma_load_2d(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row,
-                      &ring_full[stage], pol);
+          tma_load_2d(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row, full, pol);
           tma_load_2d(st + kCodeBytes + bb * (kRows * kSK / 16 / 4), bx[bb].ms, kb * (kSK / 16),
-                      bx[bb].row, &ring_full[stage], pol);
+                      bx[bb].row, full, pol);
         }
-        ++issued;
-        if (++stage == n_stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      } else {
+        tma_load_2d(st, bx[0].mc, kb * (kSK / 2), bx[0].row, full, pol);
+        tma_load_2d(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, full, pol);
       }
-      // wait for the TMA writes still in flight (bounded, ignores aborts)
-      const int n = issued < n_stages ? static_cast<int>(issued) : n_stages;
-      for (int i = 0; i < n; ++i) {
-        if (stage == 0) {
-          stage = n_stages - 1;
-          phase ^= 1u;
-        } else {
-          --stage;
-        }
-        mbar_wait(&ring_full[stage], phase, a.status);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0 && u0 < u1) {
-      XState xst;
-      uint32_t acount = 0, dcount = 0, xcount = 0;
-      const uint32_t xs_addr = smem_u32(xs);
-      const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
-      for (long u = u0; u < u1;) {
-        const int tile = static_cast<int>(u / wk.nkb);
-        const int kbs = static_cast<int>(u % wk.nkb);
-        const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
-        const int key = kk.b_key(tile);
-        const int nr = kk.b_rows(tile);
-        const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32);
-        for (int w0 = kbs; w0 < kbe;) {
-          const int w1 = window_end(kk, w0, kbe);
-          if (!xst.covers(key, w0, w1)) {
-            restage_range(kk, w0, w1, xst.k0, xst.k1);
-            xst.key = key;
-            wait_bar(x_full, xcount & 1u, a.status, abort_flag);
-            ++xcount;
-          }
-          const uint32_t db = dcount & 1u;
-          wait_bar(&d_empty[db], ((dcount >> 1) & 1u) ^ 1u, a.status, abort_flag);
-          const uint32_t d_t = tmem + kDCol + 32u * db;
-          for (int kb = w0; kb < w1; ++kb) {
-            const uint32_t ab = acount % kABufs;
-            wait_bar(&a_full[ab], (acount / kABufs) & 1u, a.status, abort_flag);
-            tc::fence_after_sync();
-            if (!*abort_flag) {
-              const uint32_t a_t = tmem + kACols * ab;
-              const uint32_t bbase = xs_addr + static_cast<uint32_t>(kb - xst.k0) * 4096u;
-#pragma unroll
-              for (int j = 0; j < kSK / 16; ++j)
-                tc::mma_f16_ts(d_t, a_t + 8 * j, tc::smem_desc(bbase + 256u * j, sbo), idesc,
-                               (kb > w0 || j > 0) ? 1u : 0u);
-            }
-            tc::commit(&a_empty[ab]);
-            ++acount;
-          }
-          tc::commit(&d_full[db]);
-          ++dcount;
-          w0 = w1;
-        }
-        u += kbe - kbs;
-      }
-      // every MMA has completed before tensor memory is released
-      tc::commit(mma_done);
-      mbar_wait(mma_done, 0, a.status);
     }
     __syncwarp();
-  } else if (warp < kEpiWarp0) {
-    // ------------------------------------------------ decode warps
-    const int dw = warp - 2, q = warp & 3, half = dw >> 2;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    uint32_t acount = 0;
-    int rstage = 0;
-    uint32_t rphase = 0;
-    for (long u = u0; u < u1; ++u) {
-      wait_bar(&ring_full[rstage], rphase, a.status, abort_flag);
-      const uint8_t* st = ring + rstage * kTcStageBytes;
-      const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
-      // all shared-memory reads of this stage first (their latency overlaps)
-      const uint2 sb =
-          *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
-      uint4 cw[4];
-#pragma unroll
-      for (int ci = 0; ci < 4; ++ci)
-        cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ring_empty[rstage]);
-      const uint32_t ab = acount % kABufs;
-      wait_bar(&a_empty[ab], ((acount / kABufs) & 1u) ^ 1u, a.status, abort_flag);
-      tc::fence_after_sync();
-      const uint32_t sbw[2] = {sb.x, sb.y};
-#pragma unroll
-      for (int ci = 0; ci < 4; ++ci) {
-        const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
-        const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
-        const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
-        const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
-        uint32_t v[16];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-          const uint32_t sv = wi < 2 ? s_lo : s_hi;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
-        }
-        tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
+    ++issued;
+    if (++stage == n_stages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+}
+
+// The MMA warp, one op.  The warp stays converged: lane 0 waits on the
+// barriers, then one elected lane issues the stage's 16 MMAs and the commits
+// (a tcgen05.mma issued from a divergent single-lane loop is several times
+// slower).
+template <int MODE>
+__device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor& cur, int lane,
+                                       uint32_t& acount, uint32_t& dcount, uint32_t& xcount) {
+  const TcArgs& a = op.a;
+  Sched sc{};
+  if (MODE != kTcDense) sc = cur.acquire(c, op);
+  long u0, u1;
+  const Work wk = make_work<MODE>(a, sc, c, u0, u1);
+  const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
+  XState xst;
+  const uint32_t xs_addr = smem_u32(c.xs());
+  const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
+  for (long u = u0; u < u1;) {
+    if (__any_sync(0xffffffffu, c.aborted())) break;
+    const int tile = static_cast<int>(u / wk.nkb);
+    const int kbs = static_cast<int>(u % wk.nkb);
+    const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+    const int key = kk.b_key(tile);
+    const int nr = kk.b_rows(tile);
+    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32);
+    for (int w0 = kbs; w0 < kbe;) {
+      const int w1 = window_end(kk, w0, kbe);
+      if (!xst.covers(key, w0, w1)) {
+        restage_range(kk, w0, w1, xst.k0, xst.k1);
+        xst.key = key;
+        if (lane == 0) wait_bar(c.x_full(), xcount & 1u, c.status(), c.abort_flag());
+        __syncwarp();
+        ++xcount;
       }
-      tc::wait_st();
+      const uint32_t db = dcount & 1u;
+      if (lane == 0) wait_bar(c.d_empty_at(db), ((dcount >> 1) & 1u) ^ 1u, c.status(), c.abort_flag());
+      __syncwarp();
+      const uint32_t d_t = c.tmem + kDCol + 32u * db;
+      for (int kb = w0; kb < w1; ++kb) {
+        const uint32_t ab = acount % kABufs;
+        if (lane == 0) wait_bar(c.a_full_at(ab), (acount / kABufs) & 1u, c.status(), c.abort_flag());
+        __syncwarp();
+        tc::fence_after_sync();
+        const bool run = !__any_sync(0xffffffffu, c.aborted());
+        if (tc::elect_one()) {
+          if (run) {
+            const uint32_t a_t = c.tmem + kACols * ab;
+            const uint64_t b0 =
+                tc::smem_desc(xs_addr + static_cast<uint32_t>(kb - xst.k0) * 4096u, sbo);
+            // K step j: A columns + 8 j, B start address + 256 j bytes (+16 j in
+            // the descriptor's address field, which cannot carry: < 256 KB)
+            tc::mma_f16_ts(d_t, a_t, b0, idesc, kb > w0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 1; j < kSK / 16; ++j)
+              tc::mma_f16_ts(d_t, a_t + 8 * j, b0 + static_cast<uint64_t>(16 * j), idesc, 1u);
+          }
+          tc::commit(c.a_empty_at(ab));
+        }
+        __syncwarp();
+        ++acount;
+      }
+      if (tc::elect_one()) tc::commit(c.d_full_at(db));
+      __syncwarp();
+      ++dcount;
+      w0 = w1;
+    }
+    u += kbe - kbs;
+  }
+  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+}
+
+template <int MODE>
+__device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCursor& cur,
+                                          int warp, int lane, uint32_t& acount, int& rstage,
+                                          uint32_t& rphase) {
+  Sched sc{};
+  if (MODE != kTcDense) sc = cur.acquire(c, op);
+  long u0, u1;
+  make_work<MODE>(op.a, sc, c, u0, u1);
+  const int dw = warp - 2, q = warp & 3, half = dw >> 2;
+  const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
+  for (long u = u0; u < u1; ++u) {
+    if (c.aborted()) break;
+    wait_bar(c.ring_full_at(rstage), rphase, c.status(), c.abort_flag());
+    const uint8_t* st = c.ring() + rstage * kTcStageBytes;
+    const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
+    // all shared-memory reads of this stage first (their latency overlaps)
+    const uint2 sb =
+        *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
+    uint4 cw[4];
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci)
+      cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.ring_empty_at(rstage));
+    const uint32_t ab = acount % kABufs;
+    wait_bar(c.a_empty_at(ab), ((acount / kABufs) & 1u) ^ 1u, c.status(), c.abort_flag());
+    tc::fence_after_sync();
+    const uint32_t sbw[2] = {sb.x, sb.y};
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+      const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
+      const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
+      const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
+      const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
+      uint32_t v[16];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+        const uint32_t sv = wi < 2 ? s_lo : s_hi;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
+      }
+      tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
+    }
+    tc::wait_st();
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.a_full_at(ab));
+    ++acount;
+    if (++rstage == c.n_stages()) {
+      rstage = 0;
+      rphase ^= 1u;
+    }
+  }
+  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+}
+
+// Epilogue warps, one op: activation staging, accumulator folds, stream-K
+// reduction and the op's epilogue.
+// (Not inlined: each mode gets its own register allocation.)
+template <int MODE>
+__device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
+                                         int ew, int lane, uint32_t& dcount) {
+  const TcArgs& a = op.a;
+  const int q = (kEpiWarp0 + ew) & 3;
+  const int etid = ew * 32 + lane;
+  const int r = 32 * q + lane;  // tile row = tensor-memory lane
+  const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
+  const int b = blockIdx.x;
+  Sched sc{};
+  if (MODE != kTcDense) sc = cur.acquire(c, op);
+  long u0, u1;
+  const Work wk = make_work<MODE>(a, sc, c, u0, u1);
+  const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
+  int* sig = c.sig();
+  float* rms = c.rms();
+  float* ep = c.ep();
+  volatile int* bcast = c.bcast();
+
+  if (MODE == kTcDown && wk.n_tiles == 0 && b == 0 && !c.aborted()) {
+    // nothing routed and no shared expert: the layer output is zero
+    for (int i = etid; i < a.T * a.H; i += kEpiThreads)
+      a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
+  }
+  // dense: the RMS factor of each row over the whole K
+  if (MODE == kTcDense && a.rms && u0 < u1) {
+    for (int m = ew; m < a.M; m += kEpiWarps) {
+      float ss = 0.0f;
+      const __nv_bfloat16* row = a.A + m * a.lda;
+      for (int v = lane; v < a.K / 8; v += 32) {
+        const uint4 uu = *reinterpret_cast<const uint4*>(row + v * 8);
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(static_cast<float>(e[i]), static_cast<float>(e[i]), ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+    }
+  }
+  const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
+  XState xst;
+  const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
+  const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
+
+  for (long u = u0; u < u1;) {
+    if (c.aborted()) break;
+    const int tile = static_cast<int>(u / wk.nkb);
+    const int kbs = static_cast<int>(u % wk.nkb);
+    const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+    const int key = kk.b_key(tile);
+    const int nr = kk.b_rows(tile);
+    const int npad = nr <= 16 ? 16 : 32;
+    float tot[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
+
+    for (int w0 = kbs; w0 < kbe;) {
+      const int w1 = window_end(kk, w0, kbe);
+      if (!xst.covers(key, w0, w1)) {
+        restage_range(kk, w0, w1, xst.k0, xst.k1);
+        xst.key = key;
+        // the previous window's MMAs are complete (its accumulator was read)
+        const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
+        if (MODE == kTcDown) {
+          const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
+          const int I = a.I;
+          stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, npad,
+                         kbeg, klen, c.xs(), sbo, sig, nullptr, ew, lane, kEpiWarps);
+        } else {
+          const __nv_bfloat16* base = (MODE == kTcDense) ? a.A : a.x;
+          const int64_t ld = (MODE == kTcDense) ? a.lda : a.ldx;
+          stage_b<__nv_bfloat16>([&](int n) { return base + n * ld; }, nr, npad, kbeg, klen,
+                                 c.xs(), sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr,
+                                 ew, lane, kEpiWarps);
+        }
+        fence_proxy_async_smem();
+        esync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.x_full());
+      }
+      // ---- fold the window's accumulator into the segment total
+      const uint32_t db = dcount & 1u;
+      wait_bar(c.d_full_at(db), (dcount >> 1) & 1u, c.status(), c.abort_flag());
+      tc::fence_after_sync();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dv[16];
+        tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * h, dv);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (16 * h + j < nr) tot[16 * h + j] += scale_pow2(__uint_as_float(dv[j]), -sig[16 * h + j]);
+      }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[ab]);
-      ++acount;
-      if (++rstage == n_stages) {
-        rstage = 0;
-        rphase ^= 1u;
-      }
+      if (lane == 0) mbar_arrive(c.d_empty_at(db));
+      ++dcount;
+      w0 = w1;
     }
-  } else {
-    // ------------------------------------------------ epilogue warps
-    const int ew = warp - kEpiWarp0, q = warp & 3;
-    const int etid = threadIdx.x - kEpiWarp0 * 32;
-    const int r = 32 * q + lane;  // tile row = tensor-memory lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    if (MODE == kTcDense || MODE == kTcDown || a.ids_ready) pdl_wait();
-    pdl_launch_dependents();
+    u += kbe - kbs;
 
-    if (MODE == kTcDown && wk.n_tiles == 0 && b == 0) {
-      // nothing routed and no shared expert: the layer output is zero
-      for (int i = etid; i < a.T * a.H; i += kEpiThreads)
-        a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
-    }
-    // dense: the RMS factor of each row over the whole K
-    if (MODE == kTcDense && a.rms) {
-      for (int m = ew; m < a.M; m += kEpiWarps) {
-        float ss = 0.0f;
-        const __nv_bfloat16* row = a.A + m * a.lda;
-        for (int v = lane; v < a.K / 8; v += 32) {
-          const uint4 uu = *reinterpret_cast<const uint4*>(row + v * 8);
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+    // ---- stream-K: a tile split between CTAs is reduced by its last CTA
+    if (!(kbs == 0 && kbe == wk.nkb)) {
+      const int slot = (tile == first_tile) ? 0 : 1;
+      float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ss = fmaf(static_cast<float>(e[i]), static_cast<float>(e[i]), ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+      for (int j = 0; j < 32; ++j)
+        if (j < nr) part[j * kRows + r] = tot[j];
+      esync();
+      const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
+      const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
+      if (etid == 0) {
+        __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
+        const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
+        *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
+        if (*bcast) __threadfence();
       }
-    }
-    const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
-    XState xst;
-    uint32_t dcount = 0;
-    const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
-    const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
-
-    for (long u = u0; u < u1;) {
-      const int tile = static_cast<int>(u / wk.nkb);
-      const int kbs = static_cast<int>(u % wk.nkb);
-      const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
-      const int key = kk.b_key(tile);
-      const int nr = kk.b_rows(tile);
-      const int npad = nr <= 16 ? 16 : 32;
-      float tot[32];
+      esync();
+      if (!*bcast) continue;  // uniform across the epilogue warps
 #pragma unroll
       for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
-
-      for (int w0 = kbs; w0 < kbe;) {
-        const int w1 = window_end(kk, w0, kbe);
-        if (!xst.covers(key, w0, w1)) {
-          restage_range(kk, w0, w1, xst.k0, xst.k1);
-          xst.key = key;
-          // the previous window's MMAs are complete (its accumulator was read)
-          const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
-          if (MODE == kTcDown) {
-            const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
-            const int I = a.I;
-            stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, npad,
-                           kbeg, klen, xs, sbo, sig, nullptr, ew, lane, kEpiWarps);
-          } else {
-            const __nv_bfloat16* base = (MODE == kTcDense) ? a.A : a.x;
-            const int64_t ld = (MODE == kTcDense) ? a.lda : a.ldx;
-            stage_b<__nv_bfloat16>([&](int n) { return base + n * ld; }, nr, npad, kbeg, klen, xs,
-                                   sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr, ew,
-                                   lane, kEpiWarps);
-          }
-          fence_proxy_async_smem();
-          esync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(x_full);
-        }
-        // ---- fold the window's accumulator into the segment total
-        const uint32_t db = dcount & 1u;
-        wait_bar(&d_full[db], (dcount >> 1) & 1u, a.status, abort_flag);
-        tc::fence_after_sync();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t dv[16];
-          tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * h, dv);
-          tc::wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (16 * h + j < nr) tot[16 * h + j] += scale_pow2(__uint_as_float(dv[j]), -sig[16 * h + j]);
-        }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&d_empty[db]);
-        ++dcount;
-        w0 = w1;
-      }
-      u += kbe - kbs;
-
-      // ---- stream-K: a tile split between CTAs is reduced by its last CTA
-      if (!(kbs == 0 && kbe == wk.nkb)) {
-        const int slot = (tile == first_tile) ? 0 : 1;
-        float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
+      for (int bb = blo; bb <= bhi; ++bb) {
+        const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
+        const float* pp = a.partials + static_cast<size_t>(bb * 2 + sl) * (32 * kRows);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < nr) part[j * kRows + r] = tot[j];
-        esync();
-        const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
-        const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
-        if (etid == 0) {
-          __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
-          const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
-          *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
-          if (*bcast) __threadfence();
-        }
-        esync();
-        if (!*bcast) continue;  // uniform across the epilogue warps
-#pragma unroll
-        for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
-        for (int bb = blo; bb <= bhi; ++bb) {
-          const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
-          const float* pp = a.partials + static_cast<size_t>(bb * 2 + sl) * (32 * kRows);
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nr) tot[j] += __ldcg(pp + j * kRows + r);
-        }
-        if (etid == 0) a.tile_cnt[tile] = 0u;
+          if (j < nr) tot[j] += __ldcg(pp + j * kRows + r);
       }
+      if (etid == 0) a.tile_cnt[tile] = 0u;
+    }
 
-      // ---- epilogues
-      if (MODE == kTcDense) {
+    // ---- epilogues
+    if (MODE == kTcDense) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < a.M) ep[j * kRows + r] = tot[j] * gs * (a.rms ? rms[j] : 1.0f);
-        esync();
-        const int n0 = tile * kRows;
-        for (int m = ew; m < a.M; m += kEpiWarps) {
-          float bv = -FLT_MAX;
-          int bi = 0x7fffffff;
+      for (int j = 0; j < 32; ++j)
+        if (j < a.M) ep[j * kRows + r] = tot[j] * gs * (a.rms ? rms[j] : 1.0f);
+      esync();
+      const int n0 = tile * kRows;
+      for (int m = ew; m < a.M; m += kEpiWarps) {
+        float bv = -FLT_MAX;
+        int bi = 0x7fffffff;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int rr = 4 * lane + i, n = n0 + rr;
-            if (n < a.N) {
-              const __nv_bfloat16 o = __float2bfloat16_rn(ep[m * kRows + rr]);
-              a.C[m * a.ldc + n] = o;
-              const float ov = __bfloat162float(o);
-              if (am_better(ov, n, bv, bi)) {
-                bv = ov;
-                bi = n;
-              }
+        for (int i = 0; i < 4; ++i) {
+          const int rr = 4 * lane + i, n = n0 + rr;
+          if (n < a.N) {
+            const __nv_bfloat16 o = __float2bfloat16_rn(ep[m * kRows + rr]);
+            a.C[m * a.ldc + n] = o;
+            const float ov = __bfloat162float(o);
+            if (am_better(ov, n, bv, bi)) {
+              bv = ov;
+              bi = n;
             }
-          }
-          if (a.argmax_out) {
-            am_warp_reduce(bv, bi);
-            if (lane == 0) a.am_part[m * wk.n_tiles + tile] = make_int2(__float_as_int(bv), bi);
           }
         }
         if (a.argmax_out) {
-          esync();
-          if (etid == 0) {
-            __threadfence();
-            const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
-            *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
-            if (*bcast) __threadfence();
-          }
-          esync();
-          if (*bcast) {
-            for (int m = ew; m < a.M; m += kEpiWarps) {
-              float bv = -FLT_MAX;
-              int bi = 0x7fffffff;
-              for (int j = lane; j < wk.n_tiles; j += 32) {
-                const int2 pr = __ldcg(a.am_part + m * wk.n_tiles + j);
-                const float v = __int_as_float(pr.x);
-                if (pr.y != 0x7fffffff && am_better(v, pr.y, bv, bi)) {
-                  bv = v;
-                  bi = pr.y;
-                }
-              }
-              am_warp_reduce(bv, bi);
-              if (lane == 0) a.argmax_out[m] = bi;
-            }
-            if (etid == 0) *a.argmax_cnt = 0u;
-          }
+          am_warp_reduce(bv, bi);
+          if (lane == 0) a.am_part[m * wk.n_tiles + tile] = make_int2(__float_as_int(bv), bi);
         }
-      } else if (MODE == kTcGateUp) {
-        // rows 0-31 gate and 32-63 up of pair-box 2*tile; 64-127 likewise
-        // for pair-box 2*tile+1 (absent when the count is odd)
-        if (q & 1) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ep[j * kRows + r] = tot[j];
-        }
+      }
+      if (a.argmax_out) {
         esync();
-        const int pb = 2 * tile + (q >> 1);
-        if (!(q & 1) && pb < wk.pb_count) {
-          const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
-          const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
-          const int cnt = sc.cnt[e], off = sc.off[e];
-          for (int qq = 0; qq < cnt; ++qq) {
-            const int p = off + qq;
-            const int t = sc.pair_tok[p];
-            const float f = a.rms ? g * rms[t] : g;
-            float gt = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j == t) gt = tot[j];
-            gt *= f;
-            const float up = ep[t * kRows + r + 32] * f;
-            a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
-          }
-        }
-      } else {
-        const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
-        const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
-        const int cnt = sc.cnt[e], off = sc.off[e];
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
-        esync();
-        uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
         if (etid == 0) {
           __threadfence();
-          const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
-          *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
+          const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
+          *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
           if (*bcast) __threadfence();
         }
         esync();
         if (*bcast) {
-          // the last expert to finish this 128-column slice: weighted combine
-          // in slot order, shared expert last; warp per token, 4 columns a lane
-          const int sh_off = sc.off[a.E];
-          const int n = nt * kRows + 4 * lane;
-          for (int t = ew; t < a.T; t += kEpiWarps) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j0 = 0; j0 <= a.k; j0 += 8) {
-              float4 yv[8];
-              float wv[8];
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int j = j0 + jj;
-                yv[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-                wv[jj] = 0.0f;
-                int pr = -1;
-                if (j < a.k) {
-                  pr = sc.flat_pair[t * a.k + j];
-                  if (pr >= 0) wv[jj] = a.w[t * a.k + j];
-                } else if (j == a.k && a.has_shared) {
-                  pr = sh_off + t;
-                  wv[jj] = 1.0f;
-                }
-                if (pr >= 0)
-                  yv[jj] = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pr) * a.H + n));
-              }
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                acc.x = fmaf(wv[jj], yv[jj].x, acc.x);
-                acc.y = fmaf(wv[jj], yv[jj].y, acc.y);
-                acc.z = fmaf(wv[jj], yv[jj].z, acc.z);
-                acc.w = fmaf(wv[jj], yv[jj].w, acc.w);
+          for (int m = ew; m < a.M; m += kEpiWarps) {
+            float bv = -FLT_MAX;
+            int bi = 0x7fffffff;
+            for (int j = lane; j < wk.n_tiles; j += 32) {
+              const int2 pr = __ldcg(a.am_part + m * wk.n_tiles + j);
+              const float v = __int_as_float(pr.x);
+              if (pr.y != 0x7fffffff && am_better(v, pr.y, bv, bi)) {
+                bv = v;
+                bi = pr.y;
               }
             }
-            __nv_bfloat16* o = a.out + t * a.ldo + n;
-            o[0] = __float2bfloat16_rn(acc.x);
-            o[1] = __float2bfloat16_rn(acc.y);
-            o[2] = __float2bfloat16_rn(acc.z);
-            o[3] = __float2bfloat16_rn(acc.w);
+            am_warp_reduce(bv, bi);
+            if (lane == 0) a.argmax_out[m] = bi;
           }
-          if (etid == 0) col_cnt[nt] = 0u;
+          if (etid == 0) *a.argmax_cnt = 0u;
         }
       }
+    } else if (MODE == kTcGateUp) {
+      // rows 0-31 gate and 32-63 up of pair-box 2*tile; 64-127 likewise
+      // for pair-box 2*tile+1 (absent when the count is odd)
+      if (q & 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ep[j * kRows + r] = tot[j];
+      }
+      esync();
+      const int pb = 2 * tile + (q >> 1);
+      if (!(q & 1) && pb < wk.pb_count) {
+        const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
+        const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+        const int cnt = sc.cnt[e], off = sc.off[e];
+        for (int qq = 0; qq < cnt; ++qq) {
+          const int p = off + qq;
+          const int t = sc.pair_tok[p];
+          const float f = a.rms ? g * rms[t] : g;
+          float gt = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == t) gt = tot[j];
+          gt *= f;
+          const float up = ep[t * kRows + r + 32] * f;
+          a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
+        }
+      }
+    } else {
+      const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
+      const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+      const int cnt = sc.cnt[e], off = sc.off[e];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
+      esync();
+      uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
+      if (etid == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
+        *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
+        if (*bcast) __threadfence();
+      }
+      esync();
+      if (*bcast) {
+        // the last expert to finish this 128-column slice: weighted combine
+        // in slot order, shared expert last; warp per token, 4 columns a lane
+        const int sh_off = sc.off[a.E];
+        const int n = nt * kRows + 4 * lane;
+        for (int t = ew; t < a.T; t += kEpiWarps) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j0 = 0; j0 <= a.k; j0 += 8) {
+            float4 yv[8];
+            float wv[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const int j = j0 + jj;
+              yv[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+              wv[jj] = 0.0f;
+              int pr = -1;
+              if (j < a.k) {
+                pr = sc.flat_pair[t * a.k + j];
+                if (pr >= 0) wv[jj] = a.w[t * a.k + j];
+              } else if (j == a.k && a.has_shared) {
+                pr = sh_off + t;
+                wv[jj] = 1.0f;
+              }
+              if (pr >= 0)
+                yv[jj] = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pr) * a.H + n));
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              acc.x = fmaf(wv[jj], yv[jj].x, acc.x);
+              acc.y = fmaf(wv[jj], yv[jj].y, acc.y);
+              acc.z = fmaf(wv[jj], yv[jj].z, acc.z);
+              acc.w = fmaf(wv[jj], yv[jj].w, acc.w);
+            }
+          }
+          __nv_bfloat16* o = a.out + t * a.ldo + n;
+          o[0] = __float2bfloat16_rn(acc.x);
+          o[1] = __float2bfloat16_rn(acc.y);
+          o[2] = __float2bfloat16_rn(acc.z);
+          o[3] = __float2bfloat16_rn(acc.w);
+        }
+        if (etid == 0) col_cnt[nt] = 0u;
+      }
+    }
+    esync();
+  }
+  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+}
+
+// ------------------------------------------------------------ roles
+
+__device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& c, int lane) {
+  const uint64_t pol = l2_policy_evict_first();
+  const bool table = prog.ops != nullptr;
+  SchedCursor cur;
+  int stage = 0;
+  uint32_t phase = 0;
+  long issued = 0;
+  for (int i = 0; i < prog.n_ops; ++i) {
+    if (__any_sync(0xffffffffu, c.aborted())) break;
+    const TcOp& op = op_at(prog, i);
+    switch (op.mode) {
+      case kTcDense: produce_op<kTcDense>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      case kTcGateUp: produce_op<kTcGateUp>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      default: produce_op<kTcDown>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+    }
+  }
+  // wait for the TMA writes still in flight (bounded, ignores aborts)
+  if (lane == 0) {
+    const int n = issued < c.n_stages() ? static_cast<int>(issued) : c.n_stages();
+    for (int i = 0; i < n; ++i) {
+      if (stage == 0) {
+        stage = c.n_stages() - 1;
+        phase ^= 1u;
+      } else {
+        --stage;
+      }
+      mbar_wait(c.ring_full_at(stage), phase, c.status());
+    }
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void mma_role(const TcProgram& prog, const Cta& c, int lane) {
+  SchedCursor cur;
+  uint32_t acount = 0, dcount = 0, xcount = 0;
+  for (int i = 0; i < prog.n_ops; ++i) {
+    if (__any_sync(0xffffffffu, c.aborted())) break;
+    const TcOp& op = op_at(prog, i);
+    switch (op.mode) {
+      case kTcDense: mma_op<kTcDense>(c, op, cur, lane, acount, dcount, xcount); break;
+      case kTcGateUp: mma_op<kTcGateUp>(c, op, cur, lane, acount, dcount, xcount); break;
+      default: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount); break;
+    }
+  }
+  // every MMA has completed before tensor memory is released
+  if (tc::elect_one()) tc::commit(c.mma_done());
+  __syncwarp();
+  if (lane == 0) mbar_wait(c.mma_done(), 0, c.status());
+  __syncwarp();
+}
+
+__device__ __forceinline__ void decode_role(const TcProgram& prog, const Cta& c, int warp, int lane) {
+  SchedCursor cur;
+  uint32_t acount = 0;
+  int rstage = 0;
+  uint32_t rphase = 0;
+  for (int i = 0; i < prog.n_ops && !c.aborted(); ++i) {
+    const TcOp& op = op_at(prog, i);
+    switch (op.mode) {
+      case kTcDense: decode_op<kTcDense>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      case kTcGateUp: decode_op<kTcGateUp>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      default: decode_op<kTcDown>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& c, int warp, int lane) {
+  const int ew = warp - kEpiWarp0, etid = ew * 32 + lane;
+  const int n_ops = prog.n_ops;
+  SchedCursor cur;
+  uint32_t dcount = 0;
+  // inputs may come from the previous kernel on the stream
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int i = 0; i < n_ops && !c.aborted(); ++i) {
+    const TcOp& op = op_at(prog, i);
+    if (i > 0 && op.wait_prev) {
+      // every CTA has finished op i - 1: its outputs are complete
+      if (etid == 0) grid_wait(&prog.done[i - 1], gridDim.x, c.status(), c.abort_flag());
       esync();
     }
+    switch (op.mode) {
+      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount); break;
+      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount); break;
+      default: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount); break;
+    }
+    if (n_ops > 1) {
+      esync();
+      if (etid == 0) {
+        __threadfence();
+        atomicAdd(&prog.done[i], 1u);
+      }
+    }
+  }
+  if (n_ops > 1 && etid == 0) {
+    // the last CTA to leave returns the completion counters to zero
+    __threadfence();
+    if (atomicAdd(&prog.done[n_ops], 1u) == gridDim.x - 1) {
+      for (int i = 0; i <= n_ops; ++i) prog.done[i] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+// One warp builds the expert schedule of each MoE op that starts one, into
+// the slot its previous users released.
+__device__ __forceinline__ void sched_role(const TcProgram& prog, const Cta& c, int lane) {
+  int idx = -1;
+  for (int i = 0; i < prog.n_ops && !c.aborted(); ++i) {
+    const TcOp& op = op_at(prog, i);
+    if (op.mode == kTcDense || !op.new_sched) continue;
+    ++idx;
+    const int slot = idx % c.sched_slots();
+    wait_bar(c.sched_empty_at(slot), ((idx / c.sched_slots()) & 1) ^ 1, c.status(), c.abort_flag());
+    if (c.aborted()) break;
+    // gate_up may read ids written before the previous kernel started
+    // (NVFP4_FLAG_IDS_READY) before its dependency wait; down always can:
+    // the gate_up grid before it read them after its own wait.
+    if (op.mode == kTcGateUp && !op.a.ids_ready) pdl_wait();
+    const Sched sc = sched_layout(c.sched() + slot * c.sched_bytes(), op.a.E, op.a.T * op.a.k);
+    build_schedule_warp(op.a.ids, op.a.T, op.a.k, op.a.E, op.a.has_shared, sc, c.status(), lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.sched_full_at(slot));
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    stream_tc_kernel(const __grid_constant__ TcProgram prog) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Cta c{smem, prog, 0u};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < c.n_stages(); ++s) {
+      mbar_init(c.ring_full_at(s), 1);
+      mbar_init(c.ring_empty_at(s), kDecWarps);
+    }
+    for (int b = 0; b < kABufs; ++b) {
+      mbar_init(c.a_full_at(b), kDecWarps);
+      mbar_init(c.a_empty_at(b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(c.d_full_at(b), 1);
+      mbar_init(c.d_empty_at(b), kEpiWarps);
+      mbar_init(c.sched_full_at(b), 1);
+      mbar_init(c.sched_empty_at(b), kSchedUsers);
+    }
+    mbar_init(c.x_full(), kEpiWarps);
+    mbar_init(c.mma_done(), 1);
+    fence_mbarrier_init();
+    *c.abort_flag() = 0;
+  }
+  if (warp == 1) tc::tmem_alloc(c.tmem_slot(), kTmemCols);
+  __syncthreads();
+  tc::fence_after_sync();
+  c.tmem = *c.tmem_slot();
+
+  if (warp == 0) {
+    producer_role(prog, c, lane);
+  } else if (warp == 1) {
+    mma_role(prog, c, lane);
+  } else if (warp < kEpiWarp0) {
+    decode_role(prog, c, warp, lane);
+  } else if (warp < kSchedWarp) {
+    epilogue_role(prog, c, warp, lane);
+  } else {
+    sched_role(prog, c, lane);
   }
 
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(c.tmem, kTmemCols);
   }
 }
 
-template <int MODE>
-cudaError_t launch_mode(const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
-                        cudaStream_t s, bool pdl) {
+}  // namespace
+
+cudaError_t launch_tc(const TcProgram& p, int grid, size_t smem, cudaStream_t s, bool pdl,
+                      bool cooperative) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(stream_tc_kernel<MODE>,
+    cudaError_t e = cudaFuncSetAttribute(stream_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -797,26 +1082,21 @@ cudaError_t launch_mode(const CUtensorMap* maps, const TcArgs& a, int grid, size
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem < kOnePerSm ? kOnePerSm : smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, stream_tc_kernel<MODE>, maps[0], maps[1], maps[2], maps[3], a);
-}
-
-}  // namespace
-
-cudaError_t launch_tc(int mode, const CUtensorMap* maps, const TcArgs& a, int grid, size_t smem,
-                      cudaStream_t s, bool pdl) {
-  switch (mode) {
-    case kTcDense:
-      return launch_mode<kTcDense>(maps, a, grid, smem, s, pdl);
-    case kTcGateUp:
-      return launch_mode<kTcGateUp>(maps, a, grid, smem, s, pdl);
-    default:
-      return launch_mode<kTcDown>(maps, a, grid, smem, s, pdl);
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
   }
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, stream_tc_kernel, p);
 }
 
 }  // namespace nvfp4

@@ -128,13 +128,47 @@ class DecodeStep:
         launches += 1
         return launches
 
-    def capture(self, b: dict, pdl: bool = True) -> torch.cuda.CUDAGraph:
-        """Warm up, then capture one step as a CUDA graph."""
-        self.run(b, pdl)
+    # ------------------------------------------------------------ as a program
+    def program_ops(self, b: dict) -> list:
+        """The step's projections, MoE layers and head as one op chain."""
+        s, T = self.s, b["T"]
+        chain = []
+        x = b["x"]
+        for l in range(s.layers):
+            i = l if b["keep"] else 0
+            q, o = b["q"][i], b["o"][i]
+            y = b["y"][l if b["keep"] else l % 2]
+            chain.append(ops.gemm_op(x, self.qkv[l], q, rms_input=True))
+            chain.append(ops.gemm_op(q[:, :s.o_in], self.o[l], o, rms_input=True))
+            chain.append(ops.moe_op(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T],
+                                    self.experts[l], y, shared=self.shared[l], rms_input=True))
+            x = y
+        chain.append(ops.gemm_op(x, self.head, b["head"], argmax_out=b["argmax"], rms_input=True))
+        return chain
+
+    def program(self, b: dict) -> "ops.Program":
+        """Create the step's program on the buffers ``b`` (once)."""
+        chain = self.program_ops(b)
+        need = ops.program_workspace_bytes(chain)
+        if b["ws"].nbytes < need:
+            b["ws"] = ops.Workspace(need, self.device)
+        return ops.Program(chain, b["ws"])
+
+    def run_program(self, b: dict, prog: "ops.Program") -> int:
+        """One step as two launches: routing of every layer, then the program."""
+        ops.route(b["logits"], self.s.top_k, True, b["ids"], b["w"])
+        prog.launch()
+        return 2
+
+    def capture(self, b: dict, pdl: bool = True, prog: "ops.Program" = None) -> torch.cuda.CUDAGraph:
+        """Warm up, then capture one step (call by call, or as ``prog``) as a
+        CUDA graph."""
+        step = (lambda: self.run(b, pdl)) if prog is None else (lambda: self.run_program(b, prog))
+        step()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.run(b, pdl)
+            step()
         torch.cuda.synchronize()
         return g
 

@@ -43,6 +43,21 @@ class _Stack(ctypes.Structure):
                 ("inter", ctypes.c_int32)]
 
 
+OP_GEMM = 1
+OP_MOE = 2
+
+
+class _Op(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("M", ctypes.c_int32),
+                ("W", _Weight), ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("argmax_out", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("T", ctypes.c_int32),
+                ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("k", ctypes.c_int32),
+                ("experts", _Stack), ("shared", _Stack), ("out", ctypes.c_void_p),
+                ("ldo", ctypes.c_int64)]
+
+
 _lib: Optional[ctypes.CDLL] = None
 
 
@@ -71,6 +86,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.moe_nvfp4_decode_workspace.restype = sz
     L.moe_nvfp4_decode.argtypes = [vp, i64, i32, vp, vp, i32, ctypes.POINTER(_Stack),
                                    ctypes.POINTER(_Stack), vp, i64, u32, vp, sz, vp]
+    L.nvfp4_program_workspace.argtypes = [ctypes.POINTER(_Op), i32]
+    L.nvfp4_program_workspace.restype = sz
+    L.nvfp4_program_create.argtypes = [ctypes.POINTER(_Op), i32, vp, sz, ctypes.POINTER(vp)]
+    L.nvfp4_program_launch.argtypes = [vp, vp]
+    L.nvfp4_program_destroy.argtypes = [vp]
     L.nvfp4_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     L.nvfp4_last_dispatch.argtypes = [ctypes.c_char_p, sz]
     L.nvfp4_last_error.restype = ctypes.c_char_p
@@ -263,3 +283,82 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
                               out.data_ptr(), out.stride(0), flags, workspace.ptr(),
                               workspace.nbytes, _stream(stream)), "moe_nvfp4_decode")
     return out
+
+
+# ------------------------------------------------------------------ programs
+
+def gemm_op(a: torch.Tensor, w: NVFP4Weight, out: torch.Tensor,
+            argmax_out: Optional[torch.Tensor] = None, rms_input: bool = False) -> dict:
+    """One GEMM of a program: out = A W^T (as gemm())."""
+    return dict(kind=OP_GEMM, a=a, w=w, out=out, argmax_out=argmax_out, rms_input=rms_input)
+
+
+def moe_op(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
+           out: torch.Tensor, shared: Optional[ExpertStack] = None,
+           rms_input: bool = False) -> dict:
+    """One MoE layer of a program (as moe()); ids / weights must be complete
+    before the program is launched."""
+    return dict(kind=OP_MOE, x=x, ids=ids, weights=weights, experts=experts, out=out,
+                shared=shared, rms_input=rms_input)
+
+
+def _c_ops(ops: list) -> ctypes.Array:
+    arr = (_Op * len(ops))()
+    for i, o in enumerate(ops):
+        c = arr[i]
+        c.kind = o["kind"]
+        c.flags = FLAG_RMS_INPUT if o.get("rms_input") else 0
+        if o["kind"] == OP_GEMM:
+            a, out = o["a"], o["out"]
+            c.A, c.lda, c.M = a.data_ptr(), a.stride(0), a.shape[0]
+            c.W = o["w"].c()
+            c.C, c.ldc = out.data_ptr(), out.stride(0)
+            c.argmax_out = _ptr(o.get("argmax_out"))
+        else:
+            x, ids, out = o["x"], o["ids"], o["out"]
+            assert ids.is_contiguous() and o["weights"].is_contiguous()
+            c.x, c.ldx, c.T = x.data_ptr(), x.stride(0), ids.shape[0]
+            c.topk_ids, c.topk_w, c.k = ids.data_ptr(), o["weights"].data_ptr(), ids.shape[1]
+            c.experts = o["experts"].c()
+            if o.get("shared") is not None:
+                c.shared = o["shared"].c()
+            c.out, c.ldo = out.data_ptr(), out.stride(0)
+    return arr
+
+
+def program_workspace_bytes(ops: list) -> int:
+    arr = _c_ops(ops)
+    return int(load().nvfp4_program_workspace(arr, len(ops)))
+
+
+class Program:
+    """A fixed chain of GEMM / MoE calls run by one persistent launch.  The
+    tensors of ``ops`` (and the workspace) are bound at creation: keep them
+    alive and write new inputs into them in place."""
+
+    def __init__(self, ops: list, workspace: Optional[Workspace] = None):
+        L = load()
+        self._keep = ops
+        arr = _c_ops(ops)
+        if workspace is None:
+            dev = ops[0]["a"].device if ops[0]["kind"] == OP_GEMM else ops[0]["x"].device
+            workspace = Workspace(L.nvfp4_program_workspace(arr, len(ops)), dev)
+        self.workspace = workspace
+        h = ctypes.c_void_p()
+        _check(L.nvfp4_program_create(arr, len(ops), workspace.ptr(), workspace.nbytes,
+                                      ctypes.byref(h)), "nvfp4_program_create")
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(load().nvfp4_program_launch(self._h, _stream(stream)), "nvfp4_program_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().nvfp4_program_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -85,3 +85,25 @@ def test_moe_validation_codes(lib):
     assert call(ex=_stack(base=p + 4)) == -2
     assert call(sh=_stack(e=2)) == -1
     assert call(x=p + 2) == -2
+
+
+def test_program_validation_codes(lib):
+    p = 1 << 20
+    h = ctypes.c_void_p()
+    op = ops._Op()
+    op.kind = ops.OP_GEMM
+    op.A, op.lda, op.M, op.W, op.C, op.ldc = p, 2048, 4, _w(), p, 64
+    assert lib.nvfp4_program_create(None, 1, p, 1 << 30, ctypes.byref(h)) == -1
+    assert lib.nvfp4_program_create(ctypes.byref(op), 0, p, 1 << 30, ctypes.byref(h)) == -1
+    assert lib.nvfp4_program_create(ctypes.byref(op), 1, p, 1 << 30, None) == -1
+    op.M = 33
+    assert lib.nvfp4_program_create(ctypes.byref(op), 1, p, 1 << 30, ctypes.byref(h)) == -3
+    op.M, op.kind = 4, 7
+    assert lib.nvfp4_program_create(ctypes.byref(op), 1, p, 1 << 30, ctypes.byref(h)) == -1
+    moe = ops._Op()
+    moe.kind = ops.OP_MOE
+    moe.x, moe.ldx, moe.T, moe.topk_ids, moe.topk_w, moe.k = p, 2048, 4, p, p, 17
+    moe.experts, moe.out, moe.ldo = _stack(), p, 2048
+    assert lib.nvfp4_program_create(ctypes.byref(moe), 1, p, 1 << 30, ctypes.byref(h)) == -3
+    assert not h.value
+    assert lib.nvfp4_program_destroy(None) == 0

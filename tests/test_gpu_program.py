@@ -1,0 +1,155 @@
+"""GPU checks of programs (a chain of GEMM / MoE calls in one persistent
+launch): results bit-identical to the same calls issued one by one (which the
+other files check against the float64 oracle), one chain also checked against
+the oracle directly, and the workspace counters back at zero afterwards."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import (assert_close, device_experts, device_shared, device_weight, f64,
+                     host_weight)
+from moe_expert_nvfp4_gb300 import ops, synth
+from moe_expert_nvfp4_gb300.decode_step import DecodeStep, StepShape
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from moe_expert_nvfp4_gb300 import build
+    build.build()
+    ops.load()
+    assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
+
+
+def _counters_zero(ws):
+    torch.cuda.synchronize()
+    hdr = ws.buf[:256 + 4 * 16384].view(torch.int32)
+    return int(hdr[1:].abs().sum().item()) == 0 and int(hdr[0].item()) == 0
+
+
+def test_single_gemm_program_equals_call():
+    W = device_weight(11, 3000, 2048)
+    a = synth.activations_bf16(11, 8, 2048).cuda()
+    ref = ops.gemm(a, W)
+    out = torch.empty_like(ref)
+    prog = ops.Program([ops.gemm_op(a, W, out)])
+    prog.launch()
+    torch.cuda.synchronize()
+    assert ops.last_dispatch().startswith("stream_tc_kernel program ops=1")
+    assert torch.equal(out, ref)
+    assert _counters_zero(prog.workspace)
+
+
+@pytest.mark.parametrize("m", [1, 8, 32])
+def test_gemm_chain_equals_calls_and_oracle(m):
+    """x -> (rms) W1 [4096 x 2048] -> (rms) W2 [2048 x 4096] -> W3 [1000 x 2048] + argmax."""
+    W1 = device_weight(12, 4096, 2048)
+    W2 = device_weight(13, 2048, 4096)
+    W3 = device_weight(14, 1000, 2048)
+    x = synth.activations_bf16(12, m, 2048).cuda()
+    h1 = ops.gemm(x, W1, rms_input=True)
+    h2 = ops.gemm(h1, W2, rms_input=True)
+    h3, am = ops.gemm(h2, W3, argmax=True)
+    torch.cuda.synchronize()
+    p1, p2, p3 = torch.empty_like(h1), torch.empty_like(h2), torch.empty_like(h3)
+    pam = torch.empty_like(am)
+    prog = ops.Program([ops.gemm_op(x, W1, p1, rms_input=True),
+                        ops.gemm_op(p1, W2, p2, rms_input=True),
+                        ops.gemm_op(p2, W3, p3, argmax_out=pam)])
+    for _ in range(3):   # repeated launches reuse the zeroed counters
+        prog.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(p1, h1) and torch.equal(p2, h2) and torch.equal(p3, h3)
+    assert torch.equal(pam, am)
+    assert prog.workspace.status() == 0
+    assert _counters_zero(prog.workspace)
+    # teacher-forced oracle check of the chain's middle link
+    ref2 = O.gemm_bf16(O.rms_scale(f64(p1)), *host_weight(13, 2048, 4096))
+    assert_close(f64(p2), ref2, f"chain M={m}")
+
+
+@pytest.fixture(scope="module")
+def layer():
+    E, H, I = 64, 2048, 512
+    return device_experts(21, 0, E, H, I), device_shared(21, 0, E, H, I)
+
+
+@pytest.mark.parametrize("t", [1, 8, 32])
+def test_moe_in_program_equals_call(layer, t):
+    ex, sh = layer
+    x = synth.activations_bf16(21, t, 2048).cuda()
+    ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
+    W = device_weight(22, 2048, 2048)
+    # GEMM -> MoE -> GEMM, so the MoE reads a program-written input and its
+    # output feeds a later op
+    g1 = ops.gemm(x, W, rms_input=True)
+    y = ops.moe(g1, ids, w, ex, sh, rms_input=True, ids_ready=True)
+    g2 = ops.gemm(y, W, rms_input=True)
+    torch.cuda.synchronize()
+    pg1, py, pg2 = torch.empty_like(g1), torch.empty_like(y), torch.empty_like(g2)
+    prog = ops.Program([ops.gemm_op(x, W, pg1, rms_input=True),
+                        ops.moe_op(pg1, ids, w, ex, py, shared=sh, rms_input=True),
+                        ops.gemm_op(py, W, pg2, rms_input=True)])
+    prog.launch()
+    prog.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(pg1, g1) and torch.equal(py, y) and torch.equal(pg2, g2)
+    assert prog.workspace.status() == 0
+    assert _counters_zero(prog.workspace)
+
+
+def test_two_moe_layers_share_schedule_slots(layer):
+    """Four MoE layers in a row cycle both schedule slots twice."""
+    ex, sh = layer
+    t = 8
+    x = synth.activations_bf16(23, t, 2048).cuda()
+    lg = synth.router_logits(23, 4 * t, 64).cuda()
+    ids, w = ops.route(lg, 8)
+    outs, cur = [], x
+    for l in range(4):
+        cur = ops.moe(cur, ids[l * t:(l + 1) * t], w[l * t:(l + 1) * t], ex,
+                      sh if l % 2 == 0 else None, rms_input=True, ids_ready=True)
+        outs.append(cur)
+    torch.cuda.synchronize()
+    pouts = [torch.empty_like(o) for o in outs]
+    chain, src = [], x
+    for l in range(4):
+        chain.append(ops.moe_op(src, ids[l * t:(l + 1) * t], w[l * t:(l + 1) * t], ex, pouts[l],
+                                shared=sh if l % 2 == 0 else None, rms_input=True))
+        src = pouts[l]
+    prog = ops.Program(chain)
+    prog.launch()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(pouts, outs))
+    assert _counters_zero(prog.workspace)
+
+
+@pytest.mark.parametrize("tokens", [1, 8])
+def test_decode_step_program_equals_calls(tokens):
+    m = DecodeStep(seed=6, shape=StepShape(layers=3))
+    b = m.buffers(tokens, keep=True)
+    x, lg = m.inputs(tokens)
+    b["x"].copy_(x)
+    b["logits"].copy_(lg)
+    m.run(b)
+    torch.cuda.synchronize()
+    ref = {k: [t.clone() for t in b[k]] for k in ("q", "o", "y")}
+    ref_head, ref_am = b["head"].clone(), b["argmax"].clone()
+    for k in ("q", "o", "y"):
+        for t in b[k]:
+            t.zero_()
+    b["head"].zero_()
+    b["argmax"].zero_()
+    prog = m.program(b)
+    g = m.capture(b, prog=prog)
+    g.replay()
+    torch.cuda.synchronize()
+    for k in ("q", "o", "y"):
+        assert all(torch.equal(a, c) for a, c in zip(b[k], ref[k])), k
+    assert torch.equal(b["head"], ref_head) and torch.equal(b["argmax"], ref_am)
+    assert b["ws"].status() == 0
+    assert _counters_zero(b["ws"])
