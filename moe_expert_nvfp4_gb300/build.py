@@ -69,7 +69,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
                os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
-        r = subprocess.run(cmd, capture_output=True, text=True)
+        # nvcc 13.0's device front end has been seen to crash (SIGSEGV) now and
+        # then on the large persistent kernel with the same input that
+        # compiles on the next try: retry a crash, never a compile error
+        for attempt in range(4):
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            crashed = r.returncode < 0 or "Segmentation fault" in r.stderr
+            if r.returncode == 0 or not crashed:
+                break
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
         if verbose and r.stderr:

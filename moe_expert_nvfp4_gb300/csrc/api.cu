@@ -5,6 +5,7 @@
 // and the per-thread error and dispatch records.
 #include <cudaTypedefs.h>
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -191,7 +192,7 @@ struct TcLayout {
 };
 
 bool tc_layout(int sched_bytes, size_t x_bytes, TcLayout* L) {
-  L->x_offset = static_cast<int>(round_up(kTcOffSched + sched_bytes, 128));
+  L->x_offset = static_cast<int>(round_up(kTcOffSched + sched_bytes, 1024));
   L->ring_offset = static_cast<int>(round_up(L->x_offset + x_bytes, 1024));
   const long room = static_cast<long>(kSmemLimit) - kSmemAlignPad - L->ring_offset;
   L->n_stages = static_cast<int>(room / kTcStageBytes);
@@ -202,7 +203,8 @@ bool tc_layout(int sched_bytes, size_t x_bytes, TcLayout* L) {
 }
 
 struct TcDensePlan {
-  int n_tiles, nkb, grid, npad, win_k;
+  int n_tiles, nkb, grid, npad, xrows, win_k;
+  size_t x_bytes;
   long units;
   TcLayout L;
   size_t off_partials, off_am, ws_bytes;
@@ -215,16 +217,21 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
   p->units = static_cast<long>(p->n_tiles) * p->nkb;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   p->npad = M <= 16 ? 16 : 32;
-  p->win_k = K < kTcMaxWinK ? K : kTcMaxWinK;
-  if (!tc_layout(0, static_cast<size_t>(p->npad) * p->win_k * 2, &p->L)) return false;
-  p->off_partials = kWsScratch;
-  p->off_am = round_up(p->off_partials + 4ull * p->grid * 2 * 32 * 128, 256);
+  p->xrows = tc_xrows(M);
+  const int cap = p->xrows == 8 ? 2 * kTcMaxWinK : kTcMaxWinK;  // 64 KB (8, 16 rows), 128 KB (32)
+  p->win_k = K < cap ? K : cap;
+  p->x_bytes = static_cast<size_t>(p->xrows) * p->win_k * 2;
+  if (!tc_layout(0, p->x_bytes, &p->L)) return false;
+  p->off_partials = kWsScratch;  // one pair of partial slots for every SM: programs
+                                 // may place the op on any CTA
+  p->off_am = round_up(p->off_partials + 4ull * sms * 2 * 32 * 128, 256);
   p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
   return true;
 }
 
 struct TcMoePlan {
-  int P, npad, sched_bytes, grid;
+  int P, npad, xrows, sched_bytes, grid;
+  size_t x_bytes;
   TcLayout gu, dn;
   size_t off_partials, off_h, off_y, ws_bytes;
 };
@@ -232,10 +239,12 @@ struct TcMoePlan {
 bool plan_tc_moe(int T, int k, int E, int H, int I, int sms, TcMoePlan* p) {
   p->P = T * k;
   p->npad = T <= 16 ? 16 : 32;
+  p->xrows = tc_xrows(T);
   if (H > 4096 || I > 2048) return false;  // staged rows are read once into registers
   p->sched_bytes = static_cast<int>(round_up(4ull * (4 * E + 5 + 2 * p->P + 33), 128));
-  if (!tc_layout(p->sched_bytes, static_cast<size_t>(p->npad) * H * 2, &p->gu) ||
-      !tc_layout(p->sched_bytes, static_cast<size_t>(p->npad) * I * 2, &p->dn))
+  p->x_bytes = static_cast<size_t>(p->xrows) * (H > I ? H : I) * 2;
+  if (!tc_layout(p->sched_bytes, static_cast<size_t>(p->xrows) * H * 2, &p->gu) ||
+      !tc_layout(p->sched_bytes, static_cast<size_t>(p->xrows) * I * 2, &p->dn))
     return false;
   const long max_active = (p->P < E ? p->P : E) + 1;
   if (max_active * (H / 128) > kTcColCntBase || H / 128 > kWsMaxCounters - kTcColCntBase) return false;
@@ -263,6 +272,23 @@ int check_stack(const nvfp4_expert_stack* s, const char* name) {
   return NVFP4_OK;
 }
 
+
+// Activation map of a tcgen05 op: BF16 [rows, k] with row stride ld
+// elements, boxes of 64 x xrows (128 bytes x rows, 128-byte swizzle); rows
+// past `rows` read as zero.
+int act_map(CUtensorMap* m, const void* base, int rows, int64_t ld, int k, int xrows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(xrows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (activations) failed (%d)", (int)r);
+  return NVFP4_OK;
+}
 
 // ------------------------------------------------------------- validation
 int check_gemm(const void* A, int64_t lda, int M, const nvfp4_weight* W, const void* C,
@@ -318,6 +344,7 @@ int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* 
   if (rc) return rc;
   op->maps[2] = op->maps[0];
   op->maps[3] = op->maps[1];
+  if ((rc = act_map(&op->xmap, A, M, lda, W->k, p.xrows))) return rc;
   TcArgs& a = op->a;
   a.A = static_cast<const __nv_bfloat16*>(A);
   a.lda = lda;
@@ -330,6 +357,8 @@ int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* 
   a.K = W->k;
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.win_k = p.win_k;
+  a.n_ctas = p.grid;
+  a.cta0 = 0;
   ws_header(a, ws);
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
@@ -350,7 +379,8 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   if ((rc = weight_maps(&gu->maps[0], &gu->maps[1], experts->gu_codes, experts->gu_scales,
                         2ull * I * E, H)) ||
       (rc = weight_maps(&gu->maps[2], &gu->maps[3], sh->gu_codes, sh->gu_scales,
-                        2ull * I * sh->num_experts, H)))
+                        2ull * I * sh->num_experts, H)) ||
+      (rc = act_map(&gu->xmap, x, T, ldx, H, p.xrows)))
     return rc;
   TcArgs& a = gu->a;
   a.x = static_cast<const __nv_bfloat16*>(x);
@@ -376,6 +406,8 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   a.h = reinterpret_cast<float*>(ws + p.off_h);
   a.y = reinterpret_cast<float*>(ws + p.off_y);
   a.win_k = H;
+  a.n_ctas = p.grid;
+  a.cta0 = 0;
   gu->mode = kTcGateUp;
   gu->new_sched = 1;
   gu->wait_prev = 1;
@@ -498,7 +530,7 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
     if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, flags, ws, p, &op))) return rc;
     int n_stages = 0;
     size_t smem = 0;
-    rc = tc_launch_one(op, static_cast<size_t>(p.npad) * p.win_k * 2, 0, p.grid, ws,
+    rc = tc_launch_one(op, p.x_bytes, 0, p.grid, ws,
                        reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL),
                        &n_stages, &smem, "stream_tc_kernel<dense> launch");
     if (rc) return rc;
@@ -611,10 +643,10 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int st_gu = 0, st_dn = 0;
     size_t sm_gu = 0, sm_dn = 0;
-    if ((rc = tc_launch_one(gu, static_cast<size_t>(p.npad) * H * 2, p.sched_bytes, p.grid, ws, s,
-                            pdl, &st_gu, &sm_gu, "stream_tc_kernel<gate_up> launch")) ||
-        (rc = tc_launch_one(dn, static_cast<size_t>(p.npad) * I * 2, p.sched_bytes, p.grid, ws, s,
-                            pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
+    if ((rc = tc_launch_one(gu, static_cast<size_t>(p.xrows) * H * 2, p.sched_bytes, p.grid, ws,
+                            s, pdl, &st_gu, &sm_gu, "stream_tc_kernel<gate_up> launch")) ||
+        (rc = tc_launch_one(dn, static_cast<size_t>(p.xrows) * I * 2, p.sched_bytes, p.grid, ws,
+                            s, pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
       return rc;
     char buf[256];
     snprintf(buf, sizeof(buf),
@@ -752,7 +784,7 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
       if ((rc = tc_dense_op(o.A, o.lda, o.M, &o.W, o.C, o.ldc, o.argmax_out, o.flags, ws, p, &op)))
         return rc;
       table.push_back(op);
-      x_bytes = std::max(x_bytes, static_cast<size_t>(p.npad) * p.win_k * 2);
+      x_bytes = std::max(x_bytes, p.x_bytes);
       need = std::max(need, p.ws_bytes);
       ++n_gemm;
     } else if (o.kind == NVFP4_OP_MOE) {
@@ -770,7 +802,7 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
         return rc;
       table.push_back(gu);
       table.push_back(dn);
-      x_bytes = std::max(x_bytes, static_cast<size_t>(p.npad) * std::max(H, I) * 2);
+      x_bytes = std::max(x_bytes, p.x_bytes);
       sched_bytes = std::max(sched_bytes, p.sched_bytes);
       need = std::max(need, p.ws_bytes);
       ++n_moe;
@@ -780,6 +812,28 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
   }
   const int n = static_cast<int>(table.size());
   if (n > kTcMaxOps) return fail(NVFP4_ERR_SHAPE, "program of %d kernel ops > %d", n, kTcMaxOps);
+  // CTA ranges.  A dense op with fewer 128-row tiles than SMs is spread over
+  // only tiles x ceil(K stages / target) CTAs (whole tiles, or few splits per
+  // tile: short reductions), placed after the previous small op's CTAs, so
+  // that the other SMs stream the following ops' weights meanwhile.  Ops with
+  // at least one tile per SM (and MoE ops) use every SM.  Environment
+  // NVFP4_PROGRAM_TARGET_STAGES (default 8; 0 = every op on every SM).
+  int target = 8;
+  if (const char* env = getenv("NVFP4_PROGRAM_TARGET_STAGES")) target = atoi(env);
+  int next_cta = 0;
+  for (TcOp& op : table) {
+    int g = sms;
+    if (op.mode == kTcDense && target > 0) {
+      const int n_tiles = (op.a.N + 127) / 128, nkb = op.a.K / kStageK;
+      if (n_tiles < sms) {
+        const int splits = (nkb + target - 1) / target;
+        g = std::min(sms, n_tiles * splits);
+      }
+    }
+    op.a.n_ctas = g;
+    op.a.cta0 = next_cta;
+    next_cta = (next_cta + (g < sms ? g : 0)) % sms;
+  }
   if (!workspace || workspace_bytes < need)
     return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", need);
   table[0].wait_prev = 0;

@@ -119,6 +119,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// The same without an L2 cache hint (activations read by every CTA).
+__device__ __forceinline__ void tma_load_2d_nohint(void* smem_dst, const CUtensorMap* map, int x,
+                                                   int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -197,6 +207,25 @@ __device__ __forceinline__ int f16_row_shift(float amax) {
 __device__ __forceinline__ float scale_pow2(float v, int s) {
   const int h = s / 2;
   return (v * exp2i(h)) * exp2i(s - h);
+}
+
+// ------------------------------------------------------------------ gpu-scope sync
+// Counter add with acquire-release semantics at GPU scope: after a CTA
+// barrier, one thread's add publishes the CTA's earlier stores (release) and
+// makes the stores published by the earlier adders visible (acquire).
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+// The same, release only, without a result (the caller does not wait).
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -82,10 +82,10 @@ struct MoeArgs {
 constexpr int kTcTileRows = 128;                                // weight rows per tile
 constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;  // 18432
 constexpr int kTcMaxStages = 8;
-constexpr int kTcOffBars = 0;
-constexpr int kTcOffMisc = 256;
-constexpr int kTcOffEp = 768;
-constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17152
+constexpr int kTcOffBars = 0;                            // up to 64 mbarriers
+constexpr int kTcOffMisc = 512;
+constexpr int kTcOffEp = 1024;
+constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17408
 constexpr int kTcThreads = 480;   // producer, MMA, 8 decode, 4 epilogue warps, scheduler warp
 constexpr int kTcColCntBase = 8192;                      // down combine counters
 constexpr int kTcDoneBase = 12288;                       // per-op completion counters
@@ -121,17 +121,25 @@ struct TcArgs {
   // common
   int rms;
   int win_k;            // staged activation window capacity (elements, multiple of 256)
+  int n_ctas;           // CTAs the op's units are spread over (at most gridDim.x) ...
+  int cta0;             // ... starting at this CTA (wrapping around)
   uint32_t* tile_cnt;   // counters region
   uint32_t* argmax_cnt;
   float* partials;      // [grid][2][32][128]
   int2* am_part;        // [M][n_tiles]
 };
 
-// One op of a program: its four tensor maps (dense: codes, scales of W, twice;
-// MoE: routed codes, routed scales, shared codes, shared scales) and its
-// arguments.
+// Staged activation rows for n real rows: 8, 16 or 32 (the MMA's N is 16
+// or 32; with 8 staged rows its rows 8..15 repeat rows 0..7).
+__host__ __device__ constexpr int tc_xrows(int n) { return n <= 8 ? 8 : (n <= 16 ? 16 : 32); }
+
+// One op of a program: its four weight tensor maps (dense: codes, scales of
+// W, twice; MoE: routed codes, routed scales, shared codes, shared scales),
+// the activation map (dense A / MoE x: BF16, boxes of 64 x tc_xrows rows with
+// the 128-byte swizzle; unused by down) and its arguments.
 struct TcOp {
   CUtensorMap maps[4];
+  CUtensorMap xmap;
   TcArgs a;
   int mode;            // TcMode
   int new_sched;       // MoE: build a new expert schedule from this op's ids

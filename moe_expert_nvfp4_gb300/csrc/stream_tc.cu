@@ -66,7 +66,8 @@ constexpr int kSchedWarp = kEpiWarp0 + kEpiWarps;  // warp 14
 constexpr int kSchedUsers = 2 + kDecWarps + kEpiWarps;
 constexpr int kABufs = 3;                      // A operand buffers in tensor memory
 constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
-constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384 and 416
+constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384, 416, 448, 480
+constexpr int kDBufs = 4;                      // accumulator buffers (32 columns each)
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
@@ -127,14 +128,20 @@ struct Box {
 
 // Per-launch work description shared by all roles (all fields derived
 // deterministically from the arguments and the schedule).
+// The op's units are split over G CTAs: relative index r = the CTA
+// (blockIdx.x - cta0) mod gridDim.x; r >= G has none.
 struct Work {
   int n_tiles, nkb, per_e, pb_count;
   long U;
-  int G;
-  __device__ __forceinline__ long begin(int b) const { return static_cast<long>(b) * U / G; }
+  int G, cta0;
+  __device__ __forceinline__ long begin(int r) const { return static_cast<long>(r) * U / G; }
   __device__ __forceinline__ int cta_of(long u) const {
     return static_cast<int>(((u + 1) * G - 1) / U);
   }
+  __device__ __forceinline__ int rel(int b) const {
+    return (b - cta0 + static_cast<int>(gridDim.x)) % static_cast<int>(gridDim.x);
+  }
+  __device__ __forceinline__ int abs_cta(int r) const { return (r + cta0) % static_cast<int>(gridDim.x); }
 };
 
 template <int MODE>
@@ -199,12 +206,13 @@ __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kb
   return min(kbe, w0 + kk.win_stages());
 }
 
-// Stage range restaged when a window is not covered: dense, the window;
-// MoE, the whole K.
+// Stage range restaged when a window is not covered: the whole K when it
+// fits (MoE always; dense when the window capacity covers K: then staged once
+// per op), else the window.
 template <int MODE>
 __device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1, int& k0,
                                               int& k1) {
-  if (MODE == kTcDense) {
+  if (MODE == kTcDense && kk.win_stages() < kk.wk.nkb) {
     k0 = w0;
     k1 = w1;
   } else {
@@ -213,22 +221,29 @@ __device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, in
   }
 }
 
-// Stage B rows [0, npad) of K range [kbeg, kbeg + klen) into shared memory as
-// FP16 core matrices (see tc::smem_desc), one power-of-two shift per row
-// (sig), and optionally rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged
-// range.  Warp dw of nwarps takes rows dw, dw + nwarps, ...; a row is read
-// once into registers (at most 16 x 16 bytes per lane).
+// Byte offset of 8 staged elements (row n, k .. k + 7, k % 8 == 0) in the
+// activation layout: 64-element K-blocks of rb rows, one 128-byte line per
+// row, the line's 16-byte chunks swizzled by row (the layout TMA writes with
+// the 128-byte swizzle; the block base is 1024-byte aligned).
+__device__ __forceinline__ uint32_t xoff(int n, int k, int rb) {
+  return static_cast<uint32_t>((k >> 6) * rb * 128 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4));
+}
+
+// Stage rows [0, rb) of K range [kbeg, kbeg + klen) from registers: FP16
+// with one power-of-two shift per row (sig), rows past nr zero, optionally
+// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.  Warp dw of nwarps
+// takes rows dw, dw + nwarps, ...; a row is read once into registers (at
+// most 16 x 16 bytes per lane).
 template <typename T, typename RowFn>
-__device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, int klen,
-                                        uint8_t* xs, uint32_t sbo, int* sig, float* rms, int dw,
-                                        int lane, int nwarps) {
+__device__ __forceinline__ void stage_b(RowFn rowp, int nr, int rb, int kbeg, int klen,
+                                        uint8_t* xs, int* sig, float* rms, int dw, int lane,
+                                        int nwarps) {
   constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
   const int nv = klen / (32 * kVec);    // loads per lane
-  for (int n = dw; n < npad; n += nwarps) {
-    uint8_t* rowbase = xs + (n >> 3) * sbo + (n & 7) * 16;
+  for (int n = dw; n < rb; n += nwarps) {
     if (n >= nr) {
       for (int v = lane; v < klen / 8; v += 32)
-        *reinterpret_cast<uint4*>(rowbase + v * 128) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(xs + xoff(n, 8 * v, rb)) = make_uint4(0u, 0u, 0u, 0u);
       if (lane == 0) sig[n] = 0;
       continue;
     }
@@ -278,13 +293,13 @@ __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, 
             for (int j = 0; j < 4; ++j)
               pk[j] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * j]), sh),
                                  scale_pow2(static_cast<float>(e[2 * j + 1]), sh));
-            *reinterpret_cast<uint4*>(rowbase + (kq >> 3) * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(xs + xoff(n, kq, rb)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           } else {
             const uint32_t p0 = pack_f16x2(scale_pow2(static_cast<float>(e[0]), sh),
                                            scale_pow2(static_cast<float>(e[1]), sh));
             const uint32_t p1 = pack_f16x2(scale_pow2(static_cast<float>(e[2]), sh),
                                            scale_pow2(static_cast<float>(e[3]), sh));
-            *reinterpret_cast<uint2*>(rowbase + (kq >> 3) * 128 + (kq & 7) * 2) = make_uint2(p0, p1);
+            *reinterpret_cast<uint2*>(xs + xoff(n, kq & ~7, rb) + (kq & 7) * 2) = make_uint2(p0, p1);
           }
         }
     }
@@ -292,6 +307,7 @@ __device__ __forceinline__ void stage_b(RowFn rowp, int nr, int npad, int kbeg, 
 }
 
 // ------------------------------------------------------------ CTA context
+
 
 // Shared-memory objects and program-wide constants of one CTA, derived on
 // use from the aligned shared-memory base and the launch parameters (nothing
@@ -305,12 +321,13 @@ struct Cta {
   __device__ __forceinline__ uint64_t* ring_empty_at(int s) const { return bars() + kTcMaxStages + s; }
   __device__ __forceinline__ uint64_t* a_full_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + b; }
   __device__ __forceinline__ uint64_t* a_empty_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + kABufs + b; }
-  __device__ __forceinline__ uint64_t* d_full_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + b; }
-  __device__ __forceinline__ uint64_t* d_empty_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 2 + b; }
+  __device__ __forceinline__ uint64_t* d_full_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 12 + b; }
+  __device__ __forceinline__ uint64_t* d_empty_at(uint32_t b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 16 + b; }
   __device__ __forceinline__ uint64_t* x_full() const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 4; }
   __device__ __forceinline__ uint64_t* mma_done() const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 5; }
   __device__ __forceinline__ uint64_t* sched_full_at(int b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 6 + b; }
   __device__ __forceinline__ uint64_t* sched_empty_at(int b) const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 8 + b; }
+  __device__ __forceinline__ uint64_t* x_tma() const { return bars() + 2 * kTcMaxStages + 2 * kABufs + 10; }
   __device__ __forceinline__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + kTcOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 4); }
   __device__ __forceinline__ volatile int* bcast() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 8); }
@@ -326,7 +343,8 @@ struct Cta {
   __device__ __forceinline__ uint32_t* status() const { return prog.status; }
   __device__ __forceinline__ bool aborted() const { return *abort_flag() != 0; }
 };
-static_assert(2 * kTcMaxStages + 2 * kABufs + 10 <= kTcOffMisc / 8, "barrier area");
+static_assert(2 * kTcMaxStages + 2 * kABufs + 12 + 2 * kDBufs <= kTcOffMisc / 8, "barrier area");
+static_assert(kDCol + 32 * kDBufs <= static_cast<int>(kTmemCols), "tensor memory columns");
 
 __device__ __forceinline__ const TcOp& op_at(const TcProgram& p, int i) {
   return p.ops ? p.ops[i] : p.inline_ops[i];
@@ -375,8 +393,9 @@ __device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, cons
     }
   }
   wk.U = static_cast<long>(wk.n_tiles) * wk.nkb;
-  wk.G = static_cast<int>(min(static_cast<long>(gridDim.x), wk.U));
-  const int b = blockIdx.x;
+  wk.G = static_cast<int>(min(static_cast<long>(a.n_ctas), wk.U));
+  wk.cta0 = a.cta0;
+  const int b = wk.rel(blockIdx.x);
   const bool active = b < wk.G && !c.aborted();
   u0 = active ? wk.begin(b) : 0;
   u1 = active ? wk.begin(b + 1) : 0;
@@ -389,9 +408,7 @@ __device__ __forceinline__ void grid_wait(const uint32_t* ctr, uint32_t target, 
                                           volatile int* abort_flag) {
   const unsigned long long t0 = globaltimer();
   while (true) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= target) break;
+    if (ld_acquire_gpu(ctr) >= target) break;
     if (*abort_flag) return;
     if (*reinterpret_cast<volatile uint32_t*>(status) & kStatusTimeout) {
       *abort_flag = 1;
@@ -402,9 +419,8 @@ __device__ __forceinline__ void grid_wait(const uint32_t* ctr, uint32_t target, 
       *abort_flag = 1;
       return;
     }
-    __nanosleep(64);
+    __nanosleep(32);
   }
-  __threadfence();
 }
 
 // Tensor maps of the device op table were written by the host before the
@@ -413,14 +429,115 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
 }
 
+// Activations staged by TMA (dense A, MoE x): K range [kbeg, kbeg + klen)
+// of rows [0, rb) (rows past the tensor read as zero) in the 128-byte
+// swizzled K-block layout, then converted in place BF16 -> FP16 with one
+// power-of-two shift per row (sig), and optionally rms[n] =
+// 1/sqrt(mean x^2 + 1e-6) over the range.  The four epilogue warps; part
+// (64 floats of scratch) collects per-group row statistics in a fixed order.
+__device__ __forceinline__ void stage_tma(const Cta& c, const CUtensorMap* xmap, int rb, int kbeg,
+                                          int klen, int* sig, float* rms, float* part, int ew,
+                                          int lane, uint32_t& xphase) {
+  uint8_t* xs = c.xs();
+  if (ew == 0) {
+    // the activations were written by generic stores (of other CTAs, ordered
+    // before us by the completion counters): order them before the copy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(c.x_tma(), static_cast<uint32_t>(rb * klen * 2));
+    __syncwarp();
+    for (int j = lane; j < klen / 64; j += 32)
+      tma_load_2d_nohint(xs + j * rb * 128, xmap, kbeg + 64 * j, 0, c.x_tma());
+  }
+  wait_bar(c.x_tma(), xphase, c.status(), c.abort_flag());
+  xphase ^= 1u;
+  const int etid = ew * 32 + lane;
+  const int g = etid >> 3;                          // 8-thread group: one 128-byte line
+  const int n_it = rb * klen / (8 * kEpiThreads);   // 16-byte chunks per thread (even)
+  // chunk etid + 128 i lies in line etid / 8 + 16 i: row (g + 16 i) % rb
+  float mx[2] = {0.0f, 0.0f}, sq[2] = {0.0f, 0.0f};
+  for (int i0 = 0; i0 < n_it; i0 += 4) {  // n_it is even; 4 (or 2) chunks in flight
+    uint4 v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (i0 + t < n_it) v[t] = *reinterpret_cast<const uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t)));
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (i0 + t < n_it) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[t]);
+        float m = 0.0f, s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float f = __bfloat162float(e[j]);
+          m = fmaxf(m, fabsf(f));
+          s = fmaf(f, f, s);
+        }
+        mx[t & 1] = fmaxf(mx[t & 1], m);
+        sq[t & 1] += s;
+      }
+  }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+      sq[h] += __shfl_xor_sync(0xffffffffu, sq[h], o);
+    }
+  }
+  if ((lane & 7) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      part[2 * (2 * g + h)] = mx[h];
+      part[2 * (2 * g + h) + 1] = sq[h];
+    }
+  }
+  esync();
+  if (etid < rb) {
+    float m = 0.0f, s = 0.0f;
+    for (int gg = 0; gg < kEpiThreads / 8; ++gg)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if ((gg + 16 * h) % rb == etid) {
+          m = fmaxf(m, part[2 * (2 * gg + h)]);
+          s += part[2 * (2 * gg + h) + 1];
+        }
+    sig[etid] = f16_row_shift(m);
+    if (rms) rms[etid] = rsqrtf(s / static_cast<float>(klen) + 1e-6f);
+  }
+  esync();
+  const int sh0 = sig[g % rb], sh1 = sig[(g + 16) % rb];
+  for (int i0 = 0; i0 < n_it; i0 += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (i0 + t < n_it) v[t] = *reinterpret_cast<const uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t)));
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (i0 + t < n_it) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[t]);
+        const int sh = (t & 1) ? sh1 : sh0;
+        uint32_t pk[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          pk[j] = pack_f16x2(scale_pow2(__bfloat162float(e[2 * j]), sh),
+                             scale_pow2(__bfloat162float(e[2 * j + 1]), sh));
+        *reinterpret_cast<uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t))) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+  }
+}
+
 // ------------------------------------------------------------ roles, per op
 
+// (The producer and epilogue bodies are not inlined: with every role inlined
+// into the kernel, nvcc 13.0's device front end crashes on this file now and
+// then; the decode and MMA loops are inlined, which measurably matters.)
+//
 // The producer warp, one op.  Converged like the MMA warp: lane 0 waits for
 // a free ring stage, one elected lane issues the copies.  Dense and down
 // tiles are 128 consecutive weight rows: one box of codes and one of scales
 // per stage; a gate_up tile is four 32-row boxes.
 template <int MODE>
-__device__ __forceinline__ void produce_op(const Cta& c, const TcOp& op, bool table, int lane,
+__device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table, int lane,
                                            SchedCursor& cur, int& stage, uint32_t& phase,
                                            long& issued, uint64_t pol) {
   const TcArgs& a = op.a;
@@ -493,7 +610,6 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   XState xst;
   const uint32_t xs_addr = smem_u32(c.xs());
-  const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
   for (long u = u0; u < u1;) {
     if (__any_sync(0xffffffffu, c.aborted())) break;
     const int tile = static_cast<int>(u / wk.nkb);
@@ -502,6 +618,8 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
     const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32);
+    const int rb = tc_xrows(nr);
+    const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
     for (int w0 = kbs; w0 < kbe;) {
       const int w1 = window_end(kk, w0, kbe);
       if (!xst.covers(key, w0, w1)) {
@@ -511,8 +629,8 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
         __syncwarp();
         ++xcount;
       }
-      const uint32_t db = dcount & 1u;
-      if (lane == 0) wait_bar(c.d_empty_at(db), ((dcount >> 1) & 1u) ^ 1u, c.status(), c.abort_flag());
+      const uint32_t db = dcount % kDBufs;
+      if (lane == 0) wait_bar(c.d_empty_at(db), ((dcount / kDBufs) & 1u) ^ 1u, c.status(), c.abort_flag());
       __syncwarp();
       const uint32_t d_t = c.tmem + kDCol + 32u * db;
       for (int kb = w0; kb < w1; ++kb) {
@@ -524,14 +642,17 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
         if (tc::elect_one()) {
           if (run) {
             const uint32_t a_t = c.tmem + kACols * ab;
-            const uint64_t b0 =
-                tc::smem_desc(xs_addr + static_cast<uint32_t>(kb - xst.k0) * 4096u, sbo);
-            // K step j: A columns + 8 j, B start address + 256 j bytes (+16 j in
-            // the descriptor's address field, which cannot carry: < 256 KB)
+            // stage kb = four 64-element K-blocks of rb rows; K step j: A
+            // columns + 8 j, B block j / 4 at + 32 (j % 4) bytes (descriptor
+            // address field in 16-byte units; no carry: < 256 KB)
+            const uint64_t b0 = tc::smem_desc_sw128(
+                xs_addr + static_cast<uint32_t>((kb - xst.k0) * 4 * rb * 128), sbo);
+            const uint32_t blk = static_cast<uint32_t>(rb * 128 / 16);
             tc::mma_f16_ts(d_t, a_t, b0, idesc, kb > w0 ? 1u : 0u);
 #pragma unroll
             for (int j = 1; j < kSK / 16; ++j)
-              tc::mma_f16_ts(d_t, a_t + 8 * j, b0 + static_cast<uint64_t>(16 * j), idesc, 1u);
+              tc::mma_f16_ts(d_t, a_t + 8 * j, b0 + static_cast<uint64_t>((j >> 2) * blk + 2 * (j & 3)),
+                             idesc, 1u);
           }
           tc::commit(c.a_empty_at(ab));
         }
@@ -610,7 +731,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 // (Not inlined: each mode gets its own register allocation.)
 template <int MODE>
 __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
-                                         int ew, int lane, uint32_t& dcount) {
+                                         int ew, int lane, uint32_t& dcount, uint32_t& xphase) {
   const TcArgs& a = op.a;
   const int q = (kEpiWarp0 + ew) & 3;
   const int etid = ew * 32 + lane;
@@ -632,22 +753,31 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
     for (int i = etid; i < a.T * a.H; i += kEpiThreads)
       a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
   }
-  // dense: the RMS factor of each row over the whole K
-  if (MODE == kTcDense && a.rms && u0 < u1) {
+  // dense staged in windows shorter than K: the RMS factor of each row over
+  // the whole K, 8 loads a lane in flight (with one window covering K it
+  // comes from the staging pass)
+  if (MODE == kTcDense && a.rms && a.win_k < a.K && u0 < u1) {
     for (int m = ew; m < a.M; m += kEpiWarps) {
       float ss = 0.0f;
       const __nv_bfloat16* row = a.A + m * a.lda;
-      for (int v = lane; v < a.K / 8; v += 32) {
-        const uint4 uu = *reinterpret_cast<const uint4*>(row + v * 8);
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&uu);
+      for (int v0 = 0; v0 < a.K / 8; v0 += 8 * 32) {
+        uint4 buf[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(static_cast<float>(e[i]), static_cast<float>(e[i]), ss);
+        for (int i = 0; i < 8; ++i) {
+          const int v = v0 + 32 * i + lane;
+          buf[i] = v < a.K / 8 ? *reinterpret_cast<const uint4*>(row + v * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&buf[i]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ss = fmaf(static_cast<float>(e[j]), static_cast<float>(e[j]), ss);
+        }
       }
       ss = warp_sum(ss);
       if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
     }
   }
-  const uint32_t sbo = static_cast<uint32_t>(a.win_k) * 16u;
   XState xst;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
   const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
@@ -659,7 +789,7 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
     const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
-    const int npad = nr <= 16 ? 16 : 32;
+    const int rb = tc_xrows(nr);
     float tot[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
@@ -674,14 +804,12 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
         if (MODE == kTcDown) {
           const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
           const int I = a.I;
-          stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, npad,
-                         kbeg, klen, c.xs(), sbo, sig, nullptr, ew, lane, kEpiWarps);
+          stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
+                         kbeg, klen, c.xs(), sig, nullptr, ew, lane, kEpiWarps);
         } else {
-          const __nv_bfloat16* base = (MODE == kTcDense) ? a.A : a.x;
-          const int64_t ld = (MODE == kTcDense) ? a.lda : a.ldx;
-          stage_b<__nv_bfloat16>([&](int n) { return base + n * ld; }, nr, npad, kbeg, klen,
-                                 c.xs(), sbo, sig, (MODE == kTcGateUp && a.rms) ? rms : nullptr,
-                                 ew, lane, kEpiWarps);
+          const bool want_rms = a.rms && (MODE == kTcGateUp || a.win_k >= a.K);
+          stage_tma(c, &op.xmap, rb, kbeg, klen, sig, want_rms ? rms : nullptr, ep, ew, lane,
+                    xphase);
         }
         fence_proxy_async_smem();
         esync();
@@ -689,8 +817,8 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
         if (lane == 0) mbar_arrive(c.x_full());
       }
       // ---- fold the window's accumulator into the segment total
-      const uint32_t db = dcount & 1u;
-      wait_bar(c.d_full_at(db), (dcount >> 1) & 1u, c.status(), c.abort_flag());
+      const uint32_t db = dcount % kDBufs;
+      wait_bar(c.d_full_at(db), (dcount / kDBufs) & 1u, c.status(), c.abort_flag());
       tc::fence_after_sync();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -720,10 +848,10 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
       const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
       if (etid == 0) {
-        __threadfence();  // the CTA's partial (ordered before by the barrier) is visible
-        const uint32_t prev = atomicAdd(&a.tile_cnt[tile], 1u);
+        // releases the CTA's partial (ordered before by the barrier); the last
+        // adder acquires the others'
+        const uint32_t prev = atom_add_acq_rel_gpu(&a.tile_cnt[tile], 1u);
         *bcast = (prev == static_cast<uint32_t>(bhi - blo)) ? 1 : 0;
-        if (*bcast) __threadfence();
       }
       esync();
       if (!*bcast) continue;  // uniform across the epilogue warps
@@ -731,7 +859,7 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
       for (int bb = blo; bb <= bhi; ++bb) {
         const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
-        const float* pp = a.partials + static_cast<size_t>(bb * 2 + sl) * (32 * kRows);
+        const float* pp = a.partials + static_cast<size_t>(wk.abs_cta(bb) * 2 + sl) * (32 * kRows);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j < nr) tot[j] += __ldcg(pp + j * kRows + r);
@@ -770,10 +898,8 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       if (a.argmax_out) {
         esync();
         if (etid == 0) {
-          __threadfence();
-          const uint32_t prev = atomicAdd(a.argmax_cnt, 1u);
+          const uint32_t prev = atom_add_acq_rel_gpu(a.argmax_cnt, 1u);
           *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
-          if (*bcast) __threadfence();
         }
         esync();
         if (*bcast) {
@@ -830,10 +956,10 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       esync();
       uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
       if (etid == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(&col_cnt[nt], 1u);
+        // releases this tile's outputs; the last expert of the slice acquires
+        // the others'
+        const uint32_t prev = atom_add_acq_rel_gpu(&col_cnt[nt], 1u);
         *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
-        if (*bcast) __threadfence();
       }
       esync();
       if (*bcast) {
@@ -956,7 +1082,7 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
   const int ew = warp - kEpiWarp0, etid = ew * 32 + lane;
   const int n_ops = prog.n_ops;
   SchedCursor cur;
-  uint32_t dcount = 0;
+  uint32_t dcount = 0, xphase = 0;
   // inputs may come from the previous kernel on the stream
   pdl_wait();
   pdl_launch_dependents();
@@ -968,22 +1094,20 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
       esync();
     }
     switch (op.mode) {
-      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount); break;
-      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount); break;
-      default: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount); break;
+      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount, xphase); break;
+      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount, xphase); break;
+      default: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount, xphase); break;
     }
     if (n_ops > 1) {
       esync();
       if (etid == 0) {
-        __threadfence();
-        atomicAdd(&prog.done[i], 1u);
+        red_add_release_gpu(&prog.done[i], 1u);
       }
     }
   }
   if (n_ops > 1 && etid == 0) {
     // the last CTA to leave returns the completion counters to zero
-    __threadfence();
-    if (atomicAdd(&prog.done[n_ops], 1u) == gridDim.x - 1) {
+    if (atom_add_acq_rel_gpu(&prog.done[n_ops], 1u) == gridDim.x - 1) {
       for (int i = 0; i <= n_ops; ++i) prog.done[i] = 0u;
       __threadfence();
     }
@@ -1028,14 +1152,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(c.a_full_at(b), kDecWarps);
       mbar_init(c.a_empty_at(b), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kDBufs; ++b) {
       mbar_init(c.d_full_at(b), 1);
       mbar_init(c.d_empty_at(b), kEpiWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(c.sched_full_at(b), 1);
       mbar_init(c.sched_empty_at(b), kSchedUsers);
     }
     mbar_init(c.x_full(), kEpiWarps);
     mbar_init(c.mma_done(), 1);
+    mbar_init(c.x_tma(), 1);
     fence_mbarrier_init();
     *c.abort_flag() = 0;
   }

@@ -100,5 +100,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo) {
   return d;
 }
 
+// Shared-memory descriptor of a K-major operand with the 128-byte swizzle,
+// as TMA writes it with CU_TENSOR_MAP_SWIZZLE_128B: rows of 64 16-bit
+// elements (128 bytes), 8-row atoms of 1024 bytes (1024-byte aligned), sbo =
+// distance between 8-row groups (1024, or 0 to repeat the first 8 rows).  K
+// steps of 16 elements inside an atom add 32 bytes to the start address; the
+// leading-dimension field is unused; layout code 2 (bits 61..63) = 128-byte
+// swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 }  // namespace tc
 }  // namespace nvfp4

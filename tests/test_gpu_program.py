@@ -1,7 +1,13 @@
 """GPU checks of programs (a chain of GEMM / MoE calls in one persistent
-launch): results bit-identical to the same calls issued one by one (which the
-other files check against the float64 oracle), one chain also checked against
-the oracle directly, and the workspace counters back at zero afterwards."""
+launch).  With every op spread over every SM (NVFP4_PROGRAM_TARGET_STAGES=0)
+a program splits the work exactly like the single calls, and its results are
+bit-identical to the same calls issued one by one (which the other files
+check against the float64 oracle).  With the default placement (small dense
+ops on a rotating subset of SMs, fewer split-K partial sums) results are
+checked against the oracle, teacher-forced op by op.  The workspace counters
+are back at zero after every launch."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -25,13 +31,25 @@ def _lib():
     assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
 
 
+@pytest.fixture
+def every_sm():
+    """Programs created inside the test spread every op over every SM."""
+    old = os.environ.get("NVFP4_PROGRAM_TARGET_STAGES")
+    os.environ["NVFP4_PROGRAM_TARGET_STAGES"] = "0"
+    yield
+    if old is None:
+        del os.environ["NVFP4_PROGRAM_TARGET_STAGES"]
+    else:
+        os.environ["NVFP4_PROGRAM_TARGET_STAGES"] = old
+
+
 def _counters_zero(ws):
     torch.cuda.synchronize()
     hdr = ws.buf[:256 + 4 * 16384].view(torch.int32)
     return int(hdr[1:].abs().sum().item()) == 0 and int(hdr[0].item()) == 0
 
 
-def test_single_gemm_program_equals_call():
+def test_single_gemm_program_equals_call(every_sm):
     W = device_weight(11, 3000, 2048)
     a = synth.activations_bf16(11, 8, 2048).cuda()
     ref = ops.gemm(a, W)
@@ -45,7 +63,7 @@ def test_single_gemm_program_equals_call():
 
 
 @pytest.mark.parametrize("m", [1, 8, 32])
-def test_gemm_chain_equals_calls_and_oracle(m):
+def test_gemm_chain_equals_calls_and_oracle(m, every_sm):
     """x -> (rms) W1 [4096 x 2048] -> (rms) W2 [2048 x 4096] -> W3 [1000 x 2048] + argmax."""
     W1 = device_weight(12, 4096, 2048)
     W2 = device_weight(13, 2048, 4096)
@@ -79,7 +97,7 @@ def layer():
 
 
 @pytest.mark.parametrize("t", [1, 8, 32])
-def test_moe_in_program_equals_call(layer, t):
+def test_moe_in_program_equals_call(layer, t, every_sm):
     ex, sh = layer
     x = synth.activations_bf16(21, t, 2048).cuda()
     ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
@@ -102,7 +120,7 @@ def test_moe_in_program_equals_call(layer, t):
     assert _counters_zero(prog.workspace)
 
 
-def test_two_moe_layers_share_schedule_slots(layer):
+def test_two_moe_layers_share_schedule_slots(layer, every_sm):
     """Four MoE layers in a row cycle both schedule slots twice."""
     ex, sh = layer
     t = 8
@@ -129,7 +147,7 @@ def test_two_moe_layers_share_schedule_slots(layer):
 
 
 @pytest.mark.parametrize("tokens", [1, 8])
-def test_decode_step_program_equals_calls(tokens):
+def test_decode_step_program_equals_calls(tokens, every_sm):
     m = DecodeStep(seed=6, shape=StepShape(layers=3))
     b = m.buffers(tokens, keep=True)
     x, lg = m.inputs(tokens)
@@ -153,3 +171,63 @@ def test_decode_step_program_equals_calls(tokens):
     assert torch.equal(b["head"], ref_head) and torch.equal(b["argmax"], ref_am)
     assert b["ws"].status() == 0
     assert _counters_zero(b["ws"])
+
+
+@pytest.mark.parametrize("m", [1, 8, 17, 32])
+def test_default_placement_chain_against_oracle(m):
+    """Default placement: QKV-, O- and head-shaped GEMMs chained, each checked
+    against the oracle from its own (program-written) input."""
+    W1 = device_weight(31, 5120, 2048)
+    W2 = device_weight(32, 2048, 4096)
+    W3 = device_weight(33, 3000, 2048)
+    x = synth.activations_bf16(31, m, 2048).cuda()
+    p1 = torch.empty(m, 5120, dtype=torch.bfloat16, device="cuda")
+    p2 = torch.empty(m, 2048, dtype=torch.bfloat16, device="cuda")
+    p3 = torch.empty(m, 3000, dtype=torch.bfloat16, device="cuda")
+    am = torch.empty(m, dtype=torch.int32, device="cuda")
+    prog = ops.Program([ops.gemm_op(x, W1, p1, rms_input=True),
+                        ops.gemm_op(p1[:, :4096], W2, p2, rms_input=True),
+                        ops.gemm_op(p2, W3, p3, argmax_out=am, rms_input=True)])
+    prog.launch()
+    prog.launch()
+    torch.cuda.synchronize()
+    assert prog.workspace.status() == 0
+    assert _counters_zero(prog.workspace)
+    assert_close(f64(p1), O.gemm_bf16(O.rms_scale(f64(x)), *host_weight(31, 5120, 2048)), "QKV")
+    assert_close(f64(p2), O.gemm_bf16(O.rms_scale(f64(p1)[:, :4096]), *host_weight(32, 2048, 4096)),
+                 "O")
+    assert_close(f64(p3), O.gemm_bf16(O.rms_scale(f64(p2)), *host_weight(33, 3000, 2048)), "head")
+    assert np.array_equal(am.cpu().numpy(), O.argmax_first(f64(p3), axis=1))
+
+
+def test_default_placement_decode_step_against_oracle():
+    """Default placement, 3-layer step at T=8: every layer's QKV, O and MoE
+    from its own inputs, and the head, against the oracle."""
+    from helpers import host_expert_fn
+    from moe_expert_nvfp4_gb300.decode_step import ROLE_HEAD, ROLE_O, ROLE_QKV
+    t = 8
+    m = DecodeStep(seed=6, shape=StepShape(layers=3))
+    s = m.s
+    b = m.buffers(t, keep=True)
+    x, lg = m.inputs(t)
+    b["x"].copy_(x)
+    b["logits"].copy_(lg)
+    prog = m.program(b)
+    m.run_program(b, prog)
+    torch.cuda.synchronize()
+    assert b["ws"].status() == 0
+    for l in range(s.layers):
+        xin = f64(b["x"] if l == 0 else b["y"][l - 1])
+        q = f64(b["q"][l])
+        assert_close(q, O.gemm_bf16(O.rms_scale(xin), *host_weight(6, s.qkv_out, s.hidden, ROLE_QKV, l)),
+                     f"layer {l} QKV")
+        o = f64(b["o"][l])
+        assert_close(o, O.gemm_bf16(O.rms_scale(q[:, :s.o_in]),
+                                    *host_weight(6, s.hidden, s.o_in, ROLE_O, l)), f"layer {l} O")
+        get = host_expert_fn(6, l, s.hidden, s.inter)
+        ids = b["ids"][l * t:(l + 1) * t].cpu().numpy()
+        w = b["w"][l * t:(l + 1) * t].cpu().double().numpy()
+        y_ref = O.moe_decode_bf16(O.rms_scale(o), ids, w, get, s.num_experts, get(s.num_experts))
+        assert_close(f64(b["y"][l]), y_ref, f"layer {l} MoE")
+    head = f64(b["head"])
+    assert np.array_equal(b["argmax"].cpu().numpy(), O.argmax_first(head, axis=1))
