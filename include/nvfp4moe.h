@@ -188,7 +188,8 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
  * NVFP4_FLAG_RMS_INPUT per op (NVFP4_FLAG_NO_PDL and NVFP4_FLAG_IDS_READY are
  * accepted and ignored).  Every MoE op's topk_ids / topk_w must be complete
  * before the launch (e.g. routed earlier on the stream).  Limits as for the
- * single calls; at most 4,095 kernel ops (a MoE op counts two).
+ * single calls; at most 4,095 kernel ops (a MoE op counts three: gate_up,
+ * down, combine).
  *
  * nvfp4_program_create validates every op, encodes its tensor maps, and
  * copies the op table to device memory: the one call of this library that

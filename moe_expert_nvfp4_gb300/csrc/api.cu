@@ -371,7 +371,7 @@ int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* 
 int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const float* topk_w,
                int k, const nvfp4_expert_stack* experts, const nvfp4_expert_stack* shared,
                void* out, int64_t ldo, uint32_t flags, uint8_t* ws, const TcMoePlan& p,
-               TcOp* gu, TcOp* dn) {
+               TcOp* gu, TcOp* dn, TcOp* cb) {
   const int E = experts->num_experts, H = experts->hidden, I = experts->inter;
   const nvfp4_expert_stack* sh = shared ? shared : experts;
   memset(gu, 0, sizeof(*gu));
@@ -420,7 +420,9 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   dn->a.win_k = I;
   dn->mode = kTcDown;
   dn->new_sched = 0;
-  dn->last_sched_use = 1;
+  *cb = *dn;  // the combine reads the down op's per-pair outputs; no weights
+  cb->mode = kTcCombine;
+  cb->last_sched_use = 1;
   return NVFP4_OK;
 }
 
@@ -635,9 +637,9 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
       return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
     if ((rc = get_encoder())) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    TcOp gu, dn;
+    TcOp gu, dn, cb;
     if ((rc = tc_moe_ops(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo, flags, ws, p,
-                         &gu, &dn)))
+                         &gu, &dn, &cb)))
       return rc;
     const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -648,12 +650,18 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
         (rc = tc_launch_one(dn, static_cast<size_t>(p.xrows) * I * 2, p.sched_bytes, p.grid, ws,
                             s, pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
       return rc;
+    int st_cb = 0;
+    size_t sm_cb = 0;
+    if ((rc = tc_launch_one(cb, 0, p.sched_bytes, p.grid, ws, s, pdl, &st_cb, &sm_cb,
+                            "stream_tc_kernel<combine> launch")))
+      return rc;
     char buf[256];
     snprintf(buf, sizeof(buf),
              "stream_tc_kernel<gate_up> grid=%d stages=%d smem=%zu; stream_tc_kernel<down> grid=%d "
-             "stages=%d smem=%zu; T=%d k=%d E=%d n=%d shared=%d rms=%d ids_ready=%d",
-             p.grid, st_gu, sm_gu, p.grid, st_dn, sm_dn, T, k, E, p.npad, gu.a.has_shared,
-             gu.a.rms, gu.a.ids_ready);
+             "stages=%d smem=%zu; stream_tc_kernel<combine> grid=%d; T=%d k=%d E=%d n=%d "
+             "shared=%d rms=%d ids_ready=%d",
+             p.grid, st_gu, sm_gu, p.grid, st_dn, sm_dn, p.grid, T, k, E, p.npad,
+             gu.a.has_shared, gu.a.rms, gu.a.ids_ready);
     g_dispatch = buf;
     return NVFP4_OK;
   }
@@ -796,12 +804,13 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
       TcMoePlan p;
       if (!plan_tc_moe(o.T, o.k, E, H, I, sms, &p))
         return fail(NVFP4_ERR_SHAPE, "op %d: T=%d, H=%d, E=%d: no feasible plan", i, o.T, H, E);
-      TcOp gu, dn;
+      TcOp gu, dn, cb;
       if ((rc = tc_moe_ops(o.x, o.ldx, o.T, o.topk_ids, o.topk_w, o.k, &o.experts, sh, o.out,
-                           o.ldo, o.flags | NVFP4_FLAG_IDS_READY, ws, p, &gu, &dn)))
+                           o.ldo, o.flags | NVFP4_FLAG_IDS_READY, ws, p, &gu, &dn, &cb)))
         return rc;
       table.push_back(gu);
       table.push_back(dn);
+      table.push_back(cb);
       x_bytes = std::max(x_bytes, p.x_bytes);
       sched_bytes = std::max(sched_bytes, p.sched_bytes);
       need = std::max(need, p.ws_bytes);

@@ -87,13 +87,15 @@ constexpr int kTcOffMisc = 512;
 constexpr int kTcOffEp = 1024;
 constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17408
 constexpr int kTcThreads = 480;   // producer, MMA, 8 decode, 4 epilogue warps, scheduler warp
-constexpr int kTcColCntBase = 8192;                      // down combine counters
+constexpr int kTcColCntBase = 8192;                      // tile counters stay below this index
 constexpr int kTcDoneBase = 12288;                       // per-op completion counters
 constexpr int kTcMaxOps = kWsMaxCounters - kTcDoneBase - 1;
 constexpr int kTcMaxWinK = 2048;                         // activations staged per window
 constexpr int kTcInlineOps = 1;                          // ops passed by value in the launch
 
-enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2 };
+// kTcCombine: the weighted top-k combine of a MoE layer's per-pair down
+// outputs (no weights: only the epilogue warps work).
+enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2, kTcCombine = 3 };
 
 struct TcArgs {
   // dense

@@ -748,11 +748,6 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
   float* ep = c.ep();
   volatile int* bcast = c.bcast();
 
-  if (MODE == kTcDown && wk.n_tiles == 0 && b == 0 && !c.aborted()) {
-    // nothing routed and no shared expert: the layer output is zero
-    for (int i = etid; i < a.T * a.H; i += kEpiThreads)
-      a.out[(i / a.H) * a.ldo + (i % a.H)] = __float2bfloat16_rn(0.0f);
-  }
   // dense staged in windows shorter than K: the RMS factor of each row over
   // the whole K, 8 loads a lane in flight (with one window covering K it
   // comes from the staging pass)
@@ -953,61 +948,60 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
-      esync();
-      uint32_t* col_cnt = a.tile_cnt + kTcColCntBase;
-      if (etid == 0) {
-        // releases this tile's outputs; the last expert of the slice acquires
-        // the others'
-        const uint32_t prev = atom_add_acq_rel_gpu(&col_cnt[nt], 1u);
-        *bcast = (prev == static_cast<uint32_t>(*sc.n_active - 1)) ? 1 : 0;
-      }
-      esync();
-      if (*bcast) {
-        // the last expert to finish this 128-column slice: weighted combine
-        // in slot order, shared expert last; warp per token, 4 columns a lane
-        const int sh_off = sc.off[a.E];
-        const int n = nt * kRows + 4 * lane;
-        for (int t = ew; t < a.T; t += kEpiWarps) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int j0 = 0; j0 <= a.k; j0 += 8) {
-            float4 yv[8];
-            float wv[8];
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const int j = j0 + jj;
-              yv[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-              wv[jj] = 0.0f;
-              int pr = -1;
-              if (j < a.k) {
-                pr = sc.flat_pair[t * a.k + j];
-                if (pr >= 0) wv[jj] = a.w[t * a.k + j];
-              } else if (j == a.k && a.has_shared) {
-                pr = sh_off + t;
-                wv[jj] = 1.0f;
-              }
-              if (pr >= 0)
-                yv[jj] = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pr) * a.H + n));
-            }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              acc.x = fmaf(wv[jj], yv[jj].x, acc.x);
-              acc.y = fmaf(wv[jj], yv[jj].y, acc.y);
-              acc.z = fmaf(wv[jj], yv[jj].z, acc.z);
-              acc.w = fmaf(wv[jj], yv[jj].w, acc.w);
-            }
-          }
-          __nv_bfloat16* o = a.out + t * a.ldo + n;
-          o[0] = __float2bfloat16_rn(acc.x);
-          o[1] = __float2bfloat16_rn(acc.y);
-          o[2] = __float2bfloat16_rn(acc.z);
-          o[3] = __float2bfloat16_rn(acc.w);
-        }
-        if (etid == 0) col_cnt[nt] = 0u;
-      }
     }
     esync();
   }
   if (MODE != kTcDense) cur.release(c, op, lane == 0);
+}
+
+// The weighted combine of a MoE layer, after every CTA finished its down
+// op: out[t] = sum over slots j (in order) of w[t][j] * y[pair(t, j)], the
+// shared expert last (weight 1); ids outside [0, E) contribute nothing.  The
+// T x H/4 four-column groups are spread over all CTAs, one per thread.
+__device__ __noinline__ void combine_op(const Cta& c, const TcOp& op, SchedCursor& cur, int ew,
+                                        int lane) {
+  const TcArgs& a = op.a;
+  const Sched sc = cur.acquire(c, op);
+  const int etid = ew * 32 + lane;
+  const int groups = a.H / 4;
+  const int items = a.T * groups;
+  const int sh_off = sc.off[a.E];
+  for (int it = blockIdx.x * kEpiThreads + etid; it < items && !c.aborted();
+       it += gridDim.x * kEpiThreads) {
+    const int t = it / groups, n = 4 * (it - t * groups);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 <= a.k; j0 += 8) {
+      float4 yv[8];
+      float wv[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        yv[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[jj] = 0.0f;
+        int pr = -1;
+        if (j < a.k) {
+          pr = sc.flat_pair[t * a.k + j];
+          if (pr >= 0) wv[jj] = a.w[t * a.k + j];
+        } else if (j == a.k && a.has_shared) {
+          pr = sh_off + t;
+          wv[jj] = 1.0f;
+        }
+        if (pr >= 0)
+          yv[jj] = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<size_t>(pr) * a.H + n));
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        acc.x = fmaf(wv[jj], yv[jj].x, acc.x);
+        acc.y = fmaf(wv[jj], yv[jj].y, acc.y);
+        acc.z = fmaf(wv[jj], yv[jj].z, acc.z);
+        acc.w = fmaf(wv[jj], yv[jj].w, acc.w);
+      }
+    }
+    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(a.out + t * a.ldo + n);
+    o[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    o[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  cur.release(c, op, lane == 0);
 }
 
 // ------------------------------------------------------------ roles
@@ -1025,7 +1019,8 @@ __device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& 
     switch (op.mode) {
       case kTcDense: produce_op<kTcDense>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       case kTcGateUp: produce_op<kTcGateUp>(c, op, table, lane, cur, stage, phase, issued, pol); break;
-      default: produce_op<kTcDown>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      case kTcDown: produce_op<kTcDown>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;  // combine: no weights
     }
   }
   // wait for the TMA writes still in flight (bounded, ignores aborts)
@@ -1053,7 +1048,8 @@ __device__ __forceinline__ void mma_role(const TcProgram& prog, const Cta& c, in
     switch (op.mode) {
       case kTcDense: mma_op<kTcDense>(c, op, cur, lane, acount, dcount, xcount); break;
       case kTcGateUp: mma_op<kTcGateUp>(c, op, cur, lane, acount, dcount, xcount); break;
-      default: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount); break;
+      case kTcDown: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount); break;
+      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
     }
   }
   // every MMA has completed before tensor memory is released
@@ -1073,7 +1069,8 @@ __device__ __forceinline__ void decode_role(const TcProgram& prog, const Cta& c,
     switch (op.mode) {
       case kTcDense: decode_op<kTcDense>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcGateUp: decode_op<kTcGateUp>(c, op, cur, warp, lane, acount, rstage, rphase); break;
-      default: decode_op<kTcDown>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      case kTcDown: decode_op<kTcDown>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
     }
   }
 }
@@ -1096,7 +1093,8 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
     switch (op.mode) {
       case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount, xphase); break;
       case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount, xphase); break;
-      default: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount, xphase); break;
+      case kTcDown: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount, xphase); break;
+      default: combine_op(c, op, cur, ew, lane); break;
     }
     if (n_ops > 1) {
       esync();
