@@ -161,6 +161,35 @@ __device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
   return d;
 }
 
+// Two E2M1 values held as FP16 (from cvt.rn.f16x2.e2m1x2: 0 or an FP16
+// normal with at most one mantissa bit) -> the same values times 2^-112 as
+// BF16 (exact): the FP16 exponent field lands in the low five bits of the
+// BF16 exponent field (bias 15 read against 127), zero stays zero.
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t v) {
+  return ((v >> 3) & 0x0FFF0FFFu) | (v & 0x80008000u);
+}
+
+// One E4M3 byte times 2^112 as BF16, broadcast to both halves (exact: E4M3
+// values 2^-9 .. 448 become 2^103 .. 448 * 2^112 < 2^128).
+__device__ __forceinline__ uint32_t e4m3_bcast_bf16x2_x2p112(uint32_t byte) {
+  const uint16_t two = static_cast<uint16_t>((byte & 0xFFu) * 0x0101u);
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  float f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f) : "r"(h2));
+  f *= 5.192296858534828e+33f;  // 2^112
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(f));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

@@ -68,6 +68,14 @@ constexpr int kABufs = 3;                      // A operand buffers in tensor me
 constexpr int kACols = kSK / 2;                // tensor-memory columns per A buffer
 constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384, 416, 448, 480
 constexpr int kDBufs = 4;                      // accumulator buffers (32 columns each)
+
+// Operand type of the MMAs: dense and gate_up multiply BF16 activations (as
+// staged, unconverted) by weights decoded to BF16; down multiplies the FP32 h
+// brought to FP16 (power-of-two shift per row) by weights decoded to FP16.
+// Both decodes are exact: a code x scale product has at most 6 significant
+// bits and lies in [2^-10, 2688].
+template <int MODE>
+constexpr bool kBf16Operands = MODE != kTcDown;
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
@@ -430,14 +438,11 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
 }
 
 // Activations staged by TMA (dense A, MoE x): K range [kbeg, kbeg + klen)
-// of rows [0, rb) (rows past the tensor read as zero) in the 128-byte
-// swizzled K-block layout, then converted in place BF16 -> FP16 with one
-// power-of-two shift per row (sig), and optionally rms[n] =
-// 1/sqrt(mean x^2 + 1e-6) over the range.  The four epilogue warps; part
-// (64 floats of scratch) collects per-group row statistics in a fixed order.
+// of rows [0, rb) (rows past the tensor read as zero) as BF16 in the 128-byte
+// swizzled K-block layout, used by the MMA as they are (sig = 0).  The four
+// epilogue warps; returns when the copy has landed.
 __device__ __forceinline__ void stage_tma(const Cta& c, const CUtensorMap* xmap, int rb, int kbeg,
-                                          int klen, int* sig, float* rms, float* part, int ew,
-                                          int lane, uint32_t& xphase) {
+                                          int klen, int* sig, int ew, int lane, uint32_t& xphase) {
   uint8_t* xs = c.xs();
   if (ew == 0) {
     // the activations were written by generic stores (of other CTAs, ordered
@@ -448,63 +453,22 @@ __device__ __forceinline__ void stage_tma(const Cta& c, const CUtensorMap* xmap,
     for (int j = lane; j < klen / 64; j += 32)
       tma_load_2d_nohint(xs + j * rb * 128, xmap, kbeg + 64 * j, 0, c.x_tma());
   }
+  if (ew * 32 + lane < kMaxM) sig[ew * 32 + lane] = 0;
   wait_bar(c.x_tma(), xphase, c.status(), c.abort_flag());
   xphase ^= 1u;
+}
+
+// rms[n] = 1/sqrt(mean x^2 + 1e-6) of the rb staged BF16 rows (klen each),
+// from shared memory while the MMAs run.  Chunk etid + 128 i (16 bytes)
+// lies in line etid / 8 + 16 i: row (g + 16 i) % rb; per-group sums are
+// reduced in a fixed order (part: 64 floats of scratch).
+__device__ __forceinline__ void staged_rms(const Cta& c, int rb, int klen, float* rms, float* part,
+                                           int ew, int lane) {
+  const uint8_t* xs = c.xs();
   const int etid = ew * 32 + lane;
-  const int g = etid >> 3;                          // 8-thread group: one 128-byte line
-  const int n_it = rb * klen / (8 * kEpiThreads);   // 16-byte chunks per thread (even)
-  // chunk etid + 128 i lies in line etid / 8 + 16 i: row (g + 16 i) % rb
-  float mx[2] = {0.0f, 0.0f}, sq[2] = {0.0f, 0.0f};
-  for (int i0 = 0; i0 < n_it; i0 += 4) {  // n_it is even; 4 (or 2) chunks in flight
-    uint4 v[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (i0 + t < n_it) v[t] = *reinterpret_cast<const uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t)));
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (i0 + t < n_it) {
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[t]);
-        float m = 0.0f, s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float f = __bfloat162float(e[j]);
-          m = fmaxf(m, fabsf(f));
-          s = fmaf(f, f, s);
-        }
-        mx[t & 1] = fmaxf(mx[t & 1], m);
-        sq[t & 1] += s;
-      }
-  }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
-      sq[h] += __shfl_xor_sync(0xffffffffu, sq[h], o);
-    }
-  }
-  if ((lane & 7) == 0) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      part[2 * (2 * g + h)] = mx[h];
-      part[2 * (2 * g + h) + 1] = sq[h];
-    }
-  }
-  esync();
-  if (etid < rb) {
-    float m = 0.0f, s = 0.0f;
-    for (int gg = 0; gg < kEpiThreads / 8; ++gg)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if ((gg + 16 * h) % rb == etid) {
-          m = fmaxf(m, part[2 * (2 * gg + h)]);
-          s += part[2 * (2 * gg + h) + 1];
-        }
-    sig[etid] = f16_row_shift(m);
-    if (rms) rms[etid] = rsqrtf(s / static_cast<float>(klen) + 1e-6f);
-  }
-  esync();
-  const int sh0 = sig[g % rb], sh1 = sig[(g + 16) % rb];
+  const int g = etid >> 3;
+  const int n_it = rb * klen / (8 * kEpiThreads);  // even
+  float sq[2] = {0.0f, 0.0f};
   for (int i0 = 0; i0 < n_it; i0 += 4) {
     uint4 v[4];
 #pragma unroll
@@ -514,16 +478,34 @@ __device__ __forceinline__ void stage_tma(const Cta& c, const CUtensorMap* xmap,
     for (int t = 0; t < 4; ++t)
       if (i0 + t < n_it) {
         const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[t]);
-        const int sh = (t & 1) ? sh1 : sh0;
-        uint32_t pk[4];
+        float s = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          pk[j] = pack_f16x2(scale_pow2(__bfloat162float(e[2 * j]), sh),
-                             scale_pow2(__bfloat162float(e[2 * j + 1]), sh));
-        *reinterpret_cast<uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t))) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int j = 0; j < 8; ++j) {
+          const float f = __bfloat162float(e[j]);
+          s = fmaf(f, f, s);
+        }
+        sq[t & 1] += s;
       }
   }
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) {
+    sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], o);
+    sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], o);
+  }
+  if ((lane & 7) == 0) {
+    part[2 * g] = sq[0];
+    part[2 * g + 1] = sq[1];
+  }
+  esync();
+  if (etid < rb) {
+    float s = 0.0f;
+    for (int gg = 0; gg < kEpiThreads / 8; ++gg)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        if ((gg + 16 * h) % rb == etid) s += part[2 * gg + h];
+    rms[etid] = rsqrtf(s / static_cast<float>(klen) + 1e-6f);
+  }
+  esync();
 }
 
 // ------------------------------------------------------------ roles, per op
@@ -617,7 +599,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
-    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32);
+    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, kBf16Operands<MODE>);
     const int rb = tc_xrows(nr);
     const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
     for (int w0 = kbs; w0 < kbe;) {
@@ -700,16 +682,30 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
-      const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
-      const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
       const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
       uint32_t v[16];
+      if (kBf16Operands<MODE>) {
+        // code (x 2^-112, BF16) times scale (x 2^112, BF16): exact
+        const uint32_t s_lo = e4m3_bcast_bf16x2_x2p112(sw & 0xFFu);
+        const uint32_t s_hi = e4m3_bcast_bf16x2_x2p112((sw >> 8) & 0xFFu);
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-        const uint32_t sv = wi < 2 ? s_lo : s_hi;
+        for (int wi = 0; wi < 4; ++wi) {
+          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+          const uint32_t sv = wi < 2 ? s_lo : s_hi;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
+          for (int e = 0; e < 4; ++e)
+            v[4 * wi + e] = hmul2_bf16(f16x2_to_bf16x2_scaled(v[4 * wi + e]), sv);
+        }
+      } else {
+        const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
+        const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+          const uint32_t sv = wi < 2 ? s_lo : s_hi;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
+        }
       }
       tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
     }
@@ -802,14 +798,15 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
           stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
                          kbeg, klen, c.xs(), sig, nullptr, ew, lane, kEpiWarps);
         } else {
-          const bool want_rms = a.rms && (MODE == kTcGateUp || a.win_k >= a.K);
-          stage_tma(c, &op.xmap, rb, kbeg, klen, sig, want_rms ? rms : nullptr, ep, ew, lane,
-                    xphase);
+          stage_tma(c, &op.xmap, rb, kbeg, klen, sig, ew, lane, xphase);
         }
         fence_proxy_async_smem();
         esync();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.x_full());
+        // the RMS factors of a single window covering K, while the MMAs run
+        if (MODE != kTcDown && a.rms && (MODE == kTcGateUp || a.win_k >= a.K))
+          staged_rms(c, rb, klen, rms, ep, ew, lane);
       }
       // ---- fold the window's accumulator into the segment total
       const uint32_t db = dcount % kDBufs;

@@ -80,10 +80,12 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor of kind::f16: D f32, A and B f16, both K-major,
-// M = 128, N = n (multiple of 16).
-__device__ __forceinline__ uint32_t idesc_f16(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+// Instruction descriptor of kind::f16: D f32, A and B f16 (or both bf16:
+// format code 1 in bits 7..9 and 10..12), both K-major, M = 128, N = n
+// (multiple of 16).
+__device__ __forceinline__ uint32_t idesc_f16(int n, bool bf16 = false) {
+  return (1u << 4) | (bf16 ? ((1u << 7) | (1u << 10)) : 0u) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
 // Shared-memory descriptor of a K-major operand without swizzle, stored as
