@@ -69,13 +69,11 @@ constexpr int kACols = kSK / 2;                // tensor-memory columns per A bu
 constexpr int kDCol = kABufs * kACols;         // D buffers at columns 384, 416, 448, 480
 constexpr int kDBufs = 4;                      // accumulator buffers (32 columns each)
 
-// Operand type of the MMAs: dense and gate_up multiply BF16 activations (as
-// staged, unconverted) by weights decoded to BF16; down multiplies the FP32 h
-// brought to FP16 (power-of-two shift per row) by weights decoded to FP16.
-// Both decodes are exact: a code x scale product has at most 6 significant
-// bits and lies in [2^-10, 2688].
-template <int MODE>
-constexpr bool kBf16Operands = MODE != kTcDown;
+// Operand type of the MMAs: FP16 x FP16 -> FP32.  The weights are decoded
+// to FP16 exactly (a code x scale product has at most 6 significant bits and
+// lies in [2^-10, 2688]); the activations are staged as FP16 after a
+// power-of-two shift per row that puts the row's largest magnitude in
+// [2^14, 2^15) (BF16 rows: exact; FP32 h rows: one rounding).
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
@@ -93,6 +91,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
                                               volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (*abort_flag) return false;
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// The same on a barrier given by its shared-memory address; no abort check
+// while the phase is already complete.
+__device__ __forceinline__ bool wait_u32(uint32_t a, uint32_t parity, uint32_t* status,
+                                         volatile int* abort_flag) {
+  if (mbar_try_wait(a, parity)) return !*abort_flag;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (*abort_flag) return false;
@@ -437,75 +453,80 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
 }
 
-// Activations staged by TMA (dense A, MoE x): K range [kbeg, kbeg + klen)
-// of rows [0, rb) (rows past the tensor read as zero) as BF16 in the 128-byte
-// swizzled K-block layout, used by the MMA as they are (sig = 0).  The four
-// epilogue warps; returns when the copy has landed.
-__device__ __forceinline__ void stage_tma(const Cta& c, const CUtensorMap* xmap, int rb, int kbeg,
-                                          int klen, int* sig, int ew, int lane, uint32_t& xphase) {
-  uint8_t* xs = c.xs();
-  if (ew == 0) {
-    // the activations were written by generic stores (of other CTAs, ordered
-    // before us by the completion counters): order them before the copy
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    if (lane == 0) mbar_arrive_expect_tx(c.x_tma(), static_cast<uint32_t>(rb * klen * 2));
-    __syncwarp();
-    for (int j = lane; j < klen / 64; j += 32)
-      tma_load_2d_nohint(xs + j * rb * 128, xmap, kbeg + 64 * j, 0, c.x_tma());
-  }
-  if (ew * 32 + lane < kMaxM) sig[ew * 32 + lane] = 0;
-  wait_bar(c.x_tma(), xphase, c.status(), c.abort_flag());
-  xphase ^= 1u;
-}
-
-// rms[n] = 1/sqrt(mean x^2 + 1e-6) of the rb staged BF16 rows (klen each),
-// from shared memory while the MMAs run.  Chunk etid + 128 i (16 bytes)
-// lies in line etid / 8 + 16 i: row (g + 16 i) % rb; per-group sums are
-// reduced in a fixed order (part: 64 floats of scratch).
-__device__ __forceinline__ void staged_rms(const Cta& c, int rb, int klen, float* rms, float* part,
-                                           int ew, int lane) {
-  const uint8_t* xs = c.xs();
+// Activations staged through cp.async (16-byte copies that go through the
+// load/store path, not behind the weight tiles queued on the TMA unit): BF16
+// rows [0, nr) of the K range [kbeg, kbeg + klen) into the 128-byte swizzled
+// K-block layout, rows [nr, rb) zero.  Then every thread converts the chunks
+// it copied to FP16 times 2^sig[n], the shift that puts row n's largest
+// magnitude in [2^14, 2^15) (exact for BF16), and with rms != nullptr sets
+// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.  Row statistics
+// are combined in a fixed order (part: 256 floats of scratch).  The four
+// epilogue warps.
+template <typename RowFn>
+__device__ __forceinline__ void stage_bf16_rows(RowFn rowp, int nr, int rb, int kbeg, int klen,
+                                                uint32_t xs, int* sig, float* rms, float* part,
+                                                int ew, int lane) {
   const int etid = ew * 32 + lane;
-  const int g = etid >> 3;
-  const int n_it = rb * klen / (8 * kEpiThreads);  // even
-  float sq[2] = {0.0f, 0.0f};
-  for (int i0 = 0; i0 < n_it; i0 += 4) {
-    uint4 v[4];
+  const int cpr = klen >> 3;  // 16-byte chunks per row
+  for (int n = 0; n < rb; ++n)
+    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
+      const uint32_t dst = xs + xoff(n, 8 * kc, rb);
+      if (n < nr)
+        cp_async_16(dst, rowp(n) + kbeg + 8 * kc);
+      else
+        st_shared_v4(dst, make_uint4(0u, 0u, 0u, 0u));
+    }
+  cp_async_wait_all();
+  for (int n = 0; n < nr; ++n) {
+    float m = 0.0f, sq = 0.0f;
+    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
+      const uint4 v = ld_shared_v4(xs + xoff(n, 8 * kc, rb));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (i0 + t < n_it) v[t] = *reinterpret_cast<const uint4*>(xs + 16 * (etid + kEpiThreads * (i0 + t)));
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (i0 + t < n_it) {
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&v[t]);
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float f = __bfloat162float(e[j]);
-          s = fmaf(f, f, s);
-        }
-        sq[t & 1] += s;
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
+        sq = fmaf(lo, lo, sq);
+        sq = fmaf(hi, hi, sq);
       }
-  }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], o);
-    sq[1] += __shfl_xor_sync(0xffffffffu, sq[1], o);
-  }
-  if ((lane & 7) == 0) {
-    part[2 * g] = sq[0];
-    part[2 * g + 1] = sq[1];
+    }
+    m = warp_max(m);
+    sq = warp_sum(sq);
+    if (lane == 0) {
+      part[ew * 32 + n] = sq;
+      part[128 + ew * 32 + n] = m;
+    }
   }
   esync();
   if (etid < rb) {
-    float s = 0.0f;
-    for (int gg = 0; gg < kEpiThreads / 8; ++gg)
+    int shv = 0;
+    if (etid < nr) {
+      float sq = 0.0f, m = 0.0f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if ((gg + 16 * h) % rb == etid) s += part[2 * gg + h];
-    rms[etid] = rsqrtf(s / static_cast<float>(klen) + 1e-6f);
+      for (int w = 0; w < kEpiWarps; ++w) {
+        sq += part[w * 32 + etid];
+        m = fmaxf(m, part[128 + w * 32 + etid]);
+      }
+      shv = f16_row_shift(m);
+      if (rms) rms[etid] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
+    }
+    sig[etid] = shv;
   }
   esync();
+  for (int n = 0; n < nr; ++n) {
+    const int sh = sig[n], h1 = sh / 2;
+    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
+      const uint32_t a = xs + xoff(n, 8 * kc, rb);
+      const uint4 v = ld_shared_v4(a);
+      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = pack_f16x2(__uint_as_float(w[j] << 16) * f1 * f2,
+                          __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
+      st_shared_v4(a, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  }
 }
 
 // ------------------------------------------------------------ roles, per op
@@ -536,35 +557,41 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
     }
   }
   __syncwarp();
-  uint8_t* const ring = c.ring();
+  // everything the loop touches lives in registers: shared-memory addresses
+  // as 32-bit values, the stage counters advanced without divisions
+  const uint32_t ring_u = smem_u32(c.ring());
+  const uint32_t full_u = smem_u32(c.ring_full_at(0));
+  const uint32_t empty_u = smem_u32(c.ring_empty_at(0));
   const int n_stages = c.n_stages();
+  volatile int* const abort_flag = c.abort_flag();
+  uint32_t* const status = c.status();
+  const int nkb = wk.nkb;
+  int tile = u0 < u1 ? static_cast<int>(u0 / nkb) : 0;
+  int kb = u0 < u1 ? static_cast<int>(u0 - static_cast<long>(tile) * nkb) : 0;
   int cur_tile = -1;
   Box bx[4];
   for (long u = u0; u < u1; ++u) {
-    const int tile = static_cast<int>(u / wk.nkb);
-    const int kb = static_cast<int>(u - static_cast<long>(tile) * wk.nkb);
     if (tile != cur_tile) {
       kk.tile_boxes(tile, bx);
       cur_tile = tile;
     }
     bool ok = true;
-    if (lane == 0)
-      ok = !c.aborted() && wait_or_abort(c.ring_empty_at(stage), phase ^ 1u, c.status(), c.abort_flag());
+    if (lane == 0) ok = wait_u32(empty_u + 8u * stage, phase ^ 1u, status, abort_flag);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     if (tc::elect_one()) {
-      uint64_t* full = c.ring_full_at(stage);
-      mbar_arrive_expect_tx(full, kTcStageBytes);
-      uint8_t* st = ring + stage * kTcStageBytes;
+      const uint32_t full = full_u + 8u * stage;
+      mbar_arrive_expect_tx_u32(full, kTcStageBytes);
+      const uint32_t st = ring_u + static_cast<uint32_t>(stage) * kTcStageBytes;
       if (MODE == kTcGateUp) {
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
-          tma_load_2d(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row, full, pol);
-          tma_load_2d(st + kCodeBytes + bb * (kRows * kSK / 16 / 4), bx[bb].ms, kb * (kSK / 16),
-                      bx[bb].row, full, pol);
+          tma_load_2d_u32(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row, full, pol);
+          tma_load_2d_u32(st + kCodeBytes + bb * (kRows * kSK / 16 / 4), bx[bb].ms, kb * (kSK / 16),
+                          bx[bb].row, full, pol);
         }
       } else {
-        tma_load_2d(st, bx[0].mc, kb * (kSK / 2), bx[0].row, full, pol);
-        tma_load_2d(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, full, pol);
+        tma_load_2d_u32(st, bx[0].mc, kb * (kSK / 2), bx[0].row, full, pol);
+        tma_load_2d_u32(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, full, pol);
       }
     }
     __syncwarp();
@@ -572,6 +599,10 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
     if (++stage == n_stages) {
       stage = 0;
       phase ^= 1u;
+    }
+    if (++kb == nkb) {
+      kb = 0;
+      ++tile;
     }
   }
   if (MODE != kTcDense) cur.release(c, op, lane == 0);
@@ -599,7 +630,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
-    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, kBf16Operands<MODE>);
+    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, false);
     const int rb = tc_xrows(nr);
     const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
     for (int w0 = kbs; w0 < kbe;) {
@@ -661,60 +692,65 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   make_work<MODE>(op.a, sc, c, u0, u1);
   const int dw = warp - 2, q = warp & 3, half = dw >> 2;
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
+  // loop constants in registers (shared-memory addresses as 32-bit values)
+  const uint32_t ring_u = smem_u32(c.ring());
+  const uint32_t rfull_u = smem_u32(c.ring_full_at(0));
+  const uint32_t rempty_u = smem_u32(c.ring_empty_at(0));
+  const uint32_t afull_u = smem_u32(c.a_full_at(0));
+  const uint32_t aempty_u = smem_u32(c.a_empty_at(0));
+  const int n_stages = c.n_stages();
+  volatile int* const abort_flag = c.abort_flag();
+  uint32_t* const status = c.status();
+  // this lane's row of a stage: codes at row * 128 (chunks swizzled by row
+  // % 8), its eight scale bytes of this half at 16 * row + 8 * half
+  const uint32_t code_off = static_cast<uint32_t>(q * (kCodeBytes / 4) + lane * 128);
+  const uint32_t scale_off = static_cast<uint32_t>(kCodeBytes + q * 512 + lane * 16 + 8 * half);
+  uint32_t chunk_off[4];
+#pragma unroll
+  for (int ci = 0; ci < 4; ++ci) chunk_off[ci] = code_off + ((((4 * half + ci) ^ (lane & 7))) << 4);
+  uint32_t ab = acount % kABufs, aph = (acount / kABufs) & 1u;
   for (long u = u0; u < u1; ++u) {
-    if (c.aborted()) break;
-    wait_bar(c.ring_full_at(rstage), rphase, c.status(), c.abort_flag());
-    const uint8_t* st = c.ring() + rstage * kTcStageBytes;
-    const uint8_t* crow = st + q * (kCodeBytes / 4) + lane * 128;
+    if (!wait_u32(rfull_u + 8u * rstage, rphase, status, abort_flag)) break;
+    const uint32_t st = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
     // all shared-memory reads of this stage first (their latency overlaps)
-    const uint2 sb =
-        *reinterpret_cast<const uint2*>(st + kCodeBytes + q * 512 + lane * 16 + 8 * half);
+    const uint2 sb = ld_shared_v2(st + scale_off);
     uint4 cw[4];
 #pragma unroll
-    for (int ci = 0; ci < 4; ++ci)
-      cw[ci] = *reinterpret_cast<const uint4*>(crow + (((4 * half + ci) ^ (lane & 7)) << 4));
+    for (int ci = 0; ci < 4; ++ci) cw[ci] = ld_shared_v4(st + chunk_off[ci]);
     __syncwarp();
-    if (lane == 0) mbar_arrive(c.ring_empty_at(rstage));
-    const uint32_t ab = acount % kABufs;
-    wait_bar(c.a_empty_at(ab), ((acount / kABufs) & 1u) ^ 1u, c.status(), c.abort_flag());
+    if (lane == 0) mbar_arrive_u32(rempty_u + 8u * rstage);
+    if (!wait_u32(aempty_u + 8u * ab, aph ^ 1u, status, abort_flag)) break;
     tc::fence_after_sync();
+    // E2M1 -> FP16 (hardware convert) times the E4M3 block scale as FP16:
+    // the product is exact (at most 6 significant bits, magnitude in
+    // [2^-10, 2688])
     const uint32_t sbw[2] = {sb.x, sb.y};
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
       const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
+      const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
+      const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
       uint32_t v[16];
-      if (kBf16Operands<MODE>) {
-        // code (x 2^-112, BF16) times scale (x 2^112, BF16): exact
-        const uint32_t s_lo = e4m3_bcast_bf16x2_x2p112(sw & 0xFFu);
-        const uint32_t s_hi = e4m3_bcast_bf16x2_x2p112((sw >> 8) & 0xFFu);
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-          const uint32_t sv = wi < 2 ? s_lo : s_hi;
+      for (int wi = 0; wi < 4; ++wi) {
+        e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
+        const uint32_t sv = wi < 2 ? s_lo : s_hi;
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            v[4 * wi + e] = hmul2_bf16(f16x2_to_bf16x2_scaled(v[4 * wi + e]), sv);
-        }
-      } else {
-        const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
-        const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          e2m1x8_to_f16x2(wds[wi], v[4 * wi], v[4 * wi + 1], v[4 * wi + 2], v[4 * wi + 3]);
-          const uint32_t sv = wi < 2 ? s_lo : s_hi;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
-        }
+        for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
       }
       tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
     }
     tc::wait_st();
     tc::fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(c.a_full_at(ab));
+    if (lane == 0) mbar_arrive_u32(afull_u + 8u * ab);
     ++acount;
-    if (++rstage == c.n_stages()) {
+    if (++ab == kABufs) {
+      ab = 0;
+      aph ^= 1u;
+    }
+    if (++rstage == n_stages) {
       rstage = 0;
       rphase ^= 1u;
     }
@@ -727,7 +763,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 // (Not inlined: each mode gets its own register allocation.)
 template <int MODE>
 __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
-                                         int ew, int lane, uint32_t& dcount, uint32_t& xphase) {
+                                         int ew, int lane, uint32_t& dcount) {
   const TcArgs& a = op.a;
   const int q = (kEpiWarp0 + ew) & 3;
   const int etid = ew * 32 + lane;
@@ -798,15 +834,17 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
           stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
                          kbeg, klen, c.xs(), sig, nullptr, ew, lane, kEpiWarps);
         } else {
-          stage_tma(c, &op.xmap, rb, kbeg, klen, sig, ew, lane, xphase);
+          // the RMS factors too when one window covers K
+          const bool want_rms = a.rms && (MODE == kTcGateUp || a.win_k >= a.K);
+          const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
+          const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
+          stage_bf16_rows([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen, smem_u32(c.xs()),
+                          sig, want_rms ? rms : nullptr, ep, ew, lane);
         }
         fence_proxy_async_smem();
         esync();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.x_full());
-        // the RMS factors of a single window covering K, while the MMAs run
-        if (MODE != kTcDown && a.rms && (MODE == kTcGateUp || a.win_k >= a.K))
-          staged_rms(c, rb, klen, rms, ep, ew, lane);
       }
       // ---- fold the window's accumulator into the segment total
       const uint32_t db = dcount % kDBufs;
@@ -1076,7 +1114,7 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
   const int ew = warp - kEpiWarp0, etid = ew * 32 + lane;
   const int n_ops = prog.n_ops;
   SchedCursor cur;
-  uint32_t dcount = 0, xphase = 0;
+  uint32_t dcount = 0;
   // inputs may come from the previous kernel on the stream
   pdl_wait();
   pdl_launch_dependents();
@@ -1088,9 +1126,9 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
       esync();
     }
     switch (op.mode) {
-      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount, xphase); break;
-      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount, xphase); break;
-      case kTcDown: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount, xphase); break;
+      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount); break;
+      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount); break;
+      case kTcDown: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount); break;
       default: combine_op(c, op, cur, ew, lane); break;
     }
     if (n_ops > 1) {
