@@ -56,7 +56,8 @@ constexpr int kRows = 128;
 constexpr int kBox = 32;
 constexpr int kSK = 256;                       // K per stage
 constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = NVFP4_DEC_WARPS;
+constexpr int kDecChunks = 8 * 4 / kDecWarps;  // 32-K chunks a decode warp converts per stage
 constexpr int kEpiWarps = 4;                   // one per tensor-memory lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kEpiWarp0 = 2 + kDecWarps;       // warps 10..13
@@ -78,6 +79,7 @@ constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
 static_assert(kTcThreads == (3 + kDecWarps + kEpiWarps) * 32, "thread count");
+static_assert(kDecWarps == 4 || kDecWarps == 8, "decode warps cover the 4 lane quarters");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -230,13 +232,14 @@ __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kb
   return min(kbe, w0 + kk.win_stages());
 }
 
-// Stage range restaged when a window is not covered: the whole K when it
-// fits (MoE always; dense when the window capacity covers K: then staged once
-// per op), else the window.
+// Stage range restaged when a window is not covered: MoE, the whole K (its
+// K is staged once per expert / layer); dense, exactly the window when the
+// window capacity is shorter than K or when the CTA's remaining units of the
+// op all lie in this tile (one_tile), else the whole K (staged once per op).
 template <int MODE>
-__device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1, int& k0,
-                                              int& k1) {
-  if (MODE == kTcDense && kk.win_stages() < kk.wk.nkb) {
+__device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1,
+                                              bool one_tile, int& k0, int& k1) {
+  if (MODE == kTcDense && (kk.win_stages() < kk.wk.nkb || one_tile)) {
     k0 = w0;
     k1 = w1;
   } else {
@@ -456,18 +459,17 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
 // Activations staged through cp.async (16-byte copies that go through the
 // load/store path, not behind the weight tiles queued on the TMA unit): BF16
 // rows [0, nr) of the K range [kbeg, kbeg + klen) into the 128-byte swizzled
-// K-block layout, rows [nr, rb) zero.  Then every thread converts the chunks
-// it copied to FP16 times 2^sig[n], the shift that puts row n's largest
+// K-block layout, rows [nr, rb) zero.  Then warp ew converts rows ew, ew + 4,
+// ... in place to FP16 times 2^sig[n], the shift that puts row n's largest
 // magnitude in [2^14, 2^15) (exact for BF16), and with rms != nullptr sets
-// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.  Row statistics
-// are combined in a fixed order (part: 256 floats of scratch).  The four
-// epilogue warps.
+// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range (each row reduced
+// by one warp: a fixed order).  The four epilogue warps.
 template <typename RowFn>
 __device__ __forceinline__ void stage_bf16_rows(RowFn rowp, int nr, int rb, int kbeg, int klen,
-                                                uint32_t xs, int* sig, float* rms, float* part,
-                                                int ew, int lane) {
+                                                uint32_t xs, int* sig, float* rms, int ew,
+                                                int lane) {
   const int etid = ew * 32 + lane;
-  const int cpr = klen >> 3;  // 16-byte chunks per row
+  const int cpr = klen >> 3;  // 16-byte chunks per row, a multiple of 32
   for (int n = 0; n < rb; ++n)
     for (int kc = etid; kc < cpr; kc += kEpiThreads) {
       const uint32_t dst = xs + xoff(n, 8 * kc, rb);
@@ -476,56 +478,44 @@ __device__ __forceinline__ void stage_bf16_rows(RowFn rowp, int nr, int rb, int 
       else
         st_shared_v4(dst, make_uint4(0u, 0u, 0u, 0u));
     }
+  if (etid < kMaxM) sig[etid] = 0;  // rows past nr; rows below are set after the barrier
   cp_async_wait_all();
-  for (int n = 0; n < nr; ++n) {
-    float m = 0.0f, sq = 0.0f;
-    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
+  esync();
+  for (int n = ew; n < nr; n += kEpiWarps) {
+    uint32_t mx = 0u;  // largest |x| of the lane's chunks, as two BF16 bit patterns
+    float sq = 0.0f;
+    for (int kc = lane; kc < cpr; kc += 32) {
       const uint4 v = ld_shared_v4(xs + xoff(n, 8 * kc, rb));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-        m = fmaxf(m, fmaxf(fabsf(lo), fabsf(hi)));
-        sq = fmaf(lo, lo, sq);
-        sq = fmaf(hi, hi, sq);
+        mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);  // |x| orders like its bits
+        if (rms) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+          sq = fmaf(lo, lo, sq);
+          sq = fmaf(hi, hi, sq);
+        }
       }
     }
-    m = warp_max(m);
-    sq = warp_sum(sq);
-    if (lane == 0) {
-      part[ew * 32 + n] = sq;
-      part[128 + ew * 32 + n] = m;
+    const float m = warp_max(fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u)));
+    const int sh = f16_row_shift(m);
+    if (rms) {
+      sq = warp_sum(sq);
+      if (lane == 0) rms[n] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
     }
-  }
-  esync();
-  if (etid < rb) {
-    int shv = 0;
-    if (etid < nr) {
-      float sq = 0.0f, m = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kEpiWarps; ++w) {
-        sq += part[w * 32 + etid];
-        m = fmaxf(m, part[128 + w * 32 + etid]);
-      }
-      shv = f16_row_shift(m);
-      if (rms) rms[etid] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
-    }
-    sig[etid] = shv;
-  }
-  esync();
-  for (int n = 0; n < nr; ++n) {
-    const int sh = sig[n], h1 = sh / 2;
+    const int h1 = sh / 2;
     const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
-    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
-      const uint32_t a = xs + xoff(n, 8 * kc, rb);
-      const uint4 v = ld_shared_v4(a);
+    for (int kc = lane; kc < cpr; kc += 32) {
+      const uint32_t ad = xs + xoff(n, 8 * kc, rb);
+      const uint4 v = ld_shared_v4(ad);
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         w[j] = pack_f16x2(__uint_as_float(w[j] << 16) * f1 * f2,
                           __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
-      st_shared_v4(a, make_uint4(w[0], w[1], w[2], w[3]));
+      st_shared_v4(ad, make_uint4(w[0], w[1], w[2], w[3]));
     }
+    if (lane == 0) sig[n] = sh;
   }
 }
 
@@ -633,10 +623,11 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, false);
     const int rb = tc_xrows(nr);
     const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
+    const bool one_tile = u1 <= static_cast<long>(tile + 1) * wk.nkb;
     for (int w0 = kbs; w0 < kbe;) {
       const int w1 = window_end(kk, w0, kbe);
       if (!xst.covers(key, w0, w1)) {
-        restage_range(kk, w0, w1, xst.k0, xst.k1);
+        restage_range(kk, w0, w1, one_tile, xst.k0, xst.k1);
         xst.key = key;
         if (lane == 0) wait_bar(c.x_full(), xcount & 1u, c.status(), c.abort_flag());
         __syncwarp();
@@ -690,7 +681,9 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   if (MODE != kTcDense) sc = cur.acquire(c, op);
   long u0, u1;
   make_work<MODE>(op.a, sc, c, u0, u1);
-  const int dw = warp - 2, q = warp & 3, half = dw >> 2;
+  // warp dw decodes lane quarter q (tile rows 32q .. 32q + 31), chunks
+  // [c0, c0 + kDecChunks) of 32 K each (8 chunks per 256-K stage)
+  const int dw = warp - 2, q = warp & 3, c0 = (dw >> 2) * kDecChunks;
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
   // loop constants in registers (shared-memory addresses as 32-bit values)
   const uint32_t ring_u = smem_u32(c.ring());
@@ -701,22 +694,33 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   const int n_stages = c.n_stages();
   volatile int* const abort_flag = c.abort_flag();
   uint32_t* const status = c.status();
-  // this lane's row of a stage: codes at row * 128 (chunks swizzled by row
-  // % 8), its eight scale bytes of this half at 16 * row + 8 * half
+  // this lane's row of a stage: codes at row * 128 (16-byte chunks swizzled
+  // by row % 8), its scale bytes (two per chunk) at 16 * row + 2 * c0
   const uint32_t code_off = static_cast<uint32_t>(q * (kCodeBytes / 4) + lane * 128);
-  const uint32_t scale_off = static_cast<uint32_t>(kCodeBytes + q * 512 + lane * 16 + 8 * half);
-  uint32_t chunk_off[4];
+  const uint32_t scale_off = static_cast<uint32_t>(kCodeBytes + q * 512 + lane * 16 + 2 * c0);
+  uint32_t chunk_off[kDecChunks];
 #pragma unroll
-  for (int ci = 0; ci < 4; ++ci) chunk_off[ci] = code_off + ((((4 * half + ci) ^ (lane & 7))) << 4);
+  for (int ci = 0; ci < kDecChunks; ++ci) chunk_off[ci] = code_off + (((c0 + ci) ^ (lane & 7)) << 4);
   uint32_t ab = acount % kABufs, aph = (acount / kABufs) & 1u;
   for (long u = u0; u < u1; ++u) {
     if (!wait_u32(rfull_u + 8u * rstage, rphase, status, abort_flag)) break;
     const uint32_t st = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
     // all shared-memory reads of this stage first (their latency overlaps)
-    const uint2 sb = ld_shared_v2(st + scale_off);
-    uint4 cw[4];
+    uint32_t sbw[kDecChunks / 2];
+    if (kDecChunks == 8) {
+      const uint4 sb = ld_shared_v4(st + scale_off);
+      sbw[0] = sb.x;
+      sbw[kDecChunks / 2 > 1 ? 1 : 0] = sb.y;
+      sbw[kDecChunks / 2 > 2 ? 2 : 0] = sb.z;
+      sbw[kDecChunks / 2 > 3 ? 3 : 0] = sb.w;
+    } else {
+      const uint2 sb = ld_shared_v2(st + scale_off);
+      sbw[0] = sb.x;
+      sbw[kDecChunks / 2 > 1 ? 1 : 0] = sb.y;
+    }
+    uint4 cw[kDecChunks];
 #pragma unroll
-    for (int ci = 0; ci < 4; ++ci) cw[ci] = ld_shared_v4(st + chunk_off[ci]);
+    for (int ci = 0; ci < kDecChunks; ++ci) cw[ci] = ld_shared_v4(st + chunk_off[ci]);
     __syncwarp();
     if (lane == 0) mbar_arrive_u32(rempty_u + 8u * rstage);
     if (!wait_u32(aempty_u + 8u * ab, aph ^ 1u, status, abort_flag)) break;
@@ -724,9 +728,8 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
     // E2M1 -> FP16 (hardware convert) times the E4M3 block scale as FP16:
     // the product is exact (at most 6 significant bits, magnitude in
     // [2^-10, 2688])
-    const uint32_t sbw[2] = {sb.x, sb.y};
 #pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
+    for (int ci = 0; ci < kDecChunks; ++ci) {
       const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
       const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
       const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
@@ -739,7 +742,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
       }
-      tc::st_x16(lane_addr + kACols * ab + 16 * (4 * half + ci), v);
+      tc::st_x16(lane_addr + kACols * ab + 16 * (c0 + ci), v);
     }
     tc::wait_st();
     tc::fence_before_sync();
@@ -761,7 +764,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 // Epilogue warps, one op: activation staging, accumulator folds, stream-K
 // reduction and the op's epilogue.
 // (Not inlined: each mode gets its own register allocation.)
-template <int MODE>
+template <int MODE, int NC>
 __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
                                          int ew, int lane, uint32_t& dcount) {
   const TcArgs& a = op.a;
@@ -780,32 +783,10 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
   float* ep = c.ep();
   volatile int* bcast = c.bcast();
 
-  // dense staged in windows shorter than K: the RMS factor of each row over
-  // the whole K, 8 loads a lane in flight (with one window covering K it
-  // comes from the staging pass)
-  if (MODE == kTcDense && a.rms && a.win_k < a.K && u0 < u1) {
-    for (int m = ew; m < a.M; m += kEpiWarps) {
-      float ss = 0.0f;
-      const __nv_bfloat16* row = a.A + m * a.lda;
-      for (int v0 = 0; v0 < a.K / 8; v0 += 8 * 32) {
-        uint4 buf[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int v = v0 + 32 * i + lane;
-          buf[i] = v < a.K / 8 ? *reinterpret_cast<const uint4*>(row + v * 8) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&buf[i]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) ss = fmaf(static_cast<float>(e[j]), static_cast<float>(e[j]), ss);
-        }
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
-    }
-  }
   XState xst;
+  bool rms_ready = false;
+  int g_expert = -1;
+  float g_tile = 0.0f;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
   const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
 
@@ -817,14 +798,34 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
     const int rb = tc_xrows(nr);
-    float tot[32];
+    const bool one_tile = u1 <= static_cast<long>(tile + 1) * wk.nkb;
+    // the tile's expert's global scale: a global load (microseconds while the
+    // weights stream) only when the expert changes, issued before the MMAs
+    // are waited for
+    if (MODE == kTcGateUp) {
+      const int pb = 2 * tile + (q >> 1);
+      if (!(q & 1) && pb < wk.pb_count) {
+        const int e = kk.pb_expert(pb);
+        if (e != g_expert) {
+          g_tile = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+          g_expert = e;
+        }
+      }
+    } else if (MODE == kTcDown) {
+      const int e = sc.active[tile / wk.per_e];
+      if (e != g_expert) {
+        g_tile = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+        g_expert = e;
+      }
+    }
+    float tot[NC];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
+    for (int j = 0; j < NC; ++j) tot[j] = 0.0f;
 
     for (int w0 = kbs; w0 < kbe;) {
       const int w1 = window_end(kk, w0, kbe);
       if (!xst.covers(key, w0, w1)) {
-        restage_range(kk, w0, w1, xst.k0, xst.k1);
+        restage_range(kk, w0, w1, one_tile, xst.k0, xst.k1);
         xst.key = key;
         // the previous window's MMAs are complete (its accumulator was read)
         const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
@@ -834,24 +835,56 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
           stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
                          kbeg, klen, c.xs(), sig, nullptr, ew, lane, kEpiWarps);
         } else {
-          // the RMS factors too when one window covers K
-          const bool want_rms = a.rms && (MODE == kTcGateUp || a.win_k >= a.K);
+          // the RMS factors too when the staged range covers K
+          const bool stage_rms = a.rms && !rms_ready && xst.k0 == 0 && xst.k1 == wk.nkb;
+          rms_ready = rms_ready || stage_rms;
           const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
           const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
           stage_bf16_rows([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen, smem_u32(c.xs()),
-                          sig, want_rms ? rms : nullptr, ep, ew, lane);
+                          sig, stage_rms ? rms : nullptr, ew, lane);
         }
         fence_proxy_async_smem();
         esync();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.x_full());
+        // dense staged over part of K: the RMS factor of each row over the
+        // whole K from global memory, while the MMAs run
+        if (MODE == kTcDense && a.rms && !rms_ready) {
+          for (int m = ew; m < a.M; m += kEpiWarps) {
+            float ss = 0.0f;
+            const __nv_bfloat16* row = a.A + m * a.lda;
+            for (int v0 = 0; v0 < a.K / 8; v0 += 8 * 32) {
+              uint4 buf[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int v = v0 + 32 * i + lane;
+                buf[i] = v < a.K / 8 ? *reinterpret_cast<const uint4*>(row + v * 8)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+                  ss = fmaf(lo, lo, ss);
+                  ss = fmaf(hi, hi, ss);
+                }
+              }
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+          }
+          rms_ready = true;
+          esync();
+        }
       }
       // ---- fold the window's accumulator into the segment total
       const uint32_t db = dcount % kDBufs;
       wait_bar(c.d_full_at(db), (dcount / kDBufs) & 1u, c.status(), c.abort_flag());
       tc::fence_after_sync();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NC / 16; ++h) {
         uint32_t dv[16];
         tc::ld_x16(lane_addr + kDCol + 32u * db + 16u * h, dv);
         tc::wait_ld();
@@ -872,7 +905,7 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       const int slot = (tile == first_tile) ? 0 : 1;
       float* part = a.partials + static_cast<size_t>(b * 2 + slot) * (32 * kRows);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < NC; ++j)
         if (j < nr) part[j * kRows + r] = tot[j];
       esync();
       const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
@@ -885,13 +918,23 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       }
       esync();
       if (!*bcast) continue;  // uniform across the epilogue warps
+      // sum in CTA order; this CTA's own partial comes from registers
+      float own[NC];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) tot[j] = 0.0f;
+      for (int j = 0; j < NC; ++j) {
+        own[j] = tot[j];
+        tot[j] = 0.0f;
+      }
       for (int bb = blo; bb <= bhi; ++bb) {
+        if (wk.abs_cta(bb) == b) {
+#pragma unroll
+          for (int j = 0; j < NC; ++j) tot[j] += own[j];
+          continue;
+        }
         const int sl = (wk.begin(bb) / wk.nkb == tile) ? 0 : 1;
         const float* pp = a.partials + static_cast<size_t>(wk.abs_cta(bb) * 2 + sl) * (32 * kRows);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < NC; ++j)
           if (j < nr) tot[j] += __ldcg(pp + j * kRows + r);
       }
       if (etid == 0) a.tile_cnt[tile] = 0u;
@@ -900,7 +943,7 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
     // ---- epilogues
     if (MODE == kTcDense) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < NC; ++j)
         if (j < a.M) ep[j * kRows + r] = tot[j] * gs * (a.rms ? rms[j] : 1.0f);
       esync();
       const int n0 = tile * kRows;
@@ -955,13 +998,13 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       // for pair-box 2*tile+1 (absent when the count is odd)
       if (q & 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ep[j * kRows + r] = tot[j];
+        for (int j = 0; j < NC; ++j) ep[j * kRows + r] = tot[j];
       }
       esync();
       const int pb = 2 * tile + (q >> 1);
       if (!(q & 1) && pb < wk.pb_count) {
         const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
-        const float g = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+        const float g = g_tile;
         const int cnt = sc.cnt[e], off = sc.off[e];
         for (int qq = 0; qq < cnt; ++qq) {
           const int p = off + qq;
@@ -969,7 +1012,7 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
           const float f = a.rms ? g * rms[t] : g;
           float gt = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
+          for (int j = 0; j < NC; ++j)
             if (j == t) gt = tot[j];
           gt *= f;
           const float up = ep[t * kRows + r + 32] * f;
@@ -978,10 +1021,10 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
       }
     } else {
       const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
-      const float g = (e == a.E) ? *a.sh_dn_global : a.dn_global[e];
+      const float g = g_tile;
       const int cnt = sc.cnt[e], off = sc.off[e];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < NC; ++j)
         if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
     }
     esync();
@@ -1126,9 +1169,19 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
       esync();
     }
     switch (op.mode) {
-      case kTcDense: epilogue_op<kTcDense>(c, op, cur, ew, lane, dcount); break;
-      case kTcGateUp: epilogue_op<kTcGateUp>(c, op, cur, ew, lane, dcount); break;
-      case kTcDown: epilogue_op<kTcDown>(c, op, cur, ew, lane, dcount); break;
+      // accumulator columns: 16 when the op has at most 16 activation rows
+      case kTcDense:
+        if (op.a.M <= 16) epilogue_op<kTcDense, 16>(c, op, cur, ew, lane, dcount);
+        else epilogue_op<kTcDense, 32>(c, op, cur, ew, lane, dcount);
+        break;
+      case kTcGateUp:
+        if (op.a.T <= 16) epilogue_op<kTcGateUp, 16>(c, op, cur, ew, lane, dcount);
+        else epilogue_op<kTcGateUp, 32>(c, op, cur, ew, lane, dcount);
+        break;
+      case kTcDown:
+        if (op.a.T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount);
+        else epilogue_op<kTcDown, 32>(c, op, cur, ew, lane, dcount);
+        break;
       default: combine_op(c, op, cur, ew, lane); break;
     }
     if (n_ops > 1) {
