@@ -196,7 +196,14 @@ bool tc_layout(int sched_bytes, size_t x_bytes, TcLayout* L) {
   L->ring_offset = static_cast<int>(round_up(L->x_offset + x_bytes, 1024));
   const long room = static_cast<long>(kSmemLimit) - kSmemAlignPad - L->ring_offset;
   L->n_stages = static_cast<int>(room / kTcStageBytes);
-  if (L->n_stages > kTcMaxStages) L->n_stages = kTcMaxStages;
+  // NVFP4_MAX_STAGES caps the weight ring (3..8): a shallower ring keeps
+  // fewer weight bytes queued ahead of the activation loads at op starts
+  static const int cap = [] {
+    const char* e = getenv("NVFP4_MAX_STAGES");
+    const int v = e ? atoi(e) : kTcMaxStages;
+    return v < 3 ? 3 : (v > kTcMaxStages ? kTcMaxStages : v);
+  }();
+  if (L->n_stages > cap) L->n_stages = cap;
   if (L->n_stages < 3) return false;
   L->smem = kSmemAlignPad + L->ring_offset + static_cast<size_t>(L->n_stages) * kTcStageBytes;
   return true;

@@ -121,6 +121,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_u32(uint32_t bar, uint32_t
       : "memory");
 }
 
+// Non-blocking test of a phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -137,7 +150,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 // kWaitLimitNs, records the timeout in *status (global) and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
@@ -223,6 +236,15 @@ __device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
   uint32_t d;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(two));
   return d;
+}
+
+// Two E4M3 bytes (low byte: first block) -> each broadcast to both halves
+// of an f16x2 (exact).
+__device__ __forceinline__ void e4m3x2_bcast_f16x2(uint32_t two, uint32_t& lo, uint32_t& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two & 0xFFFFu)));
+  lo = __byte_perm(h2, 0u, 0x1010);
+  hi = __byte_perm(h2, 0u, 0x3232);
 }
 
 // Two E2M1 values held as FP16 (from cvt.rn.f16x2.e2m1x2: 0 or an FP16

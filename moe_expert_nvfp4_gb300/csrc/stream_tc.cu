@@ -92,7 +92,7 @@ __device__ __forceinline__ void esync() {  // the four epilogue warps
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* status,
                                               volatile int* abort_flag) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_test_wait(a, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (*abort_flag) return false;
@@ -110,7 +110,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
 // while the phase is already complete.
 __device__ __forceinline__ bool wait_u32(uint32_t a, uint32_t parity, uint32_t* status,
                                          volatile int* abort_flag) {
-  if (mbar_try_wait(a, parity)) return !*abort_flag;
+  if (mbar_test_wait(a, parity)) return !*abort_flag;
   const unsigned long long t0 = globaltimer();
   while (true) {
     if (*abort_flag) return false;
@@ -256,83 +256,6 @@ __device__ __forceinline__ uint32_t xoff(int n, int k, int rb) {
   return static_cast<uint32_t>((k >> 6) * rb * 128 + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4));
 }
 
-// Stage rows [0, rb) of K range [kbeg, kbeg + klen) from registers: FP16
-// with one power-of-two shift per row (sig), rows past nr zero, optionally
-// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.  Warp dw of nwarps
-// takes rows dw, dw + nwarps, ...; a row is read once into registers (at
-// most 16 x 16 bytes per lane).
-template <typename T, typename RowFn>
-__device__ __forceinline__ void stage_b(RowFn rowp, int nr, int rb, int kbeg, int klen,
-                                        uint8_t* xs, int* sig, float* rms, int dw, int lane,
-                                        int nwarps) {
-  constexpr int kVec = 16 / sizeof(T);  // elements per 16-byte load
-  const int nv = klen / (32 * kVec);    // loads per lane
-  for (int n = dw; n < rb; n += nwarps) {
-    if (n >= nr) {
-      for (int v = lane; v < klen / 8; v += 32)
-        *reinterpret_cast<uint4*>(xs + xoff(n, 8 * v, rb)) = make_uint4(0u, 0u, 0u, 0u);
-      if (lane == 0) sig[n] = 0;
-      continue;
-    }
-    const T* src = rowp(n) + kbeg;
-    // pass 1: max |x| (and sum of squares); rows of up to 8 loads per lane
-    // stay in registers for pass 2, longer rows are read again
-    uint4 buf[8];
-    float amax = 0.0f, ss = 0.0f;
-    for (int i0 = 0; i0 < nv; i0 += 8) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + ((i0 + i) * 32 + lane) * kVec);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < nv) {
-          const T* e = reinterpret_cast<const T*>(&buf[i]);
-#pragma unroll
-          for (int j = 0; j < kVec; ++j) {
-            const float f = static_cast<float>(e[j]);
-            amax = fmaxf(amax, fabsf(f));
-            ss = fmaf(f, f, ss);
-          }
-        }
-    }
-    amax = warp_max(amax);
-    const int sh = f16_row_shift(amax);
-    if (lane == 0) sig[n] = sh;
-    if (rms) {
-      ss = warp_sum(ss);
-      if (lane == 0) rms[n] = rsqrtf(ss / static_cast<float>(klen) + 1e-6f);
-    }
-    // pass 2: convert and store
-    for (int i0 = 0; i0 < nv; i0 += 8) {
-      if (nv > 8) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i0 + i < nv) buf[i] = *reinterpret_cast<const uint4*>(src + ((i0 + i) * 32 + lane) * kVec);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i0 + i < nv) {
-          const T* e = reinterpret_cast<const T*>(&buf[i]);
-          const int kq = ((i0 + i) * 32 + lane) * kVec;  // element offset of this load
-          if constexpr (sizeof(T) == 2) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              pk[j] = pack_f16x2(scale_pow2(static_cast<float>(e[2 * j]), sh),
-                                 scale_pow2(static_cast<float>(e[2 * j + 1]), sh));
-            *reinterpret_cast<uint4*>(xs + xoff(n, kq, rb)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          } else {
-            const uint32_t p0 = pack_f16x2(scale_pow2(static_cast<float>(e[0]), sh),
-                                           scale_pow2(static_cast<float>(e[1]), sh));
-            const uint32_t p1 = pack_f16x2(scale_pow2(static_cast<float>(e[2]), sh),
-                                           scale_pow2(static_cast<float>(e[3]), sh));
-            *reinterpret_cast<uint2*>(xs + xoff(n, kq & ~7, rb) + (kq & 7) * 2) = make_uint2(p0, p1);
-          }
-        }
-    }
-  }
-}
-
 // ------------------------------------------------------------ CTA context
 
 
@@ -456,66 +379,109 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
 }
 
-// Activations staged through cp.async (16-byte copies that go through the
-// load/store path, not behind the weight tiles queued on the TMA unit): BF16
-// rows [0, nr) of the K range [kbeg, kbeg + klen) into the 128-byte swizzled
-// K-block layout, rows [nr, rb) zero.  Then warp ew converts rows ew, ew + 4,
-// ... in place to FP16 times 2^sig[n], the shift that puts row n's largest
-// magnitude in [2^14, 2^15) (exact for BF16), and with rms != nullptr sets
-// rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range (each row reduced
-// by one warp: a fixed order).  The four epilogue warps.
-template <typename RowFn>
-__device__ __forceinline__ void stage_bf16_rows(RowFn rowp, int nr, int rb, int kbeg, int klen,
-                                                uint32_t xs, int* sig, float* rms, int ew,
-                                                int lane) {
-  const int etid = ew * 32 + lane;
-  const int cpr = klen >> 3;  // 16-byte chunks per row, a multiple of 32
-  for (int n = 0; n < rb; ++n)
-    for (int kc = etid; kc < cpr; kc += kEpiThreads) {
-      const uint32_t dst = xs + xoff(n, 8 * kc, rb);
-      if (n < nr)
-        cp_async_16(dst, rowp(n) + kbeg + 8 * kc);
-      else
-        st_shared_v4(dst, make_uint4(0u, 0u, 0u, 0u));
-    }
-  if (etid < kMaxM) sig[etid] = 0;  // rows past nr; rows below are set after the barrier
-  cp_async_wait_all();
-  esync();
-  for (int n = ew; n < nr; n += kEpiWarps) {
-    uint32_t mx = 0u;  // largest |x| of the lane's chunks, as two BF16 bit patterns
-    float sq = 0.0f;
-    for (int kc = lane; kc < cpr; kc += 32) {
-      const uint4 v = ld_shared_v4(xs + xoff(n, 8 * kc, rb));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// One row of the staged operand, held in registers: the lane's 16-byte
+// loads of row n (chunks kc = lane + 32 i of 8 elements; FP32 rows take two
+// loads a chunk), at most kStageSlots loads.
+constexpr int kStageSlots = 16;
+
+template <typename T>
+__device__ __forceinline__ void stage_row_load(const T* row, int n, int nr, int kbeg, int ppr,
+                                               int lane, uint4 (&b)[kStageSlots]) {
+  constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);  // |x| orders like its bits
-        if (rms) {
-          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-          sq = fmaf(lo, lo, sq);
-          sq = fmaf(hi, hi, sq);
-        }
+  for (int i = 0; i < kStageSlots; ++i) {
+    b[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < ppr && n < nr) {
+      const int kc = lane + 32 * (i / kLd), sub = i % kLd;
+      b[i] = __ldcg(reinterpret_cast<const uint4*>(row + kbeg + 8 * kc + 4 * sub));
+    }
+  }
+}
+
+// Two elements of a load as floats.
+template <typename T>
+__device__ __forceinline__ float2 stage_pair(const uint4& v, int j) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (sizeof(T) == 2) {
+    return make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+  } else {
+    return make_float2(__uint_as_float(w[(2 * j) & 3]), __uint_as_float(w[(2 * j + 1) & 3]));
+  }
+}
+
+// Largest magnitude and sum of squares of a row's loads, the row shift, and
+// the FP16 conversion stored into the staged layout.
+template <typename T>
+__device__ __forceinline__ void stage_row_finish(const uint4 (&b)[kStageSlots], int n, int nr,
+                                                 int rb, int ppr, uint32_t xs, int* sig,
+                                                 float* rms, int klen, int lane) {
+  constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
+  constexpr int kPairs = sizeof(T) == 2 ? 4 : 2;  // element pairs per 16-byte load
+  if (n >= rb) return;
+  float m = 0.0f, sq = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kStageSlots; ++i)
+    if (i < ppr) {
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const float2 f = stage_pair<T>(b[i], j);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+        sq = fmaf(f.x, f.x, sq);
+        sq = fmaf(f.y, f.y, sq);
       }
     }
-    const float m = warp_max(fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u)));
-    const int sh = f16_row_shift(m);
-    if (rms) {
-      sq = warp_sum(sq);
-      if (lane == 0) rms[n] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
-    }
-    const int h1 = sh / 2;
-    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
-    for (int kc = lane; kc < cpr; kc += 32) {
-      const uint32_t ad = xs + xoff(n, 8 * kc, rb);
-      const uint4 v = ld_shared_v4(ad);
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  m = warp_max(m);
+  const int sh = n < nr ? f16_row_shift(m) : 0;
+  if (rms && n < nr) {
+    sq = warp_sum(sq);
+    if (lane == 0) rms[n] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
+  }
+  const int h1 = sh / 2;
+  const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w[j] = pack_f16x2(__uint_as_float(w[j] << 16) * f1 * f2,
-                          __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
-      st_shared_v4(ad, make_uint4(w[0], w[1], w[2], w[3]));
+  for (int i = 0; i < kStageSlots; i += kLd)
+    if (i < ppr) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = stage_pair<T>(b[i + (kLd == 2 ? (j >> 1) : 0)], kLd == 2 ? (j & 1) : j);
+        o[j] = pack_f16x2(f.x * f1 * f2, f.y * f1 * f2);
+      }
+      const int kc = lane + 32 * (i / kLd);
+      st_shared_v4(xs + xoff(n, 8 * kc, rb), make_uint4(o[0], o[1], o[2], o[3]));
     }
-    if (lane == 0) sig[n] = sh;
+  if (lane == 0) sig[n] = sh;
+}
+
+// Activations staged through registers in one pass: BF16 (dense A, MoE x)
+// or FP32 (MoE h) rows [0, nr) of the K range [kbeg, kbeg + klen) read with
+// 16-byte loads, converted to FP16 times 2^sig[n] (the shift that puts row
+// n's largest magnitude in [2^14, 2^15); exact for BF16, one rounding for
+// FP32) into the 128-byte swizzled K-block layout, rows [nr, rb) zero; with
+// rms != nullptr also rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.
+// Warp ew takes rows ew, ew + 4, ... two at a time (their loads in flight
+// together) when a row needs at most 8 loads a lane.  The four epilogue
+// warps; klen / 256 * (4 / sizeof(T)) <= kStageSlots.
+template <typename T, typename RowFn>
+__device__ __forceinline__ void stage_rows(RowFn rowp, int nr, int rb, int kbeg, int klen,
+                                           uint32_t xs, int* sig, float* rms, int ew, int lane) {
+  constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
+  const int ppr = (klen >> 8) * kLd;  // loads per lane per row
+  if (ppr * 2 <= kStageSlots) {
+    for (int n = ew; n < rb; n += 2 * kEpiWarps) {
+      uint4 b0[kStageSlots], b1[kStageSlots];
+      const int n1 = n + kEpiWarps;
+      stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
+      stage_row_load<T>(rowp(n1 < nr ? n1 : 0), n1, nr, kbeg, ppr, lane, b1);
+      stage_row_finish<T>(b0, n, nr, rb, ppr, xs, sig, rms, klen, lane);
+      stage_row_finish<T>(b1, n1, nr, rb, ppr, xs, sig, rms, klen, lane);
+    }
+  } else {
+    for (int n = ew; n < rb; n += kEpiWarps) {
+      uint4 b0[kStageSlots];
+      stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
+      stage_row_finish<T>(b0, n, nr, rb, ppr, xs, sig, rms, klen, lane);
+    }
   }
 }
 
@@ -702,6 +668,10 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 #pragma unroll
   for (int ci = 0; ci < kDecChunks; ++ci) chunk_off[ci] = code_off + (((c0 + ci) ^ (lane & 7)) << 4);
   uint32_t ab = acount % kABufs, aph = (acount / kABufs) & 1u;
+  // A buffer whose tensor-memory stores are issued but not yet waited for:
+  // announced (a_full) after the first chunk of the next stage is converted,
+  // so the wait for the stores overlaps that conversion
+  int pend = -1;
   for (long u = u0; u < u1; ++u) {
     if (!wait_u32(rfull_u + 8u * rstage, rphase, status, abort_flag)) break;
     const uint32_t st = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
@@ -732,8 +702,8 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
     for (int ci = 0; ci < kDecChunks; ++ci) {
       const uint32_t sw = sbw[ci >> 1] >> (16 * (ci & 1));
       const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
-      const uint32_t s_lo = e4m3_bcast_f16x2(sw & 0xFFu);
-      const uint32_t s_hi = e4m3_bcast_f16x2((sw >> 8) & 0xFFu);
+      uint32_t s_lo, s_hi;
+      e4m3x2_bcast_f16x2(sw, s_lo, s_hi);
       uint32_t v[16];
 #pragma unroll
       for (int wi = 0; wi < 4; ++wi) {
@@ -742,12 +712,16 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[4 * wi + e] = hmul2(v[4 * wi + e], sv);
       }
+      if (ci == 0 && pend >= 0) {
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_u32(afull_u + 8u * static_cast<uint32_t>(pend));
+        pend = -1;
+      }
       tc::st_x16(lane_addr + kACols * ab + 16 * (c0 + ci), v);
     }
-    tc::wait_st();
-    tc::fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive_u32(afull_u + 8u * ab);
+    pend = static_cast<int>(ab);
     ++acount;
     if (++ab == kABufs) {
       ab = 0;
@@ -757,6 +731,12 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
       rstage = 0;
       rphase ^= 1u;
     }
+  }
+  if (pend >= 0) {
+    tc::wait_st();
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_u32(afull_u + 8u * static_cast<uint32_t>(pend));
   }
   if (MODE != kTcDense) cur.release(c, op, lane == 0);
 }
@@ -832,16 +812,16 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
         if (MODE == kTcDown) {
           const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
           const int I = a.I;
-          stage_b<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
-                         kbeg, klen, c.xs(), sig, nullptr, ew, lane, kEpiWarps);
+          stage_rows<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
+                            kbeg, klen, smem_u32(c.xs()), sig, nullptr, ew, lane);
         } else {
           // the RMS factors too when the staged range covers K
           const bool stage_rms = a.rms && !rms_ready && xst.k0 == 0 && xst.k1 == wk.nkb;
           rms_ready = rms_ready || stage_rms;
           const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
           const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
-          stage_bf16_rows([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen, smem_u32(c.xs()),
-                          sig, stage_rms ? rms : nullptr, ew, lane);
+          stage_rows<__nv_bfloat16>([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen,
+                                    smem_u32(c.xs()), sig, stage_rms ? rms : nullptr, ew, lane);
         }
         fence_proxy_async_smem();
         esync();
