@@ -281,6 +281,10 @@ struct Cta {
   __device__ __forceinline__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + kTcOffMisc); }
   __device__ __forceinline__ volatile int* abort_flag() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 4); }
   __device__ __forceinline__ volatile int* bcast() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 8); }
+  // ops whose epilogue this CTA has finished (the decode warps start an op's
+  // weights only after the previous op's epilogue: its tail and the next
+  // op's activation staging then run without the decode competing for issue)
+  __device__ __forceinline__ volatile int* epi_done() const { return reinterpret_cast<volatile int*>(base + kTcOffMisc + 448); }
   __device__ __forceinline__ int* sig() const { return reinterpret_cast<int*>(base + kTcOffMisc + 64); }
   __device__ __forceinline__ float* rms() const { return reinterpret_cast<float*>(base + kTcOffMisc + 192); }
   __device__ __forceinline__ float* ep() const { return reinterpret_cast<float*>(base + kTcOffEp); }
@@ -1124,6 +1128,18 @@ __device__ __forceinline__ void decode_role(const TcProgram& prog, const Cta& c,
   uint32_t rphase = 0;
   for (int i = 0; i < prog.n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);
+    if (i > 0 && op.mode != kTcCombine) {
+      // wait (bounded) until this CTA's epilogue finished op i - 1
+      const unsigned long long t0 = globaltimer();
+      while (*c.epi_done() < i && !c.aborted()) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+          atomicOr(c.status(), kStatusTimeout);
+          *c.abort_flag() = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
     switch (op.mode) {
       case kTcDense: decode_op<kTcDense>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcGateUp: decode_op<kTcGateUp>(c, op, cur, warp, lane, acount, rstage, rphase); break;
@@ -1168,6 +1184,7 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
       esync();
       if (etid == 0) {
         red_add_release_gpu(&prog.done[i], 1u);
+        *c.epi_done() = i + 1;
       }
     }
   }
@@ -1231,6 +1248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(c.x_tma(), 1);
     fence_mbarrier_init();
     *c.abort_flag() = 0;
+    *c.epi_done() = 0;
   }
   if (warp == 1) tc::tmem_alloc(c.tmem_slot(), kTmemCols);
   __syncthreads();
