@@ -120,6 +120,33 @@ int weight_maps(CUtensorMap* mc, CUtensorMap* ms, const uint8_t* codes, const ui
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// gate_up stack [E, 2I, K] (codes: K/2 bytes a row, scales: K/16) as a 4-D
+// uint8 map (bytes of a row, row within the half, gate/up half, expert) read
+// in boxes of 64 rows of both halves: one box = a 128-row gate_up tile (gate
+// rows then the same up rows).  Codes use the 128-byte swizzle.
+int gate_up_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t inter,
+                uint64_t experts, uint32_t box_bytes, bool swizzle) {
+  const cuuint64_t dims[4] = {row_bytes, inter, 2, experts};
+  const cuuint64_t strides[3] = {row_bytes, row_bytes * inter, row_bytes * inter * 2};
+  const cuuint32_t box[4] = {box_bytes, 64, 2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (gate_up) failed (%d)", (int)r);
+  return NVFP4_OK;
+}
+
+int gate_up_maps(CUtensorMap* mc, CUtensorMap* ms, const uint8_t* codes, const uint8_t* scales,
+                 int I, int H, int E) {
+  int rc = gate_up_map(mc, codes, static_cast<uint64_t>(H) / 2, I, E, kStageK / 2, true);
+  if (rc) return rc;
+  return gate_up_map(ms, scales, static_cast<uint64_t>(H) / 16, I, E, kStageK / 16, false);
+}
+
+
+
 // ------------------------------------------------------------- dense plan
 struct DensePlan {
   int n_tiles, nkb, grid, mpad, win_stages, xrow_bytes;
@@ -383,10 +410,10 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   const nvfp4_expert_stack* sh = shared ? shared : experts;
   memset(gu, 0, sizeof(*gu));
   int rc;
-  if ((rc = weight_maps(&gu->maps[0], &gu->maps[1], experts->gu_codes, experts->gu_scales,
-                        2ull * I * E, H)) ||
-      (rc = weight_maps(&gu->maps[2], &gu->maps[3], sh->gu_codes, sh->gu_scales,
-                        2ull * I * sh->num_experts, H)) ||
+  if ((rc = gate_up_maps(&gu->maps[0], &gu->maps[1], experts->gu_codes, experts->gu_scales, I, H,
+                         E)) ||
+      (rc = gate_up_maps(&gu->maps[2], &gu->maps[3], sh->gu_codes, sh->gu_scales, I, H,
+                         sh->num_experts)) ||
       (rc = act_map(&gu->xmap, x, T, ldx, H, p.xrows)))
     return rc;
   TcArgs& a = gu->a;

@@ -185,6 +185,17 @@ __device__ __forceinline__ void tma_load_2d_u32(uint32_t smem_dst, const CUtenso
       : "memory");
 }
 
+// 4-D tiled bulk tensor load (x innermost, a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_4d_u32(uint32_t smem_dst, const CUtensorMap* map, int x,
+                                                int y, int z, int w, uint32_t bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Contiguous bulk copy global -> shared (16-byte aligned addresses, size a
 // multiple of 16), completion signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load_u32(uint32_t smem_dst, const void* src, uint32_t bytes,
@@ -210,6 +221,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

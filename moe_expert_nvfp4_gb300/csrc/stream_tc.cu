@@ -53,7 +53,7 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kBox = 32;
+constexpr int kGuRows = 64;                    // gate (and up) rows of a gate_up tile
 constexpr int kSK = 256;                       // K per stage
 constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
 constexpr int kDecWarps = NVFP4_DEC_WARPS;
@@ -150,6 +150,7 @@ struct Box {
   const CUtensorMap* mc;
   const CUtensorMap* ms;
   int row;
+  int expert;  // gate_up (4-D maps): expert coordinate
 };
 
 // Per-launch work description shared by all roles (all fields derived
@@ -157,7 +158,7 @@ struct Box {
 // The op's units are split over G CTAs: relative index r = the CTA
 // (blockIdx.x - cta0) mod gridDim.x; r >= G has none.
 struct Work {
-  int n_tiles, nkb, per_e, pb_count;
+  int n_tiles, nkb, per_e;
   long U;
   int G, cta0;
   __device__ __forceinline__ long begin(int r) const { return static_cast<long>(r) * U / G; }
@@ -177,27 +178,21 @@ struct Kernel {
   const Work& wk;
   const CUtensorMap *m0, *m1, *m2, *m3;
 
-  // expert of a gate_up pair-box / down tile
-  __device__ __forceinline__ int pb_expert(int pb) const { return sc.active[pb / wk.per_e]; }
+  // expert of a MoE tile
+  __device__ __forceinline__ int tile_expert(int tile) const { return sc.active[tile / wk.per_e]; }
 
   __device__ __forceinline__ void tile_boxes(int tile, Box (&bx)[4]) const {
     if (MODE == kTcDense) {
-      bx[0] = Box{m0, m1, tile * kRows};  // one 128-row box
+      bx[0] = Box{m0, m1, tile * kRows, 0};  // one 128-row box
     } else if (MODE == kTcGateUp) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        int pb = 2 * tile + h;
-        if (pb >= wk.pb_count) pb = 2 * tile;  // odd count: repeat the first pair-box
-        const int e = pb_expert(pb), jb = pb % wk.per_e;
-        const bool sh = (e == a.E);
-        const int base = sh ? 0 : e * 2 * a.I;
-        bx[2 * h] = Box{sh ? m2 : m0, sh ? m3 : m1, base + jb * kBox};
-        bx[2 * h + 1] = Box{sh ? m2 : m0, sh ? m3 : m1, base + a.I + jb * kBox};
-      }
+      // one 4-D box: gate rows 64 j .. 64 j + 63 then the same up rows
+      const int e = tile_expert(tile), j = tile % wk.per_e;
+      const bool sh = (e == a.E);
+      bx[0] = Box{sh ? m2 : m0, sh ? m3 : m1, kGuRows * j, sh ? 0 : e};
     } else {
       const int e = sc.active[tile / wk.per_e], nt = tile % wk.per_e;
       const bool sh = (e == a.E);
-      bx[0] = Box{sh ? m2 : m0, sh ? m3 : m1, (sh ? 0 : e * a.H) + nt * kRows};  // one 128-row box
+      bx[0] = Box{sh ? m2 : m0, sh ? m3 : m1, (sh ? 0 : e * a.H) + nt * kRows, 0};  // one 128-row box
     }
   }
 
@@ -336,9 +331,8 @@ __device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, cons
   } else {
     const int na = c.aborted() ? 0 : min(max(*sc.n_active, 0), a.E + 1);
     if (MODE == kTcGateUp) {
-      wk.per_e = a.I / kBox;
-      wk.pb_count = na * wk.per_e;
-      wk.n_tiles = (wk.pb_count + 1) / 2;
+      wk.per_e = a.I / kGuRows;
+      wk.n_tiles = na * wk.per_e;
       wk.nkb = a.H / kSK;
     } else {
       wk.per_e = a.H / kRows;
@@ -543,12 +537,9 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
       mbar_arrive_expect_tx_u32(full, kTcStageBytes);
       const uint32_t st = ring_u + static_cast<uint32_t>(stage) * kTcStageBytes;
       if (MODE == kTcGateUp) {
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          tma_load_2d_u32(st + bb * (kCodeBytes / 4), bx[bb].mc, kb * (kSK / 2), bx[bb].row, full, pol);
-          tma_load_2d_u32(st + kCodeBytes + bb * (kRows * kSK / 16 / 4), bx[bb].ms, kb * (kSK / 16),
-                          bx[bb].row, full, pol);
-        }
+        tma_load_4d_u32(st, bx[0].mc, kb * (kSK / 2), bx[0].row, 0, bx[0].expert, full, pol);
+        tma_load_4d_u32(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, 0, bx[0].expert, full,
+                        pol);
       } else {
         tma_load_2d_u32(st, bx[0].mc, kb * (kSK / 2), bx[0].row, full, pol);
         tma_load_2d_u32(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, full, pol);
@@ -787,13 +778,10 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
     // weights stream) only when the expert changes, issued before the MMAs
     // are waited for
     if (MODE == kTcGateUp) {
-      const int pb = 2 * tile + (q >> 1);
-      if (!(q & 1) && pb < wk.pb_count) {
-        const int e = kk.pb_expert(pb);
-        if (e != g_expert) {
-          g_tile = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
-          g_expert = e;
-        }
+      const int e = kk.tile_expert(tile);
+      if (q < 2 && e != g_expert) {
+        g_tile = (e == a.E) ? *a.sh_gu_global : a.gu_global[e];
+        g_expert = e;
       }
     } else if (MODE == kTcDown) {
       const int e = sc.active[tile / wk.per_e];
@@ -978,16 +966,14 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
         }
       }
     } else if (MODE == kTcGateUp) {
-      // rows 0-31 gate and 32-63 up of pair-box 2*tile; 64-127 likewise
-      // for pair-box 2*tile+1 (absent when the count is odd)
-      if (q & 1) {
+      // rows 0-63: gate rows 64 j + r of expert e; rows 64-127 the same up rows
+      if (q >= 2) {
 #pragma unroll
         for (int j = 0; j < NC; ++j) ep[j * kRows + r] = tot[j];
       }
       esync();
-      const int pb = 2 * tile + (q >> 1);
-      if (!(q & 1) && pb < wk.pb_count) {
-        const int e = kk.pb_expert(pb), jb = pb % wk.per_e;
+      if (q < 2) {
+        const int e = kk.tile_expert(tile), jb = tile % wk.per_e;
         const float g = g_tile;
         const int cnt = sc.cnt[e], off = sc.off[e];
         for (int qq = 0; qq < cnt; ++qq) {
@@ -999,8 +985,8 @@ __device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCurs
           for (int j = 0; j < NC; ++j)
             if (j == t) gt = tot[j];
           gt *= f;
-          const float up = ep[t * kRows + r + 32] * f;
-          a.h[static_cast<size_t>(p) * a.I + jb * kBox + lane] = gt / (1.0f + expf(-gt)) * up;
+          const float up = ep[t * kRows + r + kGuRows] * f;
+          a.h[static_cast<size_t>(p) * a.I + jb * kGuRows + r] = gt / (1.0f + expf(-gt)) * up;
         }
       }
     } else {
@@ -1159,6 +1145,11 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
   pdl_launch_dependents();
   for (int i = 0; i < n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);
+    // the op's arguments (device op table, global memory) into L1 while
+    // waiting for the previous op: their first reads would otherwise be
+    // dependent trips to L2 after the wait
+    if (prog.ops && ew == 0 && lane < (static_cast<int>(sizeof(TcArgs)) + 127) / 128)
+      prefetch_l1(reinterpret_cast<const uint8_t*>(&op.a) + 128 * lane);
     if (i > 0 && op.wait_prev) {
       // every CTA has finished op i - 1: its outputs are complete
       if (etid == 0) grid_wait(&prog.done[i - 1], gridDim.x, c.status(), c.abort_flag());
