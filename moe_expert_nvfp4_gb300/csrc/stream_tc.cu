@@ -6,35 +6,33 @@
 // projection with the weighted top-k combine.  A single call of the C ABI is
 // a one-op program; a decode step is a program of a few hundred ops.
 //
-// Tile = 128 weight rows = the 128 lanes of tensor memory, built from four
-// independent 32-row TMA boxes (for gate_up: the gate and up boxes of two
-// 32-wide intermediate blocks, possibly of different experts).  Stage = one
-// tile x 256 K: 16 KB of 128B-swizzled E2M1 codes + 2 KB of E4M3 scales.
-// Work split: the (tile, stage) units of each op are cut into gridDim.x
-// equal contiguous ranges, one per CTA ("stream-K"); a tile split between
-// CTAs is reduced by the last CTA to finish it (atomic counter), adding the
-// per-CTA partials in CTA order, so results do not depend on timing.
+// Tile = 128 weight rows = the 128 lanes of tensor memory: 128 consecutive
+// rows (dense, down) or, for gate_up, one 4-D box of 64 gate rows of an
+// expert followed by the same 64 up rows.  Stage = one tile x 256 K: 16 KB
+// of 128B-swizzled E2M1 codes + 2 KB of E4M3 scales.
+// Work split: the (tile, stage) units of each op are cut into equal
+// contiguous ranges, one per CTA ("stream-K"); a tile split between CTAs is
+// reduced by the last CTA to finish it (atomic counter), adding the per-CTA
+// partials in CTA order, so results do not depend on timing.
 //
-// Warp roles (480 threads), each walking the whole program:
+// Warp roles (352 threads), each walking the whole program:
 //   warp 0       TMA producer: streams stages into a shared-memory ring of
 //                3..8 stages (full/empty mbarriers), running ahead into the
 //                next ops' weights while the current op finishes;
 //   warp 1       allocates tensor memory; one thread issues tcgen05.mma:
 //                D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
 //                memory), 16 MMAs per stage, N = tokens rounded up to 16;
-//   warps 2-9    decode: lane l of a warp in lane quarter q owns tile row
-//                32q + l; warps 2-5 decode the first 128 K of each stage,
-//                6-9 the second.  E2M1 -> FP16 by the hardware convert, times
-//                the E4M3 block scale (exact in FP16), written to one of three
-//                tensor-memory A buffers with tcgen05.st.  They only stream.
-//   warps 10-13  epilogue: wait until every CTA finished the previous op
+//   warps 2-5    decode: warp w owns lane quarter q = w % 4 (tile rows 32q ..
+//                32q + 31, lane l = row 32q + l) over the whole 256 K of a
+//                stage.  E2M1 -> FP16 by the hardware convert, times the E4M3
+//                block scale (exact in FP16), written to one of three
+//                tensor-memory A buffers with tcgen05.st;
+//   warps 6-9    epilogue: wait until every CTA finished the previous op
 //                (a completion counter per op), stage the activations (B)
-//                into shared memory as FP16 with a power-of-two shift per row
-//                and window, read the FP32 accumulator (two buffers) with
-//                tcgen05.ld, undo the shift, and run the stream-K reduction
-//                and the op's epilogue while the other roles go on with the
-//                next op;
-//   warp 14      builds the expert schedule of each MoE layer into one of
+//                into shared memory as FP16 with a power-of-two shift per row,
+//                read the FP32 accumulator with tcgen05.ld, undo the shift,
+//                and run the stream-K reduction and the op's epilogue;
+//   warp 10      builds the expert schedule of each MoE layer into one of
 //                two shared-memory slots.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
