@@ -86,11 +86,9 @@ constexpr int kTcOffBars = 0;                            // up to 64 mbarriers
 constexpr int kTcOffMisc = 512;
 constexpr int kTcOffEp = 1024;
 constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17408
-#ifndef NVFP4_DEC_WARPS
-#define NVFP4_DEC_WARPS 4
-#endif
-// producer, MMA, NVFP4_DEC_WARPS decode, 4 epilogue warps, scheduler warp
-constexpr int kTcThreads = (3 + NVFP4_DEC_WARPS + 4) * 32;
+// four warpgroups: {producer, MMA, scheduler, idle}, 4 epilogue warps,
+// 8 decode warps (registers rebalanced per warpgroup with setmaxnreg)
+constexpr int kTcThreads = 512;
 constexpr int kTcColCntBase = 8192;                      // tile counters stay below this index
 constexpr int kTcDoneBase = 12288;                       // per-op completion counters
 constexpr int kTcMaxOps = kWsMaxCounters - kTcDoneBase - 1;

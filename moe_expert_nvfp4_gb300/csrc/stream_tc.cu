@@ -15,24 +15,25 @@
 // reduced by the last CTA to finish it (atomic counter), adding the per-CTA
 // partials in CTA order, so results do not depend on timing.
 //
-// Warp roles (352 threads), each walking the whole program:
+// Warp roles (512 threads, four warpgroups; setmaxnreg moves registers to
+// the epilogue warpgroup), each walking the whole program:
 //   warp 0       TMA producer: streams stages into a shared-memory ring of
 //                3..8 stages (full/empty mbarriers), running ahead into the
 //                next ops' weights while the current op finishes;
 //   warp 1       allocates tensor memory; one thread issues tcgen05.mma:
 //                D[128 x N] += A[128 x 16] (tensor memory) * B[N x 16] (shared
 //                memory), 16 MMAs per stage, N = tokens rounded up to 16;
-//   warps 2-5    decode: warp w owns lane quarter q = w % 4 (tile rows 32q ..
-//                32q + 31, lane l = row 32q + l) over the whole 256 K of a
-//                stage.  E2M1 -> FP16 by the hardware convert, times the E4M3
+//   warps 8-15   decode: warp w owns lane quarter q = w % 4 (tile rows 32q ..
+//                32q + 31, lane l = row 32q + l); warps 8-11 the first 128 K
+//                of each stage, 12-15 the second.  E2M1 -> FP16 by the hardware convert, times the E4M3
 //                block scale (exact in FP16), written to one of three
 //                tensor-memory A buffers with tcgen05.st;
-//   warps 6-9    epilogue: wait until every CTA finished the previous op
+//   warps 4-7    epilogue: wait until every CTA finished the previous op
 //                (a completion counter per op), stage the activations (B)
 //                into shared memory as FP16 with a power-of-two shift per row,
 //                read the FP32 accumulator with tcgen05.ld, undo the shift,
 //                and run the stream-K reduction and the op's epilogue;
-//   warp 10      builds the expert schedule of each MoE layer into one of
+//   warp 2       builds the expert schedule of each MoE layer into one of
 //                two shared-memory slots.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
@@ -54,12 +55,14 @@ constexpr int kRows = 128;
 constexpr int kGuRows = 64;                    // gate (and up) rows of a gate_up tile
 constexpr int kSK = 256;                       // K per stage
 constexpr int kCodeBytes = kRows * kSK / 2;    // 16384
-constexpr int kDecWarps = NVFP4_DEC_WARPS;
+constexpr int kDecWarps = 8;
 constexpr int kDecChunks = 8 * 4 / kDecWarps;  // 32-K chunks a decode warp converts per stage
 constexpr int kEpiWarps = 4;                   // one per tensor-memory lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kEpiWarp0 = 2 + kDecWarps;       // warps 10..13
-constexpr int kSchedWarp = kEpiWarp0 + kEpiWarps;  // warp 14
+// warpgroup 0: producer (warp 0), MMA (1), scheduler (2), idle (3);
+// warpgroup 1: epilogue (4-7); warpgroups 2-3: decode (8-15)
+constexpr int kEpiWarp0 = 4;
+constexpr int kDecWarp0 = 8;
 // arrivals that release a schedule slot: producer, MMA thread, 8 decode
 // warps, 4 epilogue warps
 constexpr int kSchedUsers = 2 + kDecWarps + kEpiWarps;
@@ -76,11 +79,25 @@ constexpr int kDBufs = 4;                      // accumulator buffers (32 column
 constexpr uint32_t kTmemCols = 512;
 
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
-static_assert(kTcThreads == (3 + kDecWarps + kEpiWarps) * 32, "thread count");
-static_assert(kDecWarps == 4 || kDecWarps == 8, "decode warps cover the 4 lane quarters");
+static_assert(kTcThreads == (kDecWarp0 + kDecWarps) * 32, "thread count");
+static_assert(kDecWarps == 8 && kEpiWarp0 == 4 && kEpiWarps == 4, "warpgroup layout");
+// per-warpgroup registers after setmaxnreg: 128 x (96 + 200) + 256 x 96 =
+// 62,464 <= 65,536 (512 threads x 128 at launch)
+constexpr int kRegsSmall = 96;
+constexpr int kRegsEpilogue = 200;
+static_assert(128 * (kRegsSmall + kRegsEpilogue) + 256 * kRegsSmall <= 65536, "register split");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void esync() {  // the four epilogue warps
@@ -642,7 +659,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   make_work<MODE>(op.a, sc, c, u0, u1);
   // warp dw decodes lane quarter q (tile rows 32q .. 32q + 31), chunks
   // [c0, c0 + kDecChunks) of 32 K each (8 chunks per 256-K stage)
-  const int dw = warp - 2, q = warp & 3, c0 = (dw >> 2) * kDecChunks;
+  const int dw = warp - kDecWarp0, q = warp & 3, c0 = (dw >> 2) * kDecChunks;
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
   // loop constants in registers (shared-memory addresses as 32-bit values)
   const uint32_t ring_u = smem_u32(c.ring());
@@ -736,9 +753,8 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 
 // Epilogue warps, one op: activation staging, accumulator folds, stream-K
 // reduction and the op's epilogue.
-// (Not inlined: each mode gets its own register allocation.)
 template <int MODE, int NC>
-__device__ __noinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
+__device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
                                          int ew, int lane, uint32_t& dcount) {
   const TcArgs& a = op.a;
   const int q = (kEpiWarp0 + ew) & 3;
@@ -1244,16 +1260,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::fence_after_sync();
   c.tmem = *c.tmem_slot();
 
-  if (warp == 0) {
-    producer_role(prog, c, lane);
-  } else if (warp == 1) {
-    mma_role(prog, c, lane);
-  } else if (warp < kEpiWarp0) {
-    decode_role(prog, c, warp, lane);
-  } else if (warp < kSchedWarp) {
+  // registers move from the warpgroups that need few (producer, MMA,
+  // scheduler; decode) to the epilogue warpgroup
+  if (warp < kEpiWarp0) {
+    setmaxnreg_dec<kRegsSmall>();
+    if (warp == 0) producer_role(prog, c, lane);
+    else if (warp == 1) mma_role(prog, c, lane);
+    else if (warp == 2) sched_role(prog, c, lane);
+  } else if (warp < kDecWarp0) {
+    setmaxnreg_inc<kRegsEpilogue>();
     epilogue_role(prog, c, warp, lane);
   } else {
-    sched_role(prog, c, lane);
+    setmaxnreg_dec<kRegsSmall>();
+    decode_role(prog, c, warp, lane);
   }
 
   __syncthreads();
