@@ -246,6 +246,118 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ per-workload context
+
+def graph_us(fn, reps, warmup=3):
+    """Device microseconds per replay of a CUDA graph of fn() (CUDA events on
+    the current stream, after warm-up replays)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ms = timed_replays(g, reps, torch.cuda.current_stream())
+    del g
+    return ms * 1e3
+
+
+def workload_table(model, reps=10):
+    """Microseconds and weight GB/s of the other workloads the metric is quoted
+    on, each timed as a CUDA graph of back-to-back calls over weight copies
+    that together exceed L2 (so every call reads HBM):
+
+    * the 2048 -> 64 projection at M = 4 (one call: latency-bound);
+    * the dense sweep: M in {1, 4, 8, 16, 32} x {4096 x 2048, 8192 x 2048,
+      2048 x 4096} (seeds 1-3);
+    * the MoE layer (256 routed + 1 shared experts, hidden 2048, inter 512,
+      top-8) at T in {1, 4, 8, 16, 32}, over the step's layer weights;
+    * the MTP-verify batch: the MoE layer at T = 32 then the 151,936 x 2048
+      head with argmax."""
+    import torch
+    from moe_expert_nvfp4_gb300 import ops, synth
+    from moe_expert_nvfp4_gb300.decode_step import nvfp4_bytes
+    dev = "cuda"
+    g1 = torch.full((1,), synth.GLOBAL_SCALE, dtype=torch.float32, device=dev)
+    out = {}
+
+    def weights(seed, n, k, count):
+        return [ops.NVFP4Weight(*synth.nvfp4_weight(seed, n, k, 40 + i, device=dev), g1)
+                for i in range(count)]
+
+    # the 2048 -> 64 projection at M = 4
+    ws64 = weights(0, 64, 2048, 1)
+    a = synth.activations_bf16(0, 4, 2048).to(dev)
+    c = torch.empty(4, 64, dtype=torch.bfloat16, device=dev)
+    wk = ops.Workspace(ops.gemm_workspace_bytes(4, 64, 2048))
+    us = graph_us(lambda: ops.gemm(a, ws64[0], out=c, workspace=wk), reps)
+    out["proj_2048x64_M4"] = {"us": us, "gbs": nvfp4_bytes(64, 2048) / us / 1e3}
+
+    # dense sweep; 24 rotating copies of each shape (>= 113 MB each set)
+    for seed, (n, k) in zip((1, 2, 3), ((4096, 2048), (8192, 2048), (2048, 4096))):
+        copies = weights(seed, n, k, 24 if n * k <= 4096 * 2048 else 16)
+        wk = ops.Workspace(max(ops.gemm_workspace_bytes(m, n, k) for m in (1, 32)))
+        for m in (1, 4, 8, 16, 32):
+            a = synth.activations_bf16(seed, m, k).to(dev)
+            c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+
+            def calls():
+                for w in copies:
+                    ops.gemm(a, w, out=c, workspace=wk)
+            us = graph_us(calls, reps) / len(copies)
+            out[f"dense_{n}x{k}_M{m}"] = {"us": us, "gbs": nvfp4_bytes(n, k) / us / 1e3}
+        del copies
+
+    # MoE layer over the step's layers (each layer's experts are distinct weights)
+    s = model.s
+    per_expert = nvfp4_bytes(2 * s.inter, s.hidden) + nvfp4_bytes(s.hidden, s.inter)
+    L = min(16, s.layers)
+    for t in (1, 4, 8, 16, 32):
+        x = synth.activations_bf16(4, t, s.hidden).to(dev)
+        lg = torch.cat([synth.router_logits(4, t, s.num_experts, l) for l in range(L)]).to(dev)
+        ids, wts = ops.route(lg, s.top_k)
+        y = torch.empty(t, s.hidden, dtype=torch.bfloat16, device=dev)
+        wk = ops.Workspace(ops.moe_workspace_bytes(t, s.top_k, model.experts[0]))
+        idl = ids.view(L, -1).cpu()
+        nbytes = sum((torch.unique(idl[l]).numel() + 1) * per_expert for l in range(L))
+
+        def layers():
+            for l in range(L):
+                ops.moe(x, ids[l * t:(l + 1) * t], wts[l * t:(l + 1) * t], model.experts[l],
+                        model.shared[l], out=y, workspace=wk, ids_ready=True)
+        us = graph_us(layers, reps)
+        out[f"moe_T{t}"] = {"us": us / L, "gbs": nbytes / us / 1e3}
+
+    # MTP-verify batch: MoE layer at T = 32, then the head with argmax
+    t = 32
+    x = synth.activations_bf16(5, t, s.hidden).to(dev)
+    lg = torch.cat([synth.router_logits(5, t, s.num_experts, l) for l in range(L)]).to(dev)
+    ids, wts = ops.route(lg, s.top_k)
+    y = torch.empty(t, s.hidden, dtype=torch.bfloat16, device=dev)
+    logits = torch.empty(t, s.vocab, dtype=torch.bfloat16, device=dev)
+    am = torch.empty(t, dtype=torch.int32, device=dev)
+    wk = ops.Workspace(max(ops.moe_workspace_bytes(t, s.top_k, model.experts[0]),
+                           ops.gemm_workspace_bytes(t, s.vocab, s.hidden)))
+    idl = ids.view(L, -1).cpu()
+    head_bytes = nvfp4_bytes(s.vocab, s.hidden)
+    nbytes = sum((torch.unique(idl[l]).numel() + 1) * per_expert + head_bytes for l in range(L))
+
+    def verify():
+        for l in range(L):
+            ops.moe(x, ids[l * t:(l + 1) * t], wts[l * t:(l + 1) * t], model.experts[l],
+                    model.shared[l], out=y, workspace=wk, ids_ready=True)
+            ops.gemm(y, model.head, out=logits, argmax_out=am, workspace=wk)
+    us = graph_us(verify, reps)
+    out["mtp_verify_T32"] = {"us": us / L, "gbs": nbytes / us / 1e3}
+    for v in out.values():
+        v["us"] = round(v["us"], 2)
+        v["gbs"] = round(v["gbs"], 1)
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, rank, world, local):
@@ -393,6 +505,9 @@ def run_ours(args, rank, world, local):
                               "weight_bytes": nb2}
             del g2
 
+    # ---- the other workloads of the metric (context: µs and GB/s per call)
+    workloads = workload_table(model) if not args.no_sweep else None
+
     # ---- the same step issued call by call (one kernel per call), for context
     calls = None
     if args.path == "program" and not args.no_sweep:
@@ -429,7 +544,7 @@ def run_ours(args, rank, world, local):
                        "parallelism": f"{world} independent replica(s)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": n_launch * args.steps, "clocks": clocks, "sweep": sweep,
-            "path": args.path, "call_by_call": calls,
+            "path": args.path, "call_by_call": calls, "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
