@@ -411,59 +411,111 @@ __device__ __forceinline__ void stage_row_load(const T* row, int n, int nr, int 
   }
 }
 
-// Two elements of a load as floats.
+// Largest magnitude (as a float) and sum of squares of a row's loads.
 template <typename T>
-__device__ __forceinline__ float2 stage_pair(const uint4& v, int j) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  if constexpr (sizeof(T) == 2) {
-    return make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
-  } else {
-    return make_float2(__uint_as_float(w[(2 * j) & 3]), __uint_as_float(w[(2 * j + 1) & 3]));
-  }
-}
-
-// Largest magnitude and sum of squares of a row's loads, the row shift, and
-// the FP16 conversion stored into the staged layout.
-template <typename T>
-__device__ __forceinline__ void stage_row_finish(const uint4 (&b)[kStageSlots], int n, int nr,
-                                                 int rb, int ppr, uint32_t xs, int* sig,
-                                                 float* rms, int klen, int lane) {
-  constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
-  constexpr int kPairs = sizeof(T) == 2 ? 4 : 2;  // element pairs per 16-byte load
-  if (n >= rb) return;
-  float m = 0.0f, sq = 0.0f;
+__device__ __forceinline__ void stage_row_stats(const uint4 (&b)[kStageSlots], int ppr, bool want_sq,
+                                                float& m, float& sq) {
+  uint32_t mx = 0u;  // BF16: the largest |x| of each half as bits (|x| orders like its bits)
+  float mf = 0.0f;
+  sq = 0.0f;
 #pragma unroll
   for (int i = 0; i < kStageSlots; ++i)
     if (i < ppr) {
+      const uint32_t w[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
 #pragma unroll
-      for (int j = 0; j < kPairs; ++j) {
-        const float2 f = stage_pair<T>(b[i], j);
-        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-        sq = fmaf(f.x, f.x, sq);
-        sq = fmaf(f.y, f.y, sq);
+      for (int j = 0; j < 4; ++j) {
+        if constexpr (sizeof(T) == 2) {
+          mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);
+          if (want_sq) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+          }
+        } else {
+          const float f = __uint_as_float(w[j]);
+          mf = fmaxf(mf, fabsf(f));
+          if (want_sq) sq = fmaf(f, f, sq);
+        }
       }
     }
-  m = warp_max(m);
-  const int sh = n < nr ? f16_row_shift(m) : 0;
-  if (rms && n < nr) {
-    sq = warp_sum(sq);
-    if (lane == 0) rms[n] = rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
-  }
-  const int h1 = sh / 2;
+  if constexpr (sizeof(T) == 2)
+    m = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+  else
+    m = mf;
+}
+
+// The FP16 conversion of a row's loads times 2^sh, stored into the staged
+// layout: load i of lane l holds chunk kc = l + 32 i / kLd, whose 16-byte
+// slot is at base(n, l) + (i / kLd) * 4 * rb * 128 (xoff with k = 8 kc).
+template <typename T>
+__device__ __forceinline__ void stage_row_store(const uint4 (&b)[kStageSlots], int n, int rb,
+                                                int ppr, int sh, uint32_t xs, int lane) {
+  constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
+  // one factor when 2^sh is a normal float, else two steps
+  const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
   const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+  const bool two = h1 != sh;
+  const uint32_t base = xs + xoff(n, 8 * lane, rb);
+  const uint32_t step = static_cast<uint32_t>(4 * rb * 128);
 #pragma unroll
   for (int i = 0; i < kStageSlots; i += kLd)
     if (i < ppr) {
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 f = stage_pair<T>(b[i + (kLd == 2 ? (j >> 1) : 0)], kLd == 2 ? (j & 1) : j);
-        o[j] = pack_f16x2(f.x * f1 * f2, f.y * f1 * f2);
+        float lo, hi;
+        if constexpr (sizeof(T) == 2) {
+          const uint32_t w = j == 0 ? b[i].x : j == 1 ? b[i].y : j == 2 ? b[i].z : b[i].w;
+          lo = __uint_as_float(w << 16);
+          hi = __uint_as_float(w & 0xFFFF0000u);
+        } else {
+          const uint4& v = b[i + (j >> 1)];
+          lo = __uint_as_float((j & 1) ? v.z : v.x);
+          hi = __uint_as_float((j & 1) ? v.w : v.y);
+        }
+        lo *= f1;
+        hi *= f1;
+        if (two) {
+          lo *= f2;
+          hi *= f2;
+        }
+        o[j] = pack_f16x2(lo, hi);
       }
-      const int kc = lane + 32 * (i / kLd);
-      st_shared_v4(xs + xoff(n, 8 * kc, rb), make_uint4(o[0], o[1], o[2], o[3]));
+      st_shared_v4(base + static_cast<uint32_t>(i / kLd) * step, make_uint4(o[0], o[1], o[2], o[3]));
     }
-  if (lane == 0) sig[n] = sh;
+}
+
+// Rows n0 and n1 (n1 may be past rb): statistics of both, their warp
+// reductions interleaved, the shifts, rms and the stores.
+template <typename T>
+__device__ __forceinline__ void stage_row_pair(const uint4 (&b0)[kStageSlots],
+                                               const uint4 (&b1)[kStageSlots], int n0, int n1,
+                                               int nr, int rb, int ppr, uint32_t xs, int* sig,
+                                               float* rms, int klen, int lane) {
+  float m0, s0, m1 = 0.0f, s1 = 0.0f;
+  const bool has1 = n1 < rb;
+  stage_row_stats<T>(b0, ppr, rms != nullptr, m0, s0);
+  if (has1) stage_row_stats<T>(b1, ppr, rms != nullptr, m1, s1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    if (rms) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    }
+  }
+  const int sh0 = n0 < nr ? f16_row_shift(m0) : 0;
+  const int sh1 = n1 < nr ? f16_row_shift(m1) : 0;
+  if (lane == 0) {
+    sig[n0] = sh0;
+    if (rms && n0 < nr) rms[n0] = rsqrtf(s0 / static_cast<float>(klen) + 1e-6f);
+    if (has1) {
+      sig[n1] = sh1;
+      if (rms && n1 < nr) rms[n1] = rsqrtf(s1 / static_cast<float>(klen) + 1e-6f);
+    }
+  }
+  stage_row_store<T>(b0, n0, rb, ppr, sh0, xs, lane);
+  if (has1) stage_row_store<T>(b1, n1, rb, ppr, sh1, xs, lane);
 }
 
 // Activations staged through registers in one pass: BF16 (dense A, MoE x)
@@ -486,14 +538,13 @@ __device__ __forceinline__ void stage_rows(RowFn rowp, int nr, int rb, int kbeg,
       const int n1 = n + kEpiWarps;
       stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
       stage_row_load<T>(rowp(n1 < nr ? n1 : 0), n1, nr, kbeg, ppr, lane, b1);
-      stage_row_finish<T>(b0, n, nr, rb, ppr, xs, sig, rms, klen, lane);
-      stage_row_finish<T>(b1, n1, nr, rb, ppr, xs, sig, rms, klen, lane);
+      stage_row_pair<T>(b0, b1, n, n1, nr, rb, ppr, xs, sig, rms, klen, lane);
     }
   } else {
     for (int n = ew; n < rb; n += kEpiWarps) {
       uint4 b0[kStageSlots];
       stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
-      stage_row_finish<T>(b0, n, nr, rb, ppr, xs, sig, rms, klen, lane);
+      stage_row_pair<T>(b0, b0, n, rb, nr, rb, ppr, xs, sig, rms, klen, lane);
     }
   }
 }
@@ -821,8 +872,11 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
           stage_rows<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
                             kbeg, klen, smem_u32(c.xs()), sig, nullptr, ew, lane);
         } else {
-          // the RMS factors too when the staged range covers K
-          const bool stage_rms = a.rms && !rms_ready && xst.k0 == 0 && xst.k1 == wk.nkb;
+          // gate_up: the RMS factors from the staged rows (its K is always
+          // staged whole).  Dense ops take them from global memory below, in
+          // every CTA the same way: the CTA that finishes a split tile applies
+          // its own factor, so all CTAs must compute it bit for bit alike.
+          const bool stage_rms = MODE == kTcGateUp && a.rms && !rms_ready;
           rms_ready = rms_ready || stage_rms;
           const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
           const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
@@ -833,8 +887,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         esync();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.x_full());
-        // dense staged over part of K: the RMS factor of each row over the
-        // whole K from global memory, while the MMAs run
+        // dense: the RMS factor of each row over the whole K from global
+        // memory, while the MMAs run
         if (MODE == kTcDense && a.rms && !rms_ready) {
           for (int m = ew; m < a.M; m += kEpiWarps) {
             float ss = 0.0f;
