@@ -259,7 +259,7 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
   p->off_partials = kWsScratch;  // one pair of partial slots for every SM: programs
                                  // may place the op on any CTA
   p->off_am = round_up(p->off_partials + 4ull * sms * 2 * 32 * 128, 256);
-  p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
+  p->ws_bytes = round_up(p->off_am + 8ull * M * sms, 256);  // argmax: one partial per CTA
   return true;
 }
 

@@ -130,7 +130,7 @@ struct TcArgs {
   uint32_t* tile_cnt;   // counters region
   uint32_t* argmax_cnt;
   float* partials;      // [grid][2][32][128]
-  int2* am_part;        // [M][n_tiles]
+  int2* am_part;        // [M][CTAs of the op]: each CTA's best (value bits, index) per row
 };
 
 // Staged activation rows for n real rows: 8, 16 or 32 (the MMA's N is 16

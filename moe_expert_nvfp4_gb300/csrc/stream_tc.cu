@@ -829,6 +829,10 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   float g_tile = 0.0f;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
   const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
+  // dense argmax: lane i of epilogue warp ew keeps the running best of row
+  // m = ew + kEpiWarps i over the CTA's finished tiles
+  float am_v = -FLT_MAX;
+  int am_i = 0x7fffffff;
 
   for (long u = u0; u < u1;) {
     if (c.aborted()) break;
@@ -1005,32 +1009,10 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         }
         if (a.argmax_out) {
           am_warp_reduce(bv, bi);
-          if (lane == 0) a.am_part[m * wk.n_tiles + tile] = make_int2(__float_as_int(bv), bi);
-        }
-      }
-      if (a.argmax_out) {
-        esync();
-        if (etid == 0) {
-          const uint32_t prev = atom_add_acq_rel_gpu(a.argmax_cnt, 1u);
-          *bcast = (prev == static_cast<uint32_t>(wk.n_tiles - 1)) ? 1 : 0;
-        }
-        esync();
-        if (*bcast) {
-          for (int m = ew; m < a.M; m += kEpiWarps) {
-            float bv = -FLT_MAX;
-            int bi = 0x7fffffff;
-            for (int j = lane; j < wk.n_tiles; j += 32) {
-              const int2 pr = __ldcg(a.am_part + m * wk.n_tiles + j);
-              const float v = __int_as_float(pr.x);
-              if (pr.y != 0x7fffffff && am_better(v, pr.y, bv, bi)) {
-                bv = v;
-                bi = pr.y;
-              }
-            }
-            am_warp_reduce(bv, bi);
-            if (lane == 0) a.argmax_out[m] = bi;
+          if (lane == (m - ew) / kEpiWarps && bi != 0x7fffffff && am_better(bv, bi, am_v, am_i)) {
+            am_v = bv;
+            am_i = bi;
           }
-          if (etid == 0) *a.argmax_cnt = 0u;
         }
       }
     } else if (MODE == kTcGateUp) {
@@ -1066,6 +1048,36 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         if (j < cnt) a.y[static_cast<size_t>(off + j) * a.H + nt * kRows + r] = tot[j] * g;
     }
     esync();
+  }
+  // ---- argmax: one partial per CTA of the op; the last CTA to add its own
+  // reduces the op's G partials per row (the order of (value, index) pairs is
+  // total, so the result does not depend on which CTA finished which tile)
+  if (MODE == kTcDense && a.argmax_out && wk.rel(b) < wk.G) {  // uniform over the warps
+    const int own = ew + kEpiWarps * lane;  // the row this lane's running best belongs to
+    if (own < a.M) a.am_part[own * wk.G + wk.rel(b)] = make_int2(__float_as_int(am_v), am_i);
+    esync();
+    if (etid == 0) {
+      const uint32_t prev = atom_add_acq_rel_gpu(a.argmax_cnt, 1u);
+      *bcast = (prev == static_cast<uint32_t>(wk.G - 1)) ? 1 : 0;
+    }
+    esync();
+    if (*bcast) {
+      for (int m = ew; m < a.M; m += kEpiWarps) {
+        float bv = -FLT_MAX;
+        int bi = 0x7fffffff;
+        for (int j = lane; j < wk.G; j += 32) {
+          const int2 pr = __ldcg(a.am_part + m * wk.G + j);
+          const float v = __int_as_float(pr.x);
+          if (pr.y != 0x7fffffff && am_better(v, pr.y, bv, bi)) {
+            bv = v;
+            bi = pr.y;
+          }
+        }
+        am_warp_reduce(bv, bi);
+        if (lane == 0) a.argmax_out[m] = bi;
+      }
+      if (etid == 0) *a.argmax_cnt = 0u;
+    }
   }
   if (MODE != kTcDense) cur.release(c, op, lane == 0);
 }
