@@ -60,6 +60,12 @@ def workload_name(t, layers=40):
 
 # ------------------------------------------------------------------ distributed
 
+def calls_launches(layers):
+    """Kernels of the step issued call by call: routing, then per layer QKV,
+    O and the MoE layer's gate_up, down and combine kernels, then the head."""
+    return 1 + 5 * layers + 1
+
+
 def dist_setup(n):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -421,7 +427,7 @@ def run_ours(args, rank, world, local):
 
     t = args.tokens
     b, g, x, lg, ms, nbytes, clocks = one_config(t, args.steps, args.warmup, True)
-    n_launch = 2 if args.path == "program" else 1 + 4 * model.s.layers + 1
+    n_launch = 2 if args.path == "program" else calls_launches(model.s.layers)
     value = nbytes * world / (ms * 1e-3) / 1e9
 
     # ---- end to end: pinned host inputs in, argmax ids out, every step
@@ -513,7 +519,7 @@ def run_ours(args, rank, world, local):
     if args.path == "program" and not args.no_sweep:
         _, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, "calls")
         calls = {"us_per_step": ms3 * 1e3, "gbs": nb3 / (ms3 * 1e-3) / 1e9,
-                 "launches_per_step": 1 + 4 * model.s.layers + 1}
+                 "launches_per_step": calls_launches(model.s.layers)}
         del g3
 
     # ---- CPU baseline: the oracle on one layer of the same step
