@@ -282,7 +282,11 @@ def workload_table(model, reps=10):
     * the MoE layer (256 routed + 1 shared experts, hidden 2048, inter 512,
       top-8) at T in {1, 4, 8, 16, 32}, over the step's layer weights;
     * the MTP-verify batch: the MoE layer at T = 32 then the 151,936 x 2048
-      head with argmax."""
+      head with argmax;
+    * the hot-vocabulary draft head: 32,768 listed rows of that head (the
+      FR-Spec list; a seeded sorted subset of the vocabulary) with argmax at
+      M in {1, 8, 32}, over 8 copies gathered from different lists, and the
+      gather that builds one (bytes read + written)."""
     import torch
     from moe_expert_nvfp4_gb300 import ops, synth
     from moe_expert_nvfp4_gb300.decode_step import nvfp4_bytes
@@ -358,6 +362,28 @@ def workload_table(model, reps=10):
             ops.gemm(y, model.head, out=logits, argmax_out=am, workspace=wk)
     us = graph_us(verify, reps)
     out["mtp_verify_T32"] = {"us": us / L, "gbs": nbytes / us / 1e3}
+    del logits
+
+    # hot-vocabulary draft head
+    n_hot = 32768
+    lists = [torch.randperm(s.vocab, generator=torch.Generator().manual_seed(60 + i))[:n_hot]
+             .sort().values.to(torch.int32).to(dev) for i in range(8)]
+    hots = [ops.gather_rows(model.head, lst) for lst in lists]
+    hot_bytes = nvfp4_bytes(n_hot, s.hidden)
+    us = graph_us(lambda: ops.gather_rows(model.head, lists[0]), reps)
+    out[f"hot_head_gather_{n_hot}x{s.hidden}"] = {"us": us, "gbs": 2 * hot_bytes / us / 1e3}
+    wk = ops.Workspace(ops.gemm_workspace_bytes(32, n_hot, s.hidden))
+    for m in (1, 8, 32):
+        a = synth.activations_bf16(61, m, s.hidden).to(dev)
+        c = torch.empty(m, n_hot, dtype=torch.bfloat16, device=dev)
+        am = torch.empty(m, dtype=torch.int32, device=dev)
+
+        def drafts():
+            for h, lst in zip(hots, lists):
+                ops.hot_vocab_head(a, h, lst, out=c, argmax_out=am, workspace=wk)
+        us = graph_us(drafts, reps) / len(hots)
+        out[f"hot_head_{n_hot}x{s.hidden}_M{m}"] = {"us": us, "gbs": hot_bytes / us / 1e3}
+    del hots
     for v in out.values():
         v["us"] = round(v["us"], 2)
         v["gbs"] = round(v["gbs"], 1)

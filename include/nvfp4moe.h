@@ -143,6 +143,34 @@ int nvfp4_gemm_skinny_noalloc(const void* A, int64_t lda, int M, const nvfp4_wei
                               void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
                               nvfp4_stream_t stream);
 
+/* ---- hot-vocabulary head --------------------------------------------------
+ * "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", section "Making decode
+ * faster", paragraph "FR-Spec, and a silent bug": the draft scores only a
+ * list of the most likely tokens (32K) through a 4-bit head built from the
+ * checkpoint's output head (37 MB a draft step instead of the full head).
+ *
+ * nvfp4_gather_rows builds that head once: codes [n_rows, K/2] and scales
+ * [n_rows, K/16] receive rows rows[0..n_rows) of src, in list order (the
+ * plain row-major layout keeps each row contiguous, so this is exact; a row
+ * id outside [0, src->n) gives an all-zero row).  rows: int32 [n_rows] on
+ * the device; codes / scales: caller-owned device arrays, 16-byte aligned,
+ * not overlapping src.  K % 256 == 0.  Asynchronous on `stream`.  The hot
+ * head's global scale is src's (pass src->global_scale).
+ *
+ * nvfp4_hot_vocab_head is nvfp4_gemm_skinny on the hot head W_hot
+ * [n_hot, K] (C [M, n_hot] = the hot rows' BF16 logits) whose argmax_out
+ * (required) reports vocabulary ids: argmax_out[m] = vocab_ids[j], j the
+ * first maximum of C[m] (ties to the lowest hot row; with ascending
+ * vocab_ids that is the lowest vocabulary id).  vocab_ids: int32 [n_hot] on
+ * the device (the list the head was gathered with).  Workspace:
+ * nvfp4_gemm_skinny_workspace(M, n_hot, K). */
+int nvfp4_gather_rows(const nvfp4_weight* src, const int32_t* rows, int n_rows, void* codes,
+                      void* scales, nvfp4_stream_t stream);
+int nvfp4_hot_vocab_head(const void* A, int64_t lda, int M, const nvfp4_weight* W_hot,
+                         const int32_t* vocab_ids, void* C, int64_t ldc, int32_t* argmax_out,
+                         uint32_t flags, void* workspace, size_t workspace_bytes,
+                         nvfp4_stream_t stream);
+
 /* ---- top-k softmax routing ----------------------------------------------
  * logits float32 [T, E] (row-major).  For each row the k experts with the
  * largest logits, compared as float32, ties to the lower index, listed in
@@ -183,7 +211,9 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
  * Results are bit-identical to issuing the same calls one by one.
  *
  * nvfp4_op: kind NVFP4_OP_GEMM takes the arguments of nvfp4_gemm_skinny (A,
- * lda, M, W, C, ldc, argmax_out), kind NVFP4_OP_MOE those of moe_nvfp4_decode
+ * lda, M, W, C, ldc, argmax_out) and, for a hot-vocabulary head, argmax_map
+ * (NULL, or vocab_ids as in nvfp4_hot_vocab_head; needs argmax_out), kind
+ * NVFP4_OP_MOE those of moe_nvfp4_decode
  * (x ... ldo; shared.num_experts == 0 means no shared expert).  flags:
  * NVFP4_FLAG_RMS_INPUT per op (NVFP4_FLAG_NO_PDL and NVFP4_FLAG_IDS_READY are
  * accepted and ignored).  Every MoE op's topk_ids / topk_w must be complete
@@ -223,6 +253,8 @@ typedef struct nvfp4_op {
   nvfp4_expert_stack shared;
   void* out;
   int64_t ldo;
+  /* NVFP4_OP_GEMM, hot-vocabulary head */
+  const int32_t* argmax_map;
 } nvfp4_op;
 
 typedef struct nvfp4_program nvfp4_program;

@@ -371,7 +371,8 @@ void ws_header(TcArgs& a, uint8_t* ws) {
 
 // Dense op of a planned GEMM (arguments already checked).
 int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C, int64_t ldc,
-                int32_t* argmax_out, uint32_t flags, uint8_t* ws, const TcDensePlan& p, TcOp* op) {
+                int32_t* argmax_out, const int32_t* am_map, uint32_t flags, uint8_t* ws,
+                const TcDensePlan& p, TcOp* op) {
   memset(op, 0, sizeof(*op));
   int rc = weight_maps(&op->maps[0], &op->maps[1], W->codes, W->scales,
                        static_cast<uint64_t>(W->n), W->k, kTcTileRows);
@@ -385,6 +386,7 @@ int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* 
   a.C = static_cast<__nv_bfloat16*>(C);
   a.ldc = ldc;
   a.argmax_out = argmax_out;
+  a.am_map = am_map;
   a.gscale = W->global_scale;
   a.M = M;
   a.N = W->n;
@@ -546,9 +548,11 @@ size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
   return a > b ? a : b;
 }
 
-int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
-                      int64_t ldc, int32_t* argmax_out, uint32_t flags, void* workspace,
-                      size_t workspace_bytes, nvfp4_stream_t stream) {
+// The dense skinny GEMM; am_map (nullable) maps the argmax's row index to
+// the id reported.
+static int gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
+                       int64_t ldc, int32_t* argmax_out, const int32_t* am_map, uint32_t flags,
+                       void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
   int rc = check_gemm(A, lda, M, W, C, ldc);
   if (rc) return rc;
   const int N = W->n, K = W->k;
@@ -563,7 +567,7 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
     if ((rc = get_encoder())) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     TcOp op;
-    if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, flags, ws, p, &op))) return rc;
+    if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, am_map, flags, ws, p, &op))) return rc;
     int n_stages = 0;
     size_t smem = 0;
     rc = tc_launch_one(op, p.x_bytes, 0, p.grid, ws,
@@ -594,6 +598,7 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   a.C = static_cast<__nv_bfloat16*>(C);
   a.ldc = ldc;
   a.argmax_out = argmax_out;
+  a.am_map = am_map;
   a.gscale = W->global_scale;
   a.M = M;
   a.N = N;
@@ -618,6 +623,51 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
            "argmax=%d rms=%d",
            p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_stages,
            p.smem, argmax_out ? 1 : 0, a.rms);
+  g_dispatch = buf;
+  return NVFP4_OK;
+}
+
+int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
+                      int64_t ldc, int32_t* argmax_out, uint32_t flags, void* workspace,
+                      size_t workspace_bytes, nvfp4_stream_t stream) {
+  return gemm_skinny(A, lda, M, W, C, ldc, argmax_out, nullptr, flags, workspace,
+                     workspace_bytes, stream);
+}
+
+int nvfp4_hot_vocab_head(const void* A, int64_t lda, int M, const nvfp4_weight* W_hot,
+                         const int32_t* vocab_ids, void* C, int64_t ldc, int32_t* argmax_out,
+                         uint32_t flags, void* workspace, size_t workspace_bytes,
+                         nvfp4_stream_t stream) {
+  if (!vocab_ids || !argmax_out)
+    return fail(NVFP4_ERR_INVALID, "vocab_ids and argmax_out must be non-NULL");
+  return gemm_skinny(A, lda, M, W_hot, C, ldc, argmax_out, vocab_ids, flags, workspace,
+                     workspace_bytes, stream);
+}
+
+int nvfp4_gather_rows(const nvfp4_weight* src, const int32_t* rows, int n_rows, void* codes,
+                      void* scales, nvfp4_stream_t stream) {
+  if (!src || !rows || !codes || !scales)
+    return fail(NVFP4_ERR_INVALID, "src, rows, codes and scales must be non-NULL");
+  if (!src->codes || !src->scales) return fail(NVFP4_ERR_INVALID, "src has a NULL pointer");
+  if (n_rows < 1 || src->n < 1 || src->k < 1)
+    return fail(NVFP4_ERR_INVALID, "n_rows=%d, N=%d, K=%d must be positive", n_rows, src->n,
+                src->k);
+  if (src->k % kStageK) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 256", src->k);
+  if (!aligned16(src->codes) || !aligned16(src->scales) || !aligned16(codes) || !aligned16(scales))
+    return fail(NVFP4_ERR_ALIGN, "code and scale arrays must be 16-byte aligned");
+  GatherArgs a;
+  a.src_codes = src->codes;
+  a.src_scales = src->scales;
+  a.N = src->n;
+  a.K = src->k;
+  a.rows = rows;
+  a.n_rows = n_rows;
+  a.dst_codes = static_cast<uint8_t*>(codes);
+  a.dst_scales = static_cast<uint8_t*>(scales);
+  const cudaError_t e = launch_gather_rows(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather_rows_kernel launch");
+  char buf[128];
+  snprintf(buf, sizeof(buf), "gather_rows_kernel rows=%d N=%d K=%d", n_rows, src->n, src->k);
   g_dispatch = buf;
   return NVFP4_OK;
 }
@@ -823,7 +873,10 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
       if (!plan_tc_dense(o.M, o.W.n, o.W.k, sms, &p))
         return fail(NVFP4_ERR_SHAPE, "op %d: N=%d, K=%d: no feasible plan", i, o.W.n, o.W.k);
       TcOp op;
-      if ((rc = tc_dense_op(o.A, o.lda, o.M, &o.W, o.C, o.ldc, o.argmax_out, o.flags, ws, p, &op)))
+      if (o.argmax_map && !o.argmax_out)
+        return fail(NVFP4_ERR_INVALID, "op %d: argmax_map without argmax_out", i);
+      if ((rc = tc_dense_op(o.A, o.lda, o.M, &o.W, o.C, o.ldc, o.argmax_out, o.argmax_map, o.flags,
+                            ws, p, &op)))
         return rc;
       table.push_back(op);
       x_bytes = std::max(x_bytes, p.x_bytes);

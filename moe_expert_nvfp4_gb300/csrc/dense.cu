@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           am_warp_reduce(bv, bi);
-          if (lane == 0) a.argmax_out[m] = bi;
+          if (lane == 0) a.argmax_out[m] = (a.am_map && bi != 0x7fffffff) ? a.am_map[bi] : bi;
         }
         if (tid == 0) *a.argmax_cnt = 0u;
       }

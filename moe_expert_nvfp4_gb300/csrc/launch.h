@@ -35,6 +35,7 @@ struct DenseArgs {
   __nv_bfloat16* C;
   int64_t ldc;
   int32_t* argmax_out;     // nullable
+  const int32_t* am_map;   // nullable: argmax_out reports am_map[n] instead of n
   const float* gscale;
   int M, N, K;
   int n_tiles, nkb;        // 64-row tiles; K / 256 stages per tile
@@ -106,6 +107,7 @@ struct TcArgs {
   __nv_bfloat16* C;
   int64_t ldc;
   int32_t* argmax_out;
+  const int32_t* am_map;  // nullable: argmax_out reports am_map[n] instead of n
   const float* gscale;
   int M, N, K;
   // MoE
@@ -182,6 +184,20 @@ cudaError_t launch_moe_gate_up(const CUtensorMap* maps, const MoeArgs& a, int gr
 cudaError_t launch_moe_down(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
                             cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
+
+// Row gather of an NVFP4 matrix [N, K]: dst row i = src row rows[i] (codes
+// and scales), all-zero for a row id outside [0, N).  K % 256 == 0; every
+// pointer 16-byte aligned.
+struct GatherArgs {
+  const uint8_t* src_codes;
+  const uint8_t* src_scales;
+  int N, K;
+  const int32_t* rows;
+  int n_rows;
+  uint8_t* dst_codes;
+  uint8_t* dst_scales;
+};
+cudaError_t launch_gather_rows(const GatherArgs& a, cudaStream_t s);
 
 // Record the message returned by nvfp4_last_error() for this thread.
 void set_last_error(const char* msg);

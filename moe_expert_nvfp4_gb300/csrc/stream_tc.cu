@@ -1074,7 +1074,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
           }
         }
         am_warp_reduce(bv, bi);
-        if (lane == 0) a.argmax_out[m] = bi;
+        if (lane == 0) a.argmax_out[m] = (a.am_map && bi != 0x7fffffff) ? a.am_map[bi] : bi;
       }
       if (etid == 0) *a.argmax_cnt = 0u;
     }

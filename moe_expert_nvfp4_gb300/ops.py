@@ -55,7 +55,7 @@ class _Op(ctypes.Structure):
                 ("x", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("T", ctypes.c_int32),
                 ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("k", ctypes.c_int32),
                 ("experts", _Stack), ("shared", _Stack), ("out", ctypes.c_void_p),
-                ("ldo", ctypes.c_int64)]
+                ("ldo", ctypes.c_int64), ("argmax_map", ctypes.c_void_p)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -81,6 +81,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_gemm_skinny_workspace.argtypes = [i32, i32, i32]
     L.nvfp4_gemm_skinny_workspace.restype = sz
     L.nvfp4_gemm_skinny.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, i64, vp, u32, vp, sz, vp]
+    L.nvfp4_hot_vocab_head.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, vp, i64, vp, u32,
+                                       vp, sz, vp]
+    L.nvfp4_gather_rows.argtypes = [ctypes.POINTER(_Weight), vp, i32, vp, vp, vp]
     L.topk_softmax_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
     L.moe_nvfp4_decode_workspace.argtypes = [i32, i32, ctypes.POINTER(_Stack)]
     L.moe_nvfp4_decode_workspace.restype = sz
@@ -243,6 +246,47 @@ def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
     return (out, ids) if argmax else out
 
 
+def gather_rows(w: NVFP4Weight, rows: torch.Tensor, stream=None) -> NVFP4Weight:
+    """The NVFP4 matrix of rows ``rows`` (int32 [n], device) of ``w``, in
+    list order: the hot-vocabulary head of an output head (a row id outside
+    [0, N) gives an all-zero row).  Shares w's global scale."""
+    assert rows.dtype == torch.int32 and rows.is_contiguous() and rows.dim() == 1
+    n = rows.numel()
+    codes = torch.empty(n, w.k // 2, dtype=torch.uint8, device=w.codes.device)
+    scales = torch.empty(n, w.k // 16, dtype=torch.uint8, device=w.codes.device)
+    wc = w.c()
+    _check(load().nvfp4_gather_rows(ctypes.byref(wc), rows.data_ptr(), n, codes.data_ptr(),
+                                    scales.data_ptr(), _stream(stream)), "nvfp4_gather_rows")
+    return NVFP4Weight(codes, scales, w.global_scale)
+
+
+def hot_vocab_head(a: torch.Tensor, w_hot: NVFP4Weight, vocab_ids: torch.Tensor,
+                   out: Optional[torch.Tensor] = None, argmax_out: Optional[torch.Tensor] = None,
+                   rms_input: bool = False, workspace: Optional[Workspace] = None,
+                   pdl: bool = True, stream=None, warp_mma: bool = False):
+    """Greedy draft token through a hot-vocabulary head: the hot rows' BF16
+    logits C = A W_hot^T [M, n_hot] and the vocabulary id of each row's
+    first maximum, vocab_ids[argmax] (int32 [M])."""
+    L = load()
+    m = a.shape[0]
+    assert vocab_ids.dtype == torch.int32 and vocab_ids.is_contiguous()
+    assert vocab_ids.numel() == w_hot.n
+    if out is None:
+        out = torch.empty(m, w_hot.n, dtype=torch.bfloat16, device=a.device)
+    if argmax_out is None:
+        argmax_out = torch.empty(m, dtype=torch.int32, device=a.device)
+    if workspace is None:
+        workspace = Workspace(gemm_workspace_bytes(m, w_hot.n, w_hot.k), a.device)
+    flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+             | (FLAG_WARP_MMA if warp_mma else 0))
+    wc = w_hot.c()
+    _check(L.nvfp4_hot_vocab_head(a.data_ptr(), a.stride(0), m, ctypes.byref(wc),
+                                  vocab_ids.data_ptr(), out.data_ptr(), out.stride(0),
+                                  argmax_out.data_ptr(), flags, workspace.ptr(), workspace.nbytes,
+                                  _stream(stream)), "nvfp4_hot_vocab_head")
+    return out, argmax_out
+
+
 def route(logits: torch.Tensor, k: int, renormalize: bool = True,
           ids: Optional[torch.Tensor] = None, weights: Optional[torch.Tensor] = None, stream=None):
     """Top-k softmax routing of float32 logits [T, E] -> (ids int32 [T, k],
@@ -288,9 +332,14 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
 # ------------------------------------------------------------------ programs
 
 def gemm_op(a: torch.Tensor, w: NVFP4Weight, out: torch.Tensor,
-            argmax_out: Optional[torch.Tensor] = None, rms_input: bool = False) -> dict:
-    """One GEMM of a program: out = A W^T (as gemm())."""
-    return dict(kind=OP_GEMM, a=a, w=w, out=out, argmax_out=argmax_out, rms_input=rms_input)
+            argmax_out: Optional[torch.Tensor] = None, rms_input: bool = False,
+            argmax_map: Optional[torch.Tensor] = None) -> dict:
+    """One GEMM of a program: out = A W^T (as gemm()); with argmax_map (the
+    vocabulary ids of a hot-vocabulary head, as hot_vocab_head()) argmax_out
+    reports argmax_map[argmax]."""
+    assert argmax_map is None or (argmax_map.dtype == torch.int32 and argmax_map.is_contiguous())
+    return dict(kind=OP_GEMM, a=a, w=w, out=out, argmax_out=argmax_out, rms_input=rms_input,
+                argmax_map=argmax_map)
 
 
 def moe_op(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
@@ -314,6 +363,7 @@ def _c_ops(ops: list) -> ctypes.Array:
             c.W = o["w"].c()
             c.C, c.ldc = out.data_ptr(), out.stride(0)
             c.argmax_out = _ptr(o.get("argmax_out"))
+            c.argmax_map = _ptr(o.get("argmax_map"))
         else:
             x, ids, out = o["x"], o["ids"], o["out"]
             assert ids.is_contiguous() and o["weights"].is_contiguous()

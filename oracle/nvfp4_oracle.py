@@ -41,7 +41,7 @@ __all__ = [
     "dec_e2m1", "dec_e4m3", "E2M1_TABLE", "E4M3_TABLE", "bf16_round",
     "dequant", "gemm64", "gemm_bf16", "topk_softmax_route", "silu",
     "expert_ffn64", "moe_decode64", "moe_decode_bf16", "argmax_first",
-    "lm_head_argmax", "rms_scale", "decode_layer", "nvfp4_weight_bytes",
+    "lm_head_argmax", "hot_vocab_head_argmax", "rms_scale", "decode_layer", "nvfp4_weight_bytes",
     "moe_weight_bytes", "decode_roofline_tok_s", "roofline_share",
     "RMS_EPS",
 ]
@@ -174,6 +174,26 @@ def lm_head_argmax(a, codes, scales, global_scale) -> Tuple[np.ndarray, np.ndarr
     first maximum per row.  Returns (ids int32 [M], bf16 logits [M, N])."""
     logits = gemm_bf16(a, codes, scales, global_scale)
     return argmax_first(logits, axis=1), logits
+
+
+def hot_vocab_head_argmax(a, codes, scales, global_scale,
+                          vocab_ids) -> Tuple[np.ndarray, np.ndarray]:
+    """Greedy draft token through a hot-vocabulary head ("Qwen3.6-35B-A3B
+    NVFP4 on an RTX 5090 (Elsa)", section "Making decode faster", paragraph
+    "FR-Spec, and a silent bug"): the 4-bit head restricted to the rows of a
+    list of likely tokens, those rows taken from the full head [N, K] itself.
+    The listed rows' logits are rounded to BF16; the first maximum in list
+    order is reported as its vocabulary id.  A listed id outside [0, N)
+    stands for an all-zero row.  Returns (ids int32 [M], bf16 logits
+    [M, len(vocab_ids)])."""
+    vocab_ids = np.asarray(vocab_ids, dtype=np.int64)
+    ok = (vocab_ids >= 0) & (vocab_ids < codes.shape[0])
+    hot_codes = np.zeros((vocab_ids.size, codes.shape[1]), dtype=np.uint8)
+    hot_scales = np.zeros((vocab_ids.size, scales.shape[1]), dtype=np.uint8)
+    hot_codes[ok] = codes[vocab_ids[ok]]
+    hot_scales[ok] = scales[vocab_ids[ok]]
+    logits = gemm_bf16(a, hot_codes, hot_scales, global_scale)
+    return vocab_ids[argmax_first(logits, axis=1)].astype(np.int32), logits
 
 
 # --------------------------------------------------------------------------

@@ -435,6 +435,61 @@ def test_argmax_first_and_lm_head_ties():
     assert np.all(ids == 0)
 
 
+def test_hot_vocab_head_whole_list_is_the_head():
+    """Listing every row in order reduces the hot head to the full head."""
+    rng = np.random.default_rng(21)
+    codes, scales = _rand_nvfp4(40, 64, rng)
+    a = _rand_bf16((3, 64), rng)
+    ids, logits = O.hot_vocab_head_argmax(a, codes, scales, 0.5, np.arange(40))
+    ref_ids, ref_logits = O.lm_head_argmax(a, codes, scales, 0.5)
+    assert np.array_equal(ids, ref_ids) and np.array_equal(logits, ref_logits)
+
+
+def test_hot_vocab_head_rows_and_ids_come_from_the_full_head():
+    """The listed rows' logits are the full head's logits of those rows (each
+    dot product is independent), and the answer is a vocabulary id: the
+    listed id with the largest logit, the first in list order on a tie."""
+    rng = np.random.default_rng(22)
+    codes, scales = _rand_nvfp4(60, 96, rng)
+    a = _rand_bf16((4, 96), rng)
+    _, full = O.lm_head_argmax(a, codes, scales, 0.5)
+    full_ids = O.argmax_first(full, axis=1)
+    for lst in (rng.permutation(60)[:17], np.array([full_ids[0], 3, 59, 0]),
+                np.setdiff1d(np.arange(60), full_ids)[::-1]):
+        ids, logits = O.hot_vocab_head_argmax(a, codes, scales, 0.5, lst)
+        assert np.array_equal(logits, full[:, lst])
+        for r in range(4):
+            best = max(range(len(lst)), key=lambda j: (full[r, lst[j]], -j))
+            assert ids[r] == lst[best]
+    # the full head's choice, when listed, is the hot head's choice
+    ids, _ = O.hot_vocab_head_argmax(a, codes, scales, 0.5, np.array([full_ids[1], 7, 8]))
+    assert ids[1] == full_ids[1]
+
+
+def test_hot_vocab_head_ties_go_to_list_order_and_bad_ids_are_zero_rows():
+    rng = np.random.default_rng(23)
+    codes, scales = _rand_nvfp4(12, 64, rng)
+    a = _rand_bf16((2, 64), rng)
+    _, full = O.lm_head_argmax(a, codes, scales, 0.5)
+    # a head whose only non-zero rows are two identical rows 9 and 4, with a
+    # positive logit (the activations' sign flipped where needed): the first
+    # of the two in list order wins, whichever vocabulary id is lower
+    tied, tied_s = np.zeros_like(codes), scales.copy()
+    tied[9], tied[4], tied_s[9] = codes[4], codes[4], scales[4]
+    a = a * np.where(full[:, 4] < 0, -1.0, 1.0)[:, None]
+    lg = O.gemm_bf16(a, tied, tied_s, 0.5)
+    assert np.array_equal(lg[:, 9], lg[:, 4]) and np.all(lg[:, 4] > 0)
+    ids, _ = O.hot_vocab_head_argmax(a, tied, tied_s, 0.5, np.array([0, 9, 4]))
+    assert np.array_equal(ids, [9, 9])
+    ids, _ = O.hot_vocab_head_argmax(a, tied, tied_s, 0.5, np.array([0, 4, 9]))
+    assert np.array_equal(ids, [4, 4])
+    # ids outside [0, N) are all-zero rows: logit exactly 0
+    _, full = O.lm_head_argmax(a, codes, scales, 0.5)
+    ids, logits = O.hot_vocab_head_argmax(a, codes, scales, 0.5, np.array([-1, 3, 12]))
+    assert np.all(logits[:, 0] == 0.0) and np.all(logits[:, 2] == 0.0)
+    assert np.array_equal(logits[:, 1], full[:, 3])
+
+
 # ---------------------------------------------------------------- bytes + roofline (pages)
 
 def _figs(golden_dir):
