@@ -286,7 +286,10 @@ def workload_table(model, reps=10):
     * the hot-vocabulary draft head: 32,768 listed rows of that head (the
       FR-Spec list; a seeded sorted subset of the vocabulary) with argmax at
       M in {1, 8, 32}, over 8 copies gathered from different lists, and the
-      gather that builds one (bytes read + written)."""
+      gather that builds one (bytes read + written);
+    * the BF16 -> NVFP4 quantisation of a 151,936 x 2048 BF16 head (bytes:
+      the BF16 matrix read twice -- the per-tensor maximum precedes every
+      code -- and the NVFP4 matrix written)."""
     import torch
     from moe_expert_nvfp4_gb300 import ops, synth
     from moe_expert_nvfp4_gb300.decode_step import nvfp4_bytes
@@ -384,6 +387,14 @@ def workload_table(model, reps=10):
         us = graph_us(drafts, reps) / len(hots)
         out[f"hot_head_{n_hot}x{s.hidden}_M{m}"] = {"us": us, "gbs": hot_bytes / us / 1e3}
     del hots
+
+    # BF16 -> NVFP4 quantisation of a head-sized BF16 matrix (622 MB >> L2)
+    wb = torch.randn(s.vocab, s.hidden, device=dev,
+                     generator=torch.Generator(device=dev).manual_seed(62)).to(torch.bfloat16)
+    us = graph_us(lambda: ops.quantize(wb), reps)
+    qbytes = s.vocab * s.hidden * (2 + 2) + nvfp4_bytes(s.vocab, s.hidden)
+    out[f"quantize_{s.vocab}x{s.hidden}"] = {"us": us, "gbs": qbytes / us / 1e3}
+    del wb
     for v in out.values():
         v["us"] = round(v["us"], 2)
         v["gbs"] = round(v["gbs"], 1)

@@ -171,6 +171,23 @@ int nvfp4_hot_vocab_head(const void* A, int64_t lda, int M, const nvfp4_weight* 
                          uint32_t flags, void* workspace, size_t workspace_bytes,
                          nvfp4_stream_t stream);
 
+/* ---- BF16 -> NVFP4 quantisation --------------------------------------------
+ * "Qwen3.8-27B-NVFP4-lmhead4-recipe" (model card), section "Files": a BF16
+ * head converted to NVFP4 (the tool's rule is not given; this is the usual
+ * NVFP4 recipe).  W bf16 [N, ldw] row-major (K columns used) ->
+ *   global_scale (1 float, device) g = amax|W| / (6 * 448), 1 if W is all 0;
+ *   scales [N, K/16]: E4M3 of amax of each 16-element block / (6 g);
+ *   codes [N, K/2]: E2M1 of |x| / (e4m3(scale) * g) with x's sign (a code
+ *   rounded to 0 is +0), two per byte, low nibble = even k.
+ * Roundings to nearest, ties to the even code, saturating at 448 / 6; every
+ * quotient and product one float32 operation (deterministic).  The result
+ * is a plain nvfp4_weight {codes, scales, global_scale, N, K}.  K % 32 == 0;
+ * W rows and codes 16-byte aligned; outputs caller-owned device memory.
+ * Asynchronous on `stream` (three kernels; global_scale holds a partial
+ * result until the last one ends). */
+int nvfp4_quantize(const void* W, int64_t ldw, int N, int K, void* codes, void* scales,
+                   float* global_scale, nvfp4_stream_t stream);
+
 /* ---- top-k softmax routing ----------------------------------------------
  * logits float32 [T, E] (row-major).  For each row the k experts with the
  * largest logits, compared as float32, ties to the lower index, listed in

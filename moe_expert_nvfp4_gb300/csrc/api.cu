@@ -644,6 +644,35 @@ int nvfp4_hot_vocab_head(const void* A, int64_t lda, int M, const nvfp4_weight* 
                      workspace_bytes, stream);
 }
 
+int nvfp4_quantize(const void* W, int64_t ldw, int N, int K, void* codes, void* scales,
+                   float* global_scale, nvfp4_stream_t stream) {
+  if (!W || !codes || !scales || !global_scale)
+    return fail(NVFP4_ERR_INVALID, "W, codes, scales and global_scale must be non-NULL");
+  if (N < 1 || K < 1 || ldw < K) return fail(NVFP4_ERR_INVALID, "N=%d, K=%d, ldw=%lld", N, K,
+                                            static_cast<long long>(ldw));
+  if (K % 32) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 32", K);
+  if (!aligned16(W) || (ldw * 2) % 16 || !aligned16(codes) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return fail(NVFP4_ERR_ALIGN, "W rows and codes must be 16-byte aligned");
+  int sms = 0, rc;
+  if ((rc = current_device(&sms))) return rc;
+  QuantArgs a;
+  a.W = static_cast<const __nv_bfloat16*>(W);
+  a.ldw = ldw;
+  a.N = N;
+  a.K = K;
+  a.codes = static_cast<uint8_t*>(codes);
+  a.scales = static_cast<uint8_t*>(scales);
+  a.amax_bits = reinterpret_cast<uint32_t*>(global_scale);
+  a.global_scale = global_scale;
+  const cudaError_t e = launch_quantize(a, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize kernels launch");
+  char buf[128];
+  snprintf(buf, sizeof(buf), "amax_kernel, quantize_kernel, global_scale_kernel N=%d K=%d", N, K);
+  g_dispatch = buf;
+  return NVFP4_OK;
+}
+
 int nvfp4_gather_rows(const nvfp4_weight* src, const int32_t* rows, int n_rows, void* codes,
                       void* scales, nvfp4_stream_t stream) {
   if (!src || !rows || !codes || !scales)

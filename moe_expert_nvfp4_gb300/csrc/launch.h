@@ -199,6 +199,21 @@ struct GatherArgs {
 };
 cudaError_t launch_gather_rows(const GatherArgs& a, cudaStream_t s);
 
+// BF16 -> NVFP4 quantisation of W [N, ldw] (K used; K % 32 == 0): codes
+// [N, K/2], scales [N, K/16], and the per-tensor scale, which holds the bits
+// of the matrix's largest magnitude while the kernels run (amax_bits and
+// global_scale are the same 4 bytes).
+struct QuantArgs {
+  const __nv_bfloat16* W;
+  int64_t ldw;
+  int N, K;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint32_t* amax_bits;
+  float* global_scale;
+};
+cudaError_t launch_quantize(const QuantArgs& a, int sms, cudaStream_t s);
+
 // Record the message returned by nvfp4_last_error() for this thread.
 void set_last_error(const char* msg);
 

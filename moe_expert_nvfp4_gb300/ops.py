@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_hot_vocab_head.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, vp, i64, vp, u32,
                                        vp, sz, vp]
     L.nvfp4_gather_rows.argtypes = [ctypes.POINTER(_Weight), vp, i32, vp, vp, vp]
+    L.nvfp4_quantize.argtypes = [vp, i64, i32, i32, vp, vp, vp, vp]
     L.topk_softmax_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
     L.moe_nvfp4_decode_workspace.argtypes = [i32, i32, ctypes.POINTER(_Stack)]
     L.moe_nvfp4_decode_workspace.restype = sz
@@ -244,6 +245,20 @@ def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
                                out.stride(0), _ptr(ids), flags, workspace.ptr(), workspace.nbytes,
                                _stream(stream)), "nvfp4_gemm_skinny")
     return (out, ids) if argmax else out
+
+
+def quantize(w: torch.Tensor, stream=None) -> NVFP4Weight:
+    """BF16 matrix [N, K] (row stride w.stride(0)) -> its NVFP4 weight (codes,
+    E4M3 block scales, per-tensor scale), computed on the device."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1
+    n, k = w.shape
+    codes = torch.empty(n, k // 2, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(n, k // 16, dtype=torch.uint8, device=w.device)
+    g = torch.empty(1, dtype=torch.float32, device=w.device)
+    _check(load().nvfp4_quantize(w.data_ptr(), w.stride(0), n, k, codes.data_ptr(),
+                                 scales.data_ptr(), g.data_ptr(), _stream(stream)),
+           "nvfp4_quantize")
+    return NVFP4Weight(codes, scales, g)
 
 
 def gather_rows(w: NVFP4Weight, rows: torch.Tensor, stream=None) -> NVFP4Weight:

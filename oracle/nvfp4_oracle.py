@@ -41,7 +41,8 @@ __all__ = [
     "dec_e2m1", "dec_e4m3", "E2M1_TABLE", "E4M3_TABLE", "bf16_round",
     "dequant", "gemm64", "gemm_bf16", "topk_softmax_route", "silu",
     "expert_ffn64", "moe_decode64", "moe_decode_bf16", "argmax_first",
-    "lm_head_argmax", "hot_vocab_head_argmax", "rms_scale", "decode_layer", "nvfp4_weight_bytes",
+    "lm_head_argmax", "hot_vocab_head_argmax", "rms_scale", "round_to_e2m1",
+    "round_to_e4m3", "nvfp4_quantize", "decode_layer", "nvfp4_weight_bytes",
     "moe_weight_bytes", "decode_roofline_tok_s", "roofline_share",
     "RMS_EPS",
 ]
@@ -194,6 +195,66 @@ def hot_vocab_head_argmax(a, codes, scales, global_scale,
     hot_scales[ok] = scales[vocab_ids[ok]]
     logits = gemm_bf16(a, hot_codes, hot_scales, global_scale)
     return vocab_ids[argmax_first(logits, axis=1)].astype(np.int32), logits
+
+
+# --------------------------------------------------------------------------
+# Quantisation BF16 -> NVFP4
+# --------------------------------------------------------------------------
+#
+# "Qwen3.8-27B-NVFP4-lmhead4-recipe" (model card), section "Files": the head
+# is converted from BF16 to NVFP4 by a quantisation tool, without the rule.
+# The reading taken: the usual NVFP4 recipe.  Per-tensor scale
+# g = amax / (6 * 448) (so the largest block scale is E4M3's maximum); per
+# 16-element block t = amax_b / (6 g), scale byte = t rounded to E4M3; each
+# element's code = |x| / (scale * g) rounded to E2M1, with the element's sign
+# when the code is not zero.  Every quotient and product is one float32
+# operation rounded to nearest (the precision the quantised codes are decided
+# in); roundings onto the E4M3 / E2M1 grids are to nearest, ties to the even
+# code, saturating at 448 / 6.  An all-zero matrix gets g = 1.
+
+def _round_to_grid(v: np.ndarray, grid: np.ndarray) -> np.ndarray:
+    """Index of the grid point nearest each non-negative value (grid ascending,
+    indices are the codes), ties to the even index, saturating at the top."""
+    v = np.minimum(np.asarray(v, dtype=np.float64), grid[-1])
+    hi = np.clip(np.searchsorted(grid, v, side="left"), 0, grid.size - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = v - grid[lo], grid[hi] - v
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    return np.where(take_hi, hi, lo).astype(np.uint8)
+
+
+def round_to_e2m1(v) -> np.ndarray:
+    """Non-negative values to E2M1 codes 0..7 (nearest, ties to even, > 6 -> 6)."""
+    return _round_to_grid(v, E2M1_TABLE[:8])
+
+
+def round_to_e4m3(v) -> np.ndarray:
+    """Non-negative values to E4M3 bytes 0..0x7E (nearest, ties to even,
+    > 448 -> 448)."""
+    return _round_to_grid(v, E4M3_TABLE[:127])
+
+
+def nvfp4_quantize(w) -> Tuple[np.ndarray, np.ndarray, float]:
+    """BF16 matrix [N, K] (its values as float64 or float32) -> (codes uint8
+    [N, K/2], scales uint8 [N, K/16], global scale float32), by the recipe
+    above."""
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    f32 = np.float32
+    amax = f32(np.abs(w).max()) if w.size else f32(0)
+    g = f32(1.0) if amax == 0 else f32(amax / f32(6 * 448))
+    blocks = np.abs(w).reshape(n, k // 16, 16)
+    amax_b = blocks.max(axis=2)
+    t = (amax_b / f32(f32(6) * g)).astype(np.float32)
+    scales = round_to_e4m3(t)
+    d = (E4M3_TABLE[scales].astype(np.float32) * g).astype(np.float32)  # [n, k/16]
+    dd = np.repeat(d, 16, axis=1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(dd > 0, np.abs(w) / np.where(dd > 0, dd, f32(1)), f32(0)).astype(np.float32)
+    mag = round_to_e2m1(v)
+    code = np.where((w < 0) & (mag != 0), mag | 8, mag).astype(np.uint8)
+    codes = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return codes, scales.astype(np.uint8), float(g)
 
 
 # --------------------------------------------------------------------------

@@ -490,6 +490,89 @@ def test_hot_vocab_head_ties_go_to_list_order_and_bad_ids_are_zero_rows():
     assert np.array_equal(logits[:, 1], full[:, 3])
 
 
+# ---------------------------------------------------------------- quantiser BF16 -> NVFP4
+
+def _grid_probe(grid, rng, top):
+    """Every grid point and midpoint, the float32 neighbours of each
+    midpoint, and random values, all within [0, top]."""
+    g32 = grid.astype(np.float32)
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([g32, mids, np.nextafter(mids, np.float32(0)),
+                           np.nextafter(mids, np.float32(1e9)),
+                           rng.uniform(0, top, 3000).astype(np.float32),
+                           (2.0 ** rng.uniform(-12, np.log2(top), 3000)).astype(np.float32)])
+    return vals[vals <= top]
+
+
+def test_e4m3_rounding_matches_torch_conversion():
+    vals = _grid_probe(O.E4M3_TABLE[:127], np.random.default_rng(31), 448.0)
+    want = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.round_to_e4m3(vals), want)
+    assert np.all(O.round_to_e4m3([448.0, 449.0, 464.0, 1e6]) == 0x7E)  # saturates
+
+
+def test_e2m1_rounding_matches_ml_dtypes_conversion():
+    ml = pytest.importorskip("ml_dtypes")
+    vals = _grid_probe(O.E2M1_TABLE[:8], np.random.default_rng(32), 6.0)
+    want = vals.astype(ml.float4_e2m1fn).view(np.uint8) & 0xF
+    assert np.array_equal(O.round_to_e2m1(vals), want)
+    assert np.all(O.round_to_e2m1([6.0, 6.5, 100.0]) == 7)  # saturates
+
+
+@pytest.mark.parametrize("g", [1.0, 2.0 ** -5])
+def test_quantize_recovers_an_nvfp4_matrix_exactly(g):
+    """A matrix that is exactly an NVFP4 matrix whose blocks each hold a +-6
+    and whose largest scale is 448 quantises back to the same bytes."""
+    rng = np.random.default_rng(33)
+    n, k = 12, 128
+    codes = rng.integers(0, 256, size=(n, k // 2), dtype=np.uint8)
+    lo, hi = codes & 0xF, codes >> 4
+    lo = np.where(lo == 8, 0, lo)                       # no -0 (quantises to +0)
+    lo[:, ::8] = np.where(rng.random((n, k // 16)) < 0.5, 7, 15)  # a +-6 in every block
+    codes = (lo | (np.where(hi == 8, 0, hi) << 4)).astype(np.uint8)
+    scales = rng.integers(0x08, 0x7E, size=(n, k // 16), dtype=np.uint8)
+    scales[3, 5] = 0x7E
+    w = O.dequant(codes, scales, g)
+    assert np.array_equal(w, O.bf16_round(w))          # a BF16 matrix
+    c2, s2, g2 = O.nvfp4_quantize(w)
+    assert g2 == g and np.array_equal(s2, scales) and np.array_equal(c2, codes)
+
+
+def test_quantize_error_bound_and_scale_cover():
+    """Random BF16 weights (normal, and magnitudes spread over 2^-20 .. 2^6):
+    every element is within half an E2M1 step of |x| / (scale * g), except
+    where the block maximum saturates at 6 because its E4M3 scale rounded
+    down (by at most 2^-4 relative), and the round trip has the right sign."""
+    rng = np.random.default_rng(34)
+    for w in (_rand_bf16((64, 256), rng),
+              O.bf16_round(rng.choice([-1, 1], (64, 256)) * 2.0 ** rng.uniform(-20, 6, (64, 256)))):
+        codes, scales, g = O.nvfp4_quantize(w)
+        d = np.repeat(O.E4M3_TABLE[scales] * np.float32(g), 16, axis=1)
+        q = O.dequant(codes, scales, g)
+        ok = d > 0
+        v = np.abs(w[ok]) / d[ok]
+        step = np.where(v < 2, 0.5, np.where(v < 4, 1.0, 2.0))
+        err = np.abs(np.abs(q[ok]) / d[ok] - v)
+        sat = v > 6
+        assert np.all(err[~sat] <= step[~sat] / 2 * (1 + 1e-6))
+        assert np.all(v[sat] <= 6 / (1 - 2.0 ** -4) * (1 + 1e-6))
+        assert np.all((np.sign(q) == np.sign(w)) | (q == 0))
+        amax_b = np.abs(w).reshape(64, 16, 16).max(axis=2)
+        assert np.all(O.E4M3_TABLE[scales] * g * 6 >= amax_b * (1 - 2.0 ** -4) * (1 - 1e-6))
+
+
+def test_quantize_zero_matrix_and_signless_zeros():
+    codes, scales, g = O.nvfp4_quantize(np.zeros((2, 32)))
+    assert g == 1.0 and not codes.any() and not scales.any()
+    w = np.zeros((1, 32))
+    w[0, 0] = -6.0
+    w[0, 1], w[0, 2] = -1e-3, 1e-3  # round to zero: code 0, never -0 (8)
+    codes, scales, g = O.nvfp4_quantize(w)
+    assert codes[0, 0] == (15 | (0 << 4)) and codes[0, 1] == 0
+    q = O.dequant(codes, scales, g)[0, :3]
+    assert abs(q[0] + 6.0) < 1e-5 and q[1] == 0.0 and q[2] == 0.0
+
+
 # ---------------------------------------------------------------- bytes + roofline (pages)
 
 def _figs(golden_dir):
