@@ -75,6 +75,23 @@ def dist_setup(n):
     return rank, world, local
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of the ranks' values (the slowest replica's time); x
+    itself when there is one rank (dist None)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the bytes all ranks processed over the slowest
+    rank's time, in GB/s."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -449,10 +466,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         barrier()
         clocks = clk.stop() if clk else None
-        if dist is not None:
-            tt = torch.tensor([ms], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, "cuda")
         nbytes = model.step_bytes(b["ids"], t)
         status = b["ws"].status()
         if status:
@@ -465,7 +479,7 @@ def run_ours(args, rank, world, local):
     t = args.tokens
     b, g, x, lg, ms, nbytes, clocks = one_config(t, args.steps, args.warmup, True)
     n_launch = 2 if args.path == "program" else calls_launches(model.s.layers)
-    value = nbytes * world / (ms * 1e-3) / 1e9
+    value = job_gbs(nbytes, world, ms)
 
     # ---- end to end: pinned host inputs in, argmax ids out, every step
     xh = x.pin_memory()
@@ -488,7 +502,8 @@ def run_ours(args, rank, world, local):
         stream.synchronize()
     e_ms = (time.perf_counter() - t0) * 1e3 / e_steps
     barrier()
-    e2e = {"value": nbytes * world / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+    e_ms = max_over_ranks(e_ms, dist, "cuda")
+    e2e = {"value": job_gbs(nbytes, world, e_ms), "unit": UNIT,
            "h2d_bytes_per_step": xh.numel() * xh.element_size() + lgh.numel() * lgh.element_size(),
            "d2h_bytes_per_step": outh.numel() * outh.element_size(), "ms_per_step": e_ms,
            "steps": e_steps}
