@@ -42,7 +42,8 @@ __all__ = [
     "dequant", "gemm64", "gemm_bf16", "topk_softmax_route", "silu",
     "expert_ffn64", "moe_decode64", "moe_decode_bf16", "argmax_first",
     "lm_head_argmax", "hot_vocab_head_argmax", "rms_scale", "round_to_e2m1",
-    "round_to_e4m3", "nvfp4_quantize", "decode_layer", "nvfp4_weight_bytes",
+    "round_to_e4m3", "nvfp4_quantize", "fp8_gemm64", "fp8_gemm_bf16", "bf16w_gemm64",
+    "bf16w_gemm_bf16", "decode_layer", "nvfp4_weight_bytes",
     "moe_weight_bytes", "decode_roofline_tok_s", "roofline_share",
     "RMS_EPS",
 ]
@@ -195,6 +196,47 @@ def hot_vocab_head_argmax(a, codes, scales, global_scale,
     hot_scales[ok] = scales[vocab_ids[ok]]
     logits = gemm_bf16(a, hot_codes, hot_scales, global_scale)
     return vocab_ids[argmax_first(logits, axis=1)].astype(np.int32), logits
+
+
+# --------------------------------------------------------------------------
+# Other weight formats of the skinny GEMM
+# --------------------------------------------------------------------------
+
+def fp8_gemm64(a: np.ndarray, w: np.ndarray, scale: float,
+               row_chunk: int = 8192) -> np.ndarray:
+    """C[m, n] = sum_k A[m, k] * e4m3(W[n, k]) * scale in float64, unrounded:
+    FP8-E4M3 weights [N, K] (one byte each) with ONE per-tensor float32 scale
+    and 16-bit activations ("Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)",
+    section "Making decode faster", paragraph "An FP8 fast path that never
+    ran": the small-batch FP8 kernel engages for a single per-tensor weight
+    scale)."""
+    a = np.asarray(a, dtype=np.float64)
+    w = np.asarray(w, dtype=np.uint8)
+    s = float(np.float32(scale))
+    out = np.empty((a.shape[0], w.shape[0]), dtype=np.float64)
+    for r0 in range(0, w.shape[0], row_chunk):
+        r1 = min(w.shape[0], r0 + row_chunk)
+        out[:, r0:r1] = a @ (E4M3_TABLE[w[r0:r1]] * s).T
+    return out
+
+
+def fp8_gemm_bf16(a, w, scale) -> np.ndarray:
+    """The FP8-weight skinny GEMM's BF16 output: fp8_gemm64 rounded once."""
+    return bf16_round(fp8_gemm64(a, w, scale))
+
+
+def bf16w_gemm64(a: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """C = A W^T in float64 for 16-bit activations and BF16 weights [N, K]
+    (their values as floats): the split-K skinny GEMM of the 2048 -> 64
+    projections and of 4-bit shared experts expanded to BF16 at load
+    ("Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", section "Making decode
+    faster", paragraph "Skinny matrix multiplies")."""
+    return np.asarray(a, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+
+
+def bf16w_gemm_bf16(a, w) -> np.ndarray:
+    """The BF16-weight skinny GEMM's BF16 output: bf16w_gemm64 rounded once."""
+    return bf16_round(bf16w_gemm64(a, w))
 
 
 # --------------------------------------------------------------------------

@@ -490,6 +490,66 @@ def test_hot_vocab_head_ties_go_to_list_order_and_bad_ids_are_zero_rows():
     assert np.array_equal(logits[:, 1], full[:, 3])
 
 
+# ---------------------------------------------------------------- FP8 and BF16 weights
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 16), (2, 3, 40), (3, 2, 64)])
+def test_fp8_gemm_matches_exact_rational_brute_force(m, n, k):
+    """FP8 weights decoded by torch's E4M3 table (not the oracle's), exact
+    rational sums, one rounding to BF16."""
+    e4 = _torch_e4m3_values()
+    rng = np.random.default_rng(50 + k)
+    a = _rand_bf16((m, k), rng)
+    w = rng.integers(0, 256, size=(n, k), dtype=np.uint8)
+    w[(w & 0x7F) == 0x7F] = 0x38  # no NaN bytes
+    scale = 0.0078125 * 3  # float32-exact
+    c64 = O.fp8_gemm64(a, w, scale)
+    cb = O.fp8_gemm_bf16(a, w, scale)
+    for i in range(m):
+        for j in range(n):
+            exact = sum((Fraction(float(a[i, kk])) * Fraction(float(e4[w[j, kk]])) * Fraction(scale)
+                         for kk in range(k)), Fraction(0))
+            bound = sum(abs(float(a[i, kk])) for kk in range(k)) * 448 * scale * k * 2 ** -52
+            assert abs(Fraction(c64[i, j]) - exact) <= Fraction(bound) + Fraction(2) ** -1070
+            assert cb[i, j] == _nearest_bf16_exact(exact)
+
+
+def test_fp8_gemm_closed_forms():
+    """All weights 1.0 (byte 0x38): each output is the row sum times the
+    scale; a one-hot activation reads back one weight column; the per-tensor
+    scale is linear (a power of two exactly)."""
+    rng = np.random.default_rng(51)
+    a = _rand_bf16((3, 64), rng)
+    ones = np.full((5, 64), 0x38, dtype=np.uint8)
+    assert np.allclose(O.fp8_gemm64(a, ones, 0.5), a.sum(axis=1, keepdims=True) * 0.5 * np.ones((1, 5)),
+                       rtol=1e-14, atol=0)
+    w = rng.integers(0, 0x7E, size=(7, 64), dtype=np.uint8)
+    hot = np.zeros((1, 64))
+    hot[0, 9] = 1.0
+    assert np.array_equal(O.fp8_gemm64(hot, w, 1.0)[0], O.E4M3_TABLE[w[:, 9]])
+    assert np.array_equal(O.fp8_gemm64(a, w, 0.25) * 4, O.fp8_gemm64(a, w, 1.0))
+
+
+def test_bf16_weight_gemm_brute_force_and_expanded_nvfp4_identity():
+    """BF16 weights: exact rational brute force; and the page's claim that 4-bit
+    weights expanded to BF16 at load give identical numbers: every NVFP4 weight
+    (code x scale x 0.5) is a BF16 value, so the BF16-weight GEMM of the
+    expansion equals the NVFP4 GEMM."""
+    rng = np.random.default_rng(52)
+    a = _rand_bf16((2, 48), rng)
+    w = _rand_bf16((3, 48), rng)
+    cb = O.bf16w_gemm_bf16(a, w)
+    for i in range(2):
+        for j in range(3):
+            exact = sum((Fraction(float(a[i, kk])) * Fraction(float(w[j, kk])) for kk in range(48)),
+                        Fraction(0))
+            assert cb[i, j] == _nearest_bf16_exact(exact)
+    codes, scales = _rand_nvfp4(64, 256, rng, 0x01, 0x7E)
+    wx = O.dequant(codes, scales, 0.5)
+    assert np.array_equal(wx, O.bf16_round(wx))
+    a = _rand_bf16((4, 256), rng)
+    assert np.array_equal(O.bf16w_gemm64(a, wx), O.gemm64(a, codes, scales, 0.5))
+
+
 # ---------------------------------------------------------------- quantiser BF16 -> NVFP4
 
 def _grid_probe(grid, rng, top):
