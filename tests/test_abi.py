@@ -22,7 +22,8 @@ def test_header_declares_the_boundary():
     for n in ["nvfp4_gemm_skinny", "moe_nvfp4_decode", "topk_softmax_route",
               "nvfp4_gemm_skinny_workspace", "moe_nvfp4_decode_workspace", "nvfp4_device_check",
               "nvfp4_workspace_init", "nvfp4_read_device_status", "nvfp4_last_dispatch",
-              "nvfp4_last_error"]:
+              "nvfp4_last_error", "nvfp4_gather_rows", "nvfp4_hot_vocab_head", "nvfp4_quantize",
+              "nvfp4_program_create", "nvfp4_program_launch", "nvfp4_gemm_skinny_noalloc"]:
         assert n in names
 
 
@@ -107,3 +108,51 @@ def test_program_validation_codes(lib):
     assert lib.nvfp4_program_create(ctypes.byref(moe), 1, p, 1 << 30, ctypes.byref(h)) == -3
     assert not h.value
     assert lib.nvfp4_program_destroy(None) == 0
+
+
+def test_hot_vocab_head_validation_codes(lib):
+    p = 1 << 20
+    w = _w()
+
+    def call(a=p, m=4, ids=p, c=p, am=p):
+        return lib.nvfp4_hot_vocab_head(a, 2048, m, ctypes.byref(w), ids, c, 64, am, 0, p, 1 << 30,
+                                        None)
+
+    assert call(ids=0) == -1        # the vocabulary ids are required
+    assert call(am=0) == -1         # so is the argmax output
+    assert call(a=0) == -1
+    assert call(m=33) == -3
+    assert call(a=p + 2) == -2
+
+
+def test_gather_rows_validation_codes(lib):
+    p = 1 << 20
+
+    def call(w=None, rows=p, n=16, codes=p, scales=p):
+        w = w or _w()
+        return lib.nvfp4_gather_rows(ctypes.byref(w), rows, n, codes, scales, None)
+
+    assert call(rows=0) == -1
+    assert call(codes=0) == -1
+    assert call(n=0) == -1
+    assert call(w=_w(codes=0)) == -1
+    assert call(w=_w(k=2000)) == -3
+    assert call(codes=p + 8) == -2
+    assert call(w=_w(scales=p + 4)) == -2
+
+
+def test_quantize_validation_codes(lib):
+    p = 1 << 20
+
+    def call(w=p, ldw=2048, n=64, k=2048, codes=p, scales=p, g=p):
+        return lib.nvfp4_quantize(w, ldw, n, k, codes, scales, g, None)
+
+    assert call(w=0) == -1
+    assert call(g=0) == -1
+    assert call(n=0) == -1
+    assert call(ldw=1024) == -1     # ldw < K
+    assert call(k=48, ldw=48) == -3  # K not a multiple of 32
+    assert call(w=p + 2) == -2
+    assert call(ldw=2052) == -2     # row stride not a 16-byte multiple
+    assert call(codes=p + 8) == -2
+    assert call(g=p + 2) == -2      # the float output misaligned
