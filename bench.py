@@ -167,16 +167,76 @@ def profiled_traffic(kernel_key):
     return ent.get("dram_bytes_per_launch")
 
 
-def timed_replays(graph, steps, stream):
+def timed_replays(graph, steps, stream, spread=None):
+    """Milliseconds per replay of ``graph`` over ``steps`` back-to-back
+    replays (CUDA events on ``stream``).  With ``spread`` (a dict) an event
+    after every replay also gives the per-replay times' mean and standard
+    deviation (microseconds) and their count."""
     import torch
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
         graph.replay()
-    e1.record(stream)
-    e1.synchronize()
-    return e0.elapsed_time(e1) / steps  # ms per replay
+        if spread is not None or i == steps - 1:
+            evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    if spread is not None:
+        per = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]) * 1e3
+        spread.update({"mean_us": float(per.mean()), "std_us": float(per.std(ddof=1)) if steps > 1
+                       else 0.0, "n": steps, "min_us": float(per.min()), "max_us": float(per.max())})
+    return evs[0].elapsed_time(evs[-1]) / steps  # ms per replay
+
+
+def versions():
+    """nvcc, driver, torch, the kernel sources' hash and the git commit (when
+    the checkout has one) of this run."""
+    import torch
+    from moe_expert_nvfp4_gb300 import build as B
+    out = {"torch": torch.__version__, "source_hash": B.source_hash()}
+    try:
+        r = subprocess.run([B._nvcc(), "--version"], capture_output=True, text=True, timeout=30)
+        out["nvcc"] = r.stdout.strip().splitlines()[-1]
+    except Exception:
+        out["nvcc"] = None
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,name", "--format=csv,noheader",
+                            "-i", "0"], capture_output=True, text=True, timeout=30)
+        out["driver"], out["gpu"] = [v.strip() for v in r.stdout.strip().split(",")[:2]]
+    except Exception:
+        out["driver"] = out["gpu"] = None
+    try:
+        r = subprocess.run(["git", "rev-parse", "HEAD"], capture_output=True, text=True, cwd=ROOT,
+                           timeout=30)
+        out["git_sha"] = r.stdout.strip() or None
+    except Exception:
+        out["git_sha"] = None
+    return out
+
+
+def read_probe_gbs(reps=10):
+    """Read-only HBM bandwidth of this GPU: the library's probe kernel over a
+    4 GiB buffer (31x L2), best of ``reps`` timed launches."""
+    import torch
+    from moe_expert_nvfp4_gb300 import ops
+    buf = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    sink = torch.empty(4096, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        ops.hbm_read_probe(buf, sink)
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        ops.hbm_read_probe(buf, sink)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    n = buf.numel()
+    del buf
+    return {"gbs": n / (best * 1e-3) / 1e9, "bytes": n, "kernel": "read_probe_kernel",
+            "how": f"best of {reps} launches, CUDA events"}
 
 
 class OracleSample:
@@ -405,6 +465,73 @@ def workload_table(model, reps=10):
         out[f"hot_head_{n_hot}x{s.hidden}_M{m}"] = {"us": us, "gbs": hot_bytes / us / 1e3}
     del hots
 
+    # the other weight formats on the same path: FP8 W8A16 on the attention
+    # projection shapes, BF16 weights on the 2048 -> 64 projection and a
+    # 4096 x 2048 matrix (rotating copies > L2 for the larger shapes)
+    fscale = torch.full((1,), synth.FP8_SCALE, dtype=torch.float32, device=dev)
+    for n, k in ((5120, 2048), (2048, 4096)):
+        copies = [ops.FP8Weight(synth.fp8_weight(70 + i, n, k).to(dev), fscale) for i in range(16)]
+        wk = ops.Workspace(max(int(ops.load().fp8_gemm_skinny_workspace(m, n, k)) for m in (1, 32)))
+        for m in (1, 8, 32):
+            a = synth.activations_bf16(70, m, k).to(dev)
+            c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+
+            def f8():
+                for w in copies:
+                    ops.fp8_gemm(a, w, out=c, workspace=wk)
+            us = graph_us(f8, reps) / len(copies)
+            out[f"fp8_{n}x{k}_M{m}"] = {"us": us, "gbs": n * k / us / 1e3}
+        del copies
+    wb64 = synth.bf16_weight(71, 64, 2048).to(dev)
+    a = synth.activations_bf16(71, 4, 2048).to(dev)
+    c = torch.empty(4, 64, dtype=torch.bfloat16, device=dev)
+    wk = ops.Workspace(int(ops.load().bf16w_gemm_skinny_workspace(4, 64, 2048)))
+    us = graph_us(lambda: ops.bf16w_gemm(a, wb64, out=c, workspace=wk), reps)
+    out["bf16w_2048x64_M4"] = {"us": us, "gbs": 64 * 2048 * 2 / us / 1e3}
+    copies = [synth.bf16_weight(72 + i, 4096, 2048).to(dev) for i in range(12)]
+    wk = ops.Workspace(max(int(ops.load().bf16w_gemm_skinny_workspace(m, 4096, 2048)) for m in (1, 8)))
+    for m in (1, 8):
+        a = synth.activations_bf16(72, m, 2048).to(dev)
+        c = torch.empty(m, 4096, dtype=torch.bfloat16, device=dev)
+
+        def bw():
+            for w in copies:
+                ops.bf16w_gemm(a, w, out=c, workspace=wk)
+        us = graph_us(bw, reps) / len(copies)
+        out[f"bf16w_4096x2048_M{m}"] = {"us": us, "gbs": 4096 * 2048 * 2 / us / 1e3}
+    del copies
+
+    # CUDA cores against tensor cores on the same stream of NVFP4 rows: a
+    # 16,384-row matrix (8 copies, 151 MB), K = 2048 through the tcgen05
+    # kernel (a one-op program when the call itself would take the CUDA-core
+    # kernel) and K = 2080 through the CUDA-core kernel (every K that is not
+    # a multiple of 256 takes it); GB/s counts each call's own bytes
+    n = 16384
+    tc_w = weights(73, n, 2048, 8)
+    fm_w = weights(74, n, 2080, 8)
+    for m in (1, 2, 4, 8):
+        row = {}
+        for name, ws_, k in (("tcgen05", tc_w, 2048), ("cuda_cores", fm_w, 2080)):
+            a = synth.activations_bf16(75, m, k).to(dev)
+            c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+            wk = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
+            ops.gemm(a, ws_[0], out=c, workspace=wk)
+            kern = ops.last_dispatch().split()[0]
+            if name == "tcgen05" and kern != "stream_tc_kernel<dense>":
+                progs = [ops.Program([ops.gemm_op(a, w, c, all_sms=True)]) for w in ws_]
+                us = graph_us(lambda: [p.launch() for p in progs], reps) / len(progs)
+                kern = "stream_tc_kernel (one-op program)"
+                del progs
+            else:
+                def seq():
+                    for w in ws_:
+                        ops.gemm(a, w, out=c, workspace=wk)
+                us = graph_us(seq, reps) / len(ws_)
+            row[name] = {"us": round(us, 2), "gbs": round(nvfp4_bytes(n, k) / us / 1e3, 1),
+                         "kernel": kern}
+        out[f"tc_vs_fma_{n}_M{m}"] = row
+    del tc_w, fm_w
+
     # BF16 -> NVFP4 quantisation of a head-sized BF16 matrix (622 MB >> L2)
     wb = torch.randn(s.vocab, s.hidden, device=dev,
                      generator=torch.Generator(device=dev).manual_seed(62)).to(torch.bfloat16)
@@ -413,8 +540,9 @@ def workload_table(model, reps=10):
     out[f"quantize_{s.vocab}x{s.hidden}"] = {"us": us, "gbs": qbytes / us / 1e3}
     del wb
     for v in out.values():
-        v["us"] = round(v["us"], 2)
-        v["gbs"] = round(v["gbs"], 1)
+        if "us" in v:
+            v["us"] = round(v["us"], 2)
+            v["gbs"] = round(v["gbs"], 1)
     return out
 
 
@@ -462,10 +590,12 @@ def run_ours(args, rank, world, local):
             time.sleep(0.3)
         barrier()
         torch.cuda.synchronize()
-        ms = timed_replays(g, steps, stream)
+        spread = {}
+        ms = timed_replays(g, steps, stream, spread)
         torch.cuda.synchronize()
         barrier()
         clocks = clk.stop() if clk else None
+        b["spread"] = spread
         ms = max_over_ranks(ms, dist, "cuda")
         nbytes = model.step_bytes(b["ids"], t)
         status = b["ws"].status()
@@ -544,10 +674,14 @@ def run_ours(args, rank, world, local):
         k_name = "moe_nvfp4_decode (stream_tc_kernel gate_up + down), per call"
         k_key = f"moe_layer_T{t}"
     achieved = k_bytes / (k_ms * 1e-3) / 1e9
+    probe = read_probe_gbs() if rank == 0 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(k_key),
                 "kernel": k_name, "bytes_per_launch": k_bytes / k_launches,
-                "us_per_launch": k_ms * 1e3 / k_launches, "peak_source": peak_src}
+                "us_per_launch": k_ms * 1e3 / k_launches, "peak_source": peak_src,
+                "frac_of_8tbs": achieved / 8000.0,
+                "read_probe": probe,
+                "frac_of_read_probe": achieved / probe["gbs"] if probe else None}
     del kg
 
     # ---- other token counts of the same step (context)
@@ -601,7 +735,8 @@ def run_ours(args, rank, world, local):
                        "l2": "inputs larger than L2 (each step streams the weights once)",
                        "parallelism": f"{world} independent replica(s)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": n_launch * args.steps, "clocks": clocks, "sweep": sweep,
+            "gpu_launches": n_launch * args.steps, "clocks": clocks,
+            "step_spread": b["spread"], "versions": versions(), "sweep": sweep,
             "path": args.path, "call_by_call": calls, "workloads": workloads,
         }
         print(json.dumps(line), flush=True)

@@ -29,8 +29,10 @@
  *   - Activations are BF16 (uint16 bit patterns of bfloat16), row-major with
  *     a leading dimension in elements.  Pointers and leading dimensions must
  *     give 16-byte aligned rows; weight pointers must be 16-byte aligned.
- *   - K must be a multiple of 256 (one 256-wide stage of the weight stream);
- *     1 <= M, T <= 32.
+ *   - Dense NVFP4 calls take K % 32 == 0 (two E4M3 scale bytes per row per
+ *     32 K); everything else streams 256-K stages and takes K, H, I % 256 ==
+ *     0 (the scales' row pitch K / 16 must then be a multiple of 16 bytes,
+ *     which tensor-memory-access copies need).  1 <= M, T <= 32.
  *   - Return value: NVFP4_OK or a negative status.  On a negative status
  *     nothing was launched and nvfp4_last_error() describes why.  No C++
  *     exception crosses this boundary.
@@ -61,7 +63,7 @@ enum {
   NVFP4_OK = 0,
   NVFP4_ERR_INVALID = -1,   /* null pointer, bad count, k > E ... */
   NVFP4_ERR_ALIGN = -2,     /* pointer / leading dimension not 16-byte aligned */
-  NVFP4_ERR_SHAPE = -3,     /* K % 256 != 0, M or T outside [1, 32], E too large */
+  NVFP4_ERR_SHAPE = -3,     /* K not a supported multiple, M or T outside [1, 32], E too large */
   NVFP4_ERR_ARCH = -4,      /* current device is not compute capability 10.3 */
   NVFP4_ERR_CUDA = -5,      /* a CUDA runtime / launch error */
   NVFP4_ERR_WORKSPACE = -6  /* workspace missing or smaller than required */
@@ -75,9 +77,12 @@ enum {
  * the kernels may read them, and start streaming the routed experts'
  * weights, before waiting for that kernel to finish. */
 #define NVFP4_FLAG_IDS_READY 4u
-/* Use the warp-level MMA kernels (mma.sync) instead of the default tcgen05
- * kernels; kept for comparison, with the same results. */
-#define NVFP4_FLAG_WARP_MMA 8u
+/* Program ops (nvfp4_program_create) only: spread this op over every SM and
+ * split it exactly as its single call does, so its results are bit-identical
+ * to the single call's.  Without it a small dense op of a program runs on
+ * fewer SMs (whole 128-row tiles or few K splits each) while the other SMs
+ * stream the next ops' weights. */
+#define NVFP4_FLAG_ALL_SMS 8u
 
 /* device status bits */
 #define NVFP4_STATUS_BAD_EXPERT_ID 1u /* an id outside [0, E): its slot was skipped */
@@ -120,11 +125,54 @@ int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream);
  *   argmax_out: NULL, or int32 [M]: index of the first maximum of each row of
  *   the BF16 output C (ties to the lowest index).
  * Split-K partial sums are reduced in a fixed order: results are
- * deterministic. */
+ * deterministic.  K % 32 == 0.  Two kernels serve it, chosen by shape alone:
+ * K % 256 == 0 streams 256-K stages through the tensor cores (tcgen05);
+ * other K run on the CUDA cores (whole rows per warp, FP32 accumulation of
+ * the same exact FP16 products), which the dispatch record names. */
 size_t nvfp4_gemm_skinny_workspace(int M, int N, int K);
 int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                       void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
                       void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ---- other weight formats on the same path ------------------------------
+ * "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", section "Making decode
+ * faster": paragraph "An FP8 fast path that never ran" (small-batch
+ * projections with FP8 weights and one per-tensor weight scale: 0.85 -> 1.4
+ * TB/s once the FP8 kernel engaged) and paragraph "Skinny matrix
+ * multiplies" (the 2048 -> 64 projections and the 4-bit shared experts
+ * expanded to BF16 at load, run by a split-K kernel: 8.7 us -> 2.8 us).
+ *
+ * fp8_gemm_skinny: W8A16.  codes uint8 [n, k] E4M3 ("fn") bytes, row-major;
+ * scale: device pointer to one float32.
+ *   C[m][n] = bf16( scale * sum_k A'[m][k] * e4m3(codes[n][k]) ).
+ * bf16w_gemm_skinny: BF16 weights w [n, ldw] (k columns used), row-major.
+ *   C[m][n] = bf16( sum_k A'[m][k] * w[n][k] ).
+ * Everything else as nvfp4_gemm_skinny: A' (NVFP4_FLAG_RMS_INPUT), argmax_out,
+ * flags, FP32 accumulation, deterministic split-K, the workspace rules, the
+ * status codes.  K % 256 == 0; codes / w 16-byte aligned (ldw % 8 == 0).  The
+ * FP8 codes are decoded to FP16 exactly and multiply activation rows staged
+ * as FP16 exactly (as for NVFP4); BF16 weights multiply the BF16
+ * activations as they are. */
+typedef struct fp8_weight {
+  const uint8_t* codes;  /* [n, k] */
+  const float* scale;    /* 1 float */
+  int32_t n, k;
+} fp8_weight;
+
+typedef struct bf16_weight {
+  const void* w;  /* [n, ldw] bf16 */
+  int64_t ldw;
+  int32_t n, k;
+} bf16_weight;
+
+size_t fp8_gemm_skinny_workspace(int M, int N, int K);
+int fp8_gemm_skinny(const void* A, int64_t lda, int M, const fp8_weight* W, void* C, int64_t ldc,
+                    int32_t* argmax_out, uint32_t flags, void* workspace, size_t workspace_bytes,
+                    nvfp4_stream_t stream);
+size_t bf16w_gemm_skinny_workspace(int M, int N, int K);
+int bf16w_gemm_skinny(const void* A, int64_t lda, int M, const bf16_weight* W, void* C,
+                      int64_t ldc, int32_t* argmax_out, uint32_t flags, void* workspace,
+                      size_t workspace_bytes, nvfp4_stream_t stream);
 
 /* ---- dense skinny GEMM without a workspace -------------------------------
  * (This library's own addition; the pages have no counterpart.)  Same
@@ -135,10 +183,12 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
  * built into the library, held on every GPU that loads it until exit; a
  * shape that needs more is rejected with NVFP4_ERR_WORKSPACE.  The first call
  * on a device (with that device current) looks the array's address up; make
- * it before any stream capture.  Each call clears the array's status word
- * and counters on `stream` first.  All calls share the one array: calls that
- * may overlap on the GPU (other streams, concurrent graphs) race and must not
- * be issued. */
+ * it before any stream capture.  The address is kept for the life of the
+ * process: resetting the device while the library is loaded is not
+ * supported.  Every argument is checked first; a refused call touches
+ * nothing.  Each accepted call clears the array's status word and counters on
+ * `stream` first.  All calls share the one array: calls that may overlap on
+ * the GPU (other streams, concurrent graphs) race and must not be issued. */
 int nvfp4_gemm_skinny_noalloc(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                               void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
                               nvfp4_stream_t stream);
@@ -225,15 +275,19 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
  * keeps streaming the weights of the calls ahead while the current call's
  * split-K reductions finish, and a call reads its activations only once every
  * CTA has finished the call before it (completion counters in the workspace).
- * Results are bit-identical to issuing the same calls one by one.
+ * Each op computes what its single call computes.  A small dense op may have
+ * its K range split over fewer CTAs than the single call would use, which
+ * changes the order in which FP32 split-K partials are added, so its output
+ * can differ from the single call's in the last bits; every launch of one
+ * program gives bit-identical results.
  *
  * nvfp4_op: kind NVFP4_OP_GEMM takes the arguments of nvfp4_gemm_skinny (A,
  * lda, M, W, C, ldc, argmax_out) and, for a hot-vocabulary head, argmax_map
  * (NULL, or vocab_ids as in nvfp4_hot_vocab_head; needs argmax_out), kind
  * NVFP4_OP_MOE those of moe_nvfp4_decode
  * (x ... ldo; shared.num_experts == 0 means no shared expert).  flags:
- * NVFP4_FLAG_RMS_INPUT per op (NVFP4_FLAG_NO_PDL and NVFP4_FLAG_IDS_READY are
- * accepted and ignored).  Every MoE op's topk_ids / topk_w must be complete
+ * NVFP4_FLAG_RMS_INPUT and NVFP4_FLAG_ALL_SMS per op (NVFP4_FLAG_NO_PDL and
+ * NVFP4_FLAG_IDS_READY are accepted and ignored).  Every MoE op's topk_ids / topk_w must be complete
  * before the launch (e.g. routed earlier on the stream).  Limits as for the
  * single calls; at most 4,095 kernel ops (a MoE op counts three: gate_up,
  * down, combine).
@@ -286,6 +340,17 @@ int nvfp4_program_destroy(nvfp4_program* program);
  * Copy the workspace's status word to *flags and clear it.  Synchronises
  * `stream`: for tests, not for the decode loop. */
 int nvfp4_read_device_status(void* workspace, uint32_t* flags, nvfp4_stream_t stream);
+
+/* Measurement aid (this library's own; the pages have none): read `bytes`
+ * (a positive multiple of 16) of the device buffer `buf` (16-byte aligned)
+ * once, as a plain streaming kernel does (16-byte loads that bypass L1,
+ * eight in flight per thread, two CTAs per SM), and write one word per CTA
+ * to `sink` (device, at least 8 * SMs bytes) so no load can be dropped.
+ * Timing it over a buffer much larger than L2 gives the read-only HBM
+ * bandwidth, the second denominator for the weight stream's roofline.
+ * Asynchronous on `stream`. */
+int nvfp4_hbm_read_probe(const void* buf, size_t bytes, void* sink, size_t sink_bytes,
+                         nvfp4_stream_t stream);
 
 /* Text describing the launches of this thread's last successful call
  * (kernel, grid, work items, split): tests assert the intended path ran.

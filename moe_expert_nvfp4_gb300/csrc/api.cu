@@ -18,7 +18,6 @@
 #include "nvfp4moe.h"
 #include "common.cuh"
 #include "launch.h"
-#include "stream.cuh"
 
 namespace {
 
@@ -45,6 +44,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_103
+constexpr size_t kSmemAlignPad = 1024;  // the kernel aligns its shared-memory base to 1024 bytes
 
 struct DevInfo {
   int checked = 0;  // 0 unknown, 1 ok, -1 wrong arch
@@ -93,7 +93,7 @@ int get_encoder() {
 }
 
 // uint8 matrix [rows, cols] (row stride = cols bytes) read in boxes of
-// box_cols x 32 rows; codes use the 128-byte swizzle.
+// box_cols x box_rows; codes use the 128-byte swizzle.
 int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
              bool swizzle, uint32_t box_rows) {
   const cuuint64_t dims[2] = {cols, rows};
@@ -109,10 +109,9 @@ int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uin
 }
 
 // Codes and scales of a weight, one 256-K stage wide; boxes of box_rows rows
-// (32 for the warp-MMA kernels and the gate_up tiles, 128 for whole
-// 128-row tiles).
+// (128: one whole tile).
 int weight_maps(CUtensorMap* mc, CUtensorMap* ms, const uint8_t* codes, const uint8_t* scales,
-                uint64_t rows, int k, uint32_t box_rows = kBoxRows) {
+                uint64_t rows, int k, uint32_t box_rows) {
   int rc = make_map(mc, codes, static_cast<uint64_t>(k) / 2, rows, kStageK / 2, true, box_rows);
   if (rc) return rc;
   return make_map(ms, scales, static_cast<uint64_t>(k) / 16, rows, kStageK / 16, false, box_rows);
@@ -147,68 +146,6 @@ int gate_up_maps(CUtensorMap* mc, CUtensorMap* ms, const uint8_t* codes, const u
 
 
 
-// ------------------------------------------------------------- dense plan
-struct DensePlan {
-  int n_tiles, nkb, grid, mpad, win_stages, xrow_bytes;
-  long units;
-  size_t smem;
-  size_t off_partials, off_am, ws_bytes;
-};
-
-// Stream-K: one CTA per SM (or per unit when there are fewer units), each
-// with an equal contiguous range of (tile, k-stage) units; activations are
-// staged in windows of at most win_stages stages.
-bool plan_dense(int M, int N, int K, int sms, DensePlan* p) {
-  p->n_tiles = (N + kTileRows - 1) / kTileRows;
-  if (p->n_tiles > kTcColCntBase) return false;
-  p->nkb = K / kStageK;
-  p->units = static_cast<long>(p->n_tiles) * p->nkb;
-  p->grid = static_cast<int>(p->units < sms ? p->units : sms);
-  p->mpad = (M + 7) / 8 * 8;
-  const size_t x_avail = kSmemLimit - kSmemAlignPad - kSmemSched;
-  int w = p->nkb;
-  while (w > 1 && static_cast<size_t>(p->mpad) * xrow_stride(w * kStageK) > x_avail) --w;
-  if (static_cast<size_t>(p->mpad) * xrow_stride(w * kStageK) > x_avail) return false;
-  p->win_stages = w;
-  p->xrow_bytes = xrow_stride(w * kStageK);
-  p->smem = kSmemAlignPad + kSmemSched + static_cast<size_t>(p->mpad) * p->xrow_bytes;
-  p->off_partials = kWsScratch;
-  p->off_am = round_up(p->off_partials + 4ull * p->grid * 2 * M * 64, 256);
-  p->ws_bytes = round_up(p->off_am + 8ull * M * p->n_tiles, 256);
-  return true;
-}
-
-// ------------------------------------------------------------- MoE plan
-struct MoePlan {
-  int P, tpad, sched_bytes, grid_gu, grid_dn;
-  int xrow_gu, xrow_dn;
-  size_t smem_gu, smem_dn;
-  size_t off_tile_cnt, off_h, off_y, ws_bytes;
-};
-
-bool plan_moe(int T, int k, int E, int H, int I, int sms, MoePlan* p) {
-  p->P = T * k;
-  p->tpad = (T + 7) / 8 * 8;
-  p->sched_bytes = static_cast<int>(round_up(4ull * (4 * E + 5 + 2 * p->P + 33), 16));
-  p->xrow_gu = xrow_stride(H);
-  p->xrow_dn = xrow_stride(I);
-  const size_t base = kSmemAlignPad + kSmemSched + p->sched_bytes;
-  p->smem_gu = base + static_cast<size_t>(p->tpad + 1) * p->xrow_gu;  // + an all-zero row
-  p->smem_dn = base + static_cast<size_t>(p->tpad) * p->xrow_dn;
-  if (p->smem_gu > kSmemLimit || p->smem_dn > kSmemLimit) return false;
-  const long max_active = (p->P < E ? p->P : E) + 1;
-  const long gu_items = max_active * (I / 32), dn_items = max_active * (H / kTileRows);
-  p->grid_gu = static_cast<int>(gu_items < sms ? gu_items : sms);
-  p->grid_dn = static_cast<int>(dn_items < sms ? dn_items : sms);
-  const size_t pairs = static_cast<size_t>(p->P + T);
-  if (H / kTileRows > kWsMaxCounters) return false;
-  p->off_tile_cnt = kWsCounters;
-  p->off_h = kWsScratch;
-  p->off_y = round_up(p->off_h + 4ull * pairs * I, 256);
-  p->ws_bytes = round_up(p->off_y + 4ull * pairs * H, 256);
-  return true;
-}
-
 // ------------------------------------------------------------- tcgen05 plans
 // Shared memory: fixed header (barriers, misc, epilogue tile), the expert
 // schedule, the staged activations [npad][win_k] f16, then as many 18 KB
@@ -223,14 +160,7 @@ bool tc_layout(int sched_bytes, size_t x_bytes, TcLayout* L) {
   L->ring_offset = static_cast<int>(round_up(L->x_offset + x_bytes, 1024));
   const long room = static_cast<long>(kSmemLimit) - kSmemAlignPad - L->ring_offset;
   L->n_stages = static_cast<int>(room / kTcStageBytes);
-  // NVFP4_MAX_STAGES caps the weight ring (3..8): a shallower ring keeps
-  // fewer weight bytes queued ahead of the activation loads at op starts
-  static const int cap = [] {
-    const char* e = getenv("NVFP4_MAX_STAGES");
-    const int v = e ? atoi(e) : kTcMaxStages;
-    return v < 3 ? 3 : (v > kTcMaxStages ? kTcMaxStages : v);
-  }();
-  if (L->n_stages > cap) L->n_stages = cap;
+  if (L->n_stages > kTcMaxStages) L->n_stages = kTcMaxStages;
   if (L->n_stages < 3) return false;
   L->smem = kSmemAlignPad + L->ring_offset + static_cast<size_t>(L->n_stages) * kTcStageBytes;
   return true;
@@ -244,10 +174,10 @@ struct TcDensePlan {
   size_t off_partials, off_am, ws_bytes;
 };
 
-bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p) {
+bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p, int fmt = kFmtNvfp4) {
   p->n_tiles = (N + 127) / 128;
   if (p->n_tiles > kTcColCntBase) return false;
-  p->nkb = K / kStageK;
+  p->nkb = K / tc_unit_k(fmt);
   p->units = static_cast<long>(p->n_tiles) * p->nkb;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   p->npad = M <= 16 ? 16 : 32;
@@ -333,7 +263,7 @@ int check_gemm(const void* A, int64_t lda, int M, const nvfp4_weight* W, const v
   const int N = W->n, K = W->k;
   if (M < 1 || M > kMaxM) return fail(NVFP4_ERR_SHAPE, "M=%d outside [1, 32]", M);
   if (N < 1 || K < 1) return fail(NVFP4_ERR_INVALID, "N=%d K=%d must be positive", N, K);
-  if (K % kStageK) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 256", K);
+  if (K % 32) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 32", K);
   if (lda < K || ldc < N) return fail(NVFP4_ERR_INVALID, "lda < K or ldc < N");
   if (!aligned16(A) || (lda * 2) % 16 || !aligned16(W->codes) || !aligned16(W->scales))
     return fail(NVFP4_ERR_ALIGN, "A rows and weight arrays must be 16-byte aligned");
@@ -363,23 +293,96 @@ int check_moe(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const 
   return NVFP4_OK;
 }
 
+// ------------------------------------------------------------- CUDA-core path
+// Activation rows up to which a dense NVFP4 call with K % 256 == 0 runs on
+// the CUDA cores (fma.cu) instead of the tensor cores; K % 256 != 0 always
+// does (the tensor path streams 256-K stages).
+constexpr int kFmaMaxM = 0;
+
+struct FmaPlan {
+  int grid, rows_per_cta;
+  size_t smem, off_am, ws_bytes;
+};
+
+bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
+  p->rows_per_cta = fma_rows_per_cta(M);
+  p->smem = static_cast<size_t>(p->rows_per_cta) * (K / 32) * 64;
+  if (p->smem > 200 * 1024) return false;
+  const int ru = 4 / p->rows_per_cta;           // weight rows a warp takes at once
+  const long groups = (static_cast<long>(N) + ru - 1) / ru;
+  const long ctas = (groups + 7) / 8;           // eight warps a CTA
+  p->grid = static_cast<int>(ctas < 2L * sms ? ctas : 2L * sms);
+  const int row_groups = (M + p->rows_per_cta - 1) / p->rows_per_cta;
+  if (4 + 4 * row_groups > static_cast<int>(kWsCounters)) return false;
+  p->off_am = kWsScratch;
+  p->ws_bytes = round_up(p->off_am + 8ull * M * p->grid, 256);
+  return true;
+}
+
+bool use_fma(int M, int K) { return K % kStageK != 0 || M <= kFmaMaxM; }
+
 // ------------------------------------------------------------- tcgen05 ops
+// K stages per CTA that a small dense op of a program is cut into (whole
+// tiles when K has at most this many stages).  Measured on the 40-layer
+// decode step at T = 8: 4 and 8 give the same step time; 16, and every op
+// on every SM, are slower.
+constexpr int kProgramTargetStages = 8;
+
 void ws_header(TcArgs& a, uint8_t* ws) {
   a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
   a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
 }
 
+// A dense weight of any format: NVFP4 (codes, scales, per-tensor scale),
+// FP8 E4M3 bytes [n, k] (codes) with one FP32 scale, or BF16 [n, ld] (codes).
+struct DenseW {
+  int fmt;
+  const void* codes;
+  const void* scales;
+  const float* scale;
+  int64_t ld;  // BF16: row stride in elements
+  int n, k;
+};
+
+DenseW dense_w(const nvfp4_weight* W) {
+  return DenseW{kFmtNvfp4, W->codes, W->scales, W->global_scale, W->k / 2, W->n, W->k};
+}
+
+// BF16 matrix [rows, ld] (k columns used) read in boxes of 64 x 128 rows
+// (128 bytes x 128 rows, 128-byte swizzle).
+int bf16_weight_map(CUtensorMap* m, const void* base, int64_t ld, int k, int rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (bf16 weight) failed (%d)", (int)r);
+  return NVFP4_OK;
+}
+
 // Dense op of a planned GEMM (arguments already checked).
-int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C, int64_t ldc,
+int tc_dense_op(const void* A, int64_t lda, int M, const DenseW& W, void* C, int64_t ldc,
                 int32_t* argmax_out, const int32_t* am_map, uint32_t flags, uint8_t* ws,
                 const TcDensePlan& p, TcOp* op) {
   memset(op, 0, sizeof(*op));
-  int rc = weight_maps(&op->maps[0], &op->maps[1], W->codes, W->scales,
-                       static_cast<uint64_t>(W->n), W->k, kTcTileRows);
+  int rc;
+  if (W.fmt == kFmtNvfp4) {
+    rc = weight_maps(&op->maps[0], &op->maps[1], static_cast<const uint8_t*>(W.codes),
+                     static_cast<const uint8_t*>(W.scales), static_cast<uint64_t>(W.n), W.k,
+                     kTcTileRows);
+    op->maps[2] = op->maps[0];
+    op->maps[3] = op->maps[1];
+  } else if (W.fmt == kFmtFp8) {
+    rc = make_map(&op->maps[0], W.codes, static_cast<uint64_t>(W.k), static_cast<uint64_t>(W.n),
+                  128, true, kTcTileRows);
+  } else {
+    rc = bf16_weight_map(&op->maps[0], W.codes, W.ld, W.k, W.n);
+  }
   if (rc) return rc;
-  op->maps[2] = op->maps[0];
-  op->maps[3] = op->maps[1];
-  if ((rc = act_map(&op->xmap, A, M, lda, W->k, p.xrows))) return rc;
+  if ((rc = act_map(&op->xmap, A, M, lda, W.k, p.xrows))) return rc;
   TcArgs& a = op->a;
   a.A = static_cast<const __nv_bfloat16*>(A);
   a.lda = lda;
@@ -387,10 +390,12 @@ int tc_dense_op(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* 
   a.ldc = ldc;
   a.argmax_out = argmax_out;
   a.am_map = am_map;
-  a.gscale = W->global_scale;
+  a.gscale = W.scale;
   a.M = M;
-  a.N = W->n;
-  a.K = W->k;
+  a.N = W.n;
+  a.K = W.k;
+  a.fmt = W.fmt;
+  a.uk = tc_unit_k(W.fmt);
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.win_k = p.win_k;
   a.n_ctas = p.grid;
@@ -437,6 +442,8 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   a.has_shared = shared ? 1 : 0;
   a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  a.fmt = kFmtNvfp4;
+  a.uk = kStageK;
   ws_header(a, ws);
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.h = reinterpret_cast<float*>(ws + p.off_h);
@@ -504,6 +511,10 @@ int tc_launch_one(const TcOp& op, size_t x_bytes, int sched_bytes, int grid, uin
 
 namespace nvfp4 {
 void set_last_error(const char* msg) { g_error = msg; }
+int check_gemm_args(const void* A, int64_t lda, int M, const nvfp4_weight* W, const void* C,
+                    int64_t ldc) {
+  return check_gemm(A, lda, M, W, C, ldc);
+}
 }  // namespace nvfp4
 
 // A program: its op table on the device and the launch that runs it.
@@ -539,91 +550,113 @@ int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream) {
 
 size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
   int sms = 0;
-  if (M < 1 || M > kMaxM || N < 1 || K < kStageK || K % kStageK) return 0;
+  if (M < 1 || M > kMaxM || N < 1 || K < 32 || K % 32) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
-  DensePlan p;
+  if (use_fma(M, K)) {
+    FmaPlan f;
+    return plan_fma(M, N, K, sms, &f) ? f.ws_bytes : 0;
+  }
   TcDensePlan t;
-  const size_t a = plan_dense(M, N, K, sms, &p) ? p.ws_bytes : 0;
-  const size_t b = plan_tc_dense(M, N, K, sms, &t) ? t.ws_bytes : 0;
-  return a > b ? a : b;
+  return plan_tc_dense(M, N, K, sms, &t) ? t.ws_bytes : 0;
 }
 
-// The dense skinny GEMM; am_map (nullable) maps the argmax's row index to
-// the id reported.
+// The dense skinny GEMM of any weight format (arguments already checked);
+// am_map (nullable) maps the argmax's row index to the id reported.
+static int dense_skinny(const char* name, const void* A, int64_t lda, int M, const DenseW& W,
+                        void* C, int64_t ldc, int32_t* argmax_out, const int32_t* am_map,
+                        uint32_t flags, void* workspace, size_t workspace_bytes,
+                        nvfp4_stream_t stream) {
+  int rc;
+  const int N = W.n, K = W.k;
+  int sms = 0;
+  if ((rc = current_device(&sms))) return rc;
+  TcDensePlan p;
+  if (!plan_tc_dense(M, N, K, sms, &p, W.fmt))
+    return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
+  if (!workspace || workspace_bytes < p.ws_bytes)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
+  if ((rc = get_encoder())) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  TcOp op;
+  if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, am_map, flags, ws, p, &op))) return rc;
+  int n_stages = 0;
+  size_t smem = 0;
+  rc = tc_launch_one(op, p.x_bytes, 0, p.grid, ws,
+                     reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL),
+                     &n_stages, &smem, "stream_tc_kernel<dense> launch");
+  if (rc) return rc;
+  char buf[256];
+  snprintf(buf, sizeof(buf),
+           "stream_tc_kernel<dense> weight=%s grid=%d tiles=%d units=%ld units_per_cta=%.2f "
+           "window=%d n=%d stages=%d smem=%zu argmax=%d rms=%d",
+           name, p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_k,
+           p.npad, n_stages, smem, argmax_out ? 1 : 0, op.a.rms);
+  g_dispatch = buf;
+  return NVFP4_OK;
+}
+
+// The CUDA-core kernel (arguments already checked).
+static int fma_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
+                      int64_t ldc, int32_t* argmax_out, const int32_t* am_map, uint32_t flags,
+                      void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  int sms = 0, rc;
+  if ((rc = current_device(&sms))) return rc;
+  FmaPlan p;
+  if (!plan_fma(M, W->n, W->k, sms, &p))
+    return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", W->n, W->k);
+  if (!workspace || workspace_bytes < p.ws_bytes)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FmaArgs a;
+  a.A = static_cast<const __nv_bfloat16*>(A);
+  a.lda = lda;
+  a.codes = W->codes;
+  a.scales = W->scales;
+  a.gscale = W->global_scale;
+  a.C = static_cast<__nv_bfloat16*>(C);
+  a.ldc = ldc;
+  a.argmax_out = argmax_out;
+  a.am_map = am_map;
+  a.M = M;
+  a.N = W->n;
+  a.K = W->k;
+  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
+  a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
+  const cudaError_t e = launch_fma(a, p.grid, reinterpret_cast<cudaStream_t>(stream),
+                                   !(flags & NVFP4_FLAG_NO_PDL));
+  if (e != cudaSuccess) return cuda_fail(e, "fma_kernel launch");
+  char buf[192];
+  snprintf(buf, sizeof(buf), "fma_kernel grid=%dx%d rows_per_cta=%d smem=%zu argmax=%d rms=%d",
+           p.grid, (M + p.rows_per_cta - 1) / p.rows_per_cta, p.rows_per_cta, p.smem,
+           argmax_out ? 1 : 0, a.rms);
+  g_dispatch = buf;
+  return NVFP4_OK;
+}
+
 static int gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
                        int64_t ldc, int32_t* argmax_out, const int32_t* am_map, uint32_t flags,
                        void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
   int rc = check_gemm(A, lda, M, W, C, ldc);
   if (rc) return rc;
-  const int N = W->n, K = W->k;
-  int sms = 0;
-  if ((rc = current_device(&sms))) return rc;
-  if (!(flags & NVFP4_FLAG_WARP_MMA)) {
-    TcDensePlan p;
-    if (!plan_tc_dense(M, N, K, sms, &p))
-      return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
-    if (!workspace || workspace_bytes < p.ws_bytes)
-      return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
-    if ((rc = get_encoder())) return rc;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    TcOp op;
-    if ((rc = tc_dense_op(A, lda, M, W, C, ldc, argmax_out, am_map, flags, ws, p, &op))) return rc;
-    int n_stages = 0;
-    size_t smem = 0;
-    rc = tc_launch_one(op, p.x_bytes, 0, p.grid, ws,
-                       reinterpret_cast<cudaStream_t>(stream), !(flags & NVFP4_FLAG_NO_PDL),
-                       &n_stages, &smem, "stream_tc_kernel<dense> launch");
-    if (rc) return rc;
-    char buf[256];
-    snprintf(buf, sizeof(buf),
-             "stream_tc_kernel<dense> grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d "
-             "n=%d stages=%d smem=%zu argmax=%d rms=%d",
-             p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_k, p.npad,
-             n_stages, smem, argmax_out ? 1 : 0, op.a.rms);
-    g_dispatch = buf;
-    return NVFP4_OK;
-  }
-  DensePlan p;
-  if (!plan_dense(M, N, K, sms, &p)) return fail(NVFP4_ERR_SHAPE, "N=%d, K=%d: no feasible plan", N, K);
-  if (!workspace || workspace_bytes < p.ws_bytes)
-    return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
-  if ((rc = get_encoder())) return rc;
-  CUtensorMap maps[2];
-  if ((rc = weight_maps(&maps[0], &maps[1], W->codes, W->scales, static_cast<uint64_t>(N), K)))
-    return rc;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DenseArgs a = {};
-  a.A = static_cast<const __nv_bfloat16*>(A);
-  a.lda = lda;
-  a.C = static_cast<__nv_bfloat16*>(C);
-  a.ldc = ldc;
-  a.argmax_out = argmax_out;
-  a.am_map = am_map;
-  a.gscale = W->global_scale;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.n_tiles = p.n_tiles;
-  a.nkb = p.nkb;
-  a.win_stages = p.win_stages;
-  a.xrow_bytes = p.xrow_bytes;
-  a.x_offset = kSmemSched;
-  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
-  a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
-  a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
-  a.tile_cnt = reinterpret_cast<uint32_t*>(ws + kWsCounters);
-  a.partials = reinterpret_cast<float*>(ws + p.off_partials);
-  a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
-  cudaError_t e = launch_dense(maps, a, p.grid, p.smem, reinterpret_cast<cudaStream_t>(stream),
-                               !(flags & NVFP4_FLAG_NO_PDL));
-  if (e != cudaSuccess) return cuda_fail(e, "dense_gemm_kernel launch");
-  char buf[256];
-  snprintf(buf, sizeof(buf),
-           "dense_gemm_kernel grid=%d tiles=%d units=%ld units_per_cta=%.2f window=%d smem=%zu "
-           "argmax=%d rms=%d",
-           p.grid, p.n_tiles, p.units, static_cast<double>(p.units) / p.grid, p.win_stages,
-           p.smem, argmax_out ? 1 : 0, a.rms);
-  g_dispatch = buf;
+  if (use_fma(M, W->k))
+    return fma_skinny(A, lda, M, W, C, ldc, argmax_out, am_map, flags, workspace,
+                      workspace_bytes, stream);
+  return dense_skinny("nvfp4", A, lda, M, dense_w(W), C, ldc, argmax_out, am_map, flags,
+                      workspace, workspace_bytes, stream);
+}
+
+// Checks shared by the FP8 and BF16 weight formats (K a multiple of 256, as
+// for NVFP4: activations are staged in 256-K blocks).
+static int check_dense_common(const void* A, int64_t lda, int M, int N, int K, const void* C,
+                              int64_t ldc) {
+  if (!A || !C) return fail(NVFP4_ERR_INVALID, "A and C must be non-NULL");
+  if (M < 1 || M > kMaxM) return fail(NVFP4_ERR_SHAPE, "M=%d outside [1, 32]", M);
+  if (N < 1 || K < 1) return fail(NVFP4_ERR_INVALID, "N=%d K=%d must be positive", N, K);
+  if (K % kStageK) return fail(NVFP4_ERR_SHAPE, "K=%d is not a multiple of 256", K);
+  if (lda < K || ldc < N) return fail(NVFP4_ERR_INVALID, "lda < K or ldc < N");
+  if (!aligned16(A) || (lda * 2) % 16) return fail(NVFP4_ERR_ALIGN, "A rows must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(C) & 1u) return fail(NVFP4_ERR_ALIGN, "C must be 2-byte aligned");
   return NVFP4_OK;
 }
 
@@ -632,6 +665,48 @@ int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
                       size_t workspace_bytes, nvfp4_stream_t stream) {
   return gemm_skinny(A, lda, M, W, C, ldc, argmax_out, nullptr, flags, workspace,
                      workspace_bytes, stream);
+}
+
+size_t fp8_gemm_skinny_workspace(int M, int N, int K) {
+  int sms = 0;
+  if (M < 1 || M > kMaxM || N < 1 || K < kStageK || K % kStageK) return 0;
+  if (current_device(&sms) != NVFP4_OK) return 0;
+  TcDensePlan t;
+  return plan_tc_dense(M, N, K, sms, &t, kFmtFp8) ? t.ws_bytes : 0;
+}
+
+int fp8_gemm_skinny(const void* A, int64_t lda, int M, const fp8_weight* W, void* C, int64_t ldc,
+                    int32_t* argmax_out, uint32_t flags, void* workspace, size_t workspace_bytes,
+                    nvfp4_stream_t stream) {
+  if (!W || !W->codes || !W->scale) return fail(NVFP4_ERR_INVALID, "FP8 weight has a NULL pointer");
+  int rc = check_dense_common(A, lda, M, W->n, W->k, C, ldc);
+  if (rc) return rc;
+  if (!aligned16(W->codes)) return fail(NVFP4_ERR_ALIGN, "weight must be 16-byte aligned");
+  const DenseW d{kFmtFp8, W->codes, nullptr, W->scale, W->k, W->n, W->k};
+  return dense_skinny("fp8", A, lda, M, d, C, ldc, argmax_out, nullptr, flags, workspace,
+                      workspace_bytes, stream);
+}
+
+size_t bf16w_gemm_skinny_workspace(int M, int N, int K) {
+  int sms = 0;
+  if (M < 1 || M > kMaxM || N < 1 || K < kStageK || K % kStageK) return 0;
+  if (current_device(&sms) != NVFP4_OK) return 0;
+  TcDensePlan t;
+  return plan_tc_dense(M, N, K, sms, &t, kFmtBf16) ? t.ws_bytes : 0;
+}
+
+int bf16w_gemm_skinny(const void* A, int64_t lda, int M, const bf16_weight* W, void* C,
+                      int64_t ldc, int32_t* argmax_out, uint32_t flags, void* workspace,
+                      size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (!W || !W->w) return fail(NVFP4_ERR_INVALID, "BF16 weight has a NULL pointer");
+  int rc = check_dense_common(A, lda, M, W->n, W->k, C, ldc);
+  if (rc) return rc;
+  if (W->ldw < W->k) return fail(NVFP4_ERR_INVALID, "ldw < K");
+  if (!aligned16(W->w) || (W->ldw * 2) % 16)
+    return fail(NVFP4_ERR_ALIGN, "weight rows must be 16-byte aligned");
+  const DenseW d{kFmtBf16, W->w, nullptr, nullptr, W->ldw, W->n, W->k};
+  return dense_skinny("bf16", A, lda, M, d, C, ldc, argmax_out, nullptr, flags, workspace,
+                      workspace_bytes, stream);
 }
 
 int nvfp4_hot_vocab_head(const void* A, int64_t lda, int M, const nvfp4_weight* W_hot,
@@ -723,13 +798,9 @@ size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* expert
   int sms = 0;
   if (!experts || T < 1 || T > kMaxM || k < 1 || k > 16) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
-  MoePlan p;
   TcMoePlan t;
-  const size_t a = plan_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &p)
-                       ? p.ws_bytes : 0;
-  const size_t b = plan_tc_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &t)
-                       ? t.ws_bytes : 0;
-  return a > b ? a : b;
+  return plan_tc_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &t)
+             ? t.ws_bytes : 0;
 }
 
 int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
@@ -741,99 +812,39 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   const int E = experts->num_experts, H = experts->hidden, I = experts->inter;
   int sms = 0;
   if ((rc = current_device(&sms))) return rc;
-  if (!(flags & NVFP4_FLAG_WARP_MMA)) {
-    TcMoePlan p;
-    if (!plan_tc_moe(T, k, E, H, I, sms, &p))
-      return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d, E=%d: staged activations exceed shared memory",
-                  T, H, E);
-    if (!workspace || workspace_bytes < p.ws_bytes)
-      return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
-    if ((rc = get_encoder())) return rc;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    TcOp gu, dn, cb;
-    if ((rc = tc_moe_ops(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo, flags, ws, p,
-                         &gu, &dn, &cb)))
-      return rc;
-    const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int st_gu = 0, st_dn = 0;
-    size_t sm_gu = 0, sm_dn = 0;
-    if ((rc = tc_launch_one(gu, static_cast<size_t>(p.xrows) * H * 2, p.sched_bytes, p.grid, ws,
-                            s, pdl, &st_gu, &sm_gu, "stream_tc_kernel<gate_up> launch")) ||
-        (rc = tc_launch_one(dn, static_cast<size_t>(p.xrows) * I * 2, p.sched_bytes, p.grid, ws,
-                            s, pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
-      return rc;
-    int st_cb = 0;
-    size_t sm_cb = 0;
-    if ((rc = tc_launch_one(cb, 0, p.sched_bytes, p.grid, ws, s, pdl, &st_cb, &sm_cb,
-                            "stream_tc_kernel<combine> launch")))
-      return rc;
-    char buf[256];
-    snprintf(buf, sizeof(buf),
-             "stream_tc_kernel<gate_up> grid=%d stages=%d smem=%zu; stream_tc_kernel<down> grid=%d "
-             "stages=%d smem=%zu; stream_tc_kernel<combine> grid=%d; T=%d k=%d E=%d n=%d "
-             "shared=%d rms=%d ids_ready=%d",
-             p.grid, st_gu, sm_gu, p.grid, st_dn, sm_dn, p.grid, T, k, E, p.npad,
-             gu.a.has_shared, gu.a.rms, gu.a.ids_ready);
-    g_dispatch = buf;
-    return NVFP4_OK;
-  }
-  MoePlan p;
-  if (!plan_moe(T, k, E, H, I, sms, &p))
-    return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d: staged activations exceed shared memory", T, H);
+  TcMoePlan p;
+  if (!plan_tc_moe(T, k, E, H, I, sms, &p))
+    return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d, E=%d: staged activations exceed shared memory",
+                T, H, E);
   if (!workspace || workspace_bytes < p.ws_bytes)
     return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", p.ws_bytes);
   if ((rc = get_encoder())) return rc;
-  const nvfp4_expert_stack* sh = shared ? shared : experts;
-  CUtensorMap gu[4], dn[4];
-  if ((rc = weight_maps(&gu[0], &gu[1], experts->gu_codes, experts->gu_scales,
-                        2ull * I * E, H)) ||
-      (rc = weight_maps(&gu[2], &gu[3], sh->gu_codes, sh->gu_scales, 2ull * I * sh->num_experts,
-                        H)) ||
-      (rc = weight_maps(&dn[0], &dn[1], experts->dn_codes, experts->dn_scales,
-                        static_cast<uint64_t>(H) * E, I)) ||
-      (rc = weight_maps(&dn[2], &dn[3], sh->dn_codes, sh->dn_scales,
-                        static_cast<uint64_t>(H) * sh->num_experts, I)))
-    return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  MoeArgs a = {};
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.ldx = ldx;
-  a.ids = topk_ids;
-  a.w = topk_w;
-  a.out = static_cast<__nv_bfloat16*>(out);
-  a.ldo = ldo;
-  a.gu_global = experts->gu_global;
-  a.dn_global = experts->dn_global;
-  a.sh_gu_global = sh->gu_global;
-  a.sh_dn_global = sh->dn_global;
-  a.T = T;
-  a.k = k;
-  a.E = E;
-  a.H = H;
-  a.I = I;
-  a.has_shared = shared ? 1 : 0;
-  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
-  a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
-  a.x_offset = kSmemSched + p.sched_bytes;
-  a.sched_offset = kSmemSched;
-  a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
-  a.tile_cnt = reinterpret_cast<uint32_t*>(ws + p.off_tile_cnt);
-  a.h = reinterpret_cast<float*>(ws + p.off_h);
-  a.y = reinterpret_cast<float*>(ws + p.off_y);
+  TcOp gu, dn, cb;
+  if ((rc = tc_moe_ops(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo, flags, ws, p,
+                       &gu, &dn, &cb)))
+    return rc;
   const bool pdl = !(flags & NVFP4_FLAG_NO_PDL);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  a.xrow_bytes = p.xrow_gu;
-  cudaError_t e = launch_moe_gate_up(gu, a, p.grid_gu, p.smem_gu, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_gate_up_kernel launch");
-  a.xrow_bytes = p.xrow_dn;
-  e = launch_moe_down(dn, a, p.grid_dn, p.smem_dn, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "moe_down_kernel launch");
+  int st_gu = 0, st_dn = 0;
+  size_t sm_gu = 0, sm_dn = 0;
+  if ((rc = tc_launch_one(gu, static_cast<size_t>(p.xrows) * H * 2, p.sched_bytes, p.grid, ws,
+                          s, pdl, &st_gu, &sm_gu, "stream_tc_kernel<gate_up> launch")) ||
+      (rc = tc_launch_one(dn, static_cast<size_t>(p.xrows) * I * 2, p.sched_bytes, p.grid, ws,
+                          s, pdl, &st_dn, &sm_dn, "stream_tc_kernel<down> launch")))
+    return rc;
+  int st_cb = 0;
+  size_t sm_cb = 0;
+  if ((rc = tc_launch_one(cb, 0, p.sched_bytes, p.grid, ws, s, pdl, &st_cb, &sm_cb,
+                          "stream_tc_kernel<combine> launch")))
+    return rc;
   char buf[256];
   snprintf(buf, sizeof(buf),
-           "moe_gate_up_kernel grid=%d smem=%zu; moe_down_kernel grid=%d smem=%zu; T=%d k=%d "
-           "E=%d shared=%d rms=%d ids_ready=%d",
-           p.grid_gu, p.smem_gu, p.grid_dn, p.smem_dn, T, k, E, a.has_shared, a.rms, a.ids_ready);
+           "stream_tc_kernel<gate_up> grid=%d stages=%d smem=%zu; stream_tc_kernel<down> grid=%d "
+           "stages=%d smem=%zu; stream_tc_kernel<combine> grid=%d; T=%d k=%d E=%d n=%d "
+           "shared=%d rms=%d ids_ready=%d",
+           p.grid, st_gu, sm_gu, p.grid, st_dn, sm_dn, p.grid, T, k, E, p.npad,
+           gu.a.has_shared, gu.a.rms, gu.a.ids_ready);
   g_dispatch = buf;
   return NVFP4_OK;
 }
@@ -894,19 +905,22 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
   for (int i = 0; i < n_ops; ++i) {
     const nvfp4_op& o = ops[i];
     if (o.flags & ~static_cast<uint32_t>(NVFP4_FLAG_RMS_INPUT | NVFP4_FLAG_NO_PDL |
-                                         NVFP4_FLAG_IDS_READY))
+                                         NVFP4_FLAG_IDS_READY | NVFP4_FLAG_ALL_SMS))
       return fail(NVFP4_ERR_INVALID, "op %d: unsupported flags 0x%x", i, o.flags);
     if (o.kind == NVFP4_OP_GEMM) {
       if ((rc = check_gemm(o.A, o.lda, o.M, &o.W, o.C, o.ldc))) return rc;
+      if (o.W.k % kStageK)
+        return fail(NVFP4_ERR_SHAPE, "op %d: K=%d: program ops need K %% 256 == 0", i, o.W.k);
       TcDensePlan p;
       if (!plan_tc_dense(o.M, o.W.n, o.W.k, sms, &p))
         return fail(NVFP4_ERR_SHAPE, "op %d: N=%d, K=%d: no feasible plan", i, o.W.n, o.W.k);
       TcOp op;
       if (o.argmax_map && !o.argmax_out)
         return fail(NVFP4_ERR_INVALID, "op %d: argmax_map without argmax_out", i);
-      if ((rc = tc_dense_op(o.A, o.lda, o.M, &o.W, o.C, o.ldc, o.argmax_out, o.argmax_map, o.flags,
-                            ws, p, &op)))
+      if ((rc = tc_dense_op(o.A, o.lda, o.M, dense_w(&o.W), o.C, o.ldc, o.argmax_out,
+                            o.argmax_map, o.flags, ws, p, &op)))
         return rc;
+      op.all_sms = (o.flags & NVFP4_FLAG_ALL_SMS) ? 1 : 0;
       table.push_back(op);
       x_bytes = std::max(x_bytes, p.x_bytes);
       need = std::max(need, p.ws_bytes);
@@ -941,14 +955,13 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
   // only tiles x ceil(K stages / target) CTAs (whole tiles, or few splits per
   // tile: short reductions), placed after the previous small op's CTAs, so
   // that the other SMs stream the following ops' weights meanwhile.  Ops with
-  // at least one tile per SM (and MoE ops) use every SM.  Environment
-  // NVFP4_PROGRAM_TARGET_STAGES (default 8; 0 = every op on every SM).
-  int target = 8;
-  if (const char* env = getenv("NVFP4_PROGRAM_TARGET_STAGES")) target = atoi(env);
+  // at least one tile per SM (and MoE ops, and ops flagged
+  // NVFP4_FLAG_ALL_SMS) use every SM.
+  constexpr int target = kProgramTargetStages;
   int next_cta = 0;
   for (TcOp& op : table) {
     int g = sms;
-    if (op.mode == kTcDense && target > 0) {
+    if (op.mode == kTcDense && !op.all_sms) {
       const int n_tiles = (op.a.N + 127) / 128, nkb = op.a.K / kStageK;
       if (n_tiles < sms) {
         const int splits = (nkb + target - 1) / target;
@@ -1021,6 +1034,25 @@ int nvfp4_read_device_status(void* workspace, uint32_t* flags, nvfp4_stream_t st
   if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, 4, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "status read");
+}
+
+int nvfp4_hbm_read_probe(const void* buf, size_t bytes, void* sink, size_t sink_bytes,
+                         nvfp4_stream_t stream) {
+  if (!buf || !sink) return fail(NVFP4_ERR_INVALID, "buf and sink must be non-NULL");
+  if (bytes == 0 || bytes % 16) return fail(NVFP4_ERR_INVALID, "bytes must be a positive multiple of 16");
+  if (!aligned16(buf)) return fail(NVFP4_ERR_ALIGN, "buf must be 16-byte aligned");
+  int sms = 0, rc;
+  if ((rc = current_device(&sms))) return rc;
+  const int grid = 2 * sms;
+  if (sink_bytes < 4ull * grid)
+    return fail(NVFP4_ERR_WORKSPACE, "sink needs %d bytes", 4 * grid);
+  const cudaError_t e = launch_read_probe(buf, bytes, static_cast<uint32_t*>(sink), grid,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read_probe_kernel launch");
+  char b2[96];
+  snprintf(b2, sizeof(b2), "read_probe_kernel grid=%d bytes=%zu", grid, bytes);
+  g_dispatch = b2;
+  return NVFP4_OK;
 }
 
 int nvfp4_last_dispatch(char* buf, size_t n) {

@@ -1,8 +1,8 @@
 // Device helpers shared by the NVFP4 decode kernels (sm_103a).
 //
-// Inline PTX for: mbarriers with bounded waits, 2-D TMA tile loads, the
-// hardware E2M1 / E4M3 -> FP16 conversions, packed FP16 multiply, the warp
-// MMA, and programmatic dependent launch.  Every wait here is bounded by a
+// Inline PTX for: mbarriers with bounded waits, TMA tile loads, the hardware
+// E2M1 / E4M3 -> FP16 conversions, packed FP16 multiply, GPU-scope
+// counters, and programmatic dependent launch.  Every wait here is bounded by a
 // wall-clock limit: on expiry it records NVFP4_STATUS_WAIT_TIMEOUT and
 // returns, so a kernel never hangs the GPU.
 #pragma once
@@ -13,19 +13,9 @@
 
 namespace nvfp4 {
 
-// ------------------------------------------------------------------ tiling
-constexpr int kTileRows = 64;                              // weight rows per work item
-constexpr int kBoxRows = 32;                               // rows per TMA box (2 per stage)
+// ------------------------------------------------------------------ limits
 constexpr int kStageK = 256;                               // K values per pipeline stage
-constexpr int kStageCodeBytes = kTileRows * kStageK / 2;   // 8192, 128B-swizzled
-constexpr int kStageScaleBytes = kTileRows * kStageK / 16; // 1024
-constexpr int kStageBytes = kStageCodeBytes + kStageScaleBytes;
-constexpr int kStages = 8;
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;            // + one producer warp
-constexpr int kMaxM = 32;
-constexpr int kXPad = 8;                                   // bytes of padding per staged x row
+constexpr int kMaxM = 32;                                  // activation rows per call
 constexpr unsigned long long kWaitLimitNs = 2000000000ull; // 2 s per wait
 
 constexpr uint32_t kStatusBadId = 1u;
@@ -70,14 +60,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-      "r"(bytes)
-      : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_u32(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -97,15 +79,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
-}
-
-// 16-byte global -> shared copy through L2 (cp.async.cg); the thread waits
-// for its own copies with cp_async_wait_all.
-__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t a) {
@@ -163,19 +136,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ------------------------------------------------------------------ TMA
-// 2-D tiled bulk tensor load into shared memory; completion is signalled on
-// `bar` as transaction bytes.  x = innermost coordinate (bytes for uint8
-// maps; always a multiple of 16 here), y = row.
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
-// The same with shared-memory addresses given as 32-bit values.
+// 2-D tiled bulk tensor load into shared memory (addresses as 32-bit
+// shared-memory values); completion is signalled on `bar` as transaction
+// bytes.  x = innermost coordinate (bytes for uint8 maps; always a multiple
+// of 16 here), y = row.
 __device__ __forceinline__ void tma_load_2d_u32(uint32_t smem_dst, const CUtensorMap* map, int x,
                                                 int y, uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -193,27 +157,6 @@ __device__ __forceinline__ void tma_load_4d_u32(uint32_t smem_dst, const CUtenso
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// Contiguous bulk copy global -> shared (16-byte aligned addresses, size a
-// multiple of 16), completion signalled on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_load_u32(uint32_t smem_dst, const void* src, uint32_t bytes,
-                                              uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-// The same without an L2 cache hint (activations read by every CTA).
-__device__ __forceinline__ void tma_load_2d_nohint(void* smem_dst, const CUtensorMap* map, int x,
-                                                   int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -245,12 +188,15 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& d0, uint32
       : "r"(w));
 }
 
-// One E4M3 byte, broadcast to both halves of an f16x2 (exact).
-__device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
-  const uint16_t two = static_cast<uint16_t>((byte & 0xFFu) * 0x0101u);
-  uint32_t d;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(two));
-  return d;
+// Four E4M3 bytes (byte i = element i) -> two f16x2: elements 0, 1 and 2, 3
+// (low half = the lower element; exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& d0, uint32_t& d1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(d0), "=r"(d1)
+      : "r"(w));
 }
 
 // Two E4M3 bytes (low byte: first block) -> each broadcast to both halves
@@ -260,35 +206,6 @@ __device__ __forceinline__ void e4m3x2_bcast_f16x2(uint32_t two, uint32_t& lo, u
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two & 0xFFFFu)));
   lo = __byte_perm(h2, 0u, 0x1010);
   hi = __byte_perm(h2, 0u, 0x3232);
-}
-
-// Two E2M1 values held as FP16 (from cvt.rn.f16x2.e2m1x2: 0 or an FP16
-// normal with at most one mantissa bit) -> the same values times 2^-112 as
-// BF16 (exact): the FP16 exponent field lands in the low five bits of the
-// BF16 exponent field (bias 15 read against 127), zero stays zero.
-__device__ __forceinline__ uint32_t f16x2_to_bf16x2_scaled(uint32_t v) {
-  return ((v >> 3) & 0x0FFF0FFFu) | (v & 0x80008000u);
-}
-
-// One E4M3 byte times 2^112 as BF16, broadcast to both halves (exact: E4M3
-// values 2^-9 .. 448 become 2^103 .. 448 * 2^112 < 2^128).
-__device__ __forceinline__ uint32_t e4m3_bcast_bf16x2_x2p112(uint32_t byte) {
-  const uint16_t two = static_cast<uint16_t>((byte & 0xFFu) * 0x0101u);
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-  float f;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
-      : "=f"(f) : "r"(h2));
-  f *= 5.192296858534828e+33f;  // 2^112
-  uint32_t d;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(f));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -301,16 +218,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
-}
-
-// D(16x8, f32) += A(16x16, f16, row) * B(16x8, f16, col)
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ------------------------------------------------------------------ scaling
@@ -337,6 +244,28 @@ __device__ __forceinline__ int f16_row_shift(float amax) {
 __device__ __forceinline__ float scale_pow2(float v, int s) {
   const int h = s / 2;
   return (v * exp2i(h)) * exp2i(s - h);
+}
+
+// Rows whose largest magnitude is at most 2^56 have a plain FP32 sum of
+// squares below 4096 * 2^112 (no overflow), and their squares that underflow
+// are below 2^-149 against a sum that is then either negligible next to 1e-6
+// or above 2^-100: the plain sum gives their RMS factor.
+constexpr float kSumsqSafeMax = 72057594037927936.0f;  // 2^56
+
+__device__ __forceinline__ float rms_plain(float sq, int klen) {
+  return rsqrtf(sq / static_cast<float>(klen) + 1e-6f);
+}
+
+// 1 / sqrt(mean(x^2) + 1e-6) of a row of klen elements from the sum of the
+// squares of its elements times 2^sh (sq), sh being the row's staging shift
+// (f16_row_shift of its largest magnitude, at most 250).  Rows far below 1
+// (sh > 100) have a mean square below 2^-170: the 1e-6 decides alone.
+__device__ __forceinline__ float rms_factor(float sq, int sh, int klen) {
+  const float m = sq / static_cast<float>(klen);  // mean of the shifted squares
+  if (sh >= 0) return rsqrtf((sh > 100 ? 0.0f : scale_pow2(m, -2 * sh)) + 1e-6f);
+  // large rows: 2^sh / sqrt(m + 1e-6 * 2^(2 sh)); the factor stays a normal
+  // float (sh >= -113 for BF16 rows)
+  return exp2i(sh) * rsqrtf(m + scale_pow2(1e-6f, 2 * sh));
 }
 
 // ------------------------------------------------------------------ gpu-scope sync
@@ -367,11 +296,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-
-// Named barrier among the consumer warps only (the producer never joins).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
 }  // namespace nvfp4

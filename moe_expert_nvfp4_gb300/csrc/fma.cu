@@ -1,0 +1,401 @@
+// NVFP4 skinny GEMM on the CUDA cores: decode and dot product in registers.
+//
+// The other dense path (stream_tc.cu) hands the dot product to the tensor
+// cores; at one or two activation rows a weight costs only one or two FMAs,
+// which the CUDA cores can issue at the HBM rate.  This kernel is that
+// alternative, and the path for K that is a multiple of 32 but not of 256
+// (the tensor-memory path streams 256-K stages).
+//
+// Layout of the work: one warp computes whole rows n of C (no split-K).
+// Lane l owns the 32-K chunks l, l + 32, ... of a row: per chunk it loads 16
+// bytes of E2M1 codes and the chunk's two E4M3 block scales, converts the
+// codes to FP16 (hardware convert, exact) and accumulates code x activation
+// per 16-element block with the mixed FMA (f16 x f16 + f32 -> f32, the
+// product exact), then adds block scale x block sum into the row's FP32
+// total.  A warp reduction ends the row.  The activations (1, 2 or 4 rows
+// per CTA, grid.y covering the rest) are staged once per CTA in shared memory as FP16 after the
+// same power-of-two row shift as the tensor path (exact for BF16 rows),
+// with a bank-conflict-free swizzle of each chunk's four 16-byte slots.
+//
+// Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
+// faster", "Skinny matrix multiplies" (decode matmuls of four to sixteen
+// activation rows against 4-bit weights).
+#include <cuda_bf16.h>
+#include <float.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kFmaWarps = 8;
+constexpr int kFmaThreads = kFmaWarps * 32;
+
+__device__ __forceinline__ float fma_f16(uint32_t a_half_pair, uint32_t b_half_pair, bool hi,
+                                         float c) {
+  float d;
+  if (hi)
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
+        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
+  else
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
+        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// Byte offset of 16-byte slot q (0..3) of chunk c of row m in the staged
+// activations: chunks of 64 bytes, slot index xor-ed with (c / 2) % 4 so
+// that the eight lanes of one shared-memory phase (chunks c .. c + 7, same q)
+// hit eight different 16-byte bank groups.
+__device__ __forceinline__ uint32_t act_off(int m, int c, int q, int chunks) {
+  return static_cast<uint32_t>(((m * chunks + c) * 4 + (q ^ ((c >> 1) & 3))) * 16);
+}
+
+__device__ __forceinline__ bool fm_better(float v, int i, float bv, int bi) {
+  return bi == 0x7fffffff || v > bv || (v == bv && i < bi);
+}
+
+// Sum over the CTA of one float per thread (thread 0 gets it; the warps'
+// sums are added in warp order).
+__device__ __forceinline__ float cta_sum0(float v, float* s_w) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kFmaWarps; ++w) t += s_w[w];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ float cta_max0(float v, float* s_w) {
+  v = warp_max(v);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kFmaWarps; ++w) t = fmaxf(t, s_w[w]);
+  __syncthreads();
+  return t;
+}
+
+// MB activation rows per CTA (rows m0 .. m0 + MB - 1 of A, m0 = MB *
+// blockIdx.y); grid-stride over the weight rows.
+template <int MB>
+__global__ void __launch_bounds__(kFmaThreads) fma_kernel(const FmaArgs a) {
+  extern __shared__ __align__(16) uint8_t fsm[];
+  __shared__ int s_sh[MB];
+  __shared__ float s_rms[MB];
+  __shared__ float s_w[kFmaWarps];
+  __shared__ float s_bv[kFmaWarps][MB];
+  __shared__ int s_bi[kFmaWarps][MB];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = MB * blockIdx.y;
+  const int mb = min(MB, a.M - m0);
+  const int chunks = a.K / 32;
+  const uint32_t xs = smem_u32(fsm);
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- per row: the largest magnitude and the plain sum of squares, the
+  // FP16 shift and the RMS factor (rows above 2^56 sum their shifted
+  // squares in a second pass: no overflow at any magnitude)
+  for (int r = 0; r < MB; ++r) {
+    float mx = 0.0f, sq = 0.0f;
+    const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + (r < mb ? r : 0)) * a.lda;
+    if (r < mb)
+      for (int v = threadIdx.x; v < a.K / 8; v += kFmaThreads) {
+        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+          mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
+          sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+        }
+      }
+    const float rmax = cta_max0(mx, s_w);
+    const float rsq = cta_sum0(sq, s_w);
+    if (threadIdx.x == 0) {
+      s_sh[r] = r < mb ? f16_row_shift(rmax) : 0;
+      s_rms[r] = (!a.rms || r >= mb) ? 1.0f : (rmax > kSumsqSafeMax ? -1.0f : rms_plain(rsq, a.K));
+    }
+    __syncthreads();
+    if (s_rms[r] < 0.0f) {  // uniform over the CTA
+      const int sh = s_sh[r];
+      const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+      const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+      float s3 = 0.0f;
+      for (int v = threadIdx.x; v < a.K / 8; v += kFmaThreads) {
+        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+          const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+          s3 = fmaf(lo, lo, fmaf(hi, hi, s3));
+        }
+      }
+      const float s4 = cta_sum0(s3, s_w);
+      if (threadIdx.x == 0) s_rms[r] = rms_factor(s4, sh, a.K);
+      __syncthreads();
+    }
+  }
+  // the shifted FP16 rows: 16-byte slot q of chunk c = elements 32 c + 8 q ..
+  for (int it = threadIdx.x; it < MB * chunks * 4; it += kFmaThreads) {
+    const int r = it / (chunks * 4), rem = it - r * chunks * 4, c = rem >> 2, q = rem & 3;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (r < mb) {
+      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(row + 32 * c + 8 * q));
+      const int sh = s_sh[r];
+      const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+      const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+      const bool two = h1 != sh;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo = __uint_as_float(w[j] << 16) * f1, hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1;
+        if (two) {
+          lo *= f2;
+          hi *= f2;
+        }
+        p[j] = pack_f16x2(lo, hi);
+      }
+      o = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+    st_shared_v4(xs + act_off(r, c, q, chunks), o);
+  }
+  __syncthreads();
+
+  // ---- rows of W
+  // output = (row sum x 2^-shift) x tensor scale x RMS factor, in that order
+  // (the undone shift alone could fall below FP32's range)
+  const float gs = *a.gscale;
+  int shift[MB];
+  float post[MB];
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    shift[r] = s_sh[r];
+    post[r] = a.rms ? s_rms[r] : 1.0f;
+  }
+  float am_v[MB];
+  int am_i[MB];
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    am_v[r] = -FLT_MAX;
+    am_i[r] = 0x7fffffff;
+  }
+  // A warp takes groups of RU consecutive weight rows (group G = the warp's
+  // global index + t * warps); per group the lanes walk the rows' 32-K
+  // chunks in rounds of 32.  The loads of the next round (or group) are
+  // issued before the current one is computed, so RU * 528 bytes per warp
+  // stay in flight.
+  constexpr int RU = 4 / MB;
+  const int n_warps = gridDim.x * kFmaWarps;
+  const int rounds = (chunks + 31) / 32;
+  const int n_groups = (a.N + RU - 1) / RU;
+  int G = blockIdx.x * kFmaWarps + warp, cr = 0;
+  uint4 cw[RU], nw[RU];
+  uint32_t sb[RU], ns[RU];
+  auto load = [&](int g, int round, uint4 (&w)[RU], uint32_t (&sc)[RU]) {
+    const int c = round * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < RU; ++j) {
+      const int n = g * RU + j;
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      sc[j] = 0u;
+      if (g < n_groups && n < a.N && c < chunks) {
+        w[j] = __ldcs(reinterpret_cast<const uint4*>(a.codes + static_cast<size_t>(n) * (a.K / 2) +
+                                                     16 * c));
+        sc[j] = *reinterpret_cast<const uint16_t*>(a.scales + static_cast<size_t>(n) * (a.K / 16) +
+                                                   2 * c);
+      }
+    }
+  };
+  load(G, 0, cw, sb);
+  float acc[MB][RU];
+#pragma unroll
+  for (int r = 0; r < MB; ++r)
+#pragma unroll
+    for (int j = 0; j < RU; ++j) acc[r][j] = 0.0f;
+  while (G < n_groups) {
+    // the next item's loads first
+    const int nG = cr + 1 < rounds ? G : G + n_warps;
+    const int ncr = cr + 1 < rounds ? cr + 1 : 0;
+    load(nG, ncr, nw, ns);
+    const int c = cr * 32 + lane;
+    if (c < chunks) {
+#pragma unroll
+      for (int r = 0; r < MB; ++r) {
+        // slots 0, 1: block 0 (k 0..15 of the chunk); slots 2, 3: block 1
+        const uint4 x0 = ld_shared_v4(xs + act_off(r, c, 0, chunks));
+        const uint4 x1 = ld_shared_v4(xs + act_off(r, c, 1, chunks));
+        const uint4 x2 = ld_shared_v4(xs + act_off(r, c, 2, chunks));
+        const uint4 x3 = ld_shared_v4(xs + act_off(r, c, 3, chunks));
+        const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                 x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+        for (int j = 0; j < RU; ++j) {
+          uint32_t s2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(static_cast<uint16_t>(sb[j])));
+          const float sc0 = f16_lo_to_f32(s2), sc1 = f16_lo_to_f32(s2 >> 16);
+          const uint32_t wds[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
+          uint32_t code[16];
+#pragma unroll
+          for (int wi = 0; wi < 4; ++wi)
+            e2m1x8_to_f16x2(wds[wi], code[4 * wi], code[4 * wi + 1], code[4 * wi + 2],
+                            code[4 * wi + 3]);
+          float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            b0 = fma_f16(code[e], xv[e], false, b0);
+            b0 = fma_f16(code[e], xv[e], true, b0);
+            b1 = fma_f16(code[8 + e], xv[8 + e], false, b1);
+            b1 = fma_f16(code[8 + e], xv[8 + e], true, b1);
+          }
+          acc[r][j] = fmaf(sc0, b0, acc[r][j]);
+          acc[r][j] = fmaf(sc1, b1, acc[r][j]);
+        }
+      }
+    }
+    if (cr + 1 == rounds) {  // the group's rows are complete
+#pragma unroll
+      for (int j = 0; j < RU; ++j) {
+        const int n = G * RU + j;
+#pragma unroll
+        for (int r = 0; r < MB; ++r) {
+          const float t = warp_sum(acc[r][j]);
+          acc[r][j] = 0.0f;
+          if (r < mb && n < a.N) {
+            const __nv_bfloat16 o = __float2bfloat16_rn(scale_pow2(t, -shift[r]) * gs * post[r]);
+            if (lane == 0) a.C[static_cast<size_t>(m0 + r) * a.ldc + n] = o;
+            const float ov = __bfloat162float(o);
+            if (fm_better(ov, n, am_v[r], am_i[r])) {
+              am_v[r] = ov;
+              am_i[r] = n;
+            }
+          }
+        }
+      }
+    }
+    G = nG;
+    cr = ncr;
+#pragma unroll
+    for (int j = 0; j < RU; ++j) {
+      cw[j] = nw[j];
+      sb[j] = ns[j];
+    }
+  }
+
+  // ---- argmax: the CTA's best per row, then the last CTA of the row group
+  // reduces the partials of every CTA (the order of (value, index) pairs is
+  // total, so the result does not depend on arrival order)
+  if (!a.argmax_out) return;
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    float bv = am_v[r];
+    int bi = am_i[r];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && fm_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      s_bv[warp][r] = bv;
+      s_bi[warp][r] = bi;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < mb; ++r) {
+      float bv = -FLT_MAX;
+      int bi = 0x7fffffff;
+      for (int w = 0; w < kFmaWarps; ++w)
+        if (s_bi[w][r] != 0x7fffffff && fm_better(s_bv[w][r], s_bi[w][r], bv, bi)) {
+          bv = s_bv[w][r];
+          bi = s_bi[w][r];
+        }
+      a.am_part[static_cast<size_t>(m0 + r) * gridDim.x + blockIdx.x] =
+          make_int2(__float_as_int(bv), bi);
+    }
+    // releases this CTA's partials; the last adder acquires the others'
+    const uint32_t prev = atom_add_acq_rel_gpu(a.argmax_cnt + blockIdx.y, 1u);
+    s_last = prev == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int r = warp; r < mb; r += kFmaWarps) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+    for (int j = lane; j < static_cast<int>(gridDim.x); j += 32) {
+      const int2 pr = __ldcg(a.am_part + static_cast<size_t>(m0 + r) * gridDim.x + j);
+      const float v = __int_as_float(pr.x);
+      if (pr.y != 0x7fffffff && fm_better(v, pr.y, bv, bi)) {
+        bv = v;
+        bi = pr.y;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && fm_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0) a.argmax_out[m0 + r] = (a.am_map && bi != 0x7fffffff) ? a.am_map[bi] : bi;
+  }
+  if (threadIdx.x == 0) a.argmax_cnt[blockIdx.y] = 0u;
+}
+
+template <int MB>
+cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
+  const size_t smem = static_cast<size_t>(MB) * (a.K / 32) * 64;
+  cudaError_t e = cudaFuncSetAttribute(fma_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem < 1024 ? 1024 : smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, (a.M + MB - 1) / MB);
+  cfg.blockDim = dim3(kFmaThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fma_kernel<MB>, a);
+}
+
+}  // namespace
+
+int fma_rows_per_cta(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : 4); }
+
+cudaError_t launch_fma(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
+  switch (fma_rows_per_cta(a.M)) {
+    case 1: return launch_mb<1>(a, grid, s, pdl);
+    case 2: return launch_mb<2>(a, grid, s, pdl);
+    default: return launch_mb<4>(a, grid, s, pdl);
+  }
+}
+
+}  // namespace nvfp4

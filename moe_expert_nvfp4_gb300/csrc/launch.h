@@ -8,16 +8,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
-namespace nvfp4 {
+#include "nvfp4moe.h"
 
-// Shared-memory carve-up of the streaming kernels (byte offsets from a
-// 1024-byte aligned base).  x staging comes last and is sized per launch.
-constexpr int kSmemRing = 0;
-constexpr int kSmemBars = kSmemRing + 8 * 9216;        // kStages * kStageBytes
-constexpr int kSmemMisc = kSmemBars + 2 * 8 * 8;       // full + empty mbarriers
-constexpr int kSmemEp = kSmemMisc + 512;               // sig[32], rms[32], flags
-constexpr int kSmemSched = kSmemEp + 32 * 64 * 4;      // epilogue tile [32][64] f32
-constexpr int kSmemAlignPad = 1024;
+namespace nvfp4 {
 
 // Workspace layout shared by every call, so that one workspace can serve a
 // sequence of different calls: [0, 256) status word and the argmax counter;
@@ -28,51 +21,6 @@ constexpr size_t kWsArgmaxCnt = 4;
 constexpr size_t kWsCounters = 256;
 constexpr int kWsMaxCounters = 16384;
 constexpr size_t kWsScratch = kWsCounters + 4 * kWsMaxCounters;
-
-struct DenseArgs {
-  const __nv_bfloat16* A;
-  int64_t lda;
-  __nv_bfloat16* C;
-  int64_t ldc;
-  int32_t* argmax_out;     // nullable
-  const int32_t* am_map;   // nullable: argmax_out reports am_map[n] instead of n
-  const float* gscale;
-  int M, N, K;
-  int n_tiles, nkb;        // 64-row tiles; K / 256 stages per tile
-  int win_stages;          // stages of activations staged at once
-  int xrow_bytes;          // staged row stride (bytes)
-  int x_offset;            // smem offset of the x staging area
-  int rms;                 // NVFP4_FLAG_RMS_INPUT
-  uint32_t* status;
-  uint32_t* tile_cnt;      // [n_tiles]
-  uint32_t* argmax_cnt;    // [1]
-  float* partials;         // [gridDim.x][2][M][64]
-  int2* am_part;           // [M][n_tiles] (float bits of value, index)
-};
-
-struct MoeArgs {
-  const __nv_bfloat16* x;
-  int64_t ldx;
-  const int32_t* ids;
-  const float* w;
-  __nv_bfloat16* out;
-  int64_t ldo;
-  const float* gu_global;  // [E]
-  const float* dn_global;  // [E]
-  const float* sh_gu_global;
-  const float* sh_dn_global;
-  int T, k, E, H, I;
-  int has_shared;
-  int rms;
-  int ids_ready;           // ids/weights complete before the previous kernel started
-  int xrow_bytes;
-  int x_offset;
-  int sched_offset;
-  uint32_t* status;
-  uint32_t* tile_cnt;      // [H / 64]
-  float* h;                // [T*k + T][I]
-  float* y;                // [T*k + T][H]
-};
 
 // ---- tcgen05 streaming kernel (stream_tc.cu) ------------------------------
 // One launch runs a program: a sequence of ops (dense GEMM, MoE gate_up, MoE
@@ -100,6 +48,16 @@ constexpr int kTcInlineOps = 1;                          // ops passed by value 
 // outputs (no weights: only the epilogue warps work).
 enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2, kTcCombine = 3 };
 
+// Weight format of a dense op.  Every format streams 128-row x 128-byte
+// boxes of codes (the 128-byte swizzle), one box per unit of work:
+//   NVFP4: 256 K per unit (E2M1 pairs) + a 128 x 16 box of E4M3 scales;
+//   FP8:   128 K per unit, E4M3 bytes, one FP32 scale for the matrix;
+//   BF16:  64 K per unit, read by the MMA from shared memory as it is.
+enum TcFmt { kFmtNvfp4 = 0, kFmtFp8 = 1, kFmtBf16 = 2 };
+__host__ __device__ constexpr int tc_unit_k(int fmt) {
+  return fmt == kFmtNvfp4 ? 256 : (fmt == kFmtFp8 ? 128 : 64);
+}
+
 struct TcArgs {
   // dense
   const __nv_bfloat16* A;
@@ -125,6 +83,8 @@ struct TcArgs {
   float* h;
   float* y;
   // common
+  int fmt;              // TcFmt of a dense op's weight (MoE: NVFP4)
+  int uk;               // K per unit of work: tc_unit_k(fmt)
   int rms;
   int win_k;            // staged activation window capacity (elements, multiple of 256)
   int n_ctas;           // CTAs the op's units are spread over (at most gridDim.x) ...
@@ -151,6 +111,7 @@ struct TcOp {
   int new_sched;       // MoE: build a new expert schedule from this op's ids
   int last_sched_use;  // MoE: no later op uses the current schedule
   int wait_prev;       // read inputs only after every CTA finished the previous op
+  int all_sms;         // program placement: spread over every SM (as the single call)
 };
 
 struct TcProgram {
@@ -175,14 +136,6 @@ struct RouteArgs {
   float* w;
 };
 
-// maps: codes / scales of the weight (dense), or routed gate_up, routed down,
-// shared gate_up, shared down (MoE).
-cudaError_t launch_dense(const CUtensorMap* maps, const DenseArgs& a, int grid, size_t smem,
-                         cudaStream_t s, bool pdl);
-cudaError_t launch_moe_gate_up(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
-                               cudaStream_t s, bool pdl);
-cudaError_t launch_moe_down(const CUtensorMap* maps, const MoeArgs& a, int grid, size_t smem,
-                            cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
 
 // Row gather of an NVFP4 matrix [N, K]: dst row i = src row rows[i] (codes
@@ -214,7 +167,39 @@ struct QuantArgs {
 };
 cudaError_t launch_quantize(const QuantArgs& a, int sms, cudaStream_t s);
 
+// ---- CUDA-core NVFP4 skinny GEMM (fma.cu) ----------------------------------
+// Whole rows per warp, no split-K; K % 32 == 0.  argmax: am_part [M][grid]
+// partials and argmax_cnt [row groups] counters (zero between calls).
+struct FmaArgs {
+  const __nv_bfloat16* A;
+  int64_t lda;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* gscale;
+  __nv_bfloat16* C;
+  int64_t ldc;
+  int32_t* argmax_out;
+  const int32_t* am_map;
+  int M, N, K;
+  int rms;
+  uint32_t* argmax_cnt;
+  int2* am_part;
+};
+// activation rows per CTA for M rows (1, 2 or 4); grid.y = ceil(M / that)
+int fma_rows_per_cta(int M);
+cudaError_t launch_fma(const FmaArgs& a, int grid, cudaStream_t s, bool pdl);
+
+// Read-only bandwidth probe (probe.cu): reads bytes (a multiple of 16) of
+// buf once; writes one word per CTA (grid words) to sink.
+cudaError_t launch_read_probe(const void* buf, size_t bytes, uint32_t* sink, int grid,
+                              cudaStream_t s);
+
 // Record the message returned by nvfp4_last_error() for this thread.
 void set_last_error(const char* msg);
+
+// The host-side argument checks of nvfp4_gemm_skinny (pointers, shape,
+// alignment): NVFP4_OK or the status that call would return.
+int check_gemm_args(const void* A, int64_t lda, int M, const struct nvfp4_weight* W,
+                    const void* C, int64_t ldc);
 
 }  // namespace nvfp4

@@ -14,7 +14,9 @@
 // code cannot use the array's name as a device address, so the first call
 // on each device (made with that device current) looks the address up with
 // cudaGetSymbolAddress and caches it; that first call should therefore come
-// before any stream capture.  All calls share the one array and it keeps
+// before any stream capture.  The cached address belongs to the device's
+// primary context: resetting the device (cudaDeviceReset) while the library
+// is loaded is not supported.  All calls share the one array and it keeps
 // the previous call's contents: each call first clears, on its stream, the
 // status word and tile counters that must start at zero.  Two calls that
 // may run at the same time on the GPU (different streams, or graphs
@@ -61,8 +63,19 @@ void* scratch_address(cudaError_t* err) {
 extern "C" int nvfp4_gemm_skinny_noalloc(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                                           void* C, int64_t ldc, int32_t* argmax_out,
                                           uint32_t flags, nvfp4_stream_t stream) {
-  // W == nullptr and invalid shapes are reported by nvfp4_gemm_skinny itself
-  const size_t need = W ? nvfp4_gemm_skinny_workspace(M, W->n, W->k) : 0;
+  // Every argument is checked before the shared scratch is touched: a call
+  // that is going to be refused must not clear the array under a call still
+  // running on another stream.
+  int rc = nvfp4::check_gemm_args(A, lda, M, W, C, ldc);
+  if (rc) return rc;
+  // The largest need on a GB300 is the workspace header (65,792 bytes) plus
+  // 32,768 bytes of split-K partials and 8 * 32 bytes of argmax partials per
+  // SM: about 5.1 MB for 152 SMs, under the 8 MiB built in.
+  const size_t need = nvfp4_gemm_skinny_workspace(M, W->n, W->k);
+  if (need == 0) {
+    nvfp4::set_last_error("nvfp4_gemm_skinny_noalloc: no plan for this shape");
+    return NVFP4_ERR_SHAPE;
+  }
   if (need > kNoAllocScratchBytes) {
     nvfp4::set_last_error("nvfp4_gemm_skinny_noalloc: this shape needs more than the 8 MiB "
                           "of built-in scratch; use nvfp4_gemm_skinny with a workspace");

@@ -43,6 +43,8 @@
 #include <cuda_bf16.h>
 #include <float.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "sched.cuh"
@@ -221,7 +223,9 @@ struct Kernel {
     if (MODE == kTcGateUp) return a.T;
     return sc.cnt[sc.active[tile / wk.per_e]];
   }
-  __device__ __forceinline__ int win_stages() const { return a.win_k / kSK; }
+  // K per unit: the dense op's format decides; MoE ops stream NVFP4
+  __device__ __forceinline__ int uk() const { return MODE == kTcDense ? a.uk : kSK; }
+  __device__ __forceinline__ int win_stages() const { return a.win_k / uk(); }
 };
 
 // Staged-row bookkeeping shared (identically) by the MMA thread and the
@@ -234,12 +238,20 @@ struct XState {
   }
 };
 
+// Units per 256 K: activations are staged in 256-K blocks (one 16-byte load
+// per lane and row), so a dense window starts and ends on a multiple of it.
+template <int MODE>
+__device__ __forceinline__ int units_per_256(const Kernel<MODE>& kk) { return kSK / kk.uk(); }
+
 // Window [w0, w1) of a segment starting at stage w0: MoE, the whole segment
-// (its K is staged once); dense, at most win_stages stages, staged exactly.
+// (its K is staged once); dense, at most win_stages stages from w0 rounded
+// down to a 256-K boundary (win_stages is a multiple of 256 K, so the
+// rounded window still fits).
 template <int MODE>
 __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kbe) {
   if (MODE != kTcDense) return kbe;
-  return min(kbe, w0 + kk.win_stages());
+  const int g = units_per_256(kk);
+  return min(kbe, w0 / g * g + kk.win_stages());
 }
 
 // Stage range restaged when a window is not covered: MoE, the whole K (its
@@ -250,8 +262,9 @@ template <int MODE>
 __device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1,
                                               bool one_tile, int& k0, int& k1) {
   if (MODE == kTcDense && (kk.win_stages() < kk.wk.nkb || one_tile)) {
-    k0 = w0;
-    k1 = w1;
+    const int g = units_per_256(kk);  // K % 256 == 0: nkb is a multiple of g
+    k0 = w0 / g * g;
+    k1 = (w1 + g - 1) / g * g;
   } else {
     k0 = 0;
     k1 = kk.wk.nkb;
@@ -342,7 +355,7 @@ __device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, cons
   Work wk{};
   if (MODE == kTcDense) {
     wk.n_tiles = (a.N + kRows - 1) / kRows;
-    wk.nkb = a.K / kSK;
+    wk.nkb = a.K / a.uk;
   } else {
     const int na = c.aborted() ? 0 : min(max(*sc.n_active, 0), a.E + 1);
     if (MODE == kTcGateUp) {
@@ -411,10 +424,11 @@ __device__ __forceinline__ void stage_row_load(const T* row, int n, int nr, int 
   }
 }
 
-// Largest magnitude (as a float) and sum of squares of a row's loads.
+// Largest magnitude (as a float) of a row's loads and, when want_sq, the
+// plain FP32 sum of their squares (BF16 rows only).
 template <typename T>
-__device__ __forceinline__ void stage_row_stats(const uint4 (&b)[kStageSlots], int ppr, bool want_sq,
-                                                float& m, float& sq) {
+__device__ __forceinline__ float stage_row_max(const uint4 (&b)[kStageSlots], int ppr, bool want_sq,
+                                               float& sq) {
   uint32_t mx = 0u;  // BF16: the largest |x| of each half as bits (|x| orders like its bits)
   float mf = 0.0f;
   sq = 0.0f;
@@ -431,16 +445,35 @@ __device__ __forceinline__ void stage_row_stats(const uint4 (&b)[kStageSlots], i
             sq = fmaf(lo, lo, fmaf(hi, hi, sq));
           }
         } else {
-          const float f = __uint_as_float(w[j]);
-          mf = fmaxf(mf, fabsf(f));
-          if (want_sq) sq = fmaf(f, f, sq);
+          mf = fmaxf(mf, fabsf(__uint_as_float(w[j])));
         }
       }
     }
-  if constexpr (sizeof(T) == 2)
-    m = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
-  else
-    m = mf;
+  if constexpr (sizeof(T) == 2) return fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+  return mf;
+}
+
+// Sum of the squares of a BF16 row's loads times 2^(2 sh): the row's shift
+// puts its largest square near 2^29, so the sum neither overflows nor loses
+// the row's significant terms, whatever the row's magnitude.  Scaling by a
+// power of two commutes with the roundings, so for rows inside FP32's range
+// the result is the plain sum of squares times 2^(2 sh).
+__device__ __forceinline__ float stage_row_sumsq(const uint4 (&b)[kStageSlots], int ppr, int sh) {
+  const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+  const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+  float sq = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kStageSlots; ++i)
+    if (i < ppr) {
+      const uint32_t w[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+        const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+        sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+      }
+    }
+  return sq;
 }
 
 // The FP16 conversion of a row's loads times 2^sh, stored into the staged
@@ -448,8 +481,18 @@ __device__ __forceinline__ void stage_row_stats(const uint4 (&b)[kStageSlots], i
 // slot is at base(n, l) + (i / kLd) * 4 * rb * 128 (xoff with k = 8 kc).
 template <typename T>
 __device__ __forceinline__ void stage_row_store(const uint4 (&b)[kStageSlots], int n, int rb,
-                                                int ppr, int sh, uint32_t xs, int lane) {
+                                                int ppr, int sh, uint32_t xs, int lane, bool raw) {
   constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
+  if constexpr (sizeof(T) == 2) {
+    if (raw) {  // BF16 operand: the loads as they are
+      const uint32_t base = xs + xoff(n, 8 * lane, rb);
+      const uint32_t step = static_cast<uint32_t>(4 * rb * 128);
+#pragma unroll
+      for (int i = 0; i < kStageSlots; ++i)
+        if (i < ppr) st_shared_v4(base + static_cast<uint32_t>(i) * step, b[i]);
+      return;
+    }
+  }
   // one factor when 2^sh is a normal float, else two steps
   const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
   const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
@@ -490,32 +533,44 @@ template <typename T>
 __device__ __forceinline__ void stage_row_pair(const uint4 (&b0)[kStageSlots],
                                                const uint4 (&b1)[kStageSlots], int n0, int n1,
                                                int nr, int rb, int ppr, uint32_t xs, int* sig,
-                                               float* rms, int klen, int lane) {
-  float m0, s0, m1 = 0.0f, s1 = 0.0f;
+                                               float* rms, int klen, int lane, bool raw) {
   const bool has1 = n1 < rb;
-  stage_row_stats<T>(b0, ppr, rms != nullptr, m0, s0);
-  if (has1) stage_row_stats<T>(b1, ppr, rms != nullptr, m1, s1);
+  const bool want_sq = sizeof(T) == 2 && rms != nullptr;
+  float s0, s1 = 0.0f;
+  float m0 = stage_row_max<T>(b0, ppr, want_sq, s0);
+  float m1 = has1 ? stage_row_max<T>(b1, ppr, want_sq, s1) : 0.0f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
     m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-    if (rms) {
+    if (want_sq) {
       s0 += __shfl_xor_sync(0xffffffffu, s0, o);
       s1 += __shfl_xor_sync(0xffffffffu, s1, o);
     }
   }
+  // the FP16 shift of each row (a BF16 operand keeps its rows unshifted;
+  // the RMS factors below still use the shift a row would have)
   const int sh0 = n0 < nr ? f16_row_shift(m0) : 0;
   const int sh1 = n1 < nr ? f16_row_shift(m1) : 0;
-  if (lane == 0) {
-    sig[n0] = sh0;
-    if (rms && n0 < nr) rms[n0] = rsqrtf(s0 / static_cast<float>(klen) + 1e-6f);
-    if (has1) {
-      sig[n1] = sh1;
-      if (rms && n1 < nr) rms[n1] = rsqrtf(s1 / static_cast<float>(klen) + 1e-6f);
+  if constexpr (sizeof(T) == 2) {
+    if (want_sq) {
+      // the plain sum of squares cannot overflow below kSumsqSafeMax; a row
+      // above it (warp-uniform, rare) sums its shifted squares instead
+      if (m0 > kSumsqSafeMax) s0 = warp_sum(stage_row_sumsq(b0, ppr, sh0));
+      if (has1 && m1 > kSumsqSafeMax) s1 = warp_sum(stage_row_sumsq(b1, ppr, sh1));
+      if (lane == 0) {
+        if (n0 < nr) rms[n0] = m0 > kSumsqSafeMax ? rms_factor(s0, sh0, klen) : rms_plain(s0, klen);
+        if (has1 && n1 < nr)
+          rms[n1] = m1 > kSumsqSafeMax ? rms_factor(s1, sh1, klen) : rms_plain(s1, klen);
+      }
     }
   }
-  stage_row_store<T>(b0, n0, rb, ppr, sh0, xs, lane);
-  if (has1) stage_row_store<T>(b1, n1, rb, ppr, sh1, xs, lane);
+  if (lane == 0) {
+    sig[n0] = raw ? 0 : sh0;
+    if (has1) sig[n1] = raw ? 0 : sh1;
+  }
+  stage_row_store<T>(b0, n0, rb, ppr, sh0, xs, lane, raw);
+  if (has1) stage_row_store<T>(b1, n1, rb, ppr, sh1, xs, lane, raw);
 }
 
 // Activations staged through registers in one pass: BF16 (dense A, MoE x)
@@ -529,7 +584,8 @@ __device__ __forceinline__ void stage_row_pair(const uint4 (&b0)[kStageSlots],
 // warps; klen / 256 * (4 / sizeof(T)) <= kStageSlots.
 template <typename T, typename RowFn>
 __device__ __forceinline__ void stage_rows(RowFn rowp, int nr, int rb, int kbeg, int klen,
-                                           uint32_t xs, int* sig, float* rms, int ew, int lane) {
+                                           uint32_t xs, int* sig, float* rms, int ew, int lane,
+                                           bool raw = false) {
   constexpr int kLd = sizeof(T) == 2 ? 1 : 2;
   const int ppr = (klen >> 8) * kLd;  // loads per lane per row
   if (ppr * 2 <= kStageSlots) {
@@ -538,13 +594,13 @@ __device__ __forceinline__ void stage_rows(RowFn rowp, int nr, int rb, int kbeg,
       const int n1 = n + kEpiWarps;
       stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
       stage_row_load<T>(rowp(n1 < nr ? n1 : 0), n1, nr, kbeg, ppr, lane, b1);
-      stage_row_pair<T>(b0, b1, n, n1, nr, rb, ppr, xs, sig, rms, klen, lane);
+      stage_row_pair<T>(b0, b1, n, n1, nr, rb, ppr, xs, sig, rms, klen, lane, raw);
     }
   } else {
     for (int n = ew; n < rb; n += kEpiWarps) {
       uint4 b0[kStageSlots];
       stage_row_load<T>(rowp(n < nr ? n : 0), n, nr, kbeg, ppr, lane, b0);
-      stage_row_pair<T>(b0, b0, n, rb, nr, rb, ppr, xs, sig, rms, klen, lane);
+      stage_row_pair<T>(b0, b0, n, rb, nr, rb, ppr, xs, sig, rms, klen, lane, raw);
     }
   }
 }
@@ -570,7 +626,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   if (u0 < u1 && tc::elect_one()) {
-    const int nm = MODE == kTcDense ? 2 : 4;
+    const int nm = MODE == kTcDense ? (a.fmt == kFmtNvfp4 ? 2 : 1) : 4;
     for (int m = 0; m < nm; ++m) {
       if (table) acquire_tensormap(&op.maps[m]);
       prefetch_tensormap(&op.maps[m]);
@@ -586,6 +642,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
   volatile int* const abort_flag = c.abort_flag();
   uint32_t* const status = c.status();
   const int nkb = wk.nkb;
+  const int fmt = MODE == kTcDense ? a.fmt : kFmtNvfp4;
   int tile = u0 < u1 ? static_cast<int>(u0 / nkb) : 0;
   int kb = u0 < u1 ? static_cast<int>(u0 - static_cast<long>(tile) * nkb) : 0;
   int cur_tile = -1;
@@ -600,13 +657,19 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
     if (tc::elect_one()) {
       const uint32_t full = full_u + 8u * stage;
-      mbar_arrive_expect_tx_u32(full, kTcStageBytes);
       const uint32_t st = ring_u + static_cast<uint32_t>(stage) * kTcStageBytes;
-      if (MODE == kTcGateUp) {
+      if (MODE == kTcDense && fmt != kFmtNvfp4) {
+        // one 128 x 128-byte box: 128 K of E4M3 bytes or 64 K of BF16
+        // (the x coordinate counts elements of the map's type)
+        mbar_arrive_expect_tx_u32(full, kCodeBytes);
+        tma_load_2d_u32(st, bx[0].mc, kb * (fmt == kFmtFp8 ? 128 : 64), bx[0].row, full, pol);
+      } else if (MODE == kTcGateUp) {
+        mbar_arrive_expect_tx_u32(full, kTcStageBytes);
         tma_load_4d_u32(st, bx[0].mc, kb * (kSK / 2), bx[0].row, 0, bx[0].expert, full, pol);
         tma_load_4d_u32(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, 0, bx[0].expert, full,
                         pol);
       } else {
+        mbar_arrive_expect_tx_u32(full, kTcStageBytes);
         tma_load_2d_u32(st, bx[0].mc, kb * (kSK / 2), bx[0].row, full, pol);
         tma_load_2d_u32(st + kCodeBytes, bx[0].ms, kb * (kSK / 16), bx[0].row, full, pol);
       }
@@ -626,12 +689,16 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
 }
 
 // The MMA warp, one op.  The warp stays converged: lane 0 waits on the
-// barriers, then one elected lane issues the stage's 16 MMAs and the commits
+// barriers, then one elected lane issues the stage's MMAs and the commits
 // (a tcgen05.mma issued from a divergent single-lane loop is several times
-// slower).
+// slower).  NVFP4 and FP8 units take A from a tensor-memory buffer the
+// decode warps filled; BF16 units take A straight from the ring slot (the
+// MMA then frees the slot: one commit per decode-warp arrival the slot's
+// barrier counts).  The warp follows the ring position of every unit.
 template <int MODE>
 __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor& cur, int lane,
-                                       uint32_t& acount, uint32_t& dcount, uint32_t& xcount) {
+                                       uint32_t& acount, uint32_t& dcount, uint32_t& xcount,
+                                       int& rstage, uint32_t& rphase) {
   const TcArgs& a = op.a;
   Sched sc{};
   if (MODE != kTcDense) sc = cur.acquire(c, op);
@@ -640,6 +707,10 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   XState xst;
   const uint32_t xs_addr = smem_u32(c.xs());
+  const int uk = kk.uk();
+  const bool a_smem = MODE == kTcDense && a.fmt == kFmtBf16;
+  const uint32_t ring_u = smem_u32(c.ring());
+  const int n_stages = c.n_stages();
   for (long u = u0; u < u1;) {
     if (__any_sync(0xffffffffu, c.aborted())) break;
     const int tile = static_cast<int>(u / wk.nkb);
@@ -647,7 +718,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
-    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, false);
+    const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, a_smem);
     const int rb = tc_xrows(nr);
     const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
     const bool one_tile = u1 <= static_cast<long>(tile + 1) * wk.nkb;
@@ -666,29 +737,64 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
       const uint32_t d_t = c.tmem + kDCol + 32u * db;
       for (int kb = w0; kb < w1; ++kb) {
         const uint32_t ab = acount % kABufs;
-        if (lane == 0) wait_bar(c.a_full_at(ab), (acount / kABufs) & 1u, c.status(), c.abort_flag());
+        const uint32_t rslot = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
+        if (lane == 0) {
+          if (a_smem)
+            wait_bar(c.ring_full_at(rstage), rphase, c.status(), c.abort_flag());
+          else
+            wait_bar(c.a_full_at(ab), (acount / kABufs) & 1u, c.status(), c.abort_flag());
+        }
         __syncwarp();
         tc::fence_after_sync();
         const bool run = !__any_sync(0xffffffffu, c.aborted());
         if (tc::elect_one()) {
           if (run) {
-            const uint32_t a_t = c.tmem + kACols * ab;
-            // stage kb = four 64-element K-blocks of rb rows; K step j: A
-            // columns + 8 j, B block j / 4 at + 32 (j % 4) bytes (descriptor
-            // address field in 16-byte units; no carry: < 256 KB)
+            // unit kb = uk / 64 K-blocks of 64 elements of rb staged rows;
+            // K step j of 16: A columns + 8 j (tensor memory) or + 32 j bytes
+            // (shared memory), B block j / 4 at + 32 (j % 4) bytes
+            // (descriptor address field in 16-byte units; no carry: < 256 KB)
             const uint64_t b0 = tc::smem_desc_sw128(
-                xs_addr + static_cast<uint32_t>((kb - xst.k0) * 4 * rb * 128), sbo);
+                xs_addr + static_cast<uint32_t>((kb - xst.k0) * (uk / 64) * rb * 128), sbo);
             const uint32_t blk = static_cast<uint32_t>(rb * 128 / 16);
-            tc::mma_f16_ts(d_t, a_t, b0, idesc, kb > w0 ? 1u : 0u);
+            // (fixed trip counts: the issue loops stay unrolled)
+            if (a_smem) {  // BF16: 64 K a unit
+              const uint64_t a0 = tc::smem_desc_sw128(rslot, 1024u);
+              tc::mma_f16_ss(d_t, a0, b0, idesc, kb > w0 ? 1u : 0u);
 #pragma unroll
-            for (int j = 1; j < kSK / 16; ++j)
-              tc::mma_f16_ts(d_t, a_t + 8 * j, b0 + static_cast<uint64_t>((j >> 2) * blk + 2 * (j & 3)),
-                             idesc, 1u);
+              for (int j = 1; j < 4; ++j)
+                tc::mma_f16_ss(d_t, a0 + static_cast<uint64_t>(2 * j),
+                               b0 + static_cast<uint64_t>(2 * j), idesc, 1u);
+            } else {
+              const uint32_t a_t = c.tmem + kACols * ab;
+              tc::mma_f16_ts(d_t, a_t, b0, idesc, kb > w0 ? 1u : 0u);
+              if (uk == kSK) {  // NVFP4: 256 K a unit
+#pragma unroll
+                for (int j = 1; j < kSK / 16; ++j)
+                  tc::mma_f16_ts(d_t, a_t + 8 * j,
+                                 b0 + static_cast<uint64_t>((j >> 2) * blk + 2 * (j & 3)), idesc,
+                                 1u);
+              } else {  // FP8: 128 K a unit
+#pragma unroll
+                for (int j = 1; j < 8; ++j)
+                  tc::mma_f16_ts(d_t, a_t + 8 * j,
+                                 b0 + static_cast<uint64_t>((j >> 2) * blk + 2 * (j & 3)), idesc,
+                                 1u);
+              }
+            }
           }
-          tc::commit(c.a_empty_at(ab));
+          if (a_smem) {
+#pragma unroll
+            for (int i = 0; i < kDecWarps; ++i) tc::commit(c.ring_empty_at(rstage));
+          } else {
+            tc::commit(c.a_empty_at(ab));
+          }
         }
         __syncwarp();
-        ++acount;
+        if (!a_smem) ++acount;
+        if (++rstage == n_stages) {
+          rstage = 0;
+          rphase ^= 1u;
+        }
       }
       if (tc::elect_one()) tc::commit(c.d_full_at(db));
       __syncwarp();
@@ -708,8 +814,21 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   if (MODE != kTcDense) sc = cur.acquire(c, op);
   long u0, u1;
   make_work<MODE>(op.a, sc, c, u0, u1);
+  const int fmt = MODE == kTcDense ? op.a.fmt : kFmtNvfp4;
+  if (fmt == kFmtBf16) {
+    // the MMA reads BF16 weights from the ring itself: only follow the ring
+    const long n = u1 > u0 ? u1 - u0 : 0;
+    rstage += static_cast<int>(n % c.n_stages());
+    rphase ^= static_cast<uint32_t>((n / c.n_stages()) & 1);
+    if (rstage >= c.n_stages()) {
+      rstage -= c.n_stages();
+      rphase ^= 1u;
+    }
+    return;
+  }
   // warp dw decodes lane quarter q (tile rows 32q .. 32q + 31), chunks
-  // [c0, c0 + kDecChunks) of 32 K each (8 chunks per 256-K stage)
+  // [c0, c0 + kDecChunks) of the stage's 8 16-byte chunks of a row (NVFP4:
+  // 32 K each; FP8: 16 K each)
   const int dw = warp - kDecWarp0, q = warp & 3, c0 = (dw >> 2) * kDecChunks;
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
   // loop constants in registers (shared-memory addresses as 32-bit values)
@@ -736,6 +855,32 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   for (long u = u0; u < u1; ++u) {
     if (!wait_u32(rfull_u + 8u * rstage, rphase, status, abort_flag)) break;
     const uint32_t st = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
+    if (MODE == kTcDense && fmt == kFmtFp8) {
+      // E4M3 -> FP16 (hardware convert, exact); the matrix's one scale is
+      // applied to the accumulator
+      uint4 cw[kDecChunks];
+#pragma unroll
+      for (int ci = 0; ci < kDecChunks; ++ci) cw[ci] = ld_shared_v4(st + chunk_off[ci]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_u32(rempty_u + 8u * rstage);
+      if (!wait_u32(aempty_u + 8u * ab, aph ^ 1u, status, abort_flag)) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int ci = 0; ci < kDecChunks; ++ci) {
+        const uint32_t wds[4] = {cw[ci].x, cw[ci].y, cw[ci].z, cw[ci].w};
+        uint32_t v[8];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) e4m3x4_to_f16x2(wds[wi], v[2 * wi], v[2 * wi + 1]);
+        if (ci == 0 && pend >= 0) {
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_u32(afull_u + 8u * static_cast<uint32_t>(pend));
+          pend = -1;
+        }
+        tc::st_x8(lane_addr + kACols * ab + 8 * (c0 + ci), v);
+      }
+    } else {
     // all shared-memory reads of this stage first (their latency overlaps)
     uint32_t sbw[kDecChunks / 2];
     if (kDecChunks == 8) {
@@ -781,6 +926,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
         pend = -1;
       }
       tc::st_x16(lane_addr + kACols * ab + 16 * (c0 + ci), v);
+    }
     }
     pend = static_cast<int>(ab);
     ++acount;
@@ -828,7 +974,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   int g_expert = -1;
   float g_tile = 0.0f;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
-  const float gs = (MODE == kTcDense) ? *a.gscale : 0.0f;
+  // the matrix's scale (NVFP4 per-tensor scale, FP8 scale; BF16: none)
+  const float gs = (MODE == kTcDense) ? (a.gscale ? *a.gscale : 1.0f) : 0.0f;
   // dense argmax: lane i of epilogue warp ew keeps the running best of row
   // m = ew + kEpiWarps i over the CTA's finished tiles
   float am_v = -FLT_MAX;
@@ -869,23 +1016,28 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         restage_range(kk, w0, w1, one_tile, xst.k0, xst.k1);
         xst.key = key;
         // the previous window's MMAs are complete (its accumulator was read)
-        const int kbeg = xst.k0 * kSK, klen = (xst.k1 - xst.k0) * kSK;
+        const int kbeg = xst.k0 * kk.uk(), klen = (xst.k1 - xst.k0) * kk.uk();
         if (MODE == kTcDown) {
           const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
           const int I = a.I;
           stage_rows<float>([&](int n) { return hbase + static_cast<size_t>(n) * I; }, nr, rb,
                             kbeg, klen, smem_u32(c.xs()), sig, nullptr, ew, lane);
         } else {
-          // gate_up: the RMS factors from the staged rows (its K is always
-          // staged whole).  Dense ops take them from global memory below, in
-          // every CTA the same way: the CTA that finishes a split tile applies
-          // its own factor, so all CTAs must compute it bit for bit alike.
-          const bool stage_rms = MODE == kTcGateUp && a.rms && !rms_ready;
+          // The RMS factors from the staged rows when the window is the whole
+          // K (gate_up: always).  Otherwise dense ops take them from global
+          // memory below.  The CTA that finishes a split tile applies its own
+          // factor, so every CTA must compute it bit for bit alike: both ways
+          // sum the same 16-byte chunks per lane in the same order (high half
+          // of each word first) and reduce across the warp by the same
+          // butterfly.
+          const bool stage_rms =
+              a.rms && !rms_ready && (MODE == kTcGateUp || (kbeg == 0 && klen == a.K));
           rms_ready = rms_ready || stage_rms;
           const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
           const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
           stage_rows<__nv_bfloat16>([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen,
-                                    smem_u32(c.xs()), sig, stage_rms ? rms : nullptr, ew, lane);
+                                    smem_u32(c.xs()), sig, stage_rms ? rms : nullptr, ew, lane,
+                                    MODE == kTcDense && a.fmt == kFmtBf16);
         }
         fence_proxy_async_smem();
         esync();
@@ -895,14 +1047,18 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         // memory, while the MMAs run
         if (MODE == kTcDense && a.rms && !rms_ready) {
           for (int m = ew; m < a.M; m += kEpiWarps) {
-            float ss = 0.0f;
             const __nv_bfloat16* row = a.A + m * a.lda;
+            // the row's largest magnitude and plain sum of squares in one
+            // pass; a row above kSumsqSafeMax (rare) sums its squares again,
+            // shifted by its staging shift (no overflow at any magnitude)
+            uint32_t mx = 0u;
+            float ss = 0.0f;
             for (int v0 = 0; v0 < a.K / 8; v0 += 8 * 32) {
               uint4 buf[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const int v = v0 + 32 * i + lane;
-                buf[i] = v < a.K / 8 ? *reinterpret_cast<const uint4*>(row + v * 8)
+                buf[i] = v < a.K / 8 ? __ldcg(reinterpret_cast<const uint4*>(row + v * 8))
                                      : make_uint4(0u, 0u, 0u, 0u);
               }
 #pragma unroll
@@ -910,14 +1066,32 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
                 const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                  mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);
                   const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-                  ss = fmaf(lo, lo, ss);
-                  ss = fmaf(hi, hi, ss);
+                  ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                }
+              }
+            }
+            const float mrow =
+                warp_max(fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u)));
+            const int sh = f16_row_shift(mrow);
+            if (mrow > kSumsqSafeMax) {
+              const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+              const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+              ss = 0.0f;
+              for (int v = lane; v < a.K / 8; v += 32) {
+                const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + v * 8));
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+                  const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+                  ss = fmaf(lo, lo, fmaf(hi, hi, ss));
                 }
               }
             }
             ss = warp_sum(ss);
-            if (lane == 0) rms[m] = rsqrtf(ss / static_cast<float>(a.K) + 1e-6f);
+            if (lane == 0) rms[m] = mrow > kSumsqSafeMax ? rms_factor(ss, sh, a.K) : rms_plain(ss, a.K);
           }
           rms_ready = true;
           esync();
@@ -1170,13 +1344,15 @@ __device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& 
 __device__ __forceinline__ void mma_role(const TcProgram& prog, const Cta& c, int lane) {
   SchedCursor cur;
   uint32_t acount = 0, dcount = 0, xcount = 0;
+  int rstage = 0;
+  uint32_t rphase = 0;
   for (int i = 0; i < prog.n_ops; ++i) {
     if (__any_sync(0xffffffffu, c.aborted())) break;
     const TcOp& op = op_at(prog, i);
     switch (op.mode) {
-      case kTcDense: mma_op<kTcDense>(c, op, cur, lane, acount, dcount, xcount); break;
-      case kTcGateUp: mma_op<kTcGateUp>(c, op, cur, lane, acount, dcount, xcount); break;
-      case kTcDown: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount); break;
+      case kTcDense: mma_op<kTcDense>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
+      case kTcGateUp: mma_op<kTcGateUp>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
+      case kTcDown: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
       default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
     }
   }
@@ -1352,12 +1528,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 cudaError_t launch_tc(const TcProgram& p, int grid, size_t smem, cudaStream_t s, bool pdl,
                       bool cooperative) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(stream_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+  // The shared-memory opt-in is a per-device attribute of the kernel: set it
+  // once per device, under a lock (several host threads may make their first
+  // call at once).
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static bool attr_set[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(stream_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               232448);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
   }
   // One CTA per SM: each CTA allocates all 512 tensor-memory columns, so a
   // second resident CTA would only queue on the allocation.

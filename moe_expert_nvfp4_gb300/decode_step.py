@@ -129,8 +129,9 @@ class DecodeStep:
         return launches
 
     # ------------------------------------------------------------ as a program
-    def program_ops(self, b: dict) -> list:
-        """The step's projections, MoE layers and head as one op chain."""
+    def program_ops(self, b: dict, all_sms: bool = False) -> list:
+        """The step's projections, MoE layers and head as one op chain
+        (all_sms: every op split over every SM, as the single calls)."""
         s, T = self.s, b["T"]
         chain = []
         x = b["x"]
@@ -138,17 +139,18 @@ class DecodeStep:
             i = l if b["keep"] else 0
             q, o = b["q"][i], b["o"][i]
             y = b["y"][l if b["keep"] else l % 2]
-            chain.append(ops.gemm_op(x, self.qkv[l], q, rms_input=True))
-            chain.append(ops.gemm_op(q[:, :s.o_in], self.o[l], o, rms_input=True))
+            chain.append(ops.gemm_op(x, self.qkv[l], q, rms_input=True, all_sms=all_sms))
+            chain.append(ops.gemm_op(q[:, :s.o_in], self.o[l], o, rms_input=True, all_sms=all_sms))
             chain.append(ops.moe_op(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T],
                                     self.experts[l], y, shared=self.shared[l], rms_input=True))
             x = y
-        chain.append(ops.gemm_op(x, self.head, b["head"], argmax_out=b["argmax"], rms_input=True))
+        chain.append(ops.gemm_op(x, self.head, b["head"], argmax_out=b["argmax"], rms_input=True,
+                                 all_sms=all_sms))
         return chain
 
-    def program(self, b: dict) -> "ops.Program":
+    def program(self, b: dict, all_sms: bool = False) -> "ops.Program":
         """Create the step's program on the buffers ``b`` (once)."""
-        chain = self.program_ops(b)
+        chain = self.program_ops(b, all_sms)
         need = ops.program_workspace_bytes(chain)
         if b["ws"].nbytes < need:
             b["ws"] = ops.Workspace(need, self.device)

@@ -25,7 +25,7 @@ ERRORS = {-1: "invalid argument", -2: "misaligned", -3: "unsupported shape",
 FLAG_RMS_INPUT = 1
 FLAG_NO_PDL = 2
 FLAG_IDS_READY = 4
-FLAG_WARP_MMA = 8
+FLAG_ALL_SMS = 8
 STATUS_BAD_EXPERT_ID = 1
 STATUS_WAIT_TIMEOUT = 2
 
@@ -33,6 +33,16 @@ STATUS_WAIT_TIMEOUT = 2
 class _Weight(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("global_scale", ctypes.c_void_p), ("n", ctypes.c_int32), ("k", ctypes.c_int32)]
+
+
+class _Fp8Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("n", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
+
+
+class _Bf16Weight(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("ldw", ctypes.c_int64), ("n", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
 
 
 class _Stack(ctypes.Structure):
@@ -81,6 +91,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_gemm_skinny_workspace.argtypes = [i32, i32, i32]
     L.nvfp4_gemm_skinny_workspace.restype = sz
     L.nvfp4_gemm_skinny.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, i64, vp, u32, vp, sz, vp]
+    L.fp8_gemm_skinny_workspace.argtypes = [i32, i32, i32]
+    L.fp8_gemm_skinny_workspace.restype = sz
+    L.fp8_gemm_skinny.argtypes = [vp, i64, i32, ctypes.POINTER(_Fp8Weight), vp, i64, vp, u32, vp,
+                                  sz, vp]
+    L.bf16w_gemm_skinny_workspace.argtypes = [i32, i32, i32]
+    L.bf16w_gemm_skinny_workspace.restype = sz
+    L.bf16w_gemm_skinny.argtypes = [vp, i64, i32, ctypes.POINTER(_Bf16Weight), vp, i64, vp, u32,
+                                    vp, sz, vp]
     L.nvfp4_hot_vocab_head.argtypes = [vp, i64, i32, ctypes.POINTER(_Weight), vp, vp, i64, vp, u32,
                                        vp, sz, vp]
     L.nvfp4_gather_rows.argtypes = [ctypes.POINTER(_Weight), vp, i32, vp, vp, vp]
@@ -97,6 +115,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.nvfp4_program_destroy.argtypes = [vp]
     L.nvfp4_read_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
     L.nvfp4_last_dispatch.argtypes = [ctypes.c_char_p, sz]
+    L.nvfp4_hbm_read_probe.argtypes = [vp, sz, vp, sz, vp]
     L.nvfp4_last_error.restype = ctypes.c_char_p
     for name in declared_functions():
         getattr(L, name)  # every declared symbol must resolve
@@ -222,12 +241,10 @@ def device_check(device: int = 0) -> int:
 
 def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
          argmax: bool = False, rms_input: bool = False, workspace: Optional[Workspace] = None,
-         pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None,
-         warp_mma: bool = False):
+         pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None):
     """C = A W^T for BF16 A [M, >=K] (row stride a.stride(0)).  Returns C
     (BF16 [M, N]) and, with argmax=True (or an int32 [M] ``argmax_out``),
-    also the row argmaxes.  warp_mma: use the warp-level MMA kernel instead
-    of the tcgen05 one."""
+    also the row argmaxes."""
     L = load()
     m = a.shape[0]
     if out is None:
@@ -238,13 +255,81 @@ def gemm(a: torch.Tensor, w: NVFP4Weight, out: Optional[torch.Tensor] = None,
         ids = torch.empty(m, dtype=torch.int32, device=a.device)
     if workspace is None:
         workspace = Workspace(gemm_workspace_bytes(m, w.n, w.k), a.device)
-    flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
-             | (FLAG_WARP_MMA if warp_mma else 0))
+    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
     wc = w.c()
     _check(L.nvfp4_gemm_skinny(a.data_ptr(), a.stride(0), m, ctypes.byref(wc), out.data_ptr(),
                                out.stride(0), _ptr(ids), flags, workspace.ptr(), workspace.nbytes,
                                _stream(stream)), "nvfp4_gemm_skinny")
     return (out, ids) if argmax else out
+
+
+@dataclass
+class FP8Weight:
+    """An FP8-E4M3 matrix [n, k] on the device: codes uint8 [n, k], scale
+    float32 [1] (one scale for the matrix)."""
+    codes: torch.Tensor
+    scale: torch.Tensor
+
+    @property
+    def n(self) -> int:
+        return self.codes.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.codes.shape[1]
+
+    def c(self) -> _Fp8Weight:
+        assert self.codes.dtype == torch.uint8 and self.codes.is_contiguous()
+        return _Fp8Weight(self.codes.data_ptr(), self.scale.data_ptr(), self.n, self.k)
+
+
+def _dense_call(fn, wsfn, name, a, wc, n, k, out, argmax, argmax_out, rms_input, workspace, pdl,
+                stream):
+    L = load()
+    m = a.shape[0]
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=a.device)
+    argmax = argmax or argmax_out is not None
+    ids = argmax_out
+    if argmax and ids is None:
+        ids = torch.empty(m, dtype=torch.int32, device=a.device)
+    if workspace is None:
+        workspace = Workspace(int(wsfn(m, n, k)), a.device)
+    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
+    _check(fn(a.data_ptr(), a.stride(0), m, ctypes.byref(wc), out.data_ptr(), out.stride(0),
+              _ptr(ids), flags, workspace.ptr(), workspace.nbytes, _stream(stream)), name)
+    return (out, ids) if argmax else out
+
+
+def fp8_gemm(a: torch.Tensor, w: FP8Weight, out: Optional[torch.Tensor] = None,
+             argmax: bool = False, rms_input: bool = False, workspace: Optional[Workspace] = None,
+             pdl: bool = True, stream=None, argmax_out: Optional[torch.Tensor] = None):
+    """C = scale * A e4m3(W)^T for BF16 A [M, >=K] (as gemm())."""
+    L = load()
+    return _dense_call(L.fp8_gemm_skinny, L.fp8_gemm_skinny_workspace, "fp8_gemm_skinny", a,
+                       w.c(), w.n, w.k, out, argmax, argmax_out, rms_input, workspace, pdl, stream)
+
+
+def bf16w_gemm(a: torch.Tensor, w: torch.Tensor, out: Optional[torch.Tensor] = None,
+               argmax: bool = False, rms_input: bool = False,
+               workspace: Optional[Workspace] = None, pdl: bool = True, stream=None,
+               argmax_out: Optional[torch.Tensor] = None):
+    """C = A W^T for BF16 A [M, >=K] and BF16 weights W [N, K] (row stride
+    w.stride(0)) (as gemm())."""
+    L = load()
+    assert w.dtype == torch.bfloat16 and w.stride(1) == 1
+    wc = _Bf16Weight(w.data_ptr(), w.stride(0), w.shape[0], w.shape[1])
+    return _dense_call(L.bf16w_gemm_skinny, L.bf16w_gemm_skinny_workspace, "bf16w_gemm_skinny", a,
+                       wc, w.shape[0], w.shape[1], out, argmax, argmax_out, rms_input, workspace,
+                       pdl, stream)
+
+
+def hbm_read_probe(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Read ``buf`` (device, 16-byte aligned, size a multiple of 16) once with
+    the library's read-only probe kernel; ``sink`` receives one word per CTA."""
+    _check(load().nvfp4_hbm_read_probe(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                       sink.data_ptr(), sink.numel() * sink.element_size(),
+                                       _stream(stream)), "nvfp4_hbm_read_probe")
 
 
 def quantize(w: torch.Tensor, stream=None) -> NVFP4Weight:
@@ -278,7 +363,7 @@ def gather_rows(w: NVFP4Weight, rows: torch.Tensor, stream=None) -> NVFP4Weight:
 def hot_vocab_head(a: torch.Tensor, w_hot: NVFP4Weight, vocab_ids: torch.Tensor,
                    out: Optional[torch.Tensor] = None, argmax_out: Optional[torch.Tensor] = None,
                    rms_input: bool = False, workspace: Optional[Workspace] = None,
-                   pdl: bool = True, stream=None, warp_mma: bool = False):
+                   pdl: bool = True, stream=None):
     """Greedy draft token through a hot-vocabulary head: the hot rows' BF16
     logits C = A W_hot^T [M, n_hot] and the vocabulary id of each row's
     first maximum, vocab_ids[argmax] (int32 [M])."""
@@ -292,8 +377,7 @@ def hot_vocab_head(a: torch.Tensor, w_hot: NVFP4Weight, vocab_ids: torch.Tensor,
         argmax_out = torch.empty(m, dtype=torch.int32, device=a.device)
     if workspace is None:
         workspace = Workspace(gemm_workspace_bytes(m, w_hot.n, w_hot.k), a.device)
-    flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
-             | (FLAG_WARP_MMA if warp_mma else 0))
+    flags = (FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
     wc = w_hot.c()
     _check(L.nvfp4_hot_vocab_head(a.data_ptr(), a.stride(0), m, ctypes.byref(wc),
                                   vocab_ids.data_ptr(), out.data_ptr(), out.stride(0),
@@ -322,10 +406,9 @@ def route(logits: torch.Tensor, k: int, renormalize: bool = True,
 def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
         shared: Optional[ExpertStack] = None, out: Optional[torch.Tensor] = None,
         rms_input: bool = False, workspace: Optional[Workspace] = None, pdl: bool = True,
-        stream=None, ids_ready: bool = False, warp_mma: bool = False) -> torch.Tensor:
+        stream=None, ids_ready: bool = False) -> torch.Tensor:
     """MoE decode layer: BF16 x [T, >=H] -> BF16 out [T, H].  ids_ready: the
-    ids/weights were complete before the previous kernel started.  warp_mma:
-    use the warp-level MMA kernels instead of the tcgen05 ones."""
+    ids/weights were complete before the previous kernel started."""
     L = load()
     t, k = ids.shape
     assert ids.is_contiguous() and weights.is_contiguous()
@@ -334,7 +417,7 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
     if workspace is None:
         workspace = Workspace(moe_workspace_bytes(t, k, experts), x.device)
     flags = ((FLAG_RMS_INPUT if rms_input else 0) | (0 if pdl else FLAG_NO_PDL)
-             | (FLAG_IDS_READY if ids_ready else 0) | (FLAG_WARP_MMA if warp_mma else 0))
+             | (FLAG_IDS_READY if ids_ready else 0))
     ec = experts.c()
     sc = shared.c() if shared is not None else None
     _check(L.moe_nvfp4_decode(x.data_ptr(), x.stride(0), t, ids.data_ptr(), weights.data_ptr(), k,
@@ -348,13 +431,14 @@ def moe(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: Expe
 
 def gemm_op(a: torch.Tensor, w: NVFP4Weight, out: torch.Tensor,
             argmax_out: Optional[torch.Tensor] = None, rms_input: bool = False,
-            argmax_map: Optional[torch.Tensor] = None) -> dict:
+            argmax_map: Optional[torch.Tensor] = None, all_sms: bool = False) -> dict:
     """One GEMM of a program: out = A W^T (as gemm()); with argmax_map (the
     vocabulary ids of a hot-vocabulary head, as hot_vocab_head()) argmax_out
-    reports argmax_map[argmax]."""
+    reports argmax_map[argmax].  all_sms: split the op over every SM exactly
+    as the single call does (bit-identical results to it)."""
     assert argmax_map is None or (argmax_map.dtype == torch.int32 and argmax_map.is_contiguous())
     return dict(kind=OP_GEMM, a=a, w=w, out=out, argmax_out=argmax_out, rms_input=rms_input,
-                argmax_map=argmax_map)
+                argmax_map=argmax_map, all_sms=all_sms)
 
 
 def moe_op(x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, experts: ExpertStack,
@@ -371,7 +455,8 @@ def _c_ops(ops: list) -> ctypes.Array:
     for i, o in enumerate(ops):
         c = arr[i]
         c.kind = o["kind"]
-        c.flags = FLAG_RMS_INPUT if o.get("rms_input") else 0
+        c.flags = ((FLAG_RMS_INPUT if o.get("rms_input") else 0)
+                   | (FLAG_ALL_SMS if o.get("all_sms") else 0))
         if o["kind"] == OP_GEMM:
             a, out = o["a"], o["out"]
             c.A, c.lda, c.M = a.data_ptr(), a.stride(0), a.shape[0]

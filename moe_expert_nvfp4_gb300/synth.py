@@ -163,6 +163,27 @@ def nvfp4_weight(seed: int, n: int, k: int, *ids: int, row_lo: int = 0,
             nvfp4_scales(sk, n, k, row_lo, row_hi, device))
 
 
+# ----------------------------------------------------------------- FP8 / BF16 weights
+
+ROLE_FP8 = 13
+ROLE_BF16W = 14
+FP8_SCALE = 1.0 / 64.0
+
+
+def fp8_weight(seed: int, n: int, k: int, *ids: int) -> torch.Tensor:
+    """uint8 [n, k] FP8-E4M3 ("fn") bytes of N(0, 1) * 8 draws, rounded to
+    nearest by torch's float8_e4m3fn conversion (no NaN: |x| < 448 for every
+    draw the generator can make); the matrix's one scale is FP8_SCALE."""
+    z = normal(stream_key(seed, ROLE_FP8, n, k, *ids), n * k) * 8.0
+    return z.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).view(n, k)
+
+
+def bf16_weight(seed: int, n: int, k: int, *ids: int) -> torch.Tensor:
+    """BF16 [n, k] weights ~ N(0, 1) / 16 on the host."""
+    z = normal(stream_key(seed, ROLE_BF16W, n, k, *ids), n * k) / 16.0
+    return z.to(torch.float32).to(torch.bfloat16).view(n, k)
+
+
 # ----------------------------------------------------------------- MoE experts
 
 ROLE_GATE_UP = 11

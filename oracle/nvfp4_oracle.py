@@ -43,7 +43,7 @@ __all__ = [
     "expert_ffn64", "moe_decode64", "moe_decode_bf16", "argmax_first",
     "lm_head_argmax", "hot_vocab_head_argmax", "rms_scale", "round_to_e2m1",
     "round_to_e4m3", "nvfp4_quantize", "fp8_gemm64", "fp8_gemm_bf16", "bf16w_gemm64",
-    "bf16w_gemm_bf16", "decode_layer", "nvfp4_weight_bytes",
+    "bf16w_gemm_bf16", "nvfp4_weight_bytes",
     "moe_weight_bytes", "decode_roofline_tok_s", "roofline_share",
     "RMS_EPS",
 ]
@@ -403,23 +403,6 @@ def moe_decode64(x: np.ndarray, ids: np.ndarray, w: np.ndarray,
 def moe_decode_bf16(x, ids, w, experts, num_experts, shared=None) -> np.ndarray:
     """The MoE layer's BF16 output: moe_decode64 rounded once to BF16."""
     return bf16_round(moe_decode64(x, ids, w, experts, num_experts, shared))
-
-
-def decode_layer(x, qkv, o_proj, logits, k, experts, num_experts, shared,
-                 o_in: int):
-    """One layer of the stacked decode step, each op from the given inputs.
-
-    x bf16 values [T, H].  qkv / o_proj = (codes, scales, global).  The RMS
-    glue sits before each projection block; O reads the first ``o_in``
-    columns of the QKV output.  Router logits are an input (drawn per layer).
-    Returns dict of the BF16 outputs q, o, y and the routing (ids, w).  Tests
-    call it op by op with the GPU's own BF16 inputs (teacher forcing).
-    """
-    q = gemm_bf16(rms_scale(x), *qkv)
-    o = gemm_bf16(rms_scale(q[:, :o_in]), *o_proj)
-    ids, w = topk_softmax_route(logits, k)
-    y = moe_decode_bf16(rms_scale(o), ids, w, experts, num_experts, shared)
-    return {"q": q, "o": o, "ids": ids, "w": w, "y": y}
 
 
 # --------------------------------------------------------------------------

@@ -23,7 +23,9 @@ def test_header_declares_the_boundary():
               "nvfp4_gemm_skinny_workspace", "moe_nvfp4_decode_workspace", "nvfp4_device_check",
               "nvfp4_workspace_init", "nvfp4_read_device_status", "nvfp4_last_dispatch",
               "nvfp4_last_error", "nvfp4_gather_rows", "nvfp4_hot_vocab_head", "nvfp4_quantize",
-              "nvfp4_program_create", "nvfp4_program_launch", "nvfp4_gemm_skinny_noalloc"]:
+              "nvfp4_program_create", "nvfp4_program_launch", "nvfp4_gemm_skinny_noalloc",
+              "fp8_gemm_skinny", "fp8_gemm_skinny_workspace", "bf16w_gemm_skinny",
+              "bf16w_gemm_skinny_workspace"]:
         assert n in names
 
 
@@ -49,7 +51,7 @@ def test_gemm_validation_codes(lib):
     assert _gemm(lib, a=0) == -1
     assert _gemm(lib, m=0) == -3
     assert _gemm(lib, m=33) == -3
-    assert _gemm(lib, w=_w(k=2000)) == -3           # K not a multiple of 256
+    assert _gemm(lib, w=_w(k=2000)) == -3           # K not a multiple of 32
     assert _gemm(lib, w=_w(codes=(1 << 20) + 8)) == -2  # misaligned weight
     assert _gemm(lib, a=(1 << 20) + 2) == -2           # misaligned A
     assert _gemm(lib, lda=2052) == -2                  # row stride not 16-byte multiple
@@ -156,3 +158,56 @@ def test_quantize_validation_codes(lib):
     assert call(ldw=2052) == -2     # row stride not a 16-byte multiple
     assert call(codes=p + 8) == -2
     assert call(g=p + 2) == -2      # the float output misaligned
+
+
+def test_fp8_and_bf16_weight_validation_codes(lib):
+    p = 1 << 20
+
+    def fp8(a=p, lda=2048, m=4, codes=p, scale=p, n=64, k=2048, c=p):
+        w = ops._Fp8Weight(codes, scale, n, k)
+        return lib.fp8_gemm_skinny(a, lda, m, ctypes.byref(w), c, 64, None, 0, p, 1 << 30, None)
+
+    assert fp8(codes=0) == -1
+    assert fp8(scale=0) == -1
+    assert fp8(a=0) == -1
+    assert fp8(m=33) == -3
+    assert fp8(k=2000, lda=2000) == -3       # K not a multiple of 256
+    assert fp8(codes=p + 8) == -2
+    assert fp8(a=p + 2) == -2
+    assert lib.fp8_gemm_skinny(p, 2048, 4, None, p, 64, None, 0, p, 1 << 30, None) == -1
+
+    def bf16(a=p, m=4, w=p, ldw=2048, n=64, k=2048):
+        wt = ops._Bf16Weight(w, ldw, n, k)
+        return lib.bf16w_gemm_skinny(a, 2048, m, ctypes.byref(wt), p, 64, None, 0, p, 1 << 30,
+                                     None)
+
+    assert bf16(w=0) == -1
+    assert bf16(m=0) == -3
+    assert bf16(ldw=1024) == -1              # ldw < K
+    assert bf16(ldw=2052) == -2              # row stride not a 16-byte multiple
+    assert bf16(w=p + 2) == -2
+    assert bf16(k=300) == -3
+
+
+def test_noalloc_refuses_before_touching_its_scratch(lib):
+    """A refused call returns the same status as the workspace entry point
+    and issues nothing (no device is needed to see the refusal)."""
+    p = 1 << 20
+    fn = lib.nvfp4_gemm_skinny_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ops._Weight),
+                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint32,
+                   ctypes.c_void_p]
+    w = _w()
+    assert fn(0, 2048, 4, ctypes.byref(w), p, 64, None, 0, None) == -1
+    assert fn(p, 2048, 33, ctypes.byref(w), p, 64, None, 0, None) == -3
+    assert fn(p + 2, 2048, 4, ctypes.byref(w), p, 64, None, 0, None) == -2
+    assert fn(p, 2048, 4, None, p, 64, None, 0, None) == -1
+
+
+def test_gemm_accepts_k_multiple_of_32(lib):
+    """K % 32 == 0 passes the host checks (without a GPU the call then stops
+    at the device query, never at the shape check)."""
+    for k in (32, 96, 2080):
+        rc = _gemm(lib, lda=k, w=_w(k=k))
+        assert rc not in (-1, -2, -3), (k, rc, ops.last_error())
+    assert lib.nvfp4_gemm_skinny_workspace(4, 64, 48) == 0   # K % 32 != 0

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import assert_close, device_weight, f64, host_weight
+from helpers import assert_close, check_argmax, device_weight, f64, host_weight
 from moe_expert_nvfp4_gb300 import ops, synth
 
 pytestmark = pytest.mark.gpu
@@ -20,12 +20,12 @@ def _lib():
     assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
 
 
-def _case(seed, m, n, k, *ids, rms=False, argmax=False, lda=None, warp_mma=False):
+def _case(seed, m, n, k, *ids, rms=False, argmax=False, lda=None):
     W = device_weight(seed, n, k, *ids)
     a_full = synth.activations_bf16(seed, m, lda or k, 900, *ids)
     a = a_full.cuda()[:, :k] if lda else a_full.cuda()
     ws = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
-    res = ops.gemm(a, W, argmax=argmax, rms_input=rms, workspace=ws, warp_mma=warp_mma)
+    res = ops.gemm(a, W, argmax=argmax, rms_input=rms, workspace=ws)
     disp = ops.last_dispatch()
     torch.cuda.synchronize()
     assert ws.status() == 0
@@ -52,13 +52,6 @@ def test_projection_2048_to_64_m4():
 def test_dense_sweep(seed, n, k, m):
     c, ref, disp, _ = _case(seed, m, n, k)
     assert_close(f64(c), O.bf16_round(ref), f"M={m} N={n} K={k}")
-
-
-@pytest.mark.parametrize("m,n,k", [(4, 64, 2048), (8, 4096, 2048), (32, 2048, 4096), (13, 200, 768)])
-def test_warp_mma_path(m, n, k):
-    c, ref, disp, _ = _case(1, m, n, k, warp_mma=True)
-    assert disp.startswith("dense_gemm_kernel")
-    assert_close(f64(c), O.bf16_round(ref), f"warp mma M={m} N={n} K={k}")
 
 
 @pytest.mark.parametrize("m,n,k", [(3, 200, 768), (13, 200, 768), (27, 1000, 256), (1, 64, 256),
@@ -89,27 +82,11 @@ def test_deterministic_split_k():
     assert torch.equal(c1, c2) and torch.equal(c2, c3)
 
 
-def _check_argmax(am, c, ref64):
-    """Bit-exact argmax; the one tolerated exception is a top-1 pair whose
-    float64 logits straddle a BF16 rounding boundary (reported)."""
-    gl = f64(c)
-    ids = am.cpu().numpy()
-    # the fused argmax agrees exactly with the BF16 logits the kernel wrote
-    assert np.array_equal(ids, O.argmax_first(gl, axis=1))
-    ref_ids = O.argmax_first(O.bf16_round(ref64), axis=1)
-    diff = np.nonzero(ids != ref_ids)[0]
-    for r in diff:
-        a, b = ref64[r, ids[r]], ref64[r, ref_ids[r]]
-        ulp = 2.0 ** (np.floor(np.log2(abs(b))) - 7)
-        assert abs(a - b) <= ulp, f"row {r}: argmax {ids[r]} vs {ref_ids[r]}"
-    return len(diff)
-
-
 def test_lm_head_151936_argmax_m32():
     (c, am), ref, disp, _ = _case(5, 32, 151936, 2048, 1, argmax=True)
     assert "argmax=1" in disp and "tiles=1187" in disp
     assert_close(f64(c), O.bf16_round(ref), "lm-head")
-    _check_argmax(am, c, ref)
+    check_argmax(am.cpu().numpy(), f64(c), ref, what="lm-head")
 
 
 def test_argmax_ties_go_to_lowest_index():
@@ -132,3 +109,30 @@ def test_argmax_ties_go_to_lowest_index():
     a1 = torch.ones(2, k, dtype=torch.bfloat16, device="cuda")
     C, am = ops.gemm(a1, W, argmax=True)
     assert am.tolist() == [3, 3]
+
+
+# ------------------------------------------------------------------ K % 256 != 0
+# These shapes run on the CUDA-core kernel (whole rows per warp); the same
+# tolerance and argmax rules hold.
+
+@pytest.mark.parametrize("m", [1, 2, 4, 17, 32])
+@pytest.mark.parametrize("n,k", [(64, 32), (1000, 96), (4096, 2080)])
+def test_k_multiple_of_32(m, n, k):
+    c, ref, disp, _ = _case(15, m, n, k)
+    assert disp.startswith("fma_kernel")
+    assert_close(f64(c), O.bf16_round(ref), f"K={k} M={m} N={n}")
+
+
+def test_k_multiple_of_32_rms_and_argmax():
+    (c, am), ref, disp, _ = _case(16, 8, 3000, 2080, rms=True, argmax=True)
+    assert disp.startswith("fma_kernel") and "rms=1" in disp and "argmax=1" in disp
+    assert_close(f64(c), O.bf16_round(ref), "K=2080 rms + argmax")
+    check_argmax(am.cpu().numpy(), f64(c), ref, what="K=2080 argmax")
+
+
+def test_k_multiple_of_32_deterministic_and_strided():
+    c1, ref, _, (W, a, ws) = _case(17, 5, 700, 1056, lda=1200)
+    assert_close(f64(c1), O.bf16_round(ref), "K=1056 lda=1200")
+    c2 = ops.gemm(a, W, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)

@@ -1,13 +1,11 @@
 """GPU checks of programs (a chain of GEMM / MoE calls in one persistent
-launch).  With every op spread over every SM (NVFP4_PROGRAM_TARGET_STAGES=0)
-a program splits the work exactly like the single calls, and its results are
-bit-identical to the same calls issued one by one (which the other files
-check against the float64 oracle).  With the default placement (small dense
+launch).  With every op spread over every SM (NVFP4_FLAG_ALL_SMS; MoE ops
+always are) a program splits the work exactly like the single calls, and its
+results are bit-identical to the same calls issued one by one (which the
+other files check against the float64 oracle).  With the default placement (small dense
 ops on a rotating subset of SMs, fewer split-K partial sums) results are
 checked against the oracle, teacher-forced op by op.  The workspace counters
 are back at zero after every launch."""
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -31,30 +29,18 @@ def _lib():
     assert ops.device_check(torch.cuda.current_device()) == 0, ops.last_error()
 
 
-@pytest.fixture
-def every_sm():
-    """Programs created inside the test spread every op over every SM."""
-    old = os.environ.get("NVFP4_PROGRAM_TARGET_STAGES")
-    os.environ["NVFP4_PROGRAM_TARGET_STAGES"] = "0"
-    yield
-    if old is None:
-        del os.environ["NVFP4_PROGRAM_TARGET_STAGES"]
-    else:
-        os.environ["NVFP4_PROGRAM_TARGET_STAGES"] = old
-
-
 def _counters_zero(ws):
     torch.cuda.synchronize()
     hdr = ws.buf[:256 + 4 * 16384].view(torch.int32)
     return int(hdr[1:].abs().sum().item()) == 0 and int(hdr[0].item()) == 0
 
 
-def test_single_gemm_program_equals_call(every_sm):
+def test_single_gemm_program_equals_call():
     W = device_weight(11, 3000, 2048)
     a = synth.activations_bf16(11, 8, 2048).cuda()
     ref = ops.gemm(a, W)
     out = torch.empty_like(ref)
-    prog = ops.Program([ops.gemm_op(a, W, out)])
+    prog = ops.Program([ops.gemm_op(a, W, out, all_sms=True)])
     prog.launch()
     torch.cuda.synchronize()
     assert ops.last_dispatch().startswith("stream_tc_kernel program ops=1")
@@ -63,7 +49,7 @@ def test_single_gemm_program_equals_call(every_sm):
 
 
 @pytest.mark.parametrize("m", [1, 8, 32])
-def test_gemm_chain_equals_calls_and_oracle(m, every_sm):
+def test_gemm_chain_equals_calls_and_oracle(m):
     """x -> (rms) W1 [4096 x 2048] -> (rms) W2 [2048 x 4096] -> W3 [1000 x 2048] + argmax."""
     W1 = device_weight(12, 4096, 2048)
     W2 = device_weight(13, 2048, 4096)
@@ -75,9 +61,9 @@ def test_gemm_chain_equals_calls_and_oracle(m, every_sm):
     torch.cuda.synchronize()
     p1, p2, p3 = torch.empty_like(h1), torch.empty_like(h2), torch.empty_like(h3)
     pam = torch.empty_like(am)
-    prog = ops.Program([ops.gemm_op(x, W1, p1, rms_input=True),
-                        ops.gemm_op(p1, W2, p2, rms_input=True),
-                        ops.gemm_op(p2, W3, p3, argmax_out=pam)])
+    prog = ops.Program([ops.gemm_op(x, W1, p1, rms_input=True, all_sms=True),
+                        ops.gemm_op(p1, W2, p2, rms_input=True, all_sms=True),
+                        ops.gemm_op(p2, W3, p3, argmax_out=pam, all_sms=True)])
     for _ in range(3):   # repeated launches reuse the zeroed counters
         prog.launch()
     torch.cuda.synchronize()
@@ -97,7 +83,7 @@ def layer():
 
 
 @pytest.mark.parametrize("t", [1, 8, 32])
-def test_moe_in_program_equals_call(layer, t, every_sm):
+def test_moe_in_program_equals_call(layer, t):
     ex, sh = layer
     x = synth.activations_bf16(21, t, 2048).cuda()
     ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
@@ -109,9 +95,9 @@ def test_moe_in_program_equals_call(layer, t, every_sm):
     g2 = ops.gemm(y, W, rms_input=True)
     torch.cuda.synchronize()
     pg1, py, pg2 = torch.empty_like(g1), torch.empty_like(y), torch.empty_like(g2)
-    prog = ops.Program([ops.gemm_op(x, W, pg1, rms_input=True),
+    prog = ops.Program([ops.gemm_op(x, W, pg1, rms_input=True, all_sms=True),
                         ops.moe_op(pg1, ids, w, ex, py, shared=sh, rms_input=True),
-                        ops.gemm_op(py, W, pg2, rms_input=True)])
+                        ops.gemm_op(py, W, pg2, rms_input=True, all_sms=True)])
     prog.launch()
     prog.launch()
     torch.cuda.synchronize()
@@ -120,7 +106,7 @@ def test_moe_in_program_equals_call(layer, t, every_sm):
     assert _counters_zero(prog.workspace)
 
 
-def test_two_moe_layers_share_schedule_slots(layer, every_sm):
+def test_two_moe_layers_share_schedule_slots(layer):
     """Four MoE layers in a row cycle both schedule slots twice."""
     ex, sh = layer
     t = 8
@@ -147,7 +133,7 @@ def test_two_moe_layers_share_schedule_slots(layer, every_sm):
 
 
 @pytest.mark.parametrize("tokens", [1, 8])
-def test_decode_step_program_equals_calls(tokens, every_sm):
+def test_decode_step_program_equals_calls(tokens):
     m = DecodeStep(seed=6, shape=StepShape(layers=3))
     b = m.buffers(tokens, keep=True)
     x, lg = m.inputs(tokens)
@@ -162,7 +148,7 @@ def test_decode_step_program_equals_calls(tokens, every_sm):
             t.zero_()
     b["head"].zero_()
     b["argmax"].zero_()
-    prog = m.program(b)
+    prog = m.program(b, all_sms=True)
     g = m.capture(b, prog=prog)
     g.replay()
     torch.cuda.synchronize()
