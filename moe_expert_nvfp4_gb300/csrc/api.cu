@@ -179,6 +179,8 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p, int fmt = kFmtN
   if (p->n_tiles > kTcColCntBase) return false;
   p->nkb = K / tc_unit_k(fmt);
   p->units = static_cast<long>(p->n_tiles) * p->nkb;
+  // the kernel splits units with 32-bit arithmetic (unit index x CTAs)
+  if (p->units * (sms + 1) >= (1L << 31)) return false;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   p->npad = M <= 16 ? 16 : 32;
   p->xrows = tc_xrows(M);
@@ -403,7 +405,7 @@ int tc_dense_op(const void* A, int64_t lda, int M, const DenseW& W, void* C, int
   ws_header(a, ws);
   a.partials = reinterpret_cast<float*>(ws + p.off_partials);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
-  op->mode = kTcDense;
+  op->mode = W.fmt == kFmtNvfp4 ? kTcDense : (W.fmt == kFmtFp8 ? kTcDenseF8 : kTcDenseBF);
   op->wait_prev = 1;
   return NVFP4_OK;
 }
@@ -500,8 +502,9 @@ int tc_launch_one(const TcOp& op, size_t x_bytes, int sched_bytes, int grid, uin
   pr.ops = nullptr;
   pr.n_ops = 1;
   pr.inline_ops[0] = op;
-  pr.inline_ops[0].new_sched = op.mode == kTcDense ? 0 : 1;
-  pr.inline_ops[0].last_sched_use = op.mode == kTcDense ? 0 : 1;
+  const bool moe = op.mode == kTcGateUp || op.mode == kTcDown || op.mode == kTcCombine;
+  pr.inline_ops[0].new_sched = moe ? 1 : 0;
+  pr.inline_ops[0].last_sched_use = moe ? 1 : 0;
   *n_stages = pr.n_stages;
   cudaError_t e = launch_tc(pr, grid, *smem, s, pdl, false);
   if (e != cudaSuccess) return cuda_fail(e, what);

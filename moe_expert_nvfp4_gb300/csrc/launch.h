@@ -46,7 +46,10 @@ constexpr int kTcInlineOps = 1;                          // ops passed by value 
 
 // kTcCombine: the weighted top-k combine of a MoE layer's per-pair down
 // outputs (no weights: only the epilogue warps work).
-enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2, kTcCombine = 3 };
+// kTcDenseF8 / kTcDenseBF: the dense op with FP8 or BF16 weights (kTcDense:
+// NVFP4).
+enum TcMode { kTcDense = 0, kTcGateUp = 1, kTcDown = 2, kTcCombine = 3, kTcDenseF8 = 4,
+              kTcDenseBF = 5 };
 
 // Weight format of a dense op.  Every format streams 128-row x 128-byte
 // boxes of codes (the 128-byte swizzle), one box per unit of work:

@@ -80,6 +80,15 @@ constexpr int kDBufs = 4;                      // accumulator buffers (32 column
 // [2^14, 2^15) (BF16 rows: exact; FP32 h rows: one rounding).
 constexpr uint32_t kTmemCols = 512;
 
+// Dense op kinds (one per weight format) and their compile-time format and
+// K per unit.
+__host__ __device__ constexpr bool dense_mode(int m) {
+  return m == kTcDense || m == kTcDenseF8 || m == kTcDenseBF;
+}
+__host__ __device__ constexpr int mode_fmt(int m) {
+  return m == kTcDenseF8 ? kFmtFp8 : (m == kTcDenseBF ? kFmtBf16 : kFmtNvfp4);
+}
+
 static_assert(kTcStageBytes == kCodeBytes + kRows * kSK / 16, "stage size");
 static_assert(kTcThreads == (kDecWarp0 + kDecWarps) * 32, "thread count");
 static_assert(kDecWarps == 8 && kEpiWarp0 == 4 && kEpiWarps == 4, "warpgroup layout");
@@ -176,10 +185,10 @@ struct Box {
 // (blockIdx.x - cta0) mod gridDim.x; r >= G has none.
 struct Work {
   int n_tiles, nkb, per_e;
-  long U;
+  int U;
   int G, cta0;
-  __device__ __forceinline__ long begin(int r) const { return static_cast<long>(r) * U / G; }
-  __device__ __forceinline__ int cta_of(long u) const {
+  __device__ __forceinline__ int begin(int r) const { return r * U / G; }
+  __device__ __forceinline__ int cta_of(int u) const {
     return static_cast<int>(((u + 1) * G - 1) / U);
   }
   __device__ __forceinline__ int rel(int b) const {
@@ -199,7 +208,7 @@ struct Kernel {
   __device__ __forceinline__ int tile_expert(int tile) const { return sc.active[tile / wk.per_e]; }
 
   __device__ __forceinline__ void tile_boxes(int tile, Box (&bx)[4]) const {
-    if (MODE == kTcDense) {
+    if (dense_mode(MODE)) {
       bx[0] = Box{m0, m1, tile * kRows, 0};  // one 128-row box
     } else if (MODE == kTcGateUp) {
       // one 4-D box: gate rows 64 j .. 64 j + 63 then the same up rows
@@ -219,12 +228,12 @@ struct Kernel {
     return MODE == kTcDown ? sc.active[tile / wk.per_e] : 0;
   }
   __device__ __forceinline__ int b_rows(int tile) const {
-    if (MODE == kTcDense) return a.M;
+    if (dense_mode(MODE)) return a.M;
     if (MODE == kTcGateUp) return a.T;
     return sc.cnt[sc.active[tile / wk.per_e]];
   }
   // K per unit: the dense op's format decides; MoE ops stream NVFP4
-  __device__ __forceinline__ int uk() const { return MODE == kTcDense ? a.uk : kSK; }
+  __device__ __forceinline__ int uk() const { return tc_unit_k(mode_fmt(MODE)); }
   __device__ __forceinline__ int win_stages() const { return a.win_k / uk(); }
 };
 
@@ -249,7 +258,7 @@ __device__ __forceinline__ int units_per_256(const Kernel<MODE>& kk) { return kS
 // rounded window still fits).
 template <int MODE>
 __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kbe) {
-  if (MODE != kTcDense) return kbe;
+  if (!dense_mode(MODE)) return kbe;
   const int g = units_per_256(kk);
   return min(kbe, w0 / g * g + kk.win_stages());
 }
@@ -261,7 +270,7 @@ __device__ __forceinline__ int window_end(const Kernel<MODE>& kk, int w0, int kb
 template <int MODE>
 __device__ __forceinline__ void restage_range(const Kernel<MODE>& kk, int w0, int w1,
                                               bool one_tile, int& k0, int& k1) {
-  if (MODE == kTcDense && (kk.win_stages() < kk.wk.nkb || one_tile)) {
+  if (dense_mode(MODE) && (kk.win_stages() < kk.wk.nkb || one_tile)) {
     const int g = units_per_256(kk);  // K % 256 == 0: nkb is a multiple of g
     k0 = w0 / g * g;
     k1 = (w1 + g - 1) / g * g;
@@ -351,11 +360,11 @@ struct SchedCursor {
 // abort the schedule may be incomplete: no units then.
 template <int MODE>
 __device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, const Cta& c,
-                                          long& u0, long& u1) {
+                                          int& u0, int& u1) {
   Work wk{};
-  if (MODE == kTcDense) {
+  if (dense_mode(MODE)) {
     wk.n_tiles = (a.N + kRows - 1) / kRows;
-    wk.nkb = a.K / a.uk;
+    wk.nkb = a.K / tc_unit_k(mode_fmt(MODE));
   } else {
     const int na = c.aborted() ? 0 : min(max(*sc.n_active, 0), a.E + 1);
     if (MODE == kTcGateUp) {
@@ -368,8 +377,8 @@ __device__ __forceinline__ Work make_work(const TcArgs& a, const Sched& sc, cons
       wk.nkb = a.I / kSK;
     }
   }
-  wk.U = static_cast<long>(wk.n_tiles) * wk.nkb;
-  wk.G = static_cast<int>(min(static_cast<long>(a.n_ctas), wk.U));
+  wk.U = wk.n_tiles * wk.nkb;
+  wk.G = min(a.n_ctas, wk.U);
   wk.cta0 = a.cta0;
   const int b = wk.rel(blockIdx.x);
   const bool active = b < wk.G && !c.aborted();
@@ -618,15 +627,15 @@ __device__ __forceinline__ void stage_rows(RowFn rowp, int nr, int rb, int kbeg,
 template <int MODE>
 __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table, int lane,
                                            SchedCursor& cur, int& stage, uint32_t& phase,
-                                           long& issued, uint64_t pol) {
+                                           int& issued, uint64_t pol) {
   const TcArgs& a = op.a;
   Sched sc{};
-  if (MODE != kTcDense) sc = cur.acquire(c, op);
-  long u0, u1;
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   if (u0 < u1 && tc::elect_one()) {
-    const int nm = MODE == kTcDense ? (a.fmt == kFmtNvfp4 ? 2 : 1) : 4;
+    const int nm = dense_mode(MODE) ? (MODE == kTcDense ? 2 : 1) : 4;
     for (int m = 0; m < nm; ++m) {
       if (table) acquire_tensormap(&op.maps[m]);
       prefetch_tensormap(&op.maps[m]);
@@ -642,12 +651,12 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
   volatile int* const abort_flag = c.abort_flag();
   uint32_t* const status = c.status();
   const int nkb = wk.nkb;
-  const int fmt = MODE == kTcDense ? a.fmt : kFmtNvfp4;
+  constexpr int fmt = mode_fmt(MODE);
   int tile = u0 < u1 ? static_cast<int>(u0 / nkb) : 0;
-  int kb = u0 < u1 ? static_cast<int>(u0 - static_cast<long>(tile) * nkb) : 0;
+  int kb = u0 < u1 ? u0 - tile * nkb : 0;
   int cur_tile = -1;
   Box bx[4];
-  for (long u = u0; u < u1; ++u) {
+  for (int u = u0; u < u1; ++u) {
     if (tile != cur_tile) {
       kk.tile_boxes(tile, bx);
       cur_tile = tile;
@@ -658,7 +667,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
     if (tc::elect_one()) {
       const uint32_t full = full_u + 8u * stage;
       const uint32_t st = ring_u + static_cast<uint32_t>(stage) * kTcStageBytes;
-      if (MODE == kTcDense && fmt != kFmtNvfp4) {
+      if (fmt != kFmtNvfp4) {
         // one 128 x 128-byte box: 128 K of E4M3 bytes or 64 K of BF16
         // (the x coordinate counts elements of the map's type)
         mbar_arrive_expect_tx_u32(full, kCodeBytes);
@@ -685,7 +694,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
       ++tile;
     }
   }
-  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
 }
 
 // The MMA warp, one op.  The warp stays converged: lane 0 waits on the
@@ -701,27 +710,27 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
                                        int& rstage, uint32_t& rphase) {
   const TcArgs& a = op.a;
   Sched sc{};
-  if (MODE != kTcDense) sc = cur.acquire(c, op);
-  long u0, u1;
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   XState xst;
   const uint32_t xs_addr = smem_u32(c.xs());
-  const int uk = kk.uk();
-  const bool a_smem = MODE == kTcDense && a.fmt == kFmtBf16;
+  constexpr int uk = tc_unit_k(mode_fmt(MODE));
+  constexpr bool a_smem = MODE == kTcDenseBF;
   const uint32_t ring_u = smem_u32(c.ring());
   const int n_stages = c.n_stages();
-  for (long u = u0; u < u1;) {
+  for (int u = u0; u < u1;) {
     if (__any_sync(0xffffffffu, c.aborted())) break;
     const int tile = static_cast<int>(u / wk.nkb);
     const int kbs = static_cast<int>(u % wk.nkb);
-    const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+    const int kbe = min(wk.nkb, kbs + (u1 - u));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
     const uint32_t idesc = tc::idesc_f16(nr <= 16 ? 16 : 32, a_smem);
     const int rb = tc_xrows(nr);
     const uint32_t sbo = rb == 8 ? 0u : 1024u;  // 8 staged rows: MMA rows 8..15 repeat 0..7
-    const bool one_tile = u1 <= static_cast<long>(tile + 1) * wk.nkb;
+    const bool one_tile = u1 <= (tile + 1) * wk.nkb;
     for (int w0 = kbs; w0 < kbe;) {
       const int w1 = window_end(kk, w0, kbe);
       if (!xst.covers(key, w0, w1)) {
@@ -803,7 +812,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     }
     u += kbe - kbs;
   }
-  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
 }
 
 template <int MODE>
@@ -811,13 +820,13 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
                                           int warp, int lane, uint32_t& acount, int& rstage,
                                           uint32_t& rphase) {
   Sched sc{};
-  if (MODE != kTcDense) sc = cur.acquire(c, op);
-  long u0, u1;
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  int u0, u1;
   make_work<MODE>(op.a, sc, c, u0, u1);
-  const int fmt = MODE == kTcDense ? op.a.fmt : kFmtNvfp4;
+  constexpr int fmt = mode_fmt(MODE);
   if (fmt == kFmtBf16) {
     // the MMA reads BF16 weights from the ring itself: only follow the ring
-    const long n = u1 > u0 ? u1 - u0 : 0;
+    const int n = u1 > u0 ? u1 - u0 : 0;
     rstage += static_cast<int>(n % c.n_stages());
     rphase ^= static_cast<uint32_t>((n / c.n_stages()) & 1);
     if (rstage >= c.n_stages()) {
@@ -852,10 +861,10 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
   // announced (a_full) after the first chunk of the next stage is converted,
   // so the wait for the stores overlaps that conversion
   int pend = -1;
-  for (long u = u0; u < u1; ++u) {
+  for (int u = u0; u < u1; ++u) {
     if (!wait_u32(rfull_u + 8u * rstage, rphase, status, abort_flag)) break;
     const uint32_t st = ring_u + static_cast<uint32_t>(rstage) * kTcStageBytes;
-    if (MODE == kTcDense && fmt == kFmtFp8) {
+    if (fmt == kFmtFp8) {
       // E4M3 -> FP16 (hardware convert, exact); the matrix's one scale is
       // applied to the accumulator
       uint4 cw[kDecChunks];
@@ -945,7 +954,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
     __syncwarp();
     if (lane == 0) mbar_arrive_u32(afull_u + 8u * static_cast<uint32_t>(pend));
   }
-  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
 }
 
 // Epilogue warps, one op: activation staging, accumulator folds, stream-K
@@ -960,8 +969,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
   const int b = blockIdx.x;
   Sched sc{};
-  if (MODE != kTcDense) sc = cur.acquire(c, op);
-  long u0, u1;
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
   int* sig = c.sig();
@@ -975,21 +984,21 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   float g_tile = 0.0f;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
   // the matrix's scale (NVFP4 per-tensor scale, FP8 scale; BF16: none)
-  const float gs = (MODE == kTcDense) ? (a.gscale ? *a.gscale : 1.0f) : 0.0f;
+  const float gs = (dense_mode(MODE)) ? (a.gscale ? *a.gscale : 1.0f) : 0.0f;
   // dense argmax: lane i of epilogue warp ew keeps the running best of row
   // m = ew + kEpiWarps i over the CTA's finished tiles
   float am_v = -FLT_MAX;
   int am_i = 0x7fffffff;
 
-  for (long u = u0; u < u1;) {
+  for (int u = u0; u < u1;) {
     if (c.aborted()) break;
     const int tile = static_cast<int>(u / wk.nkb);
     const int kbs = static_cast<int>(u % wk.nkb);
-    const int kbe = static_cast<int>(min(static_cast<long>(wk.nkb), kbs + (u1 - u)));
+    const int kbe = min(wk.nkb, kbs + (u1 - u));
     const int key = kk.b_key(tile);
     const int nr = kk.b_rows(tile);
     const int rb = tc_xrows(nr);
-    const bool one_tile = u1 <= static_cast<long>(tile + 1) * wk.nkb;
+    const bool one_tile = u1 <= (tile + 1) * wk.nkb;
     // the tile's expert's global scale: a global load (microseconds while the
     // weights stream) only when the expert changes, issued before the MMAs
     // are waited for
@@ -1033,11 +1042,11 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
           const bool stage_rms =
               a.rms && !rms_ready && (MODE == kTcGateUp || (kbeg == 0 && klen == a.K));
           rms_ready = rms_ready || stage_rms;
-          const __nv_bfloat16* xb = MODE == kTcDense ? a.A : a.x;
-          const int64_t ld = MODE == kTcDense ? a.lda : a.ldx;
+          const __nv_bfloat16* xb = dense_mode(MODE) ? a.A : a.x;
+          const int64_t ld = dense_mode(MODE) ? a.lda : a.ldx;
           stage_rows<__nv_bfloat16>([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen,
                                     smem_u32(c.xs()), sig, stage_rms ? rms : nullptr, ew, lane,
-                                    MODE == kTcDense && a.fmt == kFmtBf16);
+                                    MODE == kTcDenseBF);
         }
         fence_proxy_async_smem();
         esync();
@@ -1045,7 +1054,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         if (lane == 0) mbar_arrive(c.x_full());
         // dense: the RMS factor of each row over the whole K from global
         // memory, while the MMAs run
-        if (MODE == kTcDense && a.rms && !rms_ready) {
+        if (dense_mode(MODE) && a.rms && !rms_ready) {
           for (int m = ew; m < a.M; m += kEpiWarps) {
             const __nv_bfloat16* row = a.A + m * a.lda;
             // the row's largest magnitude and plain sum of squares in one
@@ -1126,8 +1135,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
       for (int j = 0; j < NC; ++j)
         if (j < nr) part[j * kRows + r] = tot[j];
       esync();
-      const int blo = wk.cta_of(static_cast<long>(tile) * wk.nkb);
-      const int bhi = wk.cta_of(static_cast<long>(tile + 1) * wk.nkb - 1);
+      const int blo = wk.cta_of(tile * wk.nkb);
+      const int bhi = wk.cta_of((tile + 1) * wk.nkb - 1);
       if (etid == 0) {
         // releases the CTA's partial (ordered before by the barrier); the last
         // adder acquires the others'
@@ -1159,7 +1168,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
     }
 
     // ---- epilogues
-    if (MODE == kTcDense) {
+    if (dense_mode(MODE)) {
 #pragma unroll
       for (int j = 0; j < NC; ++j)
         if (j < a.M) ep[j * kRows + r] = tot[j] * gs * (a.rms ? rms[j] : 1.0f);
@@ -1226,7 +1235,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   // ---- argmax: one partial per CTA of the op; the last CTA to add its own
   // reduces the op's G partials per row (the order of (value, index) pairs is
   // total, so the result does not depend on which CTA finished which tile)
-  if (MODE == kTcDense && a.argmax_out && wk.rel(b) < wk.G) {  // uniform over the warps
+  if (dense_mode(MODE) && a.argmax_out && wk.rel(b) < wk.G) {  // uniform over the warps
     const int own = ew + kEpiWarps * lane;  // the row this lane's running best belongs to
     if (own < a.M) a.am_part[own * wk.G + wk.rel(b)] = make_int2(__float_as_int(am_v), am_i);
     esync();
@@ -1253,7 +1262,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
       if (etid == 0) *a.argmax_cnt = 0u;
     }
   }
-  if (MODE != kTcDense) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
 }
 
 // The weighted combine of a MoE layer, after every CTA finished its down
@@ -1314,7 +1323,7 @@ __device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& 
   SchedCursor cur;
   int stage = 0;
   uint32_t phase = 0;
-  long issued = 0;
+  int issued = 0;
   for (int i = 0; i < prog.n_ops; ++i) {
     if (__any_sync(0xffffffffu, c.aborted())) break;
     const TcOp& op = op_at(prog, i);
@@ -1322,6 +1331,8 @@ __device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& 
       case kTcDense: produce_op<kTcDense>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       case kTcGateUp: produce_op<kTcGateUp>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       case kTcDown: produce_op<kTcDown>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      case kTcDenseF8: produce_op<kTcDenseF8>(c, op, table, lane, cur, stage, phase, issued, pol); break;
+      case kTcDenseBF: produce_op<kTcDenseBF>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;  // combine: no weights
     }
   }
@@ -1353,6 +1364,12 @@ __device__ __forceinline__ void mma_role(const TcProgram& prog, const Cta& c, in
       case kTcDense: mma_op<kTcDense>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
       case kTcGateUp: mma_op<kTcGateUp>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
       case kTcDown: mma_op<kTcDown>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase); break;
+      case kTcDenseF8:
+        mma_op<kTcDenseF8>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase);
+        break;
+      case kTcDenseBF:
+        mma_op<kTcDenseBF>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase);
+        break;
       default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
     }
   }
@@ -1386,6 +1403,8 @@ __device__ __forceinline__ void decode_role(const TcProgram& prog, const Cta& c,
       case kTcDense: decode_op<kTcDense>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcGateUp: decode_op<kTcGateUp>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcDown: decode_op<kTcDown>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      case kTcDenseF8: decode_op<kTcDenseF8>(c, op, cur, warp, lane, acount, rstage, rphase); break;
+      case kTcDenseBF: decode_op<kTcDenseBF>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
     }
   }
@@ -1425,6 +1444,14 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
         if (op.a.T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcDown, 32>(c, op, cur, ew, lane, dcount);
         break;
+      case kTcDenseF8:
+        if (op.a.M <= 16) epilogue_op<kTcDenseF8, 16>(c, op, cur, ew, lane, dcount);
+        else epilogue_op<kTcDenseF8, 32>(c, op, cur, ew, lane, dcount);
+        break;
+      case kTcDenseBF:
+        if (op.a.M <= 16) epilogue_op<kTcDenseBF, 16>(c, op, cur, ew, lane, dcount);
+        else epilogue_op<kTcDenseBF, 32>(c, op, cur, ew, lane, dcount);
+        break;
       default: combine_op(c, op, cur, ew, lane); break;
     }
     if (n_ops > 1) {
@@ -1450,7 +1477,7 @@ __device__ __forceinline__ void sched_role(const TcProgram& prog, const Cta& c, 
   int idx = -1;
   for (int i = 0; i < prog.n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);
-    if (op.mode == kTcDense || !op.new_sched) continue;
+    if (dense_mode(op.mode) || !op.new_sched) continue;
     ++idx;
     const int slot = idx % c.sched_slots();
     wait_bar(c.sched_empty_at(slot), ((idx / c.sched_slots()) & 1) ^ 1, c.status(), c.abort_flag());
