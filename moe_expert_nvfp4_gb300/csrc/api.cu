@@ -454,7 +454,7 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
   a.n_ctas = p.grid;
   a.cta0 = 0;
   gu->mode = kTcGateUp;
-  gu->new_sched = 1;
+  gu->a.new_sched = 1;
   gu->wait_prev = 1;
   *dn = *gu;
   if ((rc = weight_maps(&dn->maps[0], &dn->maps[1], experts->dn_codes, experts->dn_scales,
@@ -464,10 +464,10 @@ int tc_moe_ops(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const
     return rc;
   dn->a.win_k = I;
   dn->mode = kTcDown;
-  dn->new_sched = 0;
+  dn->a.new_sched = 0;
   *cb = *dn;  // the combine reads the down op's per-pair outputs; no weights
   cb->mode = kTcCombine;
-  cb->last_sched_use = 1;
+  cb->a.last_sched_use = 1;
   return NVFP4_OK;
 }
 
@@ -503,8 +503,8 @@ int tc_launch_one(const TcOp& op, size_t x_bytes, int sched_bytes, int grid, uin
   pr.n_ops = 1;
   pr.inline_ops[0] = op;
   const bool moe = op.mode == kTcGateUp || op.mode == kTcDown || op.mode == kTcCombine;
-  pr.inline_ops[0].new_sched = moe ? 1 : 0;
-  pr.inline_ops[0].last_sched_use = moe ? 1 : 0;
+  pr.inline_ops[0].a.new_sched = moe ? 1 : 0;
+  pr.inline_ops[0].a.last_sched_use = moe ? 1 : 0;
   *n_stages = pr.n_stages;
   cudaError_t e = launch_tc(pr, grid, *smem, s, pdl, false);
   if (e != cudaSuccess) return cuda_fail(e, what);

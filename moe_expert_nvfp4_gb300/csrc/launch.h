@@ -33,8 +33,10 @@ constexpr int kTcStageBytes = 128 * 256 / 2 + 128 * 256 / 16;  // 18432
 constexpr int kTcMaxStages = 8;
 constexpr int kTcOffBars = 0;                            // up to 64 mbarriers
 constexpr int kTcOffMisc = 512;
-constexpr int kTcOffEp = 1024;
-constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17408
+constexpr int kTcOffArgs = 1024;                         // the current op's TcArgs (epilogue)
+constexpr int kTcArgsBytes = 512;
+constexpr int kTcOffEp = kTcOffArgs + kTcArgsBytes;
+constexpr int kTcOffSched = kTcOffEp + 32 * 128 * 4;     // 17920
 // four warpgroups: {producer, MMA, scheduler, idle}, 4 epilogue warps,
 // 8 decode warps (registers rebalanced per warpgroup with setmaxnreg)
 constexpr int kTcThreads = 512;
@@ -61,7 +63,7 @@ __host__ __device__ constexpr int tc_unit_k(int fmt) {
   return fmt == kFmtNvfp4 ? 256 : (fmt == kFmtFp8 ? 128 : 64);
 }
 
-struct TcArgs {
+struct alignas(16) TcArgs {  // (a whole number of 16-byte words: copied by words)
   // dense
   const __nv_bfloat16* A;
   int64_t lda;
@@ -96,6 +98,8 @@ struct TcArgs {
   uint32_t* argmax_cnt;
   float* partials;      // [grid][2][32][128]
   int2* am_part;        // [M][CTAs of the op]: each CTA's best (value bits, index) per row
+  int new_sched;        // MoE: build a new expert schedule from this op's ids
+  int last_sched_use;   // MoE: no later op uses the current schedule
 };
 
 // Staged activation rows for n real rows: 8, 16 or 32 (the MMA's N is 16
@@ -111,8 +115,6 @@ struct TcOp {
   CUtensorMap xmap;
   TcArgs a;
   int mode;            // TcMode
-  int new_sched;       // MoE: build a new expert schedule from this op's ids
-  int last_sched_use;  // MoE: no later op uses the current schedule
   int wait_prev;       // read inputs only after every CTA finished the previous op
   int all_sms;         // program placement: spread over every SM (as the single call)
 };

@@ -320,6 +320,15 @@ struct Cta {
   __device__ __forceinline__ int* sig() const { return reinterpret_cast<int*>(base + kTcOffMisc + 64); }
   __device__ __forceinline__ float* rms() const { return reinterpret_cast<float*>(base + kTcOffMisc + 192); }
   __device__ __forceinline__ float* ep() const { return reinterpret_cast<float*>(base + kTcOffEp); }
+  // the epilogue's copy of the current op's arguments (read from shared
+  // memory instead of the device op table)
+  __device__ __forceinline__ const TcArgs& args() const {
+    return *reinterpret_cast<const TcArgs*>(base + kTcOffArgs);
+  }
+  // the current dense op's matrix scale, loaded before its completion wait
+  __device__ __forceinline__ volatile float* op_scale() const {
+    return reinterpret_cast<volatile float*>(base + kTcOffMisc + 456);
+  }
   __device__ __forceinline__ uint8_t* xs() const { return base + prog.x_offset; }
   __device__ __forceinline__ uint8_t* ring() const { return base + prog.ring_offset; }
   __device__ __forceinline__ uint8_t* sched() const { return base + prog.sched_offset; }
@@ -330,6 +339,8 @@ struct Cta {
   __device__ __forceinline__ bool aborted() const { return *abort_flag() != 0; }
 };
 static_assert(2 * kTcMaxStages + 2 * kABufs + 12 + 2 * kDBufs <= kTcOffMisc / 8, "barrier area");
+static_assert(sizeof(TcArgs) <= kTcArgsBytes && sizeof(TcArgs) % 16 == 0, "argument copy");
+static_assert(alignof(TcArgs) <= 16, "argument copy");
 static_assert(kDCol + 32 * kDBufs <= static_cast<int>(kTmemCols), "tensor memory columns");
 
 __device__ __forceinline__ const TcOp& op_at(const TcProgram& p, int i) {
@@ -341,18 +352,18 @@ __device__ __forceinline__ const TcOp& op_at(const TcProgram& p, int i) {
 // only after all kSchedUsers arrivals released its previous schedule.
 struct SchedCursor {
   int idx = -1;
-  __device__ __forceinline__ Sched acquire(const Cta& c, const TcOp& op) {
-    if (op.new_sched) {
+  __device__ __forceinline__ Sched acquire(const Cta& c, const TcArgs& a) {
+    if (a.new_sched) {
       ++idx;
       wait_bar(c.sched_full_at(idx % c.sched_slots()), (idx / c.sched_slots()) & 1, c.status(),
                c.abort_flag());
     }
     const int slot = idx < 0 ? 0 : idx % c.sched_slots();
-    return sched_layout(c.sched() + slot * c.sched_bytes(), op.a.E, op.a.T * op.a.k);
+    return sched_layout(c.sched() + slot * c.sched_bytes(), a.E, a.T * a.k);
   }
   // arrive: this thread speaks for its warp (or is the role's only thread)
-  __device__ __forceinline__ void release(const Cta& c, const TcOp& op, bool arrive) {
-    if (op.last_sched_use && arrive && idx >= 0) mbar_arrive(c.sched_empty_at(idx % c.sched_slots()));
+  __device__ __forceinline__ void release(const Cta& c, const TcArgs& a, bool arrive) {
+    if (a.last_sched_use && arrive && idx >= 0) mbar_arrive(c.sched_empty_at(idx % c.sched_slots()));
   }
 };
 
@@ -404,7 +415,6 @@ __device__ __forceinline__ void grid_wait(const uint32_t* ctr, uint32_t target, 
       *abort_flag = 1;
       return;
     }
-    __nanosleep(32);
   }
 }
 
@@ -630,7 +640,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
                                            int& issued, uint64_t pol) {
   const TcArgs& a = op.a;
   Sched sc{};
-  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op.a);
   int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
@@ -694,7 +704,7 @@ __device__ __noinline__ void produce_op(const Cta& c, const TcOp& op, bool table
       ++tile;
     }
   }
-  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op.a, lane == 0);
 }
 
 // The MMA warp, one op.  The warp stays converged: lane 0 waits on the
@@ -710,7 +720,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
                                        int& rstage, uint32_t& rphase) {
   const TcArgs& a = op.a;
   Sched sc{};
-  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op.a);
   int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
@@ -812,7 +822,7 @@ __device__ __forceinline__ void mma_op(const Cta& c, const TcOp& op, SchedCursor
     }
     u += kbe - kbs;
   }
-  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op.a, lane == 0);
 }
 
 template <int MODE>
@@ -820,7 +830,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
                                           int warp, int lane, uint32_t& acount, int& rstage,
                                           uint32_t& rphase) {
   Sched sc{};
-  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  if (!dense_mode(MODE)) sc = cur.acquire(c, op.a);
   int u0, u1;
   make_work<MODE>(op.a, sc, c, u0, u1);
   constexpr int fmt = mode_fmt(MODE);
@@ -954,7 +964,7 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
     __syncwarp();
     if (lane == 0) mbar_arrive_u32(afull_u + 8u * static_cast<uint32_t>(pend));
   }
-  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, op.a, lane == 0);
 }
 
 // Epilogue warps, one op: activation staging, accumulator folds, stream-K
@@ -962,14 +972,14 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 template <int MODE, int NC>
 __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
                                          int ew, int lane, uint32_t& dcount) {
-  const TcArgs& a = op.a;
+  const TcArgs& a = c.args();
   const int q = (kEpiWarp0 + ew) & 3;
   const int etid = ew * 32 + lane;
   const int r = 32 * q + lane;  // tile row = tensor-memory lane
   const uint32_t lane_addr = c.tmem + (static_cast<uint32_t>(32 * q) << 16);
   const int b = blockIdx.x;
   Sched sc{};
-  if (!dense_mode(MODE)) sc = cur.acquire(c, op);
+  if (!dense_mode(MODE)) sc = cur.acquire(c, a);
   int u0, u1;
   const Work wk = make_work<MODE>(a, sc, c, u0, u1);
   const Kernel<MODE> kk{a, sc, wk, &op.maps[0], &op.maps[1], &op.maps[2], &op.maps[3]};
@@ -983,8 +993,9 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   int g_expert = -1;
   float g_tile = 0.0f;
   const int first_tile = (u0 < u1) ? static_cast<int>(u0 / wk.nkb) : 0;
-  // the matrix's scale (NVFP4 per-tensor scale, FP8 scale; BF16: none)
-  const float gs = (dense_mode(MODE)) ? (a.gscale ? *a.gscale : 1.0f) : 0.0f;
+  // the matrix's scale (NVFP4 per-tensor scale, FP8 scale; BF16: none),
+  // loaded before the op's completion wait
+  const float gs = dense_mode(MODE) ? *c.op_scale() : 0.0f;
   // dense argmax: lane i of epilogue warp ew keeps the running best of row
   // m = ew + kEpiWarps i over the CTA's finished tiles
   float am_v = -FLT_MAX;
@@ -1262,7 +1273,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
       if (etid == 0) *a.argmax_cnt = 0u;
     }
   }
-  if (!dense_mode(MODE)) cur.release(c, op, lane == 0);
+  if (!dense_mode(MODE)) cur.release(c, a, lane == 0);
 }
 
 // The weighted combine of a MoE layer, after every CTA finished its down
@@ -1271,8 +1282,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
 // T x H/4 four-column groups are spread over all CTAs, one per thread.
 __device__ __noinline__ void combine_op(const Cta& c, const TcOp& op, SchedCursor& cur, int ew,
                                         int lane) {
-  const TcArgs& a = op.a;
-  const Sched sc = cur.acquire(c, op);
+  const TcArgs& a = c.args();
+  const Sched sc = cur.acquire(c, a);
   const int etid = ew * 32 + lane;
   const int groups = a.H / 4;
   const int items = a.T * groups;
@@ -1312,7 +1323,7 @@ __device__ __noinline__ void combine_op(const Cta& c, const TcOp& op, SchedCurso
     o[0] = __floats2bfloat162_rn(acc.x, acc.y);
     o[1] = __floats2bfloat162_rn(acc.z, acc.w);
   }
-  cur.release(c, op, lane == 0);
+  cur.release(c, a, lane == 0);
 }
 
 // ------------------------------------------------------------ roles
@@ -1333,7 +1344,7 @@ __device__ __forceinline__ void producer_role(const TcProgram& prog, const Cta& 
       case kTcDown: produce_op<kTcDown>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       case kTcDenseF8: produce_op<kTcDenseF8>(c, op, table, lane, cur, stage, phase, issued, pol); break;
       case kTcDenseBF: produce_op<kTcDenseBF>(c, op, table, lane, cur, stage, phase, issued, pol); break;
-      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;  // combine: no weights
+      default: cur.acquire(c, op.a); cur.release(c, op.a, lane == 0); break;  // combine: no weights
     }
   }
   // wait for the TMA writes still in flight (bounded, ignores aborts)
@@ -1370,7 +1381,7 @@ __device__ __forceinline__ void mma_role(const TcProgram& prog, const Cta& c, in
       case kTcDenseBF:
         mma_op<kTcDenseBF>(c, op, cur, lane, acount, dcount, xcount, rstage, rphase);
         break;
-      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
+      default: cur.acquire(c, op.a); cur.release(c, op.a, lane == 0); break;
     }
   }
   // every MMA has completed before tensor memory is released
@@ -1405,7 +1416,7 @@ __device__ __forceinline__ void decode_role(const TcProgram& prog, const Cta& c,
       case kTcDown: decode_op<kTcDown>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcDenseF8: decode_op<kTcDenseF8>(c, op, cur, warp, lane, acount, rstage, rphase); break;
       case kTcDenseBF: decode_op<kTcDenseBF>(c, op, cur, warp, lane, acount, rstage, rphase); break;
-      default: cur.acquire(c, op); cur.release(c, op, lane == 0); break;
+      default: cur.acquire(c, op.a); cur.release(c, op.a, lane == 0); break;
     }
   }
 }
@@ -1418,38 +1429,45 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
   // inputs may come from the previous kernel on the stream
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int kArgWords = static_cast<int>(sizeof(TcArgs)) / 16;
   for (int i = 0; i < n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);
-    // the op's arguments (device op table, global memory) into L1 while
-    // waiting for the previous op: their first reads would otherwise be
-    // dependent trips to L2 after the wait
-    if (prog.ops && ew == 0 && lane < (static_cast<int>(sizeof(TcArgs)) + 127) / 128)
-      prefetch_l1(reinterpret_cast<const uint8_t*>(&op.a) + 128 * lane);
+    // the op's arguments (the device op table, or the launch parameters)
+    // and a dense op's matrix scale are loaded before waiting for the
+    // previous op (neither depends on it) and kept in shared memory: every
+    // later read is local instead of a dependent trip to global memory
+    uint4 av = make_uint4(0u, 0u, 0u, 0u);
+    if (etid < kArgWords) av = reinterpret_cast<const uint4*>(&op.a)[etid];
+    float scale = 1.0f;
+    if (etid == kArgWords && dense_mode(op.mode) && op.a.gscale) scale = *op.a.gscale;
     if (i > 0 && op.wait_prev) {
       // every CTA has finished op i - 1: its outputs are complete
       if (etid == 0) grid_wait(&prog.done[i - 1], gridDim.x, c.status(), c.abort_flag());
-      esync();
     }
+    esync();  // the previous op's readers of the copy are done
+    if (etid < kArgWords) reinterpret_cast<uint4*>(c.base + kTcOffArgs)[etid] = av;
+    if (etid == kArgWords) *c.op_scale() = scale;
+    esync();
     switch (op.mode) {
       // accumulator columns: 16 when the op has at most 16 activation rows
       case kTcDense:
-        if (op.a.M <= 16) epilogue_op<kTcDense, 16>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDense, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcDense, 32>(c, op, cur, ew, lane, dcount);
         break;
       case kTcGateUp:
-        if (op.a.T <= 16) epilogue_op<kTcGateUp, 16>(c, op, cur, ew, lane, dcount);
+        if (c.args().T <= 16) epilogue_op<kTcGateUp, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcGateUp, 32>(c, op, cur, ew, lane, dcount);
         break;
       case kTcDown:
-        if (op.a.T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount);
+        if (c.args().T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcDown, 32>(c, op, cur, ew, lane, dcount);
         break;
       case kTcDenseF8:
-        if (op.a.M <= 16) epilogue_op<kTcDenseF8, 16>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDenseF8, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcDenseF8, 32>(c, op, cur, ew, lane, dcount);
         break;
       case kTcDenseBF:
-        if (op.a.M <= 16) epilogue_op<kTcDenseBF, 16>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDenseBF, 16>(c, op, cur, ew, lane, dcount);
         else epilogue_op<kTcDenseBF, 32>(c, op, cur, ew, lane, dcount);
         break;
       default: combine_op(c, op, cur, ew, lane); break;
@@ -1477,7 +1495,7 @@ __device__ __forceinline__ void sched_role(const TcProgram& prog, const Cta& c, 
   int idx = -1;
   for (int i = 0; i < prog.n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);
-    if (dense_mode(op.mode) || !op.new_sched) continue;
+    if (dense_mode(op.mode) || !op.a.new_sched) continue;
     ++idx;
     const int slot = idx % c.sched_slots();
     wait_bar(c.sched_empty_at(slot), ((idx / c.sched_slots()) & 1) ^ 1, c.status(), c.abort_flag());
