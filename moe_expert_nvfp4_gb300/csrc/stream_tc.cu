@@ -971,7 +971,8 @@ __device__ __forceinline__ void decode_op(const Cta& c, const TcOp& op, SchedCur
 // reduction and the op's epilogue.
 template <int MODE, int NC>
 __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedCursor& cur,
-                                         int ew, int lane, uint32_t& dcount) {
+                                         int ew, int lane, uint32_t& dcount,
+                                         const uint32_t* wait_ctr) {
   const TcArgs& a = c.args();
   const int q = (kEpiWarp0 + ew) & 3;
   const int etid = ew * 32 + lane;
@@ -987,6 +988,20 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
   float* rms = c.rms();
   float* ep = c.ep();
   volatile int* bcast = c.bcast();
+
+  // The wait for the previous op (its outputs are this op's inputs) comes
+  // right before the first activations are read: everything before it
+  // depends only on this op's arguments, weights and routing, and so runs
+  // while the previous op finishes.
+  bool waited = wait_ctr == nullptr;
+  auto wait_inputs = [&]() {
+    if (!waited) {
+      if (etid == 0) grid_wait(wait_ctr, gridDim.x, c.status(), c.abort_flag());
+      esync();
+      waited = true;
+    }
+  };
+  if (u0 >= u1) wait_inputs();  // (keeps the completion order transitive)
 
   XState xst;
   bool rms_ready = false;
@@ -1033,6 +1048,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
     for (int w0 = kbs; w0 < kbe;) {
       const int w1 = window_end(kk, w0, kbe);
       if (!xst.covers(key, w0, w1)) {
+        wait_inputs();
         restage_range(kk, w0, w1, one_tile, xst.k0, xst.k1);
         xst.key = key;
         // the previous window's MMAs are complete (its accumulator was read)
@@ -1440,10 +1456,9 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
     if (etid < kArgWords) av = reinterpret_cast<const uint4*>(&op.a)[etid];
     float scale = 1.0f;
     if (etid == kArgWords && dense_mode(op.mode) && op.a.gscale) scale = *op.a.gscale;
-    if (i > 0 && op.wait_prev) {
-      // every CTA has finished op i - 1: its outputs are complete
-      if (etid == 0) grid_wait(&prog.done[i - 1], gridDim.x, c.status(), c.abort_flag());
-    }
+    // every CTA has finished op i - 1 once done[i - 1] == grid: its outputs
+    // are complete (the ops wait for it before reading their inputs)
+    const uint32_t* wait_ctr = (i > 0 && op.wait_prev) ? &prog.done[i - 1] : nullptr;
     esync();  // the previous op's readers of the copy are done
     if (etid < kArgWords) reinterpret_cast<uint4*>(c.base + kTcOffArgs)[etid] = av;
     if (etid == kArgWords) *c.op_scale() = scale;
@@ -1451,26 +1466,32 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
     switch (op.mode) {
       // accumulator columns: 16 when the op has at most 16 activation rows
       case kTcDense:
-        if (c.args().M <= 16) epilogue_op<kTcDense, 16>(c, op, cur, ew, lane, dcount);
-        else epilogue_op<kTcDense, 32>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDense, 16>(c, op, cur, ew, lane, dcount, wait_ctr);
+        else epilogue_op<kTcDense, 32>(c, op, cur, ew, lane, dcount, wait_ctr);
         break;
       case kTcGateUp:
-        if (c.args().T <= 16) epilogue_op<kTcGateUp, 16>(c, op, cur, ew, lane, dcount);
-        else epilogue_op<kTcGateUp, 32>(c, op, cur, ew, lane, dcount);
+        if (c.args().T <= 16) epilogue_op<kTcGateUp, 16>(c, op, cur, ew, lane, dcount, wait_ctr);
+        else epilogue_op<kTcGateUp, 32>(c, op, cur, ew, lane, dcount, wait_ctr);
         break;
       case kTcDown:
-        if (c.args().T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount);
-        else epilogue_op<kTcDown, 32>(c, op, cur, ew, lane, dcount);
+        if (c.args().T <= 16) epilogue_op<kTcDown, 16>(c, op, cur, ew, lane, dcount, wait_ctr);
+        else epilogue_op<kTcDown, 32>(c, op, cur, ew, lane, dcount, wait_ctr);
         break;
       case kTcDenseF8:
-        if (c.args().M <= 16) epilogue_op<kTcDenseF8, 16>(c, op, cur, ew, lane, dcount);
-        else epilogue_op<kTcDenseF8, 32>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDenseF8, 16>(c, op, cur, ew, lane, dcount, wait_ctr);
+        else epilogue_op<kTcDenseF8, 32>(c, op, cur, ew, lane, dcount, wait_ctr);
         break;
       case kTcDenseBF:
-        if (c.args().M <= 16) epilogue_op<kTcDenseBF, 16>(c, op, cur, ew, lane, dcount);
-        else epilogue_op<kTcDenseBF, 32>(c, op, cur, ew, lane, dcount);
+        if (c.args().M <= 16) epilogue_op<kTcDenseBF, 16>(c, op, cur, ew, lane, dcount, wait_ctr);
+        else epilogue_op<kTcDenseBF, 32>(c, op, cur, ew, lane, dcount, wait_ctr);
         break;
-      default: combine_op(c, op, cur, ew, lane); break;
+      default:
+        if (wait_ctr) {
+          if (etid == 0) grid_wait(wait_ctr, gridDim.x, c.status(), c.abort_flag());
+          esync();
+        }
+        combine_op(c, op, cur, ew, lane);
+        break;
     }
     if (n_ops > 1) {
       esync();
