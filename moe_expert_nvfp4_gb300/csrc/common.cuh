@@ -81,6 +81,18 @@ __device__ __forceinline__ void st_shared_v4(uint32_t a, uint4 v) {
                : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (cp.async.cg); src_bytes 0
+// writes 16 zero bytes instead.  The thread waits for its own copies with
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));

@@ -424,6 +424,97 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
 }
 
+// BF16 activation rows staged with asynchronous copies and rolled loops
+// (little code: the staging runs once per op, after other roles' code has
+// passed through the instruction cache).  Rows [0, nr) of the K range
+// [kbeg, kbeg + klen) land as BF16 in the staged layout, rows [nr, rb) as
+// zeros; then per row the largest magnitude (and, with rms, the sum of
+// squares), and unless raw the in-place conversion to FP16 times 2^sig[n].
+// Each lane walks the 16-byte chunks lane, lane + 32, ... of its warp's
+// rows in that order, as the register path and the dense RMS pass do (same
+// sums, bit for bit).  The four epilogue warps; klen % 256 == 0.
+__device__ __forceinline__ void stage_rows_async(const __nv_bfloat16* base, int64_t ld, int nr,
+                                                 int rb, int kbeg, int klen, uint32_t xs,
+                                                 int* sig, float* rms, int ew, int lane,
+                                                 bool raw) {
+  const int cpr = klen >> 3;  // 16-byte chunks per row
+  const int etid = ew * 32 + lane;
+#pragma unroll 1
+  for (int i = etid; i < rb * cpr; i += kEpiThreads) {
+    const int n = i / cpr, kc = i - n * cpr;
+    const __nv_bfloat16* src = base + static_cast<size_t>(n < nr ? n : 0) * ld + kbeg + 8 * kc;
+    cp_async_16(xs + xoff(n, 8 * kc, rb), src, n < nr ? 16u : 0u);
+  }
+  cp_async_wait_all();
+  esync();
+#pragma unroll 1
+  for (int n = ew; n < rb; n += kEpiWarps) {
+    if (n >= nr) {
+      if (lane == 0) sig[n] = 0;
+      continue;
+    }
+    uint32_t mx = 0u;
+    float sq = 0.0f;
+#pragma unroll 4
+    for (int kc = lane; kc < cpr; kc += 32) {
+      const uint4 v = ld_shared_v4(xs + xoff(n, 8 * kc, rb));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);
+        if (rms) {
+          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+          sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+        }
+      }
+    }
+    const float m = warp_max(fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u)));
+    const int sh = f16_row_shift(m);
+    if (rms) {
+      if (m > kSumsqSafeMax) {  // (warp-uniform, rare) the shifted squares
+        const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+        const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+        sq = 0.0f;
+#pragma unroll 1
+        for (int kc = lane; kc < cpr; kc += 32) {
+          const uint4 v = ld_shared_v4(xs + xoff(n, 8 * kc, rb));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+            const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+            sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+          }
+        }
+      }
+      sq = warp_sum(sq);
+      if (lane == 0) rms[n] = m > kSumsqSafeMax ? rms_factor(sq, sh, klen) : rms_plain(sq, klen);
+    }
+    if (lane == 0) sig[n] = raw ? 0 : sh;
+    if (raw) continue;
+    const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+    const bool two = h1 != sh;
+#pragma unroll 4
+    for (int kc = lane; kc < cpr; kc += 32) {
+      const uint32_t addr = xs + xoff(n, 8 * kc, rb);
+      const uint4 v = ld_shared_v4(addr);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float lo = __uint_as_float(w[j] << 16) * f1, hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1;
+        if (two) {
+          lo *= f2;
+          hi *= f2;
+        }
+        o[j] = pack_f16x2(lo, hi);
+      }
+      st_shared_v4(addr, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+}
+
 // One row of the staged operand, held in registers: the lane's 16-byte
 // loads of row n (chunks kc = lane + 32 i of 8 elements; FP32 rows take two
 // loads a chunk), at most kStageSlots loads.
@@ -1071,9 +1162,8 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
           rms_ready = rms_ready || stage_rms;
           const __nv_bfloat16* xb = dense_mode(MODE) ? a.A : a.x;
           const int64_t ld = dense_mode(MODE) ? a.lda : a.ldx;
-          stage_rows<__nv_bfloat16>([&](int n) { return xb + n * ld; }, nr, rb, kbeg, klen,
-                                    smem_u32(c.xs()), sig, stage_rms ? rms : nullptr, ew, lane,
-                                    MODE == kTcDenseBF);
+          stage_rows_async(xb, ld, nr, rb, kbeg, klen, smem_u32(c.xs()), sig,
+                           stage_rms ? rms : nullptr, ew, lane, MODE == kTcDenseBF);
         }
         fence_proxy_async_smem();
         esync();
