@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--profile", default=None, metavar="WORKLOAD",
+                   help="run one workload's calls a few times and exit (for ncu captures): "
+                        "dense:N:K:M, head:M, moe:T, fp8:N:K:M, bf16w:N:K:M")
     p.add_argument("--path", default="program", choices=["program", "calls"],
                    help="program: the step as one persistent launch after routing; calls: one "
                         "kernel launch per call")
@@ -501,36 +504,37 @@ def workload_table(model, reps=10):
         out[f"bf16w_4096x2048_M{m}"] = {"us": us, "gbs": 4096 * 2048 * 2 / us / 1e3}
     del copies
 
-    # CUDA cores against tensor cores on the same stream of NVFP4 rows: a
-    # 16,384-row matrix (8 copies, 151 MB), K = 2048 through the tcgen05
-    # kernel (a one-op program when the call itself would take the CUDA-core
-    # kernel) and K = 2080 through the CUDA-core kernel (every K that is not
-    # a multiple of 256 takes it); GB/s counts each call's own bytes
-    n = 16384
-    tc_w = weights(73, n, 2048, 8)
-    fm_w = weights(74, n, 2080, 8)
-    for m in (1, 2, 4, 8):
-        row = {}
-        for name, ws_, k in (("tcgen05", tc_w, 2048), ("cuda_cores", fm_w, 2080)):
-            a = synth.activations_bf16(75, m, k).to(dev)
-            c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
-            wk = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
-            ops.gemm(a, ws_[0], out=c, workspace=wk)
-            kern = ops.last_dispatch().split()[0]
-            if name == "tcgen05" and kern != "stream_tc_kernel<dense>":
-                progs = [ops.Program([ops.gemm_op(a, w, c, all_sms=True)]) for w in ws_]
-                us = graph_us(lambda: [p.launch() for p in progs], reps) / len(progs)
-                kern = "stream_tc_kernel (one-op program)"
-                del progs
-            else:
-                def seq():
-                    for w in ws_:
-                        ops.gemm(a, w, out=c, workspace=wk)
-                us = graph_us(seq, reps) / len(ws_)
-            row[name] = {"us": round(us, 2), "gbs": round(nvfp4_bytes(n, k) / us / 1e3, 1),
-                         "kernel": kern}
-        out[f"tc_vs_fma_{n}_M{m}"] = row
-    del tc_w, fm_w
+    # CUDA cores against tensor cores on the same NVFP4 rows: N rows (enough
+    # copies to exceed L2 where the matrix is small), K = 2048 through the
+    # tcgen05 kernel (a one-op program when the call itself would take the
+    # CUDA-core kernel) and K = 2080 through the CUDA-core kernel (every K
+    # that is not a multiple of 256 takes it); GB/s counts each call's own
+    # bytes
+    for n, n_copies in ((64, 1), (4096, 24), (16384, 8), (s.vocab, 1)):
+        tc_w = weights(73, n, 2048, n_copies)
+        fm_w = weights(74, n, 2080, n_copies)
+        for m in (1, 2, 4, 8):
+            row = {}
+            for name, ws_, k in (("tcgen05", tc_w, 2048), ("cuda_cores", fm_w, 2080)):
+                a = synth.activations_bf16(75, m, k).to(dev)
+                c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+                wk = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
+                ops.gemm(a, ws_[0], out=c, workspace=wk)
+                kern = ops.last_dispatch().split()[0]
+                if name == "tcgen05" and kern != "stream_tc_kernel<dense>":
+                    progs = [ops.Program([ops.gemm_op(a, w, c, all_sms=True)]) for w in ws_]
+                    us = graph_us(lambda: [p.launch() for p in progs], reps) / len(progs)
+                    kern = "stream_tc_kernel (one-op program)"
+                    del progs
+                else:
+                    def seq():
+                        for w in ws_:
+                            ops.gemm(a, w, out=c, workspace=wk)
+                    us = graph_us(seq, reps) / len(ws_)
+                row[name] = {"us": round(us, 2), "gbs": round(nvfp4_bytes(n, k) / us / 1e3, 1),
+                             "kernel": kern}
+            out[f"tc_vs_fma_{n}x2048_M{m}"] = row
+        del tc_w, fm_w
 
     # BF16 -> NVFP4 quantisation of a head-sized BF16 matrix (622 MB >> L2)
     wb = torch.randn(s.vocab, s.hidden, device=dev,
@@ -744,8 +748,60 @@ def run_ours(args, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_profile(spec, reps=4):
+    """One workload's calls, ``reps`` times, then exit: the launches an ncu
+    capture of that workload measures (the first is a warm-up).  Prints the
+    workload's algorithmic weight bytes per call."""
+    import torch
+    from moe_expert_nvfp4_gb300 import ops, synth
+    from moe_expert_nvfp4_gb300.decode_step import DecodeStep, StepShape, nvfp4_bytes
+    ops.load()
+    dev = "cuda"
+    g1 = torch.full((1,), synth.GLOBAL_SCALE, dtype=torch.float32, device=dev)
+    kind, *dims = spec.split(":")
+    dims = [int(v) for v in dims]
+    if kind in ("dense", "head"):
+        n, k, m = dims if kind == "dense" else (151936, 2048, dims[0])
+        w = ops.NVFP4Weight(*synth.nvfp4_weight(1, n, k, 90, device=dev), g1)
+        a = synth.activations_bf16(1, m, k).to(dev)
+        call = (lambda: ops.gemm(a, w, argmax=True)) if kind == "head" else (lambda: ops.gemm(a, w))
+        nbytes = nvfp4_bytes(n, k)
+    elif kind == "fp8":
+        n, k, m = dims
+        w = ops.FP8Weight(synth.fp8_weight(1, n, k).to(dev),
+                          torch.full((1,), synth.FP8_SCALE, dtype=torch.float32, device=dev))
+        a = synth.activations_bf16(1, m, k).to(dev)
+        call = lambda: ops.fp8_gemm(a, w)
+        nbytes = n * k
+    elif kind == "bf16w":
+        n, k, m = dims
+        w = synth.bf16_weight(1, n, k).to(dev)
+        a = synth.activations_bf16(1, m, k).to(dev)
+        call = lambda: ops.bf16w_gemm(a, w)
+        nbytes = 2 * n * k
+    elif kind == "moe":
+        t = dims[0]
+        model = DecodeStep(seed=6, shape=StepShape(layers=1))
+        s = model.s
+        x = synth.activations_bf16(4, t, s.hidden).to(dev)
+        ids, wts = ops.route(synth.router_logits(4, t, s.num_experts).to(dev), s.top_k)
+        call = lambda: ops.moe(x, ids, wts, model.experts[0], model.shared[0])
+        per_expert = nvfp4_bytes(2 * s.inter, s.hidden) + nvfp4_bytes(s.hidden, s.inter)
+        nbytes = (torch.unique(ids).numel() + 1) * per_expert
+    else:
+        raise SystemExit(f"unknown workload {spec}")
+    for _ in range(reps):
+        call()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": spec, "weight_bytes_per_call": int(nbytes),
+                      "dispatch": ops.last_dispatch()}))
+
+
 def main():
     args = parse()
+    if args.profile:
+        run_profile(args.profile)
+        return
     rank, world, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, rank)

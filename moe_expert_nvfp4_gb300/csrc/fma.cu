@@ -14,7 +14,8 @@
 // product exact), then adds block scale x block sum into the row's FP32
 // total.  A warp reduction ends the row.  The activations (1, 2 or 4 rows
 // per CTA, grid.y covering the rest) are staged once per CTA in shared memory as FP16 after the
-// same power-of-two row shift as the tensor path (exact for BF16 rows),
+// same power-of-two row shift as the tensor path (exact for BF16 elements
+// within 2^31 of the row's largest magnitude),
 // with a bank-conflict-free swizzle of each chunk's four 16-byte slots.
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode

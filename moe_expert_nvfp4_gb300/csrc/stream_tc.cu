@@ -77,7 +77,9 @@ constexpr int kDBufs = 4;                      // accumulator buffers (32 column
 // to FP16 exactly (a code x scale product has at most 6 significant bits and
 // lies in [2^-10, 2688]); the activations are staged as FP16 after a
 // power-of-two shift per row that puts the row's largest magnitude in
-// [2^14, 2^15) (BF16 rows: exact; FP32 h rows: one rounding).
+// [2^14, 2^15) (BF16 rows: exact for every element within 2^31 of the row's
+// largest magnitude, smaller ones round to FP16 subnormals or zero; FP32 h
+// rows: one rounding).
 constexpr uint32_t kTmemCols = 512;
 
 // Dense op kinds (one per weight format) and their compile-time format and
@@ -686,7 +688,8 @@ __device__ __forceinline__ void stage_row_pair(const uint4 (&b0)[kStageSlots],
 // Activations staged through registers in one pass: BF16 (dense A, MoE x)
 // or FP32 (MoE h) rows [0, nr) of the K range [kbeg, kbeg + klen) read with
 // 16-byte loads, converted to FP16 times 2^sig[n] (the shift that puts row
-// n's largest magnitude in [2^14, 2^15); exact for BF16, one rounding for
+// n's largest magnitude in [2^14, 2^15); exact for BF16 elements within 2^31
+// of the largest (smaller ones round to FP16 subnormals), one rounding for
 // FP32) into the 128-byte swizzled K-block layout, rows [nr, rb) zero; with
 // rms != nullptr also rms[n] = 1/sqrt(mean x^2 + 1e-6) over the staged range.
 // Warp ew takes rows ew, ew + 4, ... two at a time (their loads in flight
