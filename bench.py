@@ -156,7 +156,8 @@ def measured_peak():
 
 def profiled_traffic(kernel_key):
     """DRAM bytes per launch recorded from an ncu capture, valid only while
-    the kernel sources are unchanged (same hash)."""
+    the kernel's sources (the entry's ``sources``, else all of them) are
+    unchanged (same hash)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -165,7 +166,7 @@ def profiled_traffic(kernel_key):
         return None
     from moe_expert_nvfp4_gb300 import build as B
     ent = d.get(kernel_key)
-    if not ent or ent.get("source_hash") != B.source_hash():
+    if not ent or ent.get("source_hash") != B.source_hash(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
 

@@ -38,12 +38,14 @@ def _deps() -> list[str]:
     return out
 
 
-def source_hash() -> str:
+def source_hash(files=None) -> str:
     """sha256 over the kernel sources and the public header (identifies the
-    kernel version a profile was taken on)."""
+    kernel version a profile was taken on).  ``files`` (names under csrc/)
+    narrows it to one kernel's sources: a counter taken on that kernel stays
+    valid while they and the header are unchanged."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in sorted(files if files is not None else os.listdir(CSRC)):
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     with open(os.path.join(ROOT, "include", "nvfp4moe.h"), "rb") as fh:
