@@ -63,12 +63,6 @@ def workload_name(t, layers=40):
 
 # ------------------------------------------------------------------ distributed
 
-def calls_launches(layers):
-    """Kernels of the step issued call by call: routing, then per layer QKV,
-    O and the MoE layer's gate_up, down and combine kernels, then the head."""
-    return 1 + 5 * layers + 1
-
-
 def dist_setup(n):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -361,7 +355,9 @@ def workload_table(model, reps=10):
     * the dense sweep: M in {1, 4, 8, 16, 32} x {4096 x 2048, 8192 x 2048,
       2048 x 4096} (seeds 1-3);
     * the MoE layer (256 routed + 1 shared experts, hidden 2048, inter 512,
-      top-8) at T in {1, 4, 8, 16, 32}, over the step's layer weights;
+      top-8) at T in {1, 2, 4, 8, 16, 32}, over the step's layer weights
+      (where the call runs on the CUDA cores, the same layers on the tensor
+      cores too);
     * the MTP-verify batch: the MoE layer at T = 32 then the 151,936 x 2048
       head with argmax;
     * the hot-vocabulary draft head: 32,768 listed rows of that head (the
@@ -409,7 +405,7 @@ def workload_table(model, reps=10):
     s = model.s
     per_expert = nvfp4_bytes(2 * s.inter, s.hidden) + nvfp4_bytes(s.hidden, s.inter)
     L = min(16, s.layers)
-    for t in (1, 4, 8, 16, 32):
+    for t in (1, 2, 4, 8, 16, 32):
         x = synth.activations_bf16(4, t, s.hidden).to(dev)
         lg = torch.cat([synth.router_logits(4, t, s.num_experts, l) for l in range(L)]).to(dev)
         ids, wts = ops.route(lg, s.top_k)
@@ -423,7 +419,17 @@ def workload_table(model, reps=10):
                 ops.moe(x, ids[l * t:(l + 1) * t], wts[l * t:(l + 1) * t], model.experts[l],
                         model.shared[l], out=y, workspace=wk, ids_ready=True)
         us = graph_us(layers, reps)
-        out[f"moe_T{t}"] = {"us": us / L, "gbs": nbytes / us / 1e3}
+        out[f"moe_T{t}"] = {"us": us / L, "gbs": nbytes / us / 1e3,
+                            "kernel": ops.last_dispatch().split(";")[0]}
+        if ops.last_dispatch().startswith("moe_fma"):
+            # the same layers on the tensor-core kernels (one-op programs)
+            progs = [ops.Program([ops.moe_op(x, ids[l * t:(l + 1) * t], wts[l * t:(l + 1) * t],
+                                             model.experts[l], y, shared=model.shared[l])])
+                     for l in range(L)]
+            us = graph_us(lambda: [p.launch() for p in progs], reps)
+            out[f"moe_tc_T{t}"] = {"us": us / L, "gbs": nbytes / us / 1e3,
+                                   "kernel": "stream_tc_kernel (one-op program)"}
+            del progs
 
     # MTP-verify batch: MoE layer at T = 32, then the head with argmax
     t = 32
@@ -613,7 +619,7 @@ def run_ours(args, rank, world, local):
 
     t = args.tokens
     b, g, x, lg, ms, nbytes, clocks = one_config(t, args.steps, args.warmup, True)
-    n_launch = 2 if args.path == "program" else calls_launches(model.s.layers)
+    n_launch = b["launches"]
     value = job_gbs(nbytes, world, ms)
 
     # ---- end to end: pinned host inputs in, argmax ids out, every step
@@ -708,9 +714,9 @@ def run_ours(args, rank, world, local):
     # ---- the same step issued call by call (one kernel per call), for context
     calls = None
     if args.path == "program" and not args.no_sweep:
-        _, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, "calls")
+        b3, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, "calls")
         calls = {"us_per_step": ms3 * 1e3, "gbs": nb3 / (ms3 * 1e-3) / 1e9,
-                 "launches_per_step": calls_launches(model.s.layers)}
+                 "launches_per_step": b3["launches"]}
         del g3
 
     # ---- CPU baseline: the oracle on one layer of the same step

@@ -78,10 +78,11 @@ enum {
  * weights, before waiting for that kernel to finish. */
 #define NVFP4_FLAG_IDS_READY 4u
 /* Program ops (nvfp4_program_create) only: spread this op over every SM and
- * split it exactly as its single call does, so its results are bit-identical
- * to the single call's.  Without it a small dense op of a program runs on
- * fewer SMs (whole 128-row tiles or few K splits each) while the other SMs
- * stream the next ops' weights. */
+ * split it exactly as its single call does on the tensor cores, so its
+ * results are bit-identical to that call's (a single call that its shape
+ * sends to the CUDA-core kernels adds in another order).  Without it a
+ * small dense op of a program runs on fewer SMs (whole 128-row tiles or few
+ * K splits each) while the other SMs stream the next ops' weights. */
 #define NVFP4_FLAG_ALL_SMS 8u
 
 /* device status bits */
@@ -125,10 +126,15 @@ int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream);
  *   argmax_out: NULL, or int32 [M]: index of the first maximum of each row of
  *   the BF16 output C (ties to the lowest index).
  * Split-K partial sums are reduced in a fixed order: results are
- * deterministic.  K % 32 == 0.  Two kernels serve it, chosen by shape alone:
- * K % 256 == 0 streams 256-K stages through the tensor cores (tcgen05);
- * other K run on the CUDA cores (whole rows per warp, FP32 accumulation of
- * the same exact FP16 products), which the dispatch record names. */
+ * deterministic.  K % 32 == 0.  Two kernels serve it, chosen by shape alone
+ * (nvfp4_last_dispatch names the one that ran): the tensor-core kernel
+ * streams 256-K stages through tcgen05 MMAs and costs about 13 us a call
+ * before its first byte; the CUDA-core kernel (whole rows per warp, FP32
+ * accumulation of the same exact FP16 products) starts in a few us but does
+ * one FMA per weight and row.  The CUDA cores take every K % 256 != 0, and
+ * K % 256 == 0 when M = 1 and the weight is at most 128 MiB, or 2 <= M <= 8
+ * and M x the weight bytes are at most 32 MiB.  The two differ only in the
+ * order of the FP32 additions (a few units in the last place of C). */
 size_t nvfp4_gemm_skinny_workspace(int M, int N, int K);
 int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                       void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
@@ -275,7 +281,8 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
  * keeps streaming the weights of the calls ahead while the current call's
  * split-K reductions finish, and a call reads its activations only once every
  * CTA has finished the call before it (completion counters in the workspace).
- * Each op computes what its single call computes.  A small dense op may have
+ * Each op computes what its single call computes, always on the tensor
+ * cores (the tcgen05 kernel's path of that call).  A small dense op may have
  * its K range split over fewer CTAs than the single call would use, which
  * changes the order in which FP32 split-K partials are added, so its output
  * can differ from the single call's in the last bits; every launch of one

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libnvfp4moe.so")
-SOURCES = ["api.cu", "route.cu", "stream_tc.cu", "fma.cu", "noalloc.cu", "rows.cu", "quant.cu",
+SOURCES = ["api.cu", "route.cu", "stream_tc.cu", "fma.cu", "moe_fma.cu", "noalloc.cu", "rows.cu", "quant.cu",
            "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-ftz=false", "-prec-div=true", "-prec-sqrt=true"]

@@ -296,10 +296,6 @@ int check_moe(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const 
 }
 
 // ------------------------------------------------------------- CUDA-core path
-// Activation rows up to which a dense NVFP4 call with K % 256 == 0 runs on
-// the CUDA cores (fma.cu) instead of the tensor cores; K % 256 != 0 always
-// does (the tensor path streams 256-K stages).
-constexpr int kFmaMaxM = 0;
 
 struct FmaPlan {
   int grid, rows_per_cta;
@@ -321,7 +317,97 @@ bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
   return true;
 }
 
-bool use_fma(int M, int K) { return K % kStageK != 0 || M <= kFmaMaxM; }
+// Which dense NVFP4 calls run on the CUDA cores (fma.cu) rather than the
+// tensor cores: every K that is not a multiple of 256 (the tensor path
+// streams 256-K stages), and the calls whose weight stream is short enough
+// that the tensor-core kernel's fixed cost (about 13 us a call: tensor-memory
+// allocation, ring fill, split-K drain) outweighs its faster streaming.  The
+// CUDA-core kernel does one FMA per weight and activation row, so its rate
+// falls as M grows.  Measured on GB300, back-to-back calls in a CUDA graph
+// with programmatic dependent launch, K = 2048 (CUDA cores vs tensor cores):
+//   M = 1: 4096 rows 4.1 vs 14.4 us, 16384 rows 8.5 vs 13.5 us,
+//          151,936 rows 53.7 vs 47.3 us;
+//   M = 2: 4096 rows 5.7 vs 14.5 us, 16384 rows 14.2 vs 13.6 us;
+//   M = 4: 4096 rows 9.8 vs 14.7 us, 16384 rows 23.1 vs 13.6 us;
+//   M = 8: 64 rows 8.7 vs 16.8 us, 4096 rows 17.8 vs 18.4 us.
+// Hence: M = 1 up to 128 MiB of weights; 2 <= M <= 8 while M x the weight
+// bytes stay within 32 MiB.
+constexpr double kFmaBytesM1 = 128.0 * (1 << 20);
+constexpr double kFmaRowBytes = 32.0 * (1 << 20);
+
+bool use_fma(int M, int N, int K) {
+  if (K % kStageK) return true;
+  const double bytes = static_cast<double>(N) * K * 9.0 / 16.0;  // codes + block scales
+  if (M == 1) return bytes <= kFmaBytesM1;
+  return M <= 8 && M * bytes <= kFmaRowBytes;
+}
+
+// MoE calls with few tokens run on the CUDA cores (moe_fma.cu): one FMA per
+// weight and (token, slot) pair, no tensor-core pipeline to fill.  Measured
+// on GB300 (256 experts, H = 2048, I = 512, top-8 + shared, back-to-back
+// calls): see the dispatch bound kMoeFmaMaxT.  Shapes: I in {256, 512,
+// 1024} (a down row is 8, 16 or 32 chunks of 32), the staged activation rows
+// within 96 KB of shared memory.
+bool use_moe_fma(int T, int k, int H, int I) {
+  return T <= kMoeFmaMaxT && (I == 256 || I == 512 || I == 1024) &&
+         static_cast<long>(T) * H * 2 <= 96 * 1024 && moe_fma_rounds(k, 1, I) != 0;
+}
+
+size_t moe_fma_ws_bytes(int T, int k, int I) {
+  return round_up(kWsScratch + static_cast<size_t>(T) * (k + 1) * I * 4, 256);
+}
+
+// The MoE layer on the CUDA cores (arguments already checked).
+int moe_fma(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const float* topk_w, int k,
+            const nvfp4_expert_stack* experts, const nvfp4_expert_stack* shared, void* out,
+            int64_t ldo, uint32_t flags, void* workspace, size_t workspace_bytes, int sms,
+            nvfp4_stream_t stream) {
+  const int I = experts->inter;
+  const size_t need = moe_fma_ws_bytes(T, k, I);
+  if (!workspace || workspace_bytes < need)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace needs %zu bytes", need);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  MoeFmaArgs a;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.ldx = ldx;
+  a.ids = topk_ids;
+  a.w = topk_w;
+  a.T = T;
+  a.k = k;
+  a.E = experts->num_experts;
+  a.H = experts->hidden;
+  a.I = I;
+  a.gu_codes = experts->gu_codes;
+  a.gu_scales = experts->gu_scales;
+  a.dn_codes = experts->dn_codes;
+  a.dn_scales = experts->dn_scales;
+  a.gu_global = experts->gu_global;
+  a.dn_global = experts->dn_global;
+  a.has_shared = shared ? 1 : 0;
+  a.s_gu_codes = shared ? shared->gu_codes : nullptr;
+  a.s_gu_scales = shared ? shared->gu_scales : nullptr;
+  a.s_dn_codes = shared ? shared->dn_codes : nullptr;
+  a.s_dn_scales = shared ? shared->dn_scales : nullptr;
+  a.s_gu_global = shared ? shared->gu_global : nullptr;
+  a.s_dn_global = shared ? shared->dn_global : nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.ldo = ldo;
+  a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
+  a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
+  a.h = reinterpret_cast<float*>(ws + kWsScratch);
+  a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
+  const cudaError_t e = launch_moe_fma(a, sms, reinterpret_cast<cudaStream_t>(stream),
+                                       !(flags & NVFP4_FLAG_NO_PDL));
+  if (e != cudaSuccess) return cuda_fail(e, "moe_fma kernels launch");
+  char buf[192];
+  snprintf(buf, sizeof(buf),
+           "moe_fma_gate_up_kernel; moe_fma_down_kernel<%d>; T=%d k=%d E=%d shared=%d rms=%d "
+           "ids_ready=%d",
+           moe_fma_rounds(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready);
+  g_dispatch = buf;
+  return NVFP4_OK;
+}
+
 
 // ------------------------------------------------------------- tcgen05 ops
 // K stages per CTA that a small dense op of a program is cut into (whole
@@ -555,7 +641,7 @@ size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
   int sms = 0;
   if (M < 1 || M > kMaxM || N < 1 || K < 32 || K % 32) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
-  if (use_fma(M, K)) {
+  if (use_fma(M, N, K)) {
     FmaPlan f;
     return plan_fma(M, N, K, sms, &f) ? f.ws_bytes : 0;
   }
@@ -642,7 +728,7 @@ static int gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                        void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
   int rc = check_gemm(A, lda, M, W, C, ldc);
   if (rc) return rc;
-  if (use_fma(M, W->k))
+  if (use_fma(M, W->n, W->k))
     return fma_skinny(A, lda, M, W, C, ldc, argmax_out, am_map, flags, workspace,
                       workspace_bytes, stream);
   return dense_skinny("nvfp4", A, lda, M, dense_w(W), C, ldc, argmax_out, am_map, flags,
@@ -801,6 +887,8 @@ size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* expert
   int sms = 0;
   if (!experts || T < 1 || T > kMaxM || k < 1 || k > 16) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
+  if (use_moe_fma(T, k, experts->hidden, experts->inter))
+    return moe_fma_ws_bytes(T, k, experts->inter);
   TcMoePlan t;
   return plan_tc_moe(T, k, experts->num_experts, experts->hidden, experts->inter, sms, &t)
              ? t.ws_bytes : 0;
@@ -815,6 +903,9 @@ int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
   const int E = experts->num_experts, H = experts->hidden, I = experts->inter;
   int sms = 0;
   if ((rc = current_device(&sms))) return rc;
+  if (use_moe_fma(T, k, H, I))
+    return moe_fma(x, ldx, T, topk_ids, topk_w, k, experts, shared, out, ldo, flags, workspace,
+                   workspace_bytes, sms, stream);
   TcMoePlan p;
   if (!plan_tc_moe(T, k, E, H, I, sms, &p))
     return fail(NVFP4_ERR_SHAPE, "T=%d, H=%d, E=%d: staged activations exceed shared memory",

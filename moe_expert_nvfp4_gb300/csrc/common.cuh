@@ -280,6 +280,77 @@ __device__ __forceinline__ float rms_factor(float sq, int sh, int klen) {
   return exp2i(sh) * rsqrtf(m + scale_pow2(1e-6f, 2 * sh));
 }
 
+// ------------------------------------------------------------------ CUDA-core dot products
+// (the CUDA-core kernels: fma.cu, moe_fma.cu)
+__device__ __forceinline__ float fma_f16(uint32_t a_half_pair, uint32_t b_half_pair, bool hi,
+                                         float c) {
+  float d;
+  if (hi)
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
+        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
+  else
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
+        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f) : "r"(h2));
+  return f;
+}
+
+// Byte offset of 16-byte slot q (0..3) of chunk c of row m in the staged
+// activations: chunks of 64 bytes, slot index xor-ed with (c / 2) % 4 so
+// that the eight lanes of one shared-memory phase (chunks c .. c + 7, same q)
+// hit eight different 16-byte bank groups.
+__device__ __forceinline__ uint32_t act_off(int m, int c, int q, int chunks) {
+  return static_cast<uint32_t>(((m * chunks + c) * 4 + (q ^ ((c >> 1) & 3))) * 16);
+}
+
+// The 32 staged FP16 activations of chunk c of row m (act_off layout) as 16
+// f16x2 words: elements 32 c + 2 i, 2 i + 1 in word i.
+__device__ __forceinline__ void ld_act_chunk(uint32_t xs, int m, int c, int chunks,
+                                             uint32_t (&xv)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = ld_shared_v4(xs + act_off(m, c, q, chunks));
+    xv[4 * q] = v.x;
+    xv[4 * q + 1] = v.y;
+    xv[4 * q + 2] = v.z;
+    xv[4 * q + 3] = v.w;
+  }
+}
+
+// acc + the chunk's dot product: 32 E2M1 codes (16 bytes, low nibble = even
+// k) times the activations xv, one FP32 sum per 16-element block (the
+// products code x activation are exact in FP32), each block sum times its
+// E4M3 scale (the two bytes of sb, low byte first).
+__device__ __forceinline__ float nvfp4_chunk_dot(const uint4& w, uint32_t sb,
+                                                 const uint32_t (&xv)[16], float acc) {
+  uint32_t s2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(static_cast<uint16_t>(sb)));
+  const float sc0 = f16_lo_to_f32(s2), sc1 = f16_lo_to_f32(s2 >> 16);
+  const uint32_t wds[4] = {w.x, w.y, w.z, w.w};
+  uint32_t code[16];
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi)
+    e2m1x8_to_f16x2(wds[wi], code[4 * wi], code[4 * wi + 1], code[4 * wi + 2], code[4 * wi + 3]);
+  float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    b0 = fma_f16(code[e], xv[e], false, b0);
+    b0 = fma_f16(code[e], xv[e], true, b0);
+    b1 = fma_f16(code[8 + e], xv[8 + e], false, b1);
+    b1 = fma_f16(code[8 + e], xv[8 + e], true, b1);
+  }
+  acc = fmaf(sc0, b0, acc);
+  return fmaf(sc1, b1, acc);
+}
+
 // ------------------------------------------------------------------ gpu-scope sync
 // Counter add with acquire-release semantics at GPU scope: after a CTA
 // barrier, one thread's add publishes the CTA's earlier stores (release) and

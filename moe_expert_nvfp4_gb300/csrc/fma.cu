@@ -33,35 +33,6 @@ namespace {
 constexpr int kFmaWarps = 8;
 constexpr int kFmaThreads = kFmaWarps * 32;
 
-__device__ __forceinline__ float fma_f16(uint32_t a_half_pair, uint32_t b_half_pair, bool hi,
-                                         float c) {
-  float d;
-  if (hi)
-    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a1, b1, %3;\n\t}"
-        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
-  else
-    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %1;\n\tmov.b32 {b0, b1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, a0, b0, %3;\n\t}"
-        : "=f"(d) : "r"(a_half_pair), "r"(b_half_pair), "f"(c));
-  return d;
-}
-
-__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
-  float f;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
-      : "=f"(f) : "r"(h2));
-  return f;
-}
-
-// Byte offset of 16-byte slot q (0..3) of chunk c of row m in the staged
-// activations: chunks of 64 bytes, slot index xor-ed with (c / 2) % 4 so
-// that the eight lanes of one shared-memory phase (chunks c .. c + 7, same q)
-// hit eight different 16-byte bank groups.
-__device__ __forceinline__ uint32_t act_off(int m, int c, int q, int chunks) {
-  return static_cast<uint32_t>(((m * chunks + c) * 4 + (q ^ ((c >> 1) & 3))) * 16);
-}
-
 __device__ __forceinline__ bool fm_better(float v, int i, float bv, int bi) {
   return bi == 0x7fffffff || v > bv || (v == bv && i < bi);
 }
@@ -91,14 +62,16 @@ __device__ __forceinline__ float cta_max0(float v, float* s_w) {
 }
 
 // MB activation rows per CTA (rows m0 .. m0 + MB - 1 of A, m0 = MB *
-// blockIdx.y); grid-stride over the weight rows.
+// blockIdx.y); grid-stride over the weight rows.  Two CTAs share an SM (the
+// grid is twice the SM count), hence the register bound.
 template <int MB>
-__global__ void __launch_bounds__(kFmaThreads) fma_kernel(const FmaArgs a) {
+__global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ int s_sh[MB];
   __shared__ float s_rms[MB];
   __shared__ float s_w[kFmaWarps];
   __shared__ float s_bv[kFmaWarps][MB];
+  __shared__ float s_sq[kFmaWarps][MB];
   __shared__ int s_bi[kFmaWarps][MB];
   __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,104 +80,12 @@ __global__ void __launch_bounds__(kFmaThreads) fma_kernel(const FmaArgs a) {
   const int chunks = a.K / 32;
   const uint32_t xs = smem_u32(fsm);
 
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // ---- per row: the largest magnitude and the plain sum of squares, the
-  // FP16 shift and the RMS factor (rows above 2^56 sum their shifted
-  // squares in a second pass: no overflow at any magnitude)
-  for (int r = 0; r < MB; ++r) {
-    float mx = 0.0f, sq = 0.0f;
-    const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + (r < mb ? r : 0)) * a.lda;
-    if (r < mb)
-      for (int v = threadIdx.x; v < a.K / 8; v += kFmaThreads) {
-        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-          mx = fmaxf(mx, fmaxf(fabsf(lo), fabsf(hi)));
-          sq = fmaf(lo, lo, fmaf(hi, hi, sq));
-        }
-      }
-    const float rmax = cta_max0(mx, s_w);
-    const float rsq = cta_sum0(sq, s_w);
-    if (threadIdx.x == 0) {
-      s_sh[r] = r < mb ? f16_row_shift(rmax) : 0;
-      s_rms[r] = (!a.rms || r >= mb) ? 1.0f : (rmax > kSumsqSafeMax ? -1.0f : rms_plain(rsq, a.K));
-    }
-    __syncthreads();
-    if (s_rms[r] < 0.0f) {  // uniform over the CTA
-      const int sh = s_sh[r];
-      const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
-      const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
-      float s3 = 0.0f;
-      for (int v = threadIdx.x; v < a.K / 8; v += kFmaThreads) {
-        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
-          const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
-          s3 = fmaf(lo, lo, fmaf(hi, hi, s3));
-        }
-      }
-      const float s4 = cta_sum0(s3, s_w);
-      if (threadIdx.x == 0) s_rms[r] = rms_factor(s4, sh, a.K);
-      __syncthreads();
-    }
-  }
-  // the shifted FP16 rows: 16-byte slot q of chunk c = elements 32 c + 8 q ..
-  for (int it = threadIdx.x; it < MB * chunks * 4; it += kFmaThreads) {
-    const int r = it / (chunks * 4), rem = it - r * chunks * 4, c = rem >> 2, q = rem & 3;
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (r < mb) {
-      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(row + 32 * c + 8 * q));
-      const int sh = s_sh[r];
-      const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
-      const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
-      const bool two = h1 != sh;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t p[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float lo = __uint_as_float(w[j] << 16) * f1, hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1;
-        if (two) {
-          lo *= f2;
-          hi *= f2;
-        }
-        p[j] = pack_f16x2(lo, hi);
-      }
-      o = make_uint4(p[0], p[1], p[2], p[3]);
-    }
-    st_shared_v4(xs + act_off(r, c, q, chunks), o);
-  }
-  __syncthreads();
-
-  // ---- rows of W
-  // output = (row sum x 2^-shift) x tensor scale x RMS factor, in that order
-  // (the undone shift alone could fall below FP32's range)
-  const float gs = *a.gscale;
-  int shift[MB];
-  float post[MB];
-#pragma unroll
-  for (int r = 0; r < MB; ++r) {
-    shift[r] = s_sh[r];
-    post[r] = a.rms ? s_rms[r] : 1.0f;
-  }
-  float am_v[MB];
-  int am_i[MB];
-#pragma unroll
-  for (int r = 0; r < MB; ++r) {
-    am_v[r] = -FLT_MAX;
-    am_i[r] = 0x7fffffff;
-  }
-  // A warp takes groups of RU consecutive weight rows (group G = the warp's
-  // global index + t * warps); per group the lanes walk the rows' 32-K
-  // chunks in rounds of 32.  The loads of the next round (or group) are
-  // issued before the current one is computed, so RU * 528 bytes per warp
-  // stay in flight.
+  // The weights do not depend on the previous kernel on the stream: the
+  // first group's loads are issued before waiting for it.  A warp takes
+  // groups of RU consecutive weight rows (group G = the warp's global index
+  // + t * warps); per group the lanes walk the rows' 32-K chunks in rounds
+  // of 32.  The loads of the next round (or group) are issued before the
+  // current one is computed, so RU * 528 bytes per warp stay in flight.
   constexpr int RU = 4 / MB;
   const int n_warps = gridDim.x * kFmaWarps;
   const int rounds = (chunks + 31) / 32;
@@ -228,6 +109,148 @@ __global__ void __launch_bounds__(kFmaThreads) fma_kernel(const FmaArgs a) {
     }
   };
   load(G, 0, cw, sb);
+  const float gs = *a.gscale;  // (a weight-side constant too)
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  constexpr int kKeep = 4;  // segments per thread and row kept in registers (K <= 8192)
+  uint4 keep[MB][kKeep];
+  // ---- per row: the largest magnitude and the plain sum of squares in one
+  // pass over all the CTA's rows, one reduction; then the FP16 shift and the
+  // RMS factor (rows above 2^56 sum their shifted squares in a second pass:
+  // no overflow at any magnitude)
+  {
+    float mx[MB], sq[MB];
+#pragma unroll
+    for (int r = 0; r < MB; ++r) {
+      mx[r] = 0.0f;
+      sq[r] = 0.0f;
+      if (r < mb) {
+        const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
+        // 8-element segments v = thread + 256 i: the first kKeep of them
+        // stay in registers for the conversion below
+#pragma unroll
+        for (int i = 0; i < kKeep; ++i) {
+          const int v = threadIdx.x + kFmaThreads * i;
+          keep[r][i] = v < a.K / 8 ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < kKeep; ++i) {
+          const uint32_t w[4] = {keep[r][i].x, keep[r][i].y, keep[r][i].z, keep[r][i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            mx[r] = fmaxf(mx[r], fmaxf(fabsf(lo), fabsf(hi)));
+            sq[r] = fmaf(lo, lo, fmaf(hi, hi, sq[r]));
+          }
+        }
+        for (int v = threadIdx.x + kFmaThreads * kKeep; v < a.K / 8; v += kFmaThreads) {
+          const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+            mx[r] = fmaxf(mx[r], fmaxf(fabsf(lo), fabsf(hi)));
+            sq[r] = fmaf(lo, lo, fmaf(hi, hi, sq[r]));
+          }
+        }
+      }
+      mx[r] = warp_max(mx[r]);
+      sq[r] = warp_sum(sq[r]);
+      if (lane == 0) {
+        s_bv[warp][r] = mx[r];
+        s_sq[warp][r] = sq[r];
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < MB) {
+      const int r = threadIdx.x;
+      float rmax = 0.0f, rsq = 0.0f;
+      for (int w = 0; w < kFmaWarps; ++w) {
+        rmax = fmaxf(rmax, s_bv[w][r]);
+        rsq += s_sq[w][r];
+      }
+      s_sh[r] = r < mb ? f16_row_shift(rmax) : 0;
+      s_rms[r] = (!a.rms || r >= mb) ? 1.0f : (rmax > kSumsqSafeMax ? -1.0f : rms_plain(rsq, a.K));
+    }
+    __syncthreads();
+  }
+  for (int r = 0; r < MB; ++r) {
+    if (s_rms[r] < 0.0f) {  // uniform over the CTA (rare)
+      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
+      const int sh = s_sh[r];
+      const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+      const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+      float s3 = 0.0f;
+      for (int v = threadIdx.x; v < a.K / 8; v += kFmaThreads) {
+        const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+          const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+          s3 = fmaf(lo, lo, fmaf(hi, hi, s3));
+        }
+      }
+      const float s4 = cta_sum0(s3, s_w);
+      if (threadIdx.x == 0) s_rms[r] = rms_factor(s4, sh, a.K);
+      __syncthreads();
+    }
+  }
+  // the shifted FP16 rows: segment v (elements 8 v ..) is 16-byte slot
+  // q = v % 4 of chunk c = v / 4 (elements 32 c ..); rows past the CTA's are
+  // zero
+  auto to_f16 = [&](const uint4 v, int sh) {
+    const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      p[j] = pack_f16x2(__uint_as_float(w[j] << 16) * f1 * f2,
+                        __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
+    return make_uint4(p[0], p[1], p[2], p[3]);
+  };
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    const int sh = s_sh[r];
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) {
+      const int v = threadIdx.x + kFmaThreads * i;
+      if (v < a.K / 8)
+        st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks),
+                     r < mb ? to_f16(keep[r][i], sh) : make_uint4(0u, 0u, 0u, 0u));
+    }
+    for (int v = threadIdx.x + kFmaThreads * kKeep; v < a.K / 8; v += kFmaThreads) {
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (r < mb)
+        o = to_f16(__ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda +
+                                                         8 * v)),
+                   sh);
+      st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks), o);
+    }
+  }
+  __syncthreads();
+
+  // ---- rows of W
+  // output = (row sum x 2^-shift) x tensor scale x RMS factor, in that order
+  // (the undone shift alone could fall below FP32's range)
+  int shift[MB];
+  float post[MB];
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    shift[r] = s_sh[r];
+    post[r] = a.rms ? s_rms[r] : 1.0f;
+  }
+  float am_v[MB];
+  int am_i[MB];
+#pragma unroll
+  for (int r = 0; r < MB; ++r) {
+    am_v[r] = -FLT_MAX;
+    am_i[r] = 0x7fffffff;
+  }
   float acc[MB][RU];
 #pragma unroll
   for (int r = 0; r < MB; ++r)
@@ -242,35 +265,10 @@ __global__ void __launch_bounds__(kFmaThreads) fma_kernel(const FmaArgs a) {
     if (c < chunks) {
 #pragma unroll
       for (int r = 0; r < MB; ++r) {
-        // slots 0, 1: block 0 (k 0..15 of the chunk); slots 2, 3: block 1
-        const uint4 x0 = ld_shared_v4(xs + act_off(r, c, 0, chunks));
-        const uint4 x1 = ld_shared_v4(xs + act_off(r, c, 1, chunks));
-        const uint4 x2 = ld_shared_v4(xs + act_off(r, c, 2, chunks));
-        const uint4 x3 = ld_shared_v4(xs + act_off(r, c, 3, chunks));
-        const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
-                                 x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+        uint32_t xv[16];
+        ld_act_chunk(xs, r, c, chunks, xv);
 #pragma unroll
-        for (int j = 0; j < RU; ++j) {
-          uint32_t s2;
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(static_cast<uint16_t>(sb[j])));
-          const float sc0 = f16_lo_to_f32(s2), sc1 = f16_lo_to_f32(s2 >> 16);
-          const uint32_t wds[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
-          uint32_t code[16];
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi)
-            e2m1x8_to_f16x2(wds[wi], code[4 * wi], code[4 * wi + 1], code[4 * wi + 2],
-                            code[4 * wi + 3]);
-          float b0 = 0.0f, b1 = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            b0 = fma_f16(code[e], xv[e], false, b0);
-            b0 = fma_f16(code[e], xv[e], true, b0);
-            b1 = fma_f16(code[8 + e], xv[8 + e], false, b1);
-            b1 = fma_f16(code[8 + e], xv[8 + e], true, b1);
-          }
-          acc[r][j] = fmaf(sc0, b0, acc[r][j]);
-          acc[r][j] = fmaf(sc1, b1, acc[r][j]);
-        }
+        for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(cw[j], sb[j], xv, acc[r][j]);
       }
     }
     if (cr + 1 == rounds) {  // the group's rows are complete

@@ -194,6 +194,41 @@ struct FmaArgs {
 int fma_rows_per_cta(int M);
 cudaError_t launch_fma(const FmaArgs& a, int grid, cudaStream_t s, bool pdl);
 
+// MoE layer on the CUDA cores (moe_fma.cu) for T <= kMoeFmaMaxT tokens:
+// gate/up + SwiGLU per (token, slot) pair into h, then down + combine.
+constexpr int kMoeFmaMaxT = 8;
+constexpr int kMoeFmaMaxSlots = 17;                      // k <= 16, + shared
+constexpr int kMoeFmaMaxPairs = kMoeFmaMaxT * kMoeFmaMaxSlots;
+struct MoeFmaArgs {
+  const __nv_bfloat16* x;
+  int64_t ldx;
+  const int32_t* ids;  // [T, k]
+  const float* w;      // [T, k]
+  int T, k, E, H, I;
+  const uint8_t* gu_codes;  // routed stack
+  const uint8_t* gu_scales;
+  const uint8_t* dn_codes;
+  const uint8_t* dn_scales;
+  const float* gu_global;
+  const float* dn_global;
+  int has_shared;
+  const uint8_t* s_gu_codes;  // shared expert (when has_shared)
+  const uint8_t* s_gu_scales;
+  const uint8_t* s_dn_codes;
+  const uint8_t* s_dn_scales;
+  const float* s_gu_global;
+  const float* s_dn_global;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  int rms, ids_ready;
+  float* h;  // [T k + T, I] FP32 scratch
+  uint32_t* status;
+};
+// rounds of the down kernel for k slots (+ shared) and inter size I (0 if
+// the kernel does not cover them)
+int moe_fma_rounds(int k, int has_shared, int I);
+cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl);
+
 // Read-only bandwidth probe (probe.cu): reads bytes (a multiple of 16) of
 // buf once; writes one word per CTA (grid words) to sink.
 cudaError_t launch_read_probe(const void* buf, size_t bytes, uint32_t* sink, int grid,

@@ -1,0 +1,436 @@
+// MoE decode layer for a few tokens on the CUDA cores.
+//
+// With T tokens and top-k routing the layer is T * k (+ T shared) pairs of a
+// token and an expert, each a matrix-vector product with one activation row:
+// one FMA per weight, which the CUDA cores issue at several times the HBM
+// rate, and no tensor-memory set-up, ring fill or split-K drain before the
+// first byte.  Two launches:
+//
+//   gate/up: every warp takes (pair, two intermediate columns j, j + 1): the
+//     gate rows j, j + 1 and the up rows I + j, I + j + 1 of the pair's
+//     expert against the token's activation row, then
+//     h[pair][j] = silu(gate) * up in FP32;
+//   down + combine: every warp takes (token, output column n): row n of the
+//     down matrix of each of the token's experts against that pair's h row,
+//     then out[t][n] = bf16(sum over slots, in order, of w * y, the shared
+//     expert's y added last).
+//
+// Activations (BF16 x, FP32 h) are staged in shared memory as FP16 after a
+// power-of-two shift per row that puts the row's largest magnitude in
+// [2^14, 2^15) (exact for BF16 elements within 2^31 of it; one rounding for
+// FP32 h), as on the tensor-core path; codes convert to FP16 exactly and
+// every product code x activation is exact in FP32.  Each output is summed
+// by one warp in a fixed order: deterministic, whatever the grid.
+//
+// Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
+// faster" (decode is a few rows against 4-bit weights); the MoE layer's
+// definition (routed experts, SwiGLU, weighted combine, shared expert) as
+// the tensor-core path.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kMfWarps = 8;
+constexpr int kMfThreads = kMfWarps * 32;
+constexpr int kKeepSeg = 8;  // 8-element segments a lane keeps in registers while staging
+
+// Expert of pair p: its routed id (-1 when outside [0, E): skipped), or E for
+// the shared expert of token p - T k.
+__device__ __forceinline__ int pair_expert(const MoeFmaArgs& a, int p) {
+  const int tk = a.T * a.k;
+  if (p >= tk) return a.E;
+  const int e = __ldcg(a.ids + p);
+  return (e >= 0 && e < a.E) ? e : -1;
+}
+
+__device__ __forceinline__ int pair_token(const MoeFmaArgs& a, int p) {
+  const int tk = a.T * a.k;
+  return p < tk ? p / a.k : p - tk;
+}
+
+// Rows [0, T) of x, shifted to FP16, into xs (act_off layout, H / 32 chunks a
+// row) with s_sh[t] the shift and s_rms[t] the RMS factor (1 without RMS):
+// warp w stages rows w, w + 8, ...
+__device__ __forceinline__ void stage_x_rows(const MoeFmaArgs& a, uint32_t xs, int* s_sh,
+                                             float* s_rms, int warp, int lane) {
+  const int segs = a.H / 8, chunks = a.H / 32;
+  for (int t = warp; t < a.T; t += kMfWarps) {
+    const __nv_bfloat16* row = a.x + static_cast<size_t>(t) * a.ldx;
+    uint4 keep[kKeepSeg];
+#pragma unroll
+    for (int i = 0; i < kKeepSeg; ++i) {
+      const int v = lane + 32 * i;
+      keep[i] = v < segs ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t mx = 0u;
+    float sq = 0.0f;
+    auto stats = [&](const uint4& q) {
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mx = __vmaxu2(mx, w[j] & 0x7FFF7FFFu);
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+        sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kKeepSeg; ++i) stats(keep[i]);
+    for (int v = lane + 32 * kKeepSeg; v < segs; v += 32)
+      stats(__ldcg(reinterpret_cast<const uint4*>(row + 8 * v)));
+    const float m = warp_max(fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u)));
+    const int sh = f16_row_shift(m);
+    const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+    if (a.rms) {
+      if (m > kSumsqSafeMax) {  // (warp-uniform, rare) the shifted squares
+        sq = 0.0f;
+        for (int v = lane; v < segs; v += 32) {
+          const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16) * f1 * f2;
+            const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2;
+            sq = fmaf(lo, lo, fmaf(hi, hi, sq));
+          }
+        }
+      }
+      sq = warp_sum(sq);
+    }
+    if (lane == 0) {
+      s_sh[t] = sh;
+      s_rms[t] = !a.rms ? 1.0f : (m > kSumsqSafeMax ? rms_factor(sq, sh, a.H) : rms_plain(sq, a.H));
+    }
+    auto to_f16 = [&](const uint4& q) {
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = pack_f16x2(__uint_as_float(w[j] << 16) * f1 * f2,
+                          __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
+      return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+#pragma unroll
+    for (int i = 0; i < kKeepSeg; ++i) {
+      const int v = lane + 32 * i;
+      if (v < segs) st_shared_v4(xs + act_off(t, v >> 2, v & 3, chunks), to_f16(keep[i]));
+    }
+    for (int v = lane + 32 * kKeepSeg; v < segs; v += 32)
+      st_shared_v4(xs + act_off(t, v >> 2, v & 3, chunks),
+                   to_f16(__ldcg(reinterpret_cast<const uint4*>(row + 8 * v))));
+  }
+}
+
+// ---------------------------------------------------------------- gate / up
+__global__ void __launch_bounds__(kMfThreads, 2) moe_fma_gate_up_kernel(const MoeFmaArgs a) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  __shared__ int s_e[kMoeFmaMaxPairs];
+  __shared__ float s_g[kMoeFmaMaxPairs];
+  __shared__ int s_sh[kMoeFmaMaxT];
+  __shared__ float s_rms[kMoeFmaMaxT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t xs = smem_u32(msm);
+  const int H = a.H, I = a.I, chunks = H / 32;
+  const int rounds = (chunks + 31) / 32;
+  const int P = a.T * a.k + (a.has_shared ? a.T : 0);
+  const int per_p = I / 2;  // items of a pair: two intermediate columns each
+  const int n_items = P * per_p;
+  const int n_warps = gridDim.x * kMfWarps;
+  const size_t e_codes = static_cast<size_t>(2 * I) * (H / 2);
+  const size_t e_scales = static_cast<size_t>(2 * I) * (H / 16);
+
+  // the pairs' experts and gate/up scales (a bad id sets the status bit once)
+  auto read_pairs = [&]() {
+    for (int p = threadIdx.x; p < P; p += kMfThreads) {
+      const int e = pair_expert(a, p);
+      s_e[p] = e;
+      s_g[p] = e < 0 ? 0.0f : (e == a.E ? *a.s_gu_global : a.gu_global[e]);
+      if (e < 0 && blockIdx.x == 0) atomicOr(a.status, kStatusBadId);
+    }
+    __syncthreads();
+  };
+
+  // item g: the four weight rows gate j, j + 1, up j, j + 1 of pair p's
+  // expert (j = 2 (g % per_p)); round `round` of the K chunks
+  constexpr int RU = 4;
+  auto load = [&](int g, int round, uint4 (&w)[RU], uint32_t (&sc)[RU]) {
+    const int c = round * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < RU; ++j) {
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      sc[j] = 0u;
+    }
+    if (g >= n_items || c >= chunks) return;
+    const int p = g / per_p, j0 = 2 * (g - p * per_p);
+    const int e = s_e[p];
+    if (e < 0) return;
+    const uint8_t* cb = e == a.E ? a.s_gu_codes : a.gu_codes + e * e_codes;
+    const uint8_t* sb = e == a.E ? a.s_gu_scales : a.gu_scales + e * e_scales;
+#pragma unroll
+    for (int j = 0; j < RU; ++j) {
+      const int r = (j < 2 ? 0 : I) + j0 + (j & 1);
+      w[j] = __ldcs(reinterpret_cast<const uint4*>(cb + static_cast<size_t>(r) * (H / 2) + 16 * c));
+      sc[j] = *reinterpret_cast<const uint16_t*>(sb + static_cast<size_t>(r) * (H / 16) + 2 * c);
+    }
+  };
+
+  int G = blockIdx.x * kMfWarps + warp, cr = 0;
+  uint4 cw[RU], nw[RU];
+  uint32_t sb[RU], ns[RU];
+  if (a.ids_ready) {
+    read_pairs();
+    load(G, 0, cw, sb);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!a.ids_ready) {
+    read_pairs();
+    load(G, 0, cw, sb);
+  }
+  stage_x_rows(a, xs, s_sh, s_rms, warp, lane);
+  __syncthreads();
+
+  float acc[RU];
+#pragma unroll
+  for (int j = 0; j < RU; ++j) acc[j] = 0.0f;
+  while (G < n_items) {
+    const int nG = cr + 1 < rounds ? G : G + n_warps;
+    const int ncr = cr + 1 < rounds ? cr + 1 : 0;
+    load(nG, ncr, nw, ns);
+    const int p = G / per_p;
+    const int t = pair_token(a, p);
+    const int c = cr * 32 + lane;
+    if (c < chunks) {
+      uint32_t xv[16];
+      ld_act_chunk(xs, t, c, chunks, xv);
+#pragma unroll
+      for (int j = 0; j < RU; ++j) acc[j] = nvfp4_chunk_dot(cw[j], sb[j], xv, acc[j]);
+    }
+    if (cr + 1 == rounds) {  // the item's rows are complete
+      float tot[RU];
+#pragma unroll
+      for (int j = 0; j < RU; ++j) {
+        tot[j] = warp_sum(acc[j]);
+        acc[j] = 0.0f;
+      }
+      if (lane == 0 && s_e[p] >= 0) {
+        const int j0 = 2 * (G - p * per_p);
+        const float f = s_g[p] * s_rms[t];
+        float hv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float gt = scale_pow2(tot[u], -s_sh[t]) * f;
+          const float up = scale_pow2(tot[2 + u], -s_sh[t]) * f;
+          hv[u] = gt / (1.0f + expf(-gt)) * up;
+        }
+        *reinterpret_cast<float2*>(a.h + static_cast<size_t>(p) * I + j0) = make_float2(hv[0], hv[1]);
+      }
+    }
+    G = nG;
+    cr = ncr;
+#pragma unroll
+    for (int j = 0; j < RU; ++j) {
+      cw[j] = nw[j];
+      sb[j] = ns[j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- down + combine
+// R rounds of 32 lanes cover the token's S slots: lane l takes K chunk
+// l % cpr of slot r * (32 / cpr) + l / cpr in round r (cpr = I / 32 chunks a
+// row, 8, 16 or 32).
+// CTAs per SM the down kernel is built for (its registers grow with R).
+template <int R>
+constexpr int down_ctas_per_sm() { return R <= 5 ? 2 : 1; }
+
+template <int R>
+__global__ void __launch_bounds__(kMfThreads, down_ctas_per_sm<R>())
+    moe_fma_down_kernel(const MoeFmaArgs a) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  __shared__ int s_e[kMoeFmaMaxSlots];
+  __shared__ float s_w[kMoeFmaMaxSlots];
+  __shared__ float s_g[kMoeFmaMaxSlots];
+  __shared__ int s_sh[kMoeFmaMaxSlots];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t xs = smem_u32(msm);
+  const int t = blockIdx.y;
+  const int H = a.H, I = a.I, cpr = I / 32, spr = 32 / cpr;
+  const int S = a.k + (a.has_shared ? 1 : 0);
+  const int c = lane & (cpr - 1), q = lane / cpr;
+  const size_t e_codes = static_cast<size_t>(H) * (I / 2);
+  const size_t e_scales = static_cast<size_t>(H) * (I / 16);
+
+  // The slots' experts, weights and scales.  The ids are complete: this
+  // kernel starts only after the gate/up kernel passed its own wait for the
+  // kernel before it (or, without programmatic launch, after it ended).
+  if (threadIdx.x < S) {
+    const int s = threadIdx.x;
+    if (s < a.k) {
+      const int e = pair_expert(a, t * a.k + s);
+      s_e[s] = e;
+      s_w[s] = __ldcg(a.w + t * a.k + s);
+      s_g[s] = e < 0 ? 0.0f : a.dn_global[e];
+    } else {
+      s_e[s] = a.E;
+      s_w[s] = 1.0f;
+      s_g[s] = *a.s_dn_global;
+    }
+  }
+  __syncthreads();
+
+  auto load = [&](int n, uint4 (&w)[R], uint32_t (&sc)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      w[r] = make_uint4(0u, 0u, 0u, 0u);
+      sc[r] = 0u;
+      const int s = r * spr + q;
+      const int e = (n < H && s < S) ? s_e[s] : -1;
+      if (e >= 0) {
+        const uint8_t* cb = e == a.E ? a.s_dn_codes : a.dn_codes + e * e_codes;
+        const uint8_t* sb = e == a.E ? a.s_dn_scales : a.dn_scales + e * e_scales;
+        w[r] = __ldcs(reinterpret_cast<const uint4*>(cb + static_cast<size_t>(n) * (I / 2) + 16 * c));
+        sc[r] = *reinterpret_cast<const uint16_t*>(sb + static_cast<size_t>(n) * (I / 16) + 2 * c);
+      }
+    }
+  };
+
+  const int n_step = gridDim.x * kMfWarps;
+  int n = blockIdx.x * kMfWarps + warp;
+  uint4 cw[R], nw[R];
+  uint32_t sb[R], ns[R];
+  load(n, cw, sb);
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // the slots' h rows, FP32 -> FP16 times 2^sh (sh from each row's largest
+  // magnitude); warp w takes slots w, w + 8, ...; skipped slots stay unread
+  for (int s = warp; s < S; s += kMfWarps) {
+    if (s_e[s] < 0) continue;
+    const int p = s < a.k ? t * a.k + s : a.T * a.k + t;
+    const float* row = a.h + static_cast<size_t>(p) * I;
+    float m = 0.0f;
+    for (int v = lane; v < I / 4; v += 32) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(row) + v);
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    }
+    const int sh = f16_row_shift(warp_max(m));
+    const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
+    const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
+    if (lane == 0) s_sh[s] = sh;
+    for (int v = lane; v < I / 8; v += 32) {
+      const float4 lo = __ldcg(reinterpret_cast<const float4*>(row) + 2 * v);
+      const float4 hi = __ldcg(reinterpret_cast<const float4*>(row) + 2 * v + 1);
+      const uint4 o = make_uint4(pack_f16x2(lo.x * f1 * f2, lo.y * f1 * f2),
+                                 pack_f16x2(lo.z * f1 * f2, lo.w * f1 * f2),
+                                 pack_f16x2(hi.x * f1 * f2, hi.y * f1 * f2),
+                                 pack_f16x2(hi.z * f1 * f2, hi.w * f1 * f2));
+      st_shared_v4(xs + act_off(s, v >> 2, v & 3, cpr), o);
+    }
+  }
+  __syncthreads();
+
+  while (n < H) {
+    const int nn = n + n_step;
+    load(nn, nw, ns);
+    float acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      acc[r] = 0.0f;
+      const int s = r * spr + q;
+      if (s < S && s_e[s] >= 0) {
+        uint32_t xv[16];
+        ld_act_chunk(xs, s, c, cpr, xv);
+        acc[r] = nvfp4_chunk_dot(cw[r], sb[r], xv, 0.0f);
+      }
+      // the slot's sum over its cpr lanes (every one of them gets it)
+      for (int o = cpr >> 1; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+    }
+    // the combine, slots in order, the shared expert last
+    float out = 0.0f;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      for (int qq = 0; qq < spr; ++qq) {
+        const int s = r * spr + qq;
+        const float tot = __shfl_sync(0xffffffffu, acc[r], qq * cpr);
+        if (s < S && s_e[s] >= 0) {
+          const float y = scale_pow2(tot, -s_sh[s]) * s_g[s];
+          out = s < a.k ? fmaf(s_w[s], y, out) : out + y;
+        }
+      }
+    if (lane == 0) a.out[static_cast<size_t>(t) * a.ldo + n] = __float2bfloat16_rn(out);
+    n = nn;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      cw[r] = nw[r];
+      sb[r] = ns[r];
+    }
+  }
+}
+
+cudaError_t launch_ex(const void* fn, dim3 grid, size_t smem, cudaStream_t s, bool pdl,
+                      const MoeFmaArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kMfThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  void* args[] = {const_cast<MoeFmaArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// down: T rows of CTAs, down_ctas_per_sm<R>() per SM in all
+template <int R>
+cudaError_t launch_down(const MoeFmaArgs& a, int sms, size_t smem, cudaStream_t s, bool pdl) {
+  const void* fn = reinterpret_cast<const void*>(moe_fma_down_kernel<R>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem < 1024 ? 1024 : smem));
+  if (e != cudaSuccess) return e;
+  int gx = (down_ctas_per_sm<R>() * sms + a.T - 1) / a.T;
+  const int cols = (a.H + kMfWarps - 1) / kMfWarps;
+  if (gx > cols) gx = cols;
+  return launch_ex(fn, dim3(gx, a.T), smem, s, pdl, a);
+}
+
+}  // namespace
+
+int moe_fma_rounds(int k, int has_shared, int I) {
+  const int S = k + (has_shared ? 1 : 0), spr = 32 / (I / 32);
+  const int r = (S + spr - 1) / spr;
+  return r <= 2 ? 2 : r <= 3 ? 3 : r <= 5 ? 5 : r <= 9 ? 9 : 0;
+}
+
+cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl) {
+  const int P = a.T * a.k + (a.has_shared ? a.T : 0);
+  // gate/up: one warp an item, at most two CTAs per SM
+  const long items = static_cast<long>(P) * (a.I / 2);
+  const long ctas = (items + kMfWarps - 1) / kMfWarps;
+  const int grid_gu = static_cast<int>(ctas < 2L * sms ? ctas : 2L * sms);
+  const size_t smem_gu = static_cast<size_t>(a.T) * a.H * 2;
+  const void* gu = reinterpret_cast<const void*>(moe_fma_gate_up_kernel);
+  cudaError_t e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_gu < 1024 ? 1024 : smem_gu));
+  if (e != cudaSuccess) return e;
+  if ((e = launch_ex(gu, dim3(grid_gu), smem_gu, s, pdl, a)) != cudaSuccess) return e;
+  const int S = a.k + (a.has_shared ? 1 : 0);
+  const size_t smem_dn = static_cast<size_t>(S) * a.I * 2;
+  switch (moe_fma_rounds(a.k, a.has_shared, a.I)) {
+    case 2: return launch_down<2>(a, sms, smem_dn, s, pdl);
+    case 3: return launch_down<3>(a, sms, smem_dn, s, pdl);
+    case 5: return launch_down<5>(a, sms, smem_dn, s, pdl);
+    case 9: return launch_down<9>(a, sms, smem_dn, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace nvfp4

@@ -121,7 +121,8 @@ class DecodeStep:
             ops.moe(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T], self.experts[l],
                     self.shared[l], out=y, rms_input=True, workspace=ws, pdl=pdl,
                     ids_ready=True)
-            launches += 4
+            # QKV, O, and the MoE layer's two (CUDA cores) or three kernels
+            launches += 4 if ops.last_dispatch().startswith("moe_fma") else 5
             x = y
         ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,
                  pdl=pdl)
@@ -164,9 +165,9 @@ class DecodeStep:
 
     def capture(self, b: dict, pdl: bool = True, prog: "ops.Program" = None) -> torch.cuda.CUDAGraph:
         """Warm up, then capture one step (call by call, or as ``prog``) as a
-        CUDA graph."""
+        CUDA graph; b["launches"] = the kernels one step launches."""
         step = (lambda: self.run(b, pdl)) if prog is None else (lambda: self.run_program(b, prog))
-        step()
+        b["launches"] = step()
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):

@@ -44,12 +44,24 @@ def _bf16(x: np.ndarray) -> torch.Tensor:
 
 
 def _gemm_case(a_host: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, rms=False,
-               argmax=False, what=""):
+               argmax=False, what="", path="call"):
+    """path "call": the single call (these small shapes dispatch to the
+    CUDA-core kernel); "tc": the same GEMM as a one-op program, which always
+    runs on the tensor cores."""
     g = torch.full((1,), synth.GLOBAL_SCALE, dtype=torch.float32, device="cuda")
     W = ops.NVFP4Weight(codes.cuda(), scales.cuda(), g)
     a = a_host.cuda()
-    ws = ops.Workspace(ops.gemm_workspace_bytes(a.shape[0], W.n, W.k))
-    res = ops.gemm(a, W, rms_input=rms, argmax=argmax, workspace=ws)
+    if path == "call":
+        ws = ops.Workspace(ops.gemm_workspace_bytes(a.shape[0], W.n, W.k))
+        res = ops.gemm(a, W, rms_input=rms, argmax=argmax, workspace=ws)
+        assert ops.last_dispatch().startswith("fma_kernel")
+    else:
+        c = torch.empty(a.shape[0], W.n, dtype=torch.bfloat16, device="cuda")
+        am = torch.empty(a.shape[0], dtype=torch.int32, device="cuda") if argmax else None
+        prog = ops.Program([ops.gemm_op(a, W, c, argmax_out=am, rms_input=rms, all_sms=True)])
+        prog.launch()
+        ws = prog.workspace
+        res = (c, am) if argmax else c
     torch.cuda.synchronize()
     assert ws.status() == 0
     a64 = f64(a_host)
@@ -63,18 +75,23 @@ def _gemm_case(a_host: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, 
     return f64(c), ref
 
 
+PATHS = ["call", "tc"]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("rms", [False, True])
-def test_zero_activation_rows(rms):
+def test_zero_activation_rows(rms, path):
     m, n, k = 6, 640, 2048
     codes, scales = synth.nvfp4_weight(41, n, k)
     a = synth.activations_bf16(41, m, k)
     a[1] = 0
     a[4] = 0
-    c, _ = _gemm_case(a, codes, scales, rms=rms, what=f"zero rows rms={rms}")
+    c, _ = _gemm_case(a, codes, scales, rms=rms, what=f"zero rows rms={rms} {path}", path=path)
     assert np.all(c[1] == 0) and np.all(c[4] == 0)
 
 
-def test_rows_at_the_ends_of_bf16_range():
+@pytest.mark.parametrize("path", PATHS)
+def test_rows_at_the_ends_of_bf16_range(path):
     m, n, k = 5, 384, 2048
     codes, scales = synth.nvfp4_weight(42, n, k)
     base = f64(synth.activations_bf16(42, m, k))
@@ -83,21 +100,24 @@ def test_rows_at_the_ends_of_bf16_range():
                   base[2] * 2.0 ** -128,       # most elements BF16 subnormal
                   base[3],
                   base[4] * 2.0 ** 60])
-    _gemm_case(_bf16(a), codes, scales, what="2^110 / 2^-120 / 2^-128 rows")
-    _gemm_case(_bf16(a), codes, scales, rms=True, what="extreme rows, RMS input")
+    _gemm_case(_bf16(a), codes, scales, what=f"2^110 / 2^-120 / 2^-128 rows {path}", path=path)
+    _gemm_case(_bf16(a), codes, scales, rms=True, what=f"extreme rows, RMS input {path}",
+               path=path)
 
 
-def test_row_with_2_pow_60_dynamic_range():
+@pytest.mark.parametrize("path", PATHS)
+def test_row_with_2_pow_60_dynamic_range(path):
     m, n, k = 3, 512, 2048
     codes, scales = synth.nvfp4_weight(43, n, k)
     base = f64(synth.activations_bf16(43, m, k))
     tiers = 2.0 ** (-np.arange(k) % 61)          # magnitudes 2^0 .. 2^-60 along the row
     a = base * tiers[None, :]
-    _gemm_case(_bf16(a), codes, scales, what="2^60 range")
+    _gemm_case(_bf16(a), codes, scales, what=f"2^60 range {path}", path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("codes_kind", ["pm6", "all16"])
-def test_every_finite_e4m3_scale(codes_kind):
+def test_every_finite_e4m3_scale(codes_kind, path):
     """Scales cycle through 0x01..0x7E (126 finite positive codes, subnormal
     to 448); codes are +-6 (0x7 / 0xF) or all 16 codes."""
     m, n, k = 8, 1000, 2048
@@ -112,7 +132,7 @@ def test_every_finite_e4m3_scale(codes_kind):
         hi = 0x7 | (sign[..., 1] << 3)
         codes = (lo | (hi << 4)).to(torch.uint8)
     _gemm_case(synth.activations_bf16(44, m, k), codes, scales, argmax=True,
-               what=f"all E4M3 scales, codes {codes_kind}")
+               what=f"all E4M3 scales, codes {codes_kind} {path}", path=path)
 
 
 @pytest.fixture(scope="module")
@@ -134,13 +154,22 @@ def layer_zero_gates():
     return ex, sh, host
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("t", [1, 8, 32])
-def test_moe_all_zero_h_rows(layer_zero_gates, t):
+def test_moe_all_zero_h_rows(layer_zero_gates, t, path):
+    """path "call": the single call (CUDA-core kernels up to 8 tokens);
+    "tc": a one-op program (the tensor-core kernels at every T)."""
     ex, sh, get = layer_zero_gates
     x = synth.activations_bf16(45, t, H)
     ids, w = ops.route(synth.router_logits(45, t, E).cuda(), TOPK)
-    ws = ops.Workspace(ops.moe_workspace_bytes(t, TOPK, ex))
-    out = ops.moe(x.cuda(), ids, w, ex, sh, workspace=ws)
+    if path == "call":
+        ws = ops.Workspace(ops.moe_workspace_bytes(t, TOPK, ex))
+        out = ops.moe(x.cuda(), ids, w, ex, sh, workspace=ws)
+    else:
+        out = torch.empty(t, H, dtype=torch.bfloat16, device="cuda")
+        prog = ops.Program([ops.moe_op(x.cuda(), ids, w, ex, out, shared=sh)])
+        prog.launch()
+        ws = prog.workspace
     torch.cuda.synchronize()
     assert ws.status() == 0
     ref = O.moe_decode_bf16(f64(x), ids.cpu().numpy(), w.cpu().double().numpy(), get, E, get(E))
@@ -149,6 +178,7 @@ def test_moe_all_zero_h_rows(layer_zero_gates, t):
 
 @pytest.mark.parametrize("rms", [False, True])
 def test_moe_zero_token_row(rms):
+    """(8 tokens: the CUDA-core MoE kernels.)"""
     ex = device_experts(4, 0, E, H, I)
     sh = device_shared(4, 0, E, H, I)
     get = host_expert_fn(4, 0, H, I)

@@ -41,10 +41,35 @@ def test_generator_bytes_identical_on_device_and_host():
 
 
 def test_projection_2048_to_64_m4():
-    c, ref, disp, _ = _case(0, 4, 64, 2048)
+    c, ref, disp, (W, a, _) = _case(0, 4, 64, 2048)
     assert_close(f64(c), O.bf16_round(ref), "2048->64")
-    assert "grid=8 " in disp and "units_per_cta=1.00" in disp   # split-K over 8 CTAs
-    assert disp.startswith("stream_tc_kernel<dense>")
+    assert disp.startswith("fma_kernel")                 # small: the CUDA-core kernel
+    # the tensor-core kernel on the same call (a one-op program splits it
+    # over 8 CTAs exactly as the call would)
+    out = torch.empty_like(c)
+    prog = ops.Program([ops.gemm_op(a, W, out, all_sms=True)])
+    prog.launch()
+    torch.cuda.synchronize()
+    assert prog.workspace.status() == 0
+    assert_close(f64(out), O.bf16_round(ref), "2048->64 tensor cores")
+
+
+@pytest.mark.parametrize("m,n,k,kernel", [(1, 4096, 2048, "fma_kernel"),
+                                          (1, 151936, 2048, "stream_tc_kernel"),
+                                          (2, 4096, 2048, "fma_kernel"),
+                                          (2, 16384, 2048, "stream_tc_kernel"),
+                                          (8, 3000, 2048, "fma_kernel"),
+                                          (8, 4096, 2048, "stream_tc_kernel"),
+                                          (9, 64, 2048, "stream_tc_kernel")])
+def test_dispatch_by_shape(m, n, k, kernel):
+    """The CUDA cores take M = 1 up to 128 MiB of weights and 2 <= M <= 8 up
+    to 32 MiB x M; the tensor cores the rest (K % 256 == 0)."""
+    ws = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
+    W = device_weight(30, n, k)
+    a = synth.activations_bf16(30, m, k).cuda()
+    ops.gemm(a, W, workspace=ws)
+    assert ops.last_dispatch().startswith(kernel)
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("m", [1, 4, 8, 16, 32])

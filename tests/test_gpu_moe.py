@@ -90,8 +90,45 @@ def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
 def test_moe_layer_35b_shape(layer4, t):
     out, ref, disp, status, _ = _moe_case(layer4, t)
     assert status == 0
-    assert "shared=1" in disp and disp.startswith("stream_tc_kernel<gate_up>")
+    # up to 8 tokens the CUDA-core kernels, beyond them the tensor cores
+    kernel = "moe_fma_gate_up_kernel" if t <= 8 else "stream_tc_kernel<gate_up>"
+    assert "shared=1" in disp and disp.startswith(kernel)
     assert_close(f64(out), O.bf16_round(ref), f"MoE T={t}")
+
+
+@pytest.mark.parametrize("t", [1, 4, 8])
+def test_moe_layer_on_the_tensor_cores_few_tokens(layer4, t):
+    """The tensor-core MoE kernels at few tokens (a one-op program, which
+    always runs them), against the oracle."""
+    ex, sh, get = layer4
+    x = synth.activations_bf16(4, 32, H, 1)[:t].cuda()
+    ids, w = ops.route(synth.router_logits(4, 32, E, 1)[:t].cuda(), K)
+    out = torch.empty(t, H, dtype=torch.bfloat16, device="cuda")
+    prog = ops.Program([ops.moe_op(x, ids, w, ex, out, shared=sh)])
+    prog.launch()
+    torch.cuda.synchronize()
+    assert prog.workspace.status() == 0
+    ref = O.moe_decode64(f64(x), ids.cpu().numpy(), w.cpu().double().numpy(), get, E, get(E))
+    assert_close(f64(out), O.bf16_round(ref), f"tensor-core MoE T={t}")
+
+
+@pytest.mark.parametrize("e,h,i,k,t,shared", [(64, 1024, 256, 16, 3, True),   # 8 chunks a row, R = 5
+                                              (64, 1024, 1024, 8, 2, True),   # 32 chunks, R = 9
+                                              (64, 2048, 512, 4, 8, False),   # R = 2
+                                              (32, 768, 256, 1, 5, True),     # k = 1
+                                              (64, 4096, 512, 16, 8, True)])  # 64 KB of x rows
+def test_moe_cuda_core_kernels_other_shapes(e, h, i, k, t, shared):
+    ex = device_experts(6, 1, e, h, i)
+    sh = device_shared(6, 1, e, h, i) if shared else None
+    get = host_expert_fn(6, 1, h, i)
+    x = synth.activations_bf16(6, t, h, 2)
+    ids, w = ops.route(synth.router_logits(6, t, e, 2).cuda(), k)
+    out = ops.moe(x.cuda(), ids, w, ex, sh, rms_input=True)
+    assert ops.last_dispatch().startswith("moe_fma_gate_up_kernel")
+    torch.cuda.synchronize()
+    ref = O.moe_decode64(O.rms_scale(f64(x)), ids.cpu().numpy(), w.cpu().double().numpy(), get, e,
+                         get(e) if shared else None)
+    assert_close(f64(out), O.bf16_round(ref), f"CUDA-core MoE E={e} H={h} I={i} k={k} T={t}")
 
 
 def test_moe_without_shared_expert(layer4):
@@ -212,9 +249,10 @@ def test_mtp_verify_batch_moe_then_lm_head_argmax():
 
 def test_one_workspace_serves_moe_then_split_k_gemm(layer4):
     """A dense split-K GEMM after an MoE call on the same workspace: the MoE
-    scratch must not disturb the GEMM's tile counters."""
+    scratch must not disturb the GEMM's tile counters (T = 16: both on the
+    tensor cores)."""
     ex, sh, _ = layer4
-    t = 4
+    t = 16
     W = device_weight(21, 5120, H)
     ws = ops.Workspace(max(ops.gemm_workspace_bytes(t, 5120, H), ops.moe_workspace_bytes(t, K, ex)))
     x = synth.activations_bf16(21, t, H).cuda()
