@@ -49,9 +49,10 @@ def parse():
     p.add_argument("--profile", default=None, metavar="WORKLOAD",
                    help="run one workload's calls a few times and exit (for ncu captures): "
                         "dense:N:K:M, head:M, moe:T, fp8:N:K:M, bf16w:N:K:M")
-    p.add_argument("--path", default="program", choices=["program", "calls"],
+    p.add_argument("--path", default="auto", choices=["auto", "program", "calls"],
                    help="program: the step as one persistent launch after routing; calls: one "
-                        "kernel launch per call")
+                        "kernel launch per call; auto: the step's own choice for its token "
+                        "count (DecodeStep.path_for)")
     return p.parse_args()
 
 
@@ -583,8 +584,11 @@ def run_ours(args, rank, world, local):
         if dist is not None:
             dist.barrier()
 
+    def path_of(t):
+        return model.path_for(t) if args.path == "auto" else args.path
+
     def one_config(t, steps, warmup, sample_clocks, path=None):
-        path = path or args.path
+        path = path or path_of(t)
         b = model.buffers(t)
         x, lg = model.inputs(t)
         b["x"].copy_(x)
@@ -654,7 +658,8 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peak()
     peak_src = (f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s")
-    if args.path == "program":
+    path = path_of(t)
+    if path == "program":
         # the program kernel: every projection, MoE layer and the head of the step
         kg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(kg):
@@ -698,24 +703,30 @@ def run_ours(args, rank, world, local):
     # ---- other token counts of the same step (context)
     sweep = {}
     if not args.no_sweep:
-        for tt in (1, 8, 32):
+        for tt in (1, 2, 4, 8, 16, 32):
             if tt == t:
                 sweep[str(tt)] = {"us_per_step": ms * 1e3, "gbs": nbytes / (ms * 1e-3) / 1e9,
-                                  "weight_bytes": nbytes}
+                                  "weight_bytes": nbytes, "path": path}
                 continue
-            _, g2, _, _, ms2, nb2, _ = one_config(tt, max(5, min(args.steps, 100)), 3, False)
-            sweep[str(tt)] = {"us_per_step": ms2 * 1e3, "gbs": nb2 / (ms2 * 1e-3) / 1e9,
-                              "weight_bytes": nb2}
-            del g2
+            # both ways for the token counts around the switch, else the chosen one
+            paths = ("calls", "program") if tt in (2, 4, 8, 16) else (path_of(tt),)
+            for pth in paths:
+                _, g2, _, _, ms2, nb2, _ = one_config(tt, max(5, min(args.steps, 100)), 3, False,
+                                                      pth)
+                key = str(tt) if pth == path_of(tt) else f"{tt}_{pth}"
+                sweep[key] = {"us_per_step": ms2 * 1e3, "gbs": nb2 / (ms2 * 1e-3) / 1e9,
+                              "weight_bytes": nb2, "path": pth}
+                del g2
 
     # ---- the other workloads of the metric (context: µs and GB/s per call)
     workloads = workload_table(model) if not args.no_sweep else None
 
     # ---- the same step issued call by call (one kernel per call), for context
     calls = None
-    if args.path == "program" and not args.no_sweep:
-        b3, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, "calls")
-        calls = {"us_per_step": ms3 * 1e3, "gbs": nb3 / (ms3 * 1e-3) / 1e9,
+    if not args.no_sweep:
+        other = "calls" if path == "program" else "program"
+        b3, g3, _, _, ms3, nb3, _ = one_config(t, max(5, min(args.steps, 100)), 3, False, other)
+        calls = {"path": other, "us_per_step": ms3 * 1e3, "gbs": nb3 / (ms3 * 1e-3) / 1e9,
                  "launches_per_step": b3["launches"]}
         del g3
 
@@ -748,7 +759,7 @@ def run_ours(args, rank, world, local):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": n_launch * args.steps, "clocks": clocks,
             "step_spread": b["spread"], "versions": versions(), "sweep": sweep,
-            "path": args.path, "call_by_call": calls, "workloads": workloads,
+            "path": path, "other_path": calls, "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -298,7 +298,7 @@ int check_moe(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const 
 // ------------------------------------------------------------- CUDA-core path
 
 struct FmaPlan {
-  int grid, rows_per_cta;
+  int grid, rows_per_cta, ru;
   size_t smem, off_am, ws_bytes;
 };
 
@@ -306,7 +306,7 @@ bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
   p->rows_per_cta = fma_rows_per_cta(M);
   p->smem = static_cast<size_t>(p->rows_per_cta) * (K / 32) * 64;
   if (p->smem > 200 * 1024) return false;
-  const int ru = 4 / p->rows_per_cta;           // weight rows a warp takes at once
+  const int ru = p->ru = fma_rows_per_warp(p->rows_per_cta, N);  // rows a warp takes at once
   const long groups = (static_cast<long>(N) + ru - 1) / ru;
   const long ctas = (groups + 7) / 8;           // eight warps a CTA
   p->grid = static_cast<int>(ctas < 2L * sms ? ctas : 2L * sms);
@@ -350,7 +350,7 @@ bool use_fma(int M, int N, int K) {
 // within 96 KB of shared memory.
 bool use_moe_fma(int T, int k, int H, int I) {
   return T <= kMoeFmaMaxT && (I == 256 || I == 512 || I == 1024) &&
-         static_cast<long>(T) * H * 2 <= 96 * 1024 && moe_fma_rounds(k, 1, I) != 0;
+         static_cast<long>(T) * H * 2 <= 96 * 1024 && moe_fma_slots(k, 1, I) != 0;
 }
 
 size_t moe_fma_ws_bytes(int T, int k, int I) {
@@ -401,9 +401,9 @@ int moe_fma(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const fl
   if (e != cudaSuccess) return cuda_fail(e, "moe_fma kernels launch");
   char buf[192];
   snprintf(buf, sizeof(buf),
-           "moe_fma_gate_up_kernel; moe_fma_down_kernel<%d>; T=%d k=%d E=%d shared=%d rms=%d "
+           "moe_fma_gate_up_kernel; moe_fma_down_kernel slots=%d; T=%d k=%d E=%d shared=%d rms=%d "
            "ids_ready=%d",
-           moe_fma_rounds(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready);
+           moe_fma_slots(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready);
   g_dispatch = buf;
   return NVFP4_OK;
 }
@@ -712,12 +712,13 @@ static int fma_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
-  const cudaError_t e = launch_fma(a, p.grid, reinterpret_cast<cudaStream_t>(stream),
+  const cudaError_t e = launch_fma(a, p.grid, p.ru, reinterpret_cast<cudaStream_t>(stream),
                                    !(flags & NVFP4_FLAG_NO_PDL));
   if (e != cudaSuccess) return cuda_fail(e, "fma_kernel launch");
   char buf[192];
-  snprintf(buf, sizeof(buf), "fma_kernel grid=%dx%d rows_per_cta=%d smem=%zu argmax=%d rms=%d",
-           p.grid, (M + p.rows_per_cta - 1) / p.rows_per_cta, p.rows_per_cta, p.smem,
+  snprintf(buf, sizeof(buf),
+           "fma_kernel grid=%dx%d rows_per_cta=%d rows_per_warp=%d smem=%zu argmax=%d rms=%d",
+           p.grid, (M + p.rows_per_cta - 1) / p.rows_per_cta, p.rows_per_cta, p.ru, p.smem,
            argmax_out ? 1 : 0, a.rms);
   g_dispatch = buf;
   return NVFP4_OK;

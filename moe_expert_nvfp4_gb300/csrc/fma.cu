@@ -64,7 +64,7 @@ __device__ __forceinline__ float cta_max0(float v, float* s_w) {
 // MB activation rows per CTA (rows m0 .. m0 + MB - 1 of A, m0 = MB *
 // blockIdx.y); grid-stride over the weight rows.  Two CTAs share an SM (the
 // grid is twice the SM count), hence the register bound.
-template <int MB>
+template <int MB, int RU>
 __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ int s_sh[MB];
@@ -86,7 +86,6 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   // + t * warps); per group the lanes walk the rows' 32-K chunks in rounds
   // of 32.  The loads of the next round (or group) are issued before the
   // current one is computed, so RU * 528 bytes per warp stay in flight.
-  constexpr int RU = 4 / MB;
   const int n_warps = gridDim.x * kFmaWarps;
   const int rounds = (chunks + 31) / 32;
   const int n_groups = (a.N + RU - 1) / RU;
@@ -366,10 +365,11 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   if (threadIdx.x == 0) a.argmax_cnt[blockIdx.y] = 0u;
 }
 
-template <int MB>
+template <int MB, int RU>
 cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
   const size_t smem = static_cast<size_t>(MB) * (a.K / 32) * 64;
-  cudaError_t e = cudaFuncSetAttribute(fma_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fma_kernel<MB, RU>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem < 1024 ? 1024 : smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -382,18 +382,37 @@ cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fma_kernel<MB>, a);
+  return cudaLaunchKernelEx(&cfg, fma_kernel<MB, RU>, a);
 }
 
 }  // namespace
 
 int fma_rows_per_cta(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : 4); }
 
-cudaError_t launch_fma(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
-  switch (fma_rows_per_cta(a.M)) {
-    case 1: return launch_mb<1>(a, grid, s, pdl);
-    case 2: return launch_mb<2>(a, grid, s, pdl);
-    default: return launch_mb<4>(a, grid, s, pdl);
+// Rows a warp takes at once.  More rows keep more bytes in flight per warp
+// but leave fewer warps a group when N is small.  Measured on GB300 (K =
+// 2048 unless stated, back-to-back calls, us for rows a warp = 2 / 4 / 8):
+//   M = 1: 2048 x 4096 4.28 / 4.85 / 6.34; 4096 rows 4.02 / 3.51 / 4.62;
+//          8192 rows 5.85 / 4.19 / 5.21; 16384 rows 9.13 / 6.58 / 6.43;
+//          32768 rows 14.72 / 11.15 / 10.85;
+//   M = 2 (1 / 2 / 4): 4096 rows 5.38 / 4.63 / 5.05; 8192 rows 8.02 / 6.83 / 6.58;
+//   M = 4 (1 / 2): 4096 rows 8.29 / 7.77; 5120 rows 9.73 / 9.48.
+int fma_rows_per_warp(int rows_per_cta, int N) {
+  // (thresholds for GB300's 152 SMs)
+  if (rows_per_cta == 1) return N < 3072 ? 2 : (N < 12288 ? 4 : 8);
+  if (rows_per_cta == 2) return N < 6144 ? 2 : 4;
+  return 2;
+}
+
+cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool pdl) {
+  switch (fma_rows_per_cta(a.M) * 16 + ru) {
+    case 16 + 8: return launch_mb<1, 8>(a, grid, s, pdl);
+    case 16 + 4: return launch_mb<1, 4>(a, grid, s, pdl);
+    case 16 + 2: return launch_mb<1, 2>(a, grid, s, pdl);
+    case 32 + 4: return launch_mb<2, 4>(a, grid, s, pdl);
+    case 32 + 2: return launch_mb<2, 2>(a, grid, s, pdl);
+    case 64 + 2: return launch_mb<4, 2>(a, grid, s, pdl);
+    default: return cudaErrorInvalidValue;
   }
 }
 

@@ -192,7 +192,10 @@ struct FmaArgs {
 };
 // activation rows per CTA for M rows (1, 2 or 4); grid.y = ceil(M / that)
 int fma_rows_per_cta(int M);
-cudaError_t launch_fma(const FmaArgs& a, int grid, cudaStream_t s, bool pdl);
+// weight rows a warp of that kernel takes at once (its loads in flight:
+// this many times 528 bytes per 32-K round at K = 2048), for N weight rows
+int fma_rows_per_warp(int rows_per_cta, int N);
+cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool pdl);
 
 // MoE layer on the CUDA cores (moe_fma.cu) for T <= kMoeFmaMaxT tokens:
 // gate/up + SwiGLU per (token, slot) pair into h, then down + combine.
@@ -224,9 +227,9 @@ struct MoeFmaArgs {
   float* h;  // [T k + T, I] FP32 scratch
   uint32_t* status;
 };
-// rounds of the down kernel for k slots (+ shared) and inter size I (0 if
-// the kernel does not cover them)
-int moe_fma_rounds(int k, int has_shared, int I);
+// slots of a token (k + shared) when the down kernel covers them and the
+// inter size I, else 0
+int moe_fma_slots(int k, int has_shared, int I);
 cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl);
 
 // Read-only bandwidth probe (probe.cu): reads bytes (a multiple of 16) of

@@ -242,27 +242,28 @@ __global__ void __launch_bounds__(kMfThreads, 2) moe_fma_gate_up_kernel(const Mo
 }
 
 // ---------------------------------------------------------------- down + combine
-// R rounds of 32 lanes cover the token's S slots: lane l takes K chunk
-// l % cpr of slot r * (32 / cpr) + l / cpr in round r (cpr = I / 32 chunks a
-// row, 8, 16 or 32).
-// CTAs per SM the down kernel is built for (its registers grow with R).
-template <int R>
-constexpr int down_ctas_per_sm() { return R <= 5 ? 2 : 1; }
+// A warp takes 32 / cpr output columns n of one token (cpr = I / 32 chunks
+// a down row: 8, 16 or 32); lane l works on column l / cpr, K chunk l % cpr,
+// of every slot's row: the loads of all the token's slots are in flight at
+// once, each slot's sum is reduced over the column's cpr lanes, and the
+// combine runs in every lane of the column in slot order (the shared expert
+// last).  Slots go in batches of kSlotBatch (one batch for k <= 8 with the
+// shared expert).
+constexpr int kSlotBatch = 9;
 
-template <int R>
-__global__ void __launch_bounds__(kMfThreads, down_ctas_per_sm<R>())
-    moe_fma_down_kernel(const MoeFmaArgs a) {
+__global__ void __launch_bounds__(kMfThreads, 2) moe_fma_down_kernel(const MoeFmaArgs a) {
   extern __shared__ __align__(16) uint8_t msm[];
   __shared__ int s_e[kMoeFmaMaxSlots];
   __shared__ float s_w[kMoeFmaMaxSlots];
   __shared__ float s_g[kMoeFmaMaxSlots];
-  __shared__ int s_sh[kMoeFmaMaxSlots];
+  __shared__ float s_f1[kMoeFmaMaxSlots];
+  __shared__ float s_f2[kMoeFmaMaxSlots];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t xs = smem_u32(msm);
   const int t = blockIdx.y;
-  const int H = a.H, I = a.I, cpr = I / 32, spr = 32 / cpr;
+  const int H = a.H, I = a.I, cpr = I / 32, cols = 32 / cpr;
   const int S = a.k + (a.has_shared ? 1 : 0);
-  const int c = lane & (cpr - 1), q = lane / cpr;
+  const int c = lane & (cpr - 1), col = lane / cpr;
   const size_t e_codes = static_cast<size_t>(H) * (I / 2);
   const size_t e_scales = static_cast<size_t>(H) * (I / 16);
 
@@ -284,27 +285,28 @@ __global__ void __launch_bounds__(kMfThreads, down_ctas_per_sm<R>())
   }
   __syncthreads();
 
-  auto load = [&](int n, uint4 (&w)[R], uint32_t (&sc)[R]) {
+  // row n's chunk c of the down matrices of slots b .. b + kSlotBatch - 1
+  auto load = [&](int n, int b, uint4 (&w)[kSlotBatch], uint32_t (&sc)[kSlotBatch]) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      w[r] = make_uint4(0u, 0u, 0u, 0u);
-      sc[r] = 0u;
-      const int s = r * spr + q;
+    for (int j = 0; j < kSlotBatch; ++j) {
+      const int s = b + j;
+      w[j] = make_uint4(0u, 0u, 0u, 0u);
+      sc[j] = 0u;
       const int e = (n < H && s < S) ? s_e[s] : -1;
       if (e >= 0) {
         const uint8_t* cb = e == a.E ? a.s_dn_codes : a.dn_codes + e * e_codes;
         const uint8_t* sb = e == a.E ? a.s_dn_scales : a.dn_scales + e * e_scales;
-        w[r] = __ldcs(reinterpret_cast<const uint4*>(cb + static_cast<size_t>(n) * (I / 2) + 16 * c));
-        sc[r] = *reinterpret_cast<const uint16_t*>(sb + static_cast<size_t>(n) * (I / 16) + 2 * c);
+        w[j] = __ldcs(reinterpret_cast<const uint4*>(cb + static_cast<size_t>(n) * (I / 2) + 16 * c));
+        sc[j] = *reinterpret_cast<const uint16_t*>(sb + static_cast<size_t>(n) * (I / 16) + 2 * c);
       }
     }
   };
 
-  const int n_step = gridDim.x * kMfWarps;
-  int n = blockIdx.x * kMfWarps + warp;
-  uint4 cw[R], nw[R];
-  uint32_t sb[R], ns[R];
-  load(n, cw, sb);
+  const int n_step = gridDim.x * kMfWarps * cols;
+  int n = (blockIdx.x * kMfWarps + warp) * cols + col;
+  uint4 cw[kSlotBatch];
+  uint32_t sb[kSlotBatch];
+  load(n, 0, cw, sb);
   pdl_wait();
   pdl_launch_dependents();
 
@@ -322,7 +324,11 @@ __global__ void __launch_bounds__(kMfThreads, down_ctas_per_sm<R>())
     const int sh = f16_row_shift(warp_max(m));
     const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
     const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
-    if (lane == 0) s_sh[s] = sh;
+    if (lane == 0) {  // the factors that undo the shift, in the same two steps
+      const int u1 = -sh / 2;
+      s_f1[s] = exp2i(u1);
+      s_f2[s] = exp2i(-sh - u1);
+    }
     for (int v = lane; v < I / 8; v += 32) {
       const float4 lo = __ldcg(reinterpret_cast<const float4*>(row) + 2 * v);
       const float4 hi = __ldcg(reinterpret_cast<const float4*>(row) + 2 * v + 1);
@@ -335,41 +341,28 @@ __global__ void __launch_bounds__(kMfThreads, down_ctas_per_sm<R>())
   }
   __syncthreads();
 
-  while (n < H) {
-    const int nn = n + n_step;
-    load(nn, nw, ns);
-    float acc[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      acc[r] = 0.0f;
-      const int s = r * spr + q;
-      if (s < S && s_e[s] >= 0) {
-        uint32_t xv[16];
-        ld_act_chunk(xs, s, c, cpr, xv);
-        acc[r] = nvfp4_chunk_dot(cw[r], sb[r], xv, 0.0f);
-      }
-      // the slot's sum over its cpr lanes (every one of them gets it)
-      for (int o = cpr >> 1; o > 0; o >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-    }
-    // the combine, slots in order, the shared expert last
+  while (true) {
+    // (uniform over the warp: the warp's columns are consecutive)
+    if (__shfl_sync(0xffffffffu, n, 0) >= H) break;
     float out = 0.0f;
+    for (int b = 0; b < S; b += kSlotBatch) {
+      if (b > 0) load(n, b, cw, sb);
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-      for (int qq = 0; qq < spr; ++qq) {
-        const int s = r * spr + qq;
-        const float tot = __shfl_sync(0xffffffffu, acc[r], qq * cpr);
-        if (s < S && s_e[s] >= 0) {
-          const float y = scale_pow2(tot, -s_sh[s]) * s_g[s];
+      for (int j = 0; j < kSlotBatch; ++j) {
+        const int s = b + j;
+        if (s < S && s_e[s] >= 0) {  // uniform
+          uint32_t xv[16];
+          ld_act_chunk(xs, s, c, cpr, xv);
+          float d = nvfp4_chunk_dot(cw[j], sb[j], xv, 0.0f);
+          for (int o = cpr >> 1; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          const float y = ((d * s_f1[s]) * s_f2[s]) * s_g[s];
           out = s < a.k ? fmaf(s_w[s], y, out) : out + y;
         }
       }
-    if (lane == 0) a.out[static_cast<size_t>(t) * a.ldo + n] = __float2bfloat16_rn(out);
-    n = nn;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      cw[r] = nw[r];
-      sb[r] = ns[r];
     }
+    if (c == 0 && n < H) a.out[static_cast<size_t>(t) * a.ldo + n] = __float2bfloat16_rn(out);
+    n += n_step;
+    load(n, 0, cw, sb);
   }
 }
 
@@ -389,25 +382,25 @@ cudaError_t launch_ex(const void* fn, dim3 grid, size_t smem, cudaStream_t s, bo
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// down: T rows of CTAs, down_ctas_per_sm<R>() per SM in all
-template <int R>
+// down: T rows of CTAs, two CTAs per SM in all
 cudaError_t launch_down(const MoeFmaArgs& a, int sms, size_t smem, cudaStream_t s, bool pdl) {
-  const void* fn = reinterpret_cast<const void*>(moe_fma_down_kernel<R>);
+  const void* fn = reinterpret_cast<const void*>(moe_fma_down_kernel);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem < 1024 ? 1024 : smem));
   if (e != cudaSuccess) return e;
-  int gx = (down_ctas_per_sm<R>() * sms + a.T - 1) / a.T;
-  const int cols = (a.H + kMfWarps - 1) / kMfWarps;
-  if (gx > cols) gx = cols;
+  const int per_warp = 32 / (a.I / 32);  // columns a warp
+  int gx = (2 * sms + a.T - 1) / a.T;
+  const int need = (a.H + kMfWarps * per_warp - 1) / (kMfWarps * per_warp);
+  if (gx > need) gx = need;
   return launch_ex(fn, dim3(gx, a.T), smem, s, pdl, a);
 }
 
 }  // namespace
 
-int moe_fma_rounds(int k, int has_shared, int I) {
-  const int S = k + (has_shared ? 1 : 0), spr = 32 / (I / 32);
-  const int r = (S + spr - 1) / spr;
-  return r <= 2 ? 2 : r <= 3 ? 3 : r <= 5 ? 5 : r <= 9 ? 9 : 0;
+int moe_fma_slots(int k, int has_shared, int I) {
+  if (I != 256 && I != 512 && I != 1024) return 0;
+  const int S = k + (has_shared ? 1 : 0);
+  return S <= kMoeFmaMaxSlots ? S : 0;
 }
 
 cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl) {
@@ -424,13 +417,8 @@ cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pd
   if ((e = launch_ex(gu, dim3(grid_gu), smem_gu, s, pdl, a)) != cudaSuccess) return e;
   const int S = a.k + (a.has_shared ? 1 : 0);
   const size_t smem_dn = static_cast<size_t>(S) * a.I * 2;
-  switch (moe_fma_rounds(a.k, a.has_shared, a.I)) {
-    case 2: return launch_down<2>(a, sms, smem_dn, s, pdl);
-    case 3: return launch_down<3>(a, sms, smem_dn, s, pdl);
-    case 5: return launch_down<5>(a, sms, smem_dn, s, pdl);
-    case 9: return launch_down<9>(a, sms, smem_dn, s, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  if (!moe_fma_slots(a.k, a.has_shared, a.I)) return cudaErrorInvalidValue;
+  return launch_down(a, sms, smem_dn, s, pdl);
 }
 
 }  // namespace nvfp4

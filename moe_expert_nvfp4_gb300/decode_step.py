@@ -129,6 +129,19 @@ class DecodeStep:
         launches += 1
         return launches
 
+    # ------------------------------------------------------------ which way
+    # Steps of at most this many tokens run call by call: their MoE layers
+    # (and the dense calls of one or a few rows) go to the CUDA-core kernels,
+    # which start in a few us, while the persistent program pays each op's
+    # completion wait and activation staging.  Measured on GB300, 40 layers,
+    # call by call against the program: T = 1 0.93 against 2.96 ms, T = 2
+    # 1.19 / 2.82, T = 4 1.89 / 2.91, T = 8 3.41 / 3.59, T = 16 5.78 / 5.33.
+    CALLS_MAX_TOKENS = 8
+
+    def path_for(self, tokens: int) -> str:
+        """"calls" or "program": the faster way to run a step of ``tokens``."""
+        return "calls" if tokens <= self.CALLS_MAX_TOKENS else "program"
+
     # ------------------------------------------------------------ as a program
     def program_ops(self, b: dict, all_sms: bool = False) -> list:
         """The step's projections, MoE layers and head as one op chain

@@ -73,7 +73,8 @@ _lib: Optional[ctypes.CDLL] = None
 
 def declared_functions() -> list[str]:
     """Function names declared in the public header."""
-    txt = open(HEADER).read()
+    with open(HEADER) as f:
+        txt = f.read()
     return sorted(set(re.findall(r"^(?:int|size_t|const char\*)\s+(\w+)\(", txt, re.M)))
 
 
