@@ -659,46 +659,77 @@ def run_ours(args, rank, world, local):
     peak_src = (f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback 6.8 TB/s")
     path = path_of(t)
-    if path == "program":
-        # the program kernel: every projection, MoE layer and the head of the step
+    probe = read_probe_gbs() if rank == 0 else None
+
+    def family(name, key, calls_fn, nbytes_f, launches):
+        """A kernel family of the step timed alone: a CUDA graph of its calls
+        back to back, CUDA events on the stream."""
         kg = torch.cuda.CUDAGraph()
         with torch.cuda.graph(kg):
-            b["prog"].launch()
+            calls_fn()
         for _ in range(3):
             kg.replay()
         torch.cuda.synchronize()
         k_ms = timed_replays(kg, max(5, min(args.steps, 100)), stream)
-        k_bytes, k_launches = nbytes, 1
-        k_name = f"stream_tc_kernel, program of the step ({3 * s.layers + 1} calls), per launch"
-        k_key = f"program_T{t}_L{s.layers}"
+        del kg
+        achieved = nbytes_f / (k_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(key), "kernel": name,
+                "bytes_per_launch": nbytes_f / launches, "us_per_launch": k_ms * 1e3 / launches,
+                "ms_per_step": k_ms, "peak_source": peak_src, "frac_of_8tbs": achieved / 8000.0,
+                "read_probe": probe,
+                "frac_of_read_probe": achieved / probe["gbs"] if probe else None}
+
+    families = {}
+    if path == "program":
+        # the program kernel: every projection, MoE layer and the head of the step
+        families["program"] = family(
+            f"stream_tc_kernel, program of the step ({3 * s.layers + 1} calls), per launch",
+            f"program_T{t}_L{s.layers}", lambda: b["prog"].launch(), nbytes, 1)
     else:
-        # the MoE layer call (gate_up + down launches), 40 layers
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(kg):
+        # the step's two kernel families, each timed alone: its MoE layer calls
+        # and its dense calls (QKV, O, head)
+        per_expert = 3 * 2048 * 512 * 9 // 16  # gate_up + down bytes of one expert
+        ids_l = b["ids"].view(s.layers, -1).cpu()
+        moe_bytes = sum((torch.unique(ids_l[l]).numel() + 1) * per_expert for l in range(s.layers))
+
+        def moe_calls():
             for l in range(s.layers):
                 ops.moe(b["o"][0], b["ids"][l * t:(l + 1) * t], b["w"][l * t:(l + 1) * t],
                         model.experts[l], model.shared[l], out=b["y"][0], rms_input=True,
-                        workspace=b["ws"])
-        for _ in range(3):
-            kg.replay()
-        torch.cuda.synchronize()
-        k_ms = timed_replays(kg, max(5, min(args.steps, 100)), stream)
-        per_expert = 3 * 2048 * 512 * 9 // 16  # gate_up + down bytes of one expert
-        ids_l = b["ids"].view(s.layers, -1).cpu()
-        k_bytes = sum((torch.unique(ids_l[l]).numel() + 1) * per_expert for l in range(s.layers))
-        k_launches = s.layers
-        k_name = "moe_nvfp4_decode (stream_tc_kernel gate_up + down), per call"
-        k_key = f"moe_layer_T{t}"
-    achieved = k_bytes / (k_ms * 1e-3) / 1e9
-    probe = read_probe_gbs() if rank == 0 else None
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(k_key),
-                "kernel": k_name, "bytes_per_launch": k_bytes / k_launches,
-                "us_per_launch": k_ms * 1e3 / k_launches, "peak_source": peak_src,
-                "frac_of_8tbs": achieved / 8000.0,
-                "read_probe": probe,
-                "frac_of_read_probe": achieved / probe["gbs"] if probe else None}
-    del kg
+                        workspace=b["ws"], ids_ready=True)
+        moe_calls()
+        kernels = " + ".join(w.split()[0] for w in ops.last_dispatch().split(";")[:3]
+                             if w.strip() and not w.strip().startswith("T="))
+        families["moe"] = family(f"moe_nvfp4_decode ({kernels}), per call", f"moe_layer_T{t}",
+                                 moe_calls, moe_bytes, s.layers)
+
+        seen = []
+
+        def dense_calls():
+            for l in range(s.layers):
+                ops.gemm(b["x"], model.qkv[l], out=b["q"][0], rms_input=True, workspace=b["ws"])
+                seen.append(ops.last_dispatch().split()[0])
+                ops.gemm(b["q"][0][:, :s.o_in], model.o[l], out=b["o"][0], rms_input=True,
+                         workspace=b["ws"])
+                seen.append(ops.last_dispatch().split()[0])
+            ops.gemm(b["y"][0], model.head, out=b["head"], argmax_out=b["argmax"],
+                     rms_input=True, workspace=b["ws"])
+            seen.append(ops.last_dispatch().split()[0])
+        dense_calls()
+        kernels = " + ".join(sorted(set(seen)))
+        dense_bytes = nbytes - moe_bytes
+        families["dense"] = family(f"nvfp4_gemm_skinny (QKV, O and head: {kernels}), per call",
+                                   f"dense_T{t}_L{s.layers}", dense_calls, dense_bytes,
+                                   2 * s.layers + 1)
+    # the dominant family: the larger share of the device time
+    tot_ms = sum(f["ms_per_step"] for f in families.values())
+    for f in families.values():
+        f["share"] = f["ms_per_step"] / tot_ms
+    dom = max(families, key=lambda k: families[k]["ms_per_step"])
+    roofline = dict(families[dom])
+    roofline["family"] = dom
+    roofline["other_families"] = {k: v for k, v in families.items() if k != dom}
 
     # ---- other token counts of the same step (context)
     sweep = {}

@@ -132,9 +132,10 @@ int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream);
  * before its first byte; the CUDA-core kernel (whole rows per warp, FP32
  * accumulation of the same exact FP16 products) starts in a few us but does
  * one FMA per weight and row.  The CUDA cores take every K % 256 != 0, and
- * K % 256 == 0 when M = 1 and the weight is at most 128 MiB, or 2 <= M <= 8
- * and M x the weight bytes are at most 32 MiB.  The two differ only in the
- * order of the FP32 additions (a few units in the last place of C). */
+ * K % 256 == 0 when the weight (codes + scales) is at most 128 MiB for
+ * M = 1, 20 MiB for M = 2, 10 MiB for M = 3, 4 and 1 MiB for M = 5..8.
+ * The two differ only in the order of the FP32 additions (a few units in
+ * the last place of C). */
 size_t nvfp4_gemm_skinny_workspace(int M, int N, int K);
 int nvfp4_gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W,
                       void* C, int64_t ldc, int32_t* argmax_out, uint32_t flags,
@@ -264,7 +265,12 @@ int topk_softmax_route(const float* logits, int T, int E, int k, int renormalize
  * combine) are FP32; the per-slot outputs are summed in slot order, the
  * shared expert last: deterministic.  Ids outside [0, E) are skipped and set
  * NVFP4_STATUS_BAD_EXPERT_ID.  Limits: T <= 32, k <= 16, E <= 512,
- * H % 256 == 0, I % 256 == 0. */
+ * H % 256 == 0, I % 256 == 0.  Up to 16 tokens (with I in {256, 512, 1024}
+ * and T x H x 2 bytes within 96 KB) two CUDA-core kernels serve the call:
+ * gate/up + SwiGLU per (token, slot) pair, then down with the combine; the
+ * tensor-core kernels (gate_up, down, combine) take the rest.  The two
+ * differ only in the order of FP32 additions and in h's FP16 staging
+ * (nvfp4_last_dispatch names the kernels). */
 size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* experts);
 int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
                      const float* topk_w, int k, const nvfp4_expert_stack* experts,

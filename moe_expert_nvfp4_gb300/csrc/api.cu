@@ -303,13 +303,14 @@ struct FmaPlan {
 };
 
 bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
-  p->rows_per_cta = fma_rows_per_cta(M);
-  p->smem = static_cast<size_t>(p->rows_per_cta) * (K / 32) * 64;
+  p->rows_per_cta = fma_rows_per_cta(M, K);
+  p->smem = fma_smem_bytes(p->rows_per_cta, K);
   if (p->smem > 200 * 1024) return false;
   const int ru = p->ru = fma_rows_per_warp(p->rows_per_cta, N);  // rows a warp takes at once
   const long groups = (static_cast<long>(N) + ru - 1) / ru;
   const long ctas = (groups + 7) / 8;           // eight warps a CTA
-  p->grid = static_cast<int>(ctas < 2L * sms ? ctas : 2L * sms);
+  const long per_sm = p->smem <= 110 * 1024 ? 2 : 1;  // CTAs an SM holds
+  p->grid = static_cast<int>(ctas < per_sm * sms ? ctas : per_sm * sms);
   const int row_groups = (M + p->rows_per_cta - 1) / p->rows_per_cta;
   if (4 + 4 * row_groups > static_cast<int>(kWsCounters)) return false;
   p->off_am = kWsScratch;
@@ -324,30 +325,35 @@ bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
 // allocation, ring fill, split-K drain) outweighs its faster streaming.  The
 // CUDA-core kernel does one FMA per weight and activation row, so its rate
 // falls as M grows.  Measured on GB300, back-to-back calls in a CUDA graph
-// with programmatic dependent launch, K = 2048 (CUDA cores vs tensor cores):
-//   M = 1: 4096 rows 4.1 vs 14.4 us, 16384 rows 8.5 vs 13.5 us,
-//          151,936 rows 53.7 vs 47.3 us;
-//   M = 2: 4096 rows 5.7 vs 14.5 us, 16384 rows 14.2 vs 13.6 us;
-//   M = 4: 4096 rows 9.8 vs 14.7 us, 16384 rows 23.1 vs 13.6 us;
-//   M = 8: 64 rows 8.7 vs 16.8 us, 4096 rows 17.8 vs 18.4 us.
-// Hence: M = 1 up to 128 MiB of weights; 2 <= M <= 8 while M x the weight
-// bytes stay within 32 MiB.
-constexpr double kFmaBytesM1 = 128.0 * (1 << 20);
-constexpr double kFmaRowBytes = 32.0 * (1 << 20);
-
+// with programmatic dependent launch, K = 2048 (CUDA cores vs tensor cores,
+// us):
+//   M = 1: 4096 rows 3.5 vs 14.4, 16384 rows 8.3 vs 13.5, 151,936 rows 51.6
+//          vs 47.6;
+//   M = 2: 16384 rows 11.0 vs 13.6, 32768 rows 18.8 vs 17.0;
+//   M = 4: 8192 rows 11.9 vs 13.8, 16384 rows 18.9 vs 13.6;
+//   M = 8: 64 rows 10.2 vs 12.3, 4096 rows 16.2 vs 18.2, 2048 x 4096 18.1
+//          vs 15.1, 8192 rows 23.9 vs 16.5;
+//   M = 16: 64 rows 19.7 vs 15.6, 4096 rows 30.6 vs 25.4.
+// Hence, by the weight bytes: M = 1 up to 128 MiB, M = 2 up to 20 MiB,
+// M = 3, 4 up to 10 MiB, M = 5..8 up to 1 MiB, never beyond.
 bool use_fma(int M, int N, int K) {
   if (K % kStageK) return true;
-  const double bytes = static_cast<double>(N) * K * 9.0 / 16.0;  // codes + block scales
-  if (M == 1) return bytes <= kFmaBytesM1;
-  return M <= 8 && M * bytes <= kFmaRowBytes;
+  const double mib = static_cast<double>(N) * K * 9.0 / 16.0 / (1 << 20);  // codes + block scales
+  if (M == 1) return mib <= 128.0;
+  if (M == 2) return mib <= 20.0;
+  if (M <= 4) return mib <= 10.0;
+  if (M <= 8) return mib <= 1.0;
+  return false;
 }
 
 // MoE calls with few tokens run on the CUDA cores (moe_fma.cu): one FMA per
 // weight and (token, slot) pair, no tensor-core pipeline to fill.  Measured
 // on GB300 (256 experts, H = 2048, I = 512, top-8 + shared, back-to-back
-// calls): see the dispatch bound kMoeFmaMaxT.  Shapes: I in {256, 512,
-// 1024} (a down row is 8, 16 or 32 chunks of 32), the staged activation rows
-// within 96 KB of shared memory.
+// calls over 16 layers' experts; CUDA cores vs tensor cores, us a layer):
+// T = 1 12.1 vs 43.4, T = 2 15.2 vs 44.6, T = 4 24.8 vs 49.4, T = 8 44.8 vs
+// 62.7, T = 16 80.2 vs 96.3, so every T up to kMoeFmaMaxT (16).  Shapes: I
+// in {256, 512, 1024} (a down row is 8, 16 or 32 chunks of 32), the staged
+// activation rows within 96 KB of shared memory.
 bool use_moe_fma(int T, int k, int H, int I) {
   return T <= kMoeFmaMaxT && (I == 256 || I == 512 || I == 1024) &&
          static_cast<long>(T) * H * 2 <= 96 * 1024 && moe_fma_slots(k, 1, I) != 0;

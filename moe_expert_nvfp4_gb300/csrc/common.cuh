@@ -325,31 +325,50 @@ __device__ __forceinline__ void ld_act_chunk(uint32_t xs, int m, int c, int chun
   }
 }
 
-// acc + the chunk's dot product: 32 E2M1 codes (16 bytes, low nibble = even
-// k) times the activations xv, one FP32 sum per 16-element block (the
-// products code x activation are exact in FP32), each block sum times its
-// E4M3 scale (the two bytes of sb, low byte first).
-__device__ __forceinline__ float nvfp4_chunk_dot(const uint4& w, uint32_t sb,
-                                                 const uint32_t (&xv)[16], float acc) {
+// A 32-K chunk of an NVFP4 row decoded: 32 E2M1 codes (16 bytes, low nibble
+// = even k) as 16 f16x2 words and the two 16-element blocks' E4M3 scales
+// (the two bytes of sb, low byte first) as floats; all exact.
+struct Nvfp4Chunk {
+  uint32_t code[16];
+  float sc0, sc1;
+};
+
+__device__ __forceinline__ Nvfp4Chunk nvfp4_decode_chunk(const uint4& w, uint32_t sb) {
+  Nvfp4Chunk ch;
   uint32_t s2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(static_cast<uint16_t>(sb)));
-  const float sc0 = f16_lo_to_f32(s2), sc1 = f16_lo_to_f32(s2 >> 16);
+  ch.sc0 = f16_lo_to_f32(s2);
+  ch.sc1 = f16_lo_to_f32(s2 >> 16);
   const uint32_t wds[4] = {w.x, w.y, w.z, w.w};
-  uint32_t code[16];
 #pragma unroll
   for (int wi = 0; wi < 4; ++wi)
-    e2m1x8_to_f16x2(wds[wi], code[4 * wi], code[4 * wi + 1], code[4 * wi + 2], code[4 * wi + 3]);
+    e2m1x8_to_f16x2(wds[wi], ch.code[4 * wi], ch.code[4 * wi + 1], ch.code[4 * wi + 2],
+                    ch.code[4 * wi + 3]);
+  return ch;
+}
+
+// acc + the chunk's dot product with the activations xv: one FP32 sum per
+// 16-element block (the products code x activation are exact in FP32), each
+// block sum times its scale.
+__device__ __forceinline__ float nvfp4_chunk_dot(const Nvfp4Chunk& ch, const uint32_t (&xv)[16],
+                                                 float acc) {
   float b0 = 0.0f, b1 = 0.0f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    b0 = fma_f16(code[e], xv[e], false, b0);
-    b0 = fma_f16(code[e], xv[e], true, b0);
-    b1 = fma_f16(code[8 + e], xv[8 + e], false, b1);
-    b1 = fma_f16(code[8 + e], xv[8 + e], true, b1);
+    b0 = fma_f16(ch.code[e], xv[e], false, b0);
+    b0 = fma_f16(ch.code[e], xv[e], true, b0);
+    b1 = fma_f16(ch.code[8 + e], xv[8 + e], false, b1);
+    b1 = fma_f16(ch.code[8 + e], xv[8 + e], true, b1);
   }
-  acc = fmaf(sc0, b0, acc);
-  return fmaf(sc1, b1, acc);
+  acc = fmaf(ch.sc0, b0, acc);
+  return fmaf(ch.sc1, b1, acc);
 }
+
+__device__ __forceinline__ float nvfp4_chunk_dot(const uint4& w, uint32_t sb,
+                                                 const uint32_t (&xv)[16], float acc) {
+  return nvfp4_chunk_dot(nvfp4_decode_chunk(w, sb), xv, acc);
+}
+
 
 // ------------------------------------------------------------------ gpu-scope sync
 // Counter add with acquire-release semantics at GPU scope: after a CTA

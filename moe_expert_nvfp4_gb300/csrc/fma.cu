@@ -12,11 +12,14 @@
 // codes to FP16 (hardware convert, exact) and accumulates code x activation
 // per 16-element block with the mixed FMA (f16 x f16 + f32 -> f32, the
 // product exact), then adds block scale x block sum into the row's FP32
-// total.  A warp reduction ends the row.  The activations (1, 2 or 4 rows
-// per CTA, grid.y covering the rest) are staged once per CTA in shared memory as FP16 after the
-// same power-of-two row shift as the tensor path (exact for BF16 elements
-// within 2^31 of the row's largest magnitude),
-// with a bank-conflict-free swizzle of each chunk's four 16-byte slots.
+// total.  A warp reduction ends the row.  The activations (MB = 1, 2, 4, 8
+// or 16 rows per CTA, grid.y covering the rest; from four rows each decoded
+// chunk serves every row) are staged once per CTA in shared memory as FP16
+// after the same power-of-two row shift as the tensor path (exact for BF16
+// elements within 2^31 of the row's largest magnitude), with a
+// bank-conflict-free swizzle of each chunk's four 16-byte slots.  (Staging
+// the rows as FP32 instead, one FP32 FMA a weight, measured slower at every
+// M: the shared-memory traffic doubles.)
 //
 // Sources: "Qwen3.6-35B-A3B NVFP4 on an RTX 5090 (Elsa)", "Making decode
 // faster", "Skinny matrix multiplies" (decode matmuls of four to sixteen
@@ -63,7 +66,7 @@ __device__ __forceinline__ float cta_max0(float v, float* s_w) {
 
 // MB activation rows per CTA (rows m0 .. m0 + MB - 1 of A, m0 = MB *
 // blockIdx.y); grid-stride over the weight rows.  Two CTAs share an SM (the
-// grid is twice the SM count), hence the register bound.
+// grid is at most twice the SM count), hence the register bound.
 template <int MB, int RU>
 __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   extern __shared__ __align__(16) uint8_t fsm[];
@@ -113,8 +116,10 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   pdl_wait();
   pdl_launch_dependents();
 
-  constexpr int kKeep = 4;  // segments per thread and row kept in registers (K <= 8192)
-  uint4 keep[MB][kKeep];
+  // segments per thread and row kept in registers (K <= 8192 for up to four
+  // rows; more rows load theirs again for the conversion)
+  constexpr int kKeep = MB <= 4 ? 4 : 0;
+  uint4 keep[MB][kKeep > 0 ? kKeep : 1];
   // ---- per row: the largest magnitude and the plain sum of squares in one
   // pass over all the CTA's rows, one reduction; then the FP16 shift and the
   // RMS factor (rows above 2^56 sum their shifted squares in a second pass:
@@ -212,23 +217,22 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
                         __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
     return make_uint4(p[0], p[1], p[2], p[3]);
   };
+  auto store_seg = [&](int r, int v, const uint4 q, int sh) {
+    st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks), to_f16(q, sh));
+  };
 #pragma unroll
   for (int r = 0; r < MB; ++r) {
     const int sh = s_sh[r];
 #pragma unroll
     for (int i = 0; i < kKeep; ++i) {
       const int v = threadIdx.x + kFmaThreads * i;
-      if (v < a.K / 8)
-        st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks),
-                     r < mb ? to_f16(keep[r][i], sh) : make_uint4(0u, 0u, 0u, 0u));
+      if (v < a.K / 8) store_seg(r, v, r < mb ? keep[r][i] : make_uint4(0u, 0u, 0u, 0u), sh);
     }
     for (int v = threadIdx.x + kFmaThreads * kKeep; v < a.K / 8; v += kFmaThreads) {
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
       if (r < mb)
-        o = to_f16(__ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda +
-                                                         8 * v)),
-                   sh);
-      st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks), o);
+        q = __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda + 8 * v));
+      store_seg(r, v, q, sh);
     }
   }
   __syncthreads();
@@ -236,13 +240,6 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   // ---- rows of W
   // output = (row sum x 2^-shift) x tensor scale x RMS factor, in that order
   // (the undone shift alone could fall below FP32's range)
-  int shift[MB];
-  float post[MB];
-#pragma unroll
-  for (int r = 0; r < MB; ++r) {
-    shift[r] = s_sh[r];
-    post[r] = a.rms ? s_rms[r] : 1.0f;
-  }
   float am_v[MB];
   int am_i[MB];
 #pragma unroll
@@ -262,12 +259,26 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
     load(nG, ncr, nw, ns);
     const int c = cr * 32 + lane;
     if (c < chunks) {
+      if constexpr (MB <= 2) {
 #pragma unroll
-      for (int r = 0; r < MB; ++r) {
-        uint32_t xv[16];
-        ld_act_chunk(xs, r, c, chunks, xv);
+        for (int r = 0; r < MB; ++r) {
+          uint32_t xv[16];
+          ld_act_chunk(xs, r, c, chunks, xv);
 #pragma unroll
-        for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(cw[j], sb[j], xv, acc[r][j]);
+          for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(cw[j], sb[j], xv, acc[r][j]);
+        }
+      } else {  // decode each weight chunk once for all the rows
+        Nvfp4Chunk ch[RU];
+#pragma unroll
+        for (int j = 0; j < RU; ++j) ch[j] = nvfp4_decode_chunk(cw[j], sb[j]);
+#pragma unroll
+        for (int r = 0; r < MB; ++r) {
+          if (r >= mb) break;  // (uniform) rows past M
+          uint32_t xv[16];
+          ld_act_chunk(xs, r, c, chunks, xv);
+#pragma unroll
+          for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(ch[j], xv, acc[r][j]);
+        }
       }
     }
     if (cr + 1 == rounds) {  // the group's rows are complete
@@ -279,7 +290,8 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
           const float t = warp_sum(acc[r][j]);
           acc[r][j] = 0.0f;
           if (r < mb && n < a.N) {
-            const __nv_bfloat16 o = __float2bfloat16_rn(scale_pow2(t, -shift[r]) * gs * post[r]);
+            const __nv_bfloat16 o =
+                __float2bfloat16_rn(scale_pow2(t, -s_sh[r]) * gs * (a.rms ? s_rms[r] : 1.0f));
             if (lane == 0) a.C[static_cast<size_t>(m0 + r) * a.ldc + n] = o;
             const float ov = __bfloat162float(o);
             if (fm_better(ov, n, am_v[r], am_i[r])) {
@@ -367,13 +379,13 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
 
 template <int MB, int RU>
 cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
-  const size_t smem = static_cast<size_t>(MB) * (a.K / 32) * 64;
+  const size_t smem = fma_smem_bytes(MB, a.K);
   cudaError_t e = cudaFuncSetAttribute(fma_kernel<MB, RU>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem < 1024 ? 1024 : smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, (a.M + MB - 1) / MB);
+  cfg.gridDim = dim3(grid, (a.M + MB - 1) / MB);  // (MB = fma_rows_per_cta(M, K))
   cfg.blockDim = dim3(kFmaThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -387,7 +399,15 @@ cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
 
 }  // namespace
 
-int fma_rows_per_cta(int M) { return M <= 1 ? 1 : (M <= 2 ? 2 : 4); }
+constexpr size_t kFmaMaxSmem = 200 * 1024;
+
+size_t fma_smem_bytes(int rows_per_cta, int K) { return static_cast<size_t>(rows_per_cta) * K * 2; }
+
+int fma_rows_per_cta(int M, int K) {
+  int mb = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+  while (mb > 1 && fma_smem_bytes(mb, K) > kFmaMaxSmem) mb /= 2;  // (long rows)
+  return mb;
+}
 
 // Rows a warp takes at once.  More rows keep more bytes in flight per warp
 // but leave fewer warps a group when N is small.  Measured on GB300 (K =
@@ -401,17 +421,19 @@ int fma_rows_per_warp(int rows_per_cta, int N) {
   // (thresholds for GB300's 152 SMs)
   if (rows_per_cta == 1) return N < 3072 ? 2 : (N < 12288 ? 4 : 8);
   if (rows_per_cta == 2) return N < 6144 ? 2 : 4;
-  return 2;
+  return rows_per_cta == 4 ? 2 : 1;
 }
 
 cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool pdl) {
-  switch (fma_rows_per_cta(a.M) * 16 + ru) {
+  switch (fma_rows_per_cta(a.M, a.K) * 16 + ru) {
     case 16 + 8: return launch_mb<1, 8>(a, grid, s, pdl);
     case 16 + 4: return launch_mb<1, 4>(a, grid, s, pdl);
     case 16 + 2: return launch_mb<1, 2>(a, grid, s, pdl);
     case 32 + 4: return launch_mb<2, 4>(a, grid, s, pdl);
     case 32 + 2: return launch_mb<2, 2>(a, grid, s, pdl);
     case 64 + 2: return launch_mb<4, 2>(a, grid, s, pdl);
+    case 128 + 1: return launch_mb<8, 1>(a, grid, s, pdl);
+    case 256 + 1: return launch_mb<16, 1>(a, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -190,8 +190,11 @@ struct FmaArgs {
   uint32_t* argmax_cnt;
   int2* am_part;
 };
-// activation rows per CTA for M rows (1, 2 or 4); grid.y = ceil(M / that)
-int fma_rows_per_cta(int M);
+// activation rows per CTA for M rows of K (1, 2, 4, 8 or 16, fewer when the
+// staged rows would not fit in shared memory); grid.y = ceil(M / that)
+int fma_rows_per_cta(int M, int K);
+// shared memory of its staged activation rows
+size_t fma_smem_bytes(int rows_per_cta, int K);
 // weight rows a warp of that kernel takes at once (its loads in flight:
 // this many times 528 bytes per 32-K round at K = 2048), for N weight rows
 int fma_rows_per_warp(int rows_per_cta, int N);
@@ -199,7 +202,7 @@ cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool 
 
 // MoE layer on the CUDA cores (moe_fma.cu) for T <= kMoeFmaMaxT tokens:
 // gate/up + SwiGLU per (token, slot) pair into h, then down + combine.
-constexpr int kMoeFmaMaxT = 8;
+constexpr int kMoeFmaMaxT = 16;
 constexpr int kMoeFmaMaxSlots = 17;                      // k <= 16, + shared
 constexpr int kMoeFmaMaxPairs = kMoeFmaMaxT * kMoeFmaMaxSlots;
 struct MoeFmaArgs {

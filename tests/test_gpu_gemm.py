@@ -56,14 +56,17 @@ def test_projection_2048_to_64_m4():
 
 @pytest.mark.parametrize("m,n,k,kernel", [(1, 4096, 2048, "fma_kernel"),
                                           (1, 151936, 2048, "stream_tc_kernel"),
-                                          (2, 4096, 2048, "fma_kernel"),
-                                          (2, 16384, 2048, "stream_tc_kernel"),
-                                          (8, 3000, 2048, "fma_kernel"),
+                                          (2, 16384, 2048, "fma_kernel"),
+                                          (2, 32768, 2048, "stream_tc_kernel"),
+                                          (4, 8192, 2048, "fma_kernel"),
+                                          (4, 16384, 2048, "stream_tc_kernel"),
+                                          (8, 800, 2048, "fma_kernel"),
                                           (8, 4096, 2048, "stream_tc_kernel"),
                                           (9, 64, 2048, "stream_tc_kernel")])
 def test_dispatch_by_shape(m, n, k, kernel):
-    """The CUDA cores take M = 1 up to 128 MiB of weights and 2 <= M <= 8 up
-    to 32 MiB x M; the tensor cores the rest (K % 256 == 0)."""
+    """The CUDA cores take weights up to 128 MiB at M = 1, 20 MiB at M = 2,
+    10 MiB at M = 3, 4 and 1 MiB at M = 5..8; the tensor cores the rest
+    (K % 256 == 0)."""
     ws = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
     W = device_weight(30, n, k)
     a = synth.activations_bf16(30, m, k).cuda()

@@ -90,11 +90,11 @@ def layer():
     return device_experts(21, 0, E, H, I), device_shared(21, 0, E, H, I)
 
 
-@pytest.mark.parametrize("t", [16, 32])
+@pytest.mark.parametrize("t", [32])
 def test_moe_in_program_equals_call(layer, t):
-    """(T >= 16: the single MoE call runs on the tensor cores too; fewer
-    tokens go to the CUDA-core kernels, and the program op against the oracle
-    is tested in test_gpu_moe.)"""
+    """(T = 32: the single MoE call runs on the tensor cores too; up to 16
+    tokens it goes to the CUDA-core kernels, and the program op against the
+    oracle is tested in test_gpu_moe.)"""
     ex, sh = layer
     x = synth.activations_bf16(21, t, 2048).cuda()
     ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
@@ -120,7 +120,7 @@ def test_moe_in_program_equals_call(layer, t):
 def test_two_moe_layers_share_schedule_slots(layer):
     """Four MoE layers in a row cycle both schedule slots twice."""
     ex, sh = layer
-    t = 16
+    t = 32
     x = synth.activations_bf16(23, t, 2048).cuda()
     lg = synth.router_logits(23, 4 * t, 64).cuda()
     ids, w = ops.route(lg, 8)
@@ -143,9 +143,9 @@ def test_two_moe_layers_share_schedule_slots(layer):
     assert _counters_zero(prog.workspace)
 
 
-@pytest.mark.parametrize("tokens", [16])
+@pytest.mark.parametrize("tokens", [32])
 def test_decode_step_program_equals_calls(tokens):
-    """(16 tokens: every call of the step runs on the tensor cores, as the
+    """(32 tokens: every call of the step runs on the tensor cores, as the
     program's ops do.)"""
     m = DecodeStep(seed=6, shape=StepShape(layers=3))
     b = m.buffers(tokens, keep=True)
