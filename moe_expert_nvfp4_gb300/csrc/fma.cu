@@ -17,7 +17,7 @@
 // chunk serves every row) are staged once per CTA in shared memory as FP16
 // after the same power-of-two row shift as the tensor path (exact for BF16
 // elements within 2^31 of the row's largest magnitude), with a
-// bank-conflict-free swizzle of each chunk's four 16-byte slots.  (Staging
+// bank-conflict-free padding of each chunk's four 16-byte slots.  (Staging
 // the rows as FP32 instead, one FP32 FMA a weight, measured slower at every
 // M: the shared-memory traffic doubles.)
 //
@@ -35,6 +35,25 @@ namespace {
 
 constexpr int kFmaWarps = 8;
 constexpr int kFmaThreads = kFmaWarps * 32;
+
+// Staged activations: row m at m * rs bytes (rs = chunks * kChunkPitch), its
+// 32-K chunk c at c * kChunkPitch (64 bytes of FP16, 16 of padding), the
+// chunk's 16-byte slot q at q * 16.  The eight lanes of a shared-memory phase
+// (chunks c .. c + 7, same q) hit eight different 16-byte bank groups (80 c
+// mod 128 takes eight values), and every address is a per-chunk base plus
+// a row offset and constants.
+constexpr int kChunkPitch = 80;
+
+__device__ __forceinline__ void ld_chunk(uint32_t a, uint32_t (&xv)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = ld_shared_v4(a + 16 * q);
+    xv[4 * q] = v.x;
+    xv[4 * q + 1] = v.y;
+    xv[4 * q + 2] = v.z;
+    xv[4 * q + 3] = v.w;
+  }
+}
 
 __device__ __forceinline__ bool fm_better(float v, int i, float bv, int bi) {
   return bi == 0x7fffffff || v > bv || (v == bv && i < bi);
@@ -81,6 +100,7 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   const int m0 = MB * blockIdx.y;
   const int mb = min(MB, a.M - m0);
   const int chunks = a.K / 32;
+  const int rs = chunks * kChunkPitch;  // bytes per staged row
   const uint32_t xs = smem_u32(fsm);
 
   // The weights do not depend on the previous kernel on the stream: the
@@ -218,7 +238,8 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
     return make_uint4(p[0], p[1], p[2], p[3]);
   };
   auto store_seg = [&](int r, int v, const uint4 q, int sh) {
-    st_shared_v4(xs + act_off(r, v >> 2, v & 3, chunks), to_f16(q, sh));
+    st_shared_v4(xs + static_cast<uint32_t>(r * rs + (v >> 2) * kChunkPitch + (v & 3) * 16),
+                 to_f16(q, sh));
   };
 #pragma unroll
   for (int r = 0; r < MB; ++r) {
@@ -259,11 +280,12 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
     load(nG, ncr, nw, ns);
     const int c = cr * 32 + lane;
     if (c < chunks) {
+      const uint32_t cbase = xs + static_cast<uint32_t>(c * kChunkPitch);
       if constexpr (MB <= 2) {
 #pragma unroll
         for (int r = 0; r < MB; ++r) {
           uint32_t xv[16];
-          ld_act_chunk(xs, r, c, chunks, xv);
+          ld_chunk(cbase + static_cast<uint32_t>(r * rs), xv);
 #pragma unroll
           for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(cw[j], sb[j], xv, acc[r][j]);
         }
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
         for (int r = 0; r < MB; ++r) {
           if (r >= mb) break;  // (uniform) rows past M
           uint32_t xv[16];
-          ld_act_chunk(xs, r, c, chunks, xv);
+          ld_chunk(cbase + static_cast<uint32_t>(r * rs), xv);
 #pragma unroll
           for (int j = 0; j < RU; ++j) acc[r][j] = nvfp4_chunk_dot(ch[j], xv, acc[r][j]);
         }
@@ -401,7 +423,9 @@ cudaError_t launch_mb(const FmaArgs& a, int grid, cudaStream_t s, bool pdl) {
 
 constexpr size_t kFmaMaxSmem = 200 * 1024;
 
-size_t fma_smem_bytes(int rows_per_cta, int K) { return static_cast<size_t>(rows_per_cta) * K * 2; }
+size_t fma_smem_bytes(int rows_per_cta, int K) {
+  return static_cast<size_t>(rows_per_cta) * (K / 32) * kChunkPitch;
+}
 
 int fma_rows_per_cta(int M, int K) {
   int mb = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
