@@ -740,7 +740,7 @@ def run_ours(args, rank, world, local):
                                   "weight_bytes": nbytes, "path": path}
                 continue
             # both ways for the token counts around the switch, else the chosen one
-            paths = ("calls", "program") if tt in (2, 4, 8, 16) else (path_of(tt),)
+            paths = ("calls", "program") if tt in (2, 4, 8, 16, 32) else (path_of(tt),)
             for pth in paths:
                 _, g2, _, _, ms2, nb2, _ = one_config(tt, max(5, min(args.steps, 100)), 3, False,
                                                       pth)

@@ -77,12 +77,14 @@ enum {
  * the kernels may read them, and start streaming the routed experts'
  * weights, before waiting for that kernel to finish. */
 #define NVFP4_FLAG_IDS_READY 4u
-/* Program ops (nvfp4_program_create) only: spread this op over every SM and
- * split it exactly as its single call does on the tensor cores, so its
- * results are bit-identical to that call's (a single call that its shape
- * sends to the CUDA-core kernels adds in another order).  Without it a
- * small dense op of a program runs on fewer SMs (whole 128-row tiles or few
- * K splits each) while the other SMs stream the next ops' weights. */
+/* Program ops (nvfp4_program_create) only: split this op over the CTAs
+ * exactly as its single call does on the tensor cores (every SM, or for a
+ * dense op with fewer 128-row tiles than SMs, tiles x ceil(K units / 4)
+ * CTAs), so its results are bit-identical to that call's (a single call that
+ * its shape sends to the CUDA-core kernels adds in another order).  Without
+ * it a small dense op of a program runs on tiles x ceil(K units / 8) CTAs
+ * (whole 128-row tiles or few K splits each) while the other SMs stream the
+ * next ops' weights. */
 #define NVFP4_FLAG_ALL_SMS 8u
 
 /* device status bits */

@@ -174,6 +174,17 @@ struct TcDensePlan {
   size_t off_partials, off_am, ws_bytes;
 };
 
+// Weight units (256-K NVFP4 stages; 128-K FP8, 64-K BF16) per CTA a single
+// call with fewer 128-row tiles than SMs is cut
+// into (whole tiles when K has at most this many): the call then holds only
+// tiles x ceil(stages / this) SMs, and the next call's CTAs start streaming
+// their weights on the others while it runs (programmatic dependent launch).
+constexpr int kCallTargetStages = 4;
+
+bool dense_mode_host(int mode) {
+  return mode == kTcDense || mode == kTcDenseF8 || mode == kTcDenseBF;
+}
+
 bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p, int fmt = kFmtNvfp4) {
   p->n_tiles = (N + 127) / 128;
   if (p->n_tiles > kTcColCntBase) return false;
@@ -182,6 +193,11 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p, int fmt = kFmtN
   // the kernel splits units with 32-bit arithmetic (unit index x CTAs)
   if (p->units * (sms + 1) >= (1L << 31)) return false;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
+  if (p->n_tiles < sms) {
+    const long splits = (p->nkb + kCallTargetStages - 1) / kCallTargetStages;
+    const long g = static_cast<long>(p->n_tiles) * splits;
+    if (g < p->grid) p->grid = static_cast<int>(g);
+  }
   p->npad = M <= 16 ? 16 : 32;
   p->xrows = tc_xrows(M);
   const int cap = p->xrows == 8 ? 2 * kTcMaxWinK : kTcMaxWinK;  // 64 KB (8, 16 rows), 128 KB (32)
@@ -1061,7 +1077,9 @@ int nvfp4_program_create(const nvfp4_op* ops, int n_ops, void* workspace, size_t
   constexpr int target = kProgramTargetStages;
   int next_cta = 0;
   for (TcOp& op : table) {
-    int g = sms;
+    // (a dense op flagged NVFP4_FLAG_ALL_SMS keeps its single call's CTA
+    // count, set when the op was built)
+    int g = (dense_mode_host(op.mode) && op.all_sms) ? op.a.n_ctas : sms;
     if (op.mode == kTcDense && !op.all_sms) {
       const int n_tiles = (op.a.N + 127) / 128, nkb = op.a.K / kStageK;
       if (n_tiles < sms) {

@@ -132,11 +132,13 @@ class DecodeStep:
     # ------------------------------------------------------------ which way
     # Steps of at most this many tokens run call by call: their MoE layers
     # (and the dense calls of one or a few rows) go to the CUDA-core kernels,
-    # which start in a few us, while the persistent program pays each op's
-    # completion wait and activation staging.  Measured on GB300, 40 layers,
-    # call by call against the program: T = 1 0.93 against 2.96 ms, T = 2
-    # 1.19 / 2.82, T = 4 1.89 / 2.91, T = 8 3.41 / 3.59, T = 16 5.78 / 5.33.
-    CALLS_MAX_TOKENS = 8
+    # which start in a few us, and the small tensor-core calls hold only some
+    # of the SMs while the next call starts on the others; the persistent
+    # program pays each op's completion wait and activation staging instead.
+    # Measured on GB300, 40 layers, call by call against the program: T = 1
+    # 0.93 against 2.96 ms, T = 2 1.20 / 2.83, T = 4 1.96 / 2.91, T = 8
+    # 2.99 / 3.58, T = 16 4.80 / 5.35.
+    CALLS_MAX_TOKENS = 16
 
     def path_for(self, tokens: int) -> str:
         """"calls" or "program": the faster way to run a step of ``tokens``."""

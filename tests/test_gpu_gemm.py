@@ -44,8 +44,8 @@ def test_projection_2048_to_64_m4():
     c, ref, disp, (W, a, _) = _case(0, 4, 64, 2048)
     assert_close(f64(c), O.bf16_round(ref), "2048->64")
     assert disp.startswith("fma_kernel")                 # small: the CUDA-core kernel
-    # the tensor-core kernel on the same call (a one-op program splits it
-    # over 8 CTAs exactly as the call would)
+    # the tensor-core kernel on the same call (a one-op program with every
+    # op split as its tensor-core call would be: 1 tile x 2 K splits)
     out = torch.empty_like(c)
     prog = ops.Program([ops.gemm_op(a, W, out, all_sms=True)])
     prog.launch()
