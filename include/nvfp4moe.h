@@ -79,10 +79,10 @@ enum {
 #define NVFP4_FLAG_IDS_READY 4u
 /* Program ops (nvfp4_program_create) only: split this op over the CTAs
  * exactly as its single call does on the tensor cores (every SM, or for a
- * dense op with fewer 128-row tiles than SMs, tiles x ceil(K units / 4)
- * CTAs), so its results are bit-identical to that call's (a single call that
- * its shape sends to the CUDA-core kernels adds in another order).  Without
- * it a small dense op of a program runs on tiles x ceil(K units / 8) CTAs
+ * dense op with fewer 128-row tiles than SMs, tiles x ceil(K / 1024) CTAs),
+ * so its results are bit-identical to that call's (a single call that its
+ * shape sends to the CUDA-core kernels adds in another order).  Without it
+ * a small NVFP4 dense op of a program runs on tiles x ceil(K / 2048) CTAs
  * (whole 128-row tiles or few K splits each) while the other SMs stream the
  * next ops' weights. */
 #define NVFP4_FLAG_ALL_SMS 8u

@@ -174,8 +174,8 @@ struct TcDensePlan {
   size_t off_partials, off_am, ws_bytes;
 };
 
-// Weight units (256-K NVFP4 stages; 128-K FP8, 64-K BF16) per CTA a single
-// call with fewer 128-row tiles than SMs is cut
+// 256-K stages (the weight bytes of four NVFP4 units: 8 FP8 or 16 BF16
+// units) per CTA a single call with fewer 128-row tiles than SMs is cut
 // into (whole tiles when K has at most this many): the call then holds only
 // tiles x ceil(stages / this) SMs, and the next call's CTAs start streaming
 // their weights on the others while it runs (programmatic dependent launch).
@@ -194,7 +194,8 @@ bool plan_tc_dense(int M, int N, int K, int sms, TcDensePlan* p, int fmt = kFmtN
   if (p->units * (sms + 1) >= (1L << 31)) return false;
   p->grid = static_cast<int>(p->units < sms ? p->units : sms);
   if (p->n_tiles < sms) {
-    const long splits = (p->nkb + kCallTargetStages - 1) / kCallTargetStages;
+    const long target = kCallTargetStages * (kStageK / tc_unit_k(fmt));  // ~72 KB of weights
+    const long splits = (p->nkb + target - 1) / target;
     const long g = static_cast<long>(p->n_tiles) * splits;
     if (g < p->grid) p->grid = static_cast<int>(g);
   }
