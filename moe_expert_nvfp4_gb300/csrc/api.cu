@@ -368,16 +368,22 @@ bool use_fma(int M, int N, int K) {
 // on GB300 (256 experts, H = 2048, I = 512, top-8 + shared, back-to-back
 // calls over 16 layers' experts; CUDA cores vs tensor cores, us a layer):
 // T = 1 12.1 vs 43.4, T = 2 15.2 vs 44.6, T = 4 24.8 vs 49.4, T = 8 44.8 vs
-// 62.7, T = 16 80.2 vs 96.3, so every T up to kMoeFmaMaxT (16).  Shapes: I
-// in {256, 512, 1024} (a down row is 8, 16 or 32 chunks of 32), the staged
-// activation rows within 96 KB of shared memory.
+// 62.7, T = 16 80.2 vs 96.3, T = 32 (two batches of 16) 160.0 vs 202.1: every
+// T.  Shapes: I in {256, 512, 1024} (a down row is 8, 16 or 32 chunks of
+// 32), a batch's staged activation rows within 96 KB of shared memory.
+// Calls of more than kMoeFmaMaxT tokens run as batches of at most that many
+// (the tokens are independent; each batch reads its own tokens' experts).
+constexpr int kMoeFmaMaxCallT = 32;
+
 bool use_moe_fma(int T, int k, int H, int I) {
-  return T <= kMoeFmaMaxT && (I == 256 || I == 512 || I == 1024) &&
-         static_cast<long>(T) * H * 2 <= 96 * 1024 && moe_fma_slots(k, 1, I) != 0;
+  const int tb = T < kMoeFmaMaxT ? T : kMoeFmaMaxT;
+  return T <= kMoeFmaMaxCallT && (I == 256 || I == 512 || I == 1024) &&
+         static_cast<long>(tb) * H * 2 <= 96 * 1024 && moe_fma_slots(k, 1, I) != 0;
 }
 
 size_t moe_fma_ws_bytes(int T, int k, int I) {
-  return round_up(kWsScratch + static_cast<size_t>(T) * (k + 1) * I * 4, 256);
+  const int tb = T < kMoeFmaMaxT ? T : kMoeFmaMaxT;  // h of one batch
+  return round_up(kWsScratch + static_cast<size_t>(tb) * (k + 1) * I * 4, 256);
 }
 
 // The MoE layer on the CUDA cores (arguments already checked).
@@ -419,14 +425,27 @@ int moe_fma(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const fl
   a.ids_ready = (flags & NVFP4_FLAG_IDS_READY) ? 1 : 0;
   a.h = reinterpret_cast<float*>(ws + kWsScratch);
   a.status = reinterpret_cast<uint32_t*>(ws + kWsStatus);
-  const cudaError_t e = launch_moe_fma(a, sms, reinterpret_cast<cudaStream_t>(stream),
-                                       !(flags & NVFP4_FLAG_NO_PDL));
-  if (e != cudaSuccess) return cuda_fail(e, "moe_fma kernels launch");
+  // batches of at most kMoeFmaMaxT tokens, in order on the stream; a batch's
+  // gate/up kernel writes h only after the previous batch's down kernel
+  // ended (it waits for it before its main loop)
+  int batches = 0;
+  for (int t0 = 0; t0 < T; t0 += kMoeFmaMaxT, ++batches) {
+    MoeFmaArgs b = a;
+    b.T = T - t0 < kMoeFmaMaxT ? T - t0 : kMoeFmaMaxT;
+    b.x = a.x + static_cast<size_t>(t0) * ldx;
+    b.ids = a.ids + static_cast<size_t>(t0) * k;
+    b.w = a.w + static_cast<size_t>(t0) * k;
+    b.out = a.out + static_cast<size_t>(t0) * ldo;
+    const cudaError_t e = launch_moe_fma(b, sms, reinterpret_cast<cudaStream_t>(stream),
+                                         !(flags & NVFP4_FLAG_NO_PDL));
+    if (e != cudaSuccess) return cuda_fail(e, "moe_fma kernels launch");
+  }
   char buf[192];
   snprintf(buf, sizeof(buf),
            "moe_fma_gate_up_kernel; moe_fma_down_kernel slots=%d; T=%d k=%d E=%d shared=%d rms=%d "
-           "ids_ready=%d",
-           moe_fma_slots(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready);
+           "ids_ready=%d batches=%d",
+           moe_fma_slots(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready,
+           batches);
   g_dispatch = buf;
   return NVFP4_OK;
 }

@@ -136,9 +136,10 @@ class DecodeStep:
     # of the SMs while the next call starts on the others; the persistent
     # program pays each op's completion wait and activation staging instead.
     # Measured on GB300, 40 layers, call by call against the program: T = 1
-    # 0.93 against 2.96 ms, T = 2 1.20 / 2.83, T = 4 1.96 / 2.91, T = 8
-    # 2.99 / 3.58, T = 16 4.80 / 5.35.
-    CALLS_MAX_TOKENS = 16
+    # 0.96 against 2.96 ms, T = 2 1.19 / 2.83, T = 4 1.93 / 2.91, T = 8
+    # 2.99 / 3.58, T = 16 4.82 / 5.34, T = 32 9.05 / 10.44: every token count
+    # the library takes.
+    CALLS_MAX_TOKENS = 32
 
     def path_for(self, tokens: int) -> str:
         """"calls" or "program": the faster way to run a step of ``tokens``."""

@@ -157,8 +157,8 @@ def layer_zero_gates():
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("t", [1, 8, 32])
 def test_moe_all_zero_h_rows(layer_zero_gates, t, path):
-    """path "call": the single call (CUDA-core kernels up to 16 tokens);
-    "tc": a one-op program (the tensor-core kernels at every T)."""
+    """path "call": the single call (the CUDA-core kernels, in batches of 16
+    tokens); "tc": a one-op program (the tensor-core kernels)."""
     ex, sh, get = layer_zero_gates
     x = synth.activations_bf16(45, t, H)
     ids, w = ops.route(synth.router_logits(45, t, E).cuda(), TOPK)

@@ -90,13 +90,13 @@ def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
 def test_moe_layer_35b_shape(layer4, t):
     out, ref, disp, status, _ = _moe_case(layer4, t)
     assert status == 0
-    # up to 16 tokens the CUDA-core kernels, beyond them the tensor cores
-    kernel = "moe_fma_gate_up_kernel" if t <= 16 else "stream_tc_kernel<gate_up>"
+    # the CUDA-core kernels at every T up to 32 (in batches of 16 tokens)
+    kernel = "moe_fma_gate_up_kernel"
     assert "shared=1" in disp and disp.startswith(kernel)
     assert_close(f64(out), O.bf16_round(ref), f"MoE T={t}")
 
 
-@pytest.mark.parametrize("t", [1, 4, 8, 16])
+@pytest.mark.parametrize("t", [1, 4, 8, 16, 32])
 def test_moe_layer_on_the_tensor_cores_few_tokens(layer4, t):
     """The tensor-core MoE kernels at few tokens (a one-op program, which
     always runs them), against the oracle."""

@@ -86,15 +86,15 @@ def test_gemm_chain_equals_calls_and_oracle(m):
 
 @pytest.fixture(scope="module")
 def layer():
-    E, H, I = 64, 2048, 512
+    """Intermediate size 768: outside the CUDA-core MoE kernels' shapes, so
+    the single MoE calls run on the tensor cores like the program ops."""
+    E, H, I = 64, 2048, 768
     return device_experts(21, 0, E, H, I), device_shared(21, 0, E, H, I)
 
 
-@pytest.mark.parametrize("t", [32])
+@pytest.mark.parametrize("t", [8, 32])
 def test_moe_in_program_equals_call(layer, t):
-    """(T = 32: the single MoE call runs on the tensor cores too; up to 16
-    tokens it goes to the CUDA-core kernels, and the program op against the
-    oracle is tested in test_gpu_moe.)"""
+    """(8 and 32 rows: the dense calls run on the tensor cores too.)"""
     ex, sh = layer
     x = synth.activations_bf16(21, t, 2048).cuda()
     ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
@@ -145,9 +145,9 @@ def test_two_moe_layers_share_schedule_slots(layer):
 
 @pytest.mark.parametrize("tokens", [32])
 def test_decode_step_program_equals_calls(tokens):
-    """(32 tokens: every call of the step runs on the tensor cores, as the
-    program's ops do.)"""
-    m = DecodeStep(seed=6, shape=StepShape(layers=3))
+    """(32 tokens and intermediate size 768: every call of the step runs on
+    the tensor cores, as the program's ops do.)"""
+    m = DecodeStep(seed=6, shape=StepShape(layers=3, inter=768))
     b = m.buffers(tokens, keep=True)
     x, lg = m.inputs(tokens)
     b["x"].copy_(x)
