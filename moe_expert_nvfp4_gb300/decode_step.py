@@ -121,8 +121,11 @@ class DecodeStep:
             ops.moe(o, b["ids"][l * T:(l + 1) * T], b["w"][l * T:(l + 1) * T], self.experts[l],
                     self.shared[l], out=y, rms_input=True, workspace=ws, pdl=pdl,
                     ids_ready=True)
-            # QKV, O, and the MoE layer's two (CUDA cores) or three kernels
-            launches += 4 if ops.last_dispatch().startswith("moe_fma") else 5
+            # QKV, O, and the MoE layer: two CUDA-core kernels per batch of
+            # 16 tokens, or three tensor-core kernels
+            d = ops.last_dispatch()
+            launches += 2 + (2 * int(d.split("batches=")[1].split()[0]) if d.startswith("moe_fma")
+                             else 3)
             x = y
         ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,
                  pdl=pdl)
