@@ -1,7 +1,9 @@
 """GPU parity of the full stacked decode step (40 layers of QKV 2048->5120,
 O 4096->2048 and the 256+1-expert MoE layer, then the 151,936-row head with
-argmax), run the way the benchmark runs it: routing of every layer, then the
-whole chain as one program launch, replayed from a CUDA graph.
+argmax), both ways the library runs it: routing of every layer, then the
+whole chain as one program launch replayed from a CUDA graph; and call by
+call (the benchmark's path at every token count: the MoE layers and the
+small dense calls on the CUDA cores, the rest on the tensor cores).
 
 Checked: routing of every layer (ids bit-exact, weights within the FP32
 bound), sampled layers op by op from the GPU's own BF16 inputs (teacher
@@ -36,7 +38,7 @@ def _host_w(seed, n, k, *ids):
     return c.numpy(), s.numpy(), synth.GLOBAL_SCALE
 
 
-@pytest.mark.parametrize("tokens", [1, 8, 32])
+@pytest.mark.parametrize("tokens", [1, 2, 8, 16, 32])
 def test_decode_step_program(model, tokens):
     m, s = model, model.s
     b = m.buffers(tokens, keep=True)
@@ -78,9 +80,10 @@ def test_decode_step_program(model, tokens):
     assert_close(f64(b["head"]), O.bf16_round(head64), "head")
     check_argmax(b["argmax"].cpu().numpy(), f64(b["head"]), head64, what="step head")
 
-    # the same step call by call (one kernel launch per call; the single
-    # calls split K over other CTAs than the program does, so the two agree
-    # to the tolerance, not bit for bit): a sampled layer and the head
+    # the same step call by call, the way DecodeStep.path_for runs it (the
+    # CUDA-core kernels by shape, the small tensor-core calls on fewer CTAs:
+    # the two paths agree to the tolerance, not bit for bit): a sampled
+    # layer and the head
     m.run(b)
     torch.cuda.synchronize()
     assert b["ws"].status() == 0
