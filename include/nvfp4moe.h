@@ -71,7 +71,14 @@ enum {
 
 /* call flags */
 #define NVFP4_FLAG_RMS_INPUT 1u /* scale each input row by 1/sqrt(mean(x^2)+1e-6) */
-#define NVFP4_FLAG_NO_PDL 2u    /* launch without programmatic dependent launch */
+/* Launch without programmatic dependent launch.  With it (the default) a
+ * call's kernels may start while the previous kernel on the stream runs, and
+ * read their weights (codes, scales, global scales: never outputs of the
+ * previous kernel) before waiting for it; activations (and routing ids and
+ * weights, unless NVFP4_FLAG_IDS_READY) are read after the wait.  A caller
+ * whose previous kernel writes a weight and lets its dependents start early
+ * passes this flag. */
+#define NVFP4_FLAG_NO_PDL 2u
 /* moe_nvfp4_decode: the ids and weights were complete before the previous
  * kernel on the stream started (e.g. routing done earlier in the step), so
  * the kernels may read them, and start streaming the routed experts'
