@@ -315,7 +315,7 @@ int check_moe(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const 
 // ------------------------------------------------------------- CUDA-core path
 
 struct FmaPlan {
-  int grid, rows_per_cta, ru;
+  int grid, rows_per_cta, ru, ks;
   size_t smem, off_am, ws_bytes;
 };
 
@@ -325,8 +325,10 @@ bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
   if (p->smem > 200 * 1024) return false;
   const int ru = p->ru = fma_rows_per_warp(p->rows_per_cta, N);  // rows a warp takes at once
   const long groups = (static_cast<long>(N) + ru - 1) / ru;
-  const long ctas = (groups + 7) / 8;           // eight warps a CTA
   const long per_sm = p->smem <= 110 * 1024 ? 2 : 1;  // CTAs an SM holds
+  // few groups: teams of warps share a group's K rounds
+  p->ks = fma_k_split(groups, (K / 32 + 31) / 32, per_sm * sms * 8);
+  const long ctas = (groups * p->ks + 7) / 8;   // eight warps a CTA
   p->grid = static_cast<int>(ctas < per_sm * sms ? ctas : per_sm * sms);
   const int row_groups = (M + p->rows_per_cta - 1) / p->rows_per_cta;
   if (4 + 4 * row_groups > static_cast<int>(kWsCounters)) return false;
@@ -754,13 +756,15 @@ static int fma_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
   a.rms = (flags & NVFP4_FLAG_RMS_INPUT) ? 1 : 0;
   a.argmax_cnt = reinterpret_cast<uint32_t*>(ws + kWsArgmaxCnt);
   a.am_part = reinterpret_cast<int2*>(ws + p.off_am);
+  a.ks = p.ks;
   const cudaError_t e = launch_fma(a, p.grid, p.ru, reinterpret_cast<cudaStream_t>(stream),
                                    !(flags & NVFP4_FLAG_NO_PDL));
   if (e != cudaSuccess) return cuda_fail(e, "fma_kernel launch");
   char buf[192];
   snprintf(buf, sizeof(buf),
-           "fma_kernel grid=%dx%d rows_per_cta=%d rows_per_warp=%d smem=%zu argmax=%d rms=%d",
-           p.grid, (M + p.rows_per_cta - 1) / p.rows_per_cta, p.rows_per_cta, p.ru, p.smem,
+           "fma_kernel grid=%dx%d rows_per_cta=%d rows_per_warp=%d k_split=%d smem=%zu argmax=%d "
+           "rms=%d",
+           p.grid, (M + p.rows_per_cta - 1) / p.rows_per_cta, p.rows_per_cta, p.ru, p.ks, p.smem,
            argmax_out ? 1 : 0, a.rms);
   g_dispatch = buf;
   return NVFP4_OK;

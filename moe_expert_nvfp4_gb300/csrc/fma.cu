@@ -44,6 +44,20 @@ constexpr int kFmaThreads = kFmaWarps * 32;
 // a row offset and constants.
 constexpr int kChunkPitch = 80;
 
+// Barrier of the ks warps of team `team` (ks = 2: teams 0 .. 3, ks = 4:
+// teams 0, 1; named barriers 1 .. 4).  The barrier ids are immediates: with
+// an id in a register the compiler reserves all sixteen of the CTA's
+// barriers.
+__device__ __forceinline__ void team_sync(int team, int ks) {
+  const int n = ks * 32;
+  switch (team) {
+    case 0: asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); break;
+    case 1: asm volatile("bar.sync 2, %0;" ::"r"(n) : "memory"); break;
+    case 2: asm volatile("bar.sync 3, %0;" ::"r"(n) : "memory"); break;
+    default: asm volatile("bar.sync 4, %0;" ::"r"(n) : "memory"); break;
+  }
+}
+
 __device__ __forceinline__ void ld_chunk(uint32_t a, uint32_t (&xv)[16]) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -72,17 +86,6 @@ __device__ __forceinline__ float cta_sum0(float v, float* s_w) {
   return t;
 }
 
-__device__ __forceinline__ float cta_max0(float v, float* s_w) {
-  v = warp_max(v);
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.0f;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < kFmaWarps; ++w) t = fmaxf(t, s_w[w]);
-  __syncthreads();
-  return t;
-}
-
 // MB activation rows per CTA (rows m0 .. m0 + MB - 1 of A, m0 = MB *
 // blockIdx.y); grid-stride over the weight rows.  Two CTAs share an SM (the
 // grid is at most twice the SM count), hence the register bound.
@@ -96,6 +99,7 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   __shared__ float s_sq[kFmaWarps][MB];
   __shared__ int s_bi[kFmaWarps][MB];
   __shared__ int s_last;
+  __shared__ float s_part[kFmaWarps * 16];  // K-split teams: each warp's row sums
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = MB * blockIdx.y;
   const int mb = min(MB, a.M - m0);
@@ -104,15 +108,18 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
   const uint32_t xs = smem_u32(fsm);
 
   // The weights do not depend on the previous kernel on the stream: the
-  // first group's loads are issued before waiting for it.  A warp takes
-  // groups of RU consecutive weight rows (group G = the warp's global index
-  // + t * warps); per group the lanes walk the rows' 32-K chunks in rounds
-  // of 32.  The loads of the next round (or group) are issued before the
-  // current one is computed, so RU * 528 bytes per warp stay in flight.
-  const int n_warps = gridDim.x * kFmaWarps;
+  // first group's loads are issued before waiting for it.  A team of ks
+  // warps (ks = a.ks: 1, 2 or 4; more when the weight has few rows) takes
+  // groups of RU consecutive weight rows (group G = the team's global index
+  // + t * teams); per group the lanes walk the rows' 32-K chunks in rounds
+  // of 32, warp k of the team rounds k, k + ks, ... (ks <= rounds).
+  // The loads of the next round (or group) are issued before the current
+  // one is computed, so RU * 528 bytes per warp stay in flight.
+  const int ks = a.ks, kidx = warp % ks, team = warp / ks;
+  const int n_teams = gridDim.x * (kFmaWarps / ks);
   const int rounds = (chunks + 31) / 32;
   const int n_groups = (a.N + RU - 1) / RU;
-  int G = blockIdx.x * kFmaWarps + warp, cr = 0;
+  int G = blockIdx.x * (kFmaWarps / ks) + team, cr = kidx;
   uint4 cw[RU], nw[RU];
   uint32_t sb[RU], ns[RU];
   auto load = [&](int g, int round, uint4 (&w)[RU], uint32_t (&sc)[RU]) {
@@ -130,64 +137,91 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
       }
     }
   };
-  load(G, 0, cw, sb);
+  load(G, kidx, cw, sb);
   const float gs = *a.gscale;  // (a weight-side constant too)
 
   pdl_wait();
   pdl_launch_dependents();
 
-  // segments per thread and row kept in registers (K <= 8192 for up to four
-  // rows; more rows load theirs again for the conversion)
-  constexpr int kKeep = MB <= 4 ? 4 : 0;
-  uint4 keep[MB][kKeep > 0 ? kKeep : 1];
-  // ---- per row: the largest magnitude and the plain sum of squares in one
-  // pass over all the CTA's rows, one reduction; then the FP16 shift and the
-  // RMS factor (rows above 2^56 sum their shifted squares in a second pass:
-  // no overflow at any magnitude)
+  // ---- the CTA's activation rows.  Segment v (elements 8 v ..) of a row is
+  // 16-byte slot v % 4 of chunk v / 4 of the row's staging area; thread t
+  // takes segments v = t + 256 i.  Up to four rows: the first four segments
+  // per row stay in registers (K <= 8192; more are loaded again for the
+  // conversion).  Eight or more rows: every segment is copied straight into
+  // its slot (the BF16 segment sits where its FP16 conversion goes; rows past
+  // M zero-filled) and read back from there.  Either way all the loads are in
+  // flight at once.
+  const int segs = a.K / 8;
+  auto seg_addr = [&](int r, int v) {
+    return xs + static_cast<uint32_t>(r * rs + (v >> 2) * kChunkPitch + (v & 3) * 16);
+  };
+  constexpr bool kCopy = MB >= 8;
+  constexpr int kKeep = kCopy ? 1 : (MB == 4 ? 2 : 4);
+  uint4 keep[MB][kKeep];
+  if constexpr (kCopy) {
+#pragma unroll
+    for (int r = 0; r < MB; ++r) {
+      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + (r < mb ? r : 0)) * a.lda;
+      for (int v = threadIdx.x; v < segs; v += kFmaThreads)
+        cp_async_16(seg_addr(r, v), row + 8 * v, r < mb ? 16u : 0u);
+    }
+    cp_async_wait_all();  // (each thread reads back only its own segments)
+  } else {
+#pragma unroll
+    for (int r = 0; r < MB; ++r) {
+      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
+#pragma unroll
+      for (int i = 0; i < kKeep; ++i) {
+        const int v = threadIdx.x + kFmaThreads * i;
+        keep[r][i] = (r < mb && v < segs) ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  // ---- per row: the largest magnitude and the plain sum of squares, one
+  // reduction over the CTA; then the FP16 shift and the RMS factor (rows
+  // above 2^56 sum their shifted squares in a second pass: no overflow at
+  // any magnitude)
   {
     float mx[MB], sq[MB];
+    auto add = [&](int r, const uint4 q) {
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
+        mx[r] = fmaxf(mx[r], fmaxf(fabsf(lo), fabsf(hi)));
+        sq[r] = fmaf(lo, lo, fmaf(hi, hi, sq[r]));
+      }
+    };
 #pragma unroll
     for (int r = 0; r < MB; ++r) {
       mx[r] = 0.0f;
       sq[r] = 0.0f;
-      if (r < mb) {
-        const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
-        // 8-element segments v = thread + 256 i: the first kKeep of them
-        // stay in registers for the conversion below
+      if constexpr (kCopy) {
+        for (int v = threadIdx.x; v < segs; v += kFmaThreads) add(r, ld_shared_v4(seg_addr(r, v)));
+      } else {
 #pragma unroll
-        for (int i = 0; i < kKeep; ++i) {
-          const int v = threadIdx.x + kFmaThreads * i;
-          keep[r][i] = v < a.K / 8 ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
-                                   : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int i = 0; i < kKeep; ++i) {
-          const uint32_t w[4] = {keep[r][i].x, keep[r][i].y, keep[r][i].z, keep[r][i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-            mx[r] = fmaxf(mx[r], fmaxf(fabsf(lo), fabsf(hi)));
-            sq[r] = fmaf(lo, lo, fmaf(hi, hi, sq[r]));
-          }
-        }
-        for (int v = threadIdx.x + kFmaThreads * kKeep; v < a.K / 8; v += kFmaThreads) {
-          const uint4 q = __ldcg(reinterpret_cast<const uint4*>(row + 8 * v));
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xFFFF0000u);
-            mx[r] = fmaxf(mx[r], fmaxf(fabsf(lo), fabsf(hi)));
-            sq[r] = fmaf(lo, lo, fmaf(hi, hi, sq[r]));
-          }
-        }
+        for (int i = 0; i < kKeep; ++i) add(r, keep[r][i]);
+        if (r < mb)
+          for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads)
+            add(r, __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda +
+                                                         8 * v)));
       }
-      mx[r] = warp_max(mx[r]);
-      sq[r] = warp_sum(sq[r]);
-      if (lane == 0) {
+    }
+    // the rows' warp reductions side by side (same order as warp_max / warp_sum)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int r = 0; r < MB; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+        sq[r] += __shfl_xor_sync(0xffffffffu, sq[r], o);
+      }
+    if (lane == 0)
+#pragma unroll
+      for (int r = 0; r < MB; ++r) {
         s_bv[warp][r] = mx[r];
         s_sq[warp][r] = sq[r];
       }
-    }
     __syncthreads();
     if (threadIdx.x < MB) {
       const int r = threadIdx.x;
@@ -223,9 +257,7 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
       __syncthreads();
     }
   }
-  // the shifted FP16 rows: segment v (elements 8 v ..) is 16-byte slot
-  // q = v % 4 of chunk c = v / 4 (elements 32 c ..); rows past the CTA's are
-  // zero
+  // the shifted FP16 rows (rows past the CTA's are zero)
   auto to_f16 = [&](const uint4 v, int sh) {
     const int h1 = (sh > 126 || sh < -126) ? sh / 2 : sh;
     const float f1 = exp2i(h1), f2 = exp2i(sh - h1);
@@ -237,23 +269,24 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
                         __uint_as_float(w[j] & 0xFFFF0000u) * f1 * f2);
     return make_uint4(p[0], p[1], p[2], p[3]);
   };
-  auto store_seg = [&](int r, int v, const uint4 q, int sh) {
-    st_shared_v4(xs + static_cast<uint32_t>(r * rs + (v >> 2) * kChunkPitch + (v & 3) * 16),
-                 to_f16(q, sh));
-  };
 #pragma unroll
   for (int r = 0; r < MB; ++r) {
     const int sh = s_sh[r];
+    if constexpr (kCopy) {
+      for (int v = threadIdx.x; v < segs; v += kFmaThreads)
+        st_shared_v4(seg_addr(r, v), to_f16(ld_shared_v4(seg_addr(r, v)), sh));
+    } else {
 #pragma unroll
-    for (int i = 0; i < kKeep; ++i) {
-      const int v = threadIdx.x + kFmaThreads * i;
-      if (v < a.K / 8) store_seg(r, v, r < mb ? keep[r][i] : make_uint4(0u, 0u, 0u, 0u), sh);
-    }
-    for (int v = threadIdx.x + kFmaThreads * kKeep; v < a.K / 8; v += kFmaThreads) {
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (r < mb)
-        q = __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda + 8 * v));
-      store_seg(r, v, q, sh);
+      for (int i = 0; i < kKeep; ++i) {
+        const int v = threadIdx.x + kFmaThreads * i;
+        if (v < segs) st_shared_v4(seg_addr(r, v), to_f16(keep[r][i], sh));
+      }
+      for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads) {
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (r < mb)
+          q = __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda + 8 * v));
+        st_shared_v4(seg_addr(r, v), to_f16(q, sh));
+      }
     }
   }
   __syncthreads();
@@ -275,8 +308,9 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
     for (int j = 0; j < RU; ++j) acc[r][j] = 0.0f;
   while (G < n_groups) {
     // the next item's loads first
-    const int nG = cr + 1 < rounds ? G : G + n_warps;
-    const int ncr = cr + 1 < rounds ? cr + 1 : 0;
+    const bool last = cr + ks >= rounds;  // this warp's last round of the group
+    const int nG = last ? G + n_teams : G;
+    const int ncr = last ? kidx : cr + ks;
     load(nG, ncr, nw, ns);
     const int c = cr * 32 + lane;
     if (c < chunks) {
@@ -303,15 +337,43 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
         }
       }
     }
-    if (cr + 1 == rounds) {  // the group's rows are complete
+    if (last) {  // the group's rows are complete
+      // the warp sums of all the group's outputs side by side (the order of
+      // warp_sum)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < RU; ++j)
+#pragma unroll
+          for (int r = 0; r < MB; ++r) acc[r][j] += __shfl_xor_sync(0xffffffffu, acc[r][j], o);
+      if (ks > 1) {
+        // each warp's sums to shared memory; the team's first warp adds
+        // them in warp order (a named barrier per team)
+        if (lane == 0)
+#pragma unroll
+          for (int j = 0; j < RU; ++j)
+#pragma unroll
+            for (int r = 0; r < MB; ++r) s_part[warp * 16 + r * RU + j] = acc[r][j];
+        team_sync(team, ks);
+        if (kidx == 0) {
+#pragma unroll
+          for (int j = 0; j < RU; ++j)
+#pragma unroll
+            for (int r = 0; r < MB; ++r) {
+              float t = 0.0f;
+              for (int k = 0; k < ks; ++k) t += s_part[(warp + k) * 16 + r * RU + j];
+              acc[r][j] = t;
+            }
+        }
+      }
 #pragma unroll
       for (int j = 0; j < RU; ++j) {
         const int n = G * RU + j;
 #pragma unroll
         for (int r = 0; r < MB; ++r) {
-          const float t = warp_sum(acc[r][j]);
+          const float t = acc[r][j];
           acc[r][j] = 0.0f;
-          if (r < mb && n < a.N) {
+          if (kidx == 0 && r < mb && n < a.N) {
             const __nv_bfloat16 o =
                 __float2bfloat16_rn(scale_pow2(t, -s_sh[r]) * gs * (a.rms ? s_rms[r] : 1.0f));
             if (lane == 0) a.C[static_cast<size_t>(m0 + r) * a.ldc + n] = o;
@@ -323,6 +385,7 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
           }
         }
       }
+      if (ks > 1) team_sync(team, ks);  // (s_part is free again)
     }
     G = nG;
     cr = ncr;
@@ -446,6 +509,20 @@ int fma_rows_per_warp(int rows_per_cta, int N) {
   if (rows_per_cta == 1) return N < 3072 ? 2 : (N < 12288 ? 4 : 8);
   if (rows_per_cta == 2) return N < 6144 ? 2 : 4;
   return rows_per_cta == 4 ? 2 : 1;
+}
+
+int fma_k_split(long groups, int rounds, long warp_slots) {
+  // Rows of 4 or more rounds (K >= 4096) over few groups: the widest team
+  // (4, 2 warps) that leaves each warp a round and keeps the grid within
+  // 128 CTAs.  Measured on GB300, back-to-back calls, K = 4096, us for teams
+  // of 1 / 2 / 4 warps: 64 rows M = 1 3.1 / 2.7 / 2.3, M = 4 7.1 / 6.6 /
+  // 5.8; 1024 rows M = 1 4.3 / 3.8 / 5.5, 2048 rows M = 1 5.1 / 6.4 / 7.1.
+  // At K = 2048 (two rounds) a team gains at most 0.2 us or loses.
+  if (rounds < 4) return 1;
+  const long cap = warp_slots < 1024 ? warp_slots : 1024;
+  for (int ks = 4; ks > 1; ks >>= 1)
+    if (ks <= rounds && groups * ks <= cap) return ks;
+  return 1;
 }
 
 cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool pdl) {

@@ -189,6 +189,7 @@ struct FmaArgs {
   int rms;
   uint32_t* argmax_cnt;
   int2* am_part;
+  int ks;  // warps that share a group of weight rows (K split): 1, 2 or 4
 };
 // activation rows per CTA for M rows of K (1, 2, 4, 8 or 16, fewer when the
 // staged rows would not fit in shared memory); grid.y = ceil(M / that)
@@ -198,6 +199,9 @@ size_t fma_smem_bytes(int rows_per_cta, int K);
 // weight rows a warp of that kernel takes at once (its loads in flight:
 // this many times 528 bytes per 32-K round at K = 2048), for N weight rows
 int fma_rows_per_warp(int rows_per_cta, int N);
+// Warps that split the K rounds of one group of weight rows (1, 2 or 4),
+// given the groups, the 32-chunk rounds of a row and the warps the SMs hold.
+int fma_k_split(long groups, int rounds, long warp_slots);
 cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool pdl);
 
 // MoE layer on the CUDA cores (moe_fma.cu) for T <= kMoeFmaMaxT tokens:
