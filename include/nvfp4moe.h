@@ -140,9 +140,12 @@ int nvfp4_workspace_init(void* workspace, size_t bytes, nvfp4_stream_t stream);
  * streams 256-K stages through tcgen05 MMAs and costs about 13 us a call
  * before its first byte; the CUDA-core kernel (whole rows per warp, FP32
  * accumulation of the same exact FP16 products) starts in a few us but does
- * one FMA per weight and row.  The CUDA cores take every K % 256 != 0, and
+ * one FMA per weight and row (more than four rows run as CTAs of four rows
+ * in ceil(M / 4) row groups).  The CUDA cores take every K % 256 != 0, and
  * K % 256 == 0 when the weight (codes + scales) is at most 128 MiB for
- * M = 1, 20 MiB for M = 2, 10 MiB for M = 3, 4 and 1 MiB for M = 5..8.
+ * M = 1, 20 MiB for M = 2, 3 and 10 MiB for M = 4; for M = 5..16 when it is
+ * at most 5 MiB and ceil(N / 16) * ceil(M / 4) <= 2 x the SM count (one
+ * wave of its CTAs).
  * The two differ only in the order of the FP32 additions (a few units in
  * the last place of C). */
 size_t nvfp4_gemm_skinny_workspace(int M, int N, int K);

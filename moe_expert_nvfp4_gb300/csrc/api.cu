@@ -340,29 +340,36 @@ bool plan_fma(int M, int N, int K, int sms, FmaPlan* p) {
 // Which dense NVFP4 calls run on the CUDA cores (fma.cu) rather than the
 // tensor cores: every K that is not a multiple of 256 (the tensor path
 // streams 256-K stages), and the calls whose weight stream is short enough
-// that the tensor-core kernel's fixed cost (about 13 us a call: tensor-memory
-// allocation, ring fill, split-K drain) outweighs its faster streaming.  The
-// CUDA-core kernel does one FMA per weight and activation row, so its rate
-// falls as M grows.  Measured on GB300, back-to-back calls in a CUDA graph
-// with programmatic dependent launch, K = 2048 (CUDA cores vs tensor cores,
-// us):
-//   M = 1: 4096 rows 3.5 vs 14.4, 16384 rows 8.3 vs 13.5, 151,936 rows 51.6
+// that the tensor-core kernel's fixed cost (about 8 to 13 us a call:
+// tensor-memory allocation, ring fill, split-K drain) outweighs its faster
+// streaming.  The CUDA-core kernel does one FMA per weight and activation
+// row, so its rate falls as M grows; beyond four rows it runs four-row CTAs
+// in ceil(M / 4) row groups, which pays while they all fit one wave of two
+// CTAs an SM.  Measured on GB300, back-to-back calls in a CUDA graph with
+// programmatic dependent launch, K = 2048 unless stated (CUDA cores vs
+// tensor cores, us):
+//   M = 1: 4096 rows 3.4 vs 14.4, 16384 rows 6.0 vs 13.5, 151,936 rows 51.6
 //          vs 47.6;
-//   M = 2: 16384 rows 11.0 vs 13.6, 32768 rows 18.8 vs 17.0;
-//   M = 4: 8192 rows 11.9 vs 13.8, 16384 rows 18.9 vs 13.6;
-//   M = 8: 64 rows 10.2 vs 12.3, 4096 rows 16.2 vs 18.2, 2048 x 4096 18.1
-//          vs 15.1, 8192 rows 23.9 vs 16.5;
-//   M = 16: 64 rows 19.7 vs 15.6, 4096 rows 30.6 vs 25.4.
-// Hence, by the weight bytes: M = 1 up to 128 MiB, M = 2 up to 20 MiB,
-// M = 3, 4 up to 10 MiB, M = 5..8 up to 1 MiB, never beyond.
-bool use_fma(int M, int N, int K) {
+//   M = 2: 16384 rows 9.8 vs 13.6, 32768 rows 18.8 vs 17.0;
+//   M = 3: 8192 rows 8.5 vs 10.6, 16384 rows 13.7 vs 14.4;
+//   M = 4: 8192 rows 9.6 vs 10.6, 16384 rows 15.8 vs 14.4;
+//   M = 8: 64 rows 4.7 vs 9.0, 1024 rows 5.0 vs 9.5, 2048 x 4096 8.7 vs
+//          11.7, 4096 rows 11.8 vs 10.0;
+//   M = 12: 1024 rows 6.2 vs 11.1, 2048 x 4096 13.9 vs 13.8;
+//   M = 16: 1024 rows 6.2 vs 12.2, 2048 x 4096 16.5 vs 14.9, 4096 rows
+//          21.3 vs 12.7.
+// Hence, by the weight bytes: M = 1 up to 128 MiB, M = 2, 3 up to 20 MiB,
+// M = 4 up to 10 MiB; M = 5..16 up to 5 MiB and 2 CTAs an SM (ceil(N / 16)
+// CTAs of two-row warps per row group); never beyond.
+bool use_fma(int M, int N, int K, int sms) {
   if (K % kStageK) return true;
   const double mib = static_cast<double>(N) * K * 9.0 / 16.0 / (1 << 20);  // codes + block scales
   if (M == 1) return mib <= 128.0;
-  if (M == 2) return mib <= 20.0;
-  if (M <= 4) return mib <= 10.0;
-  if (M <= 8) return mib <= 1.0;
-  return false;
+  if (M <= 3) return mib <= 20.0;
+  if (M == 4) return mib <= 10.0;
+  if (M > 16 || mib > 5.0) return false;
+  const long ctas = (static_cast<long>(N) + 15) / 16 * ((M + 3) / 4);
+  return ctas <= 2L * sms;
 }
 
 // MoE calls with few tokens run on the CUDA cores (moe_fma.cu): one FMA per
@@ -685,7 +692,7 @@ size_t nvfp4_gemm_skinny_workspace(int M, int N, int K) {
   int sms = 0;
   if (M < 1 || M > kMaxM || N < 1 || K < 32 || K % 32) return 0;
   if (current_device(&sms) != NVFP4_OK) return 0;
-  if (use_fma(M, N, K)) {
+  if (use_fma(M, N, K, sms)) {
     FmaPlan f;
     return plan_fma(M, N, K, sms, &f) ? f.ws_bytes : 0;
   }
@@ -773,9 +780,10 @@ static int fma_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, 
 static int gemm_skinny(const void* A, int64_t lda, int M, const nvfp4_weight* W, void* C,
                        int64_t ldc, int32_t* argmax_out, const int32_t* am_map, uint32_t flags,
                        void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
-  int rc = check_gemm(A, lda, M, W, C, ldc);
+  int rc = check_gemm(A, lda, M, W, C, ldc), sms = 0;
   if (rc) return rc;
-  if (use_fma(M, W->n, W->k))
+  if ((rc = current_device(&sms))) return rc;
+  if (use_fma(M, W->n, W->k, sms))
     return fma_skinny(A, lda, M, W, C, ldc, argmax_out, am_map, flags, workspace,
                       workspace_bytes, stream);
   return dense_skinny("nvfp4", A, lda, M, dense_w(W), C, ldc, argmax_out, am_map, flags,

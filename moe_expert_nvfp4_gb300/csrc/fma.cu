@@ -91,6 +91,7 @@ __device__ __forceinline__ float cta_sum0(float v, float* s_w) {
 // grid is at most twice the SM count), hence the register bound.
 template <int MB, int RU>
 __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
+  static_assert(MB <= 4 && MB * RU <= 16, "rows per CTA, outputs per warp");
   extern __shared__ __align__(16) uint8_t fsm[];
   __shared__ int s_sh[MB];
   __shared__ float s_rms[MB];
@@ -145,37 +146,24 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
 
   // ---- the CTA's activation rows.  Segment v (elements 8 v ..) of a row is
   // 16-byte slot v % 4 of chunk v / 4 of the row's staging area; thread t
-  // takes segments v = t + 256 i.  Up to four rows: the first four segments
-  // per row stay in registers (K <= 8192; more are loaded again for the
-  // conversion).  Eight or more rows: every segment is copied straight into
-  // its slot (the BF16 segment sits where its FP16 conversion goes; rows past
-  // M zero-filled) and read back from there.  Either way all the loads are in
-  // flight at once.
+  // takes segments v = t + 256 i.  The first kKeep segments of every row are
+  // loaded at once, all in flight together, and stay in registers (K up to
+  // 8192 for one or two rows, 4096 for four; the rest of a longer row is
+  // loaded again for the conversion).
   const int segs = a.K / 8;
   auto seg_addr = [&](int r, int v) {
     return xs + static_cast<uint32_t>(r * rs + (v >> 2) * kChunkPitch + (v & 3) * 16);
   };
-  constexpr bool kCopy = MB >= 8;
-  constexpr int kKeep = kCopy ? 1 : (MB == 4 ? 2 : 4);
+  constexpr int kKeep = MB == 4 ? 2 : 4;
   uint4 keep[MB][kKeep];
-  if constexpr (kCopy) {
 #pragma unroll
-    for (int r = 0; r < MB; ++r) {
-      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + (r < mb ? r : 0)) * a.lda;
-      for (int v = threadIdx.x; v < segs; v += kFmaThreads)
-        cp_async_16(seg_addr(r, v), row + 8 * v, r < mb ? 16u : 0u);
-    }
-    cp_async_wait_all();  // (each thread reads back only its own segments)
-  } else {
+  for (int r = 0; r < MB; ++r) {
+    const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
 #pragma unroll
-    for (int r = 0; r < MB; ++r) {
-      const __nv_bfloat16* row = a.A + static_cast<size_t>(m0 + r) * a.lda;
-#pragma unroll
-      for (int i = 0; i < kKeep; ++i) {
-        const int v = threadIdx.x + kFmaThreads * i;
-        keep[r][i] = (r < mb && v < segs) ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
-                                          : make_uint4(0u, 0u, 0u, 0u);
-      }
+    for (int i = 0; i < kKeep; ++i) {
+      const int v = threadIdx.x + kFmaThreads * i;
+      keep[r][i] = (r < mb && v < segs) ? __ldcg(reinterpret_cast<const uint4*>(row + 8 * v))
+                                        : make_uint4(0u, 0u, 0u, 0u);
     }
   }
   // ---- per row: the largest magnitude and the plain sum of squares, one
@@ -197,16 +185,12 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
     for (int r = 0; r < MB; ++r) {
       mx[r] = 0.0f;
       sq[r] = 0.0f;
-      if constexpr (kCopy) {
-        for (int v = threadIdx.x; v < segs; v += kFmaThreads) add(r, ld_shared_v4(seg_addr(r, v)));
-      } else {
 #pragma unroll
-        for (int i = 0; i < kKeep; ++i) add(r, keep[r][i]);
-        if (r < mb)
-          for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads)
-            add(r, __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda +
-                                                         8 * v)));
-      }
+      for (int i = 0; i < kKeep; ++i) add(r, keep[r][i]);
+      if (r < mb)
+        for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads)
+          add(r, __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda +
+                                                       8 * v)));
     }
     // the rows' warp reductions side by side (same order as warp_max / warp_sum)
 #pragma unroll
@@ -272,21 +256,16 @@ __global__ void __launch_bounds__(kFmaThreads, 2) fma_kernel(const FmaArgs a) {
 #pragma unroll
   for (int r = 0; r < MB; ++r) {
     const int sh = s_sh[r];
-    if constexpr (kCopy) {
-      for (int v = threadIdx.x; v < segs; v += kFmaThreads)
-        st_shared_v4(seg_addr(r, v), to_f16(ld_shared_v4(seg_addr(r, v)), sh));
-    } else {
 #pragma unroll
-      for (int i = 0; i < kKeep; ++i) {
-        const int v = threadIdx.x + kFmaThreads * i;
-        if (v < segs) st_shared_v4(seg_addr(r, v), to_f16(keep[r][i], sh));
-      }
-      for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads) {
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (r < mb)
-          q = __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda + 8 * v));
-        st_shared_v4(seg_addr(r, v), to_f16(q, sh));
-      }
+    for (int i = 0; i < kKeep; ++i) {
+      const int v = threadIdx.x + kFmaThreads * i;
+      if (v < segs) st_shared_v4(seg_addr(r, v), to_f16(keep[r][i], sh));
+    }
+    for (int v = threadIdx.x + kFmaThreads * kKeep; v < segs; v += kFmaThreads) {
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (r < mb)
+        q = __ldcg(reinterpret_cast<const uint4*>(a.A + static_cast<size_t>(m0 + r) * a.lda + 8 * v));
+      st_shared_v4(seg_addr(r, v), to_f16(q, sh));
     }
   }
   __syncthreads();
@@ -491,7 +470,11 @@ size_t fma_smem_bytes(int rows_per_cta, int K) {
 }
 
 int fma_rows_per_cta(int M, int K) {
-  int mb = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+  // (more rows run as row groups of four: measured on GB300, eight- and
+  // sixteen-row CTAs, which decode each weight chunk once for all their
+  // rows, lost to row groups of four at every shape, e.g. 2048 x 4096 at M
+  // = 8 17.5 vs 8.7 us, 1024 x 2048 at M = 16 22.3 vs 6.2 us)
+  int mb = M <= 1 ? 1 : M <= 2 ? 2 : 4;
   while (mb > 1 && fma_smem_bytes(mb, K) > kFmaMaxSmem) mb /= 2;  // (long rows)
   return mb;
 }
@@ -508,7 +491,7 @@ int fma_rows_per_warp(int rows_per_cta, int N) {
   // (thresholds for GB300's 152 SMs)
   if (rows_per_cta == 1) return N < 3072 ? 2 : (N < 12288 ? 4 : 8);
   if (rows_per_cta == 2) return N < 6144 ? 2 : 4;
-  return rows_per_cta == 4 ? 2 : 1;
+  return 2;
 }
 
 int fma_k_split(long groups, int rounds, long warp_slots) {
@@ -533,8 +516,6 @@ cudaError_t launch_fma(const FmaArgs& a, int grid, int ru, cudaStream_t s, bool 
     case 32 + 4: return launch_mb<2, 4>(a, grid, s, pdl);
     case 32 + 2: return launch_mb<2, 2>(a, grid, s, pdl);
     case 64 + 2: return launch_mb<4, 2>(a, grid, s, pdl);
-    case 128 + 1: return launch_mb<8, 1>(a, grid, s, pdl);
-    case 256 + 1: return launch_mb<16, 1>(a, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -191,8 +191,8 @@ struct FmaArgs {
   int2* am_part;
   int ks;  // warps that share a group of weight rows (K split): 1, 2 or 4
 };
-// activation rows per CTA for M rows of K (1, 2, 4, 8 or 16, fewer when the
-// staged rows would not fit in shared memory); grid.y = ceil(M / that)
+// activation rows per CTA for M rows of K (1, 2 or 4, fewer when the staged
+// rows would not fit in shared memory); grid.y = ceil(M / that)
 int fma_rows_per_cta(int M, int K);
 // shared memory of its staged activation rows
 size_t fma_smem_bytes(int rows_per_cta, int K);

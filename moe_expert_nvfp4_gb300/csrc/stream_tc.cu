@@ -434,26 +434,24 @@ __device__ __forceinline__ void acquire_tensormap(const CUtensorMap* m) {
 // squares), and unless raw the in-place conversion to FP16 times 2^sig[n].
 // Each lane walks the 16-byte chunks lane, lane + 32, ... of its warp's
 // rows in that order, as the register path and the dense RMS pass do (same
-// sums, bit for bit).  The four epilogue warps; klen % 256 == 0.  dry: the
-// same code over rb zero rows (no global reads), only to bring it into the
-// instruction cache; sig and rms then hold nothing of use.
+// sums, bit for bit).  The four epilogue warps; klen % 256 == 0.
 __device__ __forceinline__ void stage_rows_async(const __nv_bfloat16* base, int64_t ld, int nr,
                                                  int rb, int kbeg, int klen, uint32_t xs,
                                                  int* sig, float* rms, int ew, int lane,
-                                                 bool raw, bool dry = false) {
+                                                 bool raw) {
   const int cpr = klen >> 3;  // 16-byte chunks per row
   const int etid = ew * 32 + lane;
 #pragma unroll 1
   for (int i = etid; i < rb * cpr; i += kEpiThreads) {
     const int n = i / cpr, kc = i - n * cpr;
     const __nv_bfloat16* src = base + static_cast<size_t>(n < nr ? n : 0) * ld + kbeg + 8 * kc;
-    cp_async_16(xs + xoff(n, 8 * kc, rb), src, (n < nr && !dry) ? 16u : 0u);
+    cp_async_16(xs + xoff(n, 8 * kc, rb), src, n < nr ? 16u : 0u);
   }
   cp_async_wait_all();
   esync();
 #pragma unroll 1
   for (int n = ew; n < rb; n += kEpiWarps) {
-    if (n >= nr && !dry) {
+    if (n >= nr) {
       if (lane == 0) sig[n] = 0;
       continue;
     }
@@ -1097,6 +1095,7 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         if (etid == 0) grid_wait(wait_ctr, gridDim.x, c.status(), c.abort_flag());
       } else {
         pdl_wait();
+        pdl_launch_dependents();
       }
       esync();
       waited = true;
@@ -1153,24 +1152,6 @@ __device__ __forceinline__ void epilogue_op(const Cta& c, const TcOp& op, SchedC
         xst.key = key;
         // the previous window's MMAs are complete (its accumulator was read)
         const int kbeg = xst.k0 * kk.uk(), klen = (xst.k1 - xst.k0) * kk.uk();
-        // Before the wait, a dry staging pass over zero rows (one 256-K
-        // block, no global reads) brings the staging code into the
-        // instruction cache: it runs once per op, after the other roles'
-        // code has gone through the cache, and would otherwise miss on
-        // every line.  Skipped when the previous op is already complete.
-        if (MODE != kTcDown && !waited) {
-          if (etid == 0)
-            *bcast = (wait_ctr == nullptr || ld_acquire_gpu(wait_ctr) < gridDim.x) ? 1 : 0;
-          esync();
-          if (*bcast) {
-            stage_rows_async(dense_mode(MODE) ? a.A : a.x, dense_mode(MODE) ? a.lda : a.ldx, 0, rb,
-                             0, kStageK, smem_u32(c.xs()), sig,
-                             (a.rms && !rms_ready && (MODE == kTcGateUp || (kbeg == 0 && klen == a.K)))
-                                 ? rms : nullptr,
-                             ew, lane, MODE == kTcDenseBF, true);
-          }
-          esync();
-        }
         wait_inputs();
         if (MODE == kTcDown) {
           const float* hbase = a.h + static_cast<size_t>(sc.off[key]) * a.I;
@@ -1561,10 +1542,15 @@ __device__ __forceinline__ void epilogue_role(const TcProgram& prog, const Cta& 
   SchedCursor cur;
   uint32_t dcount = 0;
   // inputs may come from the previous kernel on the stream: a dense first op
-  // waits for it just before it reads its activations, any other at once
+  // waits for it just before it reads its activations, any other at once.
+  // The next kernel is released only after that wait (released at launch,
+  // its CTAs took SMs ahead of this kernel's: measured on GB300, the
+  // 16- and 32-token decode steps 2 to 3 % slower).
   const bool pdl_first = n_ops > 0 && dense_mode(op_at(prog, 0).mode);
-  if (!pdl_first) pdl_wait();
-  pdl_launch_dependents();
+  if (!pdl_first) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   constexpr int kArgWords = static_cast<int>(sizeof(TcArgs)) / 16;
   for (int i = 0; i < n_ops && !c.aborted(); ++i) {
     const TcOp& op = op_at(prog, i);

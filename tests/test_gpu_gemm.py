@@ -60,13 +60,19 @@ def test_projection_2048_to_64_m4():
                                           (2, 32768, 2048, "stream_tc_kernel"),
                                           (4, 8192, 2048, "fma_kernel"),
                                           (4, 16384, 2048, "stream_tc_kernel"),
+                                          (3, 16384, 2048, "fma_kernel"),
                                           (8, 800, 2048, "fma_kernel"),
+                                          (8, 2048, 4096, "fma_kernel"),
                                           (8, 4096, 2048, "stream_tc_kernel"),
-                                          (9, 64, 2048, "stream_tc_kernel")])
+                                          (9, 64, 2048, "fma_kernel"),
+                                          (16, 1024, 2048, "fma_kernel"),
+                                          (16, 2048, 4096, "stream_tc_kernel"),
+                                          (17, 64, 2048, "stream_tc_kernel")])
 def test_dispatch_by_shape(m, n, k, kernel):
     """The CUDA cores take weights up to 128 MiB at M = 1, 20 MiB at M = 2,
-    10 MiB at M = 3, 4 and 1 MiB at M = 5..8; the tensor cores the rest
-    (K % 256 == 0)."""
+    3, 10 MiB at M = 4, and at M = 5..16 weights up to 5 MiB whose four-row
+    CTAs fit one wave (ceil(N / 16) * ceil(M / 4) <= 2 x 152); the tensor
+    cores the rest (K % 256 == 0)."""
     ws = ops.Workspace(ops.gemm_workspace_bytes(m, n, k))
     W = device_weight(30, n, k)
     a = synth.activations_bf16(30, m, k).cuda()
@@ -84,7 +90,7 @@ def test_dense_sweep(seed, n, k, m):
 
 @pytest.mark.parametrize("m,n,k", [(3, 200, 768), (13, 200, 768), (27, 1000, 256), (1, 64, 256),
                                    (32, 129, 2304), (9, 7, 512), (32, 1000, 4096),
-                                   (17, 3000, 6144)])
+                                   (17, 3000, 6144), (11, 300, 2080), (32, 64, 1056)])
 def test_ragged_shapes(m, n, k):
     c, ref, _, _ = _case(7, m, n, k)
     assert_close(f64(c), O.bf16_round(ref), f"ragged M={m} N={n} K={k}")

@@ -53,13 +53,13 @@ def test_single_gemm_program_equals_call():
 
 @pytest.mark.parametrize("m", [8, 16, 32])
 def test_gemm_chain_equals_calls_and_oracle(m):
-    """x -> (rms) W1 [4096 x 2048] -> (rms) W2 [2048 x 4096] -> W3 [8192 x 2048]
-    + argmax; every call on the tensor cores (M = 1, and smaller weights at
-    M <= 8, go to the CUDA-core kernel: the chain at M = 1 is checked against
-    the oracle below)."""
+    """x -> (rms) W1 [4096 x 2048] -> (rms) W2 [2560 x 4096] -> W3 [8192 x 2560]
+    + argmax; every call on the tensor cores (M = 1, and weights up to 5 MiB
+    at M <= 16 that fit one wave of four-row CTAs, go to the CUDA-core
+    kernel: the chain at M = 1 is checked against the oracle below)."""
     W1 = device_weight(12, 4096, 2048)
-    W2 = device_weight(13, 2048, 4096)
-    W3 = device_weight(14, 8192, 2048)
+    W2 = device_weight(13, 2560, 4096)
+    W3 = device_weight(14, 8192, 2560)
     x = synth.activations_bf16(12, m, 2048).cuda()
     h1 = ops.gemm(x, W1, rms_input=True)
     assert ops.last_dispatch().startswith("stream_tc_kernel<dense>")
@@ -80,7 +80,7 @@ def test_gemm_chain_equals_calls_and_oracle(m):
     assert prog.workspace.status() == 0
     assert _counters_zero(prog.workspace)
     # teacher-forced oracle check of the chain's middle link
-    ref2 = O.gemm_bf16(O.rms_scale(f64(p1)), *host_weight(13, 2048, 4096))
+    ref2 = O.gemm_bf16(O.rms_scale(f64(p1)), *host_weight(13, 2560, 4096))
     assert_close(f64(p2), ref2, f"chain M={m}")
 
 
@@ -92,9 +92,10 @@ def layer():
     return device_experts(21, 0, E, H, I), device_shared(21, 0, E, H, I)
 
 
-@pytest.mark.parametrize("t", [8, 32])
+@pytest.mark.parametrize("t", [12, 32])
 def test_moe_in_program_equals_call(layer, t):
-    """(8 and 32 rows: the dense calls run on the tensor cores too.)"""
+    """(12 and 32 rows: the 2048 x 2048 calls run on the tensor cores too; at
+    M = 5..8 that weight goes to the CUDA-core kernel.)"""
     ex, sh = layer
     x = synth.activations_bf16(21, t, 2048).cuda()
     ids, w = ops.route(synth.router_logits(21, t, 64).cuda(), 8)
