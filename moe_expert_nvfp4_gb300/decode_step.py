@@ -139,8 +139,8 @@ class DecodeStep:
     # of the SMs while the next call starts on the others; the persistent
     # program pays each op's completion wait and activation staging instead.
     # Measured on GB300, 40 layers, call by call against the program: T = 1
-    # 0.96 against 2.96 ms, T = 2 1.19 / 2.83, T = 4 1.93 / 2.91, T = 8
-    # 2.99 / 3.58, T = 16 4.82 / 5.34, T = 32 9.05 / 10.44: every token count
+    # 0.93 against 2.96 ms, T = 2 1.15 / 2.83, T = 4 1.73 / 2.90, T = 8
+    # 2.79 / 3.56, T = 16 4.74 / 5.32, T = 32 9.05 / 10.57: every token count
     # the library takes.
     CALLS_MAX_TOKENS = 32
 
