@@ -451,8 +451,10 @@ int moe_fma(const void* x, int64_t ldx, int T, const int32_t* topk_ids, const fl
   }
   char buf[192];
   snprintf(buf, sizeof(buf),
-           "moe_fma_gate_up_kernel; moe_fma_down_kernel slots=%d; T=%d k=%d E=%d shared=%d rms=%d "
-           "ids_ready=%d batches=%d",
+           "%s; moe_fma_down_kernel slots=%d; T=%d k=%d E=%d shared=%d rms=%d ids_ready=%d "
+           "batches=%d",
+           moe_gate_up_mma(a.H, T < kMoeFmaMaxT ? T : kMoeFmaMaxT) ? "moe_mma_gate_up_kernel"
+                                                                   : "moe_fma_gate_up_kernel",
            moe_fma_slots(k, a.has_shared, I), T, k, a.E, a.has_shared, a.rms, a.ids_ready,
            batches);
   g_dispatch = buf;

@@ -237,6 +237,10 @@ struct MoeFmaArgs {
 // slots of a token (k + shared) when the down kernel covers them and the
 // inter size I, else 0
 int moe_fma_slots(int k, int has_shared, int I);
+// whether the gate/up step of a batch of T tokens runs by warp MMAs
+// (moe_mma_gate_up_kernel: H a multiple of 512, 4 <= T <= 8) or by FMAs
+// (moe_fma_gate_up_kernel)
+bool moe_gate_up_mma(int H, int T);
 cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl);
 
 // Read-only bandwidth probe (probe.cu): reads bytes (a multiple of 16) of

@@ -36,7 +36,6 @@ namespace {
 
 constexpr int kMfWarps = 8;
 constexpr int kMfThreads = kMfWarps * 32;
-constexpr int kKeepSeg = 8;  // 8-element segments a lane keeps in registers while staging
 
 // Expert of pair p: its routed id (-1 when outside [0, E): skipped), or E for
 // the shared expert of token p - T k.
@@ -54,7 +53,10 @@ __device__ __forceinline__ int pair_token(const MoeFmaArgs& a, int p) {
 
 // Rows [0, T) of x, shifted to FP16, into xs (act_off layout, H / 32 chunks a
 // row) with s_sh[t] the shift and s_rms[t] the RMS factor (1 without RMS):
-// warp w stages rows w, w + 8, ...
+// warp w stages rows w, w + 8, ...; a lane keeps kKeepSeg 8-element segments
+// of a row in registers between the statistics and the conversion (the rest
+// it loads again).
+template <int kKeepSeg>
 __device__ __forceinline__ void stage_x_rows(const MoeFmaArgs& a, uint32_t xs, int* s_sh,
                                              float* s_rms, int warp, int lane) {
   const int segs = a.H / 8, chunks = a.H / 32;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kMfThreads, 2) moe_fma_gate_up_kernel(const Mo
     read_pairs();
     load(G, 0, cw, sb);
   }
-  stage_x_rows(a, xs, s_sh, s_rms, warp, lane);
+  stage_x_rows<8>(a, xs, s_sh, s_rms, warp, lane);
   __syncthreads();
 
   float acc[RU];
@@ -238,6 +240,158 @@ __global__ void __launch_bounds__(kMfThreads, 2) moe_fma_gate_up_kernel(const Mo
       cw[j] = nw[j];
       sb[j] = ns[j];
     }
+  }
+}
+
+// ---------------------------------------------------------------- gate / up by warp MMAs
+// The same layer step with the warp-level MMA (m16n8k16, FP16 operands, FP32
+// accumulation) as a wide FMA: the products code x scale x activation are
+// exact, as above, and only the order of the FP32 additions differs.  A warp
+// takes items (pair p, eight intermediate columns j0 .. j0 + 7): tile rows
+// 0 .. 7 are the gate rows j0 + g and tile rows 8 .. 15 the up rows
+// I + j0 + g of p's expert, and the activation operand is p's token row in
+// all eight columns.  Lane (g, q) = (lane / 4, lane % 4) loads, per 128-K
+// chunk c, the 32 codes 128 c + 32 q .. + 31 of its rows g and g + 8 (16
+// bytes each) and their two block scales, and the same 32 staged
+// activations of the token; k-step i of the chunk gives the MMA's K slots
+// {2q, 2q + 1} and {2q + 8, 2q + 9} the elements 128 c + 32 q + 4 i .. + 3
+// in that order in both operands, so each k-step sums 16 distinct products
+// of the row's dot product.  The codes are decoded and multiplied by their
+// block scales in FP16 (exact) into the A fragments; the FP32 accumulators
+// of lane (g, 0) end with row g's gate and up sums, which it turns into
+// h[p][j0 + g].  Loads run kMmaStages chunks ahead.
+constexpr int kMmaStages = 4;
+
+struct MmaChunk {
+  uint4 w0, w1;  // codes of tile rows g and g + 8
+  uint32_t sc;   // their two block scales each: row g low half, row g + 8 high half
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(kMfThreads, 2) moe_mma_gate_up_kernel(const MoeFmaArgs a) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  __shared__ int s_e[kMoeFmaMaxPairs];
+  __shared__ float s_g[kMoeFmaMaxPairs];
+  __shared__ int s_sh[kMoeFmaMaxT];
+  __shared__ float s_rms[kMoeFmaMaxT];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, q = lane & 3;
+  const uint32_t xs = smem_u32(msm);
+  const int H = a.H, I = a.I, chunks = H / 32, nc = H / 128;
+  const int P = a.T * a.k + (a.has_shared ? a.T : 0);
+  const int per_p = I / 8;  // items of a pair (a power of two)
+  const int per_p_log2 = __ffs(per_p) - 1;
+  const int n_items = P * per_p;
+  const int n_warps = gridDim.x * kMfWarps;
+  const size_t e_codes = static_cast<size_t>(2 * I) * (H / 2);
+  const size_t e_scales = static_cast<size_t>(2 * I) * (H / 16);
+
+  auto read_pairs = [&]() {
+    for (int p = threadIdx.x; p < P; p += kMfThreads) {
+      const int e = pair_expert(a, p);
+      s_e[p] = e;
+      s_g[p] = e < 0 ? 0.0f : (e == a.E ? *a.s_gu_global : a.gu_global[e]);
+      if (e < 0 && blockIdx.x == 0) atomicOr(a.status, kStatusBadId);
+    }
+    __syncthreads();
+  };
+
+  // load cursor: item lg, chunk lc, and the item's tile row g (codes, scales;
+  // null: no rows, the loads give zeros); row g + 8 lies I rows further
+  int lg = blockIdx.x * kMfWarps + warp, lc = 0;
+  const uint8_t *c0p = nullptr, *s0p = nullptr;
+  const size_t c_up = static_cast<size_t>(I) * (H / 2), s_up = static_cast<size_t>(I) * (H / 16);
+  auto item_rows = [&]() {
+    c0p = s0p = nullptr;
+    if (lg >= n_items) return;
+    const int p = lg >> per_p_log2, j0 = 8 * (lg & (per_p - 1));
+    const int e = s_e[p];
+    if (e < 0) return;
+    const uint8_t* cb = e == a.E ? a.s_gu_codes : a.gu_codes + e * e_codes;
+    const uint8_t* sb = e == a.E ? a.s_gu_scales : a.gu_scales + e * e_scales;
+    const size_t r0 = j0 + g;
+    c0p = cb + r0 * (H / 2) + 16 * q;
+    s0p = sb + r0 * (H / 16) + 2 * q;
+  };
+  auto load_next = [&](MmaChunk& b) {
+    b.w0 = b.w1 = make_uint4(0u, 0u, 0u, 0u);
+    b.sc = 0u;
+    if (c0p) {
+      const uint8_t* cp = c0p + 64 * lc;
+      const uint8_t* sp = s0p + 8 * lc;
+      b.w0 = __ldcs(reinterpret_cast<const uint4*>(cp));
+      b.w1 = __ldcs(reinterpret_cast<const uint4*>(cp + c_up));
+      b.sc = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(sp)) |
+             (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(sp + s_up)) << 16);
+    }
+    if (++lc == nc) {
+      lc = 0;
+      lg += n_warps;
+      item_rows();
+    }
+  };
+
+  MmaChunk buf[kMmaStages];
+  auto prologue = [&]() {
+    read_pairs();
+    item_rows();
+#pragma unroll
+    for (int j = 0; j < kMmaStages; ++j) load_next(buf[j]);
+  };
+  if (a.ids_ready) prologue();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!a.ids_ready) prologue();
+  stage_x_rows<4>(a, xs, s_sh, s_rms, warp, lane);  // (fewer registers: the loads in flight)
+  __syncthreads();
+
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int G = blockIdx.x * kMfWarps + warp; G < n_items; G += n_warps) {
+    const int p = G >> per_p_log2;
+    const int t = pair_token(a, p);
+    for (int cb = 0; cb < nc; cb += kMmaStages) {
+#pragma unroll
+      for (int j = 0; j < kMmaStages; ++j) {
+        const MmaChunk cur = buf[j];
+        load_next(buf[j]);  // kMmaStages chunks ahead
+        uint32_t xv[16];
+        ld_act_chunk(xs, t, 4 * (cb + j) + q, chunks, xv);
+        uint32_t s0lo, s0hi, s1lo, s1hi;
+        e4m3x2_bcast_f16x2(cur.sc & 0xFFFFu, s0lo, s0hi);
+        e4m3x2_bcast_f16x2(cur.sc >> 16, s1lo, s1hi);
+        const uint32_t w0[4] = {cur.w0.x, cur.w0.y, cur.w0.z, cur.w0.w};
+        const uint32_t w1[4] = {cur.w1.x, cur.w1.y, cur.w1.z, cur.w1.w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {  // word w: elements 8 w .. 8 w + 7 (k-steps 2 w, 2 w + 1)
+          uint32_t d0, d1, d2, d3, e0, e1, e2, e3;
+          e2m1x8_to_f16x2(w0[w], d0, d1, d2, d3);
+          e2m1x8_to_f16x2(w1[w], e0, e1, e2, e3);
+          const uint32_t sa = w < 2 ? s0lo : s0hi, sb = w < 2 ? s1lo : s1hi;
+          mma_16816(acc, hmul2(d0, sa), hmul2(e0, sb), hmul2(d1, sa), hmul2(e1, sb), xv[4 * w],
+                    xv[4 * w + 1]);
+          mma_16816(acc, hmul2(d2, sa), hmul2(e2, sb), hmul2(d3, sa), hmul2(e3, sb),
+                    xv[4 * w + 2], xv[4 * w + 3]);
+        }
+      }
+    }
+    // lane (g, 0): acc[0] = gate row j0 + g, acc[2] = up row j0 + g (column 0)
+    if (q == 0 && s_e[p] >= 0) {
+      const int j0 = 8 * (G & (per_p - 1));
+      const float f = s_g[p] * s_rms[t];
+      const float gt = scale_pow2(acc[0], -s_sh[t]) * f;
+      const float up = scale_pow2(acc[2], -s_sh[t]) * f;
+      a.h[static_cast<size_t>(p) * I + j0 + g] = gt / (1.0f + expf(-gt)) * up;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
   }
 }
 
@@ -403,14 +557,26 @@ int moe_fma_slots(int k, int has_shared, int I) {
   return S <= kMoeFmaMaxSlots ? S : 0;
 }
 
+// By warp MMAs for batches of 4 to 8 tokens.  Measured on GB300 (256
+// experts, H = 2048, I = 512, top-8 + shared; 40-layer decode step, us, FMAs
+// / MMAs): T = 4 1,727 / 1,657, T = 8 2,792 / 2,632; with fewer tokens the
+// MMA kernel's items (eight columns of a pair) leave SMs idle (T = 1 925 /
+// 1,068, T = 2 1,150 / 1,240), and with batches of 16 the step slowed
+// although the MoE calls alone ran faster (T = 16 4,740 / 5,424, MoE calls
+// alone 80.2 / 68.8 us a layer).
+bool moe_gate_up_mma(int H, int T) { return H % (128 * kMmaStages) == 0 && T >= 4 && T <= 8; }
+
 cudaError_t launch_moe_fma(const MoeFmaArgs& a, int sms, cudaStream_t s, bool pdl) {
   const int P = a.T * a.k + (a.has_shared ? a.T : 0);
-  // gate/up: one warp an item, at most two CTAs per SM
-  const long items = static_cast<long>(P) * (a.I / 2);
+  // gate/up: one warp an item (two or, by MMAs, eight intermediate columns of
+  // a pair), at most two CTAs per SM
+  const bool mma = moe_gate_up_mma(a.H, a.T);
+  const long items = static_cast<long>(P) * (a.I / (mma ? 8 : 2));
   const long ctas = (items + kMfWarps - 1) / kMfWarps;
   const int grid_gu = static_cast<int>(ctas < 2L * sms ? ctas : 2L * sms);
   const size_t smem_gu = static_cast<size_t>(a.T) * a.H * 2;
-  const void* gu = reinterpret_cast<const void*>(moe_fma_gate_up_kernel);
+  const void* gu = mma ? reinterpret_cast<const void*>(moe_mma_gate_up_kernel)
+                       : reinterpret_cast<const void*>(moe_fma_gate_up_kernel);
   cudaError_t e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem_gu < 1024 ? 1024 : smem_gu));
   if (e != cudaSuccess) return e;

@@ -124,8 +124,8 @@ class DecodeStep:
             # QKV, O, and the MoE layer: two CUDA-core kernels per batch of
             # 16 tokens, or three tensor-core kernels
             d = ops.last_dispatch()
-            launches += 2 + (2 * int(d.split("batches=")[1].split()[0]) if d.startswith("moe_fma")
-                             else 3)
+            launches += 2 + (2 * int(d.split("batches=")[1].split()[0])
+                             if "moe_fma_down_kernel" in d else 3)
             x = y
         ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,
                  pdl=pdl)

@@ -90,9 +90,11 @@ def _moe_case(layer4, t, shared=True, rms=False, ids=None, w=None, seed=4):
 def test_moe_layer_35b_shape(layer4, t):
     out, ref, disp, status, _ = _moe_case(layer4, t)
     assert status == 0
-    # the CUDA-core kernels at every T up to 32 (in batches of 16 tokens)
-    kernel = "moe_fma_gate_up_kernel"
-    assert "shared=1" in disp and disp.startswith(kernel)
+    # the CUDA-core kernels at every T up to 32 (in batches of 16 tokens);
+    # gate/up by warp MMAs for 4 to 8 tokens (H a multiple of 512)
+    gate_up = "moe_mma_gate_up_kernel" if 4 <= t <= 8 else "moe_fma_gate_up_kernel"
+    assert "shared=1" in disp and disp.startswith(gate_up)
+    assert "moe_fma_down_kernel" in disp
     assert_close(f64(out), O.bf16_round(ref), f"MoE T={t}")
 
 
@@ -124,7 +126,8 @@ def test_moe_cuda_core_kernels_other_shapes(e, h, i, k, t, shared):
     x = synth.activations_bf16(6, t, h, 2)
     ids, w = ops.route(synth.router_logits(6, t, e, 2).cuda(), k)
     out = ops.moe(x.cuda(), ids, w, ex, sh, rms_input=True)
-    assert ops.last_dispatch().startswith("moe_fma_gate_up_kernel")
+    gate_up = "moe_mma_gate_up_kernel" if h % 512 == 0 and 4 <= t <= 8 else "moe_fma_gate_up_kernel"
+    assert ops.last_dispatch().startswith(gate_up)
     torch.cuda.synchronize()
     ref = O.moe_decode64(O.rms_scale(f64(x)), ids.cpu().numpy(), w.cpu().double().numpy(), get, e,
                          get(e) if shared else None)
@@ -197,8 +200,9 @@ def test_moe_all_tokens_one_expert(layer4):
     assert_close(f64(out), O.bf16_round(ref), "all tokens on experts 0..7")
 
 
-def test_moe_deterministic(layer4):
-    out, _, _, _, (x, ids, w, ws) = _moe_case(layer4, 16)
+@pytest.mark.parametrize("t", [8, 16])
+def test_moe_deterministic(layer4, t):
+    out, _, _, _, (x, ids, w, ws) = _moe_case(layer4, t)
     ex, sh, _ = layer4
     again = [ops.moe(x.cuda(), ids, w, ex, sh, workspace=ws) for _ in range(3)]
     torch.cuda.synchronize()
