@@ -279,10 +279,12 @@ int topk_softmax_route(const float* logits, int T, int E, int k, int renormalize
  * NVFP4_STATUS_BAD_EXPERT_ID.  Limits: T <= 32, k <= 16, E <= 512,
  * H % 256 == 0, I % 256 == 0.  With I in {256, 512, 1024} (and 16 x H x 2
  * bytes within 96 KB) two CUDA-core kernels serve the call, per batch of at
- * most 16 tokens: gate/up + SwiGLU per (token, slot) pair, then down with
- * the combine; the tensor-core kernels (gate_up, down, combine) take the
- * other shapes.  The two differ only in the order of FP32 additions and in
- * h's FP16 staging (nvfp4_last_dispatch names the kernels). */
+ * most 16 tokens: gate/up + SwiGLU per (token, slot) pair (for batches of 4
+ * to 8 tokens with H % 512 == 0 by warp-level MMAs, FP16 x FP16 -> FP32),
+ * then down with the combine; the tensor-core kernels (gate_up, down,
+ * combine) take the other shapes.  They differ only in the order of FP32
+ * additions and in h's FP16 staging (nvfp4_last_dispatch names the
+ * kernels). */
 size_t moe_nvfp4_decode_workspace(int T, int k, const nvfp4_expert_stack* experts);
 int moe_nvfp4_decode(const void* x, int64_t ldx, int T, const int32_t* topk_ids,
                      const float* topk_w, int k, const nvfp4_expert_stack* experts,
