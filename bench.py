@@ -422,7 +422,7 @@ def workload_table(model, reps=10):
         us = graph_us(layers, reps)
         out[f"moe_T{t}"] = {"us": us / L, "gbs": nbytes / us / 1e3,
                             "kernel": ops.last_dispatch().split(";")[0]}
-        if "moe_fma_down_kernel" in ops.last_dispatch():
+        if "batches=" in ops.last_dispatch():  # the CUDA-core kernels
             # the same layers on the tensor-core kernels (one-op programs)
             progs = [ops.Program([ops.moe_op(x, ids[l * t:(l + 1) * t], wts[l * t:(l + 1) * t],
                                              model.experts[l], y, shared=model.shared[l])])

@@ -125,7 +125,7 @@ class DecodeStep:
             # 16 tokens, or three tensor-core kernels
             d = ops.last_dispatch()
             launches += 2 + (2 * int(d.split("batches=")[1].split()[0])
-                             if "moe_fma_down_kernel" in d else 3)
+                             if "batches=" in d else 3)
             x = y
         ops.gemm(x, self.head, out=b["head"], argmax_out=b["argmax"], rms_input=True, workspace=ws,
                  pdl=pdl)
