@@ -352,7 +352,10 @@ def workload_table(model, reps=10):
     on, each timed as a CUDA graph of back-to-back calls over weight copies
     that together exceed L2 (so every call reads HBM):
 
-    * the 2048 -> 64 projection at M = 4 (one call: latency-bound);
+    * the 2048 -> 64 projection at M = 4 (latency-bound; its 74 KB weight
+      stays in L2): one call per graph replay (the replay's own launch
+      included), and per call in a graph of 32 back-to-back calls over 32
+      weight copies (``proj_2048x64_M4_chain``);
     * the dense sweep: M in {1, 4, 8, 16, 32} x {4096 x 2048, 8192 x 2048,
       2048 x 4096} (seeds 1-3);
     * the MoE layer (256 routed + 1 shared experts, hidden 2048, inter 512,
@@ -386,6 +389,15 @@ def workload_table(model, reps=10):
     wk = ops.Workspace(ops.gemm_workspace_bytes(4, 64, 2048))
     us = graph_us(lambda: ops.gemm(a, ws64[0], out=c, workspace=wk), reps)
     out["proj_2048x64_M4"] = {"us": us, "gbs": nvfp4_bytes(64, 2048) / us / 1e3}
+    ws64 = weights(0, 64, 2048, 32)
+
+    def chain():
+        for w in ws64:
+            ops.gemm(a, w, out=c, workspace=wk)
+    us = graph_us(chain, reps) / len(ws64)
+    out["proj_2048x64_M4_chain"] = {"us": us, "gbs": nvfp4_bytes(64, 2048) / us / 1e3,
+                                    "kernel": ops.last_dispatch().split()[0]}
+    del ws64
 
     # dense sweep; 24 rotating copies of each shape (>= 113 MB each set)
     for seed, (n, k) in zip((1, 2, 3), ((4096, 2048), (8192, 2048), (2048, 4096))):
