@@ -15,6 +15,11 @@
 //     then out[t][n] = bf16(sum over slots, in order, of w * y, the shared
 //     expert's y added last).
 //
+// For batches of 4 to 8 tokens the gate/up step runs instead on the warp-
+// level MMA used as a wide FMA (moe_mma_gate_up_kernel, below): the same
+// exact products, without the per-element FMAs and half extractions that
+// bound the FMA kernel's issue rate.
+//
 // Activations (BF16 x, FP32 h) are staged in shared memory as FP16 after a
 // power-of-two shift per row that puts the row's largest magnitude in
 // [2^14, 2^15) (exact for BF16 elements within 2^31 of it; one rounding for
